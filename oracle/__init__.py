@@ -1,0 +1,107 @@
+"""fp64 CPU oracle for the attention forward pass -- test infrastructure only.
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package. The product (the CUDA library and its
+Python binding) never calls it and shares no code with it.
+
+The arithmetic lives in ``attention_oracle.c`` (plain loops in double
+precision; see its header for the definition it follows and the passages of
+the pages it cites). This module compiles it with gcc and marshals arguments.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attention_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+FP16, BF16 = 0, 1
+MASKS = {"none": 0, "causal": 1, "window": 2, 0: 0, 1: 1, 2: 2}
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle (plain gcc, no fast-math) next to its source."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                               "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        lib.oracle_attention.restype = ctypes.c_int
+        lib.oracle_attention.argtypes = [
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+            ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_double, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_void_p, ctypes.c_int64,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int]
+        lib.oracle_fp16_to_double.restype = ctypes.c_double
+        lib.oracle_fp16_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_to_double.restype = ctypes.c_double
+        lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+        _lib = lib
+    return _lib
+
+
+def decode16(bits: int, dtype: torch.dtype) -> float:
+    lib = _load()
+    if dtype == torch.float16:
+        return lib.oracle_fp16_to_double(bits)
+    return lib.oracle_bf16_to_double(bits)
+
+
+def _bits(t: torch.Tensor) -> np.ndarray:
+    assert t.device.type == "cpu" and t.dtype in (torch.float16, torch.bfloat16)
+    return np.ascontiguousarray(t.contiguous().view(torch.int16).numpy()).view(np.uint16)
+
+
+def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float,
+              mask="none", window=(0, 0), units=None, nthreads: int | None = None,
+              return_p: bool = False, online_bc: int = 0):
+    """fp64 attention over (B, H, N, d) 16-bit CPU tensors.
+
+    ``units`` is a list of (b*H + h, row0, row1); by default every row of
+    every head. Returns (O, LSE[, P]) as float64 numpy arrays with rows packed
+    in unit order: O (rows, d), LSE (rows,), P (rows, N).
+    ``online_bc > 0`` evaluates the online-softmax recurrence with key blocks
+    of that size instead of the direct definition.
+    """
+    lib = _load()
+    B, H, N, d = q.shape
+    assert k.shape == q.shape and v.shape == q.shape
+    assert q.dtype == k.dtype == v.dtype
+    dt = FP16 if q.dtype == torch.float16 else BF16
+    if units is None:
+        units = [(bh, 0, N) for bh in range(B * H)]
+    u = np.ascontiguousarray(np.array(units, dtype=np.int64).reshape(-1, 3))
+    rows = int((u[:, 2] - u[:, 1]).sum()) if len(u) else 0
+    O = np.zeros((rows, d), dtype=np.float64)
+    LSE = np.zeros((rows,), dtype=np.float64)
+    P = np.zeros((rows, N), dtype=np.float64) if return_p else None
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    if nthreads is None:
+        nthreads = len(os.sched_getaffinity(0))
+    rc = lib.oracle_attention(
+        qb.ctypes.data, kb.ctypes.data, vb.ctypes.data, dt, B, H, N, d,
+        float(scale), MASKS[mask], int(window[0]), int(window[1]),
+        u.ctypes.data, len(u), O.ctypes.data, LSE.ctypes.data,
+        P.ctypes.data if P is not None else None, int(online_bc), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_attention rejected its arguments")
+    if return_p:
+        return O, LSE, P
+    return O, LSE

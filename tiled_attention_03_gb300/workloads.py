@@ -1,0 +1,133 @@
+"""Seeded synthetic inputs for the attention forward pass.
+
+This module only draws random numbers and describes workload shapes. It holds
+none of the attention arithmetic, so both the CUDA path and the CPU oracle can
+be fed from it without sharing any of the method.
+
+The five workloads are the shapes the pages use: a tiny full-attention case, a
+short causal case, the benchmark shape of "ai6s.net/6a0ed07b662f9a54cb761aa2"
+(performance table: batch 4, 32 heads, head_dim 128, seq 4096), a
+sliding-window case with a sequence length that is not a tile multiple and
+peaky logits (the NaN-at-window-edges pitfall on the same page), and a long
+causal case with LLaMA-13B-like heads ("aicoding.csdn.net/6a69d3ff10ee7a33f2941f44",
+memory table, B=8 H=40).
+
+Recipe (the pages name no generator): a CPU ``torch.Generator`` seeded with
+the workload's seed draws Q, K, V in that order, each as float32
+``randn(B, H, N, d)``; Q is multiplied by ``q_std``; each is then rounded to the
+workload's 16-bit dtype. Both sides read the rounded 16-bit values.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import torch
+
+MASK_NONE = 0
+MASK_CAUSAL = 1
+MASK_WINDOW = 2
+
+MASK_NAMES = {MASK_NONE: "none", MASK_CAUSAL: "causal", MASK_WINDOW: "window"}
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    dtype: torch.dtype
+    mask: int
+    window_left: int
+    window_right: int
+    seed: int
+    q_std: float = 1.0
+
+    @property
+    def scale(self) -> float:
+        """Softmax scale 1/sqrt(d), rounded to float32 as the C ABI takes it."""
+        return float(torch.tensor(1.0 / math.sqrt(self.d), dtype=torch.float32))
+
+    @property
+    def dtype_name(self) -> str:
+        return {torch.float16: "fp16", torch.bfloat16: "bf16"}[self.dtype]
+
+    def describe(self) -> str:
+        m = MASK_NAMES[self.mask]
+        if self.mask == MASK_WINDOW:
+            m += f"({self.window_left},{self.window_right})"
+        return f"B{self.B} H{self.H} N{self.N} d{self.d} {self.dtype_name} {m}"
+
+
+WORKLOADS = [
+    Workload("tiny_full", 1, 1, 256, 64, torch.float16, MASK_NONE, 0, 0, seed=0),
+    Workload("causal_short", 1, 8, 1024, 64, torch.float16, MASK_CAUSAL, 0, 0, seed=1),
+    Workload("full_b4h32n4096d128", 4, 32, 4096, 128, torch.bfloat16, MASK_NONE, 0, 0, seed=2),
+    Workload("window_ragged_peaky", 2, 32, 4000, 128, torch.float16, MASK_WINDOW, 1024, 0,
+             seed=3, q_std=3.0),
+    Workload("causal_long_b8h40n8192", 8, 40, 8192, 128, torch.bfloat16, MASK_CAUSAL, 0, 0, seed=4),
+]
+
+BY_NAME = {w.name: w for w in WORKLOADS}
+
+
+def make_qkv(B: int, H: int, N: int, d: int, dtype: torch.dtype, seed: int,
+             q_std: float = 1.0):
+    """Return CPU tensors (Q, K, V) of shape (B, H, N, d) in ``dtype``."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    q = torch.randn(B, H, N, d, generator=g, dtype=torch.float32)
+    if q_std != 1.0:
+        q.mul_(q_std)
+    q = q.to(dtype)
+    k = torch.randn(B, H, N, d, generator=g, dtype=torch.float32).to(dtype)
+    v = torch.randn(B, H, N, d, generator=g, dtype=torch.float32).to(dtype)
+    return q, k, v
+
+
+def workload_inputs(w: Workload):
+    return make_qkv(w.B, w.H, w.N, w.d, w.dtype, w.seed, w.q_std)
+
+
+def sample_units(w: Workload, n: int = 16, block: int = 128, seed: int | None = None):
+    """Seeded sample of (bh, row0, row1) slices: always the first block, the
+    last (possibly ragged) block and one middle block, plus random ones."""
+    nblk = (w.N + block - 1) // block
+    BH = w.B * w.H
+    g = torch.Generator(device="cpu")
+    g.manual_seed(1000 + w.seed if seed is None else seed)
+    picks = [(0, 0), (BH - 1, nblk - 1), (BH // 2, nblk // 2)]
+    while len(picks) < n:
+        bh = int(torch.randint(0, BH, (1,), generator=g))
+        blk = int(torch.randint(0, nblk, (1,), generator=g))
+        if (bh, blk) not in picks:
+            picks.append((bh, blk))
+    return [(bh, blk * block, min(w.N, (blk + 1) * block)) for bh, blk in picks[:n]]
+
+
+def visible_pairs(N: int, mask: int, wl: int, wr: int) -> int:
+    """Number of (query, key) pairs a mask leaves visible for one (b, h):
+    the count the algorithmic FLOP figure is built on (4*d per pair)."""
+    if mask == MASK_NONE:
+        return N * N
+    if mask == MASK_CAUSAL:
+        wl, wr = N, 0
+    total = 0
+    for i in range(N):
+        lo = max(0, i - wl)
+        hi = min(N - 1, i + wr)
+        total += hi - lo + 1
+    return total
+
+
+def algorithmic_flops(w: Workload) -> float:
+    return 4.0 * w.d * w.B * w.H * visible_pairs(w.N, w.mask, w.window_left, w.window_right)
+
+
+def algorithmic_bytes(w: Workload) -> int:
+    """Q, K, V read once and O (16-bit) plus LSE (fp32) written once."""
+    elems = w.B * w.H * w.N * w.d
+    return 4 * elems * 2 + w.B * w.H * w.N * 4
