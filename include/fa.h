@@ -1,0 +1,108 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) attention forward library (libfa.so).
+ *
+ * The operation is the FlashAttention forward pass: for every batch b, head h
+ * and query row i,
+ *
+ *     O[b,h,i,:] = sum_j softmax_j( scale * Q[b,h,i,:] . K[b,h,j,:] + mask(i,j) ) V[b,h,j,:]
+ *     LSE[b,h,i] = ln sum_j exp( scale * Q[b,h,i,:] . K[b,h,j,:] + mask(i,j) )
+ *
+ * with mask(i,j) = 0 for a visible key and -inf for a hidden one. It follows
+ * the definition S = QK^T/sqrt(d), P = softmax(S), O = PV of
+ * "ai6s.net/6af30f4d40858c2d8819b6d5" §1 with the scale as a parameter, is
+ * computed tile by tile with the online-softmax recurrence of §2.2-§2.3 of the
+ * same page (running max m, running sum l, rescale of the output accumulator),
+ * and writes the saved statistics of §2.4 as one log-sum-exp per row
+ * (LSE = m + ln l, natural log, in units of the scaled logits). The three mask
+ * variants are those of the (None | causal | (window_left, window_right))
+ * attn_mask argument in "ai6s.net/6a0ed07b662f9a54cb761aa2", section
+ * "使用：ops-transformer 怎么调 FlashAttention"; the B x H x S x D layout is the
+ * one of "aicoding.csdn.net/6a69d3ff10ee7a33f2941f44", table "显存占用计算".
+ *
+ * All entry points are thread-safe for distinct streams and never throw.
+ */
+#ifndef TILED_ATTENTION_FA_H
+#define TILED_ATTENTION_FA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1, /* a null/misaligned/aliased pointer, a bad size or enum, a bad scale */
+    FA_ERR_UNSUPPORTED = 2, /* a valid request this build does not implement (head dim, device) */
+    FA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (launch, attribute, tensor map) */
+    FA_ERR_TIMEOUT = 4      /* a bounded in-kernel wait ran out (reported by fa_sync_status) */
+} fa_status;
+
+typedef enum {
+    FA_MASK_NONE = 0,   /* every key 0..N-1 is visible */
+    FA_MASK_CAUSAL = 1, /* key j visible to query i iff j <= i */
+    FA_MASK_WINDOW = 2  /* key j visible to query i iff i - window_left <= j <= i + window_right */
+} fa_mask_mode;
+
+typedef enum { FA_DTYPE_FP16 = 0, FA_DTYPE_BF16 = 1 } fa_dtype;
+
+/*
+ * fa_forward -- enqueue one attention forward pass on `stream`.
+ *
+ * Q, K, V : device pointers, contiguous B x H x N x d tensors of `dtype`
+ *           (row-major: d fastest, then N, then H, then B). Read only.
+ * O       : device pointer, contiguous B x H x N x d of `dtype`. Written with
+ *           O/l rounded to nearest-even. Must not overlap Q, K, V or LSE.
+ * LSE     : device pointer, contiguous B x H x N float32. Written.
+ * B, H, N : >= 1. Any N is accepted (no padding is required of the caller;
+ *           rows and keys past N are handled inside the kernel).
+ * d       : head dimension; 64 and 128 are implemented (else FA_ERR_UNSUPPORTED).
+ * scale   : multiplier of the logits, finite and > 0 (typically 1/sqrt(d)).
+ * mask_mode, window_left, window_right : see fa_mask_mode. The window
+ *           arguments are read only for FA_MASK_WINDOW and must then be >= 0
+ *           (values >= N act as N). Every query sees at least itself.
+ * dtype   : element type of Q, K, V and O; the products are exact and every
+ *           sum, max, exponent and the accumulator are float32.
+ * stream  : a cudaStream_t (NULL = the legacy default stream).
+ *
+ * Ownership: every pointer is owned by the caller; the library keeps none and
+ * allocates no device memory per call. All four data pointers must be 16-byte
+ * aligned and on the current device.
+ *
+ * Errors: arguments are checked before anything is enqueued; an invalid call
+ * returns FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED and launches nothing. A
+ * launch failure returns FA_ERR_CUDA. The call is asynchronous: a device-side
+ * timeout of a bounded wait is reported by a later fa_sync_status().
+ */
+fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                     int64_t B, int64_t H, int64_t N, int64_t d, float scale,
+                     fa_mask_mode mask_mode, int64_t window_left, int64_t window_right,
+                     fa_dtype dtype, void *stream);
+
+/* Static, NUL-terminated description of a status code. Never NULL. */
+const char *fa_status_string(fa_status status);
+
+/*
+ * fa_sync_status -- synchronise `stream`, then read and clear the device
+ * status word of the current device. Returns FA_ERR_TIMEOUT if any kernel
+ * since the last call gave up on a bounded wait, FA_ERR_CUDA if the
+ * synchronisation itself failed, else FA_OK.
+ */
+fa_status fa_sync_status(void *stream);
+
+/*
+ * fa_set_wait_budget_ns -- upper bound, in nanoseconds of GPU global time, of
+ * every in-kernel wait of later launches (default 2e9, or the value of the
+ * environment variable FA_WAIT_BUDGET_MS read at the first call). 0 restores
+ * the default. Process-wide.
+ */
+void fa_set_wait_budget_ns(uint64_t ns);
+
+/* Number of kernels this library has launched in this process. */
+int64_t fa_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TILED_ATTENTION_FA_H */

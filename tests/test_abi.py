@@ -1,0 +1,80 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/*.h declares, and rejects invalid arguments before touching CUDA."""
+
+import ctypes
+
+import pytest
+
+import tiled_attention_03_gb300 as fa
+from tiled_attention_03_gb300.binding import declared_functions, load_library
+from tiled_attention_03_gb300.build import build_library
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_library()
+    return load_library()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert {"fa_forward", "fa_status_string", "fa_sync_status"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        s = fa.fa_status_string(code)
+        assert s.startswith("FA_")
+    assert "unknown" in fa.fa_status_string(99)
+
+
+A = 0x10000  # aligned fake addresses: never dereferenced, every call below fails its checks first
+B_ = 0x20000000
+C = 0x40000000
+O_ = 0x60000000
+L_ = 0x70000000
+
+
+def call(lib, q=A, k=B_, v=C, o=O_, lse=L_, B=1, H=1, N=16, d=64, scale=0.125, mask=0,
+         wl=0, wr=0, dtype=0):
+    return lib.fa_forward(q, k, v, o, lse, B, H, N, d, scale, mask, wl, wr, dtype, None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(q=0), dict(k=0), dict(v=0), dict(o=0), dict(lse=0),
+    dict(B=0), dict(H=0), dict(N=0), dict(d=0), dict(N=-5),
+    dict(dtype=2), dict(dtype=-1), dict(mask=3), dict(mask=-1),
+    dict(mask=2, wl=-1), dict(mask=2, wr=-1),
+    dict(scale=0.0), dict(scale=-0.5), dict(scale=float("inf")), dict(scale=float("nan")),
+    dict(q=A + 8), dict(o=O_ + 2), dict(lse=L_ + 4),
+    dict(o=A),              # O aliases Q
+    dict(lse=O_ + 64),      # LSE inside O
+])
+def test_invalid_arguments(lib, kw):
+    assert call(lib, **kw) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("d", [32, 96, 256, 80])
+def test_unsupported_head_dim(lib, d):
+    assert call(lib, d=d) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_window_args_ignored_unless_window(lib):
+    # Negative window values are only an error in window mode: in the other modes
+    # the call gets past argument checks (and then fails on this GPU-less host).
+    rc = call(lib, mask=1, wl=-3, wr=-3)
+    assert rc != fa.FA_ERR_INVALID_ARG
+
+
+def test_wait_budget_and_counter(lib):
+    fa.fa_set_wait_budget_ns(0)
+    assert fa.fa_launch_count() >= 0
+
+
+def test_python_binding_rejects_cpu_tensors():
+    import torch
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.float16)
+    with pytest.raises(fa.FaError):
+        fa.fa_forward(q, q, q, q.clone(), torch.zeros(1, 1, 8), 0.125)

@@ -1,0 +1,145 @@
+"""Python binding of the C ABI in include/fa.h (libfa.so), via ctypes.
+
+Argument marshalling only: every step of the attention forward pass runs in
+the library's CUDA kernel. PyTorch supplies device memory and streams. There
+is no fallback: if the library is missing or the device is unsupported, the
+calls raise.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+from .build import INCLUDE, LIB
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
+FA_MASK_NONE, FA_MASK_CAUSAL, FA_MASK_WINDOW = range(3)
+FA_DTYPE_FP16, FA_DTYPE_BF16 = range(2)
+
+_MASKS = {"none": FA_MASK_NONE, "causal": FA_MASK_CAUSAL, "window": FA_MASK_WINDOW,
+          FA_MASK_NONE: FA_MASK_NONE, FA_MASK_CAUSAL: FA_MASK_CAUSAL, FA_MASK_WINDOW: FA_MASK_WINDOW}
+_DTYPES = {torch.float16: FA_DTYPE_FP16, torch.bfloat16: FA_DTYPE_BF16}
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, what: str = "fa_forward"):
+        self.status = status
+        super().__init__(f"{what}: {fa_status_string(status)}")
+
+
+_lib = None
+
+
+def load_library(path: str = LIB) -> ctypes.CDLL:
+    """Load libfa.so (build it first with ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library not built: {path} is missing (run __graft_entry__.build())")
+    lib = ctypes.CDLL(path)
+    lib.fa_forward.restype = ctypes.c_int
+    lib.fa_forward.argtypes = [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_float,
+        ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_status_string.argtypes = [ctypes.c_int]
+    lib.fa_sync_status.restype = ctypes.c_int
+    lib.fa_sync_status.argtypes = [ctypes.c_void_p]
+    lib.fa_set_wait_budget_ns.restype = None
+    lib.fa_set_wait_budget_ns.argtypes = [ctypes.c_uint64]
+    lib.fa_launch_count.restype = ctypes.c_int64
+    lib.fa_launch_count.argtypes = []
+    _lib = lib
+    return lib
+
+
+def declared_functions() -> list[str]:
+    """Names of the functions include/*.h declares (for export checks)."""
+    names = []
+    for fn in sorted(os.listdir(INCLUDE)):
+        if fn.endswith(".h"):
+            with open(os.path.join(INCLUDE, fn)) as f:
+                src = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+            names += re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", src)
+    return sorted(set(names))
+
+
+def fa_status_string(status: int) -> str:
+    return load_library().fa_status_string(int(status)).decode()
+
+
+def fa_sync_status(stream=None) -> int:
+    return load_library().fa_sync_status(_stream_handle(stream))
+
+
+def fa_set_wait_budget_ns(ns: int) -> None:
+    load_library().fa_set_wait_budget_ns(int(ns))
+
+
+def fa_launch_count() -> int:
+    return load_library().fa_launch_count()
+
+
+def _stream_handle(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def fa_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+               lse: torch.Tensor, scale: float, mask_mode=FA_MASK_NONE, window_left: int = 0,
+               window_right: int = 0, stream=None) -> None:
+    """Enqueue fa_forward on device tensors (B, H, N, d) -> o, lse (B, H, N)."""
+    lib = load_library()
+    for t in (q, k, v, o, lse):
+        if not t.is_cuda or not t.is_contiguous():
+            raise FaError(FA_ERR_INVALID_ARG)
+    if q.dtype not in _DTYPES or k.dtype != q.dtype or v.dtype != q.dtype or o.dtype != q.dtype \
+            or lse.dtype != torch.float32:
+        raise FaError(FA_ERR_INVALID_ARG)
+    B, H, N, d = q.shape
+    if k.shape != q.shape or v.shape != q.shape or o.shape != q.shape or lse.shape != (B, H, N):
+        raise FaError(FA_ERR_INVALID_ARG)
+    rc = lib.fa_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                        B, H, N, d, float(scale), _MASKS[mask_mode], int(window_left),
+                        int(window_right), _DTYPES[q.dtype], _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc)
+
+
+def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
+            mask="none", window=(0, 0), stream=None):
+    """Attention forward: returns (O, LSE).
+
+    Device tensors run in place on the device. Host tensors are copied to the
+    current CUDA device, processed, and the results copied back to host
+    memory (pinned host inputs make these copies asynchronous).
+    """
+    host = not q.is_cuda
+    if scale is None:
+        scale = q.shape[-1] ** -0.5
+    if host:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        q = q.to(dev, non_blocking=True)
+        k = k.to(dev, non_blocking=True)
+        v = v.to(dev, non_blocking=True)
+    q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    fa_forward(q, k, v, o, lse, scale, mask, window[0], window[1], stream)
+    if host:
+        o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        o_h.copy_(o, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        return o_h, lse_h
+    return o, lse

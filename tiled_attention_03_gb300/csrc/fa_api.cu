@@ -1,0 +1,259 @@
+// fa_api.cu -- the C ABI declared in include/fa.h: argument checks, TMA tensor
+// maps, launch of the sm_103a attention kernel, and the device status word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_fwd_kernel.cuh"
+
+namespace {
+
+// Device status word: [code, role, iteration, block]. Written by a kernel whose
+// bounded wait ran out; read and cleared by fa_sync_status.
+__device__ unsigned int g_fa_status[4];
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultBudgetNs = 2000000000ull;
+
+std::atomic<int64_t> g_launches{0};
+std::atomic<uint64_t> g_budget_ns{0};
+
+struct DeviceState {
+    std::once_flag once;
+    cudaError_t init_err = cudaSuccess;
+    int cc_major = 0, cc_minor = 0;
+    unsigned int *status = nullptr;
+};
+DeviceState g_dev[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+std::once_flag g_encode_once;
+EncodeTiledFn g_encode = nullptr;
+
+EncodeTiledFn encode_fn() {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    });
+    return g_encode;
+}
+
+uint64_t wait_budget() {
+    uint64_t b = g_budget_ns.load();
+    if (b == 0) {
+        b = kDefaultBudgetNs;
+        if (const char *e = std::getenv("FA_WAIT_BUDGET_MS")) {
+            char *end = nullptr;
+            const double ms = std::strtod(e, &end);
+            if (end != e && ms > 0 && ms < 1e9) b = static_cast<uint64_t>(ms * 1e6);
+        }
+        g_budget_ns.store(b);
+    }
+    return b;
+}
+
+template <int D, bool BF16>
+cudaError_t configure_kernel() {
+    return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, BF16>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                fa::SmemLayout<D>::kAlloc);
+}
+
+DeviceState *device_state(int dev) {
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    DeviceState &s = g_dev[dev];
+    std::call_once(s.once, [&s, dev] {
+        cudaError_t e = cudaDeviceGetAttribute(&s.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&s.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (e == cudaSuccess && s.cc_major == 10 && s.cc_minor == 3) {
+            void *addr = nullptr;
+            e = cudaGetSymbolAddress(&addr, g_fa_status);
+            s.status = static_cast<unsigned int *>(addr);
+            if (e == cudaSuccess) e = configure_kernel<64, false>();
+            if (e == cudaSuccess) e = configure_kernel<64, true>();
+            if (e == cudaSuccess) e = configure_kernel<128, false>();
+            if (e == cudaSuccess) e = configure_kernel<128, true>();
+        }
+        s.init_err = e;
+    });
+    return &s;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+bool on_device(const void *p, int dev) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (a.type == cudaMemoryTypeDevice) return a.device == dev;
+    if (a.type == cudaMemoryTypeManaged) return true;
+    return false;
+}
+
+// 3-D map over a contiguous (B*H) x N x d 16-bit tensor, box = 64 columns x 128 rows,
+// 128-byte swizzle; rows past N read as zero.
+bool make_map(CUtensorMap *map, const void *base, bool bf16, int64_t BH, int64_t N, int64_t d) {
+    EncodeTiledFn enc = encode_fn();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                                static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * 2),
+                                   static_cast<cuuint64_t>(N * d * 2)};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r =
+        enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+            const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int D, bool BF16>
+cudaError_t launch(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                   const fa::FwdParams &p, int64_t blocks, cudaStream_t stream) {
+    fa::fa_fwd_kernel<D, BF16><<<static_cast<unsigned>(blocks), fa::kThreads,
+                                 fa::SmemLayout<D>::kAlloc, stream>>>(q, k, v, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *fa_status_string(fa_status s) {
+    switch (s) {
+        case FA_OK: return "FA_OK: success";
+        case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: invalid argument";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: not supported by this build or device";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call failed";
+        case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a bounded in-kernel wait ran out";
+    }
+    return "unknown fa_status";
+}
+
+void fa_set_wait_budget_ns(uint64_t ns) { g_budget_ns.store(ns); }
+
+int64_t fa_launch_count(void) { return g_launches.load(); }
+
+fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float *LSE, int64_t B,
+                     int64_t H, int64_t N, int64_t d, float scale, fa_mask_mode mask_mode,
+                     int64_t window_left, int64_t window_right, fa_dtype dtype, void *stream) {
+    // ---- host-side checks: nothing is enqueued on failure
+    if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
+    if (mask_mode != FA_MASK_NONE && mask_mode != FA_MASK_CAUSAL && mask_mode != FA_MASK_WINDOW)
+        return FA_ERR_INVALID_ARG;
+    if (mask_mode == FA_MASK_WINDOW && (window_left < 0 || window_right < 0))
+        return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
+        return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    // Size limits of this implementation: 32-bit row indices and grid.
+    if (N > (int64_t{1} << 30) || B * H > (int64_t{1} << 31)) return FA_ERR_UNSUPPORTED;
+    const int64_t BH = B * H;
+    const int64_t q_tiles = (N + fa::kBM - 1) / fa::kBM;
+    const int64_t blocks = BH * q_tiles;
+    if (blocks > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+    const size_t elems = static_cast<size_t>(BH) * static_cast<size_t>(N) * static_cast<size_t>(d);
+    const size_t tbytes = elems * 2, lbytes = static_cast<size_t>(BH) * N * sizeof(float);
+    if (overlaps(O, tbytes, Q, tbytes) || overlaps(O, tbytes, K, tbytes) ||
+        overlaps(O, tbytes, V, tbytes) || overlaps(O, tbytes, LSE, lbytes) ||
+        overlaps(LSE, lbytes, Q, tbytes) || overlaps(LSE, lbytes, K, tbytes) ||
+        overlaps(LSE, lbytes, V, tbytes))
+        return FA_ERR_INVALID_ARG;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+    }
+    DeviceState *ds = device_state(dev);
+    if (ds == nullptr) return FA_ERR_UNSUPPORTED;
+    if (ds->init_err != cudaSuccess) return FA_ERR_CUDA;
+    if (!(ds->cc_major == 10 && ds->cc_minor == 3)) return FA_ERR_UNSUPPORTED;
+    if (!on_device(Q, dev) || !on_device(K, dev) || !on_device(V, dev) || !on_device(O, dev) ||
+        !on_device(LSE, dev))
+        return FA_ERR_INVALID_ARG;
+
+    const bool bf16 = dtype == FA_DTYPE_BF16;
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, Q, bf16, BH, N, d) || !make_map(&mk, K, bf16, BH, N, d) ||
+        !make_map(&mv, V, bf16, BH, N, d))
+        return FA_ERR_CUDA;
+
+    fa::FwdParams p{};
+    p.O = O;
+    p.LSE = LSE;
+    p.N = static_cast<int>(N);
+    p.num_q_tiles = static_cast<int>(q_tiles);
+    int64_t wl = N, wr = N;
+    if (mask_mode == FA_MASK_CAUSAL) wr = 0;
+    if (mask_mode == FA_MASK_WINDOW) {
+        wl = window_left < N ? window_left : N;
+        wr = window_right < N ? window_right : N;
+    }
+    p.wl = static_cast<int>(wl);
+    p.wr = static_cast<int>(wr);
+    p.heavy_first = wr < N ? 1 : 0;
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    p.wait_budget_ns = wait_budget();
+    p.status = ds->status;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (d == 64)
+        e = bf16 ? launch<64, true>(mq, mk, mv, p, blocks, st)
+                 : launch<64, false>(mq, mk, mv, p, blocks, st);
+    else
+        e = bf16 ? launch<128, true>(mq, mk, mv, p, blocks, st)
+                 : launch<128, false>(mq, mk, mv, p, blocks, st);
+    if (e != cudaSuccess) return FA_ERR_CUDA;
+    g_launches.fetch_add(1);
+    return FA_OK;
+}
+
+fa_status fa_sync_status(void *stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+    }
+    unsigned int st[4] = {0, 0, 0, 0};
+    if (cudaMemcpyFromSymbol(st, g_fa_status, sizeof(st)) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+    }
+    if (st[0] == 0) return FA_OK;
+    const unsigned int zero[4] = {0, 0, 0, 0};
+    if (cudaMemcpyToSymbol(g_fa_status, zero, sizeof(zero)) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+    }
+    return FA_ERR_TIMEOUT;
+}
+
+}  // extern "C"
