@@ -1,0 +1,340 @@
+"""Benchmark of the attention forward pass on GB300.
+
+One step = one forward pass (fa_forward, one kernel launch) over the
+B4 H32 N4096 d128 bf16 non-causal workload, inputs resident in HBM. Prints one
+JSON line (rank 0). Under torchrun every rank runs its own replica of the
+workload (independent problems, no collective on the data path) and the
+max-over-ranks time is reported with the whole-job throughput.
+
+--impl reference times the fp64 CPU oracle on this host's cores, on a bounded
+sample of the same workload, in the same metric.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "attn fwd TFLOP/s (% of GB300 BF16 tensor peak); tokens/s @B4 H32 N4096 d128"
+WORKLOAD = "full_b4h32n4096d128"
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+KERNEL_SOURCES = ("tiled_attention_03_gb300/csrc/fa_fwd_kernel.cuh",
+                  "tiled_attention_03_gb300/csrc/ptx.cuh")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fa_fwd_kernel_b4h32n4096d128_traffic.txt")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    try:
+        vals = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    key, val = line.split(":", 1)
+                    vals[key.strip()] = val.strip()
+        if vals.get("kernel_source_hash") == kernel_source_hash():
+            return float(vals["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        pass
+    return None
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    def __init__(self, gpu_index: int, interval_ms: int = 100):
+        self.proc = None
+        self.out = None
+        try:
+            self.out = open(_tmp_path("clocks"), "w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={interval_ms}"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.seek(0)
+        rows = [r.split(",") for r in self.out.read().strip().splitlines() if r.count(",") >= 8]
+        self.out.close()
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]
+                          and "Not" not in r[5 + i]})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _tmp_path(tag):
+    d = os.path.join(ROOT, "gpurun_out") if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else "/tmp"
+    return os.path.join(d, f".bench_{tag}_{os.getpid()}.csv")
+
+
+def dist_setup(n_gpus: int):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_slab(w):
+    """One (b, h) slab of the workload's shape, drawn with its recipe."""
+    from tiled_attention_03_gb300.workloads import make_qkv
+    return make_qkv(1, 1, w.N, w.d, w.dtype, seed=w.seed, q_std=w.q_std)
+
+
+def cpu_oracle_rate(w, min_seconds: float, max_units: int | None = None, slab=None):
+    """Time the fp64 oracle on a sample of (1 head, 128-row block) units of the
+    workload, using every core of this host. Returns (TFLOP/s, cores, sample, seconds)."""
+    import oracle
+    from tiled_attention_03_gb300.workloads import visible_in_rows
+    cores = len(os.sched_getaffinity(0))
+    q, k, v = oracle_slab(w) if slab is None else slab
+    nblk = (w.N + 127) // 128
+    n = cores if max_units is None else min(cores, max_units)
+    while True:
+        units = [(0, (u % nblk) * 128, min(w.N, (u % nblk + 1) * 128)) for u in range(n)]
+        t0 = time.perf_counter()
+        oracle.attention(q, k, v, w.scale, {0: "none", 1: "causal", 2: "window"}[w.mask],
+                         (w.window_left, w.window_right), units=units, nthreads=cores)
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds or (max_units is not None and n >= max_units) or n >= 64 * cores:
+            break
+        n *= 2
+    # algorithmic flops of the sampled rows: 4 d per visible (query, key) pair
+    pairs = sum(visible_in_rows(w.N, w.mask, w.window_left, w.window_right, r0, r1)
+                for _, r0, r1 in units)
+    flops = 4.0 * w.d * pairs
+    return flops / dt / 1e12, cores, f"{len(units)} x (1 head, 128-row block, all {w.N} keys)", dt
+
+
+def run_reference(args, w):
+    rank, world, _ = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), 0
+    if rank != 0:
+        return
+    slab = oracle_slab(w)
+    n = len(os.sched_getaffinity(0))
+    for _ in range(args.warmup):
+        cpu_oracle_rate(w, 0.0, max_units=n, slab=slab)
+    flops_total, secs_total = 0.0, 0.0
+    for _ in range(args.steps):
+        r, cores, sample, dt = cpu_oracle_rate(w, 0.0, max_units=n, slab=slab)
+        flops_total += r * 1e12 * dt
+        secs_total += dt
+    value = flops_total / secs_total / 1e12
+    wall = secs_total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000 * wall / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "mask": {0: "none", 1: "causal", 2: "window"}[w.mask], "input_dtype": w.dtype_name,
+                   "step": "oracle over one bounded sample of the workload"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, w, q_h, k_h, v_h, mask, stream, dev, world, flops):
+    """Same metric through the public API (tiled_attention_03_gb300.forward) with
+    pinned host inputs: every step copies Q, K, V to the device, runs the
+    kernel and copies O and LSE back."""
+    import tiled_attention_03_gb300 as fa
+    qp, kp, vp = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
+    for _ in range(2):
+        fa.forward(qp, kp, vp, w.scale, mask, (w.window_left, w.window_right))
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    e2 = torch.cuda.Event(enable_timing=True)
+    e3 = torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for _ in range(args.e2e_steps):
+        fa.forward(qp, kp, vp, w.scale, mask, (w.window_left, w.window_right))
+    e3.record(stream)
+    torch.cuda.synchronize(dev)
+    wall_ms = (time.perf_counter() - t0) * 1e3 / args.e2e_steps
+    e2e_ms = max_over_ranks(max(e2.elapsed_time(e3) / args.e2e_steps, wall_ms), world)
+    elems = q_h.numel()
+    h2d = 3 * elems * q_h.element_size()
+    d2h = elems * q_h.element_size() + (elems // w.d) * 4
+    return {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from tiled_attention_03_gb300.workloads import BY_NAME, algorithmic_flops
+    w = BY_NAME[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import tiled_attention_03_gb300 as fa
+    from tiled_attention_03_gb300.workloads import workload_inputs
+
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    fa.load_library()
+
+    q_h, k_h, v_h = workload_inputs(w)
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=dev)
+    mask = {0: "none", 1: "causal", 2: "window"}[w.mask]
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fa.fa_forward(q, k, v, o, lse, w.scale, mask, w.window_left, w.window_right, stream)
+
+    for _ in range(args.warmup):
+        step()
+    st = fa.fa_sync_status(stream)
+    if st != fa.FA_OK:
+        raise SystemExit(f"device status after warm-up: {fa.fa_status_string(st)}")
+
+    flops = algorithmic_flops(w)
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    launches0 = fa.fa_launch_count()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    launches = fa.fa_launch_count() - launches0
+    clocks = sampler.stop() if sampler else None
+    st = fa.fa_sync_status(stream)
+    if st != fa.FA_OK:
+        raise SystemExit(f"device status after the timed region: {fa.fa_status_string(st)}")
+    ms_local = e0.elapsed_time(e1)
+    ms_total = max_over_ranks(ms_local, world)
+    ms_step = ms_total / args.steps
+    value = world * flops / (ms_step * 1e-3) / 1e12
+    kernel_ms = ms_local / args.steps  # one launch per step on this stream
+
+    # ---- end to end through the public API with pinned host buffers
+    e2e = None
+    if args.e2e_steps > 0:
+        e2e = run_e2e(args, w, q_h, k_h, v_h, mask, stream, dev, world, flops)
+
+    if rank == 0:
+        peak_tf, _, peak_src = peaks()
+        achieved = flops / (kernel_ms * 1e-3) / 1e12
+        traffic = measured_traffic()
+        cpu = None
+        if args.cpu_seconds > 0:
+            cpu_v, cores, sample, _ = cpu_oracle_rate(w, args.cpu_seconds)
+            cpu = {"value": cpu_v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                   "sample": sample}
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype_name, "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                       "mask": mask, "seed": w.seed,
+                       "parallelism": f"{world} independent replica(s), no collective",
+                       "l2": (f"inputs (3 x {q.numel() * 2 / 1e6:.0f} MB) larger than L2, no flush"
+                              if 3 * q.numel() * 2 > 129e6 else "inputs smaller than L2, no flush")},
+            "tokens_per_s": world * w.B * w.N / (ms_step * 1e-3),
+            "pct_of_peak": 100.0 * value / (world * peak_tf),
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf,
+                         "unit": "TFLOP/s", "frac": achieved / peak_tf,
+                         "traffic": traffic, "peak_source": f"{peak_src} bf16 burst",
+                         "kernel": f"fa_fwd_kernel<{w.d}, {w.dtype_name}>"},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

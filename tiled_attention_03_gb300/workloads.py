@@ -108,19 +108,25 @@ def sample_units(w: Workload, n: int = 16, block: int = 128, seed: int | None = 
     return [(bh, blk * block, min(w.N, (blk + 1) * block)) for bh, blk in picks[:n]]
 
 
-def visible_pairs(N: int, mask: int, wl: int, wr: int) -> int:
-    """Number of (query, key) pairs a mask leaves visible for one (b, h):
-    the count the algorithmic FLOP figure is built on (4*d per pair)."""
+def visible_in_rows(N: int, mask: int, wl: int, wr: int, r0: int, r1: int) -> int:
+    """Number of (query, key) pairs a mask leaves visible for query rows
+    [r0, r1) of one (b, h): the count the algorithmic FLOP figure is built on
+    (4*d per pair)."""
     if mask == MASK_NONE:
-        return N * N
+        return (r1 - r0) * N
     if mask == MASK_CAUSAL:
         wl, wr = N, 0
     total = 0
-    for i in range(N):
+    for i in range(r0, r1):
         lo = max(0, i - wl)
         hi = min(N - 1, i + wr)
         total += hi - lo + 1
     return total
+
+
+def visible_pairs(N: int, mask: int, wl: int, wr: int) -> int:
+    """Visible (query, key) pairs of one (b, h)."""
+    return visible_in_rows(N, mask, wl, wr, 0, N)
 
 
 def algorithmic_flops(w: Workload) -> float:
