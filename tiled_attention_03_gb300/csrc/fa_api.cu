@@ -28,7 +28,7 @@ std::atomic<uint64_t> g_budget_ns{0};
 struct DeviceState {
     std::once_flag once;
     cudaError_t init_err = cudaSuccess;
-    int cc_major = 0, cc_minor = 0;
+    int cc_major = 0, cc_minor = 0, sm_count = 0;
     unsigned int *status = nullptr;
 };
 DeviceState g_dev[kMaxDevices];
@@ -66,8 +66,15 @@ uint64_t wait_budget() {
     return b;
 }
 
+// Opt in to the kernel's shared memory, and check that the registers a launch
+// allocates cover the kernel's setmaxnreg split (a split above them would make
+// setmaxnreg.inc wait forever).
 template <int D, bool BF16>
 cudaError_t configure_kernel() {
+    cudaFuncAttributes attr{};
+    cudaError_t e = cudaFuncGetAttributes(&attr, fa::fa_fwd_kernel<D, BF16>);
+    if (e != cudaSuccess) return e;
+    if (attr.numRegs * fa::kThreads < fa::kRegsNeeded) return cudaErrorInvalidConfiguration;
     return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, BF16>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 fa::SmemLayout<D>::kAlloc);
@@ -80,6 +87,8 @@ DeviceState *device_state(int dev) {
         cudaError_t e = cudaDeviceGetAttribute(&s.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
         if (e == cudaSuccess)
             e = cudaDeviceGetAttribute(&s.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&s.sm_count, cudaDevAttrMultiProcessorCount, dev);
         if (e == cudaSuccess && s.cc_major == 10 && s.cc_minor == 3) {
             void *addr = nullptr;
             e = cudaGetSymbolAddress(&addr, g_fa_status);
@@ -176,9 +185,9 @@ fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float
     // Size limits of this implementation: 32-bit row indices and grid.
     if (N > (int64_t{1} << 30) || B * H > (int64_t{1} << 31)) return FA_ERR_UNSUPPORTED;
     const int64_t BH = B * H;
-    const int64_t q_tiles = (N + fa::kBM - 1) / fa::kBM;
-    const int64_t blocks = BH * q_tiles;
-    if (blocks > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+    const int64_t n_qb = (N + fa::kUnitRows - 1) / fa::kUnitRows;
+    const int64_t n_units = BH * n_qb;
+    if (n_units > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
     const size_t elems = static_cast<size_t>(BH) * static_cast<size_t>(N) * static_cast<size_t>(d);
     const size_t tbytes = elems * 2, lbytes = static_cast<size_t>(BH) * N * sizeof(float);
     if (overlaps(O, tbytes, Q, tbytes) || overlaps(O, tbytes, K, tbytes) ||
@@ -210,7 +219,8 @@ fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float
     p.O = O;
     p.LSE = LSE;
     p.N = static_cast<int>(N);
-    p.num_q_tiles = static_cast<int>(q_tiles);
+    p.n_units = static_cast<int>(n_units);
+    p.n_qb = static_cast<int>(n_qb);
     int64_t wl = N, wr = N;
     if (mask_mode == FA_MASK_CAUSAL) wr = 0;
     if (mask_mode == FA_MASK_WINDOW) {
@@ -224,6 +234,8 @@ fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float
     p.wait_budget_ns = wait_budget();
     p.status = ds->status;
 
+    // Persistent grid: one CTA per SM (each holds the SM's whole tensor memory).
+    const int64_t blocks = n_units < ds->sm_count ? n_units : ds->sm_count;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (d == 64)

@@ -1,6 +1,6 @@
 // fa_fwd_kernel.cuh -- attention forward for sm_103a: TMA -> shared memory ->
 // tcgen05.mma with fp32 accumulators in tensor memory -> online softmax in
-// registers -> O and LSE.
+// registers -> P back into tensor memory -> tcgen05.mma -> O and LSE.
 //
 // Method (the pages): Q is cut into Br-row blocks and K/V into Bc-row blocks,
 // the outer loop runs over Q blocks and the inner loop over K/V blocks so that
@@ -11,21 +11,36 @@
 // accumulator is divided by l once after the last block and m, l are kept as
 // LSE (§2.4 and the teaching kernel's final normalisation, §2.5). exp2 with
 // log2(e) folded into the scale and the block-level skip of fully masked K/V
-// blocks are the refinements listed at the end of §2.5. The mask variants are
+// blocks are refinements listed at the end of §2.5. The mask variants are
 // applied right after the score block is formed, as the catlass epilogue does
-// ("ai6s.net/6a0ed07b662f9a54cb761aa2", Epilogue Builder).
+// ("ai6s.net/6a0ed07b662f9a54cb761aa2", Epilogue Builder). Two Q blocks are
+// kept in flight so that the matrix unit works on one while the softmax of the
+// other runs: the GPU form of the Cube/Vector overlap of
+// "ai6s.net/6af30f4d40858c2d8819b6d5" §3.3 (1). The CTA grid is persistent
+// and walks a static list of work units, the form of the per-core Q-block
+// split of the same page's host tiling (§3.2-§3.3).
 //
-// GB300 mapping of one CTA (192 threads) = one 128-row Q tile of one (b, h):
-//   warp 4  : TMA producer. Q once; K_j and V_j into a 2-stage (d = 128) or
-//             4-stage (d = 64) ring.
-//   warp 5  : MMA issuer (one thread). S_j = Q K_j^T into one of two TMEM
-//             S buffers, then O += P_{j-1} V_{j-1} into the TMEM O accumulator.
-//   warps 0-3: softmax; thread t owns query row t (= TMEM lane t). Reads S_j
-//             with tcgen05.ld, masks, updates m and l, writes P_j (16-bit)
-//             to shared memory in the MMA's swizzled K-major layout, rescales
-//             its O row in TMEM, and finally writes O / l and LSE.
-// The two S buffers let the tensor core compute S_{j+1} and P_{j-1} V_{j-1}
-// while the softmax warps work on S_j.
+// One CTA (384 threads) runs on each SM and loops over work units; a unit is
+// 256 query rows (two 128-row Q tiles, t = 0, 1) of one (b, h):
+//   warps 0-3 : softmax of Q tile 0 (thread = query row = TMEM lane)
+//   warps 4-7 : softmax of Q tile 1
+//   warp 8    : TMA producer: Q tiles, K_j and V_j into a multi-stage ring
+//   warp 9    : MMA issuer (one thread)
+//   warps 10-11: idle (they complete warpgroup 2, whose registers move to the
+//               softmax warpgroups with setmaxnreg)
+// Tensor memory (512 columns): S_t at columns 128 t (fp32, 128 keys), O_t at
+// 256 + t d (fp32). After the softmax of S_t(j) the probabilities P_t(j) are
+// written as packed 16-bit pairs over the first 64 columns of S_t, and
+// O_t += P_t(j) V_j reads them from tensor memory (A operand in TMEM).
+// Issue order per K/V tile j:  S_0(j) S_1(j) | O_0 += P_0 V_j | O_1 += P_1 V_j,
+// with S_t(j+1) issued only once O_t += P_t(j) V_j has completed (it overwrites
+// the columns that MMA reads). The softmax of tile 0 runs while the tensor core
+// computes S_1(j) and the softmax of tile 1 while it computes O_0 += P_0 V_j.
+//
+// The output accumulator is rescaled lazily: the reference max of a row only
+// moves when a block's max exceeds it by more than 2^8 (in log2 units), so
+// every probability stays below 256 and O and l share the same reference,
+// which keeps the result exact; most blocks then need no rescale at all.
 //
 // Every wait is bounded (global-timer budget); on expiry the CTA records the
 // failure in a status word, drains its own copies and MMAs, frees its tensor
@@ -39,12 +54,22 @@
 
 namespace fa {
 
-constexpr int kBM = 128;          // query rows per tile = TMEM lanes
-constexpr int kBN = 128;          // keys per K/V tile
-constexpr int kThreads = 192;     // 4 softmax warps + TMA warp + MMA warp
+constexpr int kBM = 128;       // query rows per Q tile = TMEM lanes
+constexpr int kBN = 128;       // keys per K/V tile
+constexpr int kQTiles = 2;     // Q tiles per work unit
+constexpr int kUnitRows = kBM * kQTiles;
+constexpr int kThreads = 384;  // 2 softmax warpgroups + a warpgroup with the TMA and MMA warps
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;
+// Per-thread registers after setmaxnreg. Their sum over the CTA must not exceed
+// what the launch allocated (threads x registers of the compiled kernel); the
+// host checks this before the first launch.
+constexpr int kRegsSoftmax = 224;
+constexpr int kRegsControl = 56;
+constexpr int kRegsNeeded = 2 * 128 * kRegsSoftmax + 128 * kRegsControl;
 constexpr int kRegionBytes = 128 * 128;  // 128 rows x 128 B: one 64-column swizzle region
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 256;  // first TMEM column of the O accumulator
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: probabilities stay <= 2^8
 
 constexpr unsigned kStatusTimeout = 4;  // same value as FA_ERR_TIMEOUT
 enum : int { kRoleSoftmax = 1, kRoleTma = 2, kRoleMma = 3 };
@@ -53,53 +78,81 @@ struct FwdParams {
     void *O;
     float *LSE;
     int N;            // sequence length
-    int num_q_tiles;  // ceil(N / kBM)
-    int heavy_first;  // 1: within a head, visit Q tiles from the last (most keys) to the first
+    int n_units;      // (b*H + h, 256-row block) work units
+    int n_qb;         // 256-row blocks per head: ceil(N / 256)
+    int heavy_first;  // 1: within a head, visit row blocks from the last (most keys) to the first
     int wl, wr;       // key j visible to query i iff i - wl <= j <= i + wr (clamped to [0, N])
     float scale_log2; // scale * log2(e)
     unsigned long long wait_budget_ns;
-    unsigned int *status;  // [code, role, iteration, block]
+    unsigned int *status;  // [code, role, unit, block]
 };
 
 template <int D>
 struct SmemLayout {
-    // K/V ring depth. d = 64 takes 4 stages: it pipelines deeper and keeps the
-    // footprint above half of the SM's shared memory, so that one CTA (which
-    // holds all 512 TMEM columns) runs per SM.
+    // K/V ring depth. The footprint stays above half of the SM's shared
+    // memory, so one CTA (holding all 512 TMEM columns) runs per SM.
     static constexpr int kStages = D == 64 ? 4 : 2;
     static constexpr int kTileBytes = kBM * D * 2;
     static constexpr int kQ = 0;
-    static constexpr int kK = kQ + kTileBytes;
+    static constexpr int kK = kQ + kQTiles * kTileBytes;
     static constexpr int kV = kK + kStages * kTileBytes;
-    static constexpr int kP = kV + kStages * kTileBytes;
-    static constexpr int kBar = kP + kBM * kBN * 2;
-    static constexpr int kNumBars = 24;
+    static constexpr int kBar = kV + kStages * kTileBytes;
+    static constexpr int kNumBars = 32;
     static constexpr int kMisc = kBar + kNumBars * 8;
     static constexpr int kBytes = kMisc + 16;
     static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 B
+    static constexpr uint32_t kTmemO = 256;       // O_t at kTmemO + t * D
 };
 
-// Barrier slots (kMaxStages per ring).
 constexpr int kMaxStages = 4;
 enum : int {
-    kBarQFull = 0,
-    kBarKFull = 1,                             // + stage
-    kBarVFull = kBarKFull + kMaxStages,        // + stage
-    kBarKVEmpty = kBarVFull + kMaxStages,      // + stage
-    kBarSFull = kBarKVEmpty + kMaxStages,      // + S buffer
-    kBarSEmpty = kBarSFull + 2,                // + S buffer
-    kBarPFull = kBarSEmpty + 2,
-    kBarODone = kBarPFull + 1,
-    kBarDrain = kBarODone + 1,
+    kBarQFull = 0,                          // + t
+    kBarQEmpty = kBarQFull + kQTiles,       // + t
+    kBarKFull = kBarQEmpty + kQTiles,       // + stage
+    kBarVFull = kBarKFull + kMaxStages,     // + stage
+    kBarKVEmpty = kBarVFull + kMaxStages,   // + stage
+    kBarSFull = kBarKVEmpty + kMaxStages,   // + t
+    kBarPFull = kBarSFull + kQTiles,        // + t
+    kBarODone = kBarPFull + kQTiles,        // + t
+    kBarOFree = kBarODone + kQTiles,        // + t
+    kBarDrain = kBarOFree + kQTiles,
     kNumBarsUsed = kBarDrain + 1,
 };
 
+// A work unit: rows [r0, r0 + 256) of head bh; Q tile t covers rows
+// [r0 + 128 t, r0 + 128 t + 128) and needs K/V tiles [a[t], b[t]] (empty when a > b).
+struct Unit {
+    int bh, r0;
+    int a[kQTiles], b[kQTiles];
+};
+
+__device__ __forceinline__ Unit decode_unit(int u, const FwdParams &p) {
+    Unit U;
+    U.bh = u / p.n_qb;
+    int qb = u % p.n_qb;
+    if (p.heavy_first) qb = p.n_qb - 1 - qb;
+    U.r0 = qb * kUnitRows;
+#pragma unroll
+    for (int t = 0; t < kQTiles; ++t) {
+        const int rt0 = U.r0 + t * kBM;
+        if (rt0 >= p.N) {
+            U.a[t] = 1;
+            U.b[t] = 0;
+        } else {
+            const int rl = min(rt0 + kBM, p.N) - 1;
+            U.a[t] = max(0, rt0 - p.wl) / kBN;
+            U.b[t] = min(p.N - 1, rl + p.wr) / kBN;
+        }
+    }
+    return U;
+}
+
 __device__ __forceinline__ void record_timeout(const FwdParams &p, volatile int *abort_flag,
-                                               int role, int iteration) {
+                                               int role, int unit) {
     *abort_flag = 1;
     if (atomicCAS(p.status, 0u, kStatusTimeout) == 0u) {
         p.status[1] = static_cast<unsigned>(role);
-        p.status[2] = static_cast<unsigned>(iteration);
+        p.status[2] = static_cast<unsigned>(unit);
         p.status[3] = blockIdx.x;
         __threadfence();
     }
@@ -122,7 +175,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sQ = sbase + L::kQ;
     const uint32_t sK = sbase + L::kK;
     const uint32_t sV = sbase + L::kV;
-    const uint32_t sP = sbase + L::kP;
     const uint32_t bar0 = sbase + L::kBar;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
@@ -132,39 +184,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const uint64_t budget = p.wait_budget_ns;
 
-    // ---- work unit: (b*H + h, Q tile), heads outermost so that the CTAs running
-    // at the same time share K/V in L2.
-    const int bh = static_cast<int>(blockIdx.x) / p.num_q_tiles;
-    int qt = static_cast<int>(blockIdx.x) % p.num_q_tiles;
-    if (p.heavy_first) qt = p.num_q_tiles - 1 - qt;
-    const int r0 = qt * kBM;
-    const int r_last = min(r0 + kBM, p.N) - 1;
-    // Visible key range of a row i: [max(0, i - wl), min(N - 1, i + wr)].
-    const int lo_first = max(0, r0 - p.wl);
-    const int hi_first = min(p.N - 1, r0 + p.wr);
-    const int lo_last = max(0, r_last - p.wl);
-    const int hi_last = min(p.N - 1, r_last + p.wr);
-    const int j_lo = lo_first / kBN;  // K/V tiles that hold any visible key
-    const int n_kv = hi_last / kBN - j_lo + 1;
-
     // ---- setup
     if (warp == 0) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
-    if (threadIdx.x == 128) {
-        mbar_init(bar(kBarQFull), 1);
+    if (threadIdx.x == kTmaWarp * 32) {
+        for (int t = 0; t < kQTiles; ++t) {
+            mbar_init(bar(kBarQFull + t), 1);
+            mbar_init(bar(kBarQEmpty + t), 1);
+            mbar_init(bar(kBarSFull + t), 1);
+            mbar_init(bar(kBarPFull + t), 128);
+            mbar_init(bar(kBarODone + t), 1);
+            mbar_init(bar(kBarOFree + t), 128);
+        }
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(kBarKFull + s), 1);
             mbar_init(bar(kBarVFull + s), 1);
             mbar_init(bar(kBarKVEmpty + s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(kBarSFull + b), 1);
-            mbar_init(bar(kBarSEmpty + b), 128);
-        }
-        mbar_init(bar(kBarPFull), 128);
-        mbar_init(bar(kBarODone), 1);
         mbar_init(bar(kBarDrain), 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -177,198 +215,255 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 4) {
+    // Each role's code sits inside the branch of its setmaxnreg, so the
+    // compiler allocates it under that register limit.
+    if (warp >= 8) {
+      setmaxnreg_dec<kRegsControl>();
+      if (warp == kTmaWarp) {
         // ================================================================ TMA producer
         if (lane == 0) {
-            int issued[kStages];
-            for (int s = 0; s < kStages; ++s) issued[s] = 0;
-            mbar_arrive_expect_tx(bar(kBarQFull), L::kTileBytes);
-            for (int g = 0; g < kRegions; ++g)
-                tma_load_3d(sQ + g * kRegionBytes, &tmQ, bar(kBarQFull), 64 * g, r0, bh);
-            for (int it = 0; it < n_kv; ++it) {
-                const int st = it % kStages;
-                const uint32_t ph = (it / kStages) & 1;
-                if (!mbar_wait_bounded(bar(kBarKVEmpty + st), ph ^ 1, abort_flag, budget)) {
-                    record_timeout(p, abort_flag, kRoleTma, it);
-                    break;
+            int kv_iter = 0, unit_iter = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++unit_iter) {
+                const Unit U = decode_unit(u, p);
+                for (int t = 0; t < kQTiles && ok; ++t) {
+                    ok = mbar_wait_bounded(bar(kBarQEmpty + t), (unit_iter & 1) ^ 1, abort_flag, budget);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar(kBarQFull + t), L::kTileBytes);
+                    for (int g = 0; g < kRegions; ++g)
+                        tma_load_3d(sQ + t * L::kTileBytes + g * kRegionBytes, &tmQ,
+                                    bar(kBarQFull + t), 64 * g, U.r0 + t * kBM, U.bh);
                 }
-                const int kv0 = (j_lo + it) * kBN;
-                const uint32_t kdst = sK + st * L::kTileBytes;
-                const uint32_t vdst = sV + st * L::kTileBytes;
-                mbar_arrive_expect_tx(bar(kBarKFull + st), L::kTileBytes);
-                for (int g = 0; g < kRegions; ++g)
-                    tma_load_3d(kdst + g * kRegionBytes, &tmK, bar(kBarKFull + st), 64 * g, kv0, bh);
-                mbar_arrive_expect_tx(bar(kBarVFull + st), L::kTileBytes);
-                for (int g = 0; g < kRegions; ++g)
-                    tma_load_3d(vdst + g * kRegionBytes, &tmV, bar(kBarVFull + st), 64 * g, kv0, bh);
-                issued[st] = it / kStages + 1;
+                const int j1 = U.a[1] <= U.b[1] ? U.b[1] : U.b[0];
+                for (int j = U.a[0]; ok && j <= j1; ++j, ++kv_iter) {
+                    const int st = kv_iter % kStages;
+                    const uint32_t ph = (kv_iter / kStages) & 1;
+                    ok = mbar_wait_bounded(bar(kBarKVEmpty + st), ph ^ 1, abort_flag, budget);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar(kBarKFull + st), L::kTileBytes);
+                    for (int g = 0; g < kRegions; ++g)
+                        tma_load_3d(sK + st * L::kTileBytes + g * kRegionBytes, &tmK,
+                                    bar(kBarKFull + st), 64 * g, j * kBN, U.bh);
+                    mbar_arrive_expect_tx(bar(kBarVFull + st), L::kTileBytes);
+                    for (int g = 0; g < kRegions; ++g)
+                        tma_load_3d(sV + st * L::kTileBytes + g * kRegionBytes, &tmV,
+                                    bar(kBarVFull + st), 64 * g, j * kBN, U.bh);
+                }
+                if (!ok) record_timeout(p, abort_flag, kRoleTma, u);
             }
             // Drain: no copy may still be landing in shared memory when the CTA exits.
-            mbar_wait_bounded(bar(kBarQFull), 0, nullptr, budget);
+            if (unit_iter > 0)
+                for (int t = 0; t < kQTiles; ++t)
+                    mbar_wait_bounded(bar(kBarQFull + t), (unit_iter - 1) & 1, nullptr, budget);
             for (int s = 0; s < kStages; ++s) {
-                if (issued[s] > 0) {
-                    const uint32_t ph = (issued[s] - 1) & 1;
+                if (kv_iter > s) {
+                    const int last = kv_iter - 1 - ((kv_iter - 1 - s) % kStages);
+                    const uint32_t ph = (last / kStages) & 1;
                     mbar_wait_bounded(bar(kBarKFull + s), ph, nullptr, budget);
                     mbar_wait_bounded(bar(kBarVFull + s), ph, nullptr, budget);
                 }
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == kMmaWarp) {
         // ================================================================ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_f16(BF16, kBM, kBN, false);
             constexpr uint32_t idesc_o = idesc_f16(BF16, kBM, D, true);
-            bool ok = mbar_wait_bounded(bar(kBarQFull), 0, abort_flag, budget);
-            int it = 0;
-            for (; ok && it <= n_kv; ++it) {
-                if (it < n_kv) {
-                    const int st = it % kStages;
-                    const uint32_t ph = (it / kStages) & 1;
-                    const int sb = it & 1;
-                    ok = mbar_wait_bounded(bar(kBarKFull + st), ph, abort_flag, budget) &&
-                         mbar_wait_bounded(bar(kBarSEmpty + sb), ((it >> 1) & 1) ^ 1, abort_flag,
-                                           budget);
-                    if (!ok) break;
-                    tc_fence_after();
+            int kv_iter = 0, unit_iter = 0;
+            int pv_count[kQTiles] = {0, 0};   // O_t += P_t V issued so far
+            int epi_count[kQTiles] = {0, 0};  // units in which Q tile t had an epilogue
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++unit_iter) {
+                const Unit U = decode_unit(u, p);
+                for (int t = 0; t < kQTiles && ok; ++t)
+                    ok = mbar_wait_bounded(bar(kBarQFull + t), unit_iter & 1, abort_flag, budget);
+                const int j1 = U.a[1] <= U.b[1] ? U.b[1] : U.b[0];
+                for (int j = U.a[0]; ok && j <= j1; ++j, ++kv_iter) {
+                    const int st = kv_iter % kStages;
+                    const uint32_t ph = (kv_iter / kStages) & 1;
+                    ok = mbar_wait_bounded(bar(kBarKFull + st), ph, abort_flag, budget);
                     const uint32_t kbase = sK + st * L::kTileBytes;
-#pragma unroll
-                    for (int k = 0; k < D / 16; ++k) {
-                        const uint32_t off = (k >> 2) * kRegionBytes + (k & 3) * 32;
-                        umma_f16_ss(tmem + sb * kBN, sw128_desc(sQ + off, 16, 1024),
-                                    sw128_desc(kbase + off, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
+                    for (int t = 0; t < kQTiles && ok; ++t) {
+                        if (j < U.a[t] || j > U.b[t]) continue;
+                        // S_t / P_t columns are free once the previous O_t += P_t V completed.
+                        if (pv_count[t] > 0)
+                            ok = mbar_wait_bounded(bar(kBarODone + t), (pv_count[t] - 1) & 1,
+                                                   abort_flag, budget);
+                        if (!ok) break;
+                        tc_fence_after();
+                        // K-step k reads 16 columns: 32 bytes into 64-column region k / 4.
+                        const uint64_t dq = sw128_desc(sQ + t * L::kTileBytes, 16, 1024);
+                        const uint64_t dk = sw128_desc(kbase, 16, 1024);
+#pragma unroll 1
+                        for (int k = 0; k < D / 16; ++k) {
+                            const uint32_t off = ((k >> 2) * kRegionBytes + (k & 3) * 32) >> 4;
+                            umma_f16_ss(tmem + t * kBN, dq + off, dk + off, idesc_s,
+                                        k > 0 ? 1u : 0u);
+                        }
+                        umma_commit(bar(kBarSFull + t));
                     }
-                    umma_commit(bar(kBarSFull + sb));
-                }
-                if (it > 0) {
-                    const int pj = it - 1;
-                    const int pst = pj % kStages;
-                    const uint32_t pph = (pj / kStages) & 1;
-                    ok = mbar_wait_bounded(bar(kBarVFull + pst), pph, abort_flag, budget) &&
-                         mbar_wait_bounded(bar(kBarPFull), pj & 1, abort_flag, budget);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t vbase = sV + pst * L::kTileBytes;
-#pragma unroll
-                    for (int k = 0; k < kBN / 16; ++k) {
-                        const uint32_t aoff = (k >> 2) * kRegionBytes + (k & 3) * 32;
-                        const uint32_t boff = k * 16 * 128;
-                        umma_f16_ss(tmem + kTmemO, sw128_desc(sP + aoff, 16, 1024),
-                                    sw128_desc(vbase + boff, kRegionBytes, 1024), idesc_o,
-                                    (pj > 0 || k > 0) ? 1u : 0u);
+                    if (ok && j == j1)
+                        for (int t = 0; t < kQTiles; ++t) umma_commit(bar(kBarQEmpty + t));
+                    if (ok) ok = mbar_wait_bounded(bar(kBarVFull + st), ph, abort_flag, budget);
+                    const uint32_t vbase = sV + st * L::kTileBytes;
+                    for (int t = 0; t < kQTiles && ok; ++t) {
+                        if (j < U.a[t] || j > U.b[t]) continue;
+                        ok = mbar_wait_bounded(bar(kBarPFull + t), pv_count[t] & 1, abort_flag, budget);
+                        // The first O_t += P_t V of a unit overwrites O_t: the previous
+                        // unit's epilogue of tile t must have read it.
+                        if (ok && j == U.a[t])
+                            ok = mbar_wait_bounded(bar(kBarOFree + t), (epi_count[t] & 1) ^ 1,
+                                                   abort_flag, budget);
+                        if (!ok) break;
+                        tc_fence_after();
+                        // K-step k reads keys 16k..16k+15: 16 rows of 128 B of V.
+                        const uint64_t dv = sw128_desc(vbase, kRegionBytes, 1024);
+#pragma unroll 1
+                        for (int k = 0; k < kBN / 16; ++k)
+                            umma_f16_ts(tmem + L::kTmemO + t * D, tmem + t * kBN + k * 8,
+                                        dv + ((k * 16 * 128) >> 4), idesc_o,
+                                        (j > U.a[t] || k > 0) ? 1u : 0u);
+                        umma_commit(bar(kBarODone + t));
+                        ++pv_count[t];
                     }
-                    umma_commit(bar(kBarODone));
-                    umma_commit(bar(kBarKVEmpty + pst));
+                    if (ok) umma_commit(bar(kBarKVEmpty + st));
                 }
+                for (int t = 0; t < kQTiles; ++t)
+                    if (U.a[t] <= U.b[t]) ++epi_count[t];
+                if (!ok) record_timeout(p, abort_flag, kRoleMma, u);
             }
-            if (!ok) record_timeout(p, abort_flag, kRoleMma, it);
             // Drain: every MMA this thread issued has completed before TMEM is freed.
             umma_commit(bar(kBarDrain));
             mbar_wait_bounded(bar(kBarDrain), 0, nullptr, budget);
         }
+      }
     } else {
-        // ================================================================ softmax warps
-        const int row = threadIdx.x;  // TMEM lane and row of the Q tile
-        const int i = r0 + row;       // query index
-        const int lo_i = max(0, i - p.wl);
-        const int hi_i = min(p.N - 1, i + p.wr);
-        const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+      setmaxnreg_inc<kRegsSoftmax>();
+      {
+        // ================================================================ softmax warpgroups
+        const int t = warp >> 2;                 // Q tile of this warpgroup
+        const int row = threadIdx.x & 127;       // TMEM lane and row of the Q tile
+        const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const uint32_t tS = tl + t * kBN;
+        const uint32_t tO = tl + L::kTmemO + t * D;
         const float sl2 = p.scale_log2;
-        float m = -INFINITY;  // running max of the logits, scaled to log2 units
-        float l = 0.f;        // running sum of 2^(logit - m)
+        int s_count = 0;  // S_t tiles consumed so far (= O_t += P_t V issued)
         bool ok = true;
-        int it = 0;
-        for (; it < n_kv; ++it) {
-            const int sb = it & 1;
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait_bounded(bar(kBarSFull + sb), (it >> 1) & 1, abort_flag, budget));
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t sr[4][32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(tl + sb * kBN + c * 32, sr[c]);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
-            tc_fence_before();
-            mbar_arrive(bar(kBarSEmpty + sb));  // the S buffer may be overwritten now
-
-            float x[kBN];
-#pragma unroll
-            for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(sr[c >> 5][c & 31]);
-            const int kv0 = (j_lo + it) * kBN;
-            const bool full = kv0 >= lo_last && kv0 + kBN - 1 <= hi_first;
-            if (!full) {
-#pragma unroll
-                for (int c = 0; c < kBN; ++c) {
-                    const int key = kv0 + c;
-                    if (key < lo_i || key > hi_i) x[c] = -INFINITY;
-                }
-            }
-            float mx = x[0];
-#pragma unroll
-            for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, x[c]);
-            const float m_new = fmaxf(m, mx * sl2);
-            const float m_use = m_new == -INFINITY ? 0.f : m_new;
-            const float corr = ex2_approx(m - m_use);
-            float sum = 0.f;
-#pragma unroll
-            for (int c = 0; c < kBN; ++c) {
-                x[c] = ex2_approx(fmaf(x[c], sl2, -m_use));
-                sum += x[c];
-            }
-            l = l * corr + sum;
-            m = m_new;
-
-            if (it > 0) {
-                // P_{j-1} V_{j-1} must be done: it reads the P buffer and writes O.
-                ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarODone), (it - 1) & 1,
+        for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+            const Unit U = decode_unit(u, p);
+            if (U.a[t] > U.b[t]) continue;
+            const int rt0 = U.r0 + t * kBM;
+            const int rl = min(rt0 + kBM, p.N) - 1;
+            const int i = rt0 + row;  // query index
+            const int lo_i = max(0, i - p.wl);
+            const int hi_i = min(p.N - 1, i + p.wr);
+            const int lo_last = max(0, rl - p.wl);
+            const int hi_first = min(p.N - 1, rt0 + p.wr);
+            float m = -INFINITY;  // reference max of the row, in log2 units of the scaled logits
+            float l = 0.f;        // running sum of 2^(logit - m)
+            for (int j = U.a[t]; j <= U.b[t]; ++j, ++s_count) {
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarSFull + t), s_count & 1,
                                                                abort_flag, budget));
                 if (!ok) break;
                 tc_fence_after();
-            }
-            // P row -> shared memory, K-major with the 128-byte swizzle.
-            uint8_t *prow = smem + L::kP + row * 128;
+                uint32_t sr[4][32];
 #pragma unroll
-            for (int g = 0; g < kBN / 64; ++g) {
+                for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const int b = g * 64 + c * 8;
-                    uint4 v;
-                    v.x = pack2<BF16>(x[b + 0], x[b + 1]);
-                    v.y = pack2<BF16>(x[b + 2], x[b + 3]);
-                    v.z = pack2<BF16>(x[b + 4], x[b + 5]);
-                    v.w = pack2<BF16>(x[b + 6], x[b + 7]);
-                    *reinterpret_cast<uint4 *>(prow + g * kRegionBytes + ((c ^ (row & 7)) << 4)) = v;
+                for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
+                float x[kBN];
+#pragma unroll
+                for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(sr[c >> 5][c & 31]);
+                const int kv0 = j * kBN;
+                if (!(kv0 >= lo_last && kv0 + kBN - 1 <= hi_first)) {
+#pragma unroll
+                    for (int c = 0; c < kBN; ++c) {
+                        const int key = kv0 + c;
+                        if (key < lo_i || key > hi_i) x[c] = -INFINITY;
+                    }
                 }
-            }
-            if (it > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
+                // Row max: four independent chains of 3-input max.
+                float ma = fmaxf(x[0], x[1]), mb = fmaxf(x[2], x[3]);
+                float mc = fmaxf(x[4], x[5]), md = fmaxf(x[6], x[7]);
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(tl + kTmemO + c * 32, o);
-                    tmem_ld_wait(o);
+                for (int c = 8; c < kBN; c += 8) {
+                    ma = max3f(ma, x[c + 0], x[c + 1]);
+                    mb = max3f(mb, x[c + 2], x[c + 3]);
+                    mc = max3f(mc, x[c + 4], x[c + 5]);
+                    md = max3f(md, x[c + 6], x[c + 7]);
+                }
+                const float m_tile = fmaxf(fmaxf(ma, mb), fmaxf(mc, md)) * sl2;
+                // Lazy rescale: move the reference max only when this block's max
+                // exceeds it by more than the threshold.
+                const float m_old = m;
+                if (m_tile > m + kRescaleThreshold) m = m_tile;
+                const float corr = m != m_old ? ex2_approx(m_old - m) : 1.f;
+                const float nm = m == -INFINITY ? 0.f : -m;
+                float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f, s4 = 0.f, s5 = 0.f, s6 = 0.f, s7 = 0.f;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
-                    tmem_st32(tl + kTmemO + c * 32, o);
+                for (int c = 0; c < kBN; c += 8) {
+#pragma unroll
+                    for (int e = 0; e < 8; e += 2) {
+                        ffma2(x[c + e], x[c + e + 1], sl2, sl2, nm, nm);
+                        x[c + e] = ex2_approx(x[c + e]);
+                        x[c + e + 1] = ex2_approx(x[c + e + 1]);
+                    }
+                    fadd2(s0, s1, x[c + 0], x[c + 1]);
+                    fadd2(s2, s3, x[c + 2], x[c + 3]);
+                    fadd2(s4, s5, x[c + 4], x[c + 5]);
+                    fadd2(s6, s7, x[c + 6], x[c + 7]);
+                }
+                l = l * corr + (((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7)));
+                // O_t holds the sum up to block j-1 (complete: S_t(j) was issued after it).
+                if (j > U.a[t] && __any_sync(0xffffffffu, corr != 1.f)) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + c * 32, o);
+                        tmem_ld_wait(o);
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            float a0 = __uint_as_float(o[e]), a1 = __uint_as_float(o[e + 1]);
+                            fmul2(a0, a1, corr, corr);
+                            o[e] = __float_as_uint(a0);
+                            o[e + 1] = __float_as_uint(a1);
+                        }
+                        tmem_st32(tO + c * 32, o);
+                    }
+                }
+                // P_t(j) as packed 16-bit pairs over the first 64 columns of S_t.
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        pk[e] = pack2<BF16>(x[64 * h + 2 * e], x[64 * h + 2 * e + 1]);
+                    tmem_st32(tS + 32 * h, pk);
                 }
                 tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(bar(kBarPFull + t));
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(bar(kBarPFull));
-        }
-        if (ok)
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarODone), (n_kv - 1) & 1,
+            if (!ok) {
+                if (lane == 0) record_timeout(p, abort_flag, kRoleSoftmax, u);
+                break;
+            }
+            // ---- epilogue: O = O_t / l, LSE = ln 2 * (m + log2 l)
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarODone + t), (s_count - 1) & 1,
                                                            abort_flag, budget));
-        if (ok) {
+            if (!ok) {
+                if (lane == 0) record_timeout(p, abort_flag, kRoleSoftmax, u);
+                break;
+            }
             tc_fence_after();
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
             const bool store = i < p.N;
             uint8_t *orow = reinterpret_cast<uint8_t *>(p.O) +
-                            (static_cast<size_t>(bh) * p.N + (store ? i : 0)) * (D * 2);
+                            (static_cast<size_t>(U.bh) * p.N + (store ? i : 0)) * (D * 2);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
-                tmem_ld32(tl + kTmemO + c * 32, o);
+                tmem_ld32(tO + c * 32, o);
                 tmem_ld_wait(o);
                 uint32_t pk[16];
 #pragma unroll
@@ -383,11 +478,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (store)
-                p.LSE[static_cast<size_t>(bh) * p.N + i] =
+                p.LSE[static_cast<size_t>(U.bh) * p.N + i] =
                     l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
-        } else if (lane == 0) {
-            record_timeout(p, abort_flag, kRoleSoftmax, it);
+            tc_fence_before();
+            mbar_arrive(bar(kBarOFree + t));
         }
+      }
     }
 
     // ---- teardown

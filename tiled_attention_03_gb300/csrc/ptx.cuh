@@ -124,6 +124,18 @@ __device__ __forceinline__ void umma_f16_ss(uint32_t d_tmem, uint64_t a_desc, ui
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] x B[smem desc]^T, kind::f16. A is M x 16 in tensor
+// memory: row i in lane i, two 16-bit elements per 32-bit column.
+__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 async op issued so far by this thread completes.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile(
@@ -205,11 +217,59 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, int M, int N, bool b
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// ---------------------------------------------------------------- registers
+// Warpgroup-wide change of the per-thread register allocation.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------- math
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Three-input maximum (sm_100+).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Packed two-lane fp32 arithmetic (sm_100+): one instruction for two values.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+// (a0, a1) <- (a0 * b0 + c0, a1 * b1 + c1), round to nearest.
+__device__ __forceinline__ void ffma2(float &a0, float &a1, float b0, float b1, float c0, float c1) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(d)
+        : "l"(f2_pack(a0, a1)), "l"(f2_pack(b0, b1)), "l"(f2_pack(c0, c1)));
+    f2_unpack(d, a0, a1);
+}
+// (a0, a1) <- (a0 + b0, a1 + b1)
+__device__ __forceinline__ void fadd2(float &a0, float &a1, float b0, float b1) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_pack(a0, a1)), "l"(f2_pack(b0, b1)));
+    f2_unpack(d, a0, a1);
+}
+// (a0, a1) <- (a0 * b0, a1 * b1)
+__device__ __forceinline__ void fmul2(float &a0, float &a1, float b0, float b1) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_pack(a0, a1)), "l"(f2_pack(b0, b1)));
+    f2_unpack(d, a0, a1);
 }
 
 // Two floats -> one 32-bit word holding two 16-bit values, `lo` in the low half.
