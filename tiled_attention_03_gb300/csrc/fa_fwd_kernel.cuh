@@ -64,8 +64,8 @@ constexpr int kMmaWarp = 9;
 // Per-thread registers after setmaxnreg. Their sum over the CTA must not exceed
 // what the launch allocated (threads x registers of the compiled kernel); the
 // host checks this before the first launch.
-constexpr int kRegsSoftmax = 224;
-constexpr int kRegsControl = 56;
+constexpr int kRegsSoftmax = 208;
+constexpr int kRegsControl = 88;
 constexpr int kRegsNeeded = 2 * 128 * kRegsSoftmax + 128 * kRegsControl;
 constexpr int kRegionBytes = 128 * 128;  // 128 rows x 128 B: one 64-column swizzle region
 constexpr uint32_t kTmemCols = 512;
@@ -264,78 +264,95 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else if (warp == kMmaWarp) {
+      } else if (warp == kMmaWarp) {
         // ================================================================ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_f16(BF16, kBM, kBN, false);
-            constexpr uint32_t idesc_o = idesc_f16(BF16, kBM, D, true);
-            int kv_iter = 0, unit_iter = 0;
-            int pv_count[kQTiles] = {0, 0};   // O_t += P_t V issued so far
-            int epi_count[kQTiles] = {0, 0};  // units in which Q tile t had an epilogue
-            bool ok = true;
-            for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++unit_iter) {
-                const Unit U = decode_unit(u, p);
-                for (int t = 0; t < kQTiles && ok; ++t)
-                    ok = mbar_wait_bounded(bar(kBarQFull + t), unit_iter & 1, abort_flag, budget);
-                const int j1 = U.a[1] <= U.b[1] ? U.b[1] : U.b[0];
-                for (int j = U.a[0]; ok && j <= j1; ++j, ++kv_iter) {
-                    const int st = kv_iter % kStages;
-                    const uint32_t ph = (kv_iter / kStages) & 1;
-                    ok = mbar_wait_bounded(bar(kBarKFull + st), ph, abort_flag, budget);
-                    const uint32_t kbase = sK + st * L::kTileBytes;
-                    for (int t = 0; t < kQTiles && ok; ++t) {
-                        if (j < U.a[t] || j > U.b[t]) continue;
-                        // S_t / P_t columns are free once the previous O_t += P_t V completed.
-                        if (pv_count[t] > 0)
-                            ok = mbar_wait_bounded(bar(kBarODone + t), (pv_count[t] - 1) & 1,
-                                                   abort_flag, budget);
-                        if (!ok) break;
-                        tc_fence_after();
+        // The whole warp walks the schedule (uniform control flow); one elected
+        // lane issues each group of tcgen05 instructions. A group of K-steps is
+        // fully unrolled with compile-time descriptor offsets: the tensor core
+        // accepts only about one MMA ahead, so any instruction latency between
+        // two issues becomes idle tensor-core time.
+        constexpr uint32_t idesc_s = idesc_f16(BF16, kBM, kBN, false);
+        constexpr uint32_t idesc_o = idesc_f16(BF16, kBM, D, true);
+        auto wait = [&](int b, uint32_t parity) {
+            return __all_sync(0xffffffffu, mbar_wait_bounded(bar(b), parity, abort_flag, budget));
+        };
+        int kv_iter = 0, unit_iter = 0;
+        int pv_count[kQTiles] = {0, 0};   // O_t += P_t V issued so far
+        int epi_count[kQTiles] = {0, 0};  // units in which Q tile t had an epilogue
+        bool ok = true;
+        for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++unit_iter) {
+            const Unit U = decode_unit(u, p);
+            for (int t = 0; t < kQTiles && ok; ++t) ok = wait(kBarQFull + t, unit_iter & 1);
+            const int j1 = U.a[1] <= U.b[1] ? U.b[1] : U.b[0];
+            for (int j = U.a[0]; ok && j <= j1; ++j, ++kv_iter) {
+                const int st = kv_iter % kStages;
+                const uint32_t ph = (kv_iter / kStages) & 1;
+                ok = wait(kBarKFull + st, ph);
+                const uint64_t dk = sw128_desc(sK + st * L::kTileBytes, 16, 1024);
+#pragma unroll
+                for (int t = 0; t < kQTiles; ++t) {
+                    if (!ok || j < U.a[t] || j > U.b[t]) continue;
+                    // S_t / P_t columns are free once the previous O_t += P_t V completed.
+                    if (pv_count[t] > 0) ok = wait(kBarODone + t, (pv_count[t] - 1) & 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t dq = sw128_desc(sQ + t * L::kTileBytes, 16, 1024);
+                    if (elect_one()) {
                         // K-step k reads 16 columns: 32 bytes into 64-column region k / 4.
-                        const uint64_t dq = sw128_desc(sQ + t * L::kTileBytes, 16, 1024);
-                        const uint64_t dk = sw128_desc(kbase, 16, 1024);
-#pragma unroll 1
+#pragma unroll
                         for (int k = 0; k < D / 16; ++k) {
-                            const uint32_t off = ((k >> 2) * kRegionBytes + (k & 3) * 32) >> 4;
-                            umma_f16_ss(tmem + t * kBN, dq + off, dk + off, idesc_s,
-                                        k > 0 ? 1u : 0u);
+                            constexpr uint32_t kRegion16 = kRegionBytes >> 4;
+                            const uint32_t off = (k >> 2) * kRegion16 + (k & 3) * 2;
+                            umma_f16_ss(tmem + t * kBN, dq + off, dk + off, idesc_s, k > 0 ? 1u : 0u);
                         }
                         umma_commit(bar(kBarSFull + t));
                     }
-                    if (ok && j == j1)
-                        for (int t = 0; t < kQTiles; ++t) umma_commit(bar(kBarQEmpty + t));
-                    if (ok) ok = mbar_wait_bounded(bar(kBarVFull + st), ph, abort_flag, budget);
-                    const uint32_t vbase = sV + st * L::kTileBytes;
-                    for (int t = 0; t < kQTiles && ok; ++t) {
-                        if (j < U.a[t] || j > U.b[t]) continue;
-                        ok = mbar_wait_bounded(bar(kBarPFull + t), pv_count[t] & 1, abort_flag, budget);
-                        // The first O_t += P_t V of a unit overwrites O_t: the previous
-                        // unit's epilogue of tile t must have read it.
-                        if (ok && j == U.a[t])
-                            ok = mbar_wait_bounded(bar(kBarOFree + t), (epi_count[t] & 1) ^ 1,
-                                                   abort_flag, budget);
-                        if (!ok) break;
-                        tc_fence_after();
+                    __syncwarp();
+                }
+                if (ok && j == j1) {
+                    // Both Q buffers are free once the unit's last S MMAs complete.
+                    if (elect_one())
+                        for (int q = 0; q < kQTiles; ++q) umma_commit(bar(kBarQEmpty + q));
+                    __syncwarp();
+                }
+                if (ok) ok = wait(kBarVFull + st, ph);
+                const uint64_t dv = sw128_desc(sV + st * L::kTileBytes, kRegionBytes, 1024);
+#pragma unroll
+                for (int t = 0; t < kQTiles; ++t) {
+                    if (!ok || j < U.a[t] || j > U.b[t]) continue;
+                    ok = wait(kBarPFull + t, pv_count[t] & 1);
+                    // The first O_t += P_t V of a unit overwrites O_t: the previous
+                    // unit's epilogue of tile t must have read it.
+                    if (ok && j == U.a[t]) ok = wait(kBarOFree + t, (epi_count[t] & 1) ^ 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t acc0 = j > U.a[t] ? 1u : 0u;
+                    if (elect_one()) {
                         // K-step k reads keys 16k..16k+15: 16 rows of 128 B of V.
-                        const uint64_t dv = sw128_desc(vbase, kRegionBytes, 1024);
-#pragma unroll 1
+#pragma unroll
                         for (int k = 0; k < kBN / 16; ++k)
                             umma_f16_ts(tmem + L::kTmemO + t * D, tmem + t * kBN + k * 8,
-                                        dv + ((k * 16 * 128) >> 4), idesc_o,
-                                        (j > U.a[t] || k > 0) ? 1u : 0u);
+                                        dv + k * ((16 * 128) >> 4), idesc_o, k > 0 ? 1u : acc0);
                         umma_commit(bar(kBarODone + t));
-                        ++pv_count[t];
                     }
-                    if (ok) umma_commit(bar(kBarKVEmpty + st));
+                    __syncwarp();
+                    ++pv_count[t];
                 }
-                for (int t = 0; t < kQTiles; ++t)
-                    if (U.a[t] <= U.b[t]) ++epi_count[t];
-                if (!ok) record_timeout(p, abort_flag, kRoleMma, u);
+                if (ok) {
+                    // K_j and V_j are free once every MMA issued so far completes.
+                    if (elect_one()) umma_commit(bar(kBarKVEmpty + st));
+                    __syncwarp();
+                }
             }
-            // Drain: every MMA this thread issued has completed before TMEM is freed.
-            umma_commit(bar(kBarDrain));
-            mbar_wait_bounded(bar(kBarDrain), 0, nullptr, budget);
+            for (int t = 0; t < kQTiles; ++t)
+                if (U.a[t] <= U.b[t]) ++epi_count[t];
+            if (!ok && lane == 0) record_timeout(p, abort_flag, kRoleMma, u);
         }
+        // Drain: every MMA this warp issued has completed before TMEM is freed.
+        if (elect_one()) umma_commit(bar(kBarDrain));
+        __syncwarp();
+        if (lane == 0) mbar_wait_bounded(bar(kBarDrain), 0, nullptr, budget);
+        __syncwarp();
       }
     } else {
       setmaxnreg_inc<kRegsSoftmax>();
