@@ -32,10 +32,11 @@
 // 256 + t d (fp32). After the softmax of S_t(j) the probabilities P_t(j) are
 // written as packed 16-bit pairs over the first 64 columns of S_t, and
 // O_t += P_t(j) V_j reads them from tensor memory (A operand in TMEM).
-// Issue order per K/V tile j:  S_0(j) S_1(j) | O_0 += P_0 V_j | O_1 += P_1 V_j,
-// with S_t(j+1) issued only once O_t += P_t(j) V_j has completed (it overwrites
-// the columns that MMA reads). The softmax of tile 0 runs while the tensor core
-// computes S_1(j) and the softmax of tile 1 while it computes O_0 += P_0 V_j.
+// Issue order, iteration j:  S_0(j) | O_1 += P_1(j-1) V_{j-1} | S_1(j) | O_0 += P_0(j) V_j.
+// Each softmax overlaps two MMA groups of the other tile. S_t(j+1) follows
+// O_t += P_t(j) V_j directly: tcgen05.mma operations of one thread execute in
+// issue order, so the P read of the earlier MMA precedes the S write of the
+// later one.
 //
 // The output accumulator is rescaled lazily: the reference max of a row only
 // moves when a block's max exceeds it by more than 2^8 (in log2 units), so
@@ -70,6 +71,16 @@ constexpr int kRegsNeeded = 2 * 128 * kRegsSoftmax + 128 * kRegsControl;
 constexpr int kRegionBytes = 128 * 128;  // 128 rows x 128 B: one 64-column swizzle region
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: probabilities stay <= 2^8
+// Of every 32 probabilities, how many use the FMA-pipe exp2 (the rest use MUFU),
+// and how many keys the softmax packs per TMEM store of P.
+#ifndef FA_POLY_EXP
+#define FA_POLY_EXP 0
+#endif
+#ifndef FA_P_CHUNK
+#define FA_P_CHUNK 32
+#endif
+constexpr int kPolyExp = FA_POLY_EXP;
+constexpr int kPChunk = FA_P_CHUNK;
 
 constexpr unsigned kStatusTimeout = 4;  // same value as FA_ERR_TIMEOUT
 enum : int { kRoleSoftmax = 1, kRoleTma = 2, kRoleMma = 3 };
@@ -97,7 +108,7 @@ struct SmemLayout {
     static constexpr int kK = kQ + kQTiles * kTileBytes;
     static constexpr int kV = kK + kStages * kTileBytes;
     static constexpr int kBar = kV + kStages * kTileBytes;
-    static constexpr int kNumBars = 32;
+    static constexpr int kNumBars = 40;
     static constexpr int kMisc = kBar + kNumBars * 8;
     static constexpr int kBytes = kMisc + 16;
     static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 B
@@ -110,8 +121,9 @@ enum : int {
     kBarQEmpty = kBarQFull + kQTiles,       // + t
     kBarKFull = kBarQEmpty + kQTiles,       // + stage
     kBarVFull = kBarKFull + kMaxStages,     // + stage
-    kBarKVEmpty = kBarVFull + kMaxStages,   // + stage
-    kBarSFull = kBarKVEmpty + kMaxStages,   // + t
+    kBarKEmpty = kBarVFull + kMaxStages,    // + stage
+    kBarVEmpty = kBarKEmpty + kMaxStages,   // + stage
+    kBarSFull = kBarVEmpty + kMaxStages,    // + t
     kBarPFull = kBarSFull + kQTiles,        // + t
     kBarODone = kBarPFull + kQTiles,        // + t
     kBarOFree = kBarODone + kQTiles,        // + t
@@ -158,6 +170,119 @@ __device__ __forceinline__ void record_timeout(const FwdParams &p, volatile int 
     }
 }
 
+// 2^y for two values on the FMA pipe (relieves the MUFU unit, which would
+// otherwise bound the softmax). Method: range reduction 2^y = 2^n * 2^f with
+// n = rint(y) (the 1.5 * 2^23 shifter: adding it leaves rint(y) in the low
+// mantissa bits) and f = y - n in [-1/2, 1/2]; 2^f = e^(f ln 2) by its Taylor
+// polynomial of degree 4, coefficients (ln 2)^k / k!, whose truncation error is
+// below (ln 2 / 2)^5 / 5! * sqrt(2) = 5.9e-5 relative; 2^n is added to the
+// exponent field of the result. Inputs are clamped to >= -125 so the exponent
+// stays normal (values below 2^-125 are negligible next to the row max term).
+__device__ __forceinline__ void exp2_poly2(float &a, float &b) {
+    constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
+    constexpr float c1 = 0.69314718055994529f, c2 = 0.24022650695910069f,
+                    c3 = 0.055504108664821576f, c4 = 0.0096181291076284769f;
+    a = fmaxf(a, -125.f);
+    b = fmaxf(b, -125.f);
+    float ta = a, tb = b;
+    fadd2(ta, tb, kShift, kShift);      // low bits of t = rint(y)
+    float na = ta, nb = tb;
+    fadd2(na, nb, -kShift, -kShift);    // n = rint(y) as a float
+    float fa = a, fb = b;
+    fadd2(fa, fb, -na, -nb);            // f = y - n
+    float pa = c4, pb = c4;
+    ffma2(pa, pb, fa, fb, c3, c3);
+    ffma2(pa, pb, fa, fb, c2, c2);
+    ffma2(pa, pb, fa, fb, c1, c1);
+    ffma2(pa, pb, fa, fb, 1.f, 1.f);    // 2^f
+    // bits(t) = bits(1.5 * 2^23) + n and bits(1.5 * 2^23) << 23 == 0 (mod 2^32),
+    // so (bits(t) << 23) adds exactly n to the exponent field.
+    a = __int_as_float(__float_as_int(pa) + (__float_as_int(ta) << 23));
+    b = __int_as_float(__float_as_int(pb) + (__float_as_int(tb) << 23));
+}
+
+// One online-softmax step of this thread's row over a 128-key tile whose fp32
+// scores sit at TMEM address tS (this warp's lanes). Masks hidden keys (only
+// when `boundary`), moves the reference max m lazily, adds the tile's
+// probabilities to l, and stores them as packed 16-bit pairs at TMEM address
+// tP (64 columns). Returns the factor by which the caller must rescale O
+// (1 when the reference max did not move). The stores are left in flight:
+// the caller waits with tcgen05.wait::st before signalling.
+// kPoly of every 32 probabilities are computed with exp2_poly2, the rest with
+// the MUFU ex2 instruction.
+template <bool BF16, int kPoly, int kPChunk>
+__device__ __forceinline__ float softmax_tile(uint32_t tS, uint32_t tP, bool boundary, int kv0,
+                                              int lo_i, int hi_i, float sl2, float &m, float &l) {
+    static_assert(kPoly % 2 == 0 && kPoly <= 32, "poly share");
+    uint32_t sr[4][32];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
+    float x[kBN];
+#pragma unroll
+    for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(sr[c >> 5][c & 31]);
+    if (boundary) {
+#pragma unroll
+        for (int c = 0; c < kBN; ++c) {
+            const int key = kv0 + c;
+            if (key < lo_i || key > hi_i) x[c] = -INFINITY;
+        }
+    }
+    // Row max: four independent chains of 3-input max.
+    float ma = fmaxf(x[0], x[1]), mb = fmaxf(x[2], x[3]);
+    float mc = fmaxf(x[4], x[5]), md = fmaxf(x[6], x[7]);
+#pragma unroll
+    for (int c = 8; c < kBN; c += 8) {
+        ma = max3f(ma, x[c + 0], x[c + 1]);
+        mb = max3f(mb, x[c + 2], x[c + 3]);
+        mc = max3f(mc, x[c + 4], x[c + 5]);
+        md = max3f(md, x[c + 6], x[c + 7]);
+    }
+    const float m_tile = fmaxf(fmaxf(ma, mb), fmaxf(mc, md)) * sl2;
+    // Lazy rescale: move the reference max only when this block's max exceeds
+    // it by more than the threshold.
+    const float m_old = m;
+    if (m_tile > m + kRescaleThreshold) m = m_tile;
+    const float corr = m != m_old ? ex2_approx(m_old - m) : 1.f;
+    const float nm = m == -INFINITY ? 0.f : -m;
+    // p = 2^(x * scale * log2 e - m), 32 keys at a time; each chunk is packed to
+    // 16-bit pairs and stored while the next one is computed.
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    static_assert(kPChunk == 16 || kPChunk == 32 || kPChunk == 64, "P chunk");
+#pragma unroll
+    for (int c = 0; c < kBN; c += kPChunk) {
+#pragma unroll
+        for (int e = 0; e < kPChunk; e += 2) {
+            ffma2(x[c + e], x[c + e + 1], sl2, sl2, nm, nm);
+            if ((e & 31) < kPoly) {
+                exp2_poly2(x[c + e], x[c + e + 1]);
+            } else {
+                x[c + e] = ex2_approx(x[c + e]);
+                x[c + e + 1] = ex2_approx(x[c + e + 1]);
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < kPChunk; e += 4) {
+            fadd2(s0, s1, x[c + e], x[c + e + 1]);
+            fadd2(s2, s3, x[c + e + 2], x[c + e + 3]);
+        }
+        uint32_t pk[kPChunk / 2];
+#pragma unroll
+        for (int e = 0; e < kPChunk / 2; ++e) pk[e] = pack2<BF16>(x[c + 2 * e], x[c + 2 * e + 1]);
+        if constexpr (kPChunk == 64) {
+            tmem_st16(tP + c / 2, pk);
+            tmem_st16(tP + c / 2 + 16, pk + 16);
+        } else if constexpr (kPChunk == 32) {
+            tmem_st16(tP + c / 2, pk);
+        } else {
+            tmem_st8(tP + c / 2, pk);
+        }
+    }
+    l = l * corr + ((s0 + s1) + (s2 + s3));
+    return corr;
+}
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -201,7 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(kBarKFull + s), 1);
             mbar_init(bar(kBarVFull + s), 1);
-            mbar_init(bar(kBarKVEmpty + s), 1);
+            mbar_init(bar(kBarKEmpty + s), 1);
+            mbar_init(bar(kBarVEmpty + s), 1);
         }
         mbar_init(bar(kBarDrain), 1);
         *abort_flag = 0;
@@ -238,12 +364,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = U.a[0]; ok && j <= j1; ++j, ++kv_iter) {
                     const int st = kv_iter % kStages;
                     const uint32_t ph = (kv_iter / kStages) & 1;
-                    ok = mbar_wait_bounded(bar(kBarKVEmpty + st), ph ^ 1, abort_flag, budget);
+                    ok = mbar_wait_bounded(bar(kBarKEmpty + st), ph ^ 1, abort_flag, budget);
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(kBarKFull + st), L::kTileBytes);
                     for (int g = 0; g < kRegions; ++g)
                         tma_load_3d(sK + st * L::kTileBytes + g * kRegionBytes, &tmK,
                                     bar(kBarKFull + st), 64 * g, j * kBN, U.bh);
+                    ok = mbar_wait_bounded(bar(kBarVEmpty + st), ph ^ 1, abort_flag, budget);
+                    if (!ok) break;
                     mbar_arrive_expect_tx(bar(kBarVFull + st), L::kTileBytes);
                     for (int g = 0; g < kRegions; ++g)
                         tma_load_3d(sV + st * L::kTileBytes + g * kRegionBytes, &tmV,
@@ -271,79 +399,94 @@ __global__ void __launch_bounds__(kThreads, 1)
         // fully unrolled with compile-time descriptor offsets: the tensor core
         // accepts only about one MMA ahead, so any instruction latency between
         // two issues becomes idle tensor-core time.
+        //
+        // Issue order, iteration j of a unit:
+        //     S_0(j) | O_1 += P_1(j-1) V_{j-1} | S_1(j) | O_0 += P_0(j) V_j
+        // so that each softmax overlaps two MMA groups of the other tile. S_t(j+1)
+        // is issued right after O_t += P_t(j) V_j, which reads P_t(j) from the
+        // same columns: tcgen05.mma operations from one thread execute in issue
+        // order, so the earlier MMA reads its TMEM operand before the later one
+        // writes there (an in-order pipeline has no write-after-read hazard).
         constexpr uint32_t idesc_s = idesc_f16(BF16, kBM, kBN, false);
         constexpr uint32_t idesc_o = idesc_f16(BF16, kBM, D, true);
         auto wait = [&](int b, uint32_t parity) {
             return __all_sync(0xffffffffu, mbar_wait_bounded(bar(b), parity, abort_flag, budget));
         };
-        int kv_iter = 0, unit_iter = 0;
+        int kv_base = 0, unit_iter = 0;
         int pv_count[kQTiles] = {0, 0};   // O_t += P_t V issued so far
         int epi_count[kQTiles] = {0, 0};  // units in which Q tile t had an epilogue
         bool ok = true;
+        // S_t(j) = Q_t K_j^T into TMEM columns t * 128.
+        auto issue_s = [&](int t, int st) {
+            tc_fence_after();
+            const uint64_t dq = sw128_desc(sQ + t * L::kTileBytes, 16, 1024);
+            const uint64_t dk = sw128_desc(sK + st * L::kTileBytes, 16, 1024);
+            if (elect_one()) {
+                // K-step k reads 16 columns: 32 bytes into 64-column region k / 4.
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    constexpr uint32_t kRegion16 = kRegionBytes >> 4;
+                    const uint32_t off = (k >> 2) * kRegion16 + (k & 3) * 2;
+                    umma_f16_ss(tmem + t * kBN, dq + off, dk + off, idesc_s, k > 0 ? 1u : 0u);
+                }
+                umma_commit(bar(kBarSFull + t));
+            }
+            __syncwarp();
+        };
+        // O_t (+)= P_t V_j, P_t read from TMEM.
+        auto issue_pv = [&](int t, int st, bool first) {
+            tc_fence_after();
+            const uint64_t dv = sw128_desc(sV + st * L::kTileBytes, kRegionBytes, 1024);
+            const uint32_t acc0 = first ? 0u : 1u;
+            if (elect_one()) {
+                // K-step k reads keys 16k..16k+15: 16 rows of 128 B of V.
+#pragma unroll
+                for (int k = 0; k < kBN / 16; ++k)
+                    umma_f16_ts(tmem + L::kTmemO + t * D, tmem + t * kBN + k * 8,
+                                dv + k * ((16 * 128) >> 4), idesc_o, k > 0 ? 1u : acc0);
+                umma_commit(bar(kBarODone + t));
+            }
+            __syncwarp();
+            ++pv_count[t];
+        };
+        auto commit = [&](int b) {
+            if (elect_one()) umma_commit(bar(b));
+            __syncwarp();
+        };
         for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++unit_iter) {
             const Unit U = decode_unit(u, p);
             for (int t = 0; t < kQTiles && ok; ++t) ok = wait(kBarQFull + t, unit_iter & 1);
+            const int j0 = U.a[0];
             const int j1 = U.a[1] <= U.b[1] ? U.b[1] : U.b[0];
-            for (int j = U.a[0]; ok && j <= j1; ++j, ++kv_iter) {
-                const int st = kv_iter % kStages;
-                const uint32_t ph = (kv_iter / kStages) & 1;
-                ok = wait(kBarKFull + st, ph);
-                const uint64_t dk = sw128_desc(sK + st * L::kTileBytes, 16, 1024);
-#pragma unroll
-                for (int t = 0; t < kQTiles; ++t) {
-                    if (!ok || j < U.a[t] || j > U.b[t]) continue;
-                    // S_t / P_t columns are free once the previous O_t += P_t V completed.
-                    if (pv_count[t] > 0) ok = wait(kBarODone + t, (pv_count[t] - 1) & 1);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint64_t dq = sw128_desc(sQ + t * L::kTileBytes, 16, 1024);
-                    if (elect_one()) {
-                        // K-step k reads 16 columns: 32 bytes into 64-column region k / 4.
-#pragma unroll
-                        for (int k = 0; k < D / 16; ++k) {
-                            constexpr uint32_t kRegion16 = kRegionBytes >> 4;
-                            const uint32_t off = (k >> 2) * kRegion16 + (k & 3) * 2;
-                            umma_f16_ss(tmem + t * kBN, dq + off, dk + off, idesc_s, k > 0 ? 1u : 0u);
-                        }
-                        umma_commit(bar(kBarSFull + t));
-                    }
-                    __syncwarp();
+            auto in = [&U](int t, int j) { return j >= U.a[t] && j <= U.b[t]; };
+            for (int j = j0; ok && j <= j1 + 1; ++j) {
+                const int pos = kv_base + (j - j0);  // ring position of K_j / V_j
+                const int st = pos % kStages;
+                const uint32_t ph = (pos / kStages) & 1;
+                const int pst = (pos - 1 + kStages) % kStages;
+                const uint32_t pph = ((pos - 1) / kStages) & 1;
+                if (j <= j1) ok = wait(kBarKFull + st, ph);
+                if (ok && in(0, j)) issue_s(0, st);
+                if (ok && in(1, j - 1)) {
+                    ok = wait(kBarVFull + pst, pph) && wait(kBarPFull + 1, pv_count[1] & 1);
+                    if (ok && j - 1 == U.a[1]) ok = wait(kBarOFree + 1, (epi_count[1] & 1) ^ 1);
+                    if (ok) issue_pv(1, pst, j - 1 == U.a[1]);
                 }
-                if (ok && j == j1) {
-                    // Both Q buffers are free once the unit's last S MMAs complete.
-                    if (elect_one())
-                        for (int q = 0; q < kQTiles; ++q) umma_commit(bar(kBarQEmpty + q));
-                    __syncwarp();
+                if (ok && in(1, j)) issue_s(1, st);
+                if (ok && j <= j1) {
+                    commit(kBarKEmpty + st);  // K_j is free once its S MMAs complete
+                    if (j == j1)              // both Q buffers too
+                        for (int t = 0; t < kQTiles; ++t) commit(kBarQEmpty + t);
                 }
-                if (ok) ok = wait(kBarVFull + st, ph);
-                const uint64_t dv = sw128_desc(sV + st * L::kTileBytes, kRegionBytes, 1024);
-#pragma unroll
-                for (int t = 0; t < kQTiles; ++t) {
-                    if (!ok || j < U.a[t] || j > U.b[t]) continue;
-                    ok = wait(kBarPFull + t, pv_count[t] & 1);
-                    // The first O_t += P_t V of a unit overwrites O_t: the previous
-                    // unit's epilogue of tile t must have read it.
-                    if (ok && j == U.a[t]) ok = wait(kBarOFree + t, (epi_count[t] & 1) ^ 1);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t acc0 = j > U.a[t] ? 1u : 0u;
-                    if (elect_one()) {
-                        // K-step k reads keys 16k..16k+15: 16 rows of 128 B of V.
-#pragma unroll
-                        for (int k = 0; k < kBN / 16; ++k)
-                            umma_f16_ts(tmem + L::kTmemO + t * D, tmem + t * kBN + k * 8,
-                                        dv + k * ((16 * 128) >> 4), idesc_o, k > 0 ? 1u : acc0);
-                        umma_commit(bar(kBarODone + t));
-                    }
-                    __syncwarp();
-                    ++pv_count[t];
+                if (ok && in(0, j)) {
+                    ok = wait(kBarVFull + st, ph) && wait(kBarPFull + 0, pv_count[0] & 1);
+                    if (ok && j == U.a[0]) ok = wait(kBarOFree + 0, (epi_count[0] & 1) ^ 1);
+                    if (ok) issue_pv(0, st, j == U.a[0]);
                 }
-                if (ok) {
-                    // K_j and V_j are free once every MMA issued so far completes.
-                    if (elect_one()) umma_commit(bar(kBarKVEmpty + st));
-                    __syncwarp();
-                }
+                // V_{j-1} is free once O_1 += P_1(j-1) V_{j-1} (issued above) completes.
+                if (ok && j > j0) commit(kBarVEmpty + pst);
             }
+            kv_base += j1 - j0 + 1;
             for (int t = 0; t < kQTiles; ++t)
                 if (U.a[t] <= U.b[t]) ++epi_count[t];
             if (!ok && lane == 0) record_timeout(p, abort_flag, kRoleMma, u);
@@ -383,55 +526,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                                abort_flag, budget));
                 if (!ok) break;
                 tc_fence_after();
-                uint32_t sr[4][32];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
-                float x[kBN];
-#pragma unroll
-                for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(sr[c >> 5][c & 31]);
                 const int kv0 = j * kBN;
-                if (!(kv0 >= lo_last && kv0 + kBN - 1 <= hi_first)) {
-#pragma unroll
-                    for (int c = 0; c < kBN; ++c) {
-                        const int key = kv0 + c;
-                        if (key < lo_i || key > hi_i) x[c] = -INFINITY;
-                    }
-                }
-                // Row max: four independent chains of 3-input max.
-                float ma = fmaxf(x[0], x[1]), mb = fmaxf(x[2], x[3]);
-                float mc = fmaxf(x[4], x[5]), md = fmaxf(x[6], x[7]);
-#pragma unroll
-                for (int c = 8; c < kBN; c += 8) {
-                    ma = max3f(ma, x[c + 0], x[c + 1]);
-                    mb = max3f(mb, x[c + 2], x[c + 3]);
-                    mc = max3f(mc, x[c + 4], x[c + 5]);
-                    md = max3f(md, x[c + 6], x[c + 7]);
-                }
-                const float m_tile = fmaxf(fmaxf(ma, mb), fmaxf(mc, md)) * sl2;
-                // Lazy rescale: move the reference max only when this block's max
-                // exceeds it by more than the threshold.
-                const float m_old = m;
-                if (m_tile > m + kRescaleThreshold) m = m_tile;
-                const float corr = m != m_old ? ex2_approx(m_old - m) : 1.f;
-                const float nm = m == -INFINITY ? 0.f : -m;
-                float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f, s4 = 0.f, s5 = 0.f, s6 = 0.f, s7 = 0.f;
-#pragma unroll
-                for (int c = 0; c < kBN; c += 8) {
-#pragma unroll
-                    for (int e = 0; e < 8; e += 2) {
-                        ffma2(x[c + e], x[c + e + 1], sl2, sl2, nm, nm);
-                        x[c + e] = ex2_approx(x[c + e]);
-                        x[c + e + 1] = ex2_approx(x[c + e + 1]);
-                    }
-                    fadd2(s0, s1, x[c + 0], x[c + 1]);
-                    fadd2(s2, s3, x[c + 2], x[c + 3]);
-                    fadd2(s4, s5, x[c + 4], x[c + 5]);
-                    fadd2(s6, s7, x[c + 6], x[c + 7]);
-                }
-                l = l * corr + (((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7)));
-                // O_t holds the sum up to block j-1 (complete: S_t(j) was issued after it).
+                const float corr = softmax_tile<BF16, kPolyExp, kPChunk>(
+                    tS, tS, !(kv0 >= lo_last && kv0 + kBN - 1 <= hi_first), kv0, lo_i, hi_i, sl2, m, l);
+                // O_t holds the sum up to block j-1: that MMA was issued before S_t(j),
+                // whose completion (s_full) implies its completion.
                 if (j > U.a[t] && __any_sync(0xffffffffu, corr != 1.f)) {
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
@@ -447,15 +546,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         tmem_st32(tO + c * 32, o);
                     }
-                }
-                // P_t(j) as packed 16-bit pairs over the first 64 columns of S_t.
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        pk[e] = pack2<BF16>(x[64 * h + 2 * e], x[64 * h + 2 * e + 1]);
-                    tmem_st32(tS + 32 * h, pk);
                 }
                 tmem_st_wait();
                 tc_fence_before();
