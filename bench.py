@@ -131,12 +131,19 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """Max of a per-rank scalar (the timing reduction; nothing of the data path)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(world: int, flops_per_rank: float, ms_per_step_max: float) -> float:
+    """Whole-job TFLOP/s: every rank runs its own replica; the slowest rank sets the time."""
+    return world * flops_per_rank / (ms_per_step_max * 1e-3) / 1e12
 
 
 def oracle_slab(w):
@@ -292,7 +299,7 @@ def main():
     ms_local = e0.elapsed_time(e1)
     ms_total = max_over_ranks(ms_local, world)
     ms_step = ms_total / args.steps
-    value = world * flops / (ms_step * 1e-3) / 1e12
+    value = job_throughput(world, flops, ms_step)
     kernel_ms = ms_local / args.steps  # one launch per step on this stream
 
     # ---- end to end through the public API with pinned host buffers

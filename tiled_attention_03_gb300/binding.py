@@ -55,6 +55,8 @@ def load_library(path: str = LIB) -> ctypes.CDLL:
     lib.fa_set_wait_budget_ns.argtypes = [ctypes.c_uint64]
     lib.fa_launch_count.restype = ctypes.c_int64
     lib.fa_launch_count.argtypes = []
+    lib.fa_test_arm_fault.restype = None
+    lib.fa_test_arm_fault.argtypes = [ctypes.c_int32]
     _lib = lib
     return lib
 
@@ -84,6 +86,11 @@ def fa_set_wait_budget_ns(ns: int) -> None:
 
 def fa_launch_count() -> int:
     return load_library().fa_launch_count()
+
+
+def fa_test_arm_fault(kv_position: int) -> None:
+    """Test hook: the next fa_forward skips one K load in CTA 0 (see include/fa.h)."""
+    load_library().fa_test_arm_fault(int(kv_position))
 
 
 def _stream_handle(stream) -> int | None:

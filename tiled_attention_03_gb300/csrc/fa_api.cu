@@ -23,6 +23,7 @@ constexpr int kMaxDevices = 64;
 constexpr uint64_t kDefaultBudgetNs = 2000000000ull;
 
 std::atomic<int64_t> g_launches{0};
+std::atomic<int> g_fault_pos{-1};
 std::atomic<uint64_t> g_budget_ns{0};
 
 struct DeviceState {
@@ -167,6 +168,8 @@ void fa_set_wait_budget_ns(uint64_t ns) { g_budget_ns.store(ns); }
 
 int64_t fa_launch_count(void) { return g_launches.load(); }
 
+void fa_test_arm_fault(int32_t kv_position) { g_fault_pos.store(kv_position < 0 ? -1 : kv_position); }
+
 fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float *LSE, int64_t B,
                      int64_t H, int64_t N, int64_t d, float scale, fa_mask_mode mask_mode,
                      int64_t window_left, int64_t window_right, fa_dtype dtype, void *stream) {
@@ -233,6 +236,7 @@ fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
     p.wait_budget_ns = wait_budget();
     p.status = ds->status;
+    p.fault_skip_k = g_fault_pos.exchange(-1);
 
     // Persistent grid: one CTA per SM (each holds the SM's whole tensor memory).
     const int64_t blocks = n_units < ds->sm_count ? n_units : ds->sm_count;

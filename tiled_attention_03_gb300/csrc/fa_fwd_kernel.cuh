@@ -96,6 +96,7 @@ struct FwdParams {
     float scale_log2; // scale * log2(e)
     unsigned long long wait_budget_ns;
     unsigned int *status;  // [code, role, unit, block]
+    int fault_skip_k;      // test hook: CTA 0 skips the K load at this ring position (-1: none)
 };
 
 template <int D>
@@ -366,10 +367,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t ph = (kv_iter / kStages) & 1;
                     ok = mbar_wait_bounded(bar(kBarKEmpty + st), ph ^ 1, abort_flag, budget);
                     if (!ok) break;
-                    mbar_arrive_expect_tx(bar(kBarKFull + st), L::kTileBytes);
-                    for (int g = 0; g < kRegions; ++g)
-                        tma_load_3d(sK + st * L::kTileBytes + g * kRegionBytes, &tmK,
-                                    bar(kBarKFull + st), 64 * g, j * kBN, U.bh);
+                    if (!(kv_iter == p.fault_skip_k && blockIdx.x == 0)) {
+                        mbar_arrive_expect_tx(bar(kBarKFull + st), L::kTileBytes);
+                        for (int g = 0; g < kRegions; ++g)
+                            tma_load_3d(sK + st * L::kTileBytes + g * kRegionBytes, &tmK,
+                                        bar(kBarKFull + st), 64 * g, j * kBN, U.bh);
+                    }
                     ok = mbar_wait_bounded(bar(kBarVEmpty + st), ph ^ 1, abort_flag, budget);
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(kBarVFull + st), L::kTileBytes);
