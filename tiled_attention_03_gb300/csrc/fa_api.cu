@@ -19,10 +19,17 @@ namespace {
 // bounded wait ran out; read and cleared by fa_sync_status.
 __device__ unsigned int g_fa_status[4];
 
+// Work-unit counters of the persistent kernel: {next unit, finished CTAs} per
+// launch. A launch takes slot (launch number mod kSchedSlots); its last CTA
+// zeroes the slot again. Up to kSchedSlots launches may run concurrently.
+constexpr int kSchedSlots = 64;
+__device__ unsigned int g_fa_sched[kSchedSlots][2];
+
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kDefaultBudgetNs = 2000000000ull;
 
 std::atomic<int64_t> g_launches{0};
+std::atomic<uint64_t> g_sched_next{0};
 std::atomic<int> g_fault_pos{-1};
 std::atomic<uint64_t> g_budget_ns{0};
 
@@ -31,6 +38,7 @@ struct DeviceState {
     cudaError_t init_err = cudaSuccess;
     int cc_major = 0, cc_minor = 0, sm_count = 0;
     unsigned int *status = nullptr;
+    unsigned int *sched = nullptr;
 };
 DeviceState g_dev[kMaxDevices];
 
@@ -94,6 +102,10 @@ DeviceState *device_state(int dev) {
             void *addr = nullptr;
             e = cudaGetSymbolAddress(&addr, g_fa_status);
             s.status = static_cast<unsigned int *>(addr);
+            if (e == cudaSuccess) {
+                e = cudaGetSymbolAddress(&addr, g_fa_sched);
+                s.sched = static_cast<unsigned int *>(addr);
+            }
             if (e == cudaSuccess) e = configure_kernel<64, false>();
             if (e == cudaSuccess) e = configure_kernel<64, true>();
             if (e == cudaSuccess) e = configure_kernel<128, false>();
@@ -237,6 +249,7 @@ fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float
     p.wait_budget_ns = wait_budget();
     p.status = ds->status;
     p.fault_skip_k = g_fault_pos.exchange(-1);
+    p.sched = ds->sched + 2 * (g_sched_next.fetch_add(1) % kSchedSlots);
 
     // Persistent grid: one CTA per SM (each holds the SM's whole tensor memory).
     const int64_t blocks = n_units < ds->sm_count ? n_units : ds->sm_count;

@@ -65,8 +65,14 @@ constexpr int kMmaWarp = 9;
 // Per-thread registers after setmaxnreg. Their sum over the CTA must not exceed
 // what the launch allocated (threads x registers of the compiled kernel); the
 // host checks this before the first launch.
-constexpr int kRegsSoftmax = 208;
-constexpr int kRegsControl = 88;
+#ifndef FA_REGS_SOFTMAX
+#define FA_REGS_SOFTMAX 208
+#endif
+#ifndef FA_REGS_CONTROL
+#define FA_REGS_CONTROL 88
+#endif
+constexpr int kRegsSoftmax = FA_REGS_SOFTMAX;
+constexpr int kRegsControl = FA_REGS_CONTROL;
 constexpr int kRegsNeeded = 2 * 128 * kRegsSoftmax + 128 * kRegsControl;
 constexpr int kRegionBytes = 128 * 128;  // 128 rows x 128 B: one 64-column swizzle region
 constexpr uint32_t kTmemCols = 512;
@@ -97,6 +103,7 @@ struct FwdParams {
     unsigned long long wait_budget_ns;
     unsigned int *status;  // [code, role, unit, block]
     int fault_skip_k;      // test hook: CTA 0 skips the K load at this ring position (-1: none)
+    unsigned int *sched;   // this launch's {next unit, finished CTAs} counters (zero at launch)
 };
 
 template <int D>
@@ -111,12 +118,16 @@ struct SmemLayout {
     static constexpr int kBar = kV + kStages * kTileBytes;
     static constexpr int kNumBars = 40;
     static constexpr int kMisc = kBar + kNumBars * 8;
-    static constexpr int kBytes = kMisc + 16;
+    static constexpr int kUnitRing = kMisc + 16;  // kUnitSlots ints: unit ids handed out to the roles
+    static constexpr int kBytes = kUnitRing + 16;
     static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 B
     static constexpr uint32_t kTmemO = 256;       // O_t at kTmemO + t * D
 };
 
 constexpr int kMaxStages = 4;
+constexpr int kUnitSlots = 2;  // unit ids in flight between the scheduler and the other roles
+// Arrivals that free a unit slot: the MMA warp (one elected lane) + every softmax thread.
+constexpr int kUnitConsumers = 1 + 2 * 128;
 enum : int {
     kBarQFull = 0,                          // + t
     kBarQEmpty = kBarQFull + kQTiles,       // + t
@@ -129,7 +140,9 @@ enum : int {
     kBarODone = kBarPFull + kQTiles,        // + t
     kBarOFree = kBarODone + kQTiles,        // + t
     kBarDrain = kBarOFree + kQTiles,
-    kNumBarsUsed = kBarDrain + 1,
+    kBarUnitFull = kBarDrain + 1,           // + slot
+    kBarUnitEmpty = kBarUnitFull + 2,       // + slot
+    kNumBarsUsed = kBarUnitEmpty + 2,
 };
 
 // A work unit: rows [r0, r0 + 256) of head bh; Q tile t covers rows
@@ -304,6 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar0 = sbase + L::kBar;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
+    volatile int *unit_ring = reinterpret_cast<volatile int *>(smem + L::kUnitRing);
     auto bar = [bar0](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
 
     const int warp = threadIdx.x >> 5;
@@ -331,6 +345,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(kBarVEmpty + s), 1);
         }
         mbar_init(bar(kBarDrain), 1);
+        for (int k = 0; k < kUnitSlots; ++k) {
+            mbar_init(bar(kBarUnitFull + k), 1);
+            mbar_init(bar(kBarUnitEmpty + k), kUnitConsumers);
+        }
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmQ);
@@ -349,9 +367,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (warp == kTmaWarp) {
         // ================================================================ TMA producer
         if (lane == 0) {
-            int kv_iter = 0, unit_iter = 0;
+            int kv_iter = 0, unit_iter = 0, q_loads = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++unit_iter) {
+            // Scheduler: take the next unit from the launch-wide counter and hand
+            // its id to the other roles through the shared-memory unit ring
+            // (id -1 ends the loop).
+            for (; ok; ++unit_iter) {
+                const int slot = unit_iter % kUnitSlots;
+                ok = mbar_wait_bounded(bar(kBarUnitEmpty + slot), ((unit_iter / kUnitSlots) & 1) ^ 1,
+                                       abort_flag, budget);
+                if (!ok) break;
+                const unsigned next = atomicAdd(p.sched, 1u);
+                const int u = next < static_cast<unsigned>(p.n_units) ? static_cast<int>(next) : -1;
+                unit_ring[slot] = u;
+                mbar_arrive(bar(kBarUnitFull + slot));
+                if (u < 0) break;
                 const Unit U = decode_unit(u, p);
                 for (int t = 0; t < kQTiles && ok; ++t) {
                     ok = mbar_wait_bounded(bar(kBarQEmpty + t), (unit_iter & 1) ^ 1, abort_flag, budget);
@@ -361,6 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_3d(sQ + t * L::kTileBytes + g * kRegionBytes, &tmQ,
                                     bar(kBarQFull + t), 64 * g, U.r0 + t * kBM, U.bh);
                 }
+                if (ok) ++q_loads;
                 const int j1 = U.a[1] <= U.b[1] ? U.b[1] : U.b[0];
                 for (int j = U.a[0]; ok && j <= j1; ++j, ++kv_iter) {
                     const int st = kv_iter % kStages;
@@ -383,9 +414,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) record_timeout(p, abort_flag, kRoleTma, u);
             }
             // Drain: no copy may still be landing in shared memory when the CTA exits.
-            if (unit_iter > 0)
+            if (q_loads > 0)
                 for (int t = 0; t < kQTiles; ++t)
-                    mbar_wait_bounded(bar(kBarQFull + t), (unit_iter - 1) & 1, nullptr, budget);
+                    mbar_wait_bounded(bar(kBarQFull + t), (q_loads - 1) & 1, nullptr, budget);
             for (int s = 0; s < kStages; ++s) {
                 if (kv_iter > s) {
                     const int last = kv_iter - 1 - ((kv_iter - 1 - s) % kStages);
@@ -456,7 +487,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (elect_one()) umma_commit(bar(b));
             __syncwarp();
         };
-        for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++unit_iter) {
+        for (; ok; ++unit_iter) {
+            const int slot = unit_iter % kUnitSlots;
+            ok = wait(kBarUnitFull + slot, (unit_iter / kUnitSlots) & 1);
+            if (!ok) break;
+            const int u = unit_ring[slot];
+            __syncwarp();
+            if (elect_one()) mbar_arrive(bar(kBarUnitEmpty + slot));
+            __syncwarp();
+            if (u < 0) break;
             const Unit U = decode_unit(u, p);
             for (int t = 0; t < kQTiles && ok; ++t) ok = wait(kBarQFull + t, unit_iter & 1);
             const int j0 = U.a[0];
@@ -512,7 +551,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sl2 = p.scale_log2;
         int s_count = 0;  // S_t tiles consumed so far (= O_t += P_t V issued)
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+        for (int unit_iter = 0; ok; ++unit_iter) {
+            const int slot = unit_iter % kUnitSlots;
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarUnitFull + slot),
+                                                           (unit_iter / kUnitSlots) & 1, abort_flag, budget));
+            if (!ok) {
+                if (lane == 0) record_timeout(p, abort_flag, kRoleSoftmax, -1);
+                break;
+            }
+            const int u = unit_ring[slot];
+            mbar_arrive(bar(kBarUnitEmpty + slot));
+            if (u < 0) break;
             const Unit U = decode_unit(u, p);
             if (U.a[t] > U.b[t]) continue;
             const int rt0 = U.r0 + t * kBM;
@@ -602,6 +651,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
+    }
+    // The last CTA to finish zeroes this launch's scheduler counters for the next
+    // launch that uses them (every CTA has stopped fetching units by now).
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+            atomicExch(p.sched, 0u);
+            atomicExch(p.sched + 1, 0u);
+        }
     }
 }
 
