@@ -24,9 +24,12 @@
 // 256 query rows (two 128-row Q tiles, t = 0, 1) of one (b, h):
 //   warps 0-3 : softmax of Q tile 0 (thread = query row = TMEM lane)
 //   warps 4-7 : softmax of Q tile 1
-//   warp 8    : TMA producer: Q tiles, K_j and V_j into a multi-stage ring
-//   warp 9    : MMA issuer (one thread)
-//   warps 10-11: idle (they complete warpgroup 2, whose registers move to the
+//   warp 8    : scheduler (takes work units from a launch-wide counter) and TMA
+//               producer of the Q tiles and of K_j into a multi-stage ring
+//   warp 9    : MMA issuer (one elected lane)
+//   warp 10   : TMA producer of V_j (its own thread, so K and V prefetch
+//               independently: each is issued as soon as its own slot frees)
+//   warp 11   : idle (completes warpgroup 2, whose registers move to the
 //               softmax warpgroups with setmaxnreg)
 // Tensor memory (512 columns): S_t at columns 128 t (fp32, 128 keys), O_t at
 // 256 + t d (fp32). After the softmax of S_t(j) the probabilities P_t(j) are
@@ -60,8 +63,9 @@ constexpr int kBN = 128;       // keys per K/V tile
 constexpr int kQTiles = 2;     // Q tiles per work unit
 constexpr int kUnitRows = kBM * kQTiles;
 constexpr int kThreads = 384;  // 2 softmax warpgroups + a warpgroup with the TMA and MMA warps
-constexpr int kTmaWarp = 8;
+constexpr int kTmaWarp = 8;   // scheduler, Q and K loads
 constexpr int kMmaWarp = 9;
+constexpr int kVWarp = 10;    // V loads
 // Per-thread registers after setmaxnreg. Their sum over the CTA must not exceed
 // what the launch allocated (threads x registers of the compiled kernel); the
 // host checks this before the first launch.
@@ -126,8 +130,9 @@ struct SmemLayout {
 
 constexpr int kMaxStages = 4;
 constexpr int kUnitSlots = 2;  // unit ids in flight between the scheduler and the other roles
-// Arrivals that free a unit slot: the MMA warp (one elected lane) + every softmax thread.
-constexpr int kUnitConsumers = 1 + 2 * 128;
+// Arrivals that free a unit slot: one per consumer warp (the MMA warp, the V producer
+// and the 8 softmax warps).
+constexpr int kUnitConsumers = 1 + 1 + 8;
 enum : int {
     kBarQFull = 0,                          // + t
     kBarQEmpty = kBarQFull + kQTiles,       // + t
@@ -369,19 +374,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int kv_iter = 0, unit_iter = 0, q_loads = 0;
             bool ok = true;
-            // Scheduler: take the next unit from the launch-wide counter and hand
-            // its id to the other roles through the shared-memory unit ring
-            // (id -1 ends the loop).
-            for (; ok; ++unit_iter) {
-                const int slot = unit_iter % kUnitSlots;
-                ok = mbar_wait_bounded(bar(kBarUnitEmpty + slot), ((unit_iter / kUnitSlots) & 1) ^ 1,
+            // Scheduler: take units from the launch-wide counter and hand their ids
+            // to the other roles through the shared-memory unit ring (id -1 ends
+            // every role's loop). The producer works one unit ahead: once the
+            // first K tiles of unit u are on their way it already claims and
+            // publishes the next unit and prefetches that unit's Q tiles (read
+            // once, from DRAM) into L2, so that loading them into shared memory
+            // at the unit boundary is an L2 hit.
+            auto publish = [&](int k) -> int {
+                const int slot = k % kUnitSlots;
+                ok = mbar_wait_bounded(bar(kBarUnitEmpty + slot), ((k / kUnitSlots) & 1) ^ 1,
                                        abort_flag, budget);
-                if (!ok) break;
+                if (!ok) return -1;
                 const unsigned next = atomicAdd(p.sched, 1u);
-                const int u = next < static_cast<unsigned>(p.n_units) ? static_cast<int>(next) : -1;
-                unit_ring[slot] = u;
+                const int v = next < static_cast<unsigned>(p.n_units) ? static_cast<int>(next) : -1;
+                unit_ring[slot] = v;
                 mbar_arrive(bar(kBarUnitFull + slot));
-                if (u < 0) break;
+                return v;
+            };
+            auto prefetch_q_l2 = [&](int v) {
+                const Unit W = decode_unit(v, p);
+                for (int t = 0; t < kQTiles; ++t)
+                    for (int g = 0; g < kRegions; ++g)
+                        tma_prefetch_l2_3d(&tmQ, 64 * g, W.r0 + t * kBM, W.bh);
+            };
+            int u = publish(0);
+            for (; ok && u >= 0; ++unit_iter) {
                 const Unit U = decode_unit(u, p);
                 for (int t = 0; t < kQTiles && ok; ++t) {
                     ok = mbar_wait_bounded(bar(kBarQEmpty + t), (unit_iter & 1) ^ 1, abort_flag, budget);
@@ -391,9 +409,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_3d(sQ + t * L::kTileBytes + g * kRegionBytes, &tmQ,
                                     bar(kBarQFull + t), 64 * g, U.r0 + t * kBM, U.bh);
                 }
-                if (ok) ++q_loads;
+                if (!ok) break;
+                ++q_loads;
+                int u_next = -1;
+                bool claimed = false;
                 const int j1 = U.a[1] <= U.b[1] ? U.b[1] : U.b[0];
                 for (int j = U.a[0]; ok && j <= j1; ++j, ++kv_iter) {
+                    // claim the next unit after the first two K loads (or at the last one)
+                    if (!claimed && (j == U.a[0] + 2 || j == j1)) {
+                        claimed = true;
+                        u_next = publish(unit_iter + 1);
+                        if (!ok) break;
+                        if (u_next >= 0) prefetch_q_l2(u_next);
+                    }
                     const int st = kv_iter % kStages;
                     const uint32_t ph = (kv_iter / kStages) & 1;
                     ok = mbar_wait_bounded(bar(kBarKEmpty + st), ph ^ 1, abort_flag, budget);
@@ -404,7 +432,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tma_load_3d(sK + st * L::kTileBytes + g * kRegionBytes, &tmK,
                                         bar(kBarKFull + st), 64 * g, j * kBN, U.bh);
                     }
-                    ok = mbar_wait_bounded(bar(kBarVEmpty + st), ph ^ 1, abort_flag, budget);
+                }
+                u = u_next;
+            }
+            if (!ok) record_timeout(p, abort_flag, kRoleTma, u);
+            // Drain: no copy may still be landing in shared memory when the CTA exits.
+            if (q_loads > 0)
+                for (int t = 0; t < kQTiles; ++t)
+                    mbar_wait_bounded(bar(kBarQFull + t), (q_loads - 1) & 1, nullptr, budget);
+            for (int s = 0; s < kStages; ++s) {
+                if (kv_iter > s) {
+                    const int last = kv_iter - 1 - ((kv_iter - 1 - s) % kStages);
+                    mbar_wait_bounded(bar(kBarKFull + s), (last / kStages) & 1, nullptr, budget);
+                }
+            }
+        }
+      } else if (warp == kVWarp) {
+        // ================================================================ V producer
+        if (lane == 0) {
+            int kv_iter = 0;
+            bool ok = true;
+            for (int unit_iter = 0; ok; ++unit_iter) {
+                const int slot = unit_iter % kUnitSlots;
+                ok = mbar_wait_bounded(bar(kBarUnitFull + slot), (unit_iter / kUnitSlots) & 1,
+                                       abort_flag, budget);
+                if (!ok) break;
+                const int u = unit_ring[slot];
+                mbar_arrive(bar(kBarUnitEmpty + slot));
+                if (u < 0) break;
+                const Unit U = decode_unit(u, p);
+                const int j1 = U.a[1] <= U.b[1] ? U.b[1] : U.b[0];
+                for (int j = U.a[0]; ok && j <= j1; ++j, ++kv_iter) {
+                    const int st = kv_iter % kStages;
+                    ok = mbar_wait_bounded(bar(kBarVEmpty + st), ((kv_iter / kStages) & 1) ^ 1,
+                                           abort_flag, budget);
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(kBarVFull + st), L::kTileBytes);
                     for (int g = 0; g < kRegions; ++g)
@@ -413,16 +474,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) record_timeout(p, abort_flag, kRoleTma, u);
             }
+            if (!ok) record_timeout(p, abort_flag, kRoleTma, -1);
             // Drain: no copy may still be landing in shared memory when the CTA exits.
-            if (q_loads > 0)
-                for (int t = 0; t < kQTiles; ++t)
-                    mbar_wait_bounded(bar(kBarQFull + t), (q_loads - 1) & 1, nullptr, budget);
             for (int s = 0; s < kStages; ++s) {
                 if (kv_iter > s) {
                     const int last = kv_iter - 1 - ((kv_iter - 1 - s) % kStages);
-                    const uint32_t ph = (last / kStages) & 1;
-                    mbar_wait_bounded(bar(kBarKFull + s), ph, nullptr, budget);
-                    mbar_wait_bounded(bar(kBarVFull + s), ph, nullptr, budget);
+                    mbar_wait_bounded(bar(kBarVFull + s), (last / kStages) & 1, nullptr, budget);
                 }
             }
         }
@@ -560,7 +617,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             const int u = unit_ring[slot];
-            mbar_arrive(bar(kBarUnitEmpty + slot));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarUnitEmpty + slot));
             if (u < 0) break;
             const Unit U = decode_unit(u, p);
             if (U.a[t] > U.b[t]) continue;
