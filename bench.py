@@ -229,7 +229,7 @@ def run_e2e(args, w, q_h, k_h, v_h, mask, stream, dev, world, flops):
     wall_ms = (time.perf_counter() - t0) * 1e3 / args.e2e_steps
     e2e_ms = max_over_ranks(max(e2.elapsed_time(e3) / args.e2e_steps, wall_ms), world)
     elems = q_h.numel()
-    h2d = 3 * elems * q_h.element_size()
+    h2d = (q_h.numel() + k_h.numel() + v_h.numel()) * q_h.element_size()
     d2h = elems * q_h.element_size() + (elems // w.d) * 4
     return {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
@@ -268,8 +268,10 @@ def main():
     mask = {0: "none", 1: "causal", 2: "window"}[w.mask]
     stream = torch.cuda.current_stream(dev)
 
+    call = fa.fa_forward if w.kv_heads == w.H else fa.fa_forward_gqa
+
     def step():
-        fa.fa_forward(q, k, v, o, lse, w.scale, mask, w.window_left, w.window_right, stream)
+        call(q, k, v, o, lse, w.scale, mask, w.window_left, w.window_right, stream)
 
     for _ in range(args.warmup):
         step()
@@ -324,8 +326,9 @@ def main():
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
                        "mask": mask, "seed": w.seed,
                        "parallelism": f"{world} independent replica(s), no collective",
-                       "l2": (f"inputs (3 x {q.numel() * 2 / 1e6:.0f} MB) larger than L2, no flush"
-                              if 3 * q.numel() * 2 > 129e6 else "inputs smaller than L2, no flush")},
+                       "kv_heads": w.kv_heads,
+                       "l2": (f"inputs ({(q.numel() + k.numel() + v.numel()) * 2 / 1e6:.0f} MB) larger than L2, no flush"
+                              if (q.numel() + k.numel() + v.numel()) * 2 > 129e6 else "inputs smaller than L2, no flush")},
             "tokens_per_s": world * w.B * w.N / (ms_step * 1e-3),
             "pct_of_peak": 100.0 * value / (world * peak_tf),
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf,

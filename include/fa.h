@@ -79,6 +79,20 @@ fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float
                      fa_mask_mode mask_mode, int64_t window_left, int64_t window_right,
                      fa_dtype dtype, void *stream);
 
+/*
+ * fa_forward_gqa -- fa_forward with grouped K/V heads (GQA; MQA when H_kv = 1),
+ * the "GQA/MQA" adaptation that "ai6s.net/6af30f4d40858c2d8819b6d5" §5 lists
+ * among the practical variants. K and V are contiguous B x H_kv x N x d; query
+ * head h of batch b attends with K/V head h / (H / H_kv) of batch b. H_kv must
+ * divide H (else FA_ERR_INVALID_ARG). Q, O, LSE, every other argument,
+ * ownership and errors are as for fa_forward, which equals this call with
+ * H_kv = H.
+ */
+fa_status fa_forward_gqa(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                         int64_t B, int64_t H, int64_t H_kv, int64_t N, int64_t d, float scale,
+                         fa_mask_mode mask_mode, int64_t window_left, int64_t window_right,
+                         fa_dtype dtype, void *stream);
+
 /* Static, NUL-terminated description of a status code. Never NULL. */
 const char *fa_status_string(fa_status status);
 

@@ -42,10 +42,10 @@ def _load():
     global _lib
     if _lib is None:
         lib = ctypes.CDLL(build())
-        lib.oracle_attention.restype = ctypes.c_int
-        lib.oracle_attention.argtypes = [
+        lib.oracle_attention_gqa.restype = ctypes.c_int
+        lib.oracle_attention_gqa.argtypes = [
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
-            ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
             ctypes.c_double, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
             ctypes.c_void_p, ctypes.c_int64,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int]
@@ -72,7 +72,8 @@ def _bits(t: torch.Tensor) -> np.ndarray:
 def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float,
               mask="none", window=(0, 0), units=None, nthreads: int | None = None,
               return_p: bool = False, online_bc: int = 0):
-    """fp64 attention over (B, H, N, d) 16-bit CPU tensors.
+    """fp64 attention over (B, H, N, d) 16-bit CPU tensors; K and V may have
+    fewer heads (B, Hk, N, d) with Hk dividing H (grouped-query attention).
 
     ``units`` is a list of (b*H + h, row0, row1); by default every row of
     every head. Returns (O, LSE[, P]) as float64 numpy arrays with rows packed
@@ -82,7 +83,8 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float,
     """
     lib = _load()
     B, H, N, d = q.shape
-    assert k.shape == q.shape and v.shape == q.shape
+    Hk = k.shape[1]
+    assert k.shape == (B, Hk, N, d) and v.shape == k.shape
     assert q.dtype == k.dtype == v.dtype
     dt = FP16 if q.dtype == torch.float16 else BF16
     if units is None:
@@ -95,8 +97,8 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float,
     qb, kb, vb = _bits(q), _bits(k), _bits(v)
     if nthreads is None:
         nthreads = len(os.sched_getaffinity(0))
-    rc = lib.oracle_attention(
-        qb.ctypes.data, kb.ctypes.data, vb.ctypes.data, dt, B, H, N, d,
+    rc = lib.oracle_attention_gqa(
+        qb.ctypes.data, kb.ctypes.data, vb.ctypes.data, dt, B, H, Hk, N, d,
         float(scale), MASKS[mask], int(window[0]), int(window[1]),
         u.ctypes.data, len(u), O.ctypes.data, LSE.ctypes.data,
         P.ctypes.data if P is not None else None, int(online_bc), int(nthreads))

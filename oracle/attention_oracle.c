@@ -90,7 +90,7 @@ static int is_visible(int64_t i, int64_t j, int mask, int64_t wl, int64_t wr) {
 typedef struct {
     const uint16_t *Q, *K, *V;
     int dtype;
-    int64_t H, N, d;
+    int64_t H, Hk, N, d; /* query heads, K/V heads */
     double scale;
     int mask;
     int64_t wl, wr;
@@ -210,9 +210,12 @@ static void *worker(void *arg) {
     for (int64_t u = jb->tid; u < jb->n_units; u += jb->nthreads) {
         int64_t bh = jb->units[3 * u], r0 = jb->units[3 * u + 1], r1 = jb->units[3 * u + 2];
         if (bh != cur_bh) {
+            /* query head h of batch b reads K/V head h / (H / Hk) of batch b */
+            const int64_t b = bh / jb->H, h = bh % jb->H;
+            const int64_t bkv = b * jb->Hk + h / (jb->H / jb->Hk);
             decode_slab(jb->Q + bh * N * d, jb->dtype, N * d, q);
-            decode_slab(jb->K + bh * N * d, jb->dtype, N * d, k);
-            decode_slab(jb->V + bh * N * d, jb->dtype, N * d, v);
+            decode_slab(jb->K + bkv * N * d, jb->dtype, N * d, k);
+            decode_slab(jb->V + bkv * N * d, jb->dtype, N * d, v);
             cur_bh = bh;
         }
         int64_t orow = jb->out_row[u];
@@ -227,18 +230,21 @@ static void *worker(void *arg) {
 }
 
 /*
- * Attention over a list of units (b*H+h, row0, row1). Output rows are packed
- * in unit order: O is sum(row1-row0) x d, LSE is sum(row1-row0), P (optional,
- * tiny cases only) is sum(row1-row0) x N. bc = 0 selects the direct form,
- * bc > 0 the online recurrence with key blocks of bc. nthreads <= 0 uses all
- * online cores. Returns 0, or -1 on a bad argument.
+ * Attention over a list of units (b*H+h, row0, row1). Q is B x H x N x d; K and
+ * V are B x Hk x N x d, query head h reading K/V head h / (H / Hk) (Hk = H is
+ * ordinary multi-head attention, Hk < H grouped-query attention). Output rows
+ * are packed in unit order: O is sum(row1-row0) x d, LSE is sum(row1-row0), P
+ * (optional, tiny cases only) is sum(row1-row0) x N. bc = 0 selects the direct
+ * form, bc > 0 the online recurrence with key blocks of bc. nthreads <= 0 uses
+ * all online cores. Returns 0, or -1 on a bad argument.
  */
-int oracle_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V, int dtype,
-                     int64_t B, int64_t H, int64_t N, int64_t d, double scale, int mask,
-                     int64_t wl, int64_t wr, const int64_t *units, int64_t n_units,
-                     double *O, double *LSE, double *P, int64_t bc, int nthreads) {
+int oracle_attention_gqa(const uint16_t *Q, const uint16_t *K, const uint16_t *V, int dtype,
+                         int64_t B, int64_t H, int64_t Hk, int64_t N, int64_t d, double scale,
+                         int mask, int64_t wl, int64_t wr, const int64_t *units, int64_t n_units,
+                         double *O, double *LSE, double *P, int64_t bc, int nthreads) {
     if (!Q || !K || !V || !units || !O || !LSE) return -1;
     if (B < 1 || H < 1 || N < 1 || d < 1 || n_units < 0 || bc < 0) return -1;
+    if (Hk < 1 || H % Hk != 0) return -1;
     if (dtype != ORACLE_FP16 && dtype != ORACLE_BF16) return -1;
     if (mask < ORACLE_MASK_NONE || mask > ORACLE_MASK_WINDOW) return -1;
     if (mask == ORACLE_MASK_WINDOW && (wl < 0 || wr < 0)) return -1;
@@ -257,7 +263,7 @@ int oracle_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V, in
     job_t *jobs = (job_t *)calloc((size_t)nthreads, sizeof(job_t));
     pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
     for (int t = 0; t < nthreads; ++t) {
-        job_t j = {Q, K, V, dtype, H, N, d, scale, mask, wl, wr, units, out_row, n_units,
+        job_t j = {Q, K, V, dtype, H, Hk, N, d, scale, mask, wl, wr, units, out_row, n_units,
                    O, LSE, P, bc, nthreads, t};
         jobs[t] = j;
     }
@@ -266,4 +272,13 @@ int oracle_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V, in
     for (int t = 1; t < nthreads; ++t) pthread_join(th[t], NULL);
     free(jobs); free(th); free(out_row);
     return 0;
+}
+
+/* Multi-head attention: oracle_attention_gqa with one K/V head per query head. */
+int oracle_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V, int dtype,
+                     int64_t B, int64_t H, int64_t N, int64_t d, double scale, int mask,
+                     int64_t wl, int64_t wr, const int64_t *units, int64_t n_units,
+                     double *O, double *LSE, double *P, int64_t bc, int nthreads) {
+    return oracle_attention_gqa(Q, K, V, dtype, B, H, H, N, d, scale, mask, wl, wr, units,
+                                n_units, O, LSE, P, bc, nthreads);
 }

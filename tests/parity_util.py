@@ -24,7 +24,10 @@ def run_cuda(q, k, v, scale, mask="none", window=(0, 0), check_guards=True):
     lbuf = torch.full((B * H * N + 2 * GUARD,), SENT_L, dtype=torch.float32, device=dev)
     o = obuf[GUARD:GUARD + n].view(B, H, N, d)
     lse = lbuf[GUARD:GUARD + B * H * N].view(B, H, N)
-    fa.fa_forward(q, k, v, o, lse, scale, mask, window[0], window[1])
+    if k.shape[1] == q.shape[1]:
+        fa.fa_forward(q, k, v, o, lse, scale, mask, window[0], window[1])
+    else:
+        fa.fa_forward_gqa(q, k, v, o, lse, scale, mask, window[0], window[1])
     st = fa.fa_sync_status()
     assert st == fa.FA_OK, fa.fa_status_string(st)
     if check_guards:

@@ -61,6 +61,12 @@ def test_unsupported_head_dim(lib, d):
     assert call(lib, d=d) == fa.FA_ERR_UNSUPPORTED
 
 
+@pytest.mark.parametrize("hk", [0, -1, 3, 5])
+def test_gqa_invalid_kv_heads(lib, hk):
+    rc = lib.fa_forward_gqa(A, B_, C, O_, L_, 1, 4, hk, 16, 64, 0.125, 0, 0, 0, 0, None)
+    assert rc == fa.FA_ERR_INVALID_ARG
+
+
 def test_window_args_ignored_unless_window(lib):
     # Negative window values are only an error in window mode: in the other modes
     # the call gets past argument checks (and then fails on this GPU-less host).

@@ -309,3 +309,33 @@ def test_rejects_bad_arguments():
         oracle.attention(q, k, v, 1.0, "window", (-1, 0))
     with pytest.raises(ValueError):
         oracle.attention(q, k, v, 1.0, "none", units=[(0, 0, 9)])
+
+
+# --- grouped-query attention ------------------------------------------------------
+
+@pytest.mark.parametrize("H,Hk", [(4, 2), (6, 1), (8, 4)])
+@pytest.mark.parametrize("mask,wl,wr", [("none", 0, 0), ("causal", 0, 0), ("window", 9, 2)])
+def test_gqa_equals_mha_on_repeated_kv(H, Hk, mask, wl, wr):
+    # Grouped K/V heads are shared by H / Hk consecutive query heads: the result equals
+    # multi-head attention with each K/V head repeated H / Hk times (same arithmetic).
+    B, N, d = 2, 70, 16
+    q, _, _ = make_qkv(B, H, N, d, torch.bfloat16, seed=H * 10 + Hk)
+    _, k, v = make_qkv(B, Hk, N, d, torch.bfloat16, seed=H * 10 + Hk + 1)
+    O1, L1 = oracle.attention(q, k, v, 0.25, mask, (wl, wr))
+    rep = H // Hk
+    O2, L2 = oracle.attention(q, k.repeat_interleave(rep, dim=1).contiguous(),
+                              v.repeat_interleave(rep, dim=1).contiguous(), 0.25, mask, (wl, wr))
+    np.testing.assert_array_equal(O1, O2)
+    np.testing.assert_array_equal(L1, L2)
+    # and brute force on the repeated form
+    Ob, Lb, _ = brute_force(q, k.repeat_interleave(rep, dim=1), v.repeat_interleave(rep, dim=1),
+                            0.25, mask, wl, wr)
+    np.testing.assert_allclose(O1, Ob, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(L1, Lb, rtol=1e-13, atol=1e-12)
+
+
+def test_gqa_rejects_non_dividing_heads():
+    q, _, _ = make_qkv(1, 3, 8, 4, torch.float16, seed=0)
+    _, k, v = make_qkv(1, 2, 8, 4, torch.float16, seed=1)
+    with pytest.raises(ValueError):
+        oracle.attention(q, k, v, 1.0, "none")

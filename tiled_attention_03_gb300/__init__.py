@@ -2,6 +2,6 @@
 
 from .binding import (FA_DTYPE_BF16, FA_DTYPE_FP16, FA_ERR_CUDA, FA_ERR_INVALID_ARG,  # noqa: F401
                       FA_ERR_TIMEOUT, FA_ERR_UNSUPPORTED, FA_MASK_CAUSAL, FA_MASK_NONE,
-                      FA_MASK_WINDOW, FA_OK, FaError, fa_forward, fa_launch_count,
+                      FA_MASK_WINDOW, FA_OK, FaError, fa_forward, fa_forward_gqa, fa_launch_count,
                       fa_set_wait_budget_ns, fa_status_string, fa_sync_status, fa_test_arm_fault, forward,
                       load_library)

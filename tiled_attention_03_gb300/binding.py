@@ -47,6 +47,11 @@ def load_library(path: str = LIB) -> ctypes.CDLL:
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
         ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_float,
         ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]
+    lib.fa_forward_gqa.restype = ctypes.c_int
+    lib.fa_forward_gqa.argtypes = [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+        ctypes.c_float, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_status_string.argtypes = [ctypes.c_int]
     lib.fa_sync_status.restype = ctypes.c_int
@@ -101,20 +106,30 @@ def _stream_handle(stream) -> int | None:
     return int(stream)
 
 
-def fa_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
-               lse: torch.Tensor, scale: float, mask_mode=FA_MASK_NONE, window_left: int = 0,
-               window_right: int = 0, stream=None) -> None:
-    """Enqueue fa_forward on device tensors (B, H, N, d) -> o, lse (B, H, N)."""
-    lib = load_library()
+def _check(q, k, v, o, lse):
     for t in (q, k, v, o, lse):
         if not t.is_cuda or not t.is_contiguous():
             raise FaError(FA_ERR_INVALID_ARG)
     if q.dtype not in _DTYPES or k.dtype != q.dtype or v.dtype != q.dtype or o.dtype != q.dtype \
             or lse.dtype != torch.float32:
         raise FaError(FA_ERR_INVALID_ARG)
-    B, H, N, d = q.shape
-    if k.shape != q.shape or v.shape != q.shape or o.shape != q.shape or lse.shape != (B, H, N):
+    if q.dim() != 4 or k.dim() != 4:
         raise FaError(FA_ERR_INVALID_ARG)
+    B, H, N, d = q.shape
+    if k.shape[0] != B or k.shape[2:] != q.shape[2:] or v.shape != k.shape or \
+            o.shape != q.shape or lse.shape != (B, H, N):
+        raise FaError(FA_ERR_INVALID_ARG)
+
+
+def fa_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+               lse: torch.Tensor, scale: float, mask_mode=FA_MASK_NONE, window_left: int = 0,
+               window_right: int = 0, stream=None) -> None:
+    """Enqueue fa_forward on device tensors (B, H, N, d) -> o, lse (B, H, N)."""
+    lib = load_library()
+    _check(q, k, v, o, lse)
+    if k.shape != q.shape:
+        raise FaError(FA_ERR_INVALID_ARG)
+    B, H, N, d = q.shape
     rc = lib.fa_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                         B, H, N, d, float(scale), _MASKS[mask_mode], int(window_left),
                         int(window_right), _DTYPES[q.dtype], _stream_handle(stream))
@@ -122,9 +137,25 @@ def fa_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tenso
         raise FaError(rc)
 
 
+def fa_forward_gqa(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                   lse: torch.Tensor, scale: float, mask_mode=FA_MASK_NONE, window_left: int = 0,
+                   window_right: int = 0, stream=None) -> None:
+    """Enqueue fa_forward_gqa: q, o (B, H, N, d); k, v (B, H_kv, N, d); lse (B, H, N)."""
+    lib = load_library()
+    _check(q, k, v, o, lse)
+    B, H, N, d = q.shape
+    rc = lib.fa_forward_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                            lse.data_ptr(), B, H, k.shape[1], N, d, float(scale),
+                            _MASKS[mask_mode], int(window_left), int(window_right),
+                            _DTYPES[q.dtype], _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc)
+
+
 def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
             mask="none", window=(0, 0), stream=None):
-    """Attention forward: returns (O, LSE).
+    """Attention forward: returns (O, LSE). K and V may have fewer heads than Q
+    (grouped-query attention: H_kv must divide H).
 
     Device tensors run in place on the device. Host tensors are copied to the
     current CUDA device, processed, and the results copied back to host
@@ -141,7 +172,7 @@ def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | No
     q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
-    fa_forward(q, k, v, o, lse, scale, mask, window[0], window[1], stream)
+    fa_forward_gqa(q, k, v, o, lse, scale, mask, window[0], window[1], stream)
     if host:
         o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
         lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)

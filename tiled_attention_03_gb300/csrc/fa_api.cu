@@ -182,12 +182,14 @@ int64_t fa_launch_count(void) { return g_launches.load(); }
 
 void fa_test_arm_fault(int32_t kv_position) { g_fault_pos.store(kv_position < 0 ? -1 : kv_position); }
 
-fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float *LSE, int64_t B,
-                     int64_t H, int64_t N, int64_t d, float scale, fa_mask_mode mask_mode,
-                     int64_t window_left, int64_t window_right, fa_dtype dtype, void *stream) {
+fa_status fa_forward_gqa(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                         int64_t B, int64_t H, int64_t H_kv, int64_t N, int64_t d, float scale,
+                         fa_mask_mode mask_mode, int64_t window_left, int64_t window_right,
+                         fa_dtype dtype, void *stream) {
     // ---- host-side checks: nothing is enqueued on failure
     if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+    if (H_kv < 1 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
     if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
     if (mask_mode != FA_MASK_NONE && mask_mode != FA_MASK_CAUSAL && mask_mode != FA_MASK_WINDOW)
         return FA_ERR_INVALID_ARG;
@@ -203,12 +205,14 @@ fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float
     const int64_t n_qb = (N + fa::kUnitRows - 1) / fa::kUnitRows;
     const int64_t n_units = BH * n_qb;
     if (n_units > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+    const int64_t BHkv = B * H_kv;
     const size_t elems = static_cast<size_t>(BH) * static_cast<size_t>(N) * static_cast<size_t>(d);
     const size_t tbytes = elems * 2, lbytes = static_cast<size_t>(BH) * N * sizeof(float);
-    if (overlaps(O, tbytes, Q, tbytes) || overlaps(O, tbytes, K, tbytes) ||
-        overlaps(O, tbytes, V, tbytes) || overlaps(O, tbytes, LSE, lbytes) ||
-        overlaps(LSE, lbytes, Q, tbytes) || overlaps(LSE, lbytes, K, tbytes) ||
-        overlaps(LSE, lbytes, V, tbytes))
+    const size_t kvbytes = static_cast<size_t>(BHkv) * N * d * 2;
+    if (overlaps(O, tbytes, Q, tbytes) || overlaps(O, tbytes, K, kvbytes) ||
+        overlaps(O, tbytes, V, kvbytes) || overlaps(O, tbytes, LSE, lbytes) ||
+        overlaps(LSE, lbytes, Q, tbytes) || overlaps(LSE, lbytes, K, kvbytes) ||
+        overlaps(LSE, lbytes, V, kvbytes))
         return FA_ERR_INVALID_ARG;
 
     int dev = 0;
@@ -226,14 +230,16 @@ fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float
 
     const bool bf16 = dtype == FA_DTYPE_BF16;
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, Q, bf16, BH, N, d) || !make_map(&mk, K, bf16, BH, N, d) ||
-        !make_map(&mv, V, bf16, BH, N, d))
+    if (!make_map(&mq, Q, bf16, BH, N, d) || !make_map(&mk, K, bf16, BHkv, N, d) ||
+        !make_map(&mv, V, bf16, BHkv, N, d))
         return FA_ERR_CUDA;
 
     fa::FwdParams p{};
     p.O = O;
     p.LSE = LSE;
     p.N = static_cast<int>(N);
+    p.H = static_cast<int>(H);
+    p.kv_group = static_cast<int>(H / H_kv);
     p.n_units = static_cast<int>(n_units);
     p.n_qb = static_cast<int>(n_qb);
     int64_t wl = N, wr = N;
@@ -264,6 +270,13 @@ fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float
     if (e != cudaSuccess) return FA_ERR_CUDA;
     g_launches.fetch_add(1);
     return FA_OK;
+}
+
+fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float *LSE, int64_t B,
+                     int64_t H, int64_t N, int64_t d, float scale, fa_mask_mode mask_mode,
+                     int64_t window_left, int64_t window_right, fa_dtype dtype, void *stream) {
+    return fa_forward_gqa(Q, K, V, O, LSE, B, H, H, N, d, scale, mask_mode, window_left,
+                          window_right, dtype, stream);
 }
 
 fa_status fa_sync_status(void *stream) {

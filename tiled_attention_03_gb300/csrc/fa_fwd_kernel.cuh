@@ -99,6 +99,8 @@ struct FwdParams {
     void *O;
     float *LSE;
     int N;            // sequence length
+    int H;            // query heads
+    int kv_group;     // query heads per K/V head (H / H_kv; 1 = one K/V head per query head)
     int n_units;      // (b*H + h, 256-row block) work units
     int n_qb;         // 256-row blocks per head: ceil(N / 256)
     int heavy_first;  // 1: within a head, visit row blocks from the last (most keys) to the first
@@ -150,16 +152,21 @@ enum : int {
     kNumBarsUsed = kBarUnitEmpty + 2,
 };
 
-// A work unit: rows [r0, r0 + 256) of head bh; Q tile t covers rows
+// A work unit: rows [r0, r0 + 256) of query head bh (= b * H + h), whose keys and
+// values are those of K/V head bkv (= b * H_kv + h / kv_group); Q tile t covers rows
 // [r0 + 128 t, r0 + 128 t + 128) and needs K/V tiles [a[t], b[t]] (empty when a > b).
 struct Unit {
-    int bh, r0;
+    int bh, bkv, r0;
     int a[kQTiles], b[kQTiles];
 };
 
 __device__ __forceinline__ Unit decode_unit(int u, const FwdParams &p) {
     Unit U;
     U.bh = u / p.n_qb;
+    {
+        const int b = U.bh / p.H, h = U.bh - b * p.H;
+        U.bkv = b * (p.H / p.kv_group) + h / p.kv_group;
+    }
     int qb = u % p.n_qb;
     if (p.heavy_first) qb = p.n_qb - 1 - qb;
     U.r0 = qb * kUnitRows;
@@ -430,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_arrive_expect_tx(bar(kBarKFull + st), L::kTileBytes);
                         for (int g = 0; g < kRegions; ++g)
                             tma_load_3d(sK + st * L::kTileBytes + g * kRegionBytes, &tmK,
-                                        bar(kBarKFull + st), 64 * g, j * kBN, U.bh);
+                                        bar(kBarKFull + st), 64 * g, j * kBN, U.bkv);
                     }
                 }
                 u = u_next;
@@ -470,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(bar(kBarVFull + st), L::kTileBytes);
                     for (int g = 0; g < kRegions; ++g)
                         tma_load_3d(sV + st * L::kTileBytes + g * kRegionBytes, &tmV,
-                                    bar(kBarVFull + st), 64 * g, j * kBN, U.bh);
+                                    bar(kBarVFull + st), 64 * g, j * kBN, U.bkv);
                 }
                 if (!ok) record_timeout(p, abort_flag, kRoleTma, u);
             }

@@ -45,6 +45,7 @@ class Workload:
     window_right: int
     seed: int
     q_std: float = 1.0
+    H_kv: int = 0  # K/V heads (grouped-query attention); 0 means H
 
     @property
     def scale(self) -> float:
@@ -55,11 +56,16 @@ class Workload:
     def dtype_name(self) -> str:
         return {torch.float16: "fp16", torch.bfloat16: "bf16"}[self.dtype]
 
+    @property
+    def kv_heads(self) -> int:
+        return self.H_kv or self.H
+
     def describe(self) -> str:
         m = MASK_NAMES[self.mask]
         if self.mask == MASK_WINDOW:
             m += f"({self.window_left},{self.window_right})"
-        return f"B{self.B} H{self.H} N{self.N} d{self.d} {self.dtype_name} {m}"
+        kv = f" Hkv{self.kv_heads}" if self.kv_heads != self.H else ""
+        return f"B{self.B} H{self.H}{kv} N{self.N} d{self.d} {self.dtype_name} {m}"
 
 
 WORKLOADS = [
@@ -71,25 +77,35 @@ WORKLOADS = [
     Workload("causal_long_b8h40n8192", 8, 40, 8192, 128, torch.bfloat16, MASK_CAUSAL, 0, 0, seed=4),
 ]
 
-BY_NAME = {w.name: w for w in WORKLOADS}
+# Shapes for the widened rows (grouped-query attention): the bench shape with 8 K/V
+# heads shared by 32 query heads, and a multi-query causal case.
+EXTRA_WORKLOADS = [
+    Workload("gqa_b4h32kv8n4096d128", 4, 32, 4096, 128, torch.bfloat16, MASK_NONE, 0, 0,
+             seed=5, H_kv=8),
+    Workload("mqa_causal_b2h16kv1n2048d64", 2, 16, 2048, 64, torch.float16, MASK_CAUSAL, 0, 0,
+             seed=6, H_kv=1),
+]
+
+BY_NAME = {w.name: w for w in WORKLOADS + EXTRA_WORKLOADS}
 
 
 def make_qkv(B: int, H: int, N: int, d: int, dtype: torch.dtype, seed: int,
-             q_std: float = 1.0):
-    """Return CPU tensors (Q, K, V) of shape (B, H, N, d) in ``dtype``."""
+             q_std: float = 1.0, H_kv: int = 0):
+    """Return CPU tensors Q (B, H, N, d) and K, V (B, H_kv or H, N, d) in ``dtype``."""
     g = torch.Generator(device="cpu")
     g.manual_seed(seed)
+    Hk = H_kv or H
     q = torch.randn(B, H, N, d, generator=g, dtype=torch.float32)
     if q_std != 1.0:
         q.mul_(q_std)
     q = q.to(dtype)
-    k = torch.randn(B, H, N, d, generator=g, dtype=torch.float32).to(dtype)
-    v = torch.randn(B, H, N, d, generator=g, dtype=torch.float32).to(dtype)
+    k = torch.randn(B, Hk, N, d, generator=g, dtype=torch.float32).to(dtype)
+    v = torch.randn(B, Hk, N, d, generator=g, dtype=torch.float32).to(dtype)
     return q, k, v
 
 
 def workload_inputs(w: Workload):
-    return make_qkv(w.B, w.H, w.N, w.d, w.dtype, w.seed, w.q_std)
+    return make_qkv(w.B, w.H, w.N, w.d, w.dtype, w.seed, w.q_std, w.H_kv)
 
 
 def sample_units(w: Workload, n: int = 16, block: int = 128, seed: int | None = None):
@@ -135,5 +151,6 @@ def algorithmic_flops(w: Workload) -> float:
 
 def algorithmic_bytes(w: Workload) -> int:
     """Q, K, V read once and O (16-bit) plus LSE (fp32) written once."""
-    elems = w.B * w.H * w.N * w.d
-    return 4 * elems * 2 + w.B * w.H * w.N * 4
+    q_elems = w.B * w.H * w.N * w.d
+    kv_elems = w.B * w.kv_heads * w.N * w.d
+    return (2 * q_elems + 2 * kv_elems) * 2 + w.B * w.H * w.N * 4
