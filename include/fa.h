@@ -116,13 +116,14 @@ void fa_set_wait_budget_ns(uint64_t ns);
 int64_t fa_launch_count(void);
 
 /*
- * fa_test_arm_fault -- test hook for the failure path. The next fa_forward of
- * this process (only that one) makes CTA 0 skip the TMA load of K at K/V ring
- * position `kv_position` (counted from 0 over that CTA's work). Its MMA warp
- * then waits for data that never arrives: the wait runs out after the wait
- * budget, every role of the kernel gives up, drains its copies and MMAs, frees
- * its tensor memory and returns, and fa_sync_status reports FA_ERR_TIMEOUT.
- * The GPU context stays usable. A negative position disarms the hook.
+ * fa_test_arm_fault -- test hook for the failure path. The next launch of this
+ * process (only that one) makes every CTA skip the TMA load of K at its K/V
+ * ring position `kv_position` (counted from 0 over that CTA's work; position 0
+ * exists in every CTA that gets any work). Its MMA warp then waits for data
+ * that never arrives: the wait runs out after the wait budget, every role of
+ * the kernel gives up, drains its copies and MMAs, frees its tensor memory and
+ * returns, and fa_sync_status reports FA_ERR_TIMEOUT. The GPU context stays
+ * usable. A negative position disarms the hook.
  */
 void fa_test_arm_fault(int32_t kv_position);
 

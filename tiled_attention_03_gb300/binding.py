@@ -94,7 +94,7 @@ def fa_launch_count() -> int:
 
 
 def fa_test_arm_fault(kv_position: int) -> None:
-    """Test hook: the next fa_forward skips one K load in CTA 0 (see include/fa.h)."""
+    """Test hook: the next launch skips one K load in every CTA (see include/fa.h)."""
     load_library().fa_test_arm_fault(int(kv_position))
 
 

@@ -108,7 +108,7 @@ struct FwdParams {
     float scale_log2; // scale * log2(e)
     unsigned long long wait_budget_ns;
     unsigned int *status;  // [code, role, unit, block]
-    int fault_skip_k;      // test hook: CTA 0 skips the K load at this ring position (-1: none)
+    int fault_skip_k;      // test hook: every CTA skips the K load at this ring position (-1: none)
     unsigned int *sched;   // this launch's {next unit, finished CTAs} counters (zero at launch)
 };
 
@@ -433,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t ph = (kv_iter / kStages) & 1;
                     ok = mbar_wait_bounded(bar(kBarKEmpty + st), ph ^ 1, abort_flag, budget);
                     if (!ok) break;
-                    if (!(kv_iter == p.fault_skip_k && blockIdx.x == 0)) {
+                    if (kv_iter != p.fault_skip_k) {
                         mbar_arrive_expect_tx(bar(kBarKFull + st), L::kTileBytes);
                         for (int g = 0; g < kRegions; ++g)
                             tma_load_3d(sK + st * L::kTileBytes + g * kRegionBytes, &tmK,
