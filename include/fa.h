@@ -24,6 +24,7 @@
 #ifndef TILED_ATTENTION_FA_H
 #define TILED_ATTENTION_FA_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -92,6 +93,46 @@ fa_status fa_forward_gqa(const void *Q, const void *K, const void *V, void *O, f
                          int64_t B, int64_t H, int64_t H_kv, int64_t N, int64_t d, float scale,
                          fa_mask_mode mask_mode, int64_t window_left, int64_t window_right,
                          fa_dtype dtype, void *stream);
+
+/*
+ * fa_forward_splitkv -- attention with the keys of every head cut into
+ * `num_splits` contiguous chunks that are processed in parallel and merged
+ * (the split variant of FlashAttention for few queries and many keys, the
+ * "Flash Decoding" that "ai6s.net/6af30f4d40858c2d8819b6d5" §5 names). Each
+ * chunk yields its own normalised output and log-sum-exp; the merge is
+ * LSE = ln sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s.
+ *
+ * Q, O: contiguous B x H x Nq x d; K, V: contiguous B x H_kv x Nk x d; LSE:
+ * B x H x Nq float32. Nq and Nk may differ: query i stands at key position
+ * i + Nk - Nq (the queries are the last Nq positions, as when decoding), which
+ * is what the causal and window masks refer to; masks require Nq <= Nk.
+ * num_splits >= 1 (values above the number of 128-key tiles act as that
+ * number; fa_splitkv_default_splits suggests one). The result equals
+ * fa_forward_gqa's up to rounding.
+ *
+ * workspace: device memory owned by the caller, 16-byte aligned, at least
+ * fa_splitkv_workspace_bytes(B, H, Nq, d, num_splits) bytes, not overlapping
+ * the other buffers; its contents are scratch (fp32 partial results) and are
+ * overwritten. With num_splits = 1 it is not used (it may then be NULL).
+ * Two kernels are enqueued: the split attention and the merge.
+ * Errors as for fa_forward, plus FA_ERR_INVALID_ARG for a missing or short
+ * workspace, num_splits < 1, or a mask with Nq > Nk.
+ */
+fa_status fa_forward_splitkv(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                             int64_t B, int64_t H, int64_t H_kv, int64_t Nq, int64_t Nk,
+                             int64_t d, float scale, fa_mask_mode mask_mode,
+                             int64_t window_left, int64_t window_right, fa_dtype dtype,
+                             int64_t num_splits, void *workspace, size_t workspace_bytes,
+                             void *stream);
+
+/* Workspace bytes fa_forward_splitkv needs (0 for invalid sizes). */
+size_t fa_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t d,
+                                  int64_t num_splits);
+
+/* A split count that fills the current device: 1 when the query blocks alone
+ * give about one unit per SM, otherwise up to three units per SM with at
+ * least four 128-key tiles per split. */
+int64_t fa_splitkv_default_splits(int64_t B, int64_t H, int64_t Nq, int64_t Nk);
 
 /* Static, NUL-terminated description of a status code. Never NULL. */
 const char *fa_status_string(fa_status status);

@@ -42,10 +42,11 @@ def _load():
     global _lib
     if _lib is None:
         lib = ctypes.CDLL(build())
-        lib.oracle_attention_gqa.restype = ctypes.c_int
-        lib.oracle_attention_gqa.argtypes = [
+        lib.oracle_attention_ex.restype = ctypes.c_int
+        lib.oracle_attention_ex.argtypes = [
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
             ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_int64,
             ctypes.c_double, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
             ctypes.c_void_p, ctypes.c_int64,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int]
@@ -72,8 +73,9 @@ def _bits(t: torch.Tensor) -> np.ndarray:
 def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float,
               mask="none", window=(0, 0), units=None, nthreads: int | None = None,
               return_p: bool = False, online_bc: int = 0):
-    """fp64 attention over (B, H, N, d) 16-bit CPU tensors; K and V may have
-    fewer heads (B, Hk, N, d) with Hk dividing H (grouped-query attention).
+    """fp64 attention over 16-bit CPU tensors: Q (B, H, Nq, d), K and V
+    (B, Hk, Nk, d) with Hk dividing H (grouped-query attention when Hk < H).
+    Query i stands at key position i + Nk - Nq (the masks refer to that).
 
     ``units`` is a list of (b*H + h, row0, row1); by default every row of
     every head. Returns (O, LSE[, P]) as float64 numpy arrays with rows packed
@@ -82,13 +84,13 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float,
     of that size instead of the direct definition.
     """
     lib = _load()
-    B, H, N, d = q.shape
-    Hk = k.shape[1]
+    B, H, Nq, d = q.shape
+    Hk, N = k.shape[1], k.shape[2]
     assert k.shape == (B, Hk, N, d) and v.shape == k.shape
     assert q.dtype == k.dtype == v.dtype
     dt = FP16 if q.dtype == torch.float16 else BF16
     if units is None:
-        units = [(bh, 0, N) for bh in range(B * H)]
+        units = [(bh, 0, Nq) for bh in range(B * H)]
     u = np.ascontiguousarray(np.array(units, dtype=np.int64).reshape(-1, 3))
     rows = int((u[:, 2] - u[:, 1]).sum()) if len(u) else 0
     O = np.zeros((rows, d), dtype=np.float64)
@@ -97,8 +99,8 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float,
     qb, kb, vb = _bits(q), _bits(k), _bits(v)
     if nthreads is None:
         nthreads = len(os.sched_getaffinity(0))
-    rc = lib.oracle_attention_gqa(
-        qb.ctypes.data, kb.ctypes.data, vb.ctypes.data, dt, B, H, Hk, N, d,
+    rc = lib.oracle_attention_ex(
+        qb.ctypes.data, kb.ctypes.data, vb.ctypes.data, dt, B, H, Hk, Nq, N, d,
         float(scale), MASKS[mask], int(window[0]), int(window[1]),
         u.ctypes.data, len(u), O.ctypes.data, LSE.ctypes.data,
         P.ctypes.data if P is not None else None, int(online_bc), int(nthreads))

@@ -15,10 +15,11 @@
  *   O_i   = sum_j P_ij V[j,:]
  *   LSE_i = m_i + log sum_j exp(s_ij - m_i)
  *
- * Visibility: none -> every key 0..N-1; causal -> j <= i; window ->
- * i - wl <= j <= i + wr (both ends inclusive; the reading taken for the
- * (window_left, window_right) tuple of "ai6s.net/6a0ed07b662f9a54cb761aa2",
- * section "使用：ops-transformer 怎么调 FlashAttention").
+ * Visibility: none -> every key 0..Nk-1; causal -> j <= i + off; window ->
+ * i + off - wl <= j <= i + off + wr (both ends inclusive; the reading taken for
+ * the (window_left, window_right) tuple of "ai6s.net/6a0ed07b662f9a54cb761aa2",
+ * section "使用：ops-transformer 怎么调 FlashAttention"). off = Nk - Nq places
+ * the Nq queries at the last Nq key positions (off = 0 when Nq = Nk).
  *
  * A second entry point restates the online-softmax recurrence of
  * "ai6s.net/6af30f4d40858c2d8819b6d5" §2.3 (running max m, running sum l,
@@ -81,16 +82,17 @@ static double decode(uint16_t h, int dtype) {
     return dtype == ORACLE_BF16 ? oracle_bf16_to_double(h) : oracle_fp16_to_double(h);
 }
 
-static int is_visible(int64_t i, int64_t j, int mask, int64_t wl, int64_t wr) {
-    if (mask == ORACLE_MASK_CAUSAL) return j <= i;
-    if (mask == ORACLE_MASK_WINDOW) return j >= i - wl && j <= i + wr;
+/* pos = i + off: the key position of query i */
+static int is_visible(int64_t pos, int64_t j, int mask, int64_t wl, int64_t wr) {
+    if (mask == ORACLE_MASK_CAUSAL) return j <= pos;
+    if (mask == ORACLE_MASK_WINDOW) return j >= pos - wl && j <= pos + wr;
     return 1;
 }
 
 typedef struct {
     const uint16_t *Q, *K, *V;
     int dtype;
-    int64_t H, Hk, N, d; /* query heads, K/V heads */
+    int64_t H, Hk, Nq, N, d; /* query heads, K/V heads, query rows, keys (N), head dim */
     double scale;
     int mask;
     int64_t wl, wr;
@@ -119,7 +121,7 @@ static void unit_direct(const job_t *jb, const double *q, const double *k, const
         double m = -INFINITY;
         for (int64_t j = 0; j < N; ++j) {
             double s = -INFINITY;
-            if (is_visible(i, j, jb->mask, jb->wl, jb->wr)) {
+            if (is_visible(i + jb->N - jb->Nq, j, jb->mask, jb->wl, jb->wr)) {
                 double dot = 0.0;
                 for (int64_t c = 0; c < d; ++c) dot += q[i * d + c] * k[j * d + c];
                 s = jb->scale * dot;
@@ -163,7 +165,7 @@ static void unit_online(const job_t *jb, const double *q, const double *k, const
             double bmax = -INFINITY;
             for (int64_t j = j0; j < j1; ++j) {
                 double s = -INFINITY;
-                if (is_visible(i, j, jb->mask, jb->wl, jb->wr)) {
+                if (is_visible(i + jb->N - jb->Nq, j, jb->mask, jb->wl, jb->wr)) {
                     double dot = 0.0;
                     for (int64_t c = 0; c < d; ++c) dot += q[i * d + c] * k[j * d + c];
                     s = jb->scale * dot;
@@ -196,8 +198,8 @@ static void unit_online(const job_t *jb, const double *q, const double *k, const
 
 static void *worker(void *arg) {
     job_t *jb = (job_t *)arg;
-    const int64_t N = jb->N, d = jb->d;
-    double *q = (double *)malloc((size_t)(N * d) * sizeof(double));
+    const int64_t N = jb->N, Nq = jb->Nq, d = jb->d;
+    double *q = (double *)malloc((size_t)(Nq * d) * sizeof(double));
     double *k = (double *)malloc((size_t)(N * d) * sizeof(double));
     double *v = (double *)malloc((size_t)(N * d) * sizeof(double));
     int64_t maxrows = 0;
@@ -213,7 +215,7 @@ static void *worker(void *arg) {
             /* query head h of batch b reads K/V head h / (H / Hk) of batch b */
             const int64_t b = bh / jb->H, h = bh % jb->H;
             const int64_t bkv = b * jb->Hk + h / (jb->H / jb->Hk);
-            decode_slab(jb->Q + bh * N * d, jb->dtype, N * d, q);
+            decode_slab(jb->Q + bh * Nq * d, jb->dtype, Nq * d, q);
             decode_slab(jb->K + bkv * N * d, jb->dtype, N * d, k);
             decode_slab(jb->V + bkv * N * d, jb->dtype, N * d, v);
             cur_bh = bh;
@@ -230,20 +232,22 @@ static void *worker(void *arg) {
 }
 
 /*
- * Attention over a list of units (b*H+h, row0, row1). Q is B x H x N x d; K and
- * V are B x Hk x N x d, query head h reading K/V head h / (H / Hk) (Hk = H is
- * ordinary multi-head attention, Hk < H grouped-query attention). Output rows
+ * Attention over a list of units (b*H+h, row0, row1). Q is B x H x Nq x d; K
+ * and V are B x Hk x N x d, query head h reading K/V head h / (H / Hk) (Hk = H
+ * is ordinary multi-head attention, Hk < H grouped-query attention); query i
+ * stands at key position i + N - Nq. Output rows
  * are packed in unit order: O is sum(row1-row0) x d, LSE is sum(row1-row0), P
  * (optional, tiny cases only) is sum(row1-row0) x N. bc = 0 selects the direct
  * form, bc > 0 the online recurrence with key blocks of bc. nthreads <= 0 uses
  * all online cores. Returns 0, or -1 on a bad argument.
  */
-int oracle_attention_gqa(const uint16_t *Q, const uint16_t *K, const uint16_t *V, int dtype,
-                         int64_t B, int64_t H, int64_t Hk, int64_t N, int64_t d, double scale,
-                         int mask, int64_t wl, int64_t wr, const int64_t *units, int64_t n_units,
-                         double *O, double *LSE, double *P, int64_t bc, int nthreads) {
+int oracle_attention_ex(const uint16_t *Q, const uint16_t *K, const uint16_t *V, int dtype,
+                        int64_t B, int64_t H, int64_t Hk, int64_t Nq, int64_t N, int64_t d,
+                        double scale, int mask, int64_t wl, int64_t wr, const int64_t *units,
+                        int64_t n_units, double *O, double *LSE, double *P, int64_t bc,
+                        int nthreads) {
     if (!Q || !K || !V || !units || !O || !LSE) return -1;
-    if (B < 1 || H < 1 || N < 1 || d < 1 || n_units < 0 || bc < 0) return -1;
+    if (B < 1 || H < 1 || Nq < 1 || N < 1 || d < 1 || n_units < 0 || bc < 0) return -1;
     if (Hk < 1 || H % Hk != 0) return -1;
     if (dtype != ORACLE_FP16 && dtype != ORACLE_BF16) return -1;
     if (mask < ORACLE_MASK_NONE || mask > ORACLE_MASK_WINDOW) return -1;
@@ -253,7 +257,7 @@ int oracle_attention_gqa(const uint16_t *Q, const uint16_t *K, const uint16_t *V
     int64_t acc = 0;
     for (int64_t u = 0; u < n_units; ++u) {
         int64_t bh = units[3 * u], r0 = units[3 * u + 1], r1 = units[3 * u + 2];
-        if (bh < 0 || bh >= B * H || r0 < 0 || r1 > N || r0 > r1) { free(out_row); return -1; }
+        if (bh < 0 || bh >= B * H || r0 < 0 || r1 > Nq || r0 > r1) { free(out_row); return -1; }
         out_row[u] = acc;
         acc += r1 - r0;
     }
@@ -263,7 +267,7 @@ int oracle_attention_gqa(const uint16_t *Q, const uint16_t *K, const uint16_t *V
     job_t *jobs = (job_t *)calloc((size_t)nthreads, sizeof(job_t));
     pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
     for (int t = 0; t < nthreads; ++t) {
-        job_t j = {Q, K, V, dtype, H, Hk, N, d, scale, mask, wl, wr, units, out_row, n_units,
+        job_t j = {Q, K, V, dtype, H, Hk, Nq, N, d, scale, mask, wl, wr, units, out_row, n_units,
                    O, LSE, P, bc, nthreads, t};
         jobs[t] = j;
     }
@@ -272,6 +276,15 @@ int oracle_attention_gqa(const uint16_t *Q, const uint16_t *K, const uint16_t *V
     for (int t = 1; t < nthreads; ++t) pthread_join(th[t], NULL);
     free(jobs); free(th); free(out_row);
     return 0;
+}
+
+/* Grouped-query attention with Nq = N (queries at every key position). */
+int oracle_attention_gqa(const uint16_t *Q, const uint16_t *K, const uint16_t *V, int dtype,
+                         int64_t B, int64_t H, int64_t Hk, int64_t N, int64_t d, double scale,
+                         int mask, int64_t wl, int64_t wr, const int64_t *units, int64_t n_units,
+                         double *O, double *LSE, double *P, int64_t bc, int nthreads) {
+    return oracle_attention_ex(Q, K, V, dtype, B, H, Hk, N, N, d, scale, mask, wl, wr, units,
+                               n_units, O, LSE, P, bc, nthreads);
 }
 
 /* Multi-head attention: oracle_attention_gqa with one K/V head per query head. */

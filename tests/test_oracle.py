@@ -27,18 +27,20 @@ def _f64(t):
 
 
 def brute_force(q, k, v, scale, mask, wl=0, wr=0):
-    """Independent evaluation with numpy matmuls and scipy's softmax/logsumexp."""
-    B, H, N, d = q.shape
+    """Independent evaluation with numpy matmuls and scipy's softmax/logsumexp.
+    Query i of Nq stands at key position i + Nk - Nq."""
+    B, H, Nq, d = q.shape
+    N = k.shape[2]
     Q, K, V = _f64(q), _f64(k), _f64(v)
     S = scale * np.einsum("bhid,bhjd->bhij", Q, K)
-    i = np.arange(N)[:, None]
+    i = np.arange(Nq)[:, None] + (N - Nq)
     j = np.arange(N)[None, :]
     if mask == "causal":
         vis = j <= i
     elif mask == "window":
         vis = (j >= i - wl) & (j <= i + wr)
     else:
-        vis = np.ones((N, N), dtype=bool)
+        vis = np.ones((Nq, N), dtype=bool)
     S = np.where(vis, S, -np.inf)
     P = scipy.special.softmax(S, axis=-1)
     O = np.einsum("bhij,bhjd->bhid", P, V)
@@ -339,3 +341,38 @@ def test_gqa_rejects_non_dividing_heads():
     _, k, v = make_qkv(1, 2, 8, 4, torch.float16, seed=1)
     with pytest.raises(ValueError):
         oracle.attention(q, k, v, 1.0, "none")
+
+
+# --- fewer queries than keys (queries at the last positions) ---------------------
+
+@pytest.mark.parametrize("Nq,Nk", [(1, 1), (1, 50), (7, 50), (50, 50), (33, 200)])
+@pytest.mark.parametrize("mask,wl,wr", [("none", 0, 0), ("causal", 0, 0), ("window", 11, 3)])
+def test_rectangular_brute_force(Nq, Nk, mask, wl, wr):
+    q, _, _ = make_qkv(2, 2, Nq, 16, torch.float16, seed=Nq + Nk, q_std=2.0)
+    _, k, v = make_qkv(2, 2, Nk, 16, torch.float16, seed=Nq * 7 + Nk)
+    O, LSE = oracle.attention(q, k, v, 0.25, mask, (wl, wr))
+    Ob, Lb, _ = brute_force(q, k, v, 0.25, mask, wl, wr)
+    np.testing.assert_allclose(O, Ob, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(LSE, Lb, rtol=1e-13, atol=1e-12)
+
+
+@pytest.mark.parametrize("mask,wl,wr", [("none", 0, 0), ("causal", 0, 0), ("window", 20, 0)])
+def test_rectangular_equals_last_rows_of_square(mask, wl, wr):
+    # Queries placed at the last Nq positions compute exactly the last Nq rows of the
+    # square problem whose last rows are those queries.
+    Nk, Nq, d = 120, 9, 32
+    qs, k, v = make_qkv(1, 2, Nk, d, torch.bfloat16, seed=77)
+    q = qs[:, :, Nk - Nq:].contiguous()
+    Os, Ls = oracle.attention(qs, k, v, 0.2, mask, (wl, wr))
+    O, L = oracle.attention(q, k, v, 0.2, mask, (wl, wr))
+    rows = np.concatenate([bh * Nk + np.arange(Nk - Nq, Nk) for bh in range(2)])
+    np.testing.assert_array_equal(O, Os[rows])
+    np.testing.assert_array_equal(L, Ls[rows])
+
+
+def test_single_query_uniform_scores_is_mean_of_all_values():
+    _, k, v = make_qkv(1, 1, 300, 16, torch.float16, seed=8)
+    q = torch.zeros(1, 1, 1, 16, dtype=torch.float16)
+    O, L = oracle.attention(q, k, v, 0.5, "causal")  # the one query stands at the last key
+    np.testing.assert_allclose(O[0], _f64(v)[0, 0].mean(axis=0), rtol=0, atol=1e-13)
+    assert L[0] == pytest.approx(math.log(300), abs=1e-13)

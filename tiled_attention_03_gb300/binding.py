@@ -52,6 +52,16 @@ def load_library(path: str = LIB) -> ctypes.CDLL:
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
         ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
         ctypes.c_float, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]
+    lib.fa_forward_splitkv.restype = ctypes.c_int
+    lib.fa_forward_splitkv.argtypes = [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+        ctypes.c_int64, ctypes.c_float, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+        ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    lib.fa_splitkv_workspace_bytes.restype = ctypes.c_size_t
+    lib.fa_splitkv_workspace_bytes.argtypes = [ctypes.c_int64] * 5
+    lib.fa_splitkv_default_splits.restype = ctypes.c_int64
+    lib.fa_splitkv_default_splits.argtypes = [ctypes.c_int64] * 4
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_status_string.argtypes = [ctypes.c_int]
     lib.fa_sync_status.restype = ctypes.c_int
@@ -106,7 +116,7 @@ def _stream_handle(stream) -> int | None:
     return int(stream)
 
 
-def _check(q, k, v, o, lse):
+def _check(q, k, v, o, lse, same_n=True):
     for t in (q, k, v, o, lse):
         if not t.is_cuda or not t.is_contiguous():
             raise FaError(FA_ERR_INVALID_ARG)
@@ -116,8 +126,8 @@ def _check(q, k, v, o, lse):
     if q.dim() != 4 or k.dim() != 4:
         raise FaError(FA_ERR_INVALID_ARG)
     B, H, N, d = q.shape
-    if k.shape[0] != B or k.shape[2:] != q.shape[2:] or v.shape != k.shape or \
-            o.shape != q.shape or lse.shape != (B, H, N):
+    if k.shape[0] != B or k.shape[3] != d or (same_n and k.shape[2] != N) or \
+            v.shape != k.shape or o.shape != q.shape or lse.shape != (B, H, N):
         raise FaError(FA_ERR_INVALID_ARG)
 
 
@@ -181,3 +191,39 @@ def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | No
         torch.cuda.current_stream().synchronize()
         return o_h, lse_h
     return o, lse
+
+
+def fa_splitkv_workspace_bytes(B: int, H: int, Nq: int, d: int, num_splits: int) -> int:
+    return load_library().fa_splitkv_workspace_bytes(B, H, Nq, d, num_splits)
+
+
+def fa_splitkv_default_splits(B: int, H: int, Nq: int, Nk: int) -> int:
+    return load_library().fa_splitkv_default_splits(B, H, Nq, Nk)
+
+
+def fa_forward_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                       lse: torch.Tensor, scale: float, mask_mode=FA_MASK_NONE,
+                       window_left: int = 0, window_right: int = 0, num_splits: int = 0,
+                       workspace: torch.Tensor | None = None, stream=None) -> None:
+    """Enqueue fa_forward_splitkv: q, o (B, H, Nq, d); k, v (B, H_kv, Nk, d);
+    lse (B, H, Nq). num_splits = 0 takes fa_splitkv_default_splits. Without a
+    workspace tensor one is taken from PyTorch's caching allocator."""
+    lib = load_library()
+    _check(q, k, v, o, lse, same_n=False)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if num_splits <= 0:
+        num_splits = fa_splitkv_default_splits(B, H, Nq, Nk)
+    need = fa_splitkv_workspace_bytes(B, H, Nq, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise FaError(FA_ERR_INVALID_ARG)
+    rc = lib.fa_forward_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                lse.data_ptr(), B, H, k.shape[1], Nq, Nk, d, float(scale),
+                                _MASKS[mask_mode], int(window_left), int(window_right),
+                                _DTYPES[q.dtype], int(num_splits), workspace.data_ptr(),
+                                workspace.numel() * workspace.element_size(),
+                                _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc)

@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "fa.h"
+#include "fa_combine.cuh"
 #include "fa_fwd_kernel.cuh"
 
 namespace {
@@ -161,6 +162,201 @@ cudaError_t launch(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap
     return cudaGetLastError();
 }
 
+
+// ---- one forward launch (plus the split merge when the keys are split)
+struct Call {
+    const void *Q, *K, *V;
+    void *O;
+    float *LSE;
+    int64_t B, H, H_kv, Nq, Nk, d;
+    float scale;
+    fa_mask_mode mask_mode;
+    int64_t window_left, window_right;
+    fa_dtype dtype;
+    int64_t num_splits;
+    void *workspace;
+    size_t workspace_bytes;
+    void *stream;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Workspace of a key-split call: partial LSEs, then partial outputs, fp32.
+size_t splitkv_bytes(int64_t rows, int64_t d, int64_t splits) {
+    return align256(static_cast<size_t>(splits) * rows * sizeof(float)) +
+           static_cast<size_t>(splits) * rows * d * sizeof(float);
+}
+
+// Enough splits for about three units per SM, each split keeping >= 4 K/V tiles.
+int64_t default_splits(int64_t BH, int64_t Nq, int64_t Nk, int sms) {
+    const int64_t units = BH * ((Nq + fa::kUnitRows - 1) / fa::kUnitRows);
+    const int64_t tiles = (Nk + fa::kBN - 1) / fa::kBN;
+    if (units >= sms) return 1;
+    int64_t s = (3 * sms + units - 1) / units;
+    const int64_t cap = tiles / 4 > 1 ? tiles / 4 : 1;
+    if (s > cap) s = cap;
+    if (s > 256) s = 256;
+    return s < 1 ? 1 : s;
+}
+
+template <int D, bool BF16>
+cudaError_t launch_combine(const fa::CombineParams &c, cudaStream_t stream) {
+    const int64_t rows = static_cast<int64_t>(c.BH) * c.Nq;
+    const int64_t blocks = (rows + fa::kCombineWarps - 1) / fa::kCombineWarps;
+    fa::fa_combine_kernel<D, BF16><<<static_cast<unsigned>(blocks), fa::kCombineWarps * 32, 0,
+                                     stream>>>(c);
+    return cudaGetLastError();
+}
+
+fa_status run_forward(const Call &c) {
+    const void *Q = c.Q, *K = c.K, *V = c.V;
+    void *O = c.O;
+    float *LSE = c.LSE;
+    const int64_t B = c.B, H = c.H, H_kv = c.H_kv, Nq = c.Nq, Nk = c.Nk, d = c.d;
+    // ---- host-side checks: nothing is enqueued on failure
+    if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1) return FA_ERR_INVALID_ARG;
+    if (H_kv < 1 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
+    if (c.dtype != FA_DTYPE_FP16 && c.dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
+    const fa_mask_mode mask_mode = c.mask_mode;
+    if (mask_mode != FA_MASK_NONE && mask_mode != FA_MASK_CAUSAL && mask_mode != FA_MASK_WINDOW)
+        return FA_ERR_INVALID_ARG;
+    if (mask_mode == FA_MASK_WINDOW && (c.window_left < 0 || c.window_right < 0))
+        return FA_ERR_INVALID_ARG;
+    // Masks place the queries at the last Nq key positions; more queries than keys
+    // would leave rows with no visible key.
+    if (mask_mode != FA_MASK_NONE && Nq > Nk) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(c.scale) || !(c.scale > 0.f)) return FA_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
+        return FA_ERR_INVALID_ARG;
+    if (c.num_splits < 1) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    // Size limits of this implementation: 32-bit row indices and grid.
+    if (Nq > (int64_t{1} << 29) || Nk > (int64_t{1} << 29) || B * H > (int64_t{1} << 31))
+        return FA_ERR_UNSUPPORTED;
+    const int64_t BH = B * H;
+    const int64_t BHkv = B * H_kv;
+    const int64_t n_qb = (Nq + fa::kUnitRows - 1) / fa::kUnitRows;
+    const int64_t kv_tiles = (Nk + fa::kBN - 1) / fa::kBN;
+    const int64_t splits = c.num_splits < kv_tiles ? c.num_splits : kv_tiles;
+    const int64_t split_tiles = (kv_tiles + splits - 1) / splits;
+    const int64_t n_splits = (kv_tiles + split_tiles - 1) / split_tiles;
+    const int64_t n_units = BH * n_qb * n_splits;
+    if (n_units > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+    const bool split = n_splits > 1;
+    const size_t tbytes = static_cast<size_t>(BH) * Nq * d * 2;
+    const size_t lbytes = static_cast<size_t>(BH) * Nq * sizeof(float);
+    const size_t kvbytes = static_cast<size_t>(BHkv) * Nk * d * 2;
+    if (overlaps(O, tbytes, Q, tbytes) || overlaps(O, tbytes, K, kvbytes) ||
+        overlaps(O, tbytes, V, kvbytes) || overlaps(O, tbytes, LSE, lbytes) ||
+        overlaps(LSE, lbytes, Q, tbytes) || overlaps(LSE, lbytes, K, kvbytes) ||
+        overlaps(LSE, lbytes, V, kvbytes))
+        return FA_ERR_INVALID_ARG;
+    const size_t wbytes = split ? splitkv_bytes(BH * Nq, d, n_splits) : 0;
+    if (split) {
+        if (c.workspace == nullptr || c.workspace_bytes < wbytes) return FA_ERR_INVALID_ARG;
+        const void *W = c.workspace;
+        if (overlaps(W, wbytes, Q, tbytes) || overlaps(W, wbytes, K, kvbytes) ||
+            overlaps(W, wbytes, V, kvbytes) || overlaps(W, wbytes, O, tbytes) ||
+            overlaps(W, wbytes, LSE, lbytes))
+            return FA_ERR_INVALID_ARG;
+    }
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+    }
+    DeviceState *ds = device_state(dev);
+    if (ds == nullptr) return FA_ERR_UNSUPPORTED;
+    if (ds->init_err != cudaSuccess) return FA_ERR_CUDA;
+    if (!(ds->cc_major == 10 && ds->cc_minor == 3)) return FA_ERR_UNSUPPORTED;
+    if (!on_device(Q, dev) || !on_device(K, dev) || !on_device(V, dev) || !on_device(O, dev) ||
+        !on_device(LSE, dev) || (split && !on_device(c.workspace, dev)))
+        return FA_ERR_INVALID_ARG;
+
+    const bool bf16 = c.dtype == FA_DTYPE_BF16;
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, Q, bf16, BH, Nq, d) || !make_map(&mk, K, bf16, BHkv, Nk, d) ||
+        !make_map(&mv, V, bf16, BHkv, Nk, d))
+        return FA_ERR_CUDA;
+
+    fa::FwdParams p{};
+    p.O = O;
+    p.LSE = LSE;
+    float *part_LSE = nullptr, *part_O = nullptr;
+    if (split) {
+        part_LSE = static_cast<float *>(c.workspace);
+        part_O = reinterpret_cast<float *>(static_cast<uint8_t *>(c.workspace) +
+                                           align256(static_cast<size_t>(n_splits) * BH * Nq *
+                                                    sizeof(float)));
+    }
+    p.part_O = part_O;
+    p.part_LSE = part_LSE;
+    p.Nq = static_cast<int>(Nq);
+    p.Nk = static_cast<int>(Nk);
+    p.q_off = static_cast<int>(Nk - Nq);
+    p.H = static_cast<int>(H);
+    p.BH = static_cast<int>(BH);
+    p.kv_group = static_cast<int>(H / H_kv);
+    p.n_units = static_cast<int>(n_units);
+    p.n_qb = static_cast<int>(n_qb);
+    p.n_splits = static_cast<int>(n_splits);
+    p.split_tiles = static_cast<int>(split_tiles);
+    // Visible keys of query i: [i + q_off - wl, i + q_off + wr]; "all keys" is a window
+    // wider than any offset (values are clamped so the sums stay in 32 bits).
+    const int64_t all = Nq + Nk;
+    int64_t wl = all, wr = all;
+    if (mask_mode == FA_MASK_CAUSAL) wr = 0;
+    if (mask_mode == FA_MASK_WINDOW) {
+        wl = c.window_left < all ? c.window_left : all;
+        wr = c.window_right < all ? c.window_right : all;
+    }
+    p.wl = static_cast<int>(wl);
+    p.wr = static_cast<int>(wr);
+    p.heavy_first = wr < Nk ? 1 : 0;
+    p.scale_log2 = static_cast<float>(static_cast<double>(c.scale) * 1.4426950408889634074);
+    p.wait_budget_ns = wait_budget();
+    p.status = ds->status;
+    p.fault_skip_k = g_fault_pos.exchange(-1);
+    p.sched = ds->sched + 2 * (g_sched_next.fetch_add(1) % kSchedSlots);
+
+    // Persistent grid: one CTA per SM (each holds the SM's whole tensor memory).
+    const int64_t blocks = n_units < ds->sm_count ? n_units : ds->sm_count;
+    cudaStream_t st = static_cast<cudaStream_t>(c.stream);
+    cudaError_t e;
+    if (d == 64)
+        e = bf16 ? launch<64, true>(mq, mk, mv, p, blocks, st)
+                 : launch<64, false>(mq, mk, mv, p, blocks, st);
+    else
+        e = bf16 ? launch<128, true>(mq, mk, mv, p, blocks, st)
+                 : launch<128, false>(mq, mk, mv, p, blocks, st);
+    if (e != cudaSuccess) return FA_ERR_CUDA;
+    g_launches.fetch_add(1);
+    if (split) {
+        fa::CombineParams cp{};
+        cp.part_O = part_O;
+        cp.part_LSE = part_LSE;
+        cp.O = O;
+        cp.LSE = LSE;
+        cp.BH = p.BH;
+        cp.Nq = p.Nq;
+        cp.Nk = p.Nk;
+        cp.q_off = p.q_off;
+        cp.wl = p.wl;
+        cp.wr = p.wr;
+        cp.n_splits = p.n_splits;
+        cp.split_keys = p.split_tiles * fa::kBN;
+        if (d == 64)
+            e = bf16 ? launch_combine<64, true>(cp, st) : launch_combine<64, false>(cp, st);
+        else
+            e = bf16 ? launch_combine<128, true>(cp, st) : launch_combine<128, false>(cp, st);
+        if (e != cudaSuccess) return FA_ERR_CUDA;
+        g_launches.fetch_add(1);
+    }
+    return FA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -186,90 +382,9 @@ fa_status fa_forward_gqa(const void *Q, const void *K, const void *V, void *O, f
                          int64_t B, int64_t H, int64_t H_kv, int64_t N, int64_t d, float scale,
                          fa_mask_mode mask_mode, int64_t window_left, int64_t window_right,
                          fa_dtype dtype, void *stream) {
-    // ---- host-side checks: nothing is enqueued on failure
-    if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARG;
-    if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
-    if (H_kv < 1 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
-    if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
-    if (mask_mode != FA_MASK_NONE && mask_mode != FA_MASK_CAUSAL && mask_mode != FA_MASK_WINDOW)
-        return FA_ERR_INVALID_ARG;
-    if (mask_mode == FA_MASK_WINDOW && (window_left < 0 || window_right < 0))
-        return FA_ERR_INVALID_ARG;
-    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
-    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
-        return FA_ERR_INVALID_ARG;
-    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-    // Size limits of this implementation: 32-bit row indices and grid.
-    if (N > (int64_t{1} << 30) || B * H > (int64_t{1} << 31)) return FA_ERR_UNSUPPORTED;
-    const int64_t BH = B * H;
-    const int64_t n_qb = (N + fa::kUnitRows - 1) / fa::kUnitRows;
-    const int64_t n_units = BH * n_qb;
-    if (n_units > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
-    const int64_t BHkv = B * H_kv;
-    const size_t elems = static_cast<size_t>(BH) * static_cast<size_t>(N) * static_cast<size_t>(d);
-    const size_t tbytes = elems * 2, lbytes = static_cast<size_t>(BH) * N * sizeof(float);
-    const size_t kvbytes = static_cast<size_t>(BHkv) * N * d * 2;
-    if (overlaps(O, tbytes, Q, tbytes) || overlaps(O, tbytes, K, kvbytes) ||
-        overlaps(O, tbytes, V, kvbytes) || overlaps(O, tbytes, LSE, lbytes) ||
-        overlaps(LSE, lbytes, Q, tbytes) || overlaps(LSE, lbytes, K, kvbytes) ||
-        overlaps(LSE, lbytes, V, kvbytes))
-        return FA_ERR_INVALID_ARG;
-
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        cudaGetLastError();
-        return FA_ERR_CUDA;
-    }
-    DeviceState *ds = device_state(dev);
-    if (ds == nullptr) return FA_ERR_UNSUPPORTED;
-    if (ds->init_err != cudaSuccess) return FA_ERR_CUDA;
-    if (!(ds->cc_major == 10 && ds->cc_minor == 3)) return FA_ERR_UNSUPPORTED;
-    if (!on_device(Q, dev) || !on_device(K, dev) || !on_device(V, dev) || !on_device(O, dev) ||
-        !on_device(LSE, dev))
-        return FA_ERR_INVALID_ARG;
-
-    const bool bf16 = dtype == FA_DTYPE_BF16;
-    CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, Q, bf16, BH, N, d) || !make_map(&mk, K, bf16, BHkv, N, d) ||
-        !make_map(&mv, V, bf16, BHkv, N, d))
-        return FA_ERR_CUDA;
-
-    fa::FwdParams p{};
-    p.O = O;
-    p.LSE = LSE;
-    p.N = static_cast<int>(N);
-    p.H = static_cast<int>(H);
-    p.kv_group = static_cast<int>(H / H_kv);
-    p.n_units = static_cast<int>(n_units);
-    p.n_qb = static_cast<int>(n_qb);
-    int64_t wl = N, wr = N;
-    if (mask_mode == FA_MASK_CAUSAL) wr = 0;
-    if (mask_mode == FA_MASK_WINDOW) {
-        wl = window_left < N ? window_left : N;
-        wr = window_right < N ? window_right : N;
-    }
-    p.wl = static_cast<int>(wl);
-    p.wr = static_cast<int>(wr);
-    p.heavy_first = wr < N ? 1 : 0;
-    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
-    p.wait_budget_ns = wait_budget();
-    p.status = ds->status;
-    p.fault_skip_k = g_fault_pos.exchange(-1);
-    p.sched = ds->sched + 2 * (g_sched_next.fetch_add(1) % kSchedSlots);
-
-    // Persistent grid: one CTA per SM (each holds the SM's whole tensor memory).
-    const int64_t blocks = n_units < ds->sm_count ? n_units : ds->sm_count;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    if (d == 64)
-        e = bf16 ? launch<64, true>(mq, mk, mv, p, blocks, st)
-                 : launch<64, false>(mq, mk, mv, p, blocks, st);
-    else
-        e = bf16 ? launch<128, true>(mq, mk, mv, p, blocks, st)
-                 : launch<128, false>(mq, mk, mv, p, blocks, st);
-    if (e != cudaSuccess) return FA_ERR_CUDA;
-    g_launches.fetch_add(1);
-    return FA_OK;
+    Call c{Q, K, V, O, LSE, B, H, H_kv, N, N, d, scale, mask_mode, window_left, window_right,
+           dtype, 1, nullptr, 0, stream};
+    return run_forward(c);
 }
 
 fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float *LSE, int64_t B,
@@ -277,6 +392,34 @@ fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float
                      int64_t window_left, int64_t window_right, fa_dtype dtype, void *stream) {
     return fa_forward_gqa(Q, K, V, O, LSE, B, H, H, N, d, scale, mask_mode, window_left,
                           window_right, dtype, stream);
+}
+
+size_t fa_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t d,
+                                  int64_t num_splits) {
+    if (B < 1 || H < 1 || Nq < 1 || d < 1 || num_splits < 1) return 0;
+    return splitkv_bytes(B * H * Nq, d, num_splits);
+}
+
+int64_t fa_splitkv_default_splits(int64_t B, int64_t H, int64_t Nq, int64_t Nk) {
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return 1;
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    else
+        cudaGetLastError();
+    return default_splits(B * H, Nq, Nk, sms);
+}
+
+fa_status fa_forward_splitkv(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                             int64_t B, int64_t H, int64_t H_kv, int64_t Nq, int64_t Nk,
+                             int64_t d, float scale, fa_mask_mode mask_mode,
+                             int64_t window_left, int64_t window_right, fa_dtype dtype,
+                             int64_t num_splits, void *workspace, size_t workspace_bytes,
+                             void *stream) {
+    if (workspace != nullptr && !aligned16(workspace)) return FA_ERR_INVALID_ARG;
+    Call c{Q, K, V, O, LSE, B, H, H_kv, Nq, Nk, d, scale, mask_mode, window_left, window_right,
+           dtype, num_splits, workspace, workspace_bytes, stream};
+    return run_forward(c);
 }
 
 fa_status fa_sync_status(void *stream) {

@@ -98,13 +98,19 @@ enum : int { kRoleSoftmax = 1, kRoleTma = 2, kRoleMma = 3 };
 struct FwdParams {
     void *O;
     float *LSE;
-    int N;            // sequence length
+    float *part_O;    // split mode: fp32 partial outputs [split][b*H+h][Nq][d]; null: write O, LSE
+    float *part_LSE;  // split mode: partial log-sum-exps [split][b*H+h][Nq]
+    int Nq, Nk;       // query rows and keys per head
+    int q_off;        // query i sits at key position i + q_off (Nk - Nq: the last Nq positions)
     int H;            // query heads
+    int BH;           // B * H
     int kv_group;     // query heads per K/V head (H / H_kv; 1 = one K/V head per query head)
-    int n_units;      // (b*H + h, 256-row block) work units
-    int n_qb;         // 256-row blocks per head: ceil(N / 256)
+    int n_units;      // (b*H + h, 256-row block, key split) work units
+    int n_qb;         // 256-row blocks per head: ceil(Nq / 256)
+    int n_splits;     // key splits per row block (1: no split)
+    int split_tiles;  // K/V tiles per key split
     int heavy_first;  // 1: within a head, visit row blocks from the last (most keys) to the first
-    int wl, wr;       // key j visible to query i iff i - wl <= j <= i + wr (clamped to [0, N])
+    int wl, wr;       // key j visible to query i iff i + q_off - wl <= j <= i + q_off + wr
     float scale_log2; // scale * log2(e)
     unsigned long long wait_budget_ns;
     unsigned int *status;  // [code, role, unit, block]
@@ -153,37 +159,57 @@ enum : int {
 };
 
 // A work unit: rows [r0, r0 + 256) of query head bh (= b * H + h), whose keys and
-// values are those of K/V head bkv (= b * H_kv + h / kv_group); Q tile t covers rows
-// [r0 + 128 t, r0 + 128 t + 128) and needs K/V tiles [a[t], b[t]] (empty when a > b).
+// values are those of K/V head bkv (= b * H_kv + h / kv_group), restricted to the
+// K/V tiles of key split `split`; Q tile t covers rows [r0 + 128 t, r0 + 128 t + 128)
+// and needs K/V tiles [a[t], b[t]] (empty when a > b); [j0, j1] is their union.
 struct Unit {
-    int bh, bkv, r0;
+    int bh, bkv, r0, split;
     int a[kQTiles], b[kQTiles];
+    int j0, j1;
 };
 
 __device__ __forceinline__ Unit decode_unit(int u, const FwdParams &p) {
     Unit U;
-    U.bh = u / p.n_qb;
+    const int per_head = p.n_qb * p.n_splits;
+    U.bh = u / per_head;
+    const int rem = u - U.bh * per_head;
+    int qb = rem / p.n_splits;
+    U.split = rem - qb * p.n_splits;
     {
         const int b = U.bh / p.H, h = U.bh - b * p.H;
         U.bkv = b * (p.H / p.kv_group) + h / p.kv_group;
     }
-    int qb = u % p.n_qb;
     if (p.heavy_first) qb = p.n_qb - 1 - qb;
     U.r0 = qb * kUnitRows;
+    const int s_lo = U.split * p.split_tiles;
+    const int s_hi = s_lo + p.split_tiles - 1;
+    U.j0 = 0x7fffffff;
+    U.j1 = -1;
 #pragma unroll
     for (int t = 0; t < kQTiles; ++t) {
         const int rt0 = U.r0 + t * kBM;
-        if (rt0 >= p.N) {
-            U.a[t] = 1;
-            U.b[t] = 0;
-        } else {
-            const int rl = min(rt0 + kBM, p.N) - 1;
-            U.a[t] = max(0, rt0 - p.wl) / kBN;
-            U.b[t] = min(p.N - 1, rl + p.wr) / kBN;
+        U.a[t] = 1;
+        U.b[t] = 0;
+        if (rt0 < p.Nq) {
+            const int rl = min(rt0 + kBM, p.Nq) - 1;
+            const int lo_key = rt0 + p.q_off - p.wl;  // first key any row of the tile sees
+            const int hi_key = rl + p.q_off + p.wr;   // last key any row of the tile sees
+            if (hi_key >= 0 && lo_key <= p.Nk - 1) {
+                const int a = max(max(0, lo_key) / kBN, s_lo);
+                const int b = min(min(p.Nk - 1, hi_key) / kBN, s_hi);
+                if (a <= b) {
+                    U.a[t] = a;
+                    U.b[t] = b;
+                    U.j0 = min(U.j0, a);
+                    U.j1 = max(U.j1, b);
+                }
+            }
         }
     }
     return U;
 }
+
+__device__ __forceinline__ bool unit_empty(const Unit &U) { return U.j1 < U.j0; }
 
 __device__ __forceinline__ void record_timeout(const FwdParams &p, volatile int *abort_flag,
                                                int role, int unit) {
@@ -393,8 +419,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = mbar_wait_bounded(bar(kBarUnitEmpty + slot), ((k / kUnitSlots) & 1) ^ 1,
                                        abort_flag, budget);
                 if (!ok) return -1;
-                const unsigned next = atomicAdd(p.sched, 1u);
-                const int v = next < static_cast<unsigned>(p.n_units) ? static_cast<int>(next) : -1;
+                // Units with no visible key in their split (possible only with key
+                // splits) are skipped here, so every published unit has work.
+                int v = -1;
+                while (true) {
+                    const unsigned next = atomicAdd(p.sched, 1u);
+                    if (next >= static_cast<unsigned>(p.n_units)) break;
+                    if (!unit_empty(decode_unit(static_cast<int>(next), p))) {
+                        v = static_cast<int>(next);
+                        break;
+                    }
+                }
                 unit_ring[slot] = v;
                 mbar_arrive(bar(kBarUnitFull + slot));
                 return v;
@@ -420,10 +455,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++q_loads;
                 int u_next = -1;
                 bool claimed = false;
-                const int j1 = U.a[1] <= U.b[1] ? U.b[1] : U.b[0];
-                for (int j = U.a[0]; ok && j <= j1; ++j, ++kv_iter) {
+                const int j1 = U.j1;
+                for (int j = U.j0; ok && j <= j1; ++j, ++kv_iter) {
                     // claim the next unit after the first two K loads (or at the last one)
-                    if (!claimed && (j == U.a[0] + 2 || j == j1)) {
+                    if (!claimed && (j == U.j0 + 2 || j == j1)) {
                         claimed = true;
                         u_next = publish(unit_iter + 1);
                         if (!ok) break;
@@ -468,8 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(bar(kBarUnitEmpty + slot));
                 if (u < 0) break;
                 const Unit U = decode_unit(u, p);
-                const int j1 = U.a[1] <= U.b[1] ? U.b[1] : U.b[0];
-                for (int j = U.a[0]; ok && j <= j1; ++j, ++kv_iter) {
+                for (int j = U.j0; ok && j <= U.j1; ++j, ++kv_iter) {
                     const int st = kv_iter % kStages;
                     ok = mbar_wait_bounded(bar(kBarVEmpty + st), ((kv_iter / kStages) & 1) ^ 1,
                                            abort_flag, budget);
@@ -562,8 +596,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (u < 0) break;
             const Unit U = decode_unit(u, p);
             for (int t = 0; t < kQTiles && ok; ++t) ok = wait(kBarQFull + t, unit_iter & 1);
-            const int j0 = U.a[0];
-            const int j1 = U.a[1] <= U.b[1] ? U.b[1] : U.b[0];
+            const int j0 = U.j0;
+            const int j1 = U.j1;
             auto in = [&U](int t, int j) { return j >= U.a[t] && j <= U.b[t]; };
             for (int j = j0; ok && j <= j1 + 1; ++j) {
                 const int pos = kv_base + (j - j0);  // ring position of K_j / V_j
@@ -630,12 +664,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Unit U = decode_unit(u, p);
             if (U.a[t] > U.b[t]) continue;
             const int rt0 = U.r0 + t * kBM;
-            const int rl = min(rt0 + kBM, p.N) - 1;
+            const int rl = min(rt0 + kBM, p.Nq) - 1;
             const int i = rt0 + row;  // query index
-            const int lo_i = max(0, i - p.wl);
-            const int hi_i = min(p.N - 1, i + p.wr);
-            const int lo_last = max(0, rl - p.wl);
-            const int hi_first = min(p.N - 1, rt0 + p.wr);
+            // visible keys of row i: [i + q_off - wl, i + q_off + wr] within [0, Nk)
+            const int lo_i = max(0, i + p.q_off - p.wl);
+            const int hi_i = min(p.Nk - 1, i + p.q_off + p.wr);
+            const int lo_last = max(0, rl + p.q_off - p.wl);
+            const int hi_first = min(p.Nk - 1, rt0 + p.q_off + p.wr);
             float m = -INFINITY;  // reference max of the row, in log2 units of the scaled logits
             float l = 0.f;        // running sum of 2^(logit - m)
             for (int j = U.a[t]; j <= U.b[t]; ++j, ++s_count) {
@@ -681,29 +716,51 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
-            const bool store = i < p.N;
-            uint8_t *orow = reinterpret_cast<uint8_t *>(p.O) +
-                            (static_cast<size_t>(U.bh) * p.N + (store ? i : 0)) * (D * 2);
+            const bool store = i < p.Nq;
+            const float lse = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+            if (p.part_O == nullptr) {
+                // O / l rounded to 16 bit, and LSE
+                uint8_t *orow = reinterpret_cast<uint8_t *>(p.O) +
+                                (static_cast<size_t>(U.bh) * p.Nq + (store ? i : 0)) * (D * 2);
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                tmem_ld32(tO + c * 32, o);
-                tmem_ld_wait(o);
-                uint32_t pk[16];
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + c * 32, o);
+                    tmem_ld_wait(o);
+                    uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    pk[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l,
-                                        __uint_as_float(o[2 * e + 1]) * inv_l);
-                if (store) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 64);
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l,
+                                            __uint_as_float(o[2 * e + 1]) * inv_l);
+                    if (store) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 64);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                        for (int q = 0; q < 4; ++q)
+                            dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                    }
                 }
+                if (store) p.LSE[static_cast<size_t>(U.bh) * p.Nq + i] = lse;
+            } else {
+                // key split: the split's own O / l in fp32 and its LSE, merged later
+                const size_t prow = (static_cast<size_t>(U.split) * p.BH + U.bh) * p.Nq + (store ? i : 0);
+                float *orow = p.part_O + prow * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + c * 32, o);
+                    tmem_ld_wait(o);
+                    if (store) {
+                        float4 *dst = reinterpret_cast<float4 *>(orow + c * 32);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            dst[q] = make_float4(__uint_as_float(o[4 * q]) * inv_l,
+                                                 __uint_as_float(o[4 * q + 1]) * inv_l,
+                                                 __uint_as_float(o[4 * q + 2]) * inv_l,
+                                                 __uint_as_float(o[4 * q + 3]) * inv_l);
+                    }
+                }
+                if (store) p.part_LSE[prow] = lse;
             }
-            if (store)
-                p.LSE[static_cast<size_t>(U.bh) * p.N + i] =
-                    l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
             tc_fence_before();
             mbar_arrive(bar(kBarOFree + t));
         }
