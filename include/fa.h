@@ -134,6 +134,36 @@ size_t fa_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t d,
  * least four 128-key tiles per split. */
 int64_t fa_splitkv_default_splits(int64_t B, int64_t H, int64_t Nq, int64_t Nk);
 
+/*
+ * fa_forward_splitkv_static -- fa_forward_splitkv without a caller workspace,
+ * for callers that cannot allocate device memory: runtimes that reserve all of
+ * their device memory up front and forbid later allocations (to rule out
+ * fragmentation or an out-of-memory failure in the middle of serving), and
+ * plug-in hosts that give the library no allocator. The pages have no
+ * counterpart: this is an interface choice of this library.
+ *
+ * The scratch is one fixed array of FA_SPLITKV_STATIC_SCRATCH_BYTES bytes in
+ * device memory, part of the library: every GPU that loads the library holds
+ * it until the process exits, and this call allocates nothing. Requests whose
+ * fa_splitkv_workspace_bytes(B, H, Nq, d, num_splits) exceeds that size are
+ * rejected with FA_ERR_UNSUPPORTED before anything is enqueued (use fewer
+ * splits, or fa_forward_splitkv with a workspace). num_splits >= 1.
+ *
+ * All calls on a device share the one array and leave their partial results
+ * in it; nothing in it needs to start at zero. Calls whose kernels overlap on
+ * the GPU (for example on two streams at once) race on the array: order them
+ * on one stream, or synchronise between them. The first call on each device
+ * looks up the array's device address (with that device current); make that
+ * first call before any stream capture. Everything else -- arguments, layout,
+ * masks, results and errors -- is as for fa_forward_splitkv.
+ */
+#define FA_SPLITKV_STATIC_SCRATCH_BYTES (16u << 20)
+fa_status fa_forward_splitkv_static(const void *Q, const void *K, const void *V, void *O,
+                                    float *LSE, int64_t B, int64_t H, int64_t H_kv, int64_t Nq,
+                                    int64_t Nk, int64_t d, float scale, fa_mask_mode mask_mode,
+                                    int64_t window_left, int64_t window_right, fa_dtype dtype,
+                                    int64_t num_splits, void *stream);
+
 /* Static, NUL-terminated description of a status code. Never NULL. */
 const char *fa_status_string(fa_status status);
 

@@ -58,6 +58,12 @@ def load_library(path: str = LIB) -> ctypes.CDLL:
         ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
         ctypes.c_int64, ctypes.c_float, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
         ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    lib.fa_forward_splitkv_static.restype = ctypes.c_int
+    lib.fa_forward_splitkv_static.argtypes = [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+        ctypes.c_int64, ctypes.c_float, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+        ctypes.c_int64, ctypes.c_void_p]
     lib.fa_splitkv_workspace_bytes.restype = ctypes.c_size_t
     lib.fa_splitkv_workspace_bytes.argtypes = [ctypes.c_int64] * 5
     lib.fa_splitkv_default_splits.restype = ctypes.c_int64
@@ -225,5 +231,26 @@ def fa_forward_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: tor
                                 _DTYPES[q.dtype], int(num_splits), workspace.data_ptr(),
                                 workspace.numel() * workspace.element_size(),
                                 _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc)
+
+
+FA_SPLITKV_STATIC_SCRATCH_BYTES = 16 << 20
+
+
+def fa_forward_splitkv_static(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                              lse: torch.Tensor, scale: float, mask_mode=FA_MASK_NONE,
+                              window_left: int = 0, window_right: int = 0, num_splits: int = 1,
+                              stream=None) -> None:
+    """Enqueue fa_forward_splitkv_static: split-KV attention whose scratch is the
+    library's fixed device array (no allocation; see include/fa.h)."""
+    lib = load_library()
+    _check(q, k, v, o, lse, same_n=False)
+    B, H, Nq, d = q.shape
+    rc = lib.fa_forward_splitkv_static(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                       lse.data_ptr(), B, H, k.shape[1], Nq, k.shape[2], d,
+                                       float(scale), _MASKS[mask_mode], int(window_left),
+                                       int(window_right), _DTYPES[q.dtype], int(num_splits),
+                                       _stream_handle(stream))
     if rc != FA_OK:
         raise FaError(rc)

@@ -27,6 +27,21 @@ constexpr int kSchedSlots = 64;
 __device__ unsigned int g_fa_sched[kSchedSlots][2];
 
 constexpr int kMaxDevices = 64;
+
+// Scratch of fa_forward_splitkv_static: a fixed array in device memory for
+// callers that cannot allocate. Every GPU that loads this library holds it
+// until the process exits.
+constexpr size_t kStaticScratchBytes = static_cast<size_t>(FA_SPLITKV_STATIC_SCRATCH_BYTES);
+__device__ __align__(256) unsigned char g_fa_static_scratch[kStaticScratchBytes];
+
+// Device address of g_fa_static_scratch, looked up once per device with that
+// device current (in host code the symbol is only a host-side stand-in).
+struct StaticScratch {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    void *ptr = nullptr;
+};
+StaticScratch g_static_scratch[kMaxDevices];
 constexpr uint64_t kDefaultBudgetNs = 2000000000ull;
 
 std::atomic<int64_t> g_launches{0};
@@ -419,6 +434,34 @@ fa_status fa_forward_splitkv(const void *Q, const void *K, const void *V, void *
     if (workspace != nullptr && !aligned16(workspace)) return FA_ERR_INVALID_ARG;
     Call c{Q, K, V, O, LSE, B, H, H_kv, Nq, Nk, d, scale, mask_mode, window_left, window_right,
            dtype, num_splits, workspace, workspace_bytes, stream};
+    return run_forward(c);
+}
+
+fa_status fa_forward_splitkv_static(const void *Q, const void *K, const void *V, void *O,
+                                    float *LSE, int64_t B, int64_t H, int64_t H_kv, int64_t Nq,
+                                    int64_t Nk, int64_t d, float scale, fa_mask_mode mask_mode,
+                                    int64_t window_left, int64_t window_right, fa_dtype dtype,
+                                    int64_t num_splits, void *stream) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+    StaticScratch &sc = g_static_scratch[dev];
+    std::call_once(sc.once, [&sc] {
+        void *ptr = nullptr;
+        sc.err = cudaGetSymbolAddress(&ptr, g_fa_static_scratch);
+        sc.ptr = ptr;
+        if (sc.err != cudaSuccess) cudaGetLastError();
+    });
+    if (sc.err != cudaSuccess || sc.ptr == nullptr) return FA_ERR_CUDA;
+    if (num_splits < 1) return FA_ERR_INVALID_ARG;
+    if (B >= 1 && H >= 1 && Nq >= 1 && d >= 1 &&
+        fa_splitkv_workspace_bytes(B, H, Nq, d, num_splits) > kStaticScratchBytes)
+        return FA_ERR_UNSUPPORTED;  // the request needs more than the fixed scratch
+    Call c{Q, K, V, O, LSE, B, H, H_kv, Nq, Nk, d, scale, mask_mode, window_left, window_right,
+           dtype, num_splits, sc.ptr, kStaticScratchBytes, stream};
     return run_forward(c);
 }
 
