@@ -149,7 +149,7 @@ def job_throughput(world: int, flops_per_rank: float, ms_per_step_max: float) ->
 def oracle_slab(w):
     """One (b, h) slab of the workload's shape, drawn with its recipe."""
     from tiled_attention_03_gb300.workloads import make_qkv
-    return make_qkv(1, 1, w.N, w.d, w.dtype, seed=w.seed, q_std=w.q_std)
+    return make_qkv(1, 1, w.N, w.d, w.dtype, seed=w.seed, q_std=w.q_std, Nq=w.Nq)
 
 
 def cpu_oracle_rate(w, min_seconds: float, max_units: int | None = None, slab=None):
@@ -159,10 +159,11 @@ def cpu_oracle_rate(w, min_seconds: float, max_units: int | None = None, slab=No
     from tiled_attention_03_gb300.workloads import visible_in_rows
     cores = len(os.sched_getaffinity(0))
     q, k, v = oracle_slab(w) if slab is None else slab
-    nblk = (w.N + 127) // 128
+    rows = w.q_rows
+    nblk = (rows + 127) // 128
     n = cores if max_units is None else min(cores, max_units)
     while True:
-        units = [(0, (u % nblk) * 128, min(w.N, (u % nblk + 1) * 128)) for u in range(n)]
+        units = [(0, (u % nblk) * 128, min(rows, (u % nblk + 1) * 128)) for u in range(n)]
         t0 = time.perf_counter()
         oracle.attention(q, k, v, w.scale, {0: "none", 1: "causal", 2: "window"}[w.mask],
                          (w.window_left, w.window_right), units=units, nthreads=cores)
@@ -171,10 +172,10 @@ def cpu_oracle_rate(w, min_seconds: float, max_units: int | None = None, slab=No
             break
         n *= 2
     # algorithmic flops of the sampled rows: 4 d per visible (query, key) pair
-    pairs = sum(visible_in_rows(w.N, w.mask, w.window_left, w.window_right, r0, r1)
+    pairs = sum(visible_in_rows(w.N, w.mask, w.window_left, w.window_right, r0, r1, w.Nq)
                 for _, r0, r1 in units)
     flops = 4.0 * w.d * pairs
-    return flops / dt / 1e12, cores, f"{len(units)} x (1 head, 128-row block, all {w.N} keys)", dt
+    return flops / dt / 1e12, cores, f"{len(units)} x (1 head, {min(128, rows)}-row block, all {w.N} keys)", dt
 
 
 def run_reference(args, w):
@@ -214,8 +215,14 @@ def run_e2e(args, w, q_h, k_h, v_h, mask, stream, dev, world, flops):
     kernel and copies O and LSE back."""
     import tiled_attention_03_gb300 as fa
     qp, kp, vp = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
+    splits = None if w.splits < 0 else w.splits
+
+    def run():
+        fa.forward(qp, kp, vp, w.scale, mask, (w.window_left, w.window_right),
+                   num_splits=splits)
+
     for _ in range(2):
-        fa.forward(qp, kp, vp, w.scale, mask, (w.window_left, w.window_right))
+        run()
     barrier(world)
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
@@ -223,12 +230,12 @@ def run_e2e(args, w, q_h, k_h, v_h, mask, stream, dev, world, flops):
     e3 = torch.cuda.Event(enable_timing=True)
     e2.record(stream)
     for _ in range(args.e2e_steps):
-        fa.forward(qp, kp, vp, w.scale, mask, (w.window_left, w.window_right))
+        run()
     e3.record(stream)
     torch.cuda.synchronize(dev)
     wall_ms = (time.perf_counter() - t0) * 1e3 / args.e2e_steps
     e2e_ms = max_over_ranks(max(e2.elapsed_time(e3) / args.e2e_steps, wall_ms), world)
-    elems = q_h.numel()
+    elems = q_h.numel()  # O has Q's shape
     h2d = (q_h.numel() + k_h.numel() + v_h.numel()) * q_h.element_size()
     d2h = elems * q_h.element_size() + (elems // w.d) * 4
     return {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
@@ -247,7 +254,7 @@ def main():
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
-    from tiled_attention_03_gb300.workloads import BY_NAME, algorithmic_flops
+    from tiled_attention_03_gb300.workloads import BY_NAME, algorithmic_bytes, algorithmic_flops
     w = BY_NAME[args.workload]
     if args.impl == "reference":
         run_reference(args, w)
@@ -268,10 +275,20 @@ def main():
     mask = {0: "none", 1: "causal", 2: "window"}[w.mask]
     stream = torch.cuda.current_stream(dev)
 
-    call = fa.fa_forward if w.kv_heads == w.H else fa.fa_forward_gqa
+    if w.splits >= 0:
+        splits = w.splits or fa.fa_splitkv_default_splits(w.B, w.H, w.kv_heads, w.q_rows, w.N)
+        ws = torch.empty(max(16, fa.fa_splitkv_workspace_bytes(w.B, w.H, w.q_rows, w.d, splits)),
+                         dtype=torch.uint8, device=dev)
 
-    def step():
-        call(q, k, v, o, lse, w.scale, mask, w.window_left, w.window_right, stream)
+        def step():
+            fa.fa_forward_splitkv(q, k, v, o, lse, w.scale, mask, w.window_left, w.window_right,
+                                  splits, ws, stream)
+    else:
+        splits = 1
+        call = fa.fa_forward if w.kv_heads == w.H else fa.fa_forward_gqa
+
+        def step():
+            call(q, k, v, o, lse, w.scale, mask, w.window_left, w.window_right, stream)
 
     for _ in range(args.warmup):
         step()
@@ -310,8 +327,11 @@ def main():
         e2e = run_e2e(args, w, q_h, k_h, v_h, mask, stream, dev, world, flops)
 
     if rank == 0:
-        peak_tf, _, peak_src = peaks()
+        peak_tf, peak_gbs, peak_src = peaks()
         achieved = flops / (kernel_ms * 1e-3) / 1e12
+        nbytes = algorithmic_bytes(w)
+        # tensor-bound above the ridge (peak FLOP/s / peak B/s), HBM-bound below it
+        tensor_bound = flops / nbytes > peak_tf * 1e12 / (peak_gbs * 1e9)
         traffic = measured_traffic()
         cpu = None
         if args.cpu_seconds > 0:
@@ -329,12 +349,19 @@ def main():
                        "kv_heads": w.kv_heads,
                        "l2": (f"inputs ({(q.numel() + k.numel() + v.numel()) * 2 / 1e6:.0f} MB) larger than L2, no flush"
                               if (q.numel() + k.numel() + v.numel()) * 2 > 129e6 else "inputs smaller than L2, no flush")},
-            "tokens_per_s": world * w.B * w.N / (ms_step * 1e-3),
+            "tokens_per_s": world * w.B * w.q_rows / (ms_step * 1e-3),
             "pct_of_peak": 100.0 * value / (world * peak_tf),
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf,
-                         "unit": "TFLOP/s", "frac": achieved / peak_tf,
-                         "traffic": traffic, "peak_source": f"{peak_src} bf16 burst",
-                         "kernel": f"fa_fwd_kernel<{w.d}, {w.dtype_name}>"},
+            "roofline": ({"bound": "tensor", "achieved": achieved, "peak": peak_tf,
+                          "unit": "TFLOP/s", "frac": achieved / peak_tf,
+                          "peak_source": f"{peak_src} bf16 burst"}
+                         if tensor_bound else
+                         {"bound": "hbm", "achieved": nbytes / (kernel_ms * 1e-3) / 1e9,
+                          "peak": peak_gbs, "unit": "GB/s",
+                          "frac": nbytes / (kernel_ms * 1e-3) / 1e9 / peak_gbs,
+                          "peak_source": f"{peak_src} copy bandwidth"}) | {
+                "traffic": traffic, "algorithmic_bytes": nbytes,
+                "kernel": f"fa_fwd_kernel<{w.d}, {w.dtype_name}>"
+                          + (f" + merge ({splits} key splits)" if splits > 1 else "")},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches,

@@ -131,8 +131,8 @@ size_t fa_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t d,
 
 /* A split count that fills the current device: 1 when the query blocks alone
  * give about one unit per SM, otherwise up to three units per SM with at
- * least four 128-key tiles per split. */
-int64_t fa_splitkv_default_splits(int64_t B, int64_t H, int64_t Nq, int64_t Nk);
+ * least four 128-key tiles per split (1 for invalid sizes). */
+int64_t fa_splitkv_default_splits(int64_t B, int64_t H, int64_t H_kv, int64_t Nq, int64_t Nk);
 
 /*
  * fa_forward_splitkv_static -- fa_forward_splitkv without a caller workspace,

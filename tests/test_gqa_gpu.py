@@ -37,7 +37,7 @@ def test_gqa_bit_exact_vs_repeated_kv(mask):
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-@pytest.mark.parametrize("w", EXTRA_WORKLOADS, ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [w for w in EXTRA_WORKLOADS if not w.Nq], ids=lambda w: w.name)
 def test_gqa_workloads_sampled(w):
     q, k, v = workload_inputs(w)
     o, lse = run_cuda(q, k, v, w.scale, MASK_ARG[w.mask], (w.window_left, w.window_right))

@@ -6,21 +6,29 @@ import pytest
 import torch
 
 import tiled_attention_03_gb300 as fa
-from tiled_attention_03_gb300.workloads import make_qkv
+from tiled_attention_03_gb300.workloads import (EXTRA_WORKLOADS, make_qkv, sample_units,
+                                                workload_inputs)
 
-from parity_util import TOL_LSE, TOL_O, compare, run_cuda
+from parity_util import GUARD, SENT_L, TOL_LSE, TOL_O, compare, run_cuda
 
 pytestmark = pytest.mark.gpu
 
 
 def run_split(q, k, v, scale, mask="none", window=(0, 0), splits=0):
+    """Split-KV call with sentinel guard bands around O and LSE."""
     dev = torch.device("cuda", 0)
     q, k, v = (t.to(dev).contiguous() for t in (q, k, v))
-    o = torch.full_like(q, -777.0)
-    lse = torch.full(q.shape[:-1], -12345.0, dtype=torch.float32, device=dev)
+    n, rows = q.numel(), q.numel() // q.shape[-1]
+    obuf = torch.full((n + 2 * GUARD,), -777.0, dtype=q.dtype, device=dev)
+    lbuf = torch.full((rows + 2 * GUARD,), SENT_L, dtype=torch.float32, device=dev)
+    o = obuf[GUARD:GUARD + n].view(q.shape)
+    lse = lbuf[GUARD:GUARD + rows].view(q.shape[:-1])
     fa.fa_forward_splitkv(q, k, v, o, lse, scale, mask, window[0], window[1], splits)
     st = fa.fa_sync_status()
     assert st == fa.FA_OK, fa.fa_status_string(st)
+    for buf, sent in ((obuf, -777.0), (lbuf, SENT_L)):
+        assert bool((buf[:GUARD] == sent).all()), "write before the output"
+        assert bool((buf[-GUARD:] == sent).all()), "write past the output"
     return o, lse
 
 
@@ -34,6 +42,22 @@ def test_splitkv_parity(splits, mask, window, Nq, Nk, d, dtype):
     _, k, v = make_qkv(1, 2, Nk, d, dtype, seed=Nk + 3 * splits, H_kv=2)
     o, lse = run_split(q, k, v, d ** -0.5, mask, window, splits)
     compare(o, lse, q, k, v, d ** -0.5, mask, window)
+
+
+# Few queries per head with grouped K/V heads: the query heads of a K/V head share
+# one row space, so 128-row tiles hold several heads and cut through heads.
+@pytest.mark.parametrize("B,H,Hk,Nq,Nk", [
+    (2, 16, 2, 1, 3000), (1, 16, 2, 33, 1500), (1, 8, 1, 64, 700), (3, 12, 4, 7, 129),
+    (1, 32, 8, 5, 40), (2, 6, 3, 64, 64), (1, 4, 2, 65, 900)])
+@pytest.mark.parametrize("mask,window", [("none", (0, 0)), ("causal", (0, 0)),
+                                         ("window", (200, 0)), ("window", (30, 20))])
+@pytest.mark.parametrize("splits", [1, 4])
+def test_packed_query_heads(splits, mask, window, B, H, Hk, Nq, Nk):
+    dtype = torch.bfloat16
+    q, _, _ = make_qkv(B, H, Nq, 128, dtype, seed=Nq * 7 + splits)
+    _, k, v = make_qkv(B, Hk, Nk, 128, dtype, seed=Nk + H, H_kv=Hk)
+    o, lse = run_split(q, k, v, 0.09, mask, window, splits)
+    compare(o, lse, q, k, v, 0.09, mask, window)
 
 
 @pytest.mark.parametrize("mask", ["none", "causal"])
@@ -51,7 +75,7 @@ def test_splitkv_default_splits_and_decode_shape():
     B, H, Hk, Nk, d = 4, 32, 8, 16384, 128
     q, _, _ = make_qkv(B, H, 1, d, torch.bfloat16, seed=1)
     _, k, v = make_qkv(B, Hk, Nk, d, torch.bfloat16, seed=2, H_kv=Hk)
-    s = fa.fa_splitkv_default_splits(B, H, 1, Nk)
+    s = fa.fa_splitkv_default_splits(B, H, Hk, 1, Nk)
     assert s > 1
     o, lse = run_split(q, k, v, d ** -0.5, "causal", splits=0)
     compare(o, lse, q, k, v, d ** -0.5, "causal", units=[(0, 0, 1), (B * H - 1, 0, 1), (77, 0, 1)])
@@ -71,3 +95,14 @@ def test_splitkv_workspace_checks():
         fa.fa_forward_splitkv(kk, q, v, torch.empty_like(kk), torch.empty(kk.shape[:-1], device="cuda"),
                               0.125, "causal", 0, 0, 2)
     assert fa.fa_sync_status() == fa.FA_OK
+
+
+@pytest.mark.parametrize("w", [w for w in EXTRA_WORKLOADS if w.Nq], ids=lambda w: w.name)
+def test_splitkv_workloads_sampled(w):
+    """The decode and chunked-prefill workloads at full size, in the split count
+    the benchmark uses, on sampled rows."""
+    q, k, v = workload_inputs(w)
+    window = (w.window_left, w.window_right)
+    mask = {0: "none", 1: "causal", 2: "window"}[w.mask]
+    o, lse = run_split(q, k, v, w.scale, mask, window, max(w.splits, 0))
+    compare(o, lse, q, k, v, w.scale, mask, window, units=sample_units(w))

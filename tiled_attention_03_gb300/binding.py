@@ -67,7 +67,7 @@ def load_library(path: str = LIB) -> ctypes.CDLL:
     lib.fa_splitkv_workspace_bytes.restype = ctypes.c_size_t
     lib.fa_splitkv_workspace_bytes.argtypes = [ctypes.c_int64] * 5
     lib.fa_splitkv_default_splits.restype = ctypes.c_int64
-    lib.fa_splitkv_default_splits.argtypes = [ctypes.c_int64] * 4
+    lib.fa_splitkv_default_splits.argtypes = [ctypes.c_int64] * 5
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_status_string.argtypes = [ctypes.c_int]
     lib.fa_sync_status.restype = ctypes.c_int
@@ -169,9 +169,11 @@ def fa_forward_gqa(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.T
 
 
 def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
-            mask="none", window=(0, 0), stream=None):
+            mask="none", window=(0, 0), stream=None, num_splits: int | None = None):
     """Attention forward: returns (O, LSE). K and V may have fewer heads than Q
-    (grouped-query attention: H_kv must divide H).
+    (grouped-query attention: H_kv must divide H) and more positions than Q (the
+    queries are then the last positions; this runs the split-KV entry point, as
+    does any num_splits, with 0 meaning its default).
 
     Device tensors run in place on the device. Host tensors are copied to the
     current CUDA device, processed, and the results copied back to host
@@ -188,7 +190,11 @@ def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | No
     q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
-    fa_forward_gqa(q, k, v, o, lse, scale, mask, window[0], window[1], stream)
+    if num_splits is not None or q.shape[2] != k.shape[2]:
+        fa_forward_splitkv(q, k, v, o, lse, scale, mask, window[0], window[1],
+                           num_splits or 0, None, stream)
+    else:
+        fa_forward_gqa(q, k, v, o, lse, scale, mask, window[0], window[1], stream)
     if host:
         o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
         lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
@@ -203,8 +209,8 @@ def fa_splitkv_workspace_bytes(B: int, H: int, Nq: int, d: int, num_splits: int)
     return load_library().fa_splitkv_workspace_bytes(B, H, Nq, d, num_splits)
 
 
-def fa_splitkv_default_splits(B: int, H: int, Nq: int, Nk: int) -> int:
-    return load_library().fa_splitkv_default_splits(B, H, Nq, Nk)
+def fa_splitkv_default_splits(B: int, H: int, H_kv: int, Nq: int, Nk: int) -> int:
+    return load_library().fa_splitkv_default_splits(B, H, H_kv, Nq, Nk)
 
 
 def fa_forward_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
@@ -219,7 +225,7 @@ def fa_forward_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: tor
     B, H, Nq, d = q.shape
     Nk = k.shape[2]
     if num_splits <= 0:
-        num_splits = fa_splitkv_default_splits(B, H, Nq, Nk)
+        num_splits = fa_splitkv_default_splits(B, H, k.shape[1], Nq, Nk)
     need = fa_splitkv_workspace_bytes(B, H, Nq, d, num_splits)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)

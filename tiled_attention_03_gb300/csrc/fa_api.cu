@@ -94,15 +94,21 @@ uint64_t wait_budget() {
 // Opt in to the kernel's shared memory, and check that the registers a launch
 // allocates cover the kernel's setmaxnreg split (a split above them would make
 // setmaxnreg.inc wait forever).
-template <int D, bool BF16>
-cudaError_t configure_kernel() {
+template <int D, bool BF16, bool PACKED>
+cudaError_t configure_one() {
     cudaFuncAttributes attr{};
-    cudaError_t e = cudaFuncGetAttributes(&attr, fa::fa_fwd_kernel<D, BF16>);
+    cudaError_t e = cudaFuncGetAttributes(&attr, fa::fa_fwd_kernel<D, BF16, PACKED>);
     if (e != cudaSuccess) return e;
     if (attr.numRegs * fa::kThreads < fa::kRegsNeeded) return cudaErrorInvalidConfiguration;
-    return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, BF16>,
+    return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, BF16, PACKED>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 fa::SmemLayout<D>::kAlloc);
+}
+
+template <int D, bool BF16>
+cudaError_t configure_kernel() {
+    const cudaError_t e = configure_one<D, BF16, false>();
+    return e != cudaSuccess ? e : configure_one<D, BF16, true>();
 }
 
 DeviceState *device_state(int dev) {
@@ -150,8 +156,9 @@ bool on_device(const void *p, int dev) {
     return false;
 }
 
-// 3-D map over a contiguous (B*H) x N x d 16-bit tensor, box = 64 columns x 128 rows,
-// 128-byte swizzle; rows past N read as zero.
+// 3-D map over a contiguous BH x N x d 16-bit tensor, box = 64 columns x 128 rows,
+// 128-byte swizzle; rows past N read as zero. Q is mapped by row space
+// (n_spaces x R x d), K and V by head.
 bool make_map(CUtensorMap *map, const void *base, bool bf16, int64_t BH, int64_t N, int64_t d) {
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return false;
@@ -171,9 +178,13 @@ bool make_map(CUtensorMap *map, const void *base, bool bf16, int64_t BH, int64_t
 
 template <int D, bool BF16>
 cudaError_t launch(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                   const fa::FwdParams &p, int64_t blocks, cudaStream_t stream) {
-    fa::fa_fwd_kernel<D, BF16><<<static_cast<unsigned>(blocks), fa::kThreads,
-                                 fa::SmemLayout<D>::kAlloc, stream>>>(q, k, v, p);
+                   const fa::FwdParams &p, bool packed, int64_t blocks, cudaStream_t stream) {
+    if (packed)
+        fa::fa_fwd_kernel<D, BF16, true><<<static_cast<unsigned>(blocks), fa::kThreads,
+                                           fa::SmemLayout<D>::kAlloc, stream>>>(q, k, v, p);
+    else
+        fa::fa_fwd_kernel<D, BF16, false><<<static_cast<unsigned>(blocks), fa::kThreads,
+                                            fa::SmemLayout<D>::kAlloc, stream>>>(q, k, v, p);
     return cudaGetLastError();
 }
 
@@ -202,9 +213,16 @@ size_t splitkv_bytes(int64_t rows, int64_t d, int64_t splits) {
            static_cast<size_t>(splits) * rows * d * sizeof(float);
 }
 
+// Query rows are packed per K/V head (all its query heads in one row space) when
+// there are few queries per head and the heads are grouped.
+bool pack_rows(int64_t H, int64_t H_kv, int64_t Nq) { return H_kv < H && Nq <= 64; }
+
 // Enough splits for about three units per SM, each split keeping >= 4 K/V tiles.
-int64_t default_splits(int64_t BH, int64_t Nq, int64_t Nk, int sms) {
-    const int64_t units = BH * ((Nq + fa::kUnitRows - 1) / fa::kUnitRows);
+int64_t default_splits(int64_t B, int64_t H, int64_t H_kv, int64_t Nq, int64_t Nk, int sms) {
+    const bool packed = pack_rows(H, H_kv, Nq);
+    const int64_t spaces = packed ? B * H_kv : B * H;
+    const int64_t R = packed ? (H / H_kv) * Nq : Nq;
+    const int64_t units = spaces * ((R + fa::kUnitRows - 1) / fa::kUnitRows);
     const int64_t tiles = (Nk + fa::kBN - 1) / fa::kBN;
     if (units >= sms) return 1;
     int64_t s = (3 * sms + units - 1) / units;
@@ -251,13 +269,16 @@ fa_status run_forward(const Call &c) {
         return FA_ERR_UNSUPPORTED;
     const int64_t BH = B * H;
     const int64_t BHkv = B * H_kv;
-    const int64_t n_qb = (Nq + fa::kUnitRows - 1) / fa::kUnitRows;
+    const bool packed = pack_rows(H, H_kv, Nq);
+    const int64_t R = packed ? (H / H_kv) * Nq : Nq;
+    const int64_t spaces = packed ? BHkv : BH;
+    const int64_t n_qb = (R + fa::kUnitRows - 1) / fa::kUnitRows;
     const int64_t kv_tiles = (Nk + fa::kBN - 1) / fa::kBN;
     const int64_t splits = c.num_splits < kv_tiles ? c.num_splits : kv_tiles;
     const int64_t split_tiles = (kv_tiles + splits - 1) / splits;
     const int64_t n_splits = (kv_tiles + split_tiles - 1) / split_tiles;
-    const int64_t n_units = BH * n_qb * n_splits;
-    if (n_units > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+    const int64_t n_units = spaces * n_qb * n_splits;
+    if (n_units > 0x7fffffffLL || BH * Nq > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
     const bool split = n_splits > 1;
     const size_t tbytes = static_cast<size_t>(BH) * Nq * d * 2;
     const size_t lbytes = static_cast<size_t>(BH) * Nq * sizeof(float);
@@ -292,7 +313,7 @@ fa_status run_forward(const Call &c) {
 
     const bool bf16 = c.dtype == FA_DTYPE_BF16;
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, Q, bf16, BH, Nq, d) || !make_map(&mk, K, bf16, BHkv, Nk, d) ||
+    if (!make_map(&mq, Q, bf16, spaces, R, d) || !make_map(&mk, K, bf16, BHkv, Nk, d) ||
         !make_map(&mv, V, bf16, BHkv, Nk, d))
         return FA_ERR_CUDA;
 
@@ -314,6 +335,7 @@ fa_status run_forward(const Call &c) {
     p.H = static_cast<int>(H);
     p.BH = static_cast<int>(BH);
     p.kv_group = static_cast<int>(H / H_kv);
+    p.R = static_cast<int>(R);
     p.n_units = static_cast<int>(n_units);
     p.n_qb = static_cast<int>(n_qb);
     p.n_splits = static_cast<int>(n_splits);
@@ -341,11 +363,11 @@ fa_status run_forward(const Call &c) {
     cudaStream_t st = static_cast<cudaStream_t>(c.stream);
     cudaError_t e;
     if (d == 64)
-        e = bf16 ? launch<64, true>(mq, mk, mv, p, blocks, st)
-                 : launch<64, false>(mq, mk, mv, p, blocks, st);
+        e = bf16 ? launch<64, true>(mq, mk, mv, p, packed, blocks, st)
+                 : launch<64, false>(mq, mk, mv, p, packed, blocks, st);
     else
-        e = bf16 ? launch<128, true>(mq, mk, mv, p, blocks, st)
-                 : launch<128, false>(mq, mk, mv, p, blocks, st);
+        e = bf16 ? launch<128, true>(mq, mk, mv, p, packed, blocks, st)
+                 : launch<128, false>(mq, mk, mv, p, packed, blocks, st);
     if (e != cudaSuccess) return FA_ERR_CUDA;
     g_launches.fetch_add(1);
     if (split) {
@@ -415,14 +437,14 @@ size_t fa_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t d,
     return splitkv_bytes(B * H * Nq, d, num_splits);
 }
 
-int64_t fa_splitkv_default_splits(int64_t B, int64_t H, int64_t Nq, int64_t Nk) {
-    if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return 1;
+int64_t fa_splitkv_default_splits(int64_t B, int64_t H, int64_t H_kv, int64_t Nq, int64_t Nk) {
+    if (B < 1 || H < 1 || H_kv < 1 || H % H_kv != 0 || Nq < 1 || Nk < 1) return 1;
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess)
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     else
         cudaGetLastError();
-    return default_splits(B * H, Nq, Nk, sms);
+    return default_splits(B, H, H_kv, Nq, Nk, sms);
 }
 
 fa_status fa_forward_splitkv(const void *Q, const void *K, const void *V, void *O, float *LSE,

@@ -105,8 +105,15 @@ struct FwdParams {
     int H;            // query heads
     int BH;           // B * H
     int kv_group;     // query heads per K/V head (H / H_kv; 1 = one K/V head per query head)
-    int n_units;      // (b*H + h, 256-row block, key split) work units
-    int n_qb;         // 256-row blocks per head: ceil(Nq / 256)
+    // Rows are processed in "row spaces" of R rows. Unpacked: one per query head
+    // (R = Nq). Packed (kernel template flag; few queries, grouped K/V heads): one
+    // per K/V head, holding the Nq queries of each of its kv_group query heads one
+    // after the other (R = kv_group * Nq), so that one unit streams a K/V head once
+    // for all of them. Row r of row space s is global row s * R + r of the
+    // B*H*Nq query rows (in both cases), and query index r mod Nq of its head.
+    int R;
+    int n_units;      // (row space, 256-row block, key split) work units
+    int n_qb;         // 256-row blocks per row space: ceil(R / 256)
     int n_splits;     // key splits per row block (1: no split)
     int split_tiles;  // K/V tiles per key split
     int heavy_first;  // 1: within a head, visit row blocks from the last (most keys) to the first
@@ -158,25 +165,50 @@ enum : int {
     kNumBarsUsed = kBarUnitEmpty + 2,
 };
 
-// A work unit: rows [r0, r0 + 256) of query head bh (= b * H + h), whose keys and
-// values are those of K/V head bkv (= b * H_kv + h / kv_group), restricted to the
-// K/V tiles of key split `split`; Q tile t covers rows [r0 + 128 t, r0 + 128 t + 128)
-// and needs K/V tiles [a[t], b[t]] (empty when a > b); [j0, j1] is their union.
+// A work unit: rows [r0, r0 + 256) of row space rs (global rows rs * R + r)
+// whose keys and values are those of K/V head bkv (= b * H_kv + h / kv_group),
+// restricted to the K/V tiles of key split `split`; Q tile t covers rows
+// [r0 + 128 t, r0 + 128 t + 128) and needs K/V tiles [a[t], b[t]] (empty when
+// a > b); [j0, j1] is their union.
 struct Unit {
-    int bh, bkv, r0, split;
+    int rs, bkv, r0, split;
     int a[kQTiles], b[kQTiles];
     int j0, j1;
 };
 
+// Query indices (0..Nq-1) met by the rows [rt0, rl] of a row space (an unpacked
+// row space is one head: rows are queries).
+template <bool PACKED>
+__device__ __forceinline__ void tile_queries(const FwdParams &p, int rt0, int rl, int &i_lo,
+                                             int &i_hi) {
+    if (!PACKED) {
+        i_lo = rt0;
+        i_hi = rl;
+        return;
+    }
+    const int a = rt0 % p.Nq, b = rl % p.Nq;
+    if (rl - rt0 + 1 >= p.Nq || b < a) {
+        i_lo = 0;
+        i_hi = p.Nq - 1;
+    } else {
+        i_lo = a;
+        i_hi = b;
+    }
+}
+
+template <bool PACKED>
 __device__ __forceinline__ Unit decode_unit(int u, const FwdParams &p) {
     Unit U;
-    const int per_head = p.n_qb * p.n_splits;
-    U.bh = u / per_head;
-    const int rem = u - U.bh * per_head;
+    const int per_space = p.n_qb * p.n_splits;
+    const int rs = u / per_space;
+    const int rem = u - rs * per_space;
     int qb = rem / p.n_splits;
     U.split = rem - qb * p.n_splits;
-    {
-        const int b = U.bh / p.H, h = U.bh - b * p.H;
+    U.rs = rs;
+    if (PACKED) {
+        U.bkv = rs;
+    } else {
+        const int b = rs / p.H, h = rs - b * p.H;
         U.bkv = b * (p.H / p.kv_group) + h / p.kv_group;
     }
     if (p.heavy_first) qb = p.n_qb - 1 - qb;
@@ -190,10 +222,12 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams &p) {
         const int rt0 = U.r0 + t * kBM;
         U.a[t] = 1;
         U.b[t] = 0;
-        if (rt0 < p.Nq) {
-            const int rl = min(rt0 + kBM, p.Nq) - 1;
-            const int lo_key = rt0 + p.q_off - p.wl;  // first key any row of the tile sees
-            const int hi_key = rl + p.q_off + p.wr;   // last key any row of the tile sees
+        if (rt0 < p.R) {
+            const int rl = min(rt0 + kBM, p.R) - 1;
+            int i_lo, i_hi;
+            tile_queries<PACKED>(p, rt0, rl, i_lo, i_hi);
+            const int lo_key = i_lo + p.q_off - p.wl;  // first key any row of the tile sees
+            const int hi_key = i_hi + p.q_off + p.wr;  // last key any row of the tile sees
             if (hi_key >= 0 && lo_key <= p.Nk - 1) {
                 const int a = max(max(0, lo_key) / kBN, s_lo);
                 const int b = min(min(p.Nk - 1, hi_key) / kBN, s_hi);
@@ -335,7 +369,7 @@ __device__ __forceinline__ float softmax_tile(uint32_t tS, uint32_t tP, bool bou
     return corr;
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool PACKED>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -425,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 while (true) {
                     const unsigned next = atomicAdd(p.sched, 1u);
                     if (next >= static_cast<unsigned>(p.n_units)) break;
-                    if (!unit_empty(decode_unit(static_cast<int>(next), p))) {
+                    if (!unit_empty(decode_unit<PACKED>(static_cast<int>(next), p))) {
                         v = static_cast<int>(next);
                         break;
                     }
@@ -435,21 +469,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return v;
             };
             auto prefetch_q_l2 = [&](int v) {
-                const Unit W = decode_unit(v, p);
+                const Unit W = decode_unit<PACKED>(v, p);
                 for (int t = 0; t < kQTiles; ++t)
                     for (int g = 0; g < kRegions; ++g)
-                        tma_prefetch_l2_3d(&tmQ, 64 * g, W.r0 + t * kBM, W.bh);
+                        tma_prefetch_l2_3d(&tmQ, 64 * g, W.r0 + t * kBM, W.rs);
             };
             int u = publish(0);
             for (; ok && u >= 0; ++unit_iter) {
-                const Unit U = decode_unit(u, p);
+                const Unit U = decode_unit<PACKED>(u, p);
                 for (int t = 0; t < kQTiles && ok; ++t) {
                     ok = mbar_wait_bounded(bar(kBarQEmpty + t), (unit_iter & 1) ^ 1, abort_flag, budget);
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(kBarQFull + t), L::kTileBytes);
                     for (int g = 0; g < kRegions; ++g)
                         tma_load_3d(sQ + t * L::kTileBytes + g * kRegionBytes, &tmQ,
-                                    bar(kBarQFull + t), 64 * g, U.r0 + t * kBM, U.bh);
+                                    bar(kBarQFull + t), 64 * g, U.r0 + t * kBM, U.rs);
                 }
                 if (!ok) break;
                 ++q_loads;
@@ -502,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int u = unit_ring[slot];
                 mbar_arrive(bar(kBarUnitEmpty + slot));
                 if (u < 0) break;
-                const Unit U = decode_unit(u, p);
+                const Unit U = decode_unit<PACKED>(u, p);
                 for (int j = U.j0; ok && j <= U.j1; ++j, ++kv_iter) {
                     const int st = kv_iter % kStages;
                     ok = mbar_wait_bounded(bar(kBarVEmpty + st), ((kv_iter / kStages) & 1) ^ 1,
@@ -594,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (elect_one()) mbar_arrive(bar(kBarUnitEmpty + slot));
             __syncwarp();
             if (u < 0) break;
-            const Unit U = decode_unit(u, p);
+            const Unit U = decode_unit<PACKED>(u, p);
             for (int t = 0; t < kQTiles && ok; ++t) ok = wait(kBarQFull + t, unit_iter & 1);
             const int j0 = U.j0;
             const int j1 = U.j1;
@@ -661,16 +695,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarUnitEmpty + slot));
             if (u < 0) break;
-            const Unit U = decode_unit(u, p);
+            const Unit U = decode_unit<PACKED>(u, p);
             if (U.a[t] > U.b[t]) continue;
             const int rt0 = U.r0 + t * kBM;
-            const int rl = min(rt0 + kBM, p.Nq) - 1;
-            const int i = rt0 + row;  // query index
-            // visible keys of row i: [i + q_off - wl, i + q_off + wr] within [0, Nk)
+            const int rl = min(rt0 + kBM, p.R) - 1;
+            const int r = rt0 + row;     // row of the row space
+            const int i = PACKED ? r % p.Nq : r;  // query index in its head
+            int i_lo, i_hi;
+            tile_queries<PACKED>(p, rt0, rl, i_lo, i_hi);
+            // visible keys of query i: [i + q_off - wl, i + q_off + wr] within [0, Nk)
             const int lo_i = max(0, i + p.q_off - p.wl);
             const int hi_i = min(p.Nk - 1, i + p.q_off + p.wr);
-            const int lo_last = max(0, rl + p.q_off - p.wl);
-            const int hi_first = min(p.Nk - 1, rt0 + p.q_off + p.wr);
+            const int lo_last = max(0, i_hi + p.q_off - p.wl);
+            const int hi_first = min(p.Nk - 1, i_lo + p.q_off + p.wr);
             float m = -INFINITY;  // reference max of the row, in log2 units of the scaled logits
             float l = 0.f;        // running sum of 2^(logit - m)
             for (int j = U.a[t]; j <= U.b[t]; ++j, ++s_count) {
@@ -716,12 +753,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
-            const bool store = i < p.Nq;
+            const bool store = r < p.R;
+            const size_t grow = static_cast<size_t>(U.rs) * p.R + (store ? r : 0);  // global row
             const float lse = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
             if (p.part_O == nullptr) {
                 // O / l rounded to 16 bit, and LSE
-                uint8_t *orow = reinterpret_cast<uint8_t *>(p.O) +
-                                (static_cast<size_t>(U.bh) * p.Nq + (store ? i : 0)) * (D * 2);
+                uint8_t *orow = reinterpret_cast<uint8_t *>(p.O) + grow * (D * 2);
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
@@ -739,10 +776,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
                     }
                 }
-                if (store) p.LSE[static_cast<size_t>(U.bh) * p.Nq + i] = lse;
+                if (store) p.LSE[grow] = lse;
             } else {
                 // key split: the split's own O / l in fp32 and its LSE, merged later
-                const size_t prow = (static_cast<size_t>(U.split) * p.BH + U.bh) * p.Nq + (store ? i : 0);
+                const size_t prow = static_cast<size_t>(U.split) * p.BH * p.Nq + grow;
                 float *orow = p.part_O + prow * D;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {

@@ -46,6 +46,8 @@ class Workload:
     seed: int
     q_std: float = 1.0
     H_kv: int = 0  # K/V heads (grouped-query attention); 0 means H
+    Nq: int = 0    # query rows per head when fewer than the N keys (the last Nq positions); 0 means N
+    splits: int = -1  # key splits for the split-KV entry point (0: its default); -1: not split
 
     @property
     def scale(self) -> float:
@@ -60,12 +62,17 @@ class Workload:
     def kv_heads(self) -> int:
         return self.H_kv or self.H
 
+    @property
+    def q_rows(self) -> int:
+        return self.Nq or self.N
+
     def describe(self) -> str:
         m = MASK_NAMES[self.mask]
         if self.mask == MASK_WINDOW:
             m += f"({self.window_left},{self.window_right})"
         kv = f" Hkv{self.kv_heads}" if self.kv_heads != self.H else ""
-        return f"B{self.B} H{self.H}{kv} N{self.N} d{self.d} {self.dtype_name} {m}"
+        nq = f" Nq{self.q_rows}" if self.q_rows != self.N else ""
+        return f"B{self.B} H{self.H}{kv}{nq} N{self.N} d{self.d} {self.dtype_name} {m}"
 
 
 WORKLOADS = [
@@ -84,18 +91,24 @@ EXTRA_WORKLOADS = [
              seed=5, H_kv=8),
     Workload("mqa_causal_b2h16kv1n2048d64", 2, 16, 2048, 64, torch.float16, MASK_CAUSAL, 0, 0,
              seed=6, H_kv=1),
+    # split-KV: one decode step over a long cache (memory-bound), and a 512-query chunk
+    # appended to a 16k-token cache
+    Workload("decode_b8h32kv8_nq1_nk32768_d128", 8, 32, 32768, 128, torch.bfloat16, MASK_CAUSAL,
+             0, 0, seed=7, H_kv=8, Nq=1, splits=0),
+    Workload("chunk_b1h32kv8_nq512_nk16384_d128", 1, 32, 16384, 128, torch.bfloat16, MASK_CAUSAL,
+             0, 0, seed=8, H_kv=8, Nq=512, splits=0),
 ]
 
 BY_NAME = {w.name: w for w in WORKLOADS + EXTRA_WORKLOADS}
 
 
 def make_qkv(B: int, H: int, N: int, d: int, dtype: torch.dtype, seed: int,
-             q_std: float = 1.0, H_kv: int = 0):
-    """Return CPU tensors Q (B, H, N, d) and K, V (B, H_kv or H, N, d) in ``dtype``."""
+             q_std: float = 1.0, H_kv: int = 0, Nq: int = 0):
+    """Return CPU tensors Q (B, H, Nq or N, d) and K, V (B, H_kv or H, N, d) in ``dtype``."""
     g = torch.Generator(device="cpu")
     g.manual_seed(seed)
     Hk = H_kv or H
-    q = torch.randn(B, H, N, d, generator=g, dtype=torch.float32)
+    q = torch.randn(B, H, Nq or N, d, generator=g, dtype=torch.float32)
     if q_std != 1.0:
         q.mul_(q_std)
     q = q.to(dtype)
@@ -105,13 +118,13 @@ def make_qkv(B: int, H: int, N: int, d: int, dtype: torch.dtype, seed: int,
 
 
 def workload_inputs(w: Workload):
-    return make_qkv(w.B, w.H, w.N, w.d, w.dtype, w.seed, w.q_std, w.H_kv)
+    return make_qkv(w.B, w.H, w.N, w.d, w.dtype, w.seed, w.q_std, w.H_kv, w.Nq)
 
 
 def sample_units(w: Workload, n: int = 16, block: int = 128, seed: int | None = None):
     """Seeded sample of (bh, row0, row1) slices: always the first block, the
     last (possibly ragged) block and one middle block, plus random ones."""
-    nblk = (w.N + block - 1) // block
+    nblk = (w.q_rows + block - 1) // block
     BH = w.B * w.H
     g = torch.Generator(device="cpu")
     g.manual_seed(1000 + w.seed if seed is None else seed)
@@ -121,36 +134,37 @@ def sample_units(w: Workload, n: int = 16, block: int = 128, seed: int | None = 
         blk = int(torch.randint(0, nblk, (1,), generator=g))
         if (bh, blk) not in picks:
             picks.append((bh, blk))
-    return [(bh, blk * block, min(w.N, (blk + 1) * block)) for bh, blk in picks[:n]]
+    return [(bh, blk * block, min(w.q_rows, (blk + 1) * block)) for bh, blk in picks[:n]]
 
 
-def visible_in_rows(N: int, mask: int, wl: int, wr: int, r0: int, r1: int) -> int:
+def visible_in_rows(N: int, mask: int, wl: int, wr: int, r0: int, r1: int, Nq: int = 0) -> int:
     """Number of (query, key) pairs a mask leaves visible for query rows
-    [r0, r1) of one (b, h): the count the algorithmic FLOP figure is built on
-    (4*d per pair)."""
+    [r0, r1) of one (b, h) with N keys (query i at key position i + N - Nq):
+    the count the algorithmic FLOP figure is built on (4*d per pair)."""
+    off = N - (Nq or N)
     if mask == MASK_NONE:
         return (r1 - r0) * N
     if mask == MASK_CAUSAL:
         wl, wr = N, 0
     total = 0
     for i in range(r0, r1):
-        lo = max(0, i - wl)
-        hi = min(N - 1, i + wr)
-        total += hi - lo + 1
+        lo = max(0, i + off - wl)
+        hi = min(N - 1, i + off + wr)
+        total += max(0, hi - lo + 1)
     return total
 
 
-def visible_pairs(N: int, mask: int, wl: int, wr: int) -> int:
+def visible_pairs(N: int, mask: int, wl: int, wr: int, Nq: int = 0) -> int:
     """Visible (query, key) pairs of one (b, h)."""
-    return visible_in_rows(N, mask, wl, wr, 0, N)
+    return visible_in_rows(N, mask, wl, wr, 0, Nq or N, Nq)
 
 
 def algorithmic_flops(w: Workload) -> float:
-    return 4.0 * w.d * w.B * w.H * visible_pairs(w.N, w.mask, w.window_left, w.window_right)
+    return 4.0 * w.d * w.B * w.H * visible_pairs(w.N, w.mask, w.window_left, w.window_right, w.Nq)
 
 
 def algorithmic_bytes(w: Workload) -> int:
     """Q, K, V read once and O (16-bit) plus LSE (fp32) written once."""
-    q_elems = w.B * w.H * w.N * w.d
+    q_elems = w.B * w.H * w.q_rows * w.d
     kv_elems = w.B * w.kv_heads * w.N * w.d
-    return (2 * q_elems + 2 * kv_elems) * 2 + w.B * w.H * w.N * 4
+    return (2 * q_elems + 2 * kv_elems) * 2 + w.B * w.H * w.q_rows * 4
