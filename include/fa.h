@@ -129,9 +129,10 @@ fa_status fa_forward_splitkv(const void *Q, const void *K, const void *V, void *
 size_t fa_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t d,
                                   int64_t num_splits);
 
-/* A split count that fills the current device: 1 when the query blocks alone
- * give about one unit per SM, otherwise up to three units per SM with at
- * least four 128-key tiles per split (1 for invalid sizes). */
+/* A split count that fills the current device in one wave: 1 when the query
+ * blocks alone give at least one unit per SM, otherwise as many splits as the
+ * SMs hold next to those units, each keeping at least four 128-key tiles
+ * (1 for invalid sizes). */
 int64_t fa_splitkv_default_splits(int64_t B, int64_t H, int64_t H_kv, int64_t Nq, int64_t Nk);
 
 /*

@@ -217,7 +217,10 @@ size_t splitkv_bytes(int64_t rows, int64_t d, int64_t splits) {
 // there are few queries per head and the heads are grouped.
 bool pack_rows(int64_t H, int64_t H_kv, int64_t Nq) { return H_kv < H && Nq <= 64; }
 
-// Enough splits for about three units per SM, each split keeping >= 4 K/V tiles.
+// Splits that fill one wave: as many as fit on the SMs next to the unsplit
+// units (measured on decode and chunked-prefill shapes, one wave beat both an
+// underfilled grid and several waves of shorter units), each split keeping at
+// least four 128-key tiles. 1 when the units alone fill the SMs.
 int64_t default_splits(int64_t B, int64_t H, int64_t H_kv, int64_t Nq, int64_t Nk, int sms) {
     const bool packed = pack_rows(H, H_kv, Nq);
     const int64_t spaces = packed ? B * H_kv : B * H;
@@ -225,7 +228,7 @@ int64_t default_splits(int64_t B, int64_t H, int64_t H_kv, int64_t Nq, int64_t N
     const int64_t units = spaces * ((R + fa::kUnitRows - 1) / fa::kUnitRows);
     const int64_t tiles = (Nk + fa::kBN - 1) / fa::kBN;
     if (units >= sms) return 1;
-    int64_t s = (3 * sms + units - 1) / units;
+    int64_t s = sms / units;
     const int64_t cap = tiles / 4 > 1 ? tiles / 4 : 1;
     if (s > cap) s = cap;
     if (s > 256) s = 256;
