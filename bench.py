@@ -33,7 +33,7 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 KERNEL_SOURCES = ("tiled_attention_03_gb300/csrc/fa_fwd_kernel.cuh",
                   "tiled_attention_03_gb300/csrc/ptx.cuh")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fa_fwd_kernel_b4h32n4096d128_traffic.txt")
+TRAFFIC_DIR = os.path.join(ROOT, "profiles")
 
 
 def kernel_source_hash() -> str:
@@ -44,20 +44,28 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def measured_traffic():
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source; else None."""
+def measured_traffic(workload: str):
+    """DRAM bytes per step from the committed ncu summary (profiles/*_traffic.txt)
+    of this workload, if it was taken on the current kernel source; else None."""
     try:
-        vals = {}
-        with open(TRAFFIC_FILE) as f:
-            for line in f:
-                if ":" in line and not line.startswith("#"):
-                    key, val = line.split(":", 1)
-                    vals[key.strip()] = val.strip()
-        if vals.get("kernel_source_hash") == kernel_source_hash():
-            return float(vals["dram_bytes_per_launch"])
-    except (OSError, KeyError, ValueError):
-        pass
+        names = sorted(os.listdir(TRAFFIC_DIR))
+    except OSError:
+        return None
+    for name in names:
+        if not name.endswith("_traffic.txt"):
+            continue
+        try:
+            vals = {}
+            with open(os.path.join(TRAFFIC_DIR, name)) as f:
+                for line in f:
+                    if ":" in line and not line.startswith("#"):
+                        key, val = line.split(":", 1)
+                        vals[key.strip()] = val.strip()
+            if (vals.get("workload") == workload
+                    and vals.get("kernel_source_hash") == kernel_source_hash()):
+                return float(vals["dram_bytes_per_launch"])
+        except (OSError, KeyError, ValueError):
+            continue
     return None
 
 
@@ -332,7 +340,7 @@ def main():
         nbytes = algorithmic_bytes(w)
         # tensor-bound above the ridge (peak FLOP/s / peak B/s), HBM-bound below it
         tensor_bound = flops / nbytes > peak_tf * 1e12 / (peak_gbs * 1e9)
-        traffic = measured_traffic()
+        traffic = measured_traffic(w.name)
         cpu = None
         if args.cpu_seconds > 0:
             cpu_v, cores, sample, _ = cpu_oracle_rate(w, args.cpu_seconds)
