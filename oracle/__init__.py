@@ -4,9 +4,10 @@ Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package. The product (the CUDA library and its
 Python binding) never calls it and shares no code with it.
 
-The arithmetic lives in ``attention_oracle.c`` (plain loops in double
-precision; see its header for the definition it follows and the passages of
-the pages it cites). This module compiles it with gcc and marshals arguments.
+The arithmetic lives in ``attention_oracle.c`` (forward) and
+``attention_bwd_oracle.c`` (gradients), plain loops in double precision; see
+their headers for the definitions they follow and the passages of the pages
+they cite. This module compiles them with gcc and marshals arguments.
 """
 
 from __future__ import annotations
@@ -19,7 +20,7 @@ import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "attention_oracle.c")
+_SRCS = [os.path.join(_HERE, "attention_oracle.c"), os.path.join(_HERE, "attention_bwd_oracle.c")]
 _LIB = os.path.join(_HERE, "liboracle.so")
 
 FP16, BF16 = 0, 1
@@ -30,10 +31,11 @@ _lib = None
 
 def build(force: bool = False) -> str:
     """Compile the oracle (plain gcc, no fast-math) next to its source."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+    if (force or not os.path.exists(_LIB)
+            or os.path.getmtime(_LIB) < max(os.path.getmtime(s) for s in _SRCS)):
         tmp = _LIB + f".tmp{os.getpid()}"
         subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
-                               "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"])
+                               "-fno-fast-math", "-ffp-contract=off", *_SRCS, "-o", tmp, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -50,6 +52,13 @@ def _load():
             ctypes.c_double, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
             ctypes.c_void_p, ctypes.c_int64,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int]
+        lib.oracle_attention_bwd.restype = ctypes.c_int
+        lib.oracle_attention_bwd.argtypes = [
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+            ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_int64, ctypes.c_double, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_int]
         lib.oracle_fp16_to_double.restype = ctypes.c_double
         lib.oracle_fp16_to_double.argtypes = [ctypes.c_uint16]
         lib.oracle_bf16_to_double.restype = ctypes.c_double
@@ -109,3 +118,38 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float,
     if return_p:
         return O, LSE, P
     return O, LSE
+
+
+def attention_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, do: torch.Tensor,
+                  scale: float, mask="none", window=(0, 0), kv_heads=None,
+                  nthreads: int | None = None):
+    """fp64 gradients of the attention forward over 16-bit CPU tensors, for an
+    upstream gradient ``do`` of O: Q and dO (B, H, Nq, d), K and V (B, Hk, Nk, d).
+
+    ``kv_heads`` lists K/V heads b*Hk + hk (default: all). Returns float64 numpy
+    arrays dQ (n, H/Hk, Nq, d) -- the query heads reading each listed K/V head, in
+    order -- and dK, dV (n, Nk, d).
+    """
+    lib = _load()
+    B, H, Nq, d = q.shape
+    Hk, N = k.shape[1], k.shape[2]
+    assert k.shape == (B, Hk, N, d) and v.shape == k.shape and do.shape == q.shape
+    assert q.dtype == k.dtype == v.dtype == do.dtype
+    dt = FP16 if q.dtype == torch.float16 else BF16
+    if kv_heads is None:
+        kv_heads = list(range(B * Hk))
+    kv = np.ascontiguousarray(np.array(kv_heads, dtype=np.int64).reshape(-1))
+    n, group = len(kv), H // Hk
+    dQ = np.zeros((n, group, Nq, d), dtype=np.float64)
+    dK = np.zeros((n, N, d), dtype=np.float64)
+    dV = np.zeros((n, N, d), dtype=np.float64)
+    qb, kb, vb, db = _bits(q), _bits(k), _bits(v), _bits(do)
+    if nthreads is None:
+        nthreads = len(os.sched_getaffinity(0))
+    rc = lib.oracle_attention_bwd(
+        qb.ctypes.data, kb.ctypes.data, vb.ctypes.data, db.ctypes.data, dt, B, H, Hk, Nq, N, d,
+        float(scale), MASKS[mask], int(window[0]), int(window[1]), kv.ctypes.data, n,
+        dQ.ctypes.data, dK.ctypes.data, dV.ctypes.data, int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_attention_bwd rejected its arguments")
+    return dQ, dK, dV
