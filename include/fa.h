@@ -165,14 +165,50 @@ fa_status fa_forward_splitkv_static(const void *Q, const void *K, const void *V,
                                     int64_t window_left, int64_t window_right, fa_dtype dtype,
                                     int64_t num_splits, void *stream);
 
+/*
+ * fa_backward -- gradients of the forward pass: given Q, K, V, the forward's
+ * O and LSE (as fa_forward / fa_forward_gqa wrote them) and dO, the gradient
+ * of a loss with respect to O, writes dQ, dK and dV. The forward keeps only O
+ * and the row statistics; like the method of "ai6s.net/6af30f4d40858c2d8819b6d5"
+ * §2.4 ("重计算(Recomputation)与反向传播"), this call recomputes the scores and
+ * probabilities tile by tile from them instead of storing P. With
+ * D_i = sum_c dO_ic O_ic and P_ij = exp(scale q_i.k_j - LSE_i) on visible keys:
+ *   dV_j = sum_i P_ij dO_i,  dS_ij = P_ij (dO_i . V_j - D_i),
+ *   dQ_i = scale sum_j dS_ij K_j,  dK_j = scale sum_i dS_ij Q_i,
+ * dK and dV of a K/V head summing over every query head that reads it.
+ *
+ * Layout: Q, O, dO and dQ are contiguous B x H x N x d; K, V, dK and dV are
+ * B x H_kv x N x d (H_kv divides H); LSE is B x H x N float32; all in `dtype`
+ * except LSE, on the current device, 16-byte aligned. Queries and keys share
+ * positions (as in fa_forward); the mask arguments are those of fa_forward.
+ * `workspace` is caller-owned device memory of at least
+ * fa_backward_workspace_bytes(B, H, N, d) bytes (two fp32 row terms per query
+ * row), 16-byte aligned; its contents on entry do not matter. dQ, dK, dV and
+ * the workspace overlap no input and no other output. The results are
+ * deterministic: no atomics, fixed summation order.
+ *
+ * Errors: as fa_forward, plus FA_ERR_INVALID_ARG for a missing or small
+ * workspace. Asynchronous on `stream` (three kernel launches: row terms, dK/dV,
+ * dQ); timeouts are reported by fa_sync_status.
+ */
+fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                      const float *LSE, void *dQ, void *dK, void *dV, int64_t B, int64_t H,
+                      int64_t H_kv, int64_t N, int64_t d, float scale, fa_mask_mode mask_mode,
+                      int64_t window_left, int64_t window_right, fa_dtype dtype, void *workspace,
+                      size_t workspace_bytes, void *stream);
+
+/* Workspace bytes fa_backward needs (0 for invalid sizes). */
+size_t fa_backward_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d);
+
 /* Static, NUL-terminated description of a status code. Never NULL. */
 const char *fa_status_string(fa_status status);
 
 /*
  * fa_sync_status -- synchronise `stream`, then read and clear the device
  * status word of the current device. Returns FA_ERR_TIMEOUT if any kernel
- * since the last call gave up on a bounded wait, FA_ERR_CUDA if the
- * synchronisation itself failed, else FA_OK.
+ * since the last call gave up on a bounded wait, FA_ERR_UNSUPPORTED if a
+ * kernel reported a shared-memory layout it cannot use (it then did
+ * nothing), FA_ERR_CUDA if the synchronisation itself failed, else FA_OK.
  */
 fa_status fa_sync_status(void *stream);
 

@@ -1,4 +1,4 @@
-"""GB300 (sm_103a) FlashAttention forward: C-ABI library libfa.so + Python binding."""
+"""GB300 (sm_103a) FlashAttention forward and backward: C-ABI library libfa.so + Python binding."""
 
 from .binding import (FA_DTYPE_BF16, FA_DTYPE_FP16, FA_ERR_CUDA, FA_ERR_INVALID_ARG,  # noqa: F401
                       FA_ERR_TIMEOUT, FA_ERR_UNSUPPORTED, FA_MASK_CAUSAL, FA_MASK_NONE,
@@ -8,3 +8,4 @@ from .binding import (FA_DTYPE_BF16, FA_DTYPE_FP16, FA_ERR_CUDA, FA_ERR_INVALID_
 from .binding import (FA_SPLITKV_STATIC_SCRATCH_BYTES, fa_forward_splitkv,  # noqa: F401
                       fa_forward_splitkv_static, fa_splitkv_default_splits,
                       fa_splitkv_workspace_bytes)
+from .binding import backward, fa_backward, fa_backward_workspace_bytes  # noqa: F401

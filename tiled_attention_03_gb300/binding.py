@@ -1,7 +1,7 @@
 """Python binding of the C ABI in include/fa.h (libfa.so), via ctypes.
 
-Argument marshalling only: every step of the attention forward pass runs in
-the library's CUDA kernel. PyTorch supplies device memory and streams. There
+Argument marshalling only: every step of the attention forward and backward
+passes runs in the library's CUDA kernels. PyTorch supplies device memory and streams. There
 is no fallback: if the library is missing or the device is unsupported, the
 calls raise.
 """
@@ -68,6 +68,12 @@ def load_library(path: str = LIB) -> ctypes.CDLL:
     lib.fa_splitkv_workspace_bytes.argtypes = [ctypes.c_int64] * 5
     lib.fa_splitkv_default_splits.restype = ctypes.c_int64
     lib.fa_splitkv_default_splits.argtypes = [ctypes.c_int64] * 5
+    lib.fa_backward.restype = ctypes.c_int
+    lib.fa_backward.argtypes = [ctypes.c_void_p] * 9 + [ctypes.c_int64] * 5 + [
+        ctypes.c_float, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+        ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    lib.fa_backward_workspace_bytes.restype = ctypes.c_size_t
+    lib.fa_backward_workspace_bytes.argtypes = [ctypes.c_int64] * 4
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_status_string.argtypes = [ctypes.c_int]
     lib.fa_sync_status.restype = ctypes.c_int
@@ -260,3 +266,49 @@ def fa_forward_splitkv_static(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                                        _stream_handle(stream))
     if rc != FA_OK:
         raise FaError(rc)
+
+
+def fa_backward_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return load_library().fa_backward_workspace_bytes(B, H, N, d)
+
+
+def fa_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                do: torch.Tensor, lse: torch.Tensor, dq: torch.Tensor, dk: torch.Tensor,
+                dv: torch.Tensor, scale: float, mask_mode=FA_MASK_NONE, window_left: int = 0,
+                window_right: int = 0, workspace: torch.Tensor | None = None,
+                stream=None) -> None:
+    """Enqueue fa_backward: q, o, do, dq (B, H, N, d); k, v, dk, dv (B, H_kv, N, d);
+    lse (B, H, N) float32 from the forward. Without a workspace tensor one is
+    taken from PyTorch's caching allocator."""
+    lib = load_library()
+    _check(q, k, v, o, lse)
+    for t, like in ((do, q), (dq, q), (dk, k), (dv, k)):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != q.dtype or t.shape != like.shape:
+            raise FaError(FA_ERR_INVALID_ARG, "fa_backward")
+    B, H, N, d = q.shape
+    need = fa_backward_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise FaError(FA_ERR_INVALID_ARG, "fa_backward")
+    rc = lib.fa_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                         lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                         B, H, k.shape[1], N, d, float(scale), _MASKS[mask_mode],
+                         int(window_left), int(window_right), _DTYPES[q.dtype],
+                         workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                         _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_backward")
+
+
+def backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+             lse: torch.Tensor, do: torch.Tensor, scale: float | None = None, mask="none",
+             window=(0, 0), stream=None):
+    """Attention backward on device tensors: returns (dQ, dK, dV) for the forward
+    that produced (o, lse) from (q, k, v) and the upstream gradient do."""
+    if scale is None:
+        scale = q.shape[-1] ** -0.5
+    q, k, v, o, lse, do = (t.contiguous() for t in (q, k, v, o, lse, do))
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fa_backward(q, k, v, o, do, lse, dq, dk, dv, scale, mask, window[0], window[1], None, stream)
+    return dq, dk, dv

@@ -15,7 +15,7 @@ LIB = os.path.join(PKG, "libfa.so")
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-O3", "-std=c++17", "-lineinfo",
-    "-Xcompiler", "-fPIC", "-shared",
+    "-Xcompiler", "-fPIC",
 ]
 
 
@@ -41,14 +41,32 @@ def nvcc() -> str:
 
 
 def build_library(force: bool = False, verbose: bool = False) -> str:
+    """Compile each translation unit in parallel, then link the shared library."""
     if not force and up_to_date():
         return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *NVCC_FLAGS, "-I", INCLUDE, "-I", CSRC, *_sources(), "-o", tmp]
-    if verbose:
-        print(" ".join(cmd))
-    subprocess.check_call(cmd)
-    os.replace(tmp, LIB)
+    tag = f".tmp{os.getpid()}"
+    objs, procs = [], []
+    for src in _sources():
+        obj = os.path.join(CSRC, os.path.basename(src)[:-3] + tag + ".o")
+        cmd = [nvcc(), *NVCC_FLAGS, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
+        if verbose:
+            print(" ".join(cmd))
+        objs.append(obj)
+        procs.append(subprocess.Popen(cmd))
+    failed = [p.wait() for p in procs]
+    try:
+        if any(failed):
+            raise subprocess.CalledProcessError(max(failed), "nvcc")
+        tmp = LIB + tag
+        cmd = [nvcc(), "-shared", "-gencode", "arch=compute_103a,code=sm_103a", *objs, "-o", tmp]
+        if verbose:
+            print(" ".join(cmd))
+        subprocess.check_call(cmd)
+        os.replace(tmp, LIB)
+    finally:
+        for o in objs:
+            if os.path.exists(o):
+                os.remove(o)
     return LIB
 
 

@@ -13,6 +13,7 @@
 #include "fa.h"
 #include "fa_combine.cuh"
 #include "fa_fwd_kernel.cuh"
+#include "fa_host.h"
 
 namespace {
 
@@ -205,7 +206,7 @@ struct Call {
     void *stream;
 };
 
-size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+using fa_host::align256;
 
 // Workspace of a key-split call: partial LSEs, then partial outputs, fp32.
 size_t splitkv_bytes(int64_t rows, int64_t d, int64_t splits) {
@@ -399,6 +400,31 @@ fa_status run_forward(const Call &c) {
 
 }  // namespace
 
+namespace fa_host {
+
+DeviceInfo device_info(int dev) {
+    DeviceInfo info{cudaErrorInvalidDevice, 0, 0, 0, nullptr, nullptr};
+    DeviceState *s = device_state(dev);
+    if (s == nullptr) return info;
+    info.err = s->init_err;
+    info.cc_major = s->cc_major;
+    info.cc_minor = s->cc_minor;
+    info.sm_count = s->sm_count;
+    info.status = s->status;
+    info.sched = s->sched;
+    return info;
+}
+bool aligned16(const void *p) { return ::aligned16(p); }
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) { return ::overlaps(a, na, b, nb); }
+bool on_device(const void *p, int dev) { return ::on_device(p, dev); }
+bool make_map(CUtensorMap *map, const void *base, bool bf16, int64_t BH, int64_t N, int64_t d) {
+    return ::make_map(map, base, bf16, BH, N, d);
+}
+uint64_t wait_budget() { return ::wait_budget(); }
+void count_launches(int64_t n) { g_launches += n; }
+
+}  // namespace fa_host
+
 extern "C" {
 
 const char *fa_status_string(fa_status s) {
@@ -506,7 +532,9 @@ fa_status fa_sync_status(void *stream) {
         cudaGetLastError();
         return FA_ERR_CUDA;
     }
-    return FA_ERR_TIMEOUT;
+    // The kernels store FA_ERR_TIMEOUT, or FA_ERR_UNSUPPORTED for a shared-memory
+    // layout they cannot use.
+    return st[0] == static_cast<unsigned>(FA_ERR_UNSUPPORTED) ? FA_ERR_UNSUPPORTED : FA_ERR_TIMEOUT;
 }
 
 }  // extern "C"

@@ -1,0 +1,224 @@
+// fa_bwd_api.cu -- the backward entry points of include/fa.h: argument checks,
+// workspace layout, TMA maps and the three launches (prep, dK/dV, dQ).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_bwd_kernel.cuh"
+#include "fa_host.h"
+
+namespace {
+
+using fa_host::align256;
+
+constexpr int kMaxDevices = 64;
+
+struct BwdDeviceState {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+};
+BwdDeviceState g_bwd_dev[kMaxDevices];
+
+// Opt in to the kernel's shared memory and check that the launch's registers
+// cover the setmaxnreg split (a split above them would make setmaxnreg.inc wait
+// forever).
+template <typename Kernel>
+cudaError_t configure_one(Kernel k, int smem) {
+    cudaFuncAttributes attr{};
+    cudaError_t e = cudaFuncGetAttributes(&attr, k);
+    if (e != cudaSuccess) return e;
+    if (attr.numRegs * fa::bwd::kThreads < fa::bwd::kRegsNeeded) return cudaErrorInvalidConfiguration;
+    return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+
+template <int D, bool BF16>
+cudaError_t configure_bwd() {
+    const cudaError_t e =
+        configure_one(fa::bwd::fa_bwd_dkdv_kernel<D, BF16>, fa::bwd::KvSmem<D>::kAlloc);
+    return e != cudaSuccess ? e
+                            : configure_one(fa::bwd::fa_bwd_dq_kernel<D, BF16>, fa::bwd::QSmem<D>::kAlloc);
+}
+
+cudaError_t bwd_device_init(int dev) {
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    BwdDeviceState &s = g_bwd_dev[dev];
+    std::call_once(s.once, [&s] {
+        cudaError_t e = configure_bwd<64, false>();
+        if (e == cudaSuccess) e = configure_bwd<64, true>();
+        if (e == cudaSuccess) e = configure_bwd<128, false>();
+        if (e == cudaSuccess) e = configure_bwd<128, true>();
+        s.err = e;
+    });
+    return s.err;
+}
+
+int64_t padded_rows(int64_t N) { return (N + fa::bwd::kTile - 1) / fa::bwd::kTile * fa::bwd::kTile; }
+
+// Workspace: the row terms L = LSE log2(e) and D = rowsum(dO O), fp32, rows padded
+// to 128 per head.
+struct BwdWorkspace {
+    size_t l, d, total;
+};
+BwdWorkspace bwd_layout(int64_t B, int64_t H, int64_t N) {
+    const size_t rows = static_cast<size_t>(B) * H * padded_rows(N);
+    BwdWorkspace w;
+    w.l = 0;
+    w.d = align256(rows * sizeof(float));
+    w.total = w.d + align256(rows * sizeof(float));
+    return w;
+}
+
+template <int D, bool BF16>
+cudaError_t launch_bwd(const fa::bwd::PrepParams &pp, const CUtensorMap &mq, const CUtensorMap &mk,
+                       const CUtensorMap &mv, const CUtensorMap &mdo, const fa::bwd::BwdParams &pkv,
+                       const fa::bwd::BwdParams &pq, int sms, cudaStream_t st) {
+    using namespace fa::bwd;
+    const int64_t prep_rows = static_cast<int64_t>(pp.BH) * pp.Npad;
+    fa_bwd_prep_kernel<D, BF16><<<static_cast<unsigned>((prep_rows + kPrepWarps - 1) / kPrepWarps),
+                                  kPrepWarps * 32, 0, st>>>(pp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // Persistent grids: one CTA per SM (each holds all of its SM's tensor memory).
+    fa_bwd_dkdv_kernel<D, BF16><<<static_cast<unsigned>(pkv.n_units < sms ? pkv.n_units : sms),
+                                  kThreads, KvSmem<D>::kAlloc, st>>>(mq, mk, mv, mdo, pkv);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    fa_bwd_dq_kernel<D, BF16><<<static_cast<unsigned>(pq.n_units < sms ? pq.n_units : sms),
+                                kThreads, QSmem<D>::kAlloc, st>>>(mq, mk, mv, mdo, pq);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t fa_backward_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d) {
+    if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
+    return bwd_layout(B, H, N).total;
+}
+
+fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                      const float *LSE, void *dQ, void *dK, void *dV, int64_t B, int64_t H,
+                      int64_t H_kv, int64_t N, int64_t d, float scale, fa_mask_mode mask_mode,
+                      int64_t window_left, int64_t window_right, fa_dtype dtype, void *workspace,
+                      size_t workspace_bytes, void *stream) {
+    using fa_host::aligned16;
+    using fa_host::on_device;
+    using fa_host::overlaps;
+    // ---- host-side checks: nothing is enqueued on failure
+    if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV || !workspace)
+        return FA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+    if (H_kv < 1 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
+    if (mask_mode != FA_MASK_NONE && mask_mode != FA_MASK_CAUSAL && mask_mode != FA_MASK_WINDOW)
+        return FA_ERR_INVALID_ARG;
+    if (mask_mode == FA_MASK_WINDOW && (window_left < 0 || window_right < 0))
+        return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+    const void *ptrs[] = {Q, K, V, O, dO, LSE, dQ, dK, dV, workspace};
+    for (const void *q : ptrs)
+        if (!aligned16(q)) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (N > (int64_t{1} << 29) || B * H > (int64_t{1} << 31)) return FA_ERR_UNSUPPORTED;
+    const int64_t BH = B * H, BHkv = B * H_kv;
+    const int64_t Npad = padded_rows(N);
+    const int64_t n_blk = Npad / fa::bwd::kTile;
+    if (BH * Npad > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+    const BwdWorkspace wl = bwd_layout(B, H, N);
+    if (workspace_bytes < wl.total) return FA_ERR_INVALID_ARG;
+    const size_t qb = static_cast<size_t>(BH) * N * d * 2;     // Q, O, dO, dQ
+    const size_t kb = static_cast<size_t>(BHkv) * N * d * 2;   // K, V, dK, dV
+    const size_t lb = static_cast<size_t>(BH) * N * sizeof(float);
+    // Outputs and workspace overlap no input and no other output.
+    const void *outs[] = {dQ, dK, dV, workspace};
+    const size_t out_n[] = {qb, kb, kb, wl.total};
+    const void *ins[] = {Q, K, V, O, dO, LSE};
+    const size_t in_n[] = {qb, kb, kb, qb, qb, lb};
+    for (int a = 0; a < 4; ++a) {
+        for (int b = 0; b < 6; ++b)
+            if (overlaps(outs[a], out_n[a], ins[b], in_n[b])) return FA_ERR_INVALID_ARG;
+        for (int b = a + 1; b < 4; ++b)
+            if (overlaps(outs[a], out_n[a], outs[b], out_n[b])) return FA_ERR_INVALID_ARG;
+    }
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+    const fa_host::DeviceInfo info = fa_host::device_info(dev);
+    if (info.err != cudaSuccess) return FA_ERR_CUDA;
+    if (!(info.cc_major == 10 && info.cc_minor == 3)) return FA_ERR_UNSUPPORTED;
+    if (bwd_device_init(dev) != cudaSuccess) return FA_ERR_CUDA;
+    for (const void *q : ptrs)
+        if (!on_device(q, dev)) return FA_ERR_INVALID_ARG;
+
+    const bool bf16 = dtype == FA_DTYPE_BF16;
+    CUtensorMap mq, mk, mv, mdo;
+    if (!fa_host::make_map(&mq, Q, bf16, BH, N, d) || !fa_host::make_map(&mk, K, bf16, BHkv, N, d) ||
+        !fa_host::make_map(&mv, V, bf16, BHkv, N, d) || !fa_host::make_map(&mdo, dO, bf16, BH, N, d))
+        return FA_ERR_CUDA;
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    fa::bwd::PrepParams pp{};
+    pp.O = O;
+    pp.dO = dO;
+    pp.LSE = LSE;
+    pp.Lw = reinterpret_cast<float *>(ws + wl.l);
+    pp.Dw = reinterpret_cast<float *>(ws + wl.d);
+    pp.BH = static_cast<int>(BH);
+    pp.N = static_cast<int>(N);
+    pp.Npad = static_cast<int>(Npad);
+
+    fa::bwd::BwdParams p{};
+    p.dQ = dQ;
+    p.dK = dK;
+    p.dV = dV;
+    p.Lw = pp.Lw;
+    p.Dw = pp.Dw;
+    p.N = static_cast<int>(N);
+    p.Npad = static_cast<int>(Npad);
+    p.H = static_cast<int>(H);
+    p.Hkv = static_cast<int>(H_kv);
+    p.group = static_cast<int>(H / H_kv);
+    p.BH = static_cast<int>(BH);
+    p.BHkv = static_cast<int>(BHkv);
+    p.n_blk = static_cast<int>(n_blk);
+    // visibility i - wl <= j <= i + wr, with N standing in for "unbounded"
+    int64_t wlv = N, wrv = N;
+    if (mask_mode == FA_MASK_CAUSAL) wrv = 0;
+    if (mask_mode == FA_MASK_WINDOW) {
+        wlv = window_left < N ? window_left : N;
+        wrv = window_right < N ? window_right : N;
+    }
+    p.wl = static_cast<int>(wlv);
+    p.wr = static_cast<int>(wrv);
+    p.scale = scale;
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    p.wait_budget_ns = fa_host::wait_budget();
+    p.status = info.status;
+    fa::bwd::BwdParams pkv = p, pq = p;
+    pkv.n_units = static_cast<int>(BHkv * n_blk);  // (K/V head, key block)
+    pq.n_units = static_cast<int>(BH * n_blk);     // (query head, query block)
+    pq.heavy_first = wrv < N ? 1 : 0;              // later blocks see more keys
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (d == 64)
+        e = bf16 ? launch_bwd<64, true>(pp, mq, mk, mv, mdo, pkv, pq, info.sm_count, st)
+                 : launch_bwd<64, false>(pp, mq, mk, mv, mdo, pkv, pq, info.sm_count, st);
+    else
+        e = bf16 ? launch_bwd<128, true>(pp, mq, mk, mv, mdo, pkv, pq, info.sm_count, st)
+                 : launch_bwd<128, false>(pp, mq, mk, mv, mdo, pkv, pq, info.sm_count, st);
+    if (e != cudaSuccess) return FA_ERR_CUDA;
+    fa_host::count_launches(3);
+    return FA_OK;
+}
+
+}  // extern "C"

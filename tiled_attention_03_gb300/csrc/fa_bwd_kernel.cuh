@@ -1,0 +1,986 @@
+// fa_bwd_kernel.cuh -- attention backward for sm_103a: dQ, dK, dV from Q, K, V,
+// the forward's O and LSE, and dO.
+//
+// Method. The forward keeps only O and the row statistics m, l (as LSE); the
+// backward recomputes the scores and probabilities block by block from them
+// instead of storing the N x N matrix P ("ai6s.net/6af30f4d40858c2d8819b6d5"
+// §2.4, and the recomputation row of its §4.1 table). With D_i = sum_c dO_ic O_ic
+// (equal to sum_j P_ij dP_ij, the row term of the softmax Jacobian):
+//     P_ij = exp(s_ij - LSE_i)            dV_j += P_ij dO_i
+//     dP_ij = dO_i . V_j                  dS_ij = P_ij (dP_ij - D_i)
+//     dK_j += scale dS_ij Q_i             dQ_i += scale dS_ij K_j
+// over the same 128 x 128 tiles and with the same causal / window block skip
+// as the forward (§3.3 (4) of the same page).
+//
+// GPU form: three kernels.
+//  * prep: per query row D_i and L_i = LSE_i log2(e) into a small workspace.
+//  * dK/dV: one work unit is a 128-key block of one K/V head; its CTA keeps K_j
+//    and V_j in shared memory and dK_j, dV_j in tensor memory, and walks every
+//    128-row query block (of every query head reading that K/V head) that sees
+//    one of its keys. Scores are formed transposed, S^T = K Q^T, so that the
+//    TMEM lane is the key: P^T and dS^T are written by the threads owning the
+//    key rows straight into TMEM as the A operand of dV += P^T dO and
+//    dK += dS^T Q.
+//  * dQ: one work unit is a 128-row query block of one head; it walks the key
+//    blocks that the rows see, recomputes S = Q K^T and dP = dO V^T, forms dS in
+//    TMEM and accumulates dQ += dS K there.
+// Computing dQ in its own pass costs two more matrix products (S and dP are
+// formed twice) but needs no atomics: on this GPU, adding the dQ tiles of every
+// key block into an fp32 buffer is bounded by the L2's reduction rate (about
+// 2.9 TB/s measured), which was slower than the extra products. dQ, dK and dV
+// are therefore deterministic.
+//
+// Both main kernels: 384 threads; warps 0-7 compute (two warpgroups splitting a
+// tile's 128 columns 64 / 64; thread = TMEM lane), warp 8 TMA producer, warp 9
+// MMA issuer, warp 10 second TMA producer (dQ kernel) or idle, warp 11 idle
+// (warpgroup 2's registers move to the compute warpgroups with setmaxnreg).
+// Every wait is bounded (global-timer budget); on expiry the CTA records the
+// failure in the status word, drains its copies and MMAs, frees its tensor memory
+// and returns.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+
+namespace fa {
+namespace bwd {
+
+constexpr int kTile = 128;     // rows of every tile (TMEM lanes)
+constexpr int kThreads = 384;
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kTma2Warp = 10;
+constexpr int kRegsCompute = 208;
+constexpr int kRegsControl = 88;
+constexpr int kRegsNeeded = 256 * kRegsCompute + 128 * kRegsControl;
+constexpr int kRegionBytes = 128 * 128;  // 128 rows x 128 B: one 64-column swizzle region
+constexpr uint32_t kTmemCols = 512;
+constexpr unsigned kStatusTimeout = 4;   // FA_ERR_TIMEOUT
+constexpr int kMaxDynSmem = 232448;      // per-CTA opt-in limit of sm_100-class GPUs
+enum : int { kRoleCompute = 1, kRoleTma = 2, kRoleMma = 3 };
+
+struct BwdParams {
+    void *dQ, *dK, *dV;       // dQ: B*H x N x d; dK, dV: B*H_kv x N x d (16-bit)
+    const float *Lw;          // B*H x Npad: LSE * log2(e); +inf on rows past N
+    const float *Dw;          // B*H x Npad: sum_c dO * O; 0 on rows past N
+    int N, Npad;              // keys = queries per head, N rounded up to 128
+    int H, Hkv, group;        // query heads, K/V heads, H / H_kv
+    int BH, BHkv;
+    int n_blk;                // 128-row blocks per head
+    int n_units;              // units of the kernel this struct is passed to
+    int wl, wr;               // key j visible to query i iff i - wl <= j <= i + wr
+    int heavy_first;          // dQ kernel: visit a head's query blocks from the last one
+    float scale_log2;         // scale * log2(e)
+    float scale;
+    unsigned long long wait_budget_ns;
+    unsigned int *status;     // [code, role, unit, block]
+};
+
+__device__ __forceinline__ void bwd_record_timeout(const BwdParams &p, volatile int *abort_flag,
+                                                   int role, int unit) {
+    *abort_flag = 1;
+    if (atomicCAS(p.status, 0u, kStatusTimeout) == 0u) {
+        p.status[1] = static_cast<unsigned>(role);
+        p.status[2] = static_cast<unsigned>(unit);
+        p.status[3] = blockIdx.x;
+        __threadfence();
+    }
+}
+
+// Query head (b * H + h) of the g-th query head reading K/V head bkv.
+__device__ __forceinline__ int group_head(int bkv, int g, const BwdParams &p) {
+    const int b = bkv / p.Hkv, hk = bkv - b * p.Hkv;
+    return b * p.H + hk * p.group + g;
+}
+
+// =============================================================================== dK / dV
+template <int D>
+struct KvSmem {
+    static constexpr int kStages = 2;                        // Q / dO / L / D ring
+    static constexpr int kTileBytes = kTile * D * 2;
+    static constexpr int kK = 0;
+    static constexpr int kV = kK + kTileBytes;
+    static constexpr int kStage = kV + kTileBytes;           // stage s: Q then dO
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kVec = kStage + kStages * kStageBytes;  // stage s: L[128], D[128]
+    static constexpr int kBar = kVec + kStages * 2 * kTile * 4;
+    static constexpr int kNumBars = 16;
+    static constexpr int kMisc = kBar + kNumBars * 8;        // tmem slot, abort flag
+    static constexpr int kBytes = kMisc + 16;
+    static constexpr int kAlloc = kBytes + 1024;             // slack to align the base to 1024 B
+    static_assert(kAlloc <= kMaxDynSmem, "shared memory");
+};
+
+enum : int {
+    kKvKVFull = 0,
+    kKvKVEmpty = 1,
+    kKvStFull = 2,   // + stage
+    kKvStEmpty = 4,  // + stage
+    kKvSFull = 6,
+    kKvDPFull = 7,
+    kKvDone = 8,
+    kKvPReady = 9,
+    kKvDSReady = 10,
+    kKvFree = 11,
+    kKvDrain = 12,
+};
+
+template <int D>
+struct KvTmem {
+    static constexpr uint32_t kS = 0;        // S^T, then P^T (16-bit) over columns 0-31, 64-95
+    static constexpr uint32_t kDP = 128;     // dP^T, then dS^T (16-bit) over 128-159, 192-223
+    static constexpr uint32_t kDV = 256;
+    static constexpr uint32_t kDK = 256 + D;
+    static_assert(D == 64 || D == 128, "head dim");
+};
+
+// A dK/dV unit: key block kb (keys k0 .. k0+127) of K/V head bkv; the query
+// blocks ib_lo .. ib_lo+nib-1 of each of the `group` query heads reading that
+// head see one of its keys: n_it = group * nib iterations. Units are numbered
+// head-major, so that the CTAs running at the same time share the Q and dO of
+// a few heads in L2.
+struct KvUnit {
+    int bkv, k0, ib_lo, nib, n_it;
+};
+
+__device__ __forceinline__ KvUnit decode_kv_unit(int u, const BwdParams &p) {
+    KvUnit U;
+    U.bkv = u / p.n_blk;
+    U.k0 = (u - U.bkv * p.n_blk) * kTile;
+    const int k1 = min(U.k0 + kTile, p.N) - 1;
+    const int q_lo = max(0, U.k0 - p.wr);
+    const int q_hi = min(p.N - 1, k1 + p.wl);
+    U.ib_lo = q_lo / kTile;
+    U.nib = q_hi / kTile - U.ib_lo + 1;
+    U.n_it = p.group * U.nib;
+    return U;
+}
+
+__device__ __forceinline__ void kv_unit_iter(const KvUnit &U, int n, const BwdParams &p, int &bh,
+                                             int &i0) {
+    const int g = n / U.nib;
+    bh = group_head(U.bkv, g, p);
+    i0 = (U.ib_lo + (n - g * U.nib)) * kTile;
+}
+
+// Per query block n of a unit the MMA warp issues
+//     S^T(n), dP^T(n) ... dV += P^T(n) dO(n) | S^T(n+1) | dK += dS^T(n) Q(n) | dP^T(n+1)
+// S^T(n+1) overwrites the P^T(n) that the dV product before it reads, and
+// dP^T(n+1) the dS^T(n) of the dK product before it: tcgen05.mma operations of
+// one thread execute in issue order, so each read precedes the later write.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                       const BwdParams p) {
+    using L = KvSmem<D>;
+    using T = KvTmem<D>;
+    constexpr int kRegions = D / 64;
+    constexpr int kStages = L::kStages;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sK = sbase + L::kK;
+    const uint32_t sV = sbase + L::kV;
+    const uint32_t bar0 = sbase + L::kBar;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
+    auto bar = [bar0](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+    auto sQ = [sbase](int st) { return sbase + L::kStage + st * L::kStageBytes; };
+    auto sdO = [sbase](int st) {
+        return sbase + L::kStage + st * L::kStageBytes + L::kTileBytes;
+    };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint64_t budget = p.wait_budget_ns;
+
+    // ---- setup
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == kTmaWarp * 32) {
+        mbar_init(bar(kKvKVFull), 1);
+        mbar_init(bar(kKvKVEmpty), 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar(kKvStFull + s), 1);
+            mbar_init(bar(kKvStEmpty + s), 1);
+        }
+        mbar_init(bar(kKvSFull), 1);
+        mbar_init(bar(kKvDPFull), 1);
+        mbar_init(bar(kKvDone), 1);
+        mbar_init(bar(kKvPReady), 256);
+        mbar_init(bar(kKvDSReady), 256);
+        mbar_init(bar(kKvFree), 256);
+        mbar_init(bar(kKvDrain), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmdO);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp >= 8) {
+      setmaxnreg_dec<kRegsControl>();
+      if (warp == kTmaWarp) {
+        // ================================================================ TMA producer
+        if (lane == 0) {
+            int it = 0, unit_iter = 0, kv_loads = 0;
+            bool ok = true;
+            int u = blockIdx.x;
+            for (; ok && u < p.n_units; u += gridDim.x, ++unit_iter) {
+                const KvUnit U = decode_kv_unit(u, p);
+                ok = mbar_wait_bounded(bar(kKvKVEmpty), (unit_iter & 1) ^ 1, abort_flag, budget);
+                if (!ok) break;
+                mbar_arrive_expect_tx(bar(kKvKVFull), 2 * L::kTileBytes);
+                for (int g = 0; g < kRegions; ++g) {
+                    tma_load_3d(sK + g * kRegionBytes, &tmK, bar(kKvKVFull), 64 * g, U.k0, U.bkv);
+                    tma_load_3d(sV + g * kRegionBytes, &tmV, bar(kKvKVFull), 64 * g, U.k0, U.bkv);
+                }
+                ++kv_loads;
+                // The next unit's K and V go to L2 now; its shared-memory load waits
+                // for this unit's last products.
+                if (u + static_cast<int>(gridDim.x) < p.n_units) {
+                    const KvUnit W = decode_kv_unit(u + gridDim.x, p);
+                    for (int g = 0; g < kRegions; ++g) {
+                        tma_prefetch_l2_3d(&tmK, 64 * g, W.k0, W.bkv);
+                        tma_prefetch_l2_3d(&tmV, 64 * g, W.k0, W.bkv);
+                    }
+                }
+                for (int n = 0; ok && n < U.n_it; ++n, ++it) {
+                    const int st = it % kStages;
+                    ok = mbar_wait_bounded(bar(kKvStEmpty + st), ((it / kStages) & 1) ^ 1,
+                                           abort_flag, budget);
+                    if (!ok) break;
+                    int bh, i0;
+                    kv_unit_iter(U, n, p, bh, i0);
+                    const uint32_t fb = bar(kKvStFull + st);
+                    mbar_arrive_expect_tx(fb, 2 * L::kTileBytes + 2 * kTile * 4);
+                    for (int g = 0; g < kRegions; ++g) {
+                        tma_load_3d(sQ(st) + g * kRegionBytes, &tmQ, fb, 64 * g, i0, bh);
+                        tma_load_3d(sdO(st) + g * kRegionBytes, &tmdO, fb, 64 * g, i0, bh);
+                    }
+                    const size_t vrow = static_cast<size_t>(bh) * p.Npad + i0;
+                    const uint32_t sv = sbase + L::kVec + st * 2 * kTile * 4;
+                    bulk_load(sv, p.Lw + vrow, kTile * 4, fb);
+                    bulk_load(sv + kTile * 4, p.Dw + vrow, kTile * 4, fb);
+                }
+            }
+            if (!ok) bwd_record_timeout(p, abort_flag, kRoleTma, u);
+            // Drain: no copy may still be landing in shared memory when the CTA exits.
+            if (kv_loads > 0)
+                mbar_wait_bounded(bar(kKvKVFull), (kv_loads - 1) & 1, nullptr, budget);
+            for (int s = 0; s < kStages; ++s) {
+                if (it > s) {
+                    const int last = it - 1 - ((it - 1 - s) % kStages);
+                    mbar_wait_bounded(bar(kKvStFull + s), (last / kStages) & 1, nullptr, budget);
+                }
+            }
+        }
+      } else if (warp == kMmaWarp) {
+        // ================================================================ MMA issuer
+        constexpr uint32_t idesc_kk = idesc_f16_ab(BF16, kTile, kTile, false, false);
+        constexpr uint32_t idesc_tn = idesc_f16_ab(BF16, kTile, D, false, true);
+        constexpr uint32_t kRegion16 = kRegionBytes >> 4;
+        constexpr uint32_t kKStep16 = (16 * 128) >> 4;  // 16 rows of 128 B
+        auto wait = [&](int b, uint32_t parity) {
+            return __all_sync(0xffffffffu, mbar_wait_bounded(bar(b), parity, abort_flag, budget));
+        };
+        auto commit = [&](int b) {
+            if (elect_one()) umma_commit(bar(b));
+            __syncwarp();
+        };
+        // C[128 x 128] = A B^T with A, B both K-major (rows of d): S^T = K Q^T, dP^T = V dO^T.
+        auto issue_kk = [&](uint32_t a_s, uint32_t b_s, uint32_t dcol) {
+            tc_fence_after();
+            const uint64_t da = sw128_desc(a_s, 16, 1024);
+            const uint64_t db = sw128_desc(b_s, 16, 1024);
+            if (elect_one()) {
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k >> 2) * kRegion16 + (k & 3) * 2;
+                    umma_f16_ss(tmem + dcol, da + off, db + off, idesc_kk, k > 0 ? 1u : 0u);
+                }
+            }
+            __syncwarp();
+        };
+        // C[128 x d] (+)= A^T B with A^T in TMEM (the query pairs of warpgroup w at
+        // columns acol + 64 w ...) and B MN-major in shared memory (rows = queries).
+        auto issue_tn = [&](uint32_t acol, uint32_t b_s, uint32_t dcol, bool accumulate) {
+            tc_fence_after();
+            const uint64_t db = sw128_desc(b_s, kRegionBytes, 1024);
+            const uint32_t acc0 = accumulate ? 1u : 0u;
+            if (elect_one()) {
+#pragma unroll
+                for (int k = 0; k < kTile / 16; ++k) {
+                    const uint32_t ac = acol + (k < 4 ? 8 * k : 64 + 8 * (k - 4));
+                    umma_f16_ts(tmem + dcol, tmem + ac, db + k * kKStep16, idesc_tn,
+                                k > 0 ? 1u : acc0);
+                }
+            }
+            __syncwarp();
+        };
+        int it = 0, unit_iter = 0;
+        bool ok = true;
+        int u = blockIdx.x;
+        for (; ok && u < p.n_units; u += gridDim.x, ++unit_iter) {
+            const KvUnit U = decode_kv_unit(u, p);
+            ok = wait(kKvKVFull, unit_iter & 1);
+            // prologue: S^T and dP^T of the unit's first query block
+            if (ok) ok = wait(kKvStFull + it % kStages, (it / kStages) & 1);
+            if (!ok) break;
+            issue_kk(sK, sQ(it % kStages), T::kS);
+            commit(kKvSFull);
+            issue_kk(sV, sdO(it % kStages), T::kDP);
+            commit(kKvDPFull);
+            for (int n = 0; ok && n < U.n_it; ++n, ++it) {
+                const int st = it % kStages;
+                ok = wait(kKvPReady, it & 1);
+                if (ok && n == 0 && unit_iter > 0) ok = wait(kKvFree, (unit_iter - 1) & 1);
+                if (!ok) break;
+                issue_tn(T::kS, sdO(st), T::kDV, n > 0);  // dV += P^T dO
+                if (n + 1 < U.n_it) {
+                    const int st1 = (it + 1) % kStages;
+                    ok = wait(kKvStFull + st1, ((it + 1) / kStages) & 1);
+                    if (!ok) break;
+                    issue_kk(sK, sQ(st1), T::kS);  // S^T(n+1)
+                    commit(kKvSFull);
+                }
+                ok = wait(kKvDSReady, it & 1);
+                if (!ok) break;
+                issue_tn(T::kDP, sQ(st), T::kDK, n > 0);  // dK += dS^T Q
+                commit(kKvStEmpty + st);                  // Q(n), dO(n), L, D no longer read
+                if (n + 1 < U.n_it) {
+                    issue_kk(sV, sdO((it + 1) % kStages), T::kDP);  // dP^T(n+1)
+                    commit(kKvDPFull);
+                }
+            }
+            if (!ok) break;
+            commit(kKvKVEmpty);  // K, V free once the unit's products complete
+            commit(kKvDone);     // and dK, dV are final
+        }
+        if (!ok && lane == 0) bwd_record_timeout(p, abort_flag, kRoleMma, u);
+        // Drain: every MMA this warp issued has completed before TMEM is freed.
+        if (elect_one()) umma_commit(bar(kKvDrain));
+        __syncwarp();
+        if (lane == 0) mbar_wait_bounded(bar(kKvDrain), 0, nullptr, budget);
+        __syncwarp();
+      }
+    } else {
+      setmaxnreg_inc<kRegsCompute>();
+      {
+        // ================================================================ compute warpgroups
+        const int wg = warp >> 2;                // query columns 64 wg .. 64 wg + 63
+        const int r = threadIdx.x & 127;         // key row
+        const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const float sl2 = p.scale_log2;
+        int it = 0, unit_iter = 0;
+        bool ok = true;
+        int u = blockIdx.x;
+        for (; ok && u < p.n_units; u += gridDim.x, ++unit_iter) {
+            const KvUnit U = decode_kv_unit(u, p);
+            const int key = U.k0 + r;
+            const bool key_ok = key < p.N;
+            for (int n = 0; n < U.n_it; ++n, ++it) {
+                const int st = it % kStages;
+                int bh, i0;
+                kv_unit_iter(U, n, p, bh, i0);
+                const float *vec = reinterpret_cast<const float *>(smem + L::kVec + st * 2 * kTile * 4);
+                const float *sLw = vec + 64 * wg;
+                const float *sDw = vec + kTile + 64 * wg;
+                // Element masks unless every (query, key) pair of the tile is visible.
+                const bool boundary = !(i0 + kTile - 1 - p.wl <= U.k0 && U.k0 + kTile - 1 <= i0 + p.wr);
+                const int q0 = i0 + 64 * wg;
+                // ---- P^T = 2^(S^T * scale * log2 e - LSE * log2 e)
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kKvSFull), it & 1, abort_flag, budget));
+                if (!ok) break;
+                tc_fence_after();
+                float pr[64];
+                {
+                    uint32_t a[32], b[32];
+                    tmem_ld32(tl + T::kS + 64 * wg, a);
+                    tmem_ld32(tl + T::kS + 64 * wg + 32, b);
+                    tmem_ld_wait(a);
+                    tmem_ld_wait(b);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        pr[c] = __uint_as_float(a[c]);
+                        pr[c + 32] = __uint_as_float(b[c]);
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < 64; c += 4) {
+                    const float4 lw = *reinterpret_cast<const float4 *>(sLw + c);
+                    ffma2(pr[c], pr[c + 1], sl2, sl2, -lw.x, -lw.y);
+                    ffma2(pr[c + 2], pr[c + 3], sl2, sl2, -lw.z, -lw.w);
+                }
+#pragma unroll
+                for (int c = 0; c < 64; ++c) pr[c] = ex2_approx(pr[c]);
+                if (boundary) {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) {
+                        const int q = q0 + c;
+                        if (q < key - p.wr || q > key + p.wl) pr[c] = 0.f;
+                    }
+                }
+                if (!key_ok) {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) pr[c] = 0.f;
+                }
+                {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) pk[e] = pack2<BF16>(pr[2 * e], pr[2 * e + 1]);
+                    tmem_st16(tl + T::kS + 64 * wg, pk);
+                    tmem_st16(tl + T::kS + 64 * wg + 16, pk + 16);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(bar(kKvPReady));
+                // ---- dS^T = P^T (dP^T - D)
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kKvDPFull), it & 1, abort_flag, budget));
+                if (!ok) break;
+                tc_fence_after();
+                {
+                    uint32_t a[32], b[32];
+                    tmem_ld32(tl + T::kDP + 64 * wg, a);
+                    tmem_ld32(tl + T::kDP + 64 * wg + 32, b);
+                    tmem_ld_wait(a);
+                    tmem_ld_wait(b);
+#pragma unroll
+                    for (int c = 0; c < 64; c += 4) {
+                        const float4 dw = *reinterpret_cast<const float4 *>(sDw + c);
+                        const uint32_t *src = c < 32 ? a + c : b + (c - 32);
+                        float d0 = __uint_as_float(src[0]), d1 = __uint_as_float(src[1]);
+                        float d2 = __uint_as_float(src[2]), d3 = __uint_as_float(src[3]);
+                        fadd2(d0, d1, -dw.x, -dw.y);
+                        fadd2(d2, d3, -dw.z, -dw.w);
+                        fmul2(d0, d1, pr[c], pr[c + 1]);
+                        fmul2(d2, d3, pr[c + 2], pr[c + 3]);
+                        pr[c] = d0;
+                        pr[c + 1] = d1;
+                        pr[c + 2] = d2;
+                        pr[c + 3] = d3;
+                    }
+                }
+                {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) pk[e] = pack2<BF16>(pr[2 * e], pr[2 * e + 1]);
+                    tmem_st16(tl + T::kDP + 64 * wg, pk);
+                    tmem_st16(tl + T::kDP + 64 * wg + 16, pk + 16);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(bar(kKvDSReady));
+            }
+            if (!ok) break;
+            // ---- epilogue of the unit: warpgroup 0 stores dV, warpgroup 1 dK * scale
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kKvDone), unit_iter & 1, abort_flag, budget));
+            if (!ok) break;
+            tc_fence_after();
+            {
+                const float f = wg == 0 ? 1.f : p.scale;
+                uint8_t *out = reinterpret_cast<uint8_t *>(wg == 0 ? p.dV : p.dK) +
+                               (static_cast<size_t>(U.bkv) * p.N + (key_ok ? key : 0)) * (D * 2);
+                const uint32_t col = wg == 0 ? T::kDV : T::kDK;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t a[32];
+                    tmem_ld32(tl + col + c * 32, a);
+                    tmem_ld_wait(a);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack2<BF16>(__uint_as_float(a[2 * e]) * f, __uint_as_float(a[2 * e + 1]) * f);
+                    if (key_ok) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(out + c * 64);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(kKvFree));
+        }
+        if (!ok && lane == 0) bwd_record_timeout(p, abort_flag, kRoleCompute, u);
+      }
+    }
+
+    // ---- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// =============================================================================== dQ
+template <int D>
+struct QSmem {
+    // K and V rings: K_j is read by S(j) and, later, by dQ += dS K_j, so its ring
+    // is one deeper than V's (V_j is read by dP(j) only).
+    static constexpr int kKStages = D == 64 ? 4 : 3;
+    static constexpr int kVStages = D == 64 ? 4 : 2;
+    static constexpr int kTileBytes = kTile * D * 2;
+    static constexpr int kQ = 0;
+    static constexpr int kdO = kQ + kTileBytes;
+    static constexpr int kK = kdO + kTileBytes;
+    static constexpr int kV = kK + kKStages * kTileBytes;
+    static constexpr int kBar = kV + kVStages * kTileBytes;
+    static constexpr int kNumBars = 24;
+    static constexpr int kMisc = kBar + kNumBars * 8;
+    static constexpr int kBytes = kMisc + 16;
+    static constexpr int kAlloc = kBytes + 1024;
+    static_assert(kAlloc <= kMaxDynSmem, "shared memory");
+};
+
+enum : int {
+    kQQFull = 0,
+    kQQEmpty = 1,
+    kQSFull = 2,     // + S buffer (2)
+    kQDPFull = 4,
+    kQDSReady = 5,
+    kQDone = 6,
+    kQFree = 7,
+    kQDrain = 8,
+    kQKFull = 9,     // + stage (<= 4)
+    kQKEmpty = 13,   // + stage
+    kQVFull = 17,    // + stage
+    kQVEmpty = 21,   // .. 24
+};
+
+template <int D>
+struct QTmem {
+    static constexpr uint32_t kS = 0;        // S buffers b = 0, 1 at 128 b; dS (16-bit) over their columns 0-31, 64-95
+    static constexpr uint32_t kDP = 256;
+    static constexpr uint32_t kDQ = 384;
+    static_assert(D == 64 || D == 128, "head dim");
+};
+
+// A dQ unit: query block (rows i0 .. i0+127) of query head bh and the key blocks
+// j0 .. j1 that hold a key one of its rows sees. Units are numbered head-major;
+// with heavy_first the blocks of a head run from the last one (most keys under
+// a causal mask) to the first.
+struct QUnit {
+    int bh, bkv, i0, j0, j1;
+};
+
+__device__ __forceinline__ QUnit decode_q_unit(int u, const BwdParams &p) {
+    QUnit U;
+    U.bh = u / p.n_blk;
+    int ib = u - U.bh * p.n_blk;
+    if (p.heavy_first) ib = p.n_blk - 1 - ib;
+    const int b = U.bh / p.H, h = U.bh - b * p.H;
+    U.bkv = b * p.Hkv + h / p.group;
+    U.i0 = ib * kTile;
+    const int i1 = min(U.i0 + kTile, p.N) - 1;
+    U.j0 = max(0, U.i0 - p.wl) / kTile;
+    U.j1 = min(p.N - 1, i1 + p.wr) / kTile;
+    return U;
+}
+
+// Per key block j (global iteration t) the MMA warp issues
+//     ... dQ += dS(t) K(t) | dP(t+1) | S(t+2)
+// with two S buffers, so that S(t+1) is ready when the compute warps finish
+// iteration t. S(t+2) reuses the buffer of S(t), whose dS the dQ product before
+// it reads (in-order execution), and dP(t+1) overwrites dP(t) only after the
+// compute warps reported dS(t) (and so have read dP(t)).
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                     const BwdParams p) {
+    using L = QSmem<D>;
+    using T = QTmem<D>;
+    constexpr int kRegions = D / 64;
+    constexpr int kKS = L::kKStages;
+    constexpr int kVS = L::kVStages;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sQ = sbase + L::kQ;
+    const uint32_t sdO = sbase + L::kdO;
+    const uint32_t bar0 = sbase + L::kBar;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
+    auto bar = [bar0](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+    auto sK = [sbase](int st) { return sbase + L::kK + st * L::kTileBytes; };
+    auto sV = [sbase](int st) { return sbase + L::kV + st * L::kTileBytes; };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint64_t budget = p.wait_budget_ns;
+
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == kTmaWarp * 32) {
+        mbar_init(bar(kQQFull), 1);
+        mbar_init(bar(kQQEmpty), 1);
+        mbar_init(bar(kQSFull + 0), 1);
+        mbar_init(bar(kQSFull + 1), 1);
+        mbar_init(bar(kQDPFull), 1);
+        mbar_init(bar(kQDSReady), 256);
+        mbar_init(bar(kQDone), 1);
+        mbar_init(bar(kQFree), 256);
+        mbar_init(bar(kQDrain), 1);
+        for (int s = 0; s < kKS; ++s) {
+            mbar_init(bar(kQKFull + s), 1);
+            mbar_init(bar(kQKEmpty + s), 1);
+        }
+        for (int s = 0; s < kVS; ++s) {
+            mbar_init(bar(kQVFull + s), 1);
+            mbar_init(bar(kQVEmpty + s), 1);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmdO);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp >= 8) {
+      setmaxnreg_dec<kRegsControl>();
+      if (warp == kTmaWarp || warp == kTma2Warp) {
+        // ================================================================ TMA producers
+        // warp 8: Q, dO and the K ring; warp 10: the V ring.
+        if (lane == 0) {
+            const bool kq = warp == kTmaWarp;
+            const int nst = kq ? kKS : kVS;
+            const int full0 = kq ? kQKFull : kQVFull, empty0 = kq ? kQKEmpty : kQVEmpty;
+            const CUtensorMap *map = kq ? &tmK : &tmV;
+            int t = 0, unit_iter = 0, q_loads = 0;
+            bool ok = true;
+            int u = blockIdx.x;
+            for (; ok && u < p.n_units; u += gridDim.x, ++unit_iter) {
+                const QUnit U = decode_q_unit(u, p);
+                if (kq) {
+                    ok = mbar_wait_bounded(bar(kQQEmpty), (unit_iter & 1) ^ 1, abort_flag, budget);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar(kQQFull), 2 * L::kTileBytes);
+                    for (int g = 0; g < kRegions; ++g) {
+                        tma_load_3d(sQ + g * kRegionBytes, &tmQ, bar(kQQFull), 64 * g, U.i0, U.bh);
+                        tma_load_3d(sdO + g * kRegionBytes, &tmdO, bar(kQQFull), 64 * g, U.i0, U.bh);
+                    }
+                    ++q_loads;
+                    // The next unit's Q and dO go to L2 now; their shared-memory load
+                    // waits for this unit's last products.
+                    if (u + static_cast<int>(gridDim.x) < p.n_units) {
+                        const QUnit W = decode_q_unit(u + gridDim.x, p);
+                        for (int g = 0; g < kRegions; ++g) {
+                            tma_prefetch_l2_3d(&tmQ, 64 * g, W.i0, W.bh);
+                            tma_prefetch_l2_3d(&tmdO, 64 * g, W.i0, W.bh);
+                        }
+                    }
+                }
+                for (int j = U.j0; ok && j <= U.j1; ++j, ++t) {
+                    const int st = t % nst;
+                    ok = mbar_wait_bounded(bar(empty0 + st), ((t / nst) & 1) ^ 1, abort_flag, budget);
+                    if (!ok) break;
+                    const uint32_t dst = kq ? sK(st) : sV(st);
+                    mbar_arrive_expect_tx(bar(full0 + st), L::kTileBytes);
+                    for (int g = 0; g < kRegions; ++g)
+                        tma_load_3d(dst + g * kRegionBytes, map, bar(full0 + st), 64 * g, j * kTile, U.bkv);
+                }
+            }
+            if (!ok) bwd_record_timeout(p, abort_flag, kRoleTma, u);
+            // Drain: no copy may still be landing in shared memory when the CTA exits.
+            if (q_loads > 0) mbar_wait_bounded(bar(kQQFull), (q_loads - 1) & 1, nullptr, budget);
+            for (int s = 0; s < nst; ++s) {
+                if (t > s) {
+                    const int last = t - 1 - ((t - 1 - s) % nst);
+                    mbar_wait_bounded(bar(full0 + s), (last / nst) & 1, nullptr, budget);
+                }
+            }
+        }
+      } else if (warp == kMmaWarp) {
+        // ================================================================ MMA issuer
+        constexpr uint32_t idesc_s = idesc_f16_ab(BF16, kTile, kTile, false, false);
+        constexpr uint32_t idesc_q = idesc_f16_ab(BF16, kTile, D, false, true);
+        constexpr uint32_t kRegion16 = kRegionBytes >> 4;
+        constexpr uint32_t kKStep16 = (16 * 128) >> 4;
+        auto wait = [&](int b, uint32_t parity) {
+            return __all_sync(0xffffffffu, mbar_wait_bounded(bar(b), parity, abort_flag, budget));
+        };
+        auto commit = [&](int b) {
+            if (elect_one()) umma_commit(bar(b));
+            __syncwarp();
+        };
+        // C[128 x 128] = A B^T, A (Q or dO) and B (K or V) K-major.
+        auto issue_kk = [&](uint32_t a_s, uint32_t b_s, uint32_t dcol) {
+            tc_fence_after();
+            const uint64_t da = sw128_desc(a_s, 16, 1024);
+            const uint64_t db = sw128_desc(b_s, 16, 1024);
+            if (elect_one()) {
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k >> 2) * kRegion16 + (k & 3) * 2;
+                    umma_f16_ss(tmem + dcol, da + off, db + off, idesc_s, k > 0 ? 1u : 0u);
+                }
+            }
+            __syncwarp();
+        };
+        // dQ (+)= dS K: dS in TMEM (keys of warpgroup w at columns acol + 64 w ...),
+        // K MN-major in shared memory (rows = keys).
+        auto issue_dq = [&](uint32_t acol, uint32_t k_s, bool accumulate) {
+            tc_fence_after();
+            const uint64_t db = sw128_desc(k_s, kRegionBytes, 1024);
+            const uint32_t acc0 = accumulate ? 1u : 0u;
+            if (elect_one()) {
+#pragma unroll
+                for (int k = 0; k < kTile / 16; ++k) {
+                    const uint32_t ac = acol + (k < 4 ? 8 * k : 64 + 8 * (k - 4));
+                    umma_f16_ts(tmem + T::kDQ, tmem + ac, db + k * kKStep16, idesc_q,
+                                k > 0 ? 1u : acc0);
+                }
+            }
+            __syncwarp();
+        };
+        auto kfull = [&](int t) { return wait(kQKFull + t % kKS, (t / kKS) & 1); };
+        auto vfull = [&](int t) { return wait(kQVFull + t % kVS, (t / kVS) & 1); };
+        int t = 0, unit_iter = 0;
+        bool ok = true;
+        int u = blockIdx.x;
+        for (; ok && u < p.n_units; u += gridDim.x, ++unit_iter) {
+            const QUnit U = decode_q_unit(u, p);
+            const int n = U.j1 - U.j0 + 1;
+            ok = wait(kQQFull, unit_iter & 1);
+            // prologue: S(t), dP(t), S(t+1)
+            if (ok) ok = kfull(t);
+            if (!ok) break;
+            issue_kk(sQ, sK(t % kKS), T::kS + (t & 1) * 128);
+            commit(kQSFull + (t & 1));
+            ok = vfull(t);
+            if (!ok) break;
+            issue_kk(sdO, sV(t % kVS), T::kDP);
+            commit(kQDPFull);
+            commit(kQVEmpty + t % kVS);
+            if (n > 1) {
+                ok = kfull(t + 1);
+                if (!ok) break;
+                issue_kk(sQ, sK((t + 1) % kKS), T::kS + ((t + 1) & 1) * 128);
+                commit(kQSFull + ((t + 1) & 1));
+            }
+            for (int x = 0; ok && x < n; ++x, ++t) {
+                ok = wait(kQDSReady, t & 1);
+                if (ok && x == 0 && unit_iter > 0) ok = wait(kQFree, (unit_iter - 1) & 1);
+                if (!ok) break;
+                issue_dq(T::kS + (t & 1) * 128, sK(t % kKS), x > 0);  // dQ += dS K
+                commit(kQKEmpty + t % kKS);
+                if (x + 1 < n) {
+                    ok = vfull(t + 1);
+                    if (!ok) break;
+                    issue_kk(sdO, sV((t + 1) % kVS), T::kDP);  // dP(t+1)
+                    commit(kQDPFull);
+                    commit(kQVEmpty + (t + 1) % kVS);
+                }
+                if (x + 2 < n) {
+                    ok = kfull(t + 2);
+                    if (!ok) break;
+                    issue_kk(sQ, sK((t + 2) % kKS), T::kS + (t & 1) * 128);  // S(t+2)
+                    commit(kQSFull + (t & 1));
+                }
+            }
+            if (!ok) break;
+            commit(kQQEmpty);  // Q, dO free once the unit's products complete
+            commit(kQDone);    // and dQ is final
+        }
+        if (!ok && lane == 0) bwd_record_timeout(p, abort_flag, kRoleMma, u);
+        if (elect_one()) umma_commit(bar(kQDrain));
+        __syncwarp();
+        if (lane == 0) mbar_wait_bounded(bar(kQDrain), 0, nullptr, budget);
+        __syncwarp();
+      }
+    } else {
+      setmaxnreg_inc<kRegsCompute>();
+      {
+        // ================================================================ compute warpgroups
+        const int wg = warp >> 2;                // key columns 64 wg .. 64 wg + 63
+        const int r = threadIdx.x & 127;         // query row
+        const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const float sl2 = p.scale_log2;
+        int t = 0, unit_iter = 0;
+        bool ok = true;
+        int u = blockIdx.x;
+        for (; ok && u < p.n_units; u += gridDim.x, ++unit_iter) {
+            const QUnit U = decode_q_unit(u, p);
+            const int i = U.i0 + r;
+            const size_t vrow = static_cast<size_t>(U.bh) * p.Npad + i;
+            const float lw = p.Lw[vrow], dw = p.Dw[vrow];
+            // visible keys of query i
+            const int lo_i = max(0, i - p.wl);
+            const int hi_i = min(p.N - 1, i + p.wr);
+            const int i1 = U.i0 + kTile - 1;
+            for (int j = U.j0; j <= U.j1; ++j, ++t) {
+                const int k0 = j * kTile;
+                // Element masks unless every pair of the tile is visible and every key exists.
+                const bool boundary = !(i1 - p.wl <= k0 && k0 + kTile - 1 <= U.i0 + p.wr &&
+                                        k0 + kTile <= p.N);
+                const int kc0 = k0 + 64 * wg;
+                const uint32_t tS = tl + T::kS + (t & 1) * 128 + 64 * wg;
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kQSFull + (t & 1)), (t >> 1) & 1,
+                                                               abort_flag, budget));
+                if (!ok) break;
+                tc_fence_after();
+                float pr[64];
+                {
+                    uint32_t a[32], b[32];
+                    tmem_ld32(tS, a);
+                    tmem_ld32(tS + 32, b);
+                    tmem_ld_wait(a);
+                    tmem_ld_wait(b);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        pr[c] = __uint_as_float(a[c]);
+                        pr[c + 32] = __uint_as_float(b[c]);
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < 64; c += 2) ffma2(pr[c], pr[c + 1], sl2, sl2, -lw, -lw);
+#pragma unroll
+                for (int c = 0; c < 64; ++c) pr[c] = ex2_approx(pr[c]);
+                if (boundary) {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) {
+                        const int key = kc0 + c;
+                        if (key < lo_i || key > hi_i) pr[c] = 0.f;
+                    }
+                }
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kQDPFull), t & 1, abort_flag, budget));
+                if (!ok) break;
+                tc_fence_after();
+                {
+                    uint32_t a[32], b[32];
+                    tmem_ld32(tl + T::kDP + 64 * wg, a);
+                    tmem_ld32(tl + T::kDP + 64 * wg + 32, b);
+                    tmem_ld_wait(a);
+                    tmem_ld_wait(b);
+#pragma unroll
+                    for (int c = 0; c < 64; c += 2) {
+                        const uint32_t *src = c < 32 ? a + c : b + (c - 32);
+                        float d0 = __uint_as_float(src[0]), d1 = __uint_as_float(src[1]);
+                        fadd2(d0, d1, -dw, -dw);
+                        fmul2(d0, d1, pr[c], pr[c + 1]);
+                        pr[c] = d0;
+                        pr[c + 1] = d1;
+                    }
+                }
+                {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) pk[e] = pack2<BF16>(pr[2 * e], pr[2 * e + 1]);
+                    tmem_st16(tS, pk);
+                    tmem_st16(tS + 16, pk + 16);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(bar(kQDSReady));
+            }
+            if (!ok) break;
+            // ---- epilogue: dQ * scale, rounded to 16 bit; warpgroup w stores columns w d/2 ..
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kQDone), unit_iter & 1, abort_flag, budget));
+            if (!ok) break;
+            tc_fence_after();
+            {
+                const bool store = i < p.N;
+                uint8_t *out = reinterpret_cast<uint8_t *>(p.dQ) +
+                               ((static_cast<size_t>(U.bh) * p.N + (store ? i : 0)) * D + wg * (D / 2)) * 2;
+#pragma unroll
+                for (int c = 0; c < D / 2; c += 32) {
+                    uint32_t a[32];
+                    tmem_ld32(tl + T::kDQ + wg * (D / 2) + c, a);
+                    tmem_ld_wait(a);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack2<BF16>(__uint_as_float(a[2 * e]) * p.scale,
+                                            __uint_as_float(a[2 * e + 1]) * p.scale);
+                    if (store) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(out + c * 2);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(kQFree));
+        }
+        if (!ok && lane == 0) bwd_record_timeout(p, abort_flag, kRoleCompute, u);
+      }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// =============================================================================== prep
+struct PrepParams {
+    const void *O, *dO;
+    const float *LSE;
+    float *Lw, *Dw;
+    int BH, N, Npad;
+};
+
+constexpr int kPrepWarps = 8;
+
+__device__ __forceinline__ float to_f32(uint16_t h, bool bf16) {
+    return bf16 ? __bfloat162float(__ushort_as_bfloat16(h)) : __half2float(__ushort_as_half(h));
+}
+
+// One warp per (head, padded row): D = sum_c dO * O in fp32 and L = LSE * log2(e)
+// (+inf for rows past N and for rows without a visible key, so that their
+// recomputed probabilities are 0).
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kPrepWarps * 32) fa_bwd_prep_kernel(const PrepParams p) {
+    const int row = blockIdx.x * kPrepWarps + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= p.BH * p.Npad) return;
+    const int bh = row / p.Npad, i = row - bh * p.Npad;
+    float dsum = 0.f;
+    if (i < p.N) {
+        const size_t base = (static_cast<size_t>(bh) * p.N + i) * D;
+        constexpr int kPer = D / 32;  // elements per lane
+        const uint16_t *o = reinterpret_cast<const uint16_t *>(p.O) + base + lane * kPer;
+        const uint16_t *g = reinterpret_cast<const uint16_t *>(p.dO) + base + lane * kPer;
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) dsum = fmaf(to_f32(g[e], BF16), to_f32(o[e], BF16), dsum);
+#pragma unroll
+        for (int s = 16; s > 0; s >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, s);
+    }
+    if (lane == 0) {
+        p.Dw[row] = i < p.N ? dsum : 0.f;
+        const float lse = i < p.N ? p.LSE[static_cast<size_t>(bh) * p.N + i] : -INFINITY;
+        p.Lw[row] = lse == -INFINITY ? INFINITY : lse * 1.4426950408889634f;
+    }
+}
+
+}  // namespace bwd
+}  // namespace fa

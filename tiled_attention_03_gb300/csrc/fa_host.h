@@ -1,0 +1,34 @@
+// fa_host.h -- host-side helpers shared by the library's translation units
+// (internal; not part of the C ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace fa_host {
+
+// Facts about one device, looked up once: compute capability, SM count and the
+// device addresses of the status word and the scheduler counters.
+struct DeviceInfo {
+    cudaError_t err;
+    int cc_major, cc_minor, sm_count;
+    unsigned int *status;
+    unsigned int *sched;
+};
+
+// nullptr-free: err is cudaErrorInvalidDevice for an out-of-range ordinal.
+DeviceInfo device_info(int dev);
+bool aligned16(const void *p);
+bool overlaps(const void *a, size_t na, const void *b, size_t nb);
+bool on_device(const void *p, int dev);
+// 3-D TMA map over a contiguous BH x N x d 16-bit tensor: box 64 columns x 128
+// rows, 128-byte swizzle, rows past N read as zero.
+bool make_map(CUtensorMap *map, const void *base, bool bf16, int64_t BH, int64_t N, int64_t d);
+uint64_t wait_budget();
+void count_launches(int64_t n);
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace fa_host

@@ -107,6 +107,24 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Plain (untiled) bulk copy global -> shared of `bytes` (a multiple of 16, both
+// addresses 16-byte aligned), completion counted on mbarrier `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// Fire-and-forget vector add of four floats into global memory (16-byte aligned);
+// no value comes back, so the issuing thread never waits on it.
+__device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, float d) {
+    asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a),
+                 "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
 // Prefetch the 3-D box at these coordinates into L2 (no shared memory, no completion).
 __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap *map, int32_t c0, int32_t c1,
                                                    int32_t c2) {
@@ -254,6 +272,13 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, int M, int N, bool b
     return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
            ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
            (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Same with the A operand's major order chosen too (A MN-major: A is read from
+// a buffer whose contiguous direction is M).
+__host__ __device__ constexpr uint32_t idesc_f16_ab(bool bf16, int M, int N, bool a_mn_major,
+                                                    bool b_mn_major) {
+    return idesc_f16(bf16, M, N, b_mn_major) | ((a_mn_major ? 1u : 0u) << 15);
 }
 
 // ---------------------------------------------------------------- registers
