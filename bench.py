@@ -27,6 +27,7 @@ sys.path.insert(0, ROOT)
 import torch  # noqa: E402
 
 METRIC = "attn fwd TFLOP/s (% of GB300 BF16 tensor peak); tokens/s @B4 H32 N4096 d128"
+METRIC_BWD = "attn bwd TFLOP/s (10 N^2 d FLOPs per head: dQ, dK, dV with S recomputed)"
 WORKLOAD = "full_b4h32n4096d128"
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -186,23 +187,54 @@ def cpu_oracle_rate(w, min_seconds: float, max_units: int | None = None, slab=No
     return flops / dt / 1e12, cores, f"{len(units)} x (1 head, {min(128, rows)}-row block, all {w.N} keys)", dt
 
 
+def cpu_oracle_rate_bwd(w, min_seconds: float, max_heads: int | None = None):
+    """Time the fp64 gradient oracle on a sample of whole K/V heads (each with the
+    query heads reading it) of the workload's shape, on every core. Returns
+    (TFLOP/s, cores, sample, seconds)."""
+    import oracle
+    from tiled_attention_03_gb300.workloads import make_qkv, visible_pairs
+    cores = len(os.sched_getaffinity(0))
+    group = w.H // w.kv_heads
+    n = max(1, cores // group) if max_heads is None else max(1, min(max_heads, cores // group))
+    while True:
+        q, k, v = make_qkv(1, n * group, w.N, w.d, w.dtype, seed=w.seed, q_std=w.q_std, H_kv=n)
+        do = make_qkv(1, n * group, w.N, w.d, w.dtype, seed=w.seed + 10000)[0]
+        t0 = time.perf_counter()
+        oracle.attention_bwd(q, k, v, do, w.scale, {0: "none", 1: "causal", 2: "window"}[w.mask],
+                             (w.window_left, w.window_right), nthreads=cores)
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds or max_heads is not None or n >= 8 * cores:
+            break
+        n *= 2
+    flops = 10.0 * w.d * n * group * visible_pairs(w.N, w.mask, w.window_left, w.window_right)
+    return flops / dt / 1e12, cores, f"{n} K/V head(s) x {group} query head(s), all {w.N} rows", dt
+
+
 def run_reference(args, w):
     rank, world, _ = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), 0
     if rank != 0:
         return
-    slab = oracle_slab(w)
     n = len(os.sched_getaffinity(0))
+    if w.backward:
+        def sample_once():
+            return cpu_oracle_rate_bwd(w, 0.0, max_heads=n)
+    else:
+        slab = oracle_slab(w)
+
+        def sample_once():
+            return cpu_oracle_rate(w, 0.0, max_units=n, slab=slab)
     for _ in range(args.warmup):
-        cpu_oracle_rate(w, 0.0, max_units=n, slab=slab)
+        sample_once()
     flops_total, secs_total = 0.0, 0.0
     for _ in range(args.steps):
-        r, cores, sample, dt = cpu_oracle_rate(w, 0.0, max_units=n, slab=slab)
+        r, cores, sample, dt = sample_once()
         flops_total += r * 1e12 * dt
         secs_total += dt
     value = flops_total / secs_total / 1e12
     wall = secs_total
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "impl": "reference", "metric": METRIC_BWD if w.backward else METRIC, "value": value,
+        "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000 * wall / max(1, args.steps), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -250,6 +282,38 @@ def run_e2e(args, w, q_h, k_h, v_h, mask, stream, dev, world, flops):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
 
+def run_e2e_bwd(args, w, host, mask, stream, dev, world, flops):
+    """Backward through the public API (tiled_attention_03_gb300.backward) with
+    pinned host tensors: every step copies Q, K, V, O, LSE and dO to the device,
+    runs the backward and copies dQ, dK and dV back."""
+    import tiled_attention_03_gb300 as fa
+    pinned = [t.pin_memory() for t in host]
+
+    def run():
+        q, k, v, o, lse, do = (t.to(dev, non_blocking=True) for t in pinned)
+        grads = fa.backward(q, k, v, o, lse, do, w.scale, mask, (w.window_left, w.window_right))
+        outs = [torch.empty(g.shape, dtype=g.dtype, pin_memory=True) for g in grads]
+        for dst, g in zip(outs, grads):
+            dst.copy_(g, non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()
+        return outs
+
+    for _ in range(2):
+        run()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        run()
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / args.e2e_steps, world)
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    q, k = host[0], host[1]
+    d2h = (q.numel() + 2 * k.numel()) * q.element_size()
+    return {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -283,7 +347,21 @@ def main():
     mask = {0: "none", 1: "causal", 2: "window"}[w.mask]
     stream = torch.cuda.current_stream(dev)
 
-    if w.splits >= 0:
+    if w.backward:
+        # O and LSE from one forward, outside the timed region; a step is the backward.
+        from tiled_attention_03_gb300.workloads import workload_grad_output
+        splits = 1
+        fa.fa_forward_gqa(q, k, v, o, lse, w.scale, mask, w.window_left, w.window_right, stream)
+        do_h = workload_grad_output(w)
+        do = do_h.to(dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(fa.fa_backward_workspace_bytes(w.B, w.H, w.N, w.d), dtype=torch.uint8,
+                         device=dev)
+
+        def step():
+            fa.fa_backward(q, k, v, o, do, lse, dq, dk, dv, w.scale, mask, w.window_left,
+                           w.window_right, ws, stream)
+    elif w.splits >= 0:
         splits = w.splits or fa.fa_splitkv_default_splits(w.B, w.H, w.kv_heads, w.q_rows, w.N)
         ws = torch.empty(max(16, fa.fa_splitkv_workspace_bytes(w.B, w.H, w.q_rows, w.d, splits)),
                          dtype=torch.uint8, device=dev)
@@ -327,11 +405,14 @@ def main():
     ms_total = max_over_ranks(ms_local, world)
     ms_step = ms_total / args.steps
     value = job_throughput(world, flops, ms_step)
-    kernel_ms = ms_local / args.steps  # one launch per step on this stream
+    kernel_ms = ms_local / args.steps  # the step's launches, all on this stream
 
     # ---- end to end through the public API with pinned host buffers
     e2e = None
-    if args.e2e_steps > 0:
+    if args.e2e_steps > 0 and w.backward:
+        host = [q_h, k_h, v_h, o.cpu(), lse.cpu(), do_h]
+        e2e = run_e2e_bwd(args, w, host, mask, stream, dev, world, flops)
+    elif args.e2e_steps > 0:
         e2e = run_e2e(args, w, q_h, k_h, v_h, mask, stream, dev, world, flops)
 
     if rank == 0:
@@ -342,12 +423,17 @@ def main():
         tensor_bound = flops / nbytes > peak_tf * 1e12 / (peak_gbs * 1e9)
         traffic = measured_traffic(w.name)
         cpu = None
-        if args.cpu_seconds > 0:
+        if args.cpu_seconds > 0 and w.backward:
+            cpu_v, cores, sample, _ = cpu_oracle_rate_bwd(w, args.cpu_seconds)
+            cpu = {"value": cpu_v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                   "sample": sample}
+        elif args.cpu_seconds > 0:
             cpu_v, cores, sample, _ = cpu_oracle_rate(w, args.cpu_seconds)
             cpu = {"value": cpu_v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                    "sample": sample}
         line = {
-            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "metric": METRIC_BWD if w.backward else METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype_name, "data": "synthetic",
@@ -368,8 +454,9 @@ def main():
                           "frac": nbytes / (kernel_ms * 1e-3) / 1e9 / peak_gbs,
                           "peak_source": f"{peak_src} copy bandwidth"}) | {
                 "traffic": traffic, "algorithmic_bytes": nbytes,
-                "kernel": f"fa_fwd_kernel<{w.d}, {w.dtype_name}>"
-                          + (f" + merge ({splits} key splits)" if splits > 1 else "")},
+                "kernel": (f"fa_bwd prep + dK/dV + dQ kernels <{w.d}, {w.dtype_name}>" if w.backward
+                           else f"fa_fwd_kernel<{w.d}, {w.dtype_name}>"
+                           + (f" + merge ({splits} key splits)" if splits > 1 else ""))},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches,

@@ -84,3 +84,43 @@ def test_python_binding_rejects_cpu_tensors():
     q = torch.zeros(1, 1, 8, 64, dtype=torch.float16)
     with pytest.raises(fa.FaError):
         fa.fa_forward(q, q, q, q.clone(), torch.zeros(1, 1, 8), 0.125)
+
+
+# fa_backward: Q K V O dO LSE dQ dK dV at distinct aligned fake addresses (never dereferenced)
+BW = dict(q=0x100000, k=0x200000, v=0x300000, o=0x400000, do=0x500000, lse=0x600000,
+          dq=0x700000, dk=0x800000, dv=0x900000, ws=0xA00000)
+
+
+def bwd_call(lib, B=1, H=2, Hk=2, N=16, d=64, scale=0.125, mask=0, wl=0, wr=0, dtype=0,
+             ws_bytes=None, **ptrs):
+    a = dict(BW, **ptrs)
+    if ws_bytes is None:
+        ws_bytes = lib.fa_backward_workspace_bytes(B, H, N, d)
+    return lib.fa_backward(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["dq"], a["dk"],
+                           a["dv"], B, H, Hk, N, d, scale, mask, wl, wr, dtype, a["ws"], ws_bytes, None)
+
+
+def test_backward_workspace_size(lib):
+    assert lib.fa_backward_workspace_bytes(0, 1, 1, 64) == 0
+    small = lib.fa_backward_workspace_bytes(1, 1, 1, 64)
+    big = lib.fa_backward_workspace_bytes(2, 4, 1000, 128)
+    assert 0 < small < big
+
+
+@pytest.mark.parametrize("kw", [
+    dict(q=0), dict(do=0), dict(lse=0), dict(dq=0), dict(dv=0), dict(ws=0),
+    dict(B=0), dict(N=0), dict(Hk=0), dict(Hk=3), dict(dtype=5), dict(mask=7),
+    dict(mask=2, wl=-1), dict(scale=0.0), dict(scale=float("nan")),
+    dict(q=0x100008), dict(dk=0x800004), dict(ws=0xA00002),
+    dict(dq=0x100000),            # dQ aliases Q
+    dict(dk=0x700000),            # dK overlaps dQ
+    dict(ws=0x500000),            # workspace overlaps dO
+    dict(ws_bytes=16),            # workspace too small
+])
+def test_backward_invalid_arguments(lib, kw):
+    assert bwd_call(lib, **kw) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("d", [32, 256])
+def test_backward_unsupported_head_dim(lib, d):
+    assert bwd_call(lib, d=d) == fa.FA_ERR_UNSUPPORTED

@@ -61,6 +61,13 @@ constexpr int kRegionBytes = 128 * 128;  // 128 rows x 128 B: one 64-column swiz
 constexpr uint32_t kTmemCols = 512;
 constexpr unsigned kStatusTimeout = 4;   // FA_ERR_TIMEOUT
 constexpr int kMaxDynSmem = 232448;      // per-CTA opt-in limit of sm_100-class GPUs
+// Of every 32 probabilities, how many are computed on the FMA pipe (exp2_poly2)
+// instead of the MUFU unit, which otherwise bounds the probability phase.
+#ifndef FA_BWD_POLY_EXP
+#define FA_BWD_POLY_EXP 0
+#endif
+constexpr int kPolyExp = FA_BWD_POLY_EXP;
+static_assert(kPolyExp % 2 == 0 && kPolyExp <= 32, "poly share");
 enum : int { kRoleCompute = 1, kRoleTma = 2, kRoleMma = 3 };
 
 struct BwdParams {
@@ -98,35 +105,47 @@ __device__ __forceinline__ int group_head(int bkv, int g, const BwdParams &p) {
 }
 
 // =============================================================================== dK / dV
+// Two rings: Q_i (with L of its rows), read by S^T(i) and last by dK += dS^T Q_i,
+// and dO_i (with D of its rows), read by dP^T(i) and last by dV += P^T dO_i,
+// which comes earlier. The Q ring is the deeper one: its slots are held longer.
 template <int D>
 struct KvSmem {
-    static constexpr int kStages = 2;                        // Q / dO / L / D ring
+    static constexpr int kQStages = D == 64 ? 4 : 3;
+    static constexpr int kOStages = D == 64 ? 4 : 2;
     static constexpr int kTileBytes = kTile * D * 2;
+    static constexpr int kVecBytes = kTile * 4;
     static constexpr int kK = 0;
     static constexpr int kV = kK + kTileBytes;
-    static constexpr int kStage = kV + kTileBytes;           // stage s: Q then dO
-    static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kVec = kStage + kStages * kStageBytes;  // stage s: L[128], D[128]
-    static constexpr int kBar = kVec + kStages * 2 * kTile * 4;
-    static constexpr int kNumBars = 16;
-    static constexpr int kMisc = kBar + kNumBars * 8;        // tmem slot, abort flag
+    static constexpr int kQ = kV + kTileBytes;                 // + s * kTileBytes
+    static constexpr int kO = kQ + kQStages * kTileBytes;
+    static constexpr int kL = kO + kOStages * kTileBytes;      // + s * kVecBytes
+    static constexpr int kDv = kL + kQStages * kVecBytes;
+    static constexpr int kBar = kDv + kOStages * kVecBytes;
+    static constexpr int kNumBars = 24;
+    static constexpr int kMisc = kBar + kNumBars * 8;          // tmem slot, abort flag
     static constexpr int kBytes = kMisc + 16;
-    static constexpr int kAlloc = kBytes + 1024;             // slack to align the base to 1024 B
-    static_assert(kAlloc <= kMaxDynSmem, "shared memory");
+    // Slack to align the base to 1024 B when it fits; without it (d = 128) the
+    // kernel checks the base's alignment itself.
+    static constexpr int kAlloc = kBytes + 1024 <= kMaxDynSmem ? kBytes + 1024 : kBytes;
+    static_assert(kBytes <= kMaxDynSmem, "shared memory");
 };
+
+constexpr unsigned kStatusLayout = 2;  // FA_ERR_UNSUPPORTED: shared memory base not 1024-aligned
 
 enum : int {
     kKvKVFull = 0,
     kKvKVEmpty = 1,
-    kKvStFull = 2,   // + stage
-    kKvStEmpty = 4,  // + stage
-    kKvSFull = 6,
-    kKvDPFull = 7,
-    kKvDone = 8,
-    kKvPReady = 9,
-    kKvDSReady = 10,
-    kKvFree = 11,
-    kKvDrain = 12,
+    kKvSFull = 2,
+    kKvDPFull = 3,
+    kKvDone = 4,
+    kKvPReady = 5,
+    kKvDSReady = 6,
+    kKvFree = 7,
+    kKvDrain = 8,
+    kKvQFull = 9,    // + Q stage (<= 4)
+    kKvQEmpty = 13,
+    kKvOFull = 17,   // + dO stage (<= 4)
+    kKvOEmpty = 21,  // .. 24
 };
 
 template <int D>
@@ -180,22 +199,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     using L = KvSmem<D>;
     using T = KvTmem<D>;
     constexpr int kRegions = D / 64;
-    constexpr int kStages = L::kStages;
+    constexpr int kQS = L::kQStages;
+    constexpr int kOS = L::kOStages;
 
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *smem = reinterpret_cast<uint8_t *>(smem_raw);
+    if constexpr (L::kAlloc > L::kBytes)
+        smem = reinterpret_cast<uint8_t *>(
+            (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_u32(smem);
+    // The 128-byte swizzle needs 1024-byte aligned tiles. Uniform exit before any
+    // barrier or tensor-memory allocation if the base is not.
+    if ((sbase & 1023u) != 0u) {
+        if (threadIdx.x == 0 && atomicCAS(p.status, 0u, kStatusLayout) == 0u) {
+            p.status[3] = blockIdx.x;
+            __threadfence();
+        }
+        return;
+    }
     const uint32_t sK = sbase + L::kK;
     const uint32_t sV = sbase + L::kV;
     const uint32_t bar0 = sbase + L::kBar;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
     auto bar = [bar0](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
-    auto sQ = [sbase](int st) { return sbase + L::kStage + st * L::kStageBytes; };
-    auto sdO = [sbase](int st) {
-        return sbase + L::kStage + st * L::kStageBytes + L::kTileBytes;
-    };
+    // Ring slot of query block `it` (counted over this CTA's whole sequence).
+    auto sQ = [sbase](int it) { return sbase + L::kQ + (it % kQS) * L::kTileBytes; };
+    auto sdO = [sbase](int it) { return sbase + L::kO + (it % kOS) * L::kTileBytes; };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -209,9 +239,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == kTmaWarp * 32) {
         mbar_init(bar(kKvKVFull), 1);
         mbar_init(bar(kKvKVEmpty), 1);
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar(kKvStFull + s), 1);
-            mbar_init(bar(kKvStEmpty + s), 1);
+        for (int s = 0; s < kQS; ++s) {
+            mbar_init(bar(kKvQFull + s), 1);
+            mbar_init(bar(kKvQEmpty + s), 1);
+        }
+        for (int s = 0; s < kOS; ++s) {
+            mbar_init(bar(kKvOFull + s), 1);
+            mbar_init(bar(kKvOEmpty + s), 1);
         }
         mbar_init(bar(kKvSFull), 1);
         mbar_init(bar(kKvDPFull), 1);
@@ -237,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (warp == kTmaWarp) {
         // ================================================================ TMA producer
         if (lane == 0) {
-            int it = 0, unit_iter = 0, kv_loads = 0;
+            int it = 0, unit_iter = 0, kv_loads = 0, q_loads = 0;
             bool ok = true;
             int u = blockIdx.x;
             for (; ok && u < p.n_units; u += gridDim.x, ++unit_iter) {
@@ -260,32 +294,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 for (int n = 0; ok && n < U.n_it; ++n, ++it) {
-                    const int st = it % kStages;
-                    ok = mbar_wait_bounded(bar(kKvStEmpty + st), ((it / kStages) & 1) ^ 1,
-                                           abort_flag, budget);
-                    if (!ok) break;
                     int bh, i0;
                     kv_unit_iter(U, n, p, bh, i0);
-                    const uint32_t fb = bar(kKvStFull + st);
-                    mbar_arrive_expect_tx(fb, 2 * L::kTileBytes + 2 * kTile * 4);
-                    for (int g = 0; g < kRegions; ++g) {
-                        tma_load_3d(sQ(st) + g * kRegionBytes, &tmQ, fb, 64 * g, i0, bh);
-                        tma_load_3d(sdO(st) + g * kRegionBytes, &tmdO, fb, 64 * g, i0, bh);
-                    }
                     const size_t vrow = static_cast<size_t>(bh) * p.Npad + i0;
-                    const uint32_t sv = sbase + L::kVec + st * 2 * kTile * 4;
-                    bulk_load(sv, p.Lw + vrow, kTile * 4, fb);
-                    bulk_load(sv + kTile * 4, p.Dw + vrow, kTile * 4, fb);
+                    // Q_i and L of its rows
+                    const int qs = it % kQS;
+                    ok = mbar_wait_bounded(bar(kKvQEmpty + qs), ((it / kQS) & 1) ^ 1, abort_flag, budget);
+                    if (!ok) break;
+                    uint32_t fb = bar(kKvQFull + qs);
+                    mbar_arrive_expect_tx(fb, L::kTileBytes + L::kVecBytes);
+                    for (int g = 0; g < kRegions; ++g)
+                        tma_load_3d(sQ(it) + g * kRegionBytes, &tmQ, fb, 64 * g, i0, bh);
+                    bulk_load(sbase + L::kL + qs * L::kVecBytes, p.Lw + vrow, L::kVecBytes, fb);
+                    ++q_loads;
+                    // dO_i and D of its rows
+                    const int os = it % kOS;
+                    ok = mbar_wait_bounded(bar(kKvOEmpty + os), ((it / kOS) & 1) ^ 1, abort_flag, budget);
+                    if (!ok) break;
+                    fb = bar(kKvOFull + os);
+                    mbar_arrive_expect_tx(fb, L::kTileBytes + L::kVecBytes);
+                    for (int g = 0; g < kRegions; ++g)
+                        tma_load_3d(sdO(it) + g * kRegionBytes, &tmdO, fb, 64 * g, i0, bh);
+                    bulk_load(sbase + L::kDv + os * L::kVecBytes, p.Dw + vrow, L::kVecBytes, fb);
                 }
             }
             if (!ok) bwd_record_timeout(p, abort_flag, kRoleTma, u);
             // Drain: no copy may still be landing in shared memory when the CTA exits.
+            // q_loads Q copies and `it` dO copies were issued (q_loads = it + 1 if the
+            // loop broke between the two).
             if (kv_loads > 0)
                 mbar_wait_bounded(bar(kKvKVFull), (kv_loads - 1) & 1, nullptr, budget);
-            for (int s = 0; s < kStages; ++s) {
+            for (int s = 0; s < kQS; ++s) {
+                if (q_loads > s) {
+                    const int last = q_loads - 1 - ((q_loads - 1 - s) % kQS);
+                    mbar_wait_bounded(bar(kKvQFull + s), (last / kQS) & 1, nullptr, budget);
+                }
+            }
+            for (int s = 0; s < kOS; ++s) {
                 if (it > s) {
-                    const int last = it - 1 - ((it - 1 - s) % kStages);
-                    mbar_wait_bounded(bar(kKvStFull + s), (last / kStages) & 1, nullptr, budget);
+                    const int last = it - 1 - ((it - 1 - s) % kOS);
+                    mbar_wait_bounded(bar(kKvOFull + s), (last / kOS) & 1, nullptr, budget);
                 }
             }
         }
@@ -337,33 +385,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         int u = blockIdx.x;
         for (; ok && u < p.n_units; u += gridDim.x, ++unit_iter) {
             const KvUnit U = decode_kv_unit(u, p);
+            auto qfull = [&](int i) { return wait(kKvQFull + i % kQS, (i / kQS) & 1); };
+            auto ofull = [&](int i) { return wait(kKvOFull + i % kOS, (i / kOS) & 1); };
             ok = wait(kKvKVFull, unit_iter & 1);
             // prologue: S^T and dP^T of the unit's first query block
-            if (ok) ok = wait(kKvStFull + it % kStages, (it / kStages) & 1);
+            if (ok) ok = qfull(it);
             if (!ok) break;
-            issue_kk(sK, sQ(it % kStages), T::kS);
+            issue_kk(sK, sQ(it), T::kS);
             commit(kKvSFull);
-            issue_kk(sV, sdO(it % kStages), T::kDP);
+            ok = ofull(it);
+            if (!ok) break;
+            issue_kk(sV, sdO(it), T::kDP);
             commit(kKvDPFull);
             for (int n = 0; ok && n < U.n_it; ++n, ++it) {
-                const int st = it % kStages;
                 ok = wait(kKvPReady, it & 1);
                 if (ok && n == 0 && unit_iter > 0) ok = wait(kKvFree, (unit_iter - 1) & 1);
                 if (!ok) break;
-                issue_tn(T::kS, sdO(st), T::kDV, n > 0);  // dV += P^T dO
+                issue_tn(T::kS, sdO(it), T::kDV, n > 0);  // dV += P^T dO
+                commit(kKvOEmpty + it % kOS);             // dO(n), D no longer read
                 if (n + 1 < U.n_it) {
-                    const int st1 = (it + 1) % kStages;
-                    ok = wait(kKvStFull + st1, ((it + 1) / kStages) & 1);
+                    ok = qfull(it + 1);
                     if (!ok) break;
-                    issue_kk(sK, sQ(st1), T::kS);  // S^T(n+1)
+                    issue_kk(sK, sQ(it + 1), T::kS);  // S^T(n+1)
                     commit(kKvSFull);
                 }
                 ok = wait(kKvDSReady, it & 1);
                 if (!ok) break;
-                issue_tn(T::kDP, sQ(st), T::kDK, n > 0);  // dK += dS^T Q
-                commit(kKvStEmpty + st);                  // Q(n), dO(n), L, D no longer read
+                issue_tn(T::kDP, sQ(it), T::kDK, n > 0);  // dK += dS^T Q
+                commit(kKvQEmpty + it % kQS);             // Q(n), L no longer read
                 if (n + 1 < U.n_it) {
-                    issue_kk(sV, sdO((it + 1) % kStages), T::kDP);  // dP^T(n+1)
+                    ok = ofull(it + 1);
+                    if (!ok) break;
+                    issue_kk(sV, sdO(it + 1), T::kDP);  // dP^T(n+1)
                     commit(kKvDPFull);
                 }
             }
@@ -394,12 +447,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int key = U.k0 + r;
             const bool key_ok = key < p.N;
             for (int n = 0; n < U.n_it; ++n, ++it) {
-                const int st = it % kStages;
                 int bh, i0;
                 kv_unit_iter(U, n, p, bh, i0);
-                const float *vec = reinterpret_cast<const float *>(smem + L::kVec + st * 2 * kTile * 4);
-                const float *sLw = vec + 64 * wg;
-                const float *sDw = vec + kTile + 64 * wg;
+                const float *sLw =
+                    reinterpret_cast<const float *>(smem + L::kL + (it % kQS) * L::kVecBytes) + 64 * wg;
+                const float *sDw =
+                    reinterpret_cast<const float *>(smem + L::kDv + (it % kOS) * L::kVecBytes) + 64 * wg;
                 // Element masks unless every (query, key) pair of the tile is visible.
                 const bool boundary = !(i0 + kTile - 1 - p.wl <= U.k0 && U.k0 + kTile - 1 <= i0 + p.wr);
                 const int q0 = i0 + 64 * wg;
@@ -427,7 +480,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ffma2(pr[c + 2], pr[c + 3], sl2, sl2, -lw.z, -lw.w);
                 }
 #pragma unroll
-                for (int c = 0; c < 64; ++c) pr[c] = ex2_approx(pr[c]);
+                for (int c = 0; c < 64; c += 2) {
+                    if ((c & 31) < kPolyExp) {
+                        exp2_poly2(pr[c], pr[c + 1]);
+                    } else {
+                        pr[c] = ex2_approx(pr[c]);
+                        pr[c + 1] = ex2_approx(pr[c + 1]);
+                    }
+                }
                 if (boundary) {
 #pragma unroll
                     for (int c = 0; c < 64; ++c) {
@@ -861,7 +921,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < 64; c += 2) ffma2(pr[c], pr[c + 1], sl2, sl2, -lw, -lw);
 #pragma unroll
-                for (int c = 0; c < 64; ++c) pr[c] = ex2_approx(pr[c]);
+                for (int c = 0; c < 64; c += 2) {
+                    if ((c & 31) < kPolyExp) {
+                        exp2_poly2(pr[c], pr[c + 1]);
+                    } else {
+                        pr[c] = ex2_approx(pr[c]);
+                        pr[c + 1] = ex2_approx(pr[c + 1]);
+                    }
+                }
                 if (boundary) {
 #pragma unroll
                     for (int c = 0; c < 64; ++c) {

@@ -48,6 +48,7 @@ class Workload:
     H_kv: int = 0  # K/V heads (grouped-query attention); 0 means H
     Nq: int = 0    # query rows per head when fewer than the N keys (the last Nq positions); 0 means N
     splits: int = -1  # key splits for the split-KV entry point (0: its default); -1: not split
+    backward: bool = False  # time the backward pass (dQ, dK, dV) instead of the forward
 
     @property
     def scale(self) -> float:
@@ -99,7 +100,17 @@ EXTRA_WORKLOADS = [
              0, 0, seed=8, H_kv=8, Nq=512, splits=0),
 ]
 
-BY_NAME = {w.name: w for w in WORKLOADS + EXTRA_WORKLOADS}
+# Backward pass on the bench shape (dO drawn after Q, K, V from the same generator).
+BWD_WORKLOADS = [
+    Workload("bwd_b4h32n4096d128", 4, 32, 4096, 128, torch.bfloat16, MASK_NONE, 0, 0, seed=9,
+             backward=True),
+    Workload("bwd_causal_b4h32n4096d128", 4, 32, 4096, 128, torch.bfloat16, MASK_CAUSAL, 0, 0,
+             seed=10, backward=True),
+    Workload("bwd_gqa_causal_b2h32kv8n4096d64", 2, 32, 4096, 64, torch.float16, MASK_CAUSAL, 0, 0,
+             seed=11, H_kv=8, backward=True),
+]
+
+BY_NAME = {w.name: w for w in WORKLOADS + EXTRA_WORKLOADS + BWD_WORKLOADS}
 
 
 def make_qkv(B: int, H: int, N: int, d: int, dtype: torch.dtype, seed: int,
@@ -119,6 +130,13 @@ def make_qkv(B: int, H: int, N: int, d: int, dtype: torch.dtype, seed: int,
 
 def workload_inputs(w: Workload):
     return make_qkv(w.B, w.H, w.N, w.d, w.dtype, w.seed, w.q_std, w.H_kv, w.Nq)
+
+
+def workload_grad_output(w: Workload):
+    """dO for a backward workload: N(0, 1) of Q's shape, from seed + 10000."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed + 10000)
+    return torch.randn(w.B, w.H, w.q_rows, w.d, generator=g, dtype=torch.float32).to(w.dtype)
 
 
 def sample_units(w: Workload, n: int = 16, block: int = 128, seed: int | None = None):
@@ -160,11 +178,18 @@ def visible_pairs(N: int, mask: int, wl: int, wr: int, Nq: int = 0) -> int:
 
 
 def algorithmic_flops(w: Workload) -> float:
-    return 4.0 * w.d * w.B * w.H * visible_pairs(w.N, w.mask, w.window_left, w.window_right, w.Nq)
+    """Forward: 2 products of 2 d FLOPs per visible pair. Backward: 5 (dV, dP, dQ,
+    dK and the recomputed S), i.e. 2.5x the forward."""
+    per_pair = 10.0 if w.backward else 4.0
+    return per_pair * w.d * w.B * w.H * visible_pairs(w.N, w.mask, w.window_left, w.window_right, w.Nq)
 
 
 def algorithmic_bytes(w: Workload) -> int:
-    """Q, K, V read once and O (16-bit) plus LSE (fp32) written once."""
+    """Forward: Q, K, V read once and O (16-bit) plus LSE (fp32) written once.
+    Backward: Q, K, V, O, dO and LSE read once, dQ, dK, dV written once."""
     q_elems = w.B * w.H * w.q_rows * w.d
     kv_elems = w.B * w.kv_heads * w.N * w.d
-    return (2 * q_elems + 2 * kv_elems) * 2 + w.B * w.H * w.q_rows * 4
+    rows = w.B * w.H * w.q_rows
+    if w.backward:
+        return (4 * q_elems + 4 * kv_elems) * 2 + rows * 4
+    return (2 * q_elems + 2 * kv_elems) * 2 + rows * 4
