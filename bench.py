@@ -282,6 +282,41 @@ def run_e2e(args, w, q_h, k_h, v_h, mask, stream, dev, world, flops):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
 
+def run_e2e_varlen(args, w, host, max_q, mask, stream, dev, world, flops):
+    """Variable-length forward through the public binding with pinned host tensors:
+    every step copies Q, K, V and cu_seqlens to the device, runs
+    fa_forward_varlen and copies O and LSE back."""
+    import tiled_attention_03_gb300 as fa
+    pinned = [t.pin_memory() for t in host]
+
+    def run():
+        q, k, v, cu = (t.to(dev, non_blocking=True) for t in pinned)
+        o = torch.empty_like(q)
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+        fa.fa_forward_varlen(q, k, v, o, lse, cu, cu, max_q, w.scale, mask, w.window_left,
+                             w.window_right)
+        oh = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        lh = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()
+
+    for _ in range(2):
+        run()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        run()
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / args.e2e_steps, world)
+    q = host[0]
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    d2h = q.numel() * q.element_size() + (q.numel() // w.d) * 4
+    return {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+
 def run_e2e_bwd(args, w, host, mask, stream, dev, world, flops):
     """Backward through the public API (tiled_attention_03_gb300.backward) with
     pinned host tensors: every step copies Q, K, V, O, LSE and dO to the device,
@@ -347,7 +382,19 @@ def main():
     mask = {0: "none", 1: "causal", 2: "window"}[w.mask]
     stream = torch.cuda.current_stream(dev)
 
-    if w.backward:
+    if w.varlen:
+        from tiled_attention_03_gb300.workloads import varlen_inputs, varlen_lengths
+        splits = 1
+        vq_h, vk_h, vv_h, cu_h = varlen_inputs(w)
+        vq, vk, vv, cu = vq_h.to(dev), vk_h.to(dev), vv_h.to(dev), cu_h.to(dev)
+        vo = torch.empty_like(vq)
+        vlse = torch.empty(vq.shape[:2], dtype=torch.float32, device=dev)
+        max_q = max(varlen_lengths(w))
+
+        def step():
+            fa.fa_forward_varlen(vq, vk, vv, vo, vlse, cu, cu, max_q, w.scale, mask,
+                                 w.window_left, w.window_right, stream)
+    elif w.backward:
         # O and LSE from one forward, outside the timed region; a step is the backward.
         from tiled_attention_03_gb300.workloads import workload_grad_output
         splits = 1
@@ -409,7 +456,10 @@ def main():
 
     # ---- end to end through the public API with pinned host buffers
     e2e = None
-    if args.e2e_steps > 0 and w.backward:
+    if args.e2e_steps > 0 and w.varlen:
+        e2e = run_e2e_varlen(args, w, [vq_h, vk_h, vv_h, cu_h], max_q, mask, stream, dev, world,
+                             flops)
+    elif args.e2e_steps > 0 and w.backward:
         host = [q_h, k_h, v_h, o.cpu(), lse.cpu(), do_h]
         e2e = run_e2e_bwd(args, w, host, mask, stream, dev, world, flops)
     elif args.e2e_steps > 0:
@@ -431,6 +481,8 @@ def main():
             cpu_v, cores, sample, _ = cpu_oracle_rate(w, args.cpu_seconds)
             cpu = {"value": cpu_v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                    "sample": sample}
+        in_t = (vq, vk, vv) if w.varlen else (q, k, v, do) if w.backward else (q, k, v)
+        in_bytes = sum(t.numel() * t.element_size() for t in in_t)
         line = {
             "metric": METRIC_BWD if w.backward else METRIC, "value": value, "unit": "TFLOP/s",
             "n_gpus": world,
@@ -441,9 +493,9 @@ def main():
                        "mask": mask, "seed": w.seed,
                        "parallelism": f"{world} independent replica(s), no collective",
                        "kv_heads": w.kv_heads,
-                       "l2": (f"inputs ({(q.numel() + k.numel() + v.numel()) * 2 / 1e6:.0f} MB) larger than L2, no flush"
-                              if (q.numel() + k.numel() + v.numel()) * 2 > 129e6 else "inputs smaller than L2, no flush")},
-            "tokens_per_s": world * w.B * w.q_rows / (ms_step * 1e-3),
+                       "l2": (f"inputs ({in_bytes / 1e6:.0f} MB) larger than L2, no flush"
+                              if in_bytes > 129e6 else "inputs smaller than L2, no flush")},
+            "tokens_per_s": world * (vq.shape[0] if w.varlen else w.B * w.q_rows) / (ms_step * 1e-3),
             "pct_of_peak": 100.0 * value / (world * peak_tf),
             "roofline": ({"bound": "tensor", "achieved": achieved, "peak": peak_tf,
                           "unit": "TFLOP/s", "frac": achieved / peak_tf,
@@ -455,6 +507,7 @@ def main():
                           "peak_source": f"{peak_src} copy bandwidth"}) | {
                 "traffic": traffic, "algorithmic_bytes": nbytes,
                 "kernel": (f"fa_bwd prep + dK/dV + dQ kernels <{w.d}, {w.dtype_name}>" if w.backward
+                           else f"fa_fwd_kernel<{w.d}, {w.dtype_name}, varlen>" if w.varlen
                            else f"fa_fwd_kernel<{w.d}, {w.dtype_name}>"
                            + (f" + merge ({splits} key splits)" if splits > 1 else ""))},
             "cpu_baseline": cpu,

@@ -166,6 +166,35 @@ fa_status fa_forward_splitkv_static(const void *Q, const void *K, const void *V,
                                     int64_t num_splits, void *stream);
 
 /*
+ * fa_forward_varlen -- attention forward over a batch of sequences of different
+ * lengths packed back to back (the variable-length batches that
+ * "ai6s.net/6af30f4d40858c2d8819b6d5" §4.2 lists among the cases an
+ * implementation has to handle). Sequence b owns query tokens
+ * cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and keys cu_seqlens_k[b] ..
+ * cu_seqlens_k[b+1]-1; each sequence is an independent fa_forward_gqa problem
+ * whose L_q queries stand at its last L_q key positions (as in
+ * fa_forward_splitkv), which is what the masks refer to.
+ *
+ * Layout (token-major): Q and O total_q x H x d, K and V total_k x H_kv x d, in
+ * `dtype`; LSE total_q x H float32; cu_seqlens_q and cu_seqlens_k are B + 1
+ * int32 on the device, non-decreasing from 0 to total_q / total_k. All on the
+ * current device; tensors 16-byte aligned. max_seqlen_q >= every L_q (rows
+ * past it are not computed). With a mask, every sequence needs L_q <= L_k;
+ * every sequence with queries needs L_k >= 1. The device arrays are read by
+ * the kernel, not checked on the host; offsets are clamped to the tensors, so
+ * inconsistent arrays give wrong results but no access outside them.
+ *
+ * Errors: as fa_forward. total_q = 0 or max_seqlen_q = 0 returns FA_OK with
+ * nothing read, written or enqueued (the pointers may then be NULL).
+ */
+fa_status fa_forward_varlen(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                            const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int64_t B,
+                            int64_t H, int64_t H_kv, int64_t total_q, int64_t total_k,
+                            int64_t max_seqlen_q, int64_t d, float scale, fa_mask_mode mask_mode,
+                            int64_t window_left, int64_t window_right, fa_dtype dtype,
+                            void *stream);
+
+/*
  * fa_backward -- gradients of the forward pass: given Q, K, V, the forward's
  * O and LSE (as fa_forward / fa_forward_gqa wrote them) and dO, the gradient
  * of a loss with respect to O, writes dQ, dK and dV. The forward keeps only O

@@ -124,3 +124,31 @@ def test_backward_invalid_arguments(lib, kw):
 @pytest.mark.parametrize("d", [32, 256])
 def test_backward_unsupported_head_dim(lib, d):
     assert bwd_call(lib, d=d) == fa.FA_ERR_UNSUPPORTED
+
+
+def varlen_call(lib, B=2, H=2, Hk=2, tq=100, tk=100, maxq=60, d=64, scale=0.125, mask=0, wl=0,
+                wr=0, dtype=0, **ptrs):
+    a = dict(q=0x100000, k=0x200000, v=0x300000, o=0x400000, lse=0x600000, cq=0x700000,
+             ck=0x800000)
+    a.update(ptrs)
+    return lib.fa_forward_varlen(a["q"], a["k"], a["v"], a["o"], a["lse"], a["cq"], a["ck"], B, H, Hk,
+                                 tq, tk, maxq, d, scale, mask, wl, wr, dtype, None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(q=0), dict(cq=0), dict(ck=0), dict(B=0), dict(Hk=3), dict(tk=0), dict(tq=-1),
+    dict(dtype=4), dict(mask=2, wr=-1), dict(scale=-1.0), dict(q=0x100004), dict(cq=0x700002),
+    dict(o=0x100000),            # O aliases Q
+    dict(lse=0x400010),          # LSE inside O
+])
+def test_varlen_invalid_arguments(lib, kw):
+    assert varlen_call(lib, **kw) == fa.FA_ERR_INVALID_ARG
+
+
+def test_varlen_empty_is_ok_without_pointers(lib):
+    assert varlen_call(lib, tq=0, maxq=0, q=0, k=0, v=0, o=0, lse=0, cq=0, ck=0) == fa.FA_OK
+
+
+@pytest.mark.parametrize("kw", [dict(d=96), dict(maxq=101)])
+def test_varlen_unsupported(lib, kw):
+    assert varlen_call(lib, **kw) == fa.FA_ERR_UNSUPPORTED

@@ -9,3 +9,4 @@ from .binding import (FA_SPLITKV_STATIC_SCRATCH_BYTES, fa_forward_splitkv,  # no
                       fa_forward_splitkv_static, fa_splitkv_default_splits,
                       fa_splitkv_workspace_bytes)
 from .binding import backward, fa_backward, fa_backward_workspace_bytes  # noqa: F401
+from .binding import fa_forward_varlen  # noqa: F401

@@ -68,6 +68,9 @@ def load_library(path: str = LIB) -> ctypes.CDLL:
     lib.fa_splitkv_workspace_bytes.argtypes = [ctypes.c_int64] * 5
     lib.fa_splitkv_default_splits.restype = ctypes.c_int64
     lib.fa_splitkv_default_splits.argtypes = [ctypes.c_int64] * 5
+    lib.fa_forward_varlen.restype = ctypes.c_int
+    lib.fa_forward_varlen.argtypes = [ctypes.c_void_p] * 7 + [ctypes.c_int64] * 7 + [
+        ctypes.c_float, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]
     lib.fa_backward.restype = ctypes.c_int
     lib.fa_backward.argtypes = [ctypes.c_void_p] * 9 + [ctypes.c_int64] * 5 + [
         ctypes.c_float, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
@@ -312,3 +315,32 @@ def backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     fa_backward(q, k, v, o, do, lse, dq, dk, dv, scale, mask, window[0], window[1], None, stream)
     return dq, dk, dv
+
+
+def fa_forward_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                      lse: torch.Tensor, cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor,
+                      max_seqlen_q: int, scale: float, mask_mode=FA_MASK_NONE,
+                      window_left: int = 0, window_right: int = 0, stream=None) -> None:
+    """Enqueue fa_forward_varlen: q, o (total_q, H, d); k, v (total_k, H_kv, d);
+    lse (total_q, H) float32; cu_seqlens_q / _k int32 (B + 1,) on the device."""
+    lib = load_library()
+    for t in (q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k):
+        if not t.is_cuda or not t.is_contiguous():
+            raise FaError(FA_ERR_INVALID_ARG, "fa_forward_varlen")
+    if q.dtype not in _DTYPES or k.dtype != q.dtype or v.dtype != q.dtype or o.dtype != q.dtype \
+            or lse.dtype != torch.float32 or cu_seqlens_q.dtype != torch.int32 \
+            or cu_seqlens_k.dtype != torch.int32 or q.dim() != 3 or k.dim() != 3:
+        raise FaError(FA_ERR_INVALID_ARG, "fa_forward_varlen")
+    total_q, H, d = q.shape
+    total_k, H_kv = k.shape[0], k.shape[1]
+    B = cu_seqlens_q.numel() - 1
+    if k.shape[2] != d or v.shape != k.shape or o.shape != q.shape or lse.shape != (total_q, H) \
+            or cu_seqlens_k.numel() != B + 1 or B < 1:
+        raise FaError(FA_ERR_INVALID_ARG, "fa_forward_varlen")
+    rc = lib.fa_forward_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                               lse.data_ptr(), cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(),
+                               B, H, H_kv, total_q, total_k, int(max_seqlen_q), d, float(scale),
+                               _MASKS[mask_mode], int(window_left), int(window_right),
+                               _DTYPES[q.dtype], _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_forward_varlen")

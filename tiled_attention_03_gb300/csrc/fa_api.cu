@@ -95,21 +95,22 @@ uint64_t wait_budget() {
 // Opt in to the kernel's shared memory, and check that the registers a launch
 // allocates cover the kernel's setmaxnreg split (a split above them would make
 // setmaxnreg.inc wait forever).
-template <int D, bool BF16, bool PACKED>
+template <int D, bool BF16, bool PACKED, bool VARLEN>
 cudaError_t configure_one() {
     cudaFuncAttributes attr{};
-    cudaError_t e = cudaFuncGetAttributes(&attr, fa::fa_fwd_kernel<D, BF16, PACKED>);
+    cudaError_t e = cudaFuncGetAttributes(&attr, fa::fa_fwd_kernel<D, BF16, PACKED, VARLEN>);
     if (e != cudaSuccess) return e;
     if (attr.numRegs * fa::kThreads < fa::kRegsNeeded) return cudaErrorInvalidConfiguration;
-    return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, BF16, PACKED>,
+    return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, BF16, PACKED, VARLEN>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 fa::SmemLayout<D>::kAlloc);
 }
 
 template <int D, bool BF16>
 cudaError_t configure_kernel() {
-    const cudaError_t e = configure_one<D, BF16, false>();
-    return e != cudaSuccess ? e : configure_one<D, BF16, true>();
+    cudaError_t e = configure_one<D, BF16, false, false>();
+    if (e == cudaSuccess) e = configure_one<D, BF16, true, false>();
+    return e != cudaSuccess ? e : configure_one<D, BF16, false, true>();
 }
 
 DeviceState *device_state(int dev) {
@@ -179,14 +180,38 @@ bool make_map(CUtensorMap *map, const void *base, bool bf16, int64_t BH, int64_t
 
 template <int D, bool BF16>
 cudaError_t launch(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                   const fa::FwdParams &p, bool packed, int64_t blocks, cudaStream_t stream) {
-    if (packed)
-        fa::fa_fwd_kernel<D, BF16, true><<<static_cast<unsigned>(blocks), fa::kThreads,
-                                           fa::SmemLayout<D>::kAlloc, stream>>>(q, k, v, p);
+                   const fa::FwdParams &p, bool packed, int64_t blocks, cudaStream_t stream,
+                   bool varlen = false) {
+    const unsigned g = static_cast<unsigned>(blocks);
+    constexpr int smem = fa::SmemLayout<D>::kAlloc;
+    if (varlen)
+        fa::fa_fwd_kernel<D, BF16, false, true><<<g, fa::kThreads, smem, stream>>>(q, k, v, p);
+    else if (packed)
+        fa::fa_fwd_kernel<D, BF16, true, false><<<g, fa::kThreads, smem, stream>>>(q, k, v, p);
     else
-        fa::fa_fwd_kernel<D, BF16, false><<<static_cast<unsigned>(blocks), fa::kThreads,
-                                            fa::SmemLayout<D>::kAlloc, stream>>>(q, k, v, p);
+        fa::fa_fwd_kernel<D, BF16, false, false><<<g, fa::kThreads, smem, stream>>>(q, k, v, p);
     return cudaGetLastError();
+}
+
+// 3-D map over a token-major (tokens x heads x d) 16-bit tensor, ordered (d, heads,
+// tokens): box = 64 columns x 1 head x 128 tokens, 128-byte swizzle (the same
+// shared-memory tile as make_map's); tokens past the end read as zero.
+bool make_map_tokens(CUtensorMap *map, const void *base, bool bf16, int64_t tokens,
+                     int64_t heads, int64_t d) {
+    EncodeTiledFn enc = encode_fn();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
+                                static_cast<cuuint64_t>(tokens)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * 2),
+                                   static_cast<cuuint64_t>(heads * d * 2)};
+    const cuuint32_t box[3] = {64, 1, 128};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r =
+        enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+            const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
 }
 
 
@@ -398,6 +423,130 @@ fa_status run_forward(const Call &c) {
     return FA_OK;
 }
 
+struct VarlenCall {
+    const void *Q, *K, *V;
+    void *O;
+    float *LSE;
+    const int32_t *cu_q, *cu_k;
+    int64_t B, H, H_kv, total_q, total_k, max_q, d;
+    float scale;
+    fa_mask_mode mask_mode;
+    int64_t window_left, window_right;
+    fa_dtype dtype;
+    void *stream;
+};
+
+fa_status run_forward_varlen(const VarlenCall &c) {
+    const int64_t B = c.B, H = c.H, H_kv = c.H_kv, d = c.d;
+    // ---- host-side checks: nothing is enqueued on failure
+    if (B < 1 || H < 1 || d < 1 || c.total_q < 0 || c.total_k < 0 || c.max_q < 0)
+        return FA_ERR_INVALID_ARG;
+    if (c.total_q == 0 || c.max_q == 0) return FA_OK;  // no query rows: nothing to do
+    if (!c.Q || !c.K || !c.V || !c.O || !c.LSE || !c.cu_q || !c.cu_k) return FA_ERR_INVALID_ARG;
+    if (H_kv < 1 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
+    if (c.dtype != FA_DTYPE_FP16 && c.dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
+    if (c.mask_mode != FA_MASK_NONE && c.mask_mode != FA_MASK_CAUSAL &&
+        c.mask_mode != FA_MASK_WINDOW)
+        return FA_ERR_INVALID_ARG;
+    if (c.mask_mode == FA_MASK_WINDOW && (c.window_left < 0 || c.window_right < 0))
+        return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(c.scale) || !(c.scale > 0.f)) return FA_ERR_INVALID_ARG;
+    if (!aligned16(c.Q) || !aligned16(c.K) || !aligned16(c.V) || !aligned16(c.O) ||
+        !aligned16(c.LSE) || (reinterpret_cast<uintptr_t>(c.cu_q) & 3u) ||
+        (reinterpret_cast<uintptr_t>(c.cu_k) & 3u))
+        return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (c.total_q > (int64_t{1} << 29) || c.total_k > (int64_t{1} << 29) || c.max_q > c.total_q ||
+        B * H > (int64_t{1} << 31))
+        return FA_ERR_UNSUPPORTED;
+    if (c.total_k == 0) return FA_ERR_INVALID_ARG;  // rows without any key
+    const int64_t BH = B * H;
+    const int64_t n_qb = (c.max_q + fa::kUnitRows - 1) / fa::kUnitRows;
+    const int64_t n_units = BH * n_qb;
+    if (n_units > 0x7fffffffLL || c.total_q * H > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+    const size_t tbytes = static_cast<size_t>(c.total_q) * H * d * 2;
+    const size_t lbytes = static_cast<size_t>(c.total_q) * H * sizeof(float);
+    const size_t kvbytes = static_cast<size_t>(c.total_k) * H_kv * d * 2;
+    const size_t cubytes = static_cast<size_t>(B + 1) * sizeof(int32_t);
+    const void *O = c.O, *LSE = c.LSE;
+    if (overlaps(O, tbytes, c.Q, tbytes) || overlaps(O, tbytes, c.K, kvbytes) ||
+        overlaps(O, tbytes, c.V, kvbytes) || overlaps(O, tbytes, LSE, lbytes) ||
+        overlaps(O, tbytes, c.cu_q, cubytes) || overlaps(O, tbytes, c.cu_k, cubytes) ||
+        overlaps(LSE, lbytes, c.Q, tbytes) || overlaps(LSE, lbytes, c.K, kvbytes) ||
+        overlaps(LSE, lbytes, c.V, kvbytes) || overlaps(LSE, lbytes, c.cu_q, cubytes) ||
+        overlaps(LSE, lbytes, c.cu_k, cubytes))
+        return FA_ERR_INVALID_ARG;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+    }
+    DeviceState *ds = device_state(dev);
+    if (ds == nullptr) return FA_ERR_UNSUPPORTED;
+    if (ds->init_err != cudaSuccess) return FA_ERR_CUDA;
+    if (!(ds->cc_major == 10 && ds->cc_minor == 3)) return FA_ERR_UNSUPPORTED;
+    if (!on_device(c.Q, dev) || !on_device(c.K, dev) || !on_device(c.V, dev) ||
+        !on_device(c.O, dev) || !on_device(c.LSE, dev) || !on_device(c.cu_q, dev) ||
+        !on_device(c.cu_k, dev))
+        return FA_ERR_INVALID_ARG;
+
+    const bool bf16 = c.dtype == FA_DTYPE_BF16;
+    CUtensorMap mq, mk, mv;
+    if (!make_map_tokens(&mq, c.Q, bf16, c.total_q, H, d) ||
+        !make_map_tokens(&mk, c.K, bf16, c.total_k, H_kv, d) ||
+        !make_map_tokens(&mv, c.V, bf16, c.total_k, H_kv, d))
+        return FA_ERR_CUDA;
+
+    fa::FwdParams p{};
+    p.O = c.O;
+    p.LSE = c.LSE;
+    p.Nq = static_cast<int>(c.max_q);
+    p.Nk = static_cast<int>(c.total_k);
+    p.H = static_cast<int>(H);
+    p.BH = static_cast<int>(BH);
+    p.kv_group = static_cast<int>(H / H_kv);
+    p.R = static_cast<int>(c.max_q);
+    p.n_units = static_cast<int>(n_units);
+    p.n_qb = static_cast<int>(n_qb);
+    p.n_splits = 1;
+    p.split_tiles = static_cast<int>((c.total_k + fa::kBN - 1) / fa::kBN);
+    // Every sequence's query-key offset lies in [-total_q, total_k], so a window
+    // of total_q + total_k stands for "all keys".
+    const int64_t all = c.total_q + c.total_k;
+    int64_t wl = all, wr = all;
+    if (c.mask_mode == FA_MASK_CAUSAL) wr = 0;
+    if (c.mask_mode == FA_MASK_WINDOW) {
+        wl = c.window_left < all ? c.window_left : all;
+        wr = c.window_right < all ? c.window_right : all;
+    }
+    p.wl = static_cast<int>(wl);
+    p.wr = static_cast<int>(wr);
+    p.heavy_first = wr < all ? 1 : 0;
+    p.scale_log2 = static_cast<float>(static_cast<double>(c.scale) * 1.4426950408889634074);
+    p.wait_budget_ns = wait_budget();
+    p.status = ds->status;
+    p.fault_skip_k = g_fault_pos.exchange(-1);
+    p.sched = ds->sched + 2 * (g_sched_next.fetch_add(1) % kSchedSlots);
+    p.cu_q = c.cu_q;
+    p.cu_k = c.cu_k;
+    p.total_q = static_cast<int>(c.total_q);
+    p.total_k = static_cast<int>(c.total_k);
+
+    const int64_t blocks = n_units < ds->sm_count ? n_units : ds->sm_count;
+    cudaStream_t st = static_cast<cudaStream_t>(c.stream);
+    cudaError_t e;
+    if (d == 64)
+        e = bf16 ? launch<64, true>(mq, mk, mv, p, false, blocks, st, true)
+                 : launch<64, false>(mq, mk, mv, p, false, blocks, st, true);
+    else
+        e = bf16 ? launch<128, true>(mq, mk, mv, p, false, blocks, st, true)
+                 : launch<128, false>(mq, mk, mv, p, false, blocks, st, true);
+    if (e != cudaSuccess) return FA_ERR_CUDA;
+    g_launches.fetch_add(1);
+    return FA_OK;
+}
+
 }  // namespace
 
 namespace fa_host {
@@ -514,6 +663,17 @@ fa_status fa_forward_splitkv_static(const void *Q, const void *K, const void *V,
     Call c{Q, K, V, O, LSE, B, H, H_kv, Nq, Nk, d, scale, mask_mode, window_left, window_right,
            dtype, num_splits, sc.ptr, kStaticScratchBytes, stream};
     return run_forward(c);
+}
+
+fa_status fa_forward_varlen(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                            const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int64_t B,
+                            int64_t H, int64_t H_kv, int64_t total_q, int64_t total_k,
+                            int64_t max_seqlen_q, int64_t d, float scale, fa_mask_mode mask_mode,
+                            int64_t window_left, int64_t window_right, fa_dtype dtype,
+                            void *stream) {
+    VarlenCall c{Q, K, V, O, LSE, cu_seqlens_q, cu_seqlens_k, B, H, H_kv, total_q, total_k,
+                 max_seqlen_q, d, scale, mask_mode, window_left, window_right, dtype, stream};
+    return run_forward_varlen(c);
 }
 
 fa_status fa_sync_status(void *stream) {

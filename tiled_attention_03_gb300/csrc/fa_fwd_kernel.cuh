@@ -122,6 +122,14 @@ struct FwdParams {
     unsigned long long wait_budget_ns;
     unsigned int *status;  // [code, role, unit, block]
     int fault_skip_k;      // test hook: every CTA skips the K load at this ring position (-1: none)
+    // Variable-length batches (kernel template flag): sequence b holds query tokens
+    // cu_q[b] .. cu_q[b+1]-1 and keys cu_k[b] .. cu_k[b+1]-1 of token-major tensors
+    // (total x heads x d); row spaces are (b, h) and Nq stands for the longest
+    // sequence's query count. Lengths are clamped to [0, total] so that no stray
+    // value can address memory outside the tensors.
+    const int *cu_q;
+    const int *cu_k;
+    int total_q, total_k;
     unsigned int *sched;   // this launch's {next unit, finished CTAs} counters (zero at launch)
 };
 
@@ -170,11 +178,37 @@ enum : int {
 // restricted to the K/V tiles of key split `split`; Q tile t covers rows
 // [r0 + 128 t, r0 + 128 t + 128) and needs K/V tiles [a[t], b[t]] (empty when
 // a > b); [j0, j1] is their union.
-struct Unit {
+struct UnitBase {
     int rs, bkv, r0, split;
     int a[kQTiles], b[kQTiles];
     int j0, j1;
 };
+// Variable-length batches only: this sequence's query rows and keys, the query
+// position offset, its first token rows and its heads.
+struct UnitSeq {
+    int nq, nk, q_off, q_tok0, k_tok0, h, hkv;
+};
+template <bool VARLEN>
+struct Unit : UnitBase {};
+template <>
+struct Unit<true> : UnitBase, UnitSeq {};
+
+// Sizes of the unit's problem: the launch's, or (VARLEN) its sequence's.
+template <bool VARLEN>
+__device__ __forceinline__ int unit_rows(const Unit<VARLEN> &U, const FwdParams &p) {
+    if constexpr (VARLEN) return U.nq;
+    else return p.R;
+}
+template <bool VARLEN>
+__device__ __forceinline__ int unit_keys(const Unit<VARLEN> &U, const FwdParams &p) {
+    if constexpr (VARLEN) return U.nk;
+    else return p.Nk;
+}
+template <bool VARLEN>
+__device__ __forceinline__ int unit_qoff(const Unit<VARLEN> &U, const FwdParams &p) {
+    if constexpr (VARLEN) return U.q_off;
+    else return p.q_off;
+}
 
 // Query indices (0..Nq-1) met by the rows [rt0, rl] of a row space (an unpacked
 // row space is one head: rows are queries).
@@ -196,9 +230,9 @@ __device__ __forceinline__ void tile_queries(const FwdParams &p, int rt0, int rl
     }
 }
 
-template <bool PACKED>
-__device__ __forceinline__ Unit decode_unit(int u, const FwdParams &p) {
-    Unit U;
+template <bool PACKED, bool VARLEN>
+__device__ __forceinline__ Unit<VARLEN> decode_unit(int u, const FwdParams &p) {
+    Unit<VARLEN> U;
     const int per_space = p.n_qb * p.n_splits;
     const int rs = u / per_space;
     const int rem = u - rs * per_space;
@@ -210,6 +244,19 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams &p) {
     } else {
         const int b = rs / p.H, h = rs - b * p.H;
         U.bkv = b * (p.H / p.kv_group) + h / p.kv_group;
+        if constexpr (VARLEN) {
+            U.h = h;
+            U.hkv = h / p.kv_group;
+            const int q0 = min(max(p.cu_q[b], 0), p.total_q);
+            const int q1 = min(max(p.cu_q[b + 1], q0), p.total_q);
+            const int k0 = min(max(p.cu_k[b], 0), p.total_k);
+            const int k1 = min(max(p.cu_k[b + 1], k0), p.total_k);
+            U.q_tok0 = q0;
+            U.k_tok0 = k0;
+            U.nq = q1 - q0;
+            U.nk = k1 - k0;
+            U.q_off = U.nk - U.nq;
+        }
     }
     if (p.heavy_first) qb = p.n_qb - 1 - qb;
     U.r0 = qb * kUnitRows;
@@ -222,15 +269,18 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams &p) {
         const int rt0 = U.r0 + t * kBM;
         U.a[t] = 1;
         U.b[t] = 0;
-        if (rt0 < p.R) {
-            const int rl = min(rt0 + kBM, p.R) - 1;
+        const int R = unit_rows<VARLEN>(U, p);
+        const int nk = unit_keys<VARLEN>(U, p);
+        const int q_off = unit_qoff<VARLEN>(U, p);
+        if (rt0 < R) {
+            const int rl = min(rt0 + kBM, R) - 1;
             int i_lo, i_hi;
             tile_queries<PACKED>(p, rt0, rl, i_lo, i_hi);
-            const int lo_key = i_lo + p.q_off - p.wl;  // first key any row of the tile sees
-            const int hi_key = i_hi + p.q_off + p.wr;  // last key any row of the tile sees
-            if (hi_key >= 0 && lo_key <= p.Nk - 1) {
+            const int lo_key = i_lo + q_off - p.wl;  // first key any row of the tile sees
+            const int hi_key = i_hi + q_off + p.wr;  // last key any row of the tile sees
+            if (hi_key >= 0 && lo_key <= nk - 1) {
                 const int a = max(max(0, lo_key) / kBN, s_lo);
-                const int b = min(min(p.Nk - 1, hi_key) / kBN, s_hi);
+                const int b = min(min(nk - 1, hi_key) / kBN, s_hi);
                 if (a <= b) {
                     U.a[t] = a;
                     U.b[t] = b;
@@ -243,7 +293,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams &p) {
     return U;
 }
 
-__device__ __forceinline__ bool unit_empty(const Unit &U) { return U.j1 < U.j0; }
+__device__ __forceinline__ bool unit_empty(const UnitBase &U) { return U.j1 < U.j0; }
 
 __device__ __forceinline__ void record_timeout(const FwdParams &p, volatile int *abort_flag,
                                                int role, int unit) {
@@ -338,7 +388,30 @@ __device__ __forceinline__ float softmax_tile(uint32_t tS, uint32_t tP, bool bou
     return corr;
 }
 
-template <int D, bool BF16, bool PACKED>
+// TMA coordinates of a Q tile (row r of the unit's row space) and of K/V tile j.
+// Dense maps are (d, rows, row spaces); variable-length maps (d, heads, tokens).
+template <bool VARLEN>
+__device__ __forceinline__ void q_coords(const Unit<VARLEN> &U, int r, int &y, int &z) {
+    if constexpr (VARLEN) {
+        y = U.h;
+        z = U.q_tok0 + r;
+    } else {
+        y = r;
+        z = U.rs;
+    }
+}
+template <bool VARLEN>
+__device__ __forceinline__ void kv_coords(const Unit<VARLEN> &U, int j, int &y, int &z) {
+    if constexpr (VARLEN) {
+        y = U.hkv;
+        z = U.k_tok0 + j * kBN;
+    } else {
+        y = j * kBN;
+        z = U.bkv;
+    }
+}
+
+template <int D, bool BF16, bool PACKED, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -428,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 while (true) {
                     const unsigned next = atomicAdd(p.sched, 1u);
                     if (next >= static_cast<unsigned>(p.n_units)) break;
-                    if (!unit_empty(decode_unit<PACKED>(static_cast<int>(next), p))) {
+                    if (!unit_empty(decode_unit<PACKED, VARLEN>(static_cast<int>(next), p))) {
                         v = static_cast<int>(next);
                         break;
                     }
@@ -438,21 +511,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return v;
             };
             auto prefetch_q_l2 = [&](int v) {
-                const Unit W = decode_unit<PACKED>(v, p);
-                for (int t = 0; t < kQTiles; ++t)
-                    for (int g = 0; g < kRegions; ++g)
-                        tma_prefetch_l2_3d(&tmQ, 64 * g, W.r0 + t * kBM, W.rs);
+                const auto W = decode_unit<PACKED, VARLEN>(v, p);
+                for (int t = 0; t < kQTiles; ++t) {
+                    int y, z;
+                    q_coords<VARLEN>(W, W.r0 + t * kBM, y, z);
+                    for (int g = 0; g < kRegions; ++g) tma_prefetch_l2_3d(&tmQ, 64 * g, y, z);
+                }
             };
             int u = publish(0);
             for (; ok && u >= 0; ++unit_iter) {
-                const Unit U = decode_unit<PACKED>(u, p);
+                const auto U = decode_unit<PACKED, VARLEN>(u, p);
                 for (int t = 0; t < kQTiles && ok; ++t) {
                     ok = mbar_wait_bounded(bar(kBarQEmpty + t), (unit_iter & 1) ^ 1, abort_flag, budget);
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(kBarQFull + t), L::kTileBytes);
+                    int y, z;
+                    q_coords<VARLEN>(U, U.r0 + t * kBM, y, z);
                     for (int g = 0; g < kRegions; ++g)
                         tma_load_3d(sQ + t * L::kTileBytes + g * kRegionBytes, &tmQ,
-                                    bar(kBarQFull + t), 64 * g, U.r0 + t * kBM, U.rs);
+                                    bar(kBarQFull + t), 64 * g, y, z);
                 }
                 if (!ok) break;
                 ++q_loads;
@@ -473,9 +550,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) break;
                     if (kv_iter != p.fault_skip_k) {
                         mbar_arrive_expect_tx(bar(kBarKFull + st), L::kTileBytes);
+                        int y, z;
+                        kv_coords<VARLEN>(U, j, y, z);
                         for (int g = 0; g < kRegions; ++g)
                             tma_load_3d(sK + st * L::kTileBytes + g * kRegionBytes, &tmK,
-                                        bar(kBarKFull + st), 64 * g, j * kBN, U.bkv);
+                                        bar(kBarKFull + st), 64 * g, y, z);
                     }
                 }
                 u = u_next;
@@ -505,16 +584,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int u = unit_ring[slot];
                 mbar_arrive(bar(kBarUnitEmpty + slot));
                 if (u < 0) break;
-                const Unit U = decode_unit<PACKED>(u, p);
+                const auto U = decode_unit<PACKED, VARLEN>(u, p);
                 for (int j = U.j0; ok && j <= U.j1; ++j, ++kv_iter) {
                     const int st = kv_iter % kStages;
                     ok = mbar_wait_bounded(bar(kBarVEmpty + st), ((kv_iter / kStages) & 1) ^ 1,
                                            abort_flag, budget);
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(kBarVFull + st), L::kTileBytes);
+                    int y, z;
+                    kv_coords<VARLEN>(U, j, y, z);
                     for (int g = 0; g < kRegions; ++g)
                         tma_load_3d(sV + st * L::kTileBytes + g * kRegionBytes, &tmV,
-                                    bar(kBarVFull + st), 64 * g, j * kBN, U.bkv);
+                                    bar(kBarVFull + st), 64 * g, y, z);
                 }
                 if (!ok) record_timeout(p, abort_flag, kRoleTma, u);
             }
@@ -597,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (elect_one()) mbar_arrive(bar(kBarUnitEmpty + slot));
             __syncwarp();
             if (u < 0) break;
-            const Unit U = decode_unit<PACKED>(u, p);
+            const auto U = decode_unit<PACKED, VARLEN>(u, p);
             for (int t = 0; t < kQTiles && ok; ++t) ok = wait(kBarQFull + t, unit_iter & 1);
             const int j0 = U.j0;
             const int j1 = U.j1;
@@ -664,19 +745,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarUnitEmpty + slot));
             if (u < 0) break;
-            const Unit U = decode_unit<PACKED>(u, p);
+            const auto U = decode_unit<PACKED, VARLEN>(u, p);
             if (U.a[t] > U.b[t]) continue;
+            const int R = unit_rows<VARLEN>(U, p);
+            const int nk = unit_keys<VARLEN>(U, p);
+            const int q_off = unit_qoff<VARLEN>(U, p);
             const int rt0 = U.r0 + t * kBM;
-            const int rl = min(rt0 + kBM, p.R) - 1;
+            const int rl = min(rt0 + kBM, R) - 1;
             const int r = rt0 + row;     // row of the row space
             const int i = PACKED ? r % p.Nq : r;  // query index in its head
             int i_lo, i_hi;
             tile_queries<PACKED>(p, rt0, rl, i_lo, i_hi);
             // visible keys of query i: [i + q_off - wl, i + q_off + wr] within [0, Nk)
-            const int lo_i = max(0, i + p.q_off - p.wl);
-            const int hi_i = min(p.Nk - 1, i + p.q_off + p.wr);
-            const int lo_last = max(0, i_hi + p.q_off - p.wl);
-            const int hi_first = min(p.Nk - 1, i_lo + p.q_off + p.wr);
+            const int lo_i = max(0, i + q_off - p.wl);
+            const int hi_i = min(nk - 1, i + q_off + p.wr);
+            const int lo_last = max(0, i_hi + q_off - p.wl);
+            const int hi_first = min(nk - 1, i_lo + q_off + p.wr);
             float m = -INFINITY;  // reference max of the row, in log2 units of the scaled logits
             float l = 0.f;        // running sum of 2^(logit - m)
             for (int j = U.a[t]; j <= U.b[t]; ++j, ++s_count) {
@@ -722,8 +806,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
-            const bool store = r < p.R;
-            const size_t grow = static_cast<size_t>(U.rs) * p.R + (store ? r : 0);  // global row
+            const bool store = r < R;
+            // global row of O and LSE: (row space, row), or (token, head) when VARLEN
+            size_t grow;
+            if constexpr (VARLEN)
+                grow = (static_cast<size_t>(U.q_tok0) + (store ? r : 0)) * p.H + U.h;
+            else
+                grow = static_cast<size_t>(U.rs) * p.R + (store ? r : 0);
             const float lse = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
             if (p.part_O == nullptr) {
                 // O / l rounded to 16 bit, and LSE

@@ -23,6 +23,8 @@ from __future__ import annotations
 import dataclasses
 import math
 
+import numpy as np
+
 import torch
 
 MASK_NONE = 0
@@ -49,6 +51,7 @@ class Workload:
     Nq: int = 0    # query rows per head when fewer than the N keys (the last Nq positions); 0 means N
     splits: int = -1  # key splits for the split-KV entry point (0: its default); -1: not split
     backward: bool = False  # time the backward pass (dQ, dK, dV) instead of the forward
+    varlen: bool = False    # B sequences of seeded lengths in [N/8, N], packed token-major
 
     @property
     def scale(self) -> float:
@@ -110,7 +113,30 @@ BWD_WORKLOADS = [
              seed=11, H_kv=8, backward=True),
 ]
 
-BY_NAME = {w.name: w for w in WORKLOADS + EXTRA_WORKLOADS + BWD_WORKLOADS}
+# A packed batch of 16 causal sequences of mixed lengths (N/8 .. N), token-major.
+VARLEN_WORKLOADS = [
+    Workload("varlen_causal_b16h32n4096d128", 16, 32, 4096, 128, torch.bfloat16, MASK_CAUSAL, 0, 0,
+             seed=12, varlen=True),
+]
+
+BY_NAME = {w.name: w for w in WORKLOADS + EXTRA_WORKLOADS + BWD_WORKLOADS + VARLEN_WORKLOADS}
+
+
+def varlen_lengths(w: Workload) -> list[int]:
+    """Seeded sequence lengths of a variable-length workload, uniform in [N/8, N]."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed + 20000)
+    return [int(x) for x in torch.randint(w.N // 8, w.N + 1, (w.B,), generator=g)]
+
+
+def varlen_inputs(w: Workload):
+    """Token-major Q, K, V (total, heads, d) and cu_seqlens (B + 1,) int32: sequence b
+    is the first L_b positions of batch entry b of workload_inputs(w)."""
+    q, k, v = workload_inputs(w)
+    lens = varlen_lengths(w)
+    pack = lambda t: torch.cat([t[b, :, :lens[b]].transpose(0, 1) for b in range(w.B)], 0).contiguous()
+    cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32)
+    return pack(q), pack(k), pack(v), cu
 
 
 def make_qkv(B: int, H: int, N: int, d: int, dtype: torch.dtype, seed: int,
@@ -181,15 +207,19 @@ def algorithmic_flops(w: Workload) -> float:
     """Forward: 2 products of 2 d FLOPs per visible pair. Backward: 5 (dV, dP, dQ,
     dK and the recomputed S), i.e. 2.5x the forward."""
     per_pair = 10.0 if w.backward else 4.0
+    if w.varlen:
+        pairs = sum(visible_pairs(n, w.mask, w.window_left, w.window_right) for n in varlen_lengths(w))
+        return per_pair * w.d * w.H * pairs
     return per_pair * w.d * w.B * w.H * visible_pairs(w.N, w.mask, w.window_left, w.window_right, w.Nq)
 
 
 def algorithmic_bytes(w: Workload) -> int:
     """Forward: Q, K, V read once and O (16-bit) plus LSE (fp32) written once.
     Backward: Q, K, V, O, dO and LSE read once, dQ, dK, dV written once."""
-    q_elems = w.B * w.H * w.q_rows * w.d
-    kv_elems = w.B * w.kv_heads * w.N * w.d
-    rows = w.B * w.H * w.q_rows
+    tokens = sum(varlen_lengths(w)) if w.varlen else w.B * w.q_rows
+    q_elems = tokens * w.H * w.d
+    kv_elems = (tokens if w.varlen else w.B * w.N) * w.kv_heads * w.d
+    rows = tokens * w.H
     if w.backward:
         return (4 * q_elems + 4 * kv_elems) * 2 + rows * 4
     return (2 * q_elems + 2 * kv_elems) * 2 + rows * 4
