@@ -33,6 +33,8 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 KERNEL_SOURCES = ("tiled_attention_03_gb300/csrc/fa_fwd_kernel.cuh",
+                  "tiled_attention_03_gb300/csrc/fa_bwd_kernel.cuh",
+                  "tiled_attention_03_gb300/csrc/fa_combine.cuh",
                   "tiled_attention_03_gb300/csrc/ptx.cuh")
 TRAFFIC_DIR = os.path.join(ROOT, "profiles")
 
