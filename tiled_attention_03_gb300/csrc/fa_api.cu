@@ -130,6 +130,8 @@ DeviceState *device_state(int dev) {
                 e = cudaGetSymbolAddress(&addr, g_fa_sched);
                 s.sched = static_cast<unsigned int *>(addr);
             }
+            if (e == cudaSuccess) e = configure_kernel<32, false>();
+            if (e == cudaSuccess) e = configure_kernel<32, true>();
             if (e == cudaSuccess) e = configure_kernel<64, false>();
             if (e == cudaSuccess) e = configure_kernel<64, true>();
             if (e == cudaSuccess) e = configure_kernel<128, false>();
@@ -168,13 +170,13 @@ bool make_map(CUtensorMap *map, const void *base, bool bf16, int64_t BH, int64_t
                                 static_cast<cuuint64_t>(BH)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * 2),
                                    static_cast<cuuint64_t>(N * d * 2)};
-    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(d < 64 ? d : 64), 128, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r =
         enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
             const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            d < 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -204,13 +206,13 @@ bool make_map_tokens(CUtensorMap *map, const void *base, bool bf16, int64_t toke
                                 static_cast<cuuint64_t>(tokens)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * 2),
                                    static_cast<cuuint64_t>(heads * d * 2)};
-    const cuuint32_t box[3] = {64, 1, 128};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(d < 64 ? d : 64), 1, 128};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r =
         enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
             const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            d < 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -292,7 +294,7 @@ fa_status run_forward(const Call &c) {
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
         return FA_ERR_INVALID_ARG;
     if (c.num_splits < 1) return FA_ERR_INVALID_ARG;
-    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (d != 32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
     // Size limits of this implementation: 32-bit row indices and grid.
     if (Nq > (int64_t{1} << 29) || Nk > (int64_t{1} << 29) || B * H > (int64_t{1} << 31))
         return FA_ERR_UNSUPPORTED;
@@ -391,7 +393,10 @@ fa_status run_forward(const Call &c) {
     const int64_t blocks = n_units < ds->sm_count ? n_units : ds->sm_count;
     cudaStream_t st = static_cast<cudaStream_t>(c.stream);
     cudaError_t e;
-    if (d == 64)
+    if (d == 32)
+        e = bf16 ? launch<32, true>(mq, mk, mv, p, packed, blocks, st)
+                 : launch<32, false>(mq, mk, mv, p, packed, blocks, st);
+    else if (d == 64)
         e = bf16 ? launch<64, true>(mq, mk, mv, p, packed, blocks, st)
                  : launch<64, false>(mq, mk, mv, p, packed, blocks, st);
     else
@@ -413,7 +418,9 @@ fa_status run_forward(const Call &c) {
         cp.wr = p.wr;
         cp.n_splits = p.n_splits;
         cp.split_keys = p.split_tiles * fa::kBN;
-        if (d == 64)
+        if (d == 32)
+            e = bf16 ? launch_combine<32, true>(cp, st) : launch_combine<32, false>(cp, st);
+        else if (d == 64)
             e = bf16 ? launch_combine<64, true>(cp, st) : launch_combine<64, false>(cp, st);
         else
             e = bf16 ? launch_combine<128, true>(cp, st) : launch_combine<128, false>(cp, st);
@@ -455,7 +462,7 @@ fa_status run_forward_varlen(const VarlenCall &c) {
         !aligned16(c.LSE) || (reinterpret_cast<uintptr_t>(c.cu_q) & 3u) ||
         (reinterpret_cast<uintptr_t>(c.cu_k) & 3u))
         return FA_ERR_INVALID_ARG;
-    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (d != 32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
     if (c.total_q > (int64_t{1} << 29) || c.total_k > (int64_t{1} << 29) || c.max_q > c.total_q ||
         B * H > (int64_t{1} << 31))
         return FA_ERR_UNSUPPORTED;
@@ -536,7 +543,10 @@ fa_status run_forward_varlen(const VarlenCall &c) {
     const int64_t blocks = n_units < ds->sm_count ? n_units : ds->sm_count;
     cudaStream_t st = static_cast<cudaStream_t>(c.stream);
     cudaError_t e;
-    if (d == 64)
+    if (d == 32)
+        e = bf16 ? launch<32, true>(mq, mk, mv, p, false, blocks, st, true)
+                 : launch<32, false>(mq, mk, mv, p, false, blocks, st, true);
+    else if (d == 64)
         e = bf16 ? launch<64, true>(mq, mk, mv, p, false, blocks, st, true)
                  : launch<64, false>(mq, mk, mv, p, false, blocks, st, true);
     else

@@ -78,7 +78,16 @@ constexpr int kVWarp = 10;    // V loads
 constexpr int kRegsSoftmax = FA_REGS_SOFTMAX;
 constexpr int kRegsControl = FA_REGS_CONTROL;
 constexpr int kRegsNeeded = 2 * 128 * kRegsSoftmax + 128 * kRegsControl;
-constexpr int kRegionBytes = 128 * 128;  // 128 rows x 128 B: one 64-column swizzle region
+// Tiles are stored as regions of min(d, 64) columns x 128 rows with the swizzle of
+// that row width (128 B, or 64 B for d = 32).
+template <int D>
+struct Regions {
+    static constexpr int kCols = D < 64 ? D : 64;
+    static constexpr int kRowBytes = kCols * 2;
+    static constexpr int kBytes = 128 * kRowBytes;
+    static constexpr int kCount = D / kCols;
+    static constexpr int kStepsPerRegion = kCols / 16;  // K-steps of 16 columns per region
+};
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: probabilities stay <= 2^8
 // Of every 32 probabilities, how many use the FMA-pipe exp2 (the rest use MUFU),
@@ -137,7 +146,7 @@ template <int D>
 struct SmemLayout {
     // K/V ring depth. The footprint stays above half of the SM's shared
     // memory, so one CTA (holding all 512 TMEM columns) runs per SM.
-    static constexpr int kStages = D == 64 ? 4 : 2;
+    static constexpr int kStages = D == 128 ? 2 : 4;
     static constexpr int kTileBytes = kBM * D * 2;
     static constexpr int kQ = 0;
     static constexpr int kK = kQ + kQTiles * kTileBytes;
@@ -416,10 +425,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
     using L = SmemLayout<D>;
-    constexpr int kRegions = D / 64;
+    using G = Regions<D>;
+    constexpr int kRegions = G::kCount;
     constexpr int kStages = L::kStages;
     static_assert(kStages <= kMaxStages && kNumBarsUsed <= L::kNumBars, "barrier slots");
-    static_assert(D == 64 || D == 128, "head dim");
+    static_assert(D == 32 || D == 64 || D == 128, "head dim");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -515,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int t = 0; t < kQTiles; ++t) {
                     int y, z;
                     q_coords<VARLEN>(W, W.r0 + t * kBM, y, z);
-                    for (int g = 0; g < kRegions; ++g) tma_prefetch_l2_3d(&tmQ, 64 * g, y, z);
+                    for (int g = 0; g < kRegions; ++g) tma_prefetch_l2_3d(&tmQ, G::kCols * g, y, z);
                 }
             };
             int u = publish(0);
@@ -528,8 +538,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     int y, z;
                     q_coords<VARLEN>(U, U.r0 + t * kBM, y, z);
                     for (int g = 0; g < kRegions; ++g)
-                        tma_load_3d(sQ + t * L::kTileBytes + g * kRegionBytes, &tmQ,
-                                    bar(kBarQFull + t), 64 * g, y, z);
+                        tma_load_3d(sQ + t * L::kTileBytes + g * G::kBytes, &tmQ,
+                                    bar(kBarQFull + t), G::kCols * g, y, z);
                 }
                 if (!ok) break;
                 ++q_loads;
@@ -553,8 +563,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         int y, z;
                         kv_coords<VARLEN>(U, j, y, z);
                         for (int g = 0; g < kRegions; ++g)
-                            tma_load_3d(sK + st * L::kTileBytes + g * kRegionBytes, &tmK,
-                                        bar(kBarKFull + st), 64 * g, y, z);
+                            tma_load_3d(sK + st * L::kTileBytes + g * G::kBytes, &tmK,
+                                        bar(kBarKFull + st), G::kCols * g, y, z);
                     }
                 }
                 u = u_next;
@@ -594,8 +604,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     int y, z;
                     kv_coords<VARLEN>(U, j, y, z);
                     for (int g = 0; g < kRegions; ++g)
-                        tma_load_3d(sV + st * L::kTileBytes + g * kRegionBytes, &tmV,
-                                    bar(kBarVFull + st), 64 * g, y, z);
+                        tma_load_3d(sV + st * L::kTileBytes + g * G::kBytes, &tmV,
+                                    bar(kBarVFull + st), G::kCols * g, y, z);
                 }
                 if (!ok) record_timeout(p, abort_flag, kRoleTma, u);
             }
@@ -635,14 +645,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // S_t(j) = Q_t K_j^T into TMEM columns t * 128.
         auto issue_s = [&](int t, int st) {
             tc_fence_after();
-            const uint64_t dq = sw128_desc(sQ + t * L::kTileBytes, 16, 1024);
-            const uint64_t dk = sw128_desc(sK + st * L::kTileBytes, 16, 1024);
+            const uint64_t dq = swz_desc<G::kRowBytes>(sQ + t * L::kTileBytes, 16);
+            const uint64_t dk = swz_desc<G::kRowBytes>(sK + st * L::kTileBytes, 16);
             if (elect_one()) {
                 // K-step k reads 16 columns: 32 bytes into 64-column region k / 4.
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
-                    constexpr uint32_t kRegion16 = kRegionBytes >> 4;
-                    const uint32_t off = (k >> 2) * kRegion16 + (k & 3) * 2;
+                    constexpr uint32_t kRegion16 = G::kBytes >> 4;
+                    const uint32_t off = (k / G::kStepsPerRegion) * kRegion16 +
+                                         (k % G::kStepsPerRegion) * 2;
                     umma_f16_ss(tmem + t * kBN, dq + off, dk + off, idesc_s, k > 0 ? 1u : 0u);
                 }
                 umma_commit(bar(kBarSFull + t));
@@ -652,14 +663,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // O_t (+)= P_t V_j, P_t read from TMEM.
         auto issue_pv = [&](int t, int st, bool first) {
             tc_fence_after();
-            const uint64_t dv = sw128_desc(sV + st * L::kTileBytes, kRegionBytes, 1024);
+            const uint64_t dv = swz_desc<G::kRowBytes>(sV + st * L::kTileBytes, G::kBytes);
             const uint32_t acc0 = first ? 0u : 1u;
             if (elect_one()) {
                 // K-step k reads keys 16k..16k+15: 16 rows of 128 B of V.
 #pragma unroll
                 for (int k = 0; k < kBN / 16; ++k)
                     umma_f16_ts(tmem + L::kTmemO + t * D, tmem + t * kBN + k * 8,
-                                dv + k * ((16 * 128) >> 4), idesc_o, k > 0 ? 1u : acc0);
+                                dv + k * ((16 * G::kRowBytes) >> 4), idesc_o, k > 0 ? 1u : acc0);
                 umma_commit(bar(kBarODone + t));
             }
             __syncwarp();

@@ -265,6 +265,21 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
     return d;
 }
 
+// Same for a tile whose rows are kRowBytes wide: 128 gives the 128-byte swizzle
+// above; 64 gives the 64-byte swizzle (byte-offset bits 4-5 XOR-ed with bits 7-8,
+// as TMA's 64-byte mode writes it; mode 4 at bits 61-63). SBO = 8 rows.
+template <int kRowBytes>
+__device__ __forceinline__ uint64_t swz_desc(uint32_t saddr, uint32_t lbo) {
+    static_assert(kRowBytes == 128 || kRowBytes == 64, "row width");
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>(((8 * kRowBytes) >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(kRowBytes == 128 ? 2 : 4) << 61;
+    return d;
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16 with an fp32 accumulator.
 // bits 4-5 D format (1 = f32); 7-9 A format and 10-12 B format (0 = f16, 1 = bf16);
 // 15 / 16 A / B major (0 = K-major, 1 = MN-major); 17-22 N >> 3; 24-28 M >> 4.
