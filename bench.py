@@ -510,6 +510,7 @@ def main():
                 "traffic": traffic, "algorithmic_bytes": nbytes,
                 "kernel": (f"fa_bwd prep + dK/dV + dQ kernels <{w.d}, {w.dtype_name}>" if w.backward
                            else f"fa_fwd_kernel<{w.d}, {w.dtype_name}, varlen>" if w.varlen
+                           else f"fa_fwd256_kernel<{w.dtype_name}>" if w.d == 256
                            else f"fa_fwd_kernel<{w.d}, {w.dtype_name}>"
                            + (f" + merge ({splits} key splits)" if splits > 1 else ""))},
             "cpu_baseline": cpu,

@@ -57,7 +57,10 @@ typedef enum { FA_DTYPE_FP16 = 0, FA_DTYPE_BF16 = 1 } fa_dtype;
  * LSE     : device pointer, contiguous B x H x N float32. Written.
  * B, H, N : >= 1. Any N is accepted (no padding is required of the caller;
  *           rows and keys past N are handled inside the kernel).
- * d       : head dimension; 64 and 128 are implemented (else FA_ERR_UNSUPPORTED).
+ * d       : head dimension: 32, 64, 128 or 256 (else FA_ERR_UNSUPPORTED). d = 256
+ *           runs its own kernel (one 128-row Q tile per unit, 64-key K/V tiles)
+ *           and is available in fa_forward and fa_forward_gqa only; the split-KV
+ *           and variable-length calls take 32, 64 and 128, fa_backward 64 and 128.
  * scale   : multiplier of the logits, finite and > 0 (typically 1/sqrt(d)).
  * mask_mode, window_left, window_right : see fa_mask_mode. The window
  *           arguments are read only for FA_MASK_WINDOW and must then be >= 0

@@ -56,7 +56,7 @@ def test_invalid_arguments(lib, kw):
     assert call(lib, **kw) == fa.FA_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("d", [16, 96, 256, 80])
+@pytest.mark.parametrize("d", [16, 96, 80, 512])
 def test_unsupported_head_dim(lib, d):
     assert call(lib, d=d) == fa.FA_ERR_UNSUPPORTED
 

@@ -1,5 +1,5 @@
-"""Head dimension 32 (64-byte swizzled tiles) on every forward entry point, against
-the oracle."""
+"""Head dimension 32 (64-byte swizzled tiles) on every forward entry point, and head
+dimension 256 (its own kernel) on fa_forward / fa_forward_gqa, against the oracle."""
 
 import numpy as np
 import pytest
@@ -63,3 +63,35 @@ def test_d32_varlen():
         assert np.abs(got - O).max() <= TOL_O[torch.bfloat16]
         assert np.abs(gl - LSE).max() <= TOL_LSE
         t0 += L
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("N", [1, 63, 64, 65, 129, 300, 1000])
+@pytest.mark.parametrize("mask,window", [("none", (0, 0)), ("causal", (0, 0)), ("window", (100, 7))])
+def test_d256_parity(mask, window, N, dtype):
+    q, k, v = make_qkv(1, 3, N, 256, dtype, seed=N + 256)
+    o, lse = run_cuda(q, k, v, 256 ** -0.5, mask, window)
+    compare(o, lse, q, k, v, 256 ** -0.5, mask, window)
+
+
+@pytest.mark.parametrize("mask", ["none", "causal"])
+def test_d256_gqa_long(mask):
+    """Many 64-key blocks per unit, GQA, a late dominant key per row (forces the
+    lazy O rescale) on some rows."""
+    q, _, _ = make_qkv(2, 4, 2000, 256, torch.bfloat16, seed=8, q_std=2.0)
+    _, k, v = make_qkv(2, 2, 2000, 256, torch.bfloat16, seed=9, H_kv=2)
+    k[:, :, 1900:] *= 3.0
+    o, lse = run_cuda(q, k, v, 256 ** -0.5, mask)
+    compare(o, lse, q, k, v, 256 ** -0.5, mask)
+
+
+def test_d256_rejects_split_and_rectangular():
+    dev = torch.device("cuda", 0)
+    q, k, v = (t.to(dev) for t in make_qkv(1, 2, 64, 256, torch.float16, seed=0))
+    o, lse = torch.empty_like(q), torch.empty(1, 2, 64, device=dev)
+    with pytest.raises(fa.FaError):
+        fa.fa_forward_splitkv(q, k, v, o, lse, 0.0625, "none", 0, 0, 2)
+    with pytest.raises(fa.FaError):
+        fa.fa_forward_splitkv(q[:, :, :10].contiguous(), k, v, o[:, :, :10].contiguous(),
+                              lse[:, :, :10].contiguous(), 0.0625, "none", 0, 0, 1)
+    assert fa.fa_sync_status() == fa.FA_OK

@@ -12,6 +12,7 @@
 
 #include "fa.h"
 #include "fa_combine.cuh"
+#include "fa_fwd256_kernel.cuh"
 #include "fa_fwd_kernel.cuh"
 #include "fa_host.h"
 
@@ -163,14 +164,15 @@ bool on_device(const void *p, int dev) {
 // 3-D map over a contiguous BH x N x d 16-bit tensor, box = 64 columns x 128 rows,
 // 128-byte swizzle; rows past N read as zero. Q is mapped by row space
 // (n_spaces x R x d), K and V by head.
-bool make_map(CUtensorMap *map, const void *base, bool bf16, int64_t BH, int64_t N, int64_t d) {
+bool make_map(CUtensorMap *map, const void *base, bool bf16, int64_t BH, int64_t N, int64_t d,
+              uint32_t box_rows = 128) {
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return false;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                                 static_cast<cuuint64_t>(BH)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * 2),
                                    static_cast<cuuint64_t>(N * d * 2)};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(d < 64 ? d : 64), 128, 1};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(d < 64 ? d : 64), box_rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r =
         enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
@@ -272,6 +274,72 @@ cudaError_t launch_combine(const fa::CombineParams &c, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// Head dimension 256: its own kernel (one 128-row Q tile per unit, 64-key K/V
+// tiles), for queries and keys at the same positions and without key splits.
+struct D256State {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+};
+D256State g_d256[kMaxDevices];
+
+fa_status run_forward_256(const Call &c, DeviceState *ds, int dev) {
+    if (c.Nq != c.Nk || c.num_splits != 1) return FA_ERR_UNSUPPORTED;
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+    D256State &s = g_d256[dev];
+    std::call_once(s.once, [&s] {
+        constexpr int smem = fa::d256::Smem::kAlloc;
+        cudaError_t e = cudaFuncSetAttribute(fa::d256::fa_fwd256_kernel<false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(fa::d256::fa_fwd256_kernel<true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        s.err = e;
+    });
+    if (s.err != cudaSuccess) return FA_ERR_CUDA;
+    const int64_t B = c.B, H = c.H, H_kv = c.H_kv, N = c.Nq, d = 256;
+    const bool bf16 = c.dtype == FA_DTYPE_BF16;
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, c.Q, bf16, B * H, N, d, fa::d256::kBM) ||
+        !make_map(&mk, c.K, bf16, B * H_kv, N, d, fa::d256::kBN) ||
+        !make_map(&mv, c.V, bf16, B * H_kv, N, d, fa::d256::kBN))
+        return FA_ERR_CUDA;
+    fa::d256::Params p{};
+    p.O = c.O;
+    p.LSE = c.LSE;
+    p.N = static_cast<int>(N);
+    p.H = static_cast<int>(H);
+    p.kv_group = static_cast<int>(H / H_kv);
+    const int64_t n_qb = (N + fa::d256::kBM - 1) / fa::d256::kBM;
+    const int64_t n_units = B * H * n_qb;
+    if (n_units > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+    p.n_units = static_cast<int>(n_units);
+    p.n_qb = static_cast<int>(n_qb);
+    int64_t wl = N, wr = N;
+    if (c.mask_mode == FA_MASK_CAUSAL) wr = 0;
+    if (c.mask_mode == FA_MASK_WINDOW) {
+        wl = c.window_left < N ? c.window_left : N;
+        wr = c.window_right < N ? c.window_right : N;
+    }
+    p.wl = static_cast<int>(wl);
+    p.wr = static_cast<int>(wr);
+    p.heavy_first = wr < N ? 1 : 0;
+    p.scale_log2 = static_cast<float>(static_cast<double>(c.scale) * 1.4426950408889634074);
+    p.wait_budget_ns = wait_budget();
+    p.status = ds->status;
+    p.sched = ds->sched + 2 * (g_sched_next.fetch_add(1) % kSchedSlots);
+    const unsigned blocks = static_cast<unsigned>(n_units < ds->sm_count ? n_units : ds->sm_count);
+    cudaStream_t st = static_cast<cudaStream_t>(c.stream);
+    if (bf16)
+        fa::d256::fa_fwd256_kernel<true><<<blocks, fa::d256::kThreads, fa::d256::Smem::kAlloc, st>>>(
+            mq, mk, mv, p);
+    else
+        fa::d256::fa_fwd256_kernel<false><<<blocks, fa::d256::kThreads, fa::d256::Smem::kAlloc, st>>>(
+            mq, mk, mv, p);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    g_launches.fetch_add(1);
+    return FA_OK;
+}
+
 fa_status run_forward(const Call &c) {
     const void *Q = c.Q, *K = c.K, *V = c.V;
     void *O = c.O;
@@ -294,7 +362,7 @@ fa_status run_forward(const Call &c) {
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
         return FA_ERR_INVALID_ARG;
     if (c.num_splits < 1) return FA_ERR_INVALID_ARG;
-    if (d != 32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (d != 32 && d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
     // Size limits of this implementation: 32-bit row indices and grid.
     if (Nq > (int64_t{1} << 29) || Nk > (int64_t{1} << 29) || B * H > (int64_t{1} << 31))
         return FA_ERR_UNSUPPORTED;
@@ -341,6 +409,7 @@ fa_status run_forward(const Call &c) {
     if (!on_device(Q, dev) || !on_device(K, dev) || !on_device(V, dev) || !on_device(O, dev) ||
         !on_device(LSE, dev) || (split && !on_device(c.workspace, dev)))
         return FA_ERR_INVALID_ARG;
+    if (d == 256) return run_forward_256(c, ds, dev);
 
     const bool bf16 = c.dtype == FA_DTYPE_BF16;
     CUtensorMap mq, mk, mv;

@@ -1,0 +1,518 @@
+// fa_fwd256_kernel.cuh -- attention forward for head dimension 256 on sm_103a.
+//
+// Same method as fa_fwd_kernel.cuh (tiles of Q against K/V blocks, online softmax
+// with a lazily moved reference max, P in tensor memory, O divided by l once;
+// "ai6s.net/6af30f4d40858c2d8819b6d5" §2.2-§2.5), shaped for d = 256, where two
+// 128-row Q tiles would need 2 x 256 TMEM columns for O alone and 128-key K/V
+// tiles 64 KB each:
+//   * a unit is one 128-row Q tile (64 KB of shared memory);
+//   * K/V tiles hold 64 keys (32 KB each): K ring 3 deep, V ring 2 deep;
+//   * S is formed in one of three 64-column TMEM buffers, so that the softmax of
+//     block j runs while S(j+1) and S(j+2) are computed; O (256 columns) stays in
+//     TMEM for the unit. MMA order: ... O += P(j) V_j | S(j+3) | O += P(j+1) V_{j+1} ...
+//   * one softmax warpgroup (thread = query row = TMEM lane, 64 keys per block).
+// When the reference max of a row moves (rare), the softmax thread rescales its O
+// row, after waiting for the product O += P(j-1) V_{j-1} to complete (two
+// alternating barriers, one per parity of j, so that a skipped wait never
+// confuses phases: a product two blocks later cannot complete first).
+//
+// Warps (256 threads): 0-3 softmax, 4 scheduler + Q and K producer, 5 MMA issuer,
+// 6 V producer, 7 idle. Every wait is bounded; on expiry the CTA records the
+// failure, drains its copies and MMAs, frees its tensor memory and returns.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+#include "ptx.cuh"
+
+namespace fa {
+namespace d256 {
+
+constexpr int D = 256;
+constexpr int kBM = 128;        // query rows per unit
+constexpr int kBN = 64;         // keys per K/V tile
+constexpr int kThreads = 256;
+constexpr int kTmaWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kVWarp = 6;
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
+constexpr int kSBufs = 3;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units, as in fa_fwd_kernel.cuh
+constexpr unsigned kStatusTimeout = 4;
+constexpr int kUnitSlots = 2;
+constexpr int kUnitConsumers = 6;  // warps 0-3, 5, 6 arrive once each per unit
+enum : int { kRoleSoftmax = 1, kRoleTma = 2, kRoleMma = 3 };
+
+struct Params {
+    void *O;
+    float *LSE;
+    int N, H, kv_group;
+    int n_units, n_qb;   // (b*H + h, 128-row block) units; blocks per head
+    int heavy_first;
+    int wl, wr;          // key j visible to query i iff i - wl <= j <= i + wr
+    float scale_log2;
+    unsigned long long wait_budget_ns;
+    unsigned int *status;
+    unsigned int *sched; // this launch's {next unit, finished CTAs}
+};
+
+struct Smem {
+    static constexpr int kQRegion = kBM * 128;   // 128 rows x 128 B (64 columns)
+    static constexpr int kKVRegion = kBN * 128;  // 64 rows x 128 B
+    static constexpr int kQBytes = 4 * kQRegion;
+    static constexpr int kKVBytes = 4 * kKVRegion;
+    static constexpr int kQ = 0;
+    static constexpr int kK = kQ + kQBytes;
+    static constexpr int kV = kK + kKStages * kKVBytes;
+    static constexpr int kBar = kV + kVStages * kKVBytes;
+    static constexpr int kNumBars = 32;
+    static constexpr int kMisc = kBar + kNumBars * 8;
+    static constexpr int kUnitRing = kMisc + 16;
+    static constexpr int kBytes = kUnitRing + 16;
+    static constexpr int kAlloc = kBytes + 1024;
+};
+
+enum : int {
+    kBarQFull = 0,
+    kBarQEmpty = 1,
+    kBarKFull = 2,       // + stage (3)
+    kBarKEmpty = 5,      // + stage (3)
+    kBarVFull = 8,       // + stage (2)
+    kBarVEmpty = 10,     // + stage (2)
+    kBarSFull = 12,      // + buffer (3)
+    kBarPFull = 15,      // + buffer (3)
+    kBarPVDone = 18,     // + parity of the block (2)
+    kBarODone = 20,
+    kBarOFree = 21,
+    kBarUnitFull = 22,   // + slot (2)
+    kBarUnitEmpty = 24,  // + slot (2)
+    kBarDrainIdx = 26,
+    kNumBarsUsed = 27,
+};
+static_assert(kNumBarsUsed <= Smem::kNumBars, "barrier slots");
+
+// TMEM columns: S buffers at 64 b, O at 256.
+constexpr uint32_t kTmemS = 0;
+constexpr uint32_t kTmemO = 256;
+
+struct Unit {
+    int bh, bkv, r0, j0, j1;
+};
+
+__device__ __forceinline__ Unit decode(int u, const Params &p) {
+    Unit U;
+    U.bh = u / p.n_qb;
+    int qb = u - U.bh * p.n_qb;
+    if (p.heavy_first) qb = p.n_qb - 1 - qb;
+    const int b = U.bh / p.H, h = U.bh - b * p.H;
+    U.bkv = b * (p.H / p.kv_group) + h / p.kv_group;
+    U.r0 = qb * kBM;
+    const int rl = min(U.r0 + kBM, p.N) - 1;
+    U.j0 = max(0, U.r0 - p.wl) / kBN;
+    U.j1 = min(p.N - 1, rl + p.wr) / kBN;
+    return U;
+}
+
+__device__ __forceinline__ void record_timeout(const Params &p, volatile int *abort_flag, int role,
+                                               int unit) {
+    *abort_flag = 1;
+    if (atomicCAS(p.status, 0u, kStatusTimeout) == 0u) {
+        p.status[1] = static_cast<unsigned>(role);
+        p.status[2] = static_cast<unsigned>(unit);
+        p.status[3] = blockIdx.x;
+        __threadfence();
+    }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_fwd256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const Params p) {
+    using L = Smem;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sQ = sbase + L::kQ;
+    const uint32_t bar0 = sbase + L::kBar;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
+    volatile int *unit_ring = reinterpret_cast<volatile int *>(smem + L::kUnitRing);
+    auto bar = [bar0](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+    auto sK = [sbase](int t) { return sbase + L::kK + (t % kKStages) * L::kKVBytes; };
+    auto sV = [sbase](int t) { return sbase + L::kV + (t % kVStages) * L::kKVBytes; };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint64_t budget = p.wait_budget_ns;
+
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == kTmaWarp * 32) {
+        mbar_init(bar(kBarQFull), 1);
+        mbar_init(bar(kBarQEmpty), 1);
+        for (int s = 0; s < kKStages; ++s) {
+            mbar_init(bar(kBarKFull + s), 1);
+            mbar_init(bar(kBarKEmpty + s), 1);
+        }
+        for (int s = 0; s < kVStages; ++s) {
+            mbar_init(bar(kBarVFull + s), 1);
+            mbar_init(bar(kBarVEmpty + s), 1);
+        }
+        for (int b = 0; b < kSBufs; ++b) {
+            mbar_init(bar(kBarSFull + b), 1);
+            mbar_init(bar(kBarPFull + b), 128);
+        }
+        mbar_init(bar(kBarPVDone + 0), 1);
+        mbar_init(bar(kBarPVDone + 1), 1);
+        mbar_init(bar(kBarODone), 1);
+        mbar_init(bar(kBarOFree), 128);
+        for (int k = 0; k < kUnitSlots; ++k) {
+            mbar_init(bar(kBarUnitFull + k), 1);
+            mbar_init(bar(kBarUnitEmpty + k), kUnitConsumers);
+        }
+        mbar_init(bar(kBarDrainIdx), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    // Take the next unit id from this role's ring slot (every role walks the same
+    // sequence of units, published by the producer). Returns -1 at the end.
+    auto take_unit = [&](int unit_iter, bool &ok) -> int {
+        const int slot = unit_iter % kUnitSlots;
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarUnitFull + slot),
+                                                       (unit_iter / kUnitSlots) & 1, abort_flag, budget));
+        if (!ok) return -1;
+        const int u = unit_ring[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarUnitEmpty + slot));
+        return u;
+    };
+
+    if (warp == kTmaWarp) {
+        // ================================================================ scheduler, Q and K
+        if (lane == 0) {
+            int t = 0, unit_iter = 0, q_loads = 0;
+            bool ok = true;
+            auto publish = [&](int k) -> int {
+                const int slot = k % kUnitSlots;
+                ok = mbar_wait_bounded(bar(kBarUnitEmpty + slot), ((k / kUnitSlots) & 1) ^ 1,
+                                       abort_flag, budget);
+                if (!ok) return -1;
+                const unsigned next = atomicAdd(p.sched, 1u);
+                const int v = next < static_cast<unsigned>(p.n_units) ? static_cast<int>(next) : -1;
+                unit_ring[slot] = v;
+                mbar_arrive(bar(kBarUnitFull + slot));
+                return v;
+            };
+            int u = publish(0);
+            for (; ok && u >= 0; ++unit_iter) {
+                const Unit U = decode(u, p);
+                ok = mbar_wait_bounded(bar(kBarQEmpty), (unit_iter & 1) ^ 1, abort_flag, budget);
+                if (!ok) break;
+                mbar_arrive_expect_tx(bar(kBarQFull), L::kQBytes);
+                for (int g = 0; g < 4; ++g)
+                    tma_load_3d(sQ + g * L::kQRegion, &tmQ, bar(kBarQFull), 64 * g, U.r0, U.bh);
+                ++q_loads;
+                int u_next = -1;
+                bool claimed = false;
+                for (int j = U.j0; ok && j <= U.j1; ++j, ++t) {
+                    if (!claimed && (j == U.j0 + 2 || j == U.j1)) {
+                        claimed = true;
+                        u_next = publish(unit_iter + 1);
+                        if (!ok) break;
+                        if (u_next >= 0) {
+                            const Unit W = decode(u_next, p);
+                            for (int g = 0; g < 4; ++g) tma_prefetch_l2_3d(&tmQ, 64 * g, W.r0, W.bh);
+                        }
+                    }
+                    const int st = t % kKStages;
+                    ok = mbar_wait_bounded(bar(kBarKEmpty + st), ((t / kKStages) & 1) ^ 1, abort_flag, budget);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar(kBarKFull + st), L::kKVBytes);
+                    for (int g = 0; g < 4; ++g)
+                        tma_load_3d(sK(t) + g * L::kKVRegion, &tmK, bar(kBarKFull + st), 64 * g,
+                                    j * kBN, U.bkv);
+                }
+                if (!claimed && ok) u_next = publish(unit_iter + 1);
+                u = u_next;
+            }
+            if (!ok) record_timeout(p, abort_flag, kRoleTma, u);
+            if (q_loads > 0) mbar_wait_bounded(bar(kBarQFull), (q_loads - 1) & 1, nullptr, budget);
+            for (int s = 0; s < kKStages; ++s)
+                if (t > s) {
+                    const int last = t - 1 - ((t - 1 - s) % kKStages);
+                    mbar_wait_bounded(bar(kBarKFull + s), (last / kKStages) & 1, nullptr, budget);
+                }
+        }
+    } else if (warp == kVWarp) {
+        // ================================================================ V producer
+        int t = 0;
+        bool ok = true;
+        for (int unit_iter = 0; ok; ++unit_iter) {
+            const int u = take_unit(unit_iter, ok);
+            if (!ok || u < 0) break;
+            const Unit U = decode(u, p);
+            if (lane == 0) {
+                for (int j = U.j0; ok && j <= U.j1; ++j, ++t) {
+                    const int st = t % kVStages;
+                    ok = mbar_wait_bounded(bar(kBarVEmpty + st), ((t / kVStages) & 1) ^ 1, abort_flag, budget);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar(kBarVFull + st), L::kKVBytes);
+                    for (int g = 0; g < 4; ++g)
+                        tma_load_3d(sV(t) + g * L::kKVRegion, &tmV, bar(kBarVFull + st), 64 * g,
+                                    j * kBN, U.bkv);
+                }
+            }
+            ok = __all_sync(0xffffffffu, ok);
+            t = __shfl_sync(0xffffffffu, t, 0);
+        }
+        if (!ok && lane == 0) record_timeout(p, abort_flag, kRoleTma, -1);
+        if (lane == 0)
+            for (int s = 0; s < kVStages; ++s)
+                if (t > s) {
+                    const int last = t - 1 - ((t - 1 - s) % kVStages);
+                    mbar_wait_bounded(bar(kBarVFull + s), (last / kVStages) & 1, nullptr, budget);
+                }
+    } else if (warp == kMmaWarp) {
+        // ================================================================ MMA issuer
+        constexpr uint32_t idesc_s = idesc_f16_ab(BF16, kBM, kBN, false, false);
+        constexpr uint32_t idesc_o = idesc_f16_ab(BF16, kBM, D, false, true);
+        auto wait = [&](int b, uint32_t parity) {
+            return __all_sync(0xffffffffu, mbar_wait_bounded(bar(b), parity, abort_flag, budget));
+        };
+        auto commit = [&](int b) {
+            if (elect_one()) umma_commit(bar(b));
+            __syncwarp();
+        };
+        // S(t) = Q K_t^T into S buffer t mod 3 (64 columns).
+        auto issue_s = [&](int t) {
+            tc_fence_after();
+            const uint64_t dq = sw128_desc(sQ, 16, 1024);
+            const uint64_t dk = sw128_desc(sK(t), 16, 1024);
+            if (elect_one()) {
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t offq = (k >> 2) * (L::kQRegion >> 4) + (k & 3) * 2;
+                    const uint32_t offk = (k >> 2) * (L::kKVRegion >> 4) + (k & 3) * 2;
+                    umma_f16_ss(tmem + kTmemS + (t % kSBufs) * kBN, dq + offq, dk + offk, idesc_s,
+                                k > 0 ? 1u : 0u);
+                }
+                umma_commit(bar(kBarSFull + t % kSBufs));
+            }
+            __syncwarp();
+        };
+        // O (+)= P(t) V_t, P read from the first 32 columns of S buffer t mod 3.
+        auto issue_pv = [&](int t, bool first) {
+            tc_fence_after();
+            const uint64_t dv = sw128_desc(sV(t), L::kKVRegion, 1024);
+            const uint32_t acc0 = first ? 0u : 1u;
+            if (elect_one()) {
+#pragma unroll
+                for (int k = 0; k < kBN / 16; ++k)
+                    umma_f16_ts(tmem + kTmemO, tmem + kTmemS + (t % kSBufs) * kBN + k * 8,
+                                dv + k * ((16 * 128) >> 4), idesc_o, k > 0 ? 1u : acc0);
+                umma_commit(bar(kBarPVDone + (t & 1)));
+            }
+            __syncwarp();
+        };
+        int t = 0;  // K/V blocks issued so far over all units
+        bool ok = true;
+        int unit_iter = 0, u = -1;
+        for (; ok; ++unit_iter) {
+            u = take_unit(unit_iter, ok);
+            if (!ok || u < 0) break;
+            const Unit U = decode(u, p);
+            const int n = U.j1 - U.j0 + 1;
+            ok = wait(kBarQFull, unit_iter & 1);
+            // S for the first min(3, n) blocks
+            for (int x = 0; ok && x < n && x < kSBufs; ++x) {
+                ok = wait(kBarKFull + (t + x) % kKStages, ((t + x) / kKStages) & 1);
+                if (ok) {
+                    issue_s(t + x);
+                    commit(kBarKEmpty + (t + x) % kKStages);  // K is read by S only
+                }
+            }
+            for (int x = 0; ok && x < n; ++x, ++t) {
+                ok = wait(kBarPFull + t % kSBufs, (t / kSBufs) & 1) &&
+                     wait(kBarVFull + t % kVStages, (t / kVStages) & 1);
+                if (ok && x == 0 && unit_iter > 0) ok = wait(kBarOFree, (unit_iter - 1) & 1);
+                if (!ok) break;
+                issue_pv(t, x == 0);
+                commit(kBarVEmpty + t % kVStages);
+                if (x + kSBufs < n) {
+                    ok = wait(kBarKFull + (t + kSBufs) % kKStages, ((t + kSBufs) / kKStages) & 1);
+                    if (!ok) break;
+                    issue_s(t + kSBufs);  // reuses buffer t mod 3 after O += P(t) V_t
+                    commit(kBarKEmpty + (t + kSBufs) % kKStages);
+                }
+            }
+            if (!ok) break;
+            commit(kBarQEmpty);
+            commit(kBarODone);
+        }
+        if (!ok && lane == 0) record_timeout(p, abort_flag, kRoleMma, u);
+        if (elect_one()) umma_commit(bar(kBarDrainIdx));
+        __syncwarp();
+        if (lane == 0) mbar_wait_bounded(bar(kBarDrainIdx), 0, nullptr, budget);
+        __syncwarp();
+    } else if (warp < 4) {
+        // ================================================================ softmax warpgroup
+        const int row = threadIdx.x & 127;
+        const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const float sl2 = p.scale_log2;
+        int t = 0;
+        bool ok = true;
+        int unit_iter = 0, u = -1;
+        for (; ok; ++unit_iter) {
+            u = take_unit(unit_iter, ok);
+            if (!ok || u < 0) break;
+            const Unit U = decode(u, p);
+            const int i = U.r0 + row;
+            const int rl = min(U.r0 + kBM, p.N) - 1;
+            const int lo_i = max(0, i - p.wl);
+            const int hi_i = min(p.N - 1, i + p.wr);
+            const int lo_last = max(0, rl - p.wl);
+            const int hi_first = min(p.N - 1, U.r0 + p.wr);
+            float m = -INFINITY, l = 0.f;
+            for (int j = U.j0; j <= U.j1; ++j, ++t) {
+                const uint32_t tS = tl + kTmemS + (t % kSBufs) * kBN;
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarSFull + t % kSBufs), (t / kSBufs) & 1,
+                                                               abort_flag, budget));
+                if (!ok) break;
+                tc_fence_after();
+                float x[kBN];
+                {
+                    uint32_t a[32], b[32];
+                    tmem_ld32(tS, a);
+                    tmem_ld32(tS + 32, b);
+                    tmem_ld_wait(a);
+                    tmem_ld_wait(b);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        x[c] = __uint_as_float(a[c]);
+                        x[c + 32] = __uint_as_float(b[c]);
+                    }
+                }
+                const int kv0 = j * kBN;
+                if (!(kv0 >= lo_last && kv0 + kBN - 1 <= hi_first)) {
+#pragma unroll
+                    for (int c = 0; c < kBN; ++c)
+                        if (kv0 + c < lo_i || kv0 + c > hi_i) x[c] = -INFINITY;
+                }
+                float ma = fmaxf(x[0], x[1]), mb = fmaxf(x[2], x[3]);
+#pragma unroll
+                for (int c = 4; c < kBN; c += 4) {
+                    ma = max3f(ma, x[c], x[c + 1]);
+                    mb = max3f(mb, x[c + 2], x[c + 3]);
+                }
+                const float m_tile = fmaxf(ma, mb) * sl2;
+                const float m_old = m;
+                if (m_tile > m + kRescaleThreshold) m = m_tile;
+                const float corr = m != m_old ? ex2_approx(m_old - m) : 1.f;
+                const float nm = m == -INFINITY ? 0.f : -m;
+                float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+                for (int c = 0; c < kBN; c += 2) {
+                    ffma2(x[c], x[c + 1], sl2, sl2, nm, nm);
+                    x[c] = ex2_approx(x[c]);
+                    x[c + 1] = ex2_approx(x[c + 1]);
+                }
+#pragma unroll
+                for (int c = 0; c < kBN; c += 4) {
+                    fadd2(s0, s1, x[c], x[c + 1]);
+                    fadd2(s2, s3, x[c + 2], x[c + 3]);
+                }
+                uint32_t pk[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) pk[e] = pack2<BF16>(x[2 * e], x[2 * e + 1]);
+                tmem_st16(tS, pk);
+                tmem_st16(tS + 16, pk + 16);
+                l = l * corr + ((s0 + s1) + (s2 + s3));
+                // The reference max moved: O holds the sum through block j-1 once that
+                // product completes; rescale this row's O before P(j) is released.
+                if (j > U.j0 && __any_sync(0xffffffffu, corr != 1.f)) {
+                    const int tp = t - 1;
+                    ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarPVDone + (tp & 1)), (tp >> 1) & 1,
+                                                                   abort_flag, budget));
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(tl + kTmemO + c * 32, o);
+                        tmem_ld_wait(o);
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            float a0 = __uint_as_float(o[e]), a1 = __uint_as_float(o[e + 1]);
+                            fmul2(a0, a1, corr, corr);
+                            o[e] = __float_as_uint(a0);
+                            o[e + 1] = __float_as_uint(a1);
+                        }
+                        tmem_st32(tl + kTmemO + c * 32, o);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(bar(kBarPFull + t % kSBufs));
+            }
+            if (!ok) break;
+            // ---- epilogue: O / l rounded to 16 bit, LSE = ln 2 (m + log2 l)
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarODone), unit_iter & 1, abort_flag, budget));
+            if (!ok) break;
+            tc_fence_after();
+            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            const bool store = i < p.N;
+            const size_t grow = static_cast<size_t>(U.bh) * p.N + (store ? i : 0);
+            uint8_t *orow = reinterpret_cast<uint8_t *>(p.O) + grow * (D * 2);
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(tl + kTmemO + c * 32, o);
+                tmem_ld_wait(o);
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    pk[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
+                if (store) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 64);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                }
+            }
+            if (store) p.LSE[grow] = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+            tc_fence_before();
+            mbar_arrive(bar(kBarOFree));
+        }
+        if (!ok && lane == 0) record_timeout(p, abort_flag, kRoleSoftmax, u);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+            atomicExch(p.sched, 0u);
+            atomicExch(p.sched + 1, 0u);
+        }
+    }
+}
+
+}  // namespace d256
+}  // namespace fa

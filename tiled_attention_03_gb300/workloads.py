@@ -103,6 +103,9 @@ EXTRA_WORKLOADS = [
              0, 0, seed=8, H_kv=8, Nq=512, splits=0),
     # head dimension 32 (64-byte swizzled tiles) on the bench shape
     Workload("full_b4h32n4096d32", 4, 32, 4096, 32, torch.bfloat16, MASK_NONE, 0, 0, seed=13),
+    # head dimension 256 (its own kernel), same FLOPs as the bench shape
+    Workload("full_b4h16n4096d256", 4, 16, 4096, 256, torch.bfloat16, MASK_NONE, 0, 0, seed=14),
+    Workload("causal_b4h16n4096d256", 4, 16, 4096, 256, torch.bfloat16, MASK_CAUSAL, 0, 0, seed=15),
 ]
 
 # Backward pass on the bench shape (dO drawn after Q, K, V from the same generator).
