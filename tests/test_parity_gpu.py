@@ -148,6 +148,22 @@ def test_forward_host_tensors():
     compare(o, lse, q, k, v, 0.125, "causal")
 
 
+def test_forward_host_tensors_pipelined_into_caller_buffers():
+    """Several batch entries (copies and kernels overlapped per entry), GQA, the
+    caller's pinned result buffers; and a rectangular (Nq < Nk) host call."""
+    q, _, _ = make_qkv(3, 8, 257, 128, torch.bfloat16, seed=11)
+    _, k, v = make_qkv(3, 2, 257, 128, torch.bfloat16, seed=12, H_kv=2)
+    out = torch.full(q.shape, -7.0, dtype=q.dtype).pin_memory()
+    lse_out = torch.full(q.shape[:-1], -7.0).pin_memory()
+    o, lse = fa.forward(q.pin_memory(), k.pin_memory(), v.pin_memory(), 0.09, "causal",
+                        out=out, lse_out=lse_out)
+    assert o.data_ptr() == out.data_ptr() and lse.data_ptr() == lse_out.data_ptr()
+    compare(o, lse, q, k, v, 0.09, "causal")
+    q2 = q[:, :, -5:].contiguous()
+    o2, l2 = fa.forward(q2, k, v, 0.09, "causal")
+    compare(o2, l2, q2, k, v, 0.09, "causal")
+
+
 def test_rejects_host_pointer_in_abi():
     q, k, v = make_qkv(1, 1, 64, 64, torch.float16, seed=0)
     lib = fa.load_library()

@@ -178,40 +178,73 @@ def fa_forward_gqa(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.T
 
 
 def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
-            mask="none", window=(0, 0), stream=None, num_splits: int | None = None):
+            mask="none", window=(0, 0), stream=None, num_splits: int | None = None,
+            out: torch.Tensor | None = None, lse_out: torch.Tensor | None = None):
     """Attention forward: returns (O, LSE). K and V may have fewer heads than Q
     (grouped-query attention: H_kv must divide H) and more positions than Q (the
     queries are then the last positions; this runs the split-KV entry point, as
     does any num_splits, with 0 meaning its default).
 
     Device tensors run in place on the device. Host tensors are copied to the
-    current CUDA device, processed, and the results copied back to host
-    memory (pinned host inputs make these copies asynchronous).
+    current CUDA device, processed, and copied back: batch entry by batch entry,
+    with the copy in of entry b+1, the kernel on entry b and the copy out of entry
+    b-1 on three streams, so copies and compute overlap. Pinned host inputs make
+    the copies asynchronous; `out` / `lse_out` (host, pinned) receive the results
+    and avoid allocating them per call.
     """
-    host = not q.is_cuda
     if scale is None:
         scale = q.shape[-1] ** -0.5
-    if host:
-        dev = torch.device("cuda", torch.cuda.current_device())
-        q = q.to(dev, non_blocking=True)
-        k = k.to(dev, non_blocking=True)
-        v = v.to(dev, non_blocking=True)
+    if q.is_cuda:
+        q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+        o = torch.empty_like(q) if out is None else out
+        lse = (torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+               if lse_out is None else lse_out)
+        _forward_device(q, k, v, o, lse, scale, mask, window, stream, num_splits)
+        return o, lse
+    dev = torch.device("cuda", torch.cuda.current_device())
     q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
-    o = torch.empty_like(q)
-    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    if lse_out is None:
+        lse_out = torch.empty(q.shape[:-1], dtype=torch.float32, pin_memory=True)
+    qd = torch.empty(q.shape, dtype=q.dtype, device=dev)
+    kd = torch.empty(k.shape, dtype=k.dtype, device=dev)
+    vd = torch.empty(v.shape, dtype=v.dtype, device=dev)
+    od = torch.empty_like(qd)
+    lsed = torch.empty(q.shape[:-1], dtype=torch.float32, device=dev)
+    compute = torch.cuda.current_stream(dev) if stream is None else stream
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    s_in.wait_stream(compute)
+    for b in range(q.shape[0]):
+        with torch.cuda.stream(s_in):
+            qd[b].copy_(q[b], non_blocking=True)
+            kd[b].copy_(k[b], non_blocking=True)
+            vd[b].copy_(v[b], non_blocking=True)
+        e_in = torch.cuda.Event()
+        e_in.record(s_in)
+        compute.wait_event(e_in)
+        sl = slice(b, b + 1)
+        _forward_device(qd[sl], kd[sl], vd[sl], od[sl], lsed[sl], scale, mask, window, compute,
+                        num_splits)
+        e_k = torch.cuda.Event()
+        e_k.record(compute)
+        s_out.wait_event(e_k)
+        with torch.cuda.stream(s_out):
+            out[b].copy_(od[b], non_blocking=True)
+            lse_out[b].copy_(lsed[b], non_blocking=True)
+    for t in (qd, kd, vd, od, lsed):
+        t.record_stream(s_in)
+        t.record_stream(s_out)
+    s_out.synchronize()
+    return out, lse_out
+
+
+def _forward_device(q, k, v, o, lse, scale, mask, window, stream, num_splits):
     if num_splits is not None or q.shape[2] != k.shape[2]:
         fa_forward_splitkv(q, k, v, o, lse, scale, mask, window[0], window[1],
                            num_splits or 0, None, stream)
     else:
         fa_forward_gqa(q, k, v, o, lse, scale, mask, window[0], window[1], stream)
-    if host:
-        o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-        lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-        o_h.copy_(o, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
-        return o_h, lse_h
-    return o, lse
 
 
 def fa_splitkv_workspace_bytes(B: int, H: int, Nq: int, d: int, num_splits: int) -> int:
