@@ -650,6 +650,9 @@ bool make_map(CUtensorMap *map, const void *base, bool bf16, int64_t BH, int64_t
 }
 uint64_t wait_budget() { return ::wait_budget(); }
 void count_launches(int64_t n) { g_launches += n; }
+unsigned int *next_sched_slot(unsigned int *base) {
+    return base + 2 * (g_sched_next.fetch_add(1) % kSchedSlots);
+}
 
 }  // namespace fa_host
 

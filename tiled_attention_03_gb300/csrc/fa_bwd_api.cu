@@ -206,6 +206,8 @@ fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O
     fa::bwd::BwdParams pkv = p, pq = p;
     pkv.n_units = static_cast<int>(BHkv * n_blk);  // (K/V head, key block)
     pq.n_units = static_cast<int>(BH * n_blk);     // (query head, query block)
+    pkv.sched = fa_host::next_sched_slot(info.sched);
+    pq.sched = fa_host::next_sched_slot(info.sched);
     pq.heavy_first = wrv < N ? 1 : 0;              // later blocks see more keys
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);

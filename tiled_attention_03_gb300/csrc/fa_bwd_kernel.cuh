@@ -85,7 +85,13 @@ struct BwdParams {
     float scale;
     unsigned long long wait_budget_ns;
     unsigned int *status;     // [code, role, unit, block]
+    unsigned int *sched;      // this launch's {next unit, finished CTAs} counters (zero at launch)
 };
+
+// Units are taken from a launch-wide counter by the TMA producer and handed to
+// the other roles through a two-slot ring in shared memory (id -1 ends every
+// role's loop), so that CTAs that finish early take more of the units.
+constexpr int kUnitSlots = 2;
 
 __device__ __forceinline__ void bwd_record_timeout(const BwdParams &p, volatile int *abort_flag,
                                                    int role, int unit) {
@@ -95,6 +101,18 @@ __device__ __forceinline__ void bwd_record_timeout(const BwdParams &p, volatile 
         p.status[2] = static_cast<unsigned>(unit);
         p.status[3] = blockIdx.x;
         __threadfence();
+    }
+}
+
+// The last CTA to finish zeroes this launch's scheduler counters for the next
+// launch that uses them (every CTA has stopped taking units by now).
+__device__ __forceinline__ void release_sched(const BwdParams &p) {
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+            atomicExch(p.sched, 0u);
+            atomicExch(p.sched + 1, 0u);
+        }
     }
 }
 
@@ -121,8 +139,8 @@ struct KvSmem {
     static constexpr int kL = kO + kOStages * kTileBytes;      // + s * kVecBytes
     static constexpr int kDv = kL + kQStages * kVecBytes;
     static constexpr int kBar = kDv + kOStages * kVecBytes;
-    static constexpr int kNumBars = 24;
-    static constexpr int kMisc = kBar + kNumBars * 8;          // tmem slot, abort flag
+    static constexpr int kNumBars = 32;
+    static constexpr int kMisc = kBar + kNumBars * 8;          // tmem slot, abort flag, unit ring
     static constexpr int kBytes = kMisc + 16;
     // Slack to align the base to 1024 B when it fits; without it (d = 128) the
     // kernel checks the base's alignment itself.
@@ -146,7 +164,10 @@ enum : int {
     kKvQEmpty = 13,
     kKvOFull = 17,   // + dO stage (<= 4)
     kKvOEmpty = 21,  // .. 24
+    kKvUnitFull = 25,   // + slot (2)
+    kKvUnitEmpty = 27,  // + slot (2)
 };
+constexpr int kKvUnitConsumers = 9;  // the MMA warp and the 8 compute warps
 
 template <int D>
 struct KvTmem {
@@ -222,6 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar0 = sbase + L::kBar;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
+    volatile int *unit_ring = reinterpret_cast<volatile int *>(smem + L::kMisc + 8);
     auto bar = [bar0](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
     // Ring slot of query block `it` (counted over this CTA's whole sequence).
     auto sQ = [sbase](int it) { return sbase + L::kQ + (it % kQS) * L::kTileBytes; };
@@ -254,6 +276,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(kKvDSReady), 256);
         mbar_init(bar(kKvFree), 256);
         mbar_init(bar(kKvDrain), 1);
+        for (int k = 0; k < kUnitSlots; ++k) {
+            mbar_init(bar(kKvUnitFull + k), 1);
+            mbar_init(bar(kKvUnitEmpty + k), kKvUnitConsumers);
+        }
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmQ);
@@ -273,8 +299,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int it = 0, unit_iter = 0, kv_loads = 0, q_loads = 0;
             bool ok = true;
-            int u = blockIdx.x;
-            for (; ok && u < p.n_units; u += gridDim.x, ++unit_iter) {
+            auto publish = [&](int k) -> int {
+                const int slot = k % kUnitSlots;
+                ok = mbar_wait_bounded(bar(kKvUnitEmpty + slot), ((k / kUnitSlots) & 1) ^ 1,
+                                       abort_flag, budget);
+                if (!ok) return -1;
+                const unsigned next = atomicAdd(p.sched, 1u);
+                const int v = next < static_cast<unsigned>(p.n_units) ? static_cast<int>(next) : -1;
+                unit_ring[slot] = v;
+                mbar_arrive(bar(kKvUnitFull + slot));
+                return v;
+            };
+            int u = publish(0);
+            for (; ok && u >= 0; ++unit_iter) {
                 const KvUnit U = decode_kv_unit(u, p);
                 ok = mbar_wait_bounded(bar(kKvKVEmpty), (unit_iter & 1) ^ 1, abort_flag, budget);
                 if (!ok) break;
@@ -284,10 +321,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_3d(sV + g * kRegionBytes, &tmV, bar(kKvKVFull), 64 * g, U.k0, U.bkv);
                 }
                 ++kv_loads;
-                // The next unit's K and V go to L2 now; its shared-memory load waits
-                // for this unit's last products.
-                if (u + static_cast<int>(gridDim.x) < p.n_units) {
-                    const KvUnit W = decode_kv_unit(u + gridDim.x, p);
+                // Claim the next unit now; its K and V go to L2 while this unit runs
+                // (their shared-memory load waits for this unit's last products).
+                const int u_next = publish(unit_iter + 1);
+                if (!ok) break;
+                if (u_next >= 0) {
+                    const KvUnit W = decode_kv_unit(u_next, p);
                     for (int g = 0; g < kRegions; ++g) {
                         tma_prefetch_l2_3d(&tmK, 64 * g, W.k0, W.bkv);
                         tma_prefetch_l2_3d(&tmV, 64 * g, W.k0, W.bkv);
@@ -317,6 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_3d(sdO(it) + g * kRegionBytes, &tmdO, fb, 64 * g, i0, bh);
                     bulk_load(sbase + L::kDv + os * L::kVecBytes, p.Dw + vrow, L::kVecBytes, fb);
                 }
+                u = u_next;
             }
             if (!ok) bwd_record_timeout(p, abort_flag, kRoleTma, u);
             // Drain: no copy may still be landing in shared memory when the CTA exits.
@@ -380,10 +420,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
         };
-        int it = 0, unit_iter = 0;
+        int it = 0, unit_iter = 0, u = -1;
         bool ok = true;
-        int u = blockIdx.x;
-        for (; ok && u < p.n_units; u += gridDim.x, ++unit_iter) {
+        for (; ok; ++unit_iter) {
+            const int slot = unit_iter % kUnitSlots;
+            ok = wait(kKvUnitFull + slot, (unit_iter / kUnitSlots) & 1);
+            if (!ok) break;
+            u = unit_ring[slot];
+            __syncwarp();
+            if (elect_one()) mbar_arrive(bar(kKvUnitEmpty + slot));
+            __syncwarp();
+            if (u < 0) break;
             const KvUnit U = decode_kv_unit(u, p);
             auto qfull = [&](int i) { return wait(kKvQFull + i % kQS, (i / kQS) & 1); };
             auto ofull = [&](int i) { return wait(kKvOFull + i % kOS, (i / kOS) & 1); };
@@ -439,10 +486,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = threadIdx.x & 127;         // key row
         const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         const float sl2 = p.scale_log2;
-        int it = 0, unit_iter = 0;
+        int it = 0, unit_iter = 0, u = -1;
         bool ok = true;
-        int u = blockIdx.x;
-        for (; ok && u < p.n_units; u += gridDim.x, ++unit_iter) {
+        for (; ok; ++unit_iter) {
+            const int slot = unit_iter % kUnitSlots;
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kKvUnitFull + slot),
+                                                           (unit_iter / kUnitSlots) & 1, abort_flag, budget));
+            if (!ok) break;
+            u = unit_ring[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kKvUnitEmpty + slot));
+            if (u < 0) break;
             const KvUnit U = decode_kv_unit(u, p);
             const int key = U.k0 + r;
             const bool key_ok = key < p.N;
@@ -587,6 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+    release_sched(p);
 }
 
 // =============================================================================== dQ
@@ -602,7 +657,7 @@ struct QSmem {
     static constexpr int kK = kdO + kTileBytes;
     static constexpr int kV = kK + kKStages * kTileBytes;
     static constexpr int kBar = kV + kVStages * kTileBytes;
-    static constexpr int kNumBars = 24;
+    static constexpr int kNumBars = 32;
     static constexpr int kMisc = kBar + kNumBars * 8;
     static constexpr int kBytes = kMisc + 16;
     static constexpr int kAlloc = kBytes + 1024;
@@ -622,7 +677,10 @@ enum : int {
     kQKEmpty = 13,   // + stage
     kQVFull = 17,    // + stage
     kQVEmpty = 21,   // .. 24
+    kQUnitFull = 25,   // + slot (2)
+    kQUnitEmpty = 27,  // + slot (2)
 };
+constexpr int kQUnitConsumers = 10;  // the MMA warp, the V producer warp, the 8 compute warps
 
 template <int D>
 struct QTmem {
@@ -680,6 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar0 = sbase + L::kBar;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
+    volatile int *unit_ring = reinterpret_cast<volatile int *>(smem + L::kMisc + 8);
     auto bar = [bar0](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
     auto sK = [sbase](int st) { return sbase + L::kK + st * L::kTileBytes; };
     auto sV = [sbase](int st) { return sbase + L::kV + st * L::kTileBytes; };
@@ -702,6 +761,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(kQDone), 1);
         mbar_init(bar(kQFree), 256);
         mbar_init(bar(kQDrain), 1);
+        for (int k = 0; k < kUnitSlots; ++k) {
+            mbar_init(bar(kQUnitFull + k), 1);
+            mbar_init(bar(kQUnitEmpty + k), kQUnitConsumers);
+        }
         for (int s = 0; s < kKS; ++s) {
             mbar_init(bar(kQKFull + s), 1);
             mbar_init(bar(kQKEmpty + s), 1);
@@ -734,9 +797,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             const CUtensorMap *map = kq ? &tmK : &tmV;
             int t = 0, unit_iter = 0, q_loads = 0;
             bool ok = true;
-            int u = blockIdx.x;
-            for (; ok && u < p.n_units; u += gridDim.x, ++unit_iter) {
+            // warp 8 claims units and publishes them; warp 10 takes them like the other roles
+            auto publish = [&](int k) -> int {
+                const int slot = k % kUnitSlots;
+                ok = mbar_wait_bounded(bar(kQUnitEmpty + slot), ((k / kUnitSlots) & 1) ^ 1,
+                                       abort_flag, budget);
+                if (!ok) return -1;
+                const unsigned next = atomicAdd(p.sched, 1u);
+                const int v = next < static_cast<unsigned>(p.n_units) ? static_cast<int>(next) : -1;
+                unit_ring[slot] = v;
+                mbar_arrive(bar(kQUnitFull + slot));
+                return v;
+            };
+            auto take = [&](int k) -> int {
+                const int slot = k % kUnitSlots;
+                ok = mbar_wait_bounded(bar(kQUnitFull + slot), (k / kUnitSlots) & 1, abort_flag, budget);
+                if (!ok) return -1;
+                const int v = unit_ring[slot];
+                mbar_arrive(bar(kQUnitEmpty + slot));
+                return v;
+            };
+            int u = kq ? publish(0) : take(0);
+            for (; ok && u >= 0; ++unit_iter) {
                 const QUnit U = decode_q_unit(u, p);
+                int u_next = -1;
                 if (kq) {
                     ok = mbar_wait_bounded(bar(kQQEmpty), (unit_iter & 1) ^ 1, abort_flag, budget);
                     if (!ok) break;
@@ -746,10 +830,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_3d(sdO + g * kRegionBytes, &tmdO, bar(kQQFull), 64 * g, U.i0, U.bh);
                     }
                     ++q_loads;
-                    // The next unit's Q and dO go to L2 now; their shared-memory load
-                    // waits for this unit's last products.
-                    if (u + static_cast<int>(gridDim.x) < p.n_units) {
-                        const QUnit W = decode_q_unit(u + gridDim.x, p);
+                    // Claim the next unit now; its Q and dO go to L2 while this unit
+                    // runs (their shared-memory load waits for this unit's products).
+                    u_next = publish(unit_iter + 1);
+                    if (!ok) break;
+                    if (u_next >= 0) {
+                        const QUnit W = decode_q_unit(u_next, p);
                         for (int g = 0; g < kRegions; ++g) {
                             tma_prefetch_l2_3d(&tmQ, 64 * g, W.i0, W.bh);
                             tma_prefetch_l2_3d(&tmdO, 64 * g, W.i0, W.bh);
@@ -765,6 +851,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int g = 0; g < kRegions; ++g)
                         tma_load_3d(dst + g * kRegionBytes, map, bar(full0 + st), 64 * g, j * kTile, U.bkv);
                 }
+                if (!ok) break;
+                if (!kq) u_next = take(unit_iter + 1);
+                u = u_next;
             }
             if (!ok) bwd_record_timeout(p, abort_flag, kRoleTma, u);
             // Drain: no copy may still be landing in shared memory when the CTA exits.
@@ -821,10 +910,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         auto kfull = [&](int t) { return wait(kQKFull + t % kKS, (t / kKS) & 1); };
         auto vfull = [&](int t) { return wait(kQVFull + t % kVS, (t / kVS) & 1); };
-        int t = 0, unit_iter = 0;
+        int t = 0, unit_iter = 0, u = -1;
         bool ok = true;
-        int u = blockIdx.x;
-        for (; ok && u < p.n_units; u += gridDim.x, ++unit_iter) {
+        for (; ok; ++unit_iter) {
+            const int slot = unit_iter % kUnitSlots;
+            ok = wait(kQUnitFull + slot, (unit_iter / kUnitSlots) & 1);
+            if (!ok) break;
+            u = unit_ring[slot];
+            __syncwarp();
+            if (elect_one()) mbar_arrive(bar(kQUnitEmpty + slot));
+            __syncwarp();
+            if (u < 0) break;
             const QUnit U = decode_q_unit(u, p);
             const int n = U.j1 - U.j0 + 1;
             ok = wait(kQQFull, unit_iter & 1);
@@ -882,10 +978,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = threadIdx.x & 127;         // query row
         const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         const float sl2 = p.scale_log2;
-        int t = 0, unit_iter = 0;
+        int t = 0, unit_iter = 0, u = -1;
         bool ok = true;
-        int u = blockIdx.x;
-        for (; ok && u < p.n_units; u += gridDim.x, ++unit_iter) {
+        for (; ok; ++unit_iter) {
+            const int slot = unit_iter % kUnitSlots;
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kQUnitFull + slot),
+                                                           (unit_iter / kUnitSlots) & 1, abort_flag, budget));
+            if (!ok) break;
+            u = unit_ring[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kQUnitEmpty + slot));
+            if (u < 0) break;
             const QUnit U = decode_q_unit(u, p);
             const int i = U.i0 + r;
             const size_t vrow = static_cast<size_t>(U.bh) * p.Npad + i;
@@ -1006,6 +1109,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+    release_sched(p);
 }
 
 // =============================================================================== prep

@@ -29,6 +29,9 @@ bool on_device(const void *p, int dev);
 bool make_map(CUtensorMap *map, const void *base, bool bf16, int64_t BH, int64_t N, int64_t d);
 uint64_t wait_budget();
 void count_launches(int64_t n);
+// The scheduler counters of one launch (a slot of the device's static array,
+// zero at launch; the launch's last CTA zeroes it again).
+unsigned int *next_sched_slot(unsigned int *base);
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 }  // namespace fa_host
