@@ -153,7 +153,7 @@ constexpr unsigned kStatusLayout = 2;  // FA_ERR_UNSUPPORTED: shared memory base
 enum : int {
     kKvKVFull = 0,
     kKvKVEmpty = 1,
-    kKvSFull = 2,
+    kKvSFull = 2,    // + S^T buffer (a second one at 29 when double-buffered)
     kKvDPFull = 3,
     kKvDone = 4,
     kKvPReady = 5,
@@ -166,6 +166,7 @@ enum : int {
     kKvOEmpty = 21,  // .. 24
     kKvUnitFull = 25,   // + slot (2)
     kKvUnitEmpty = 27,  // + slot (2)
+    kKvSFull1 = 29,
 };
 constexpr int kKvUnitConsumers = 9;  // the MMA warp and the 8 compute warps
 
@@ -175,7 +176,12 @@ struct KvTmem {
     static constexpr uint32_t kDP = 128;     // dP^T, then dS^T (16-bit) over 128-159, 192-223
     static constexpr uint32_t kDV = 256;
     static constexpr uint32_t kDK = 256 + D;
+    // d = 64 leaves 128 columns for a second S^T buffer (query block n uses buffer
+    // n mod 2), so S^T(n+2) needs only dV(n) before it, not the whole chain.
+    static constexpr bool kDoubleS = D == 64;
+    static constexpr uint32_t kS1 = kDoubleS ? 256 + 2 * D : kS;
     static_assert(D == 64 || D == 128, "head dim");
+    __device__ static constexpr uint32_t s_buf(int it) { return (kDoubleS && (it & 1)) ? kS1 : kS; }
 };
 
 // A dK/dV unit: key block kb (keys k0 .. k0+127) of K/V head bkv; the query
@@ -270,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(kKvOEmpty + s), 1);
         }
         mbar_init(bar(kKvSFull), 1);
+        mbar_init(bar(kKvSFull1), 1);
         mbar_init(bar(kKvDPFull), 1);
         mbar_init(bar(kKvDone), 1);
         mbar_init(bar(kKvPReady), 256);
@@ -434,27 +441,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             const KvUnit U = decode_kv_unit(u, p);
             auto qfull = [&](int i) { return wait(kKvQFull + i % kQS, (i / kQS) & 1); };
             auto ofull = [&](int i) { return wait(kKvOFull + i % kOS, (i / kOS) & 1); };
+            // S^T(i) into its buffer, completion on that buffer's barrier
+            auto issue_sT = [&](int i) {
+                issue_kk(sK, sQ(i), T::s_buf(i));
+                commit(T::kDoubleS && (i & 1) ? kKvSFull1 : kKvSFull);
+            };
             ok = wait(kKvKVFull, unit_iter & 1);
-            // prologue: S^T and dP^T of the unit's first query block
+            // prologue: S^T and dP^T of the unit's first query block (and S^T of the
+            // second one when S^T is double-buffered)
             if (ok) ok = qfull(it);
             if (!ok) break;
-            issue_kk(sK, sQ(it), T::kS);
-            commit(kKvSFull);
+            issue_sT(it);
             ok = ofull(it);
             if (!ok) break;
             issue_kk(sV, sdO(it), T::kDP);
             commit(kKvDPFull);
+            if (T::kDoubleS && U.n_it > 1) {
+                ok = qfull(it + 1);
+                if (!ok) break;
+                issue_sT(it + 1);
+            }
             for (int n = 0; ok && n < U.n_it; ++n, ++it) {
                 ok = wait(kKvPReady, it & 1);
                 if (ok && n == 0 && unit_iter > 0) ok = wait(kKvFree, (unit_iter - 1) & 1);
                 if (!ok) break;
-                issue_tn(T::kS, sdO(it), T::kDV, n > 0);  // dV += P^T dO
-                commit(kKvOEmpty + it % kOS);             // dO(n), D no longer read
-                if (n + 1 < U.n_it) {
+                issue_tn(T::s_buf(it), sdO(it), T::kDV, n > 0);  // dV += P^T dO
+                commit(kKvOEmpty + it % kOS);                    // dO(n), D no longer read
+                if (!T::kDoubleS && n + 1 < U.n_it) {
                     ok = qfull(it + 1);
                     if (!ok) break;
-                    issue_kk(sK, sQ(it + 1), T::kS);  // S^T(n+1)
-                    commit(kKvSFull);
+                    issue_sT(it + 1);  // S^T(n+1) over P^T(n), after dV read it
                 }
                 ok = wait(kKvDSReady, it & 1);
                 if (!ok) break;
@@ -465,6 +481,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) break;
                     issue_kk(sV, sdO(it + 1), T::kDP);  // dP^T(n+1)
                     commit(kKvDPFull);
+                }
+                if (T::kDoubleS && n + 2 < U.n_it) {
+                    ok = qfull(it + 2);
+                    if (!ok) break;
+                    issue_sT(it + 2);  // into the buffer of S^T(n), after dV(n)
                 }
             }
             if (!ok) break;
@@ -511,14 +532,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool boundary = !(i0 + kTile - 1 - p.wl <= U.k0 && U.k0 + kTile - 1 <= i0 + p.wr);
                 const int q0 = i0 + 64 * wg;
                 // ---- P^T = 2^(S^T * scale * log2 e - LSE * log2 e)
-                ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kKvSFull), it & 1, abort_flag, budget));
+                const uint32_t sb = T::s_buf(it);
+                const int sfb = T::kDoubleS && (it & 1) ? kKvSFull1 : kKvSFull;
+                const uint32_t sph = T::kDoubleS ? (it >> 1) & 1 : it & 1;
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(sfb), sph, abort_flag, budget));
                 if (!ok) break;
                 tc_fence_after();
                 float pr[64];
                 {
                     uint32_t a[32], b[32];
-                    tmem_ld32(tl + T::kS + 64 * wg, a);
-                    tmem_ld32(tl + T::kS + 64 * wg + 32, b);
+                    tmem_ld32(tl + sb + 64 * wg, a);
+                    tmem_ld32(tl + sb + 64 * wg + 32, b);
                     tmem_ld_wait(a);
                     tmem_ld_wait(b);
 #pragma unroll
@@ -557,8 +581,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t pk[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) pk[e] = pack2<BF16>(pr[2 * e], pr[2 * e + 1]);
-                    tmem_st16(tl + T::kS + 64 * wg, pk);
-                    tmem_st16(tl + T::kS + 64 * wg + 16, pk + 16);
+                    tmem_st16(tl + sb + 64 * wg, pk);
+                    tmem_st16(tl + sb + 64 * wg + 16, pk + 16);
                 }
                 tmem_st_wait();
                 tc_fence_before();
