@@ -232,6 +232,30 @@ fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O
 /* Workspace bytes fa_backward needs (0 for invalid sizes). */
 size_t fa_backward_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d);
 
+/*
+ * fa_backward_varlen -- fa_backward for a variable-length batch laid out as in
+ * fa_forward_varlen (token-major; sequence b owns query tokens cu_seqlens_q[b]
+ * .. cu_seqlens_q[b+1]-1 and keys cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1, its
+ * queries at its last key positions). O and LSE are fa_forward_varlen's
+ * outputs; dO and dQ are total_q x H x d, dK and dV total_k x H_kv x d.
+ * max_seqlen_q / max_seqlen_k bound every sequence's lengths. Gradients of
+ * keys that no query sees, and of queries that see no key, are zero.
+ * `workspace`: fa_backward_varlen_workspace_bytes(B, H, total_q) bytes, 16-byte
+ * aligned. d is 64 or 128. Deterministic. Errors as fa_backward; the device
+ * arrays are clamped to the tensors, as in fa_forward_varlen.
+ */
+fa_status fa_backward_varlen(const void *Q, const void *K, const void *V, const void *O,
+                             const void *dO, const float *LSE, const int32_t *cu_seqlens_q,
+                             const int32_t *cu_seqlens_k, void *dQ, void *dK, void *dV, int64_t B,
+                             int64_t H, int64_t H_kv, int64_t total_q, int64_t total_k,
+                             int64_t max_seqlen_q, int64_t max_seqlen_k, int64_t d, float scale,
+                             fa_mask_mode mask_mode, int64_t window_left, int64_t window_right,
+                             fa_dtype dtype, void *workspace, size_t workspace_bytes,
+                             void *stream);
+
+/* Workspace bytes fa_backward_varlen needs (0 for invalid sizes). */
+size_t fa_backward_varlen_workspace_bytes(int64_t B, int64_t H, int64_t total_q);
+
 /* Static, NUL-terminated description of a status code. Never NULL. */
 const char *fa_status_string(fa_status status);
 

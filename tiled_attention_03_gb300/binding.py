@@ -71,6 +71,12 @@ def load_library(path: str = LIB) -> ctypes.CDLL:
     lib.fa_forward_varlen.restype = ctypes.c_int
     lib.fa_forward_varlen.argtypes = [ctypes.c_void_p] * 7 + [ctypes.c_int64] * 7 + [
         ctypes.c_float, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]
+    lib.fa_backward_varlen.restype = ctypes.c_int
+    lib.fa_backward_varlen.argtypes = [ctypes.c_void_p] * 11 + [ctypes.c_int64] * 8 + [
+        ctypes.c_float, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+        ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    lib.fa_backward_varlen_workspace_bytes.restype = ctypes.c_size_t
+    lib.fa_backward_varlen_workspace_bytes.argtypes = [ctypes.c_int64] * 3
     lib.fa_backward.restype = ctypes.c_int
     lib.fa_backward.argtypes = [ctypes.c_void_p] * 9 + [ctypes.c_int64] * 5 + [
         ctypes.c_float, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
@@ -377,3 +383,35 @@ def fa_forward_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torc
                                _DTYPES[q.dtype], _stream_handle(stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_forward_varlen")
+
+
+def fa_backward_varlen_workspace_bytes(B: int, H: int, total_q: int) -> int:
+    return load_library().fa_backward_varlen_workspace_bytes(B, H, total_q)
+
+
+def fa_backward_varlen(q, k, v, o, do, lse, cu_seqlens_q, cu_seqlens_k, dq, dk, dv,
+                       max_seqlen_q: int, max_seqlen_k: int, scale: float, mask_mode=FA_MASK_NONE,
+                       window_left: int = 0, window_right: int = 0, workspace=None,
+                       stream=None) -> None:
+    """Enqueue fa_backward_varlen: q, o, do, dq (total_q, H, d); k, v, dk, dv
+    (total_k, H_kv, d); lse (total_q, H) float32; cu_seqlens_* int32 (B + 1,)."""
+    lib = load_library()
+    ts = (q, k, v, o, do, lse, cu_seqlens_q, cu_seqlens_k, dq, dk, dv)
+    if any(not t.is_cuda or not t.is_contiguous() for t in ts) or q.dim() != 3 or k.dim() != 3:
+        raise FaError(FA_ERR_INVALID_ARG, "fa_backward_varlen")
+    total_q, H, d = q.shape
+    total_k, H_kv = k.shape[0], k.shape[1]
+    B = cu_seqlens_q.numel() - 1
+    need = fa_backward_varlen_workspace_bytes(B, H, total_q)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    rc = lib.fa_backward_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                do.data_ptr(), lse.data_ptr(), cu_seqlens_q.data_ptr(),
+                                cu_seqlens_k.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                dv.data_ptr(), B, H, H_kv, total_q, total_k, int(max_seqlen_q),
+                                int(max_seqlen_k), d, float(scale), _MASKS[mask_mode],
+                                int(window_left), int(window_right), _DTYPES[q.dtype],
+                                workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_backward_varlen")

@@ -649,6 +649,10 @@ bool make_map(CUtensorMap *map, const void *base, bool bf16, int64_t BH, int64_t
     return ::make_map(map, base, bf16, BH, N, d);
 }
 uint64_t wait_budget() { return ::wait_budget(); }
+bool make_map_tokens(CUtensorMap *map, const void *base, bool bf16, int64_t tokens, int64_t heads,
+                     int64_t d) {
+    return ::make_map_tokens(map, base, bf16, tokens, heads, d);
+}
 void count_launches(int64_t n) { g_launches += n; }
 unsigned int *next_sched_slot(unsigned int *base) {
     return base + 2 * (g_sched_next.fetch_add(1) % kSchedSlots);

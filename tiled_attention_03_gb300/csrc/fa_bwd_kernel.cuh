@@ -40,6 +40,7 @@
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -86,7 +87,34 @@ struct BwdParams {
     unsigned long long wait_budget_ns;
     unsigned int *status;     // [code, role, unit, block]
     unsigned int *sched;      // this launch's {next unit, finished CTAs} counters (zero at launch)
+    // Variable-length batches (kernel template flag VARLEN): token-major tensors,
+    // sequence b owns query tokens cu_q[b] .. cu_q[b+1]-1 and keys cu_k[b] ..
+    // cu_k[b+1]-1 (clamped to [0, total]); its queries stand at its last positions.
+    // The row terms of sequence b, head h start at h * vstride + cu_pad[b] (each
+    // sequence padded to 128 rows); n_blk counts blocks of the longest sequence.
+    const int *cu_q, *cu_k, *cu_pad;
+    int total_q, total_k, vstride;
 };
+
+// This sequence's sizes and first rows (variable-length batches only).
+struct SeqInfo {
+    int nq, nk, q_off, q_tok0, k_tok0, pad0;
+};
+
+__device__ __forceinline__ SeqInfo seq_info(int b, const BwdParams &p) {
+    SeqInfo S;
+    const int q0 = min(max(p.cu_q[b], 0), p.total_q);
+    const int q1 = min(max(p.cu_q[b + 1], q0), p.total_q);
+    const int k0 = min(max(p.cu_k[b], 0), p.total_k);
+    const int k1 = min(max(p.cu_k[b + 1], k0), p.total_k);
+    S.nq = q1 - q0;
+    S.nk = k1 - k0;
+    S.q_off = S.nk - S.nq;
+    S.q_tok0 = q0;
+    S.k_tok0 = k0;
+    S.pad0 = p.cu_pad[b];
+    return S;
+}
 
 // Units are taken from a launch-wide counter by the TMA producer and handed to
 // the other roles through a two-slot ring in shared memory (id -1 ends every
@@ -189,28 +217,89 @@ struct KvTmem {
 // head see one of its keys: n_it = group * nib iterations. Units are numbered
 // head-major, so that the CTAs running at the same time share the Q and dO of
 // a few heads in L2.
-struct KvUnit {
+struct KvUnitBase {
     int bkv, k0, ib_lo, nib, n_it;
 };
+template <bool VARLEN>
+struct KvUnit : KvUnitBase {};
+template <>
+struct KvUnit<true> : KvUnitBase, SeqInfo {};
 
-__device__ __forceinline__ KvUnit decode_kv_unit(int u, const BwdParams &p) {
-    KvUnit U;
+// Problem sizes of a unit: the launch's (queries and keys at the same N
+// positions), or its sequence's.
+template <typename U_>
+__device__ __forceinline__ int u_nq(const U_ &U, const BwdParams &p) {
+    if constexpr (std::is_base_of<SeqInfo, U_>::value) return U.nq;
+    else return p.N;
+}
+template <typename U_>
+__device__ __forceinline__ int u_nk(const U_ &U, const BwdParams &p) {
+    if constexpr (std::is_base_of<SeqInfo, U_>::value) return U.nk;
+    else return p.N;
+}
+template <typename U_>
+__device__ __forceinline__ int u_qoff(const U_ &U) {
+    if constexpr (std::is_base_of<SeqInfo, U_>::value) return U.q_off;
+    else return 0;
+}
+
+// n_it = 0 marks a unit without work (a key block past its sequence's end).
+template <bool VARLEN>
+__device__ __forceinline__ KvUnit<VARLEN> decode_kv_unit(int u, const BwdParams &p) {
+    KvUnit<VARLEN> U;
     U.bkv = u / p.n_blk;
     U.k0 = (u - U.bkv * p.n_blk) * kTile;
-    const int k1 = min(U.k0 + kTile, p.N) - 1;
-    const int q_lo = max(0, U.k0 - p.wr);
-    const int q_hi = min(p.N - 1, k1 + p.wl);
+    if constexpr (VARLEN) static_cast<SeqInfo &>(U) = seq_info(U.bkv / p.Hkv, p);
+    const int nq = u_nq(U, p), nk = u_nk(U, p), q_off = u_qoff(U);
+    const int k1 = min(U.k0 + kTile, nk) - 1;
+    const int q_lo = max(0, U.k0 - q_off - p.wr);
+    const int q_hi = min(nq - 1, k1 - q_off + p.wl);
     U.ib_lo = q_lo / kTile;
     U.nib = q_hi / kTile - U.ib_lo + 1;
-    U.n_it = p.group * U.nib;
+    U.n_it = (U.k0 < nk && q_lo <= q_hi) ? p.group * U.nib : 0;
     return U;
 }
 
-__device__ __forceinline__ void kv_unit_iter(const KvUnit &U, int n, const BwdParams &p, int &bh,
+template <typename U_>
+__device__ __forceinline__ void kv_unit_iter(const U_ &U, int n, const BwdParams &p, int &bh,
                                              int &i0) {
     const int g = n / U.nib;
     bh = group_head(U.bkv, g, p);
     i0 = (U.ib_lo + (n - g * U.nib)) * kTile;
+}
+
+// Row of the row-term vectors (L, D) for query row i0 of query head bh.
+template <typename U_>
+__device__ __forceinline__ size_t vec_row(const U_ &U, int bh, int i0, const BwdParams &p) {
+    if constexpr (std::is_base_of<SeqInfo, U_>::value)
+        return static_cast<size_t>(bh % p.H) * p.vstride + U.pad0 + i0;
+    else
+        return static_cast<size_t>(bh) * p.Npad + i0;
+}
+
+// TMA coordinates (y, z) of a 128-row Q / dO tile and of a K / V tile: dense maps
+// are (d, N, heads), variable-length maps (d, heads, tokens).
+template <typename U_>
+__device__ __forceinline__ void q_coords(const U_ &U, int bh, int i0, const BwdParams &p, int &y,
+                                         int &z) {
+    if constexpr (std::is_base_of<SeqInfo, U_>::value) {
+        y = bh % p.H;
+        z = U.q_tok0 + i0;
+    } else {
+        y = i0;
+        z = bh;
+    }
+}
+template <typename U_>
+__device__ __forceinline__ void kv_coords(const U_ &U, int bkv, int k0, const BwdParams &p, int &y,
+                                          int &z) {
+    if constexpr (std::is_base_of<SeqInfo, U_>::value) {
+        y = bkv % p.Hkv;
+        z = U.k_tok0 + k0;
+    } else {
+        y = k0;
+        z = bkv;
+    }
 }
 
 // Per query block n of a unit the MMA warp issues
@@ -218,7 +307,7 @@ __device__ __forceinline__ void kv_unit_iter(const KvUnit &U, int n, const BwdPa
 // S^T(n+1) overwrites the P^T(n) that the dV product before it reads, and
 // dP^T(n+1) the dS^T(n) of the dK product before it: tcgen05.mma operations of
 // one thread execute in issue order, so each read precedes the later write.
-template <int D, bool BF16>
+template <int D, bool BF16, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -311,7 +400,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = mbar_wait_bounded(bar(kKvUnitEmpty + slot), ((k / kUnitSlots) & 1) ^ 1,
                                        abort_flag, budget);
                 if (!ok) return -1;
-                const unsigned next = atomicAdd(p.sched, 1u);
+                unsigned next = atomicAdd(p.sched, 1u);
+                if constexpr (VARLEN)  // key blocks past their sequence's end have no work
+                    while (next < static_cast<unsigned>(p.n_units) &&
+                           decode_kv_unit<VARLEN>(static_cast<int>(next), p).n_it == 0)
+                        next = atomicAdd(p.sched, 1u);
                 const int v = next < static_cast<unsigned>(p.n_units) ? static_cast<int>(next) : -1;
                 unit_ring[slot] = v;
                 mbar_arrive(bar(kKvUnitFull + slot));
@@ -319,13 +412,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             int u = publish(0);
             for (; ok && u >= 0; ++unit_iter) {
-                const KvUnit U = decode_kv_unit(u, p);
+                const auto U = decode_kv_unit<VARLEN>(u, p);
                 ok = mbar_wait_bounded(bar(kKvKVEmpty), (unit_iter & 1) ^ 1, abort_flag, budget);
                 if (!ok) break;
                 mbar_arrive_expect_tx(bar(kKvKVFull), 2 * L::kTileBytes);
+                int ky, kz;
+                kv_coords(U, U.bkv, U.k0, p, ky, kz);
                 for (int g = 0; g < kRegions; ++g) {
-                    tma_load_3d(sK + g * kRegionBytes, &tmK, bar(kKvKVFull), 64 * g, U.k0, U.bkv);
-                    tma_load_3d(sV + g * kRegionBytes, &tmV, bar(kKvKVFull), 64 * g, U.k0, U.bkv);
+                    tma_load_3d(sK + g * kRegionBytes, &tmK, bar(kKvKVFull), 64 * g, ky, kz);
+                    tma_load_3d(sV + g * kRegionBytes, &tmV, bar(kKvKVFull), 64 * g, ky, kz);
                 }
                 ++kv_loads;
                 // Claim the next unit now; its K and V go to L2 while this unit runs
@@ -333,16 +428,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int u_next = publish(unit_iter + 1);
                 if (!ok) break;
                 if (u_next >= 0) {
-                    const KvUnit W = decode_kv_unit(u_next, p);
+                    const auto W = decode_kv_unit<VARLEN>(u_next, p);
+                    int wy, wz;
+                    kv_coords(W, W.bkv, W.k0, p, wy, wz);
                     for (int g = 0; g < kRegions; ++g) {
-                        tma_prefetch_l2_3d(&tmK, 64 * g, W.k0, W.bkv);
-                        tma_prefetch_l2_3d(&tmV, 64 * g, W.k0, W.bkv);
+                        tma_prefetch_l2_3d(&tmK, 64 * g, wy, wz);
+                        tma_prefetch_l2_3d(&tmV, 64 * g, wy, wz);
                     }
                 }
                 for (int n = 0; ok && n < U.n_it; ++n, ++it) {
                     int bh, i0;
                     kv_unit_iter(U, n, p, bh, i0);
-                    const size_t vrow = static_cast<size_t>(bh) * p.Npad + i0;
+                    const size_t vrow = vec_row(U, bh, i0, p);
+                    int qy, qz;
+                    q_coords(U, bh, i0, p, qy, qz);
                     // Q_i and L of its rows
                     const int qs = it % kQS;
                     ok = mbar_wait_bounded(bar(kKvQEmpty + qs), ((it / kQS) & 1) ^ 1, abort_flag, budget);
@@ -350,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t fb = bar(kKvQFull + qs);
                     mbar_arrive_expect_tx(fb, L::kTileBytes + L::kVecBytes);
                     for (int g = 0; g < kRegions; ++g)
-                        tma_load_3d(sQ(it) + g * kRegionBytes, &tmQ, fb, 64 * g, i0, bh);
+                        tma_load_3d(sQ(it) + g * kRegionBytes, &tmQ, fb, 64 * g, qy, qz);
                     bulk_load(sbase + L::kL + qs * L::kVecBytes, p.Lw + vrow, L::kVecBytes, fb);
                     ++q_loads;
                     // dO_i and D of its rows
@@ -360,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fb = bar(kKvOFull + os);
                     mbar_arrive_expect_tx(fb, L::kTileBytes + L::kVecBytes);
                     for (int g = 0; g < kRegions; ++g)
-                        tma_load_3d(sdO(it) + g * kRegionBytes, &tmdO, fb, 64 * g, i0, bh);
+                        tma_load_3d(sdO(it) + g * kRegionBytes, &tmdO, fb, 64 * g, qy, qz);
                     bulk_load(sbase + L::kDv + os * L::kVecBytes, p.Dw + vrow, L::kVecBytes, fb);
                 }
                 u = u_next;
@@ -438,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (elect_one()) mbar_arrive(bar(kKvUnitEmpty + slot));
             __syncwarp();
             if (u < 0) break;
-            const KvUnit U = decode_kv_unit(u, p);
+            const auto U = decode_kv_unit<VARLEN>(u, p);
             auto qfull = [&](int i) { return wait(kKvQFull + i % kQS, (i / kQS) & 1); };
             auto ofull = [&](int i) { return wait(kKvOFull + i % kOS, (i / kOS) & 1); };
             // S^T(i) into its buffer, completion on that buffer's barrier
@@ -518,9 +617,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kKvUnitEmpty + slot));
             if (u < 0) break;
-            const KvUnit U = decode_kv_unit(u, p);
+            const auto U = decode_kv_unit<VARLEN>(u, p);
             const int key = U.k0 + r;
-            const bool key_ok = key < p.N;
+            const bool key_ok = key < u_nk(U, p);
+            const int q_off = u_qoff(U);
             for (int n = 0; n < U.n_it; ++n, ++it) {
                 int bh, i0;
                 kv_unit_iter(U, n, p, bh, i0);
@@ -529,8 +629,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float *sDw =
                     reinterpret_cast<const float *>(smem + L::kDv + (it % kOS) * L::kVecBytes) + 64 * wg;
                 // Element masks unless every (query, key) pair of the tile is visible.
-                const bool boundary = !(i0 + kTile - 1 - p.wl <= U.k0 && U.k0 + kTile - 1 <= i0 + p.wr);
-                const int q0 = i0 + 64 * wg;
+                const bool boundary =
+                    !(i0 + kTile - 1 + q_off - p.wl <= U.k0 && U.k0 + kTile - 1 <= i0 + q_off + p.wr);
+                const int q0 = i0 + 64 * wg + q_off;  // key position of the first column's query
                 // ---- P^T = 2^(S^T * scale * log2 e - LSE * log2 e)
                 const uint32_t sb = T::s_buf(it);
                 const int sfb = T::kDoubleS && (it & 1) ? kKvSFull1 : kKvSFull;
@@ -631,8 +732,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             {
                 const float f = wg == 0 ? 1.f : p.scale;
-                uint8_t *out = reinterpret_cast<uint8_t *>(wg == 0 ? p.dV : p.dK) +
-                               (static_cast<size_t>(U.bkv) * p.N + (key_ok ? key : 0)) * (D * 2);
+                size_t orow;
+                if constexpr (VARLEN)
+                    orow = static_cast<size_t>(U.k_tok0 + (key_ok ? key : 0)) * p.Hkv + U.bkv % p.Hkv;
+                else
+                    orow = static_cast<size_t>(U.bkv) * p.N + (key_ok ? key : 0);
+                uint8_t *out = reinterpret_cast<uint8_t *>(wg == 0 ? p.dV : p.dK) + orow * (D * 2);
                 const uint32_t col = wg == 0 ? T::kDV : T::kDK;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
@@ -718,21 +823,30 @@ struct QTmem {
 // j0 .. j1 that hold a key one of its rows sees. Units are numbered head-major;
 // with heavy_first the blocks of a head run from the last one (most keys under
 // a causal mask) to the first.
-struct QUnit {
+struct QUnitBase {
     int bh, bkv, i0, j0, j1;
 };
+template <bool VARLEN>
+struct QUnit : QUnitBase {};
+template <>
+struct QUnit<true> : QUnitBase, SeqInfo {};
 
-__device__ __forceinline__ QUnit decode_q_unit(int u, const BwdParams &p) {
-    QUnit U;
+// j1 < j0 marks a unit without work (a query block past its sequence's end).
+template <bool VARLEN>
+__device__ __forceinline__ QUnit<VARLEN> decode_q_unit(int u, const BwdParams &p) {
+    QUnit<VARLEN> U;
     U.bh = u / p.n_blk;
     int ib = u - U.bh * p.n_blk;
     if (p.heavy_first) ib = p.n_blk - 1 - ib;
     const int b = U.bh / p.H, h = U.bh - b * p.H;
     U.bkv = b * p.Hkv + h / p.group;
+    if constexpr (VARLEN) static_cast<SeqInfo &>(U) = seq_info(b, p);
+    const int nq = u_nq(U, p), nk = u_nk(U, p), q_off = u_qoff(U);
     U.i0 = ib * kTile;
-    const int i1 = min(U.i0 + kTile, p.N) - 1;
-    U.j0 = max(0, U.i0 - p.wl) / kTile;
-    U.j1 = min(p.N - 1, i1 + p.wr) / kTile;
+    const int i1 = min(U.i0 + kTile, nq) - 1;
+    const int lo = max(0, U.i0 + q_off - p.wl), hi = min(nk - 1, i1 + q_off + p.wr);
+    U.j0 = lo / kTile;
+    U.j1 = (U.i0 < nq && lo <= hi) ? hi / kTile : U.j0 - 1;
     return U;
 }
 
@@ -742,7 +856,7 @@ __device__ __forceinline__ QUnit decode_q_unit(int u, const BwdParams &p) {
 // iteration t. S(t+2) reuses the buffer of S(t), whose dS the dQ product before
 // it reads (in-order execution), and dP(t+1) overwrites dP(t) only after the
 // compute warps reported dS(t) (and so have read dP(t)).
-template <int D, bool BF16>
+template <int D, bool BF16, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -827,7 +941,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = mbar_wait_bounded(bar(kQUnitEmpty + slot), ((k / kUnitSlots) & 1) ^ 1,
                                        abort_flag, budget);
                 if (!ok) return -1;
-                const unsigned next = atomicAdd(p.sched, 1u);
+                unsigned next = atomicAdd(p.sched, 1u);
+                if constexpr (VARLEN) {  // query blocks past their sequence's end have no work
+                    while (next < static_cast<unsigned>(p.n_units)) {
+                        const auto W = decode_q_unit<VARLEN>(static_cast<int>(next), p);
+                        if (W.j1 >= W.j0) break;
+                        next = atomicAdd(p.sched, 1u);
+                    }
+                }
                 const int v = next < static_cast<unsigned>(p.n_units) ? static_cast<int>(next) : -1;
                 unit_ring[slot] = v;
                 mbar_arrive(bar(kQUnitFull + slot));
@@ -843,15 +964,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             int u = kq ? publish(0) : take(0);
             for (; ok && u >= 0; ++unit_iter) {
-                const QUnit U = decode_q_unit(u, p);
+                const auto U = decode_q_unit<VARLEN>(u, p);
                 int u_next = -1;
                 if (kq) {
                     ok = mbar_wait_bounded(bar(kQQEmpty), (unit_iter & 1) ^ 1, abort_flag, budget);
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(kQQFull), 2 * L::kTileBytes);
+                    int qy, qz;
+                    q_coords(U, U.bh, U.i0, p, qy, qz);
                     for (int g = 0; g < kRegions; ++g) {
-                        tma_load_3d(sQ + g * kRegionBytes, &tmQ, bar(kQQFull), 64 * g, U.i0, U.bh);
-                        tma_load_3d(sdO + g * kRegionBytes, &tmdO, bar(kQQFull), 64 * g, U.i0, U.bh);
+                        tma_load_3d(sQ + g * kRegionBytes, &tmQ, bar(kQQFull), 64 * g, qy, qz);
+                        tma_load_3d(sdO + g * kRegionBytes, &tmdO, bar(kQQFull), 64 * g, qy, qz);
                     }
                     ++q_loads;
                     // Claim the next unit now; its Q and dO go to L2 while this unit
@@ -859,10 +982,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     u_next = publish(unit_iter + 1);
                     if (!ok) break;
                     if (u_next >= 0) {
-                        const QUnit W = decode_q_unit(u_next, p);
+                        const auto W = decode_q_unit<VARLEN>(u_next, p);
+                        int wy, wz;
+                        q_coords(W, W.bh, W.i0, p, wy, wz);
                         for (int g = 0; g < kRegions; ++g) {
-                            tma_prefetch_l2_3d(&tmQ, 64 * g, W.i0, W.bh);
-                            tma_prefetch_l2_3d(&tmdO, 64 * g, W.i0, W.bh);
+                            tma_prefetch_l2_3d(&tmQ, 64 * g, wy, wz);
+                            tma_prefetch_l2_3d(&tmdO, 64 * g, wy, wz);
                         }
                     }
                 }
@@ -872,8 +997,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) break;
                     const uint32_t dst = kq ? sK(st) : sV(st);
                     mbar_arrive_expect_tx(bar(full0 + st), L::kTileBytes);
+                    int ky, kz;
+                    kv_coords(U, U.bkv, j * kTile, p, ky, kz);
                     for (int g = 0; g < kRegions; ++g)
-                        tma_load_3d(dst + g * kRegionBytes, map, bar(full0 + st), 64 * g, j * kTile, U.bkv);
+                        tma_load_3d(dst + g * kRegionBytes, map, bar(full0 + st), 64 * g, ky, kz);
                 }
                 if (!ok) break;
                 if (!kq) u_next = take(unit_iter + 1);
@@ -945,7 +1072,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (elect_one()) mbar_arrive(bar(kQUnitEmpty + slot));
             __syncwarp();
             if (u < 0) break;
-            const QUnit U = decode_q_unit(u, p);
+            const auto U = decode_q_unit<VARLEN>(u, p);
             const int n = U.j1 - U.j0 + 1;
             ok = wait(kQQFull, unit_iter & 1);
             // prologue: S(t), dP(t), S(t+1)
@@ -1013,19 +1140,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kQUnitEmpty + slot));
             if (u < 0) break;
-            const QUnit U = decode_q_unit(u, p);
+            const auto U = decode_q_unit<VARLEN>(u, p);
             const int i = U.i0 + r;
-            const size_t vrow = static_cast<size_t>(U.bh) * p.Npad + i;
+            const size_t vrow = vec_row(U, U.bh, U.i0, p) + r;
             const float lw = p.Lw[vrow], dw = p.Dw[vrow];
+            const int nk = u_nk(U, p), q_off = u_qoff(U);
             // visible keys of query i
-            const int lo_i = max(0, i - p.wl);
-            const int hi_i = min(p.N - 1, i + p.wr);
+            const int lo_i = max(0, i + q_off - p.wl);
+            const int hi_i = min(nk - 1, i + q_off + p.wr);
             const int i1 = U.i0 + kTile - 1;
             for (int j = U.j0; j <= U.j1; ++j, ++t) {
                 const int k0 = j * kTile;
                 // Element masks unless every pair of the tile is visible and every key exists.
-                const bool boundary = !(i1 - p.wl <= k0 && k0 + kTile - 1 <= U.i0 + p.wr &&
-                                        k0 + kTile <= p.N);
+                const bool boundary = !(i1 + q_off - p.wl <= k0 && k0 + kTile - 1 <= U.i0 + q_off + p.wr &&
+                                        k0 + kTile <= nk);
                 const int kc0 = k0 + 64 * wg;
                 const uint32_t tS = tl + T::kS + (t & 1) * 128 + 64 * wg;
                 ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kQSFull + (t & 1)), (t >> 1) & 1,
@@ -1099,9 +1227,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             {
-                const bool store = i < p.N;
-                uint8_t *out = reinterpret_cast<uint8_t *>(p.dQ) +
-                               ((static_cast<size_t>(U.bh) * p.N + (store ? i : 0)) * D + wg * (D / 2)) * 2;
+                const bool store = i < u_nq(U, p);
+                size_t orow;
+                if constexpr (VARLEN)
+                    orow = static_cast<size_t>(U.q_tok0 + (store ? i : 0)) * p.H + U.bh % p.H;
+                else
+                    orow = static_cast<size_t>(U.bh) * p.N + (store ? i : 0);
+                uint8_t *out = reinterpret_cast<uint8_t *>(p.dQ) + (orow * D + wg * (D / 2)) * 2;
 #pragma unroll
                 for (int c = 0; c < D / 2; c += 32) {
                     uint32_t a[32];
@@ -1173,6 +1305,68 @@ __global__ void __launch_bounds__(kPrepWarps * 32) fa_bwd_prep_kernel(const Prep
     if (lane == 0) {
         p.Dw[row] = i < p.N ? dsum : 0.f;
         const float lse = i < p.N ? p.LSE[static_cast<size_t>(bh) * p.N + i] : -INFINITY;
+        p.Lw[row] = lse == -INFINITY ? INFINITY : lse * 1.4426950408889634f;
+    }
+}
+
+// ---- variable-length batches
+// Start of each sequence's row-term block: sum of the earlier sequences' query
+// counts, each rounded up to 128 (one thread; cu_pad has B + 1 entries).
+__global__ void fa_bwd_cu_pad_kernel(const int *cu_q, int B, int total_q, int *cu_pad) {
+    if (blockIdx.x != 0 || threadIdx.x != 0) return;
+    int acc = 0;
+    for (int b = 0; b < B; ++b) {
+        cu_pad[b] = acc;
+        const int q0 = min(max(cu_q[b], 0), total_q);
+        const int q1 = min(max(cu_q[b + 1], q0), total_q);
+        acc += (q1 - q0 + kTile - 1) / kTile * kTile;
+    }
+    cu_pad[B] = acc;
+}
+
+struct PrepVarlenParams {
+    const void *O, *dO;
+    const float *LSE;        // total_q x H
+    const int *cu_q, *cu_pad;
+    float *Lw, *Dw;          // H x vstride
+    int B, H, total_q, vstride;
+};
+
+// One warp per (head, padded row) of the row-term blocks: the row's sequence by
+// binary search in cu_pad, then D and L of its token as in fa_bwd_prep_kernel;
+// rows past a sequence's queries get D = 0, L = +inf.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kPrepWarps * 32) fa_bwd_prep_varlen_kernel(const PrepVarlenParams p) {
+    const int row = blockIdx.x * kPrepWarps + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= p.H * p.vstride) return;
+    const int h = row / p.vstride, r = row - h * p.vstride;
+    int lo = 0, hi = p.B;  // largest b with cu_pad[b] <= r
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (p.cu_pad[mid] <= r) lo = mid;
+        else hi = mid;
+    }
+    const int b = lo;
+    const int i = r - p.cu_pad[b];
+    const int q0 = min(max(p.cu_q[b], 0), p.total_q);
+    const int q1 = min(max(p.cu_q[b + 1], q0), p.total_q);
+    const bool valid = r < p.cu_pad[p.B] && i < q1 - q0;
+    float dsum = 0.f;
+    size_t t = 0;
+    if (valid) {
+        t = static_cast<size_t>(q0 + i) * p.H + h;  // token-major row of O, dO, LSE
+        constexpr int kPer = D / 32;
+        const uint16_t *o = reinterpret_cast<const uint16_t *>(p.O) + t * D + lane * kPer;
+        const uint16_t *g = reinterpret_cast<const uint16_t *>(p.dO) + t * D + lane * kPer;
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) dsum = fmaf(to_f32(g[e], BF16), to_f32(o[e], BF16), dsum);
+#pragma unroll
+        for (int s = 16; s > 0; s >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, s);
+    }
+    if (lane == 0) {
+        p.Dw[row] = valid ? dsum : 0.f;
+        const float lse = valid ? p.LSE[t] : -INFINITY;
         p.Lw[row] = lse == -INFINITY ? INFINITY : lse * 1.4426950408889634f;
     }
 }
