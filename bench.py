@@ -323,6 +323,38 @@ def run_e2e_varlen(args, w, host, max_q, mask, stream, dev, world, flops):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
 
+def run_e2e_varlen_bwd(args, w, host, max_q, mask, dev, world, flops):
+    """Variable-length backward through the public binding with pinned host
+    tensors: every step copies Q, K, V, O, LSE, dO and cu_seqlens to the device,
+    runs fa_backward_varlen and copies dQ, dK, dV back."""
+    import tiled_attention_03_gb300 as fa
+    pinned = [t.pin_memory() for t in host]
+    outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in host[:3]]
+
+    def run():
+        q, k, v, o, lse, do, cu = (t.to(dev, non_blocking=True) for t in pinned)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        fa.fa_backward_varlen(q, k, v, o, do, lse, cu, cu, dq, dk, dv, max_q, max_q, w.scale, mask,
+                              w.window_left, w.window_right)
+        for dst, g in zip(outs, (dq, dk, dv)):
+            dst.copy_(g, non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()
+
+    for _ in range(2):
+        run()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        run()
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / args.e2e_steps, world)
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    return {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+
 def run_e2e_bwd(args, w, host, mask, stream, dev, world, flops):
     """Backward through the public API (tiled_attention_03_gb300.backward) with
     pinned host tensors: every step copies Q, K, V, O, LSE and dO to the device,
@@ -389,17 +421,33 @@ def main():
     stream = torch.cuda.current_stream(dev)
 
     if w.varlen:
-        from tiled_attention_03_gb300.workloads import varlen_inputs, varlen_lengths
+        from tiled_attention_03_gb300.workloads import (varlen_inputs, varlen_lengths,
+                                                        workload_grad_output)
         splits = 1
         vq_h, vk_h, vv_h, cu_h = varlen_inputs(w)
         vq, vk, vv, cu = vq_h.to(dev), vk_h.to(dev), vv_h.to(dev), cu_h.to(dev)
         vo = torch.empty_like(vq)
         vlse = torch.empty(vq.shape[:2], dtype=torch.float32, device=dev)
         max_q = max(varlen_lengths(w))
-
-        def step():
+        if w.backward:
+            # O and LSE from one forward outside the timed region; a step is the backward
             fa.fa_forward_varlen(vq, vk, vv, vo, vlse, cu, cu, max_q, w.scale, mask,
                                  w.window_left, w.window_right, stream)
+            lens = varlen_lengths(w)
+            dfull = workload_grad_output(w)
+            do_h = torch.cat([dfull[b, :, :lens[b]].transpose(0, 1) for b in range(w.B)], 0).contiguous()
+            vdo = do_h.to(dev)
+            vdq, vdk, vdv = torch.empty_like(vq), torch.empty_like(vk), torch.empty_like(vv)
+            vws = torch.empty(fa.fa_backward_varlen_workspace_bytes(w.B, w.H, vq.shape[0]),
+                              dtype=torch.uint8, device=dev)
+
+            def step():
+                fa.fa_backward_varlen(vq, vk, vv, vo, vdo, vlse, cu, cu, vdq, vdk, vdv, max_q, max_q,
+                                      w.scale, mask, w.window_left, w.window_right, vws, stream)
+        else:
+            def step():
+                fa.fa_forward_varlen(vq, vk, vv, vo, vlse, cu, cu, max_q, w.scale, mask,
+                                     w.window_left, w.window_right, stream)
     elif w.backward:
         # O and LSE from one forward, outside the timed region; a step is the backward.
         from tiled_attention_03_gb300.workloads import workload_grad_output
@@ -462,7 +510,10 @@ def main():
 
     # ---- end to end through the public API with pinned host buffers
     e2e = None
-    if args.e2e_steps > 0 and w.varlen:
+    if args.e2e_steps > 0 and w.varlen and w.backward:
+        host = [vq_h, vk_h, vv_h, vo.cpu(), vlse.cpu(), do_h, cu_h]
+        e2e = run_e2e_varlen_bwd(args, w, host, max_q, mask, dev, world, flops)
+    elif args.e2e_steps > 0 and w.varlen:
         e2e = run_e2e_varlen(args, w, [vq_h, vk_h, vv_h, cu_h], max_q, mask, stream, dev, world,
                              flops)
     elif args.e2e_steps > 0 and w.backward:
@@ -487,7 +538,8 @@ def main():
             cpu_v, cores, sample, _ = cpu_oracle_rate(w, args.cpu_seconds)
             cpu = {"value": cpu_v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                    "sample": sample}
-        in_t = (vq, vk, vv) if w.varlen else (q, k, v, do) if w.backward else (q, k, v)
+        in_t = ((vq, vk, vv, vdo) if w.varlen and w.backward else (vq, vk, vv) if w.varlen
+                else (q, k, v, do) if w.backward else (q, k, v))
         in_bytes = sum(t.numel() * t.element_size() for t in in_t)
         line = {
             "metric": METRIC_BWD if w.backward else METRIC, "value": value, "unit": "TFLOP/s",
@@ -512,7 +564,8 @@ def main():
                           "frac": nbytes / (kernel_ms * 1e-3) / 1e9 / peak_gbs,
                           "peak_source": f"{peak_src} copy bandwidth"}) | {
                 "traffic": traffic, "algorithmic_bytes": nbytes,
-                "kernel": (f"fa_bwd prep + dK/dV + dQ kernels <{w.d}, {w.dtype_name}>" if w.backward
+                "kernel": (f"fa_bwd prep + dK/dV + dQ kernels <{w.d}, {w.dtype_name}"
+                           + (", varlen>" if w.varlen else ">") if w.backward
                            else f"fa_fwd_kernel<{w.d}, {w.dtype_name}, varlen>" if w.varlen
                            else f"fa_fwd256_kernel<{w.dtype_name}>" if w.d == 256
                            else f"fa_fwd_kernel<{w.d}, {w.dtype_name}>"

@@ -122,6 +122,9 @@ BWD_WORKLOADS = [
 VARLEN_WORKLOADS = [
     Workload("varlen_causal_b16h32n4096d128", 16, 32, 4096, 128, torch.bfloat16, MASK_CAUSAL, 0, 0,
              seed=12, varlen=True),
+    # its backward (dO drawn like the dense backward workloads, then packed)
+    Workload("bwd_varlen_causal_b16h32n4096d128", 16, 32, 4096, 128, torch.bfloat16, MASK_CAUSAL,
+             0, 0, seed=12, varlen=True, backward=True),
 ]
 
 BY_NAME = {w.name: w for w in WORKLOADS + EXTRA_WORKLOADS + BWD_WORKLOADS + VARLEN_WORKLOADS}
