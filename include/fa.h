@@ -287,7 +287,10 @@ int64_t fa_launch_count(void);
  * that never arrives: the wait runs out after the wait budget, every role of
  * the kernel gives up, drains its copies and MMAs, frees its tensor memory and
  * returns, and fa_sync_status reports FA_ERR_TIMEOUT. The GPU context stays
- * usable. A negative position disarms the hook.
+ * usable. A negative position disarms the hook. When the next call is
+ * fa_backward or fa_backward_varlen, the position counts units instead: every
+ * CTA of its dK/dV kernel skips the K/V load of its unit number
+ * `kv_position`, with the same outcome.
  */
 void fa_test_arm_fault(int32_t kv_position);
 

@@ -49,3 +49,41 @@ def test_hook_is_one_shot():
     finally:
         fa.fa_set_wait_budget_ns(0)
     compare(o, lse, q, k, v, 0.125, "none")
+
+
+@pytest.mark.parametrize("varlen", [False, True])
+def test_backward_wait_timeout_is_reported_and_gpu_recovers(varlen):
+    """The same for the backward: the dK/dV kernel's first unit in every CTA never
+    gets its K/V tile; its waits run out, every role gives up, the status reads
+    FA_ERR_TIMEOUT, and the next backward is correct."""
+    from test_bwd_gpu import compare as bwd_compare, run_bwd
+    q, k, v = make_qkv(1, 4, 700, 64, torch.bfloat16, seed=3)
+    do = make_qkv(1, 4, 700, 64, torch.bfloat16, seed=4)[0]
+    dev = torch.device("cuda", 0)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o = torch.empty_like(qd)
+    lse = torch.empty(qd.shape[:-1], device=dev)
+    fa.fa_forward(qd, kd, vd, o, lse, 0.125, "causal")
+    assert fa.fa_sync_status() == fa.FA_OK
+    grads = [torch.empty_like(t) for t in (qd, kd, vd)]
+    fa.fa_set_wait_budget_ns(50_000_000)
+    try:
+        fa.fa_test_arm_fault(0)
+        t0 = time.time()
+        if varlen:
+            tok = lambda t: t[0].transpose(0, 1).contiguous()
+            cu = torch.tensor([0, 700], dtype=torch.int32, device=dev)
+            fa.fa_backward_varlen(tok(qd), tok(kd), tok(vd), tok(o), tok(dod),
+                                  lse[0].transpose(0, 1).contiguous(), cu, cu,
+                                  *(tok(g) for g in grads), 700, 700, 0.125, "causal")
+        else:
+            fa.fa_backward(qd, kd, vd, o, dod, lse, *grads, 0.125, "causal")
+        st = fa.fa_sync_status()
+        elapsed = time.time() - t0
+    finally:
+        fa.fa_set_wait_budget_ns(0)
+    assert st == fa.FA_ERR_TIMEOUT, fa.fa_status_string(st)
+    assert elapsed < 5.0
+    assert fa.fa_sync_status() == fa.FA_OK
+    dq, dk, dv = run_bwd(q, k, v, do, 0.125, "causal")
+    bwd_compare(q, k, v, do, 0.125, "causal", (0, 0), dq, dk, dv)

@@ -654,6 +654,7 @@ bool make_map_tokens(CUtensorMap *map, const void *base, bool bf16, int64_t toke
     return ::make_map_tokens(map, base, bf16, tokens, heads, d);
 }
 void count_launches(int64_t n) { g_launches += n; }
+int take_fault_position() { return g_fault_pos.exchange(-1); }
 unsigned int *next_sched_slot(unsigned int *base) {
     return base + 2 * (g_sched_next.fetch_add(1) % kSchedSlots);
 }

@@ -235,7 +235,9 @@ fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
     p.wait_budget_ns = fa_host::wait_budget();
     p.status = info.status;
+    p.fault_unit = -1;
     fa::bwd::BwdParams pkv = p, pq = p;
+    pkv.fault_unit = fa_host::take_fault_position();
     pkv.n_units = static_cast<int>(BHkv * n_blk);  // (K/V head, key block)
     pq.n_units = static_cast<int>(BH * n_blk);     // (query head, query block)
     pkv.sched = fa_host::next_sched_slot(info.sched);
@@ -404,7 +406,9 @@ fa_status fa_backward_varlen(const void *Q, const void *K, const void *V, const 
     p.total_q = static_cast<int>(total_q);
     p.total_k = static_cast<int>(total_k);
     p.vstride = static_cast<int>(wl.vstride);
+    p.fault_unit = -1;
     fa::bwd::BwdParams pkv = p, pq = p;
+    pkv.fault_unit = fa_host::take_fault_position();
     const int64_t nb_k = (max_seqlen_k + fa::bwd::kTile - 1) / fa::bwd::kTile;
     const int64_t nb_q = (max_seqlen_q + fa::bwd::kTile - 1) / fa::bwd::kTile;
     if (B * H_kv * nb_k > 0x7fffffffLL || B * H * nb_q > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;

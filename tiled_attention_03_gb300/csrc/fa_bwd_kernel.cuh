@@ -94,6 +94,9 @@ struct BwdParams {
     // sequence padded to 128 rows); n_blk counts blocks of the longest sequence.
     const int *cu_q, *cu_k, *cu_pad;
     int total_q, total_k, vstride;
+    // Test hook (dK/dV kernel): when >= 0, every CTA skips the K/V load of its
+    // unit number fault_unit, so that unit's waits run out; -1: none.
+    int fault_unit;
 };
 
 // This sequence's sizes and first rows (variable-length batches only).
@@ -415,12 +418,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const auto U = decode_kv_unit<VARLEN>(u, p);
                 ok = mbar_wait_bounded(bar(kKvKVEmpty), (unit_iter & 1) ^ 1, abort_flag, budget);
                 if (!ok) break;
-                mbar_arrive_expect_tx(bar(kKvKVFull), 2 * L::kTileBytes);
-                int ky, kz;
-                kv_coords(U, U.bkv, U.k0, p, ky, kz);
-                for (int g = 0; g < kRegions; ++g) {
-                    tma_load_3d(sK + g * kRegionBytes, &tmK, bar(kKvKVFull), 64 * g, ky, kz);
-                    tma_load_3d(sV + g * kRegionBytes, &tmV, bar(kKvKVFull), 64 * g, ky, kz);
+                if (unit_iter != p.fault_unit) {
+                    mbar_arrive_expect_tx(bar(kKvKVFull), 2 * L::kTileBytes);
+                    int ky, kz;
+                    kv_coords(U, U.bkv, U.k0, p, ky, kz);
+                    for (int g = 0; g < kRegions; ++g) {
+                        tma_load_3d(sK + g * kRegionBytes, &tmK, bar(kKvKVFull), 64 * g, ky, kz);
+                        tma_load_3d(sV + g * kRegionBytes, &tmV, bar(kKvKVFull), 64 * g, ky, kz);
+                    }
                 }
                 ++kv_loads;
                 // Claim the next unit now; its K and V go to L2 while this unit runs

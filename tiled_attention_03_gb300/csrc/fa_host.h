@@ -33,6 +33,8 @@ bool make_map_tokens(CUtensorMap *map, const void *base, bool bf16, int64_t toke
                      int64_t d);
 uint64_t wait_budget();
 void count_launches(int64_t n);
+// The armed test-hook position (fa_test_arm_fault), disarming it; -1 if none.
+int take_fault_position();
 // The scheduler counters of one launch (a slot of the device's static array,
 // zero at launch; the launch's last CTA zeroes it again).
 unsigned int *next_sched_slot(unsigned int *base);
