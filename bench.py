@@ -32,22 +32,32 @@ WORKLOAD = "full_b4h32n4096d128"
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
-KERNEL_SOURCES = ("tiled_attention_03_gb300/csrc/fa_fwd_kernel.cuh",
-                  "tiled_attention_03_gb300/csrc/fa_bwd_kernel.cuh",
-                  "tiled_attention_03_gb300/csrc/fa_combine.cuh",
-                  "tiled_attention_03_gb300/csrc/ptx.cuh")
+# The sources each kernel family compiles from: a traffic figure stays valid while
+# the sources of the kernels it was measured on are unchanged.
+CSRC = "tiled_attention_03_gb300/csrc/"
+KERNEL_SOURCES = {
+    "fwd": (CSRC + "fa_fwd_kernel.cuh", CSRC + "fa_combine.cuh", CSRC + "ptx.cuh"),
+    "fwd256": (CSRC + "fa_fwd256_kernel.cuh", CSRC + "ptx.cuh"),
+    "bwd": (CSRC + "fa_bwd_kernel.cuh", CSRC + "ptx.cuh"),
+}
 TRAFFIC_DIR = os.path.join(ROOT, "profiles")
 
 
-def kernel_source_hash() -> str:
+def kernel_family(w) -> str:
+    if w.backward:
+        return "bwd"
+    return "fwd256" if w.d == 256 else "fwd"
+
+
+def kernel_source_hash(family: str) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[family]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def measured_traffic(workload: str):
+def measured_traffic(w):
     """DRAM bytes per step from the committed ncu summary (profiles/*_traffic.txt)
     of this workload, if it was taken on the current kernel source; else None."""
     try:
@@ -64,8 +74,8 @@ def measured_traffic(workload: str):
                     if ":" in line and not line.startswith("#"):
                         key, val = line.split(":", 1)
                         vals[key.strip()] = val.strip()
-            if (vals.get("workload") == workload
-                    and vals.get("kernel_source_hash") == kernel_source_hash()):
+            if (vals.get("workload") == w.name
+                    and vals.get("kernel_source_hash") == kernel_source_hash(kernel_family(w))):
                 return float(vals["dram_bytes_per_launch"])
         except (OSError, KeyError, ValueError):
             continue
@@ -528,7 +538,7 @@ def main():
         nbytes = algorithmic_bytes(w)
         # tensor-bound above the ridge (peak FLOP/s / peak B/s), HBM-bound below it
         tensor_bound = flops / nbytes > peak_tf * 1e12 / (peak_gbs * 1e9)
-        traffic = measured_traffic(w.name)
+        traffic = measured_traffic(w)
         cpu = None
         if args.cpu_seconds > 0 and w.backward:
             cpu_v, cores, sample, _ = cpu_oracle_rate_bwd(w, args.cpu_seconds)
