@@ -499,12 +499,12 @@ def main():
     barrier(world)
     torch.cuda.synchronize(dev)
     launches0 = fa.fa_launch_count()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
+    # one event between consecutive steps: the total and each step's own duration
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record(stream)
+    for i in range(args.steps):
         step()
-    e1.record(stream)
+        ev[i + 1].record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
     launches = fa.fa_launch_count() - launches0
@@ -512,7 +512,9 @@ def main():
     st = fa.fa_sync_status(stream)
     if st != fa.FA_OK:
         raise SystemExit(f"device status after the timed region: {fa.fa_status_string(st)}")
-    ms_local = e0.elapsed_time(e1)
+    ms_local = ev[0].elapsed_time(ev[-1])
+    per_step = sorted(ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps))
+    pct = lambda f: per_step[min(len(per_step) - 1, int(f * len(per_step)))]
     ms_total = max_over_ranks(ms_local, world)
     ms_step = ms_total / args.steps
     value = job_throughput(world, flops, ms_step)
@@ -555,6 +557,7 @@ def main():
             "metric": METRIC_BWD if w.backward else METRIC, "value": value, "unit": "TFLOP/s",
             "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "step_ms": {"p10": pct(0.1), "p50": pct(0.5), "p90": pct(0.9), "rank": 0},
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype_name, "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
