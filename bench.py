@@ -264,8 +264,8 @@ def run_reference(args, w):
 def run_e2e(args, w, q_h, k_h, v_h, mask, stream, dev, world, flops):
     """Same metric through the public API (tiled_attention_03_gb300.forward) with
     pinned host inputs and pinned result buffers: every step copies Q, K, V to the
-    device, runs the kernel and copies O and LSE back (overlapped per batch entry
-    inside forward())."""
+    device, runs the kernel and copies O and LSE back (overlapped in chunks of
+    about 64 MB by the library's fa_forward_host)."""
     import tiled_attention_03_gb300 as fa
     qp, kp, vp = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
     splits = None if w.splits < 0 else w.splits

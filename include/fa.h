@@ -70,8 +70,9 @@ typedef enum { FA_DTYPE_FP16 = 0, FA_DTYPE_BF16 = 1 } fa_dtype;
  * stream  : a cudaStream_t (NULL = the legacy default stream).
  *
  * Ownership: every pointer is owned by the caller; the library keeps none and
- * allocates no device memory per call. All four data pointers must be 16-byte
- * aligned and on the current device.
+ * allocates no device memory per call. Q, K, V and O must be 16-byte aligned
+ * (they are read and written by tensor-memory-access copies); LSE, accessed one
+ * float at a time, 4-byte aligned. All on the current device.
  *
  * Errors: arguments are checked before anything is enqueued; an invalid call
  * returns FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED and launches nothing. A
@@ -181,7 +182,7 @@ fa_status fa_forward_splitkv_static(const void *Q, const void *K, const void *V,
  * Layout (token-major): Q and O total_q x H x d, K and V total_k x H_kv x d, in
  * `dtype`; LSE total_q x H float32; cu_seqlens_q and cu_seqlens_k are B + 1
  * int32 on the device, non-decreasing from 0 to total_q / total_k. All on the
- * current device; tensors 16-byte aligned. max_seqlen_q >= every L_q (rows
+ * current device; Q, K, V, O 16-byte aligned, LSE 4-byte. max_seqlen_q >= every L_q (rows
  * past it are not computed). With a mask, every sequence needs L_q <= L_k;
  * every sequence with queries needs L_k >= 1. The device arrays are read by
  * the kernel, not checked on the host; offsets are clamped to the tensors, so
@@ -198,6 +199,46 @@ fa_status fa_forward_varlen(const void *Q, const void *K, const void *V, void *O
                             void *stream);
 
 /*
+ * fa_forward_host -- the forward pass of fa_forward_splitkv over HOST buffers:
+ * the inputs are copied to the device, processed and the results copied back,
+ * in chunks (one batch entry and a range of K/V heads with their query heads,
+ * about chunk_bytes of Q + K + V each; chunk_bytes <= 0 takes 64 MiB). The copy
+ * in of chunk c+1, the kernel on chunk c and the copy out of chunk c-1 overlap:
+ * the copies run on two streams of the library's own (created once per device),
+ * the kernels on `stream`. So only the first copy in and the last copy out are
+ * not hidden behind other work.
+ *
+ * Q, K, V, O, LSE: host memory (page-locked memory makes the copies
+ * asynchronous; pageable memory works, with the host waiting on each copy), in
+ * the layout of fa_forward_splitkv; O and LSE overlap no input. `workspace`:
+ * device memory owned by the caller, 16-byte aligned, at least
+ * fa_forward_host_workspace_bytes(...) bytes with the same sizes, num_splits and
+ * chunk_bytes; it holds the device copies. num_splits: 0 runs Nq == Nk
+ * unsplit and Nq < Nk with fa_splitkv_default_splits per chunk; n >= 1 runs
+ * every chunk with n key splits.
+ *
+ * The call enqueues everything and returns; `stream` then waits for the last
+ * copy out, so a stream synchronize (or fa_sync_status(stream)) means O and LSE
+ * are in host memory. The host buffers must stay valid until then, and the
+ * workspace must not be reused meanwhile. Calls on one device are enqueued one
+ * at a time (a lock), so concurrent callers stay correct.
+ *
+ * Errors: every argument is checked before anything is enqueued (as fa_forward,
+ * plus: a device pointer among Q, K, V, O, LSE, or a workspace that is not
+ * device memory or is too small, is FA_ERR_INVALID_ARG). A CUDA failure while
+ * enqueueing returns FA_ERR_CUDA.
+ */
+size_t fa_forward_host_workspace_bytes(int64_t B, int64_t H, int64_t H_kv, int64_t Nq,
+                                       int64_t Nk, int64_t d, int64_t num_splits,
+                                       int64_t chunk_bytes);
+fa_status fa_forward_host(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                          int64_t B, int64_t H, int64_t H_kv, int64_t Nq, int64_t Nk, int64_t d,
+                          float scale, fa_mask_mode mask_mode, int64_t window_left,
+                          int64_t window_right, fa_dtype dtype, int64_t num_splits,
+                          int64_t chunk_bytes, void *workspace, size_t workspace_bytes,
+                          void *stream);
+
+/*
  * fa_backward -- gradients of the forward pass: given Q, K, V, the forward's
  * O and LSE (as fa_forward / fa_forward_gqa wrote them) and dO, the gradient
  * of a loss with respect to O, writes dQ, dK and dV. The forward keeps only O
@@ -211,7 +252,7 @@ fa_status fa_forward_varlen(const void *Q, const void *K, const void *V, void *O
  *
  * Layout: Q, O, dO and dQ are contiguous B x H x N x d; K, V, dK and dV are
  * B x H_kv x N x d (H_kv divides H); LSE is B x H x N float32; all in `dtype`
- * except LSE, on the current device, 16-byte aligned. Queries and keys share
+ * except LSE, on the current device, 16-byte aligned (LSE: 4-byte). Queries and keys share
  * positions (as in fa_forward); the mask arguments are those of fa_forward.
  * `workspace` is caller-owned device memory of at least
  * fa_backward_workspace_bytes(B, H, N, d) bytes (two fp32 row terms per query

@@ -48,7 +48,7 @@ def call(lib, q=A, k=B_, v=C, o=O_, lse=L_, B=1, H=1, N=16, d=64, scale=0.125, m
     dict(dtype=2), dict(dtype=-1), dict(mask=3), dict(mask=-1),
     dict(mask=2, wl=-1), dict(mask=2, wr=-1),
     dict(scale=0.0), dict(scale=-0.5), dict(scale=float("inf")), dict(scale=float("nan")),
-    dict(q=A + 8), dict(o=O_ + 2), dict(lse=L_ + 4),
+    dict(q=A + 8), dict(o=O_ + 2), dict(lse=L_ + 2),
     dict(o=A),              # O aliases Q
     dict(lse=O_ + 64),      # LSE inside O
 ])
@@ -152,3 +152,37 @@ def test_varlen_empty_is_ok_without_pointers(lib):
 @pytest.mark.parametrize("kw", [dict(d=96), dict(maxq=101)])
 def test_varlen_unsupported(lib, kw):
     assert varlen_call(lib, **kw) == fa.FA_ERR_UNSUPPORTED
+
+
+def host_call(lib, B=1, H=2, Hk=2, Nq=128, Nk=128, d=64, scale=0.125, mask=0, wl=0, wr=0,
+              dtype=0, splits=0, chunk=0, ws_bytes=1 << 30, **ptrs):
+    a = dict(q=0x100000, k=0x200000, v=0x300000, o=0x400000, lse=0x600000, ws=0x700000)
+    a.update(ptrs)
+    return lib.fa_forward_host(a["q"], a["k"], a["v"], a["o"], a["lse"], B, H, Hk, Nq, Nk, d, scale,
+                               mask, wl, wr, dtype, splits, chunk, a["ws"], ws_bytes, None)
+
+
+def test_host_pipeline_workspace_size(lib):
+    # Q, K, V, O copies (32 KiB each) and the LSE copy (1 KiB); no key-split scratch
+    assert lib.fa_forward_host_workspace_bytes(1, 2, 2, 128, 128, 64, 0, 0) == 4 * 32768 + 1024
+    # Nq < Nk adds the split scratch of the largest chunk
+    assert (lib.fa_forward_host_workspace_bytes(1, 2, 2, 4, 4096, 64, 0, 0) >
+            lib.fa_forward_host_workspace_bytes(1, 2, 2, 4, 4, 64, 0, 0))
+    for bad in [(0, 2, 2, 128, 128, 64, 0, 0), (1, 3, 2, 128, 128, 64, 0, 0),
+                (1, 2, 2, 128, 128, 96, 0, 0), (1, 2, 2, 128, 128, 64, -1, 0),
+                (1, 2, 2, 64, 128, 256, 0, 0)]:
+        assert lib.fa_forward_host_workspace_bytes(*bad) == 0
+
+
+@pytest.mark.parametrize("kw", [
+    dict(q=0), dict(o=0), dict(lse=0), dict(ws=0), dict(B=0), dict(Hk=3), dict(Nq=0),
+    dict(dtype=2), dict(mask=3), dict(mask=2, wl=-1), dict(scale=0.0), dict(splits=-1),
+    dict(mask=1, Nq=200), dict(lse=0x600002),
+])
+def test_host_pipeline_invalid_arguments(lib, kw):
+    assert host_call(lib, **kw) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [dict(d=96), dict(d=256, Nq=64), dict(d=256, splits=2)])
+def test_host_pipeline_unsupported(lib, kw):
+    assert host_call(lib, **kw) == fa.FA_ERR_UNSUPPORTED

@@ -149,7 +149,7 @@ def test_forward_host_tensors():
 
 
 def test_forward_host_tensors_pipelined_into_caller_buffers():
-    """Several batch entries (copies and kernels overlapped per entry), GQA, the
+    """Several batch entries (copies and kernels overlapped per chunk), GQA, the
     caller's pinned result buffers; and a rectangular (Nq < Nk) host call."""
     q, _, _ = make_qkv(3, 8, 257, 128, torch.bfloat16, seed=11)
     _, k, v = make_qkv(3, 2, 257, 128, torch.bfloat16, seed=12, H_kv=2)
@@ -162,6 +162,47 @@ def test_forward_host_tensors_pipelined_into_caller_buffers():
     q2 = q[:, :, -5:].contiguous()
     o2, l2 = fa.forward(q2, k, v, 0.09, "causal")
     compare(o2, l2, q2, k, v, 0.09, "causal")
+
+
+@pytest.mark.parametrize("chunk_bytes", [1, 300_000])
+def test_forward_host_tensors_chunked_by_heads(monkeypatch, chunk_bytes):
+    """The host pipeline cut into chunks of K/V heads (one K/V head with its query
+    heads per chunk, or two), grouped heads, and a split-KV (Nq < Nk) call."""
+    from tiled_attention_03_gb300 import binding
+    monkeypatch.setattr(binding, "HOST_CHUNK_BYTES", chunk_bytes)
+    q, _, _ = make_qkv(2, 6, 200, 64, torch.float16, seed=13)
+    _, k, v = make_qkv(2, 3, 200, 64, torch.float16, seed=14, H_kv=3)
+    o, lse = fa.forward(q.pin_memory(), k.pin_memory(), v.pin_memory(), 0.125, "causal")
+    compare(o, lse, q, k, v, 0.125, "causal")
+    q2 = q[:, :, -3:].contiguous()
+    o2, l2 = fa.forward(q2, k, v, 0.125, "causal")
+    compare(o2, l2, q2, k, v, 0.125, "causal")
+
+
+def test_forward_host_pipeline_splits_pageable_and_checks():
+    """fa_forward_host with key splits on Nq == Nk, with pageable (not pinned)
+    host tensors, and its own rejections: a device pointer among the host
+    buffers, a workspace that is too small."""
+    q, k, v = make_qkv(2, 4, 300, 64, torch.bfloat16, seed=15)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32)
+    fa.fa_forward_host(q, k, v, o, lse, 0.125, "causal", num_splits=3, chunk_bytes=1)
+    torch.cuda.synchronize()
+    compare(o, lse, q, k, v, 0.125, "causal")
+    lib = fa.load_library()
+    need = fa.fa_forward_host_workspace_bytes(2, 4, 4, 300, 300, 64)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    args = (2, 4, 4, 300, 300, 64, 0.125, 0, 0, 0, 1, 0, 0)
+    qd = q.cuda()
+    assert lib.fa_forward_host(qd.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                               *args, ws.data_ptr(), need, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_forward_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                               *args, ws.data_ptr(), need - 256, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_forward_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                               *args, ws.data_ptr(), need, None) == fa.FA_OK
+    torch.cuda.synchronize()
+    compare(o, lse, q, k, v, 0.125, "none")
+    assert fa.fa_sync_status() == fa.FA_OK
 
 
 def test_rejects_host_pointer_in_abi():

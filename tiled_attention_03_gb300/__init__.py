@@ -10,4 +10,5 @@ from .binding import (FA_SPLITKV_STATIC_SCRATCH_BYTES, fa_forward_splitkv,  # no
                       fa_splitkv_workspace_bytes)
 from .binding import backward, fa_backward, fa_backward_workspace_bytes  # noqa: F401
 from .binding import fa_forward_varlen  # noqa: F401
+from .binding import fa_forward_host, fa_forward_host_workspace_bytes  # noqa: F401
 from .binding import fa_backward_varlen, fa_backward_varlen_workspace_bytes  # noqa: F401

@@ -64,6 +64,12 @@ def load_library(path: str = LIB) -> ctypes.CDLL:
         ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
         ctypes.c_int64, ctypes.c_float, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
         ctypes.c_int64, ctypes.c_void_p]
+    lib.fa_forward_host.restype = ctypes.c_int
+    lib.fa_forward_host.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int64] * 6 + [
+        ctypes.c_float, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int64,
+        ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    lib.fa_forward_host_workspace_bytes.restype = ctypes.c_size_t
+    lib.fa_forward_host_workspace_bytes.argtypes = [ctypes.c_int64] * 8
     lib.fa_splitkv_workspace_bytes.restype = ctypes.c_size_t
     lib.fa_splitkv_workspace_bytes.argtypes = [ctypes.c_int64] * 5
     lib.fa_splitkv_default_splits.restype = ctypes.c_int64
@@ -183,6 +189,10 @@ def fa_forward_gqa(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.T
         raise FaError(rc)
 
 
+# Input bytes per chunk of forward()'s host pipeline.
+HOST_CHUNK_BYTES = 64 << 20
+
+
 def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
             mask="none", window=(0, 0), stream=None, num_splits: int | None = None,
             out: torch.Tensor | None = None, lse_out: torch.Tensor | None = None):
@@ -191,12 +201,15 @@ def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | No
     queries are then the last positions; this runs the split-KV entry point, as
     does any num_splits, with 0 meaning its default).
 
-    Device tensors run in place on the device. Host tensors are copied to the
-    current CUDA device, processed, and copied back: batch entry by batch entry,
-    with the copy in of entry b+1, the kernel on entry b and the copy out of entry
-    b-1 on three streams, so copies and compute overlap. Pinned host inputs make
-    the copies asynchronous; `out` / `lse_out` (host, pinned) receive the results
-    and avoid allocating them per call.
+    Device tensors run in place on the device. Host tensors go through
+    fa_forward_host: the library copies them to the current CUDA device, processes
+    and copies the results back in chunks of about HOST_CHUNK_BYTES (a batch entry
+    and a range of K/V heads with their query heads), with the copy in of chunk
+    c+1, the kernel on chunk c and the copy out of chunk c-1 overlapped, and this
+    call returns once O and LSE are in host memory. Pinned host tensors make the
+    copies asynchronous; `out` / `lse_out` (host, pinned) receive the results and
+    avoid allocating them per call. For host tensors, num_splits None or 0 means
+    no key split when Nq == Nk and the default split count otherwise.
     """
     if scale is None:
         scale = q.shape[-1] ** -0.5
@@ -207,42 +220,54 @@ def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | No
                if lse_out is None else lse_out)
         _forward_device(q, k, v, o, lse, scale, mask, window, stream, num_splits)
         return o, lse
-    dev = torch.device("cuda", torch.cuda.current_device())
     q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
     if out is None:
         out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
     if lse_out is None:
         lse_out = torch.empty(q.shape[:-1], dtype=torch.float32, pin_memory=True)
-    qd = torch.empty(q.shape, dtype=q.dtype, device=dev)
-    kd = torch.empty(k.shape, dtype=k.dtype, device=dev)
-    vd = torch.empty(v.shape, dtype=v.dtype, device=dev)
-    od = torch.empty_like(qd)
-    lsed = torch.empty(q.shape[:-1], dtype=torch.float32, device=dev)
-    compute = torch.cuda.current_stream(dev) if stream is None else stream
-    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    s_in.wait_stream(compute)
-    for b in range(q.shape[0]):
-        with torch.cuda.stream(s_in):
-            qd[b].copy_(q[b], non_blocking=True)
-            kd[b].copy_(k[b], non_blocking=True)
-            vd[b].copy_(v[b], non_blocking=True)
-        e_in = torch.cuda.Event()
-        e_in.record(s_in)
-        compute.wait_event(e_in)
-        sl = slice(b, b + 1)
-        _forward_device(qd[sl], kd[sl], vd[sl], od[sl], lsed[sl], scale, mask, window, compute,
-                        num_splits)
-        e_k = torch.cuda.Event()
-        e_k.record(compute)
-        s_out.wait_event(e_k)
-        with torch.cuda.stream(s_out):
-            out[b].copy_(od[b], non_blocking=True)
-            lse_out[b].copy_(lsed[b], non_blocking=True)
-    for t in (qd, kd, vd, od, lsed):
-        t.record_stream(s_in)
-        t.record_stream(s_out)
-    s_out.synchronize()
+    fa_forward_host(q, k, v, out, lse_out, scale, mask, window[0], window[1],
+                    num_splits or 0, HOST_CHUNK_BYTES, None, stream)
+    (torch.cuda.current_stream() if stream is None else stream).synchronize()
     return out, lse_out
+
+
+def fa_forward_host_workspace_bytes(B: int, H: int, H_kv: int, Nq: int, Nk: int, d: int,
+                                    num_splits: int = 0, chunk_bytes: int = 0) -> int:
+    return load_library().fa_forward_host_workspace_bytes(B, H, H_kv, Nq, Nk, d, num_splits,
+                                                          chunk_bytes)
+
+
+def fa_forward_host(q, k, v, o, lse, scale: float, mask_mode=FA_MASK_NONE, window_left: int = 0,
+                    window_right: int = 0, num_splits: int = 0, chunk_bytes: int = 0,
+                    workspace: torch.Tensor | None = None, stream=None) -> None:
+    """Enqueue fa_forward_host on host tensors q, o (B, H, Nq, d), k, v (B, H_kv, Nk,
+    d) and lse (B, H, Nq) float32. Without a workspace tensor one is taken from
+    PyTorch's caching allocator on the current device (released to it once this
+    call's work on `stream` is done)."""
+    lib = load_library()
+    for t in (q, k, v, o, lse):
+        if t.is_cuda or not t.is_contiguous():
+            raise FaError(FA_ERR_INVALID_ARG)
+    if q.dtype not in _DTYPES or k.dtype != q.dtype or v.dtype != q.dtype or o.dtype != q.dtype:
+        raise FaError(FA_ERR_INVALID_ARG)
+    if lse.dtype != torch.float32:
+        raise FaError(FA_ERR_INVALID_ARG)
+    B, H, Nq, d = q.shape
+    H_kv, Nk = k.shape[1], k.shape[2]
+    need = fa_forward_host_workspace_bytes(B, H, H_kv, Nq, Nk, d, num_splits, chunk_bytes)
+    if need == 0:
+        raise FaError(FA_ERR_INVALID_ARG)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        workspace.record_stream(torch.cuda.current_stream(dev) if stream is None else stream)
+    rc = lib.fa_forward_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                             lse.data_ptr(), B, H, H_kv, Nq, Nk, d, float(scale),
+                             _MASKS[mask_mode], int(window_left), int(window_right),
+                             _DTYPES[q.dtype], int(num_splits), int(chunk_bytes),
+                             workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc)
 
 
 def _forward_device(q, k, v, o, lse, scale, mask, window, stream, num_splits):

@@ -144,6 +144,8 @@ DeviceState *device_state(int dev) {
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// LSE is read and written one float at a time: float alignment is enough.
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
     const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
@@ -359,7 +361,7 @@ fa_status run_forward(const Call &c) {
     // would leave rows with no visible key.
     if (mask_mode != FA_MASK_NONE && Nq > Nk) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(c.scale) || !(c.scale > 0.f)) return FA_ERR_INVALID_ARG;
-    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned4(LSE))
         return FA_ERR_INVALID_ARG;
     if (c.num_splits < 1) return FA_ERR_INVALID_ARG;
     if (d != 32 && d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
@@ -528,7 +530,7 @@ fa_status run_forward_varlen(const VarlenCall &c) {
         return FA_ERR_INVALID_ARG;
     if (!std::isfinite(c.scale) || !(c.scale > 0.f)) return FA_ERR_INVALID_ARG;
     if (!aligned16(c.Q) || !aligned16(c.K) || !aligned16(c.V) || !aligned16(c.O) ||
-        !aligned16(c.LSE) || (reinterpret_cast<uintptr_t>(c.cu_q) & 3u) ||
+        !aligned4(c.LSE) || (reinterpret_cast<uintptr_t>(c.cu_q) & 3u) ||
         (reinterpret_cast<uintptr_t>(c.cu_k) & 3u))
         return FA_ERR_INVALID_ARG;
     if (d != 32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
@@ -643,6 +645,7 @@ DeviceInfo device_info(int dev) {
     return info;
 }
 bool aligned16(const void *p) { return ::aligned16(p); }
+bool aligned4(const void *p) { return ::aligned4(p); }
 bool overlaps(const void *a, size_t na, const void *b, size_t nb) { return ::overlaps(a, na, b, nb); }
 bool on_device(const void *p, int dev) { return ::on_device(p, dev); }
 bool make_map(CUtensorMap *map, const void *base, bool bf16, int64_t BH, int64_t N, int64_t d) {

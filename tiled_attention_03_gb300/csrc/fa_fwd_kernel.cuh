@@ -70,10 +70,10 @@ constexpr int kVWarp = 10;    // V loads
 // what the launch allocated (threads x registers of the compiled kernel); the
 // host checks this before the first launch.
 #ifndef FA_REGS_SOFTMAX
-#define FA_REGS_SOFTMAX 208
+#define FA_REGS_SOFTMAX 200
 #endif
 #ifndef FA_REGS_CONTROL
-#define FA_REGS_CONTROL 88
+#define FA_REGS_CONTROL 104
 #endif
 constexpr int kRegsSoftmax = FA_REGS_SOFTMAX;
 constexpr int kRegsControl = FA_REGS_CONTROL;
@@ -703,7 +703,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (j <= j1) ok = wait(kBarKFull + st, ph);
                 if (ok && in(0, j)) issue_s(0, st);
                 if (ok && in(1, j - 1)) {
-                    ok = wait(kBarVFull + pst, pph) && wait(kBarPFull + 1, pv_count[1] & 1);
+                    // V_{j-1} was already waited for by O_0 += P_0(j-1) V_{j-1}
+                    if (!in(0, j - 1)) ok = wait(kBarVFull + pst, pph);
+                    ok = ok && wait(kBarPFull + 1, pv_count[1] & 1);
                     if (ok && j - 1 == U.a[1]) ok = wait(kBarOFree + 1, (epi_count[1] & 1) ^ 1);
                     if (ok) issue_pv(1, pst, j - 1 == U.a[1]);
                 }
