@@ -754,10 +754,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int e = 0; e < 16; ++e)
                         pk[e] = pack2<BF16>(__uint_as_float(a[2 * e]) * f, __uint_as_float(a[2 * e + 1]) * f);
                     if (key_ok) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(out + c * 64);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                        st_global_v8(out + c * 64, pk);
+                        st_global_v8(out + c * 64 + 32, pk + 8);
                     }
                 }
             }
@@ -1250,10 +1248,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         pk[e] = pack2<BF16>(__uint_as_float(a[2 * e]) * p.scale,
                                             __uint_as_float(a[2 * e + 1]) * p.scale);
                     if (store) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(out + c * 2);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                        st_global_v8(out + c * 2, pk);
+                        st_global_v8(out + c * 2 + 32, pk + 8);
                     }
                 }
             }
