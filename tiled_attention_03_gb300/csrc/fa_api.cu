@@ -186,16 +186,16 @@ bool make_map(CUtensorMap *map, const void *base, bool bf16, int64_t BH, int64_t
 
 template <int D, bool BF16>
 cudaError_t launch(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                   const CUtensorMap &o, const fa::FwdParams &p, bool packed, int64_t blocks,
-                   cudaStream_t stream, bool varlen = false) {
+                   const fa::FwdParams &p, bool packed, int64_t blocks, cudaStream_t stream,
+                   bool varlen = false) {
     const unsigned g = static_cast<unsigned>(blocks);
     constexpr int smem = fa::SmemLayout<D>::kAlloc;
     if (varlen)
-        fa::fa_fwd_kernel<D, BF16, false, true><<<g, fa::kThreads, smem, stream>>>(q, k, v, o, p);
+        fa::fa_fwd_kernel<D, BF16, false, true><<<g, fa::kThreads, smem, stream>>>(q, k, v, p);
     else if (packed)
-        fa::fa_fwd_kernel<D, BF16, true, false><<<g, fa::kThreads, smem, stream>>>(q, k, v, o, p);
+        fa::fa_fwd_kernel<D, BF16, true, false><<<g, fa::kThreads, smem, stream>>>(q, k, v, p);
     else
-        fa::fa_fwd_kernel<D, BF16, false, false><<<g, fa::kThreads, smem, stream>>>(q, k, v, o, p);
+        fa::fa_fwd_kernel<D, BF16, false, false><<<g, fa::kThreads, smem, stream>>>(q, k, v, p);
     return cudaGetLastError();
 }
 
@@ -414,11 +414,9 @@ fa_status run_forward(const Call &c) {
     if (d == 256) return run_forward_256(c, ds, dev);
 
     const bool bf16 = c.dtype == FA_DTYPE_BF16;
-    // O is mapped like Q (the epilogue stores it with TMA); a key split writes its
-    // partial results with plain stores and never reads this map.
-    CUtensorMap mq, mk, mv, mo;
+    CUtensorMap mq, mk, mv;
     if (!make_map(&mq, Q, bf16, spaces, R, d) || !make_map(&mk, K, bf16, BHkv, Nk, d) ||
-        !make_map(&mv, V, bf16, BHkv, Nk, d) || !make_map(&mo, O, bf16, spaces, R, d))
+        !make_map(&mv, V, bf16, BHkv, Nk, d))
         return FA_ERR_CUDA;
 
     fa::FwdParams p{};
@@ -467,14 +465,14 @@ fa_status run_forward(const Call &c) {
     cudaStream_t st = static_cast<cudaStream_t>(c.stream);
     cudaError_t e;
     if (d == 32)
-        e = bf16 ? launch<32, true>(mq, mk, mv, mo, p, packed, blocks, st)
-                 : launch<32, false>(mq, mk, mv, mo, p, packed, blocks, st);
+        e = bf16 ? launch<32, true>(mq, mk, mv, p, packed, blocks, st)
+                 : launch<32, false>(mq, mk, mv, p, packed, blocks, st);
     else if (d == 64)
-        e = bf16 ? launch<64, true>(mq, mk, mv, mo, p, packed, blocks, st)
-                 : launch<64, false>(mq, mk, mv, mo, p, packed, blocks, st);
+        e = bf16 ? launch<64, true>(mq, mk, mv, p, packed, blocks, st)
+                 : launch<64, false>(mq, mk, mv, p, packed, blocks, st);
     else
-        e = bf16 ? launch<128, true>(mq, mk, mv, mo, p, packed, blocks, st)
-                 : launch<128, false>(mq, mk, mv, mo, p, packed, blocks, st);
+        e = bf16 ? launch<128, true>(mq, mk, mv, p, packed, blocks, st)
+                 : launch<128, false>(mq, mk, mv, p, packed, blocks, st);
     if (e != cudaSuccess) return FA_ERR_CUDA;
     g_launches.fetch_add(1);
     if (split) {
@@ -572,11 +570,10 @@ fa_status run_forward_varlen(const VarlenCall &c) {
         return FA_ERR_INVALID_ARG;
 
     const bool bf16 = c.dtype == FA_DTYPE_BF16;
-    CUtensorMap mq, mk, mv, mo;
+    CUtensorMap mq, mk, mv;
     if (!make_map_tokens(&mq, c.Q, bf16, c.total_q, H, d) ||
         !make_map_tokens(&mk, c.K, bf16, c.total_k, H_kv, d) ||
-        !make_map_tokens(&mv, c.V, bf16, c.total_k, H_kv, d) ||
-        !make_map_tokens(&mo, c.O, bf16, c.total_q, H, d))
+        !make_map_tokens(&mv, c.V, bf16, c.total_k, H_kv, d))
         return FA_ERR_CUDA;
 
     fa::FwdParams p{};
@@ -618,14 +615,14 @@ fa_status run_forward_varlen(const VarlenCall &c) {
     cudaStream_t st = static_cast<cudaStream_t>(c.stream);
     cudaError_t e;
     if (d == 32)
-        e = bf16 ? launch<32, true>(mq, mk, mv, mo, p, false, blocks, st, true)
-                 : launch<32, false>(mq, mk, mv, mo, p, false, blocks, st, true);
+        e = bf16 ? launch<32, true>(mq, mk, mv, p, false, blocks, st, true)
+                 : launch<32, false>(mq, mk, mv, p, false, blocks, st, true);
     else if (d == 64)
-        e = bf16 ? launch<64, true>(mq, mk, mv, mo, p, false, blocks, st, true)
-                 : launch<64, false>(mq, mk, mv, mo, p, false, blocks, st, true);
+        e = bf16 ? launch<64, true>(mq, mk, mv, p, false, blocks, st, true)
+                 : launch<64, false>(mq, mk, mv, p, false, blocks, st, true);
     else
-        e = bf16 ? launch<128, true>(mq, mk, mv, mo, p, false, blocks, st, true)
-                 : launch<128, false>(mq, mk, mv, mo, p, false, blocks, st, true);
+        e = bf16 ? launch<128, true>(mq, mk, mv, p, false, blocks, st, true)
+                 : launch<128, false>(mq, mk, mv, p, false, blocks, st, true);
     if (e != cudaSuccess) return FA_ERR_CUDA;
     g_launches.fetch_add(1);
     return FA_OK;

@@ -148,15 +148,10 @@ struct SmemLayout {
     // memory, so one CTA (holding all 512 TMEM columns) runs per SM.
     static constexpr int kStages = D == 128 ? 2 : 4;
     static constexpr int kTileBytes = kBM * D * 2;
-    // Output staging: one slot per Q tile, holding one 128-row region of O (64
-    // columns) in the layout the TMA store reads. d = 32 (64-byte rows) stores O
-    // with plain per-thread stores instead: measured faster there.
-    static constexpr int kSlotBytes = D >= 64 ? kBM * Regions<D>::kRowBytes : 0;
     static constexpr int kQ = 0;
     static constexpr int kK = kQ + kQTiles * kTileBytes;
     static constexpr int kV = kK + kStages * kTileBytes;
-    static constexpr int kO = kV + kStages * kTileBytes;
-    static constexpr int kBar = kO + kQTiles * kSlotBytes;
+    static constexpr int kBar = kV + kStages * kTileBytes;
     static constexpr int kNumBars = 40;
     static constexpr int kMisc = kBar + kNumBars * 8;
     static constexpr int kUnitRing = kMisc + 16;  // kUnitSlots ints: unit ids handed out to the roles
@@ -184,9 +179,7 @@ enum : int {
     kBarDrain = kBarOFree + kQTiles,
     kBarUnitFull = kBarDrain + 1,           // + slot
     kBarUnitEmpty = kBarUnitFull + 2,       // + slot
-    kBarOStaged = kBarUnitEmpty + 2,        // + t: the 4 warps of tile t wrote the slot
-    kBarOSlotFree = kBarOStaged + kQTiles,  // + t: the slot's last store has read it
-    kNumBarsUsed = kBarOSlotFree + kQTiles,
+    kNumBarsUsed = kBarUnitEmpty + 2,
 };
 
 // A work unit: rows [r0, r0 + 256) of row space rs (global rows rs * R + r)
@@ -430,13 +423,11 @@ __device__ __forceinline__ void kv_coords(const Unit<VARLEN> &U, int j, int &y, 
 template <int D, bool BF16, bool PACKED, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                  const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
     using L = SmemLayout<D>;
     using G = Regions<D>;
     constexpr int kRegions = G::kCount;
     constexpr int kStages = L::kStages;
-    constexpr bool kTmaStoreO = L::kSlotBytes > 0;
     static_assert(kStages <= kMaxStages && kNumBarsUsed <= L::kNumBars, "barrier slots");
     static_assert(D == 32 || D == 64 || D == 128, "head dim");
 
@@ -447,7 +438,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sQ = sbase + L::kQ;
     const uint32_t sK = sbase + L::kK;
     const uint32_t sV = sbase + L::kV;
-    const uint32_t sO = sbase + L::kO;
     const uint32_t bar0 = sbase + L::kBar;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
@@ -471,8 +461,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(kBarPFull + t), 128);
             mbar_init(bar(kBarODone + t), 1);
             mbar_init(bar(kBarOFree + t), 128);
-            mbar_init(bar(kBarOStaged + t), 4);
-            mbar_init(bar(kBarOSlotFree + t), 1);
         }
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(kBarKFull + s), 1);
@@ -490,7 +478,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
-        tma_prefetch_desc(&tmO);
     }
     tc_fence_before();
     __syncthreads();
@@ -758,11 +745,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tO = tl + L::kTmemO + t * D;
         const float sl2 = p.scale_log2;
         int s_count = 0;  // S_t tiles consumed so far (= O_t += P_t V issued)
-        int o_uses = 0;   // stores issued from this tile's output slot so far
-        // Lane 0 of the warpgroup's first warp issues the tile's TMA stores.
-        const bool issuer = (warp & 3) == 0 && lane == 0;
-        // 16-byte chunk c of row `row` sits at chunk c ^ swz in the slot (the TMA swizzle)
-        const uint32_t swz = G::kRowBytes == 128 ? (row & 7) : ((row >> 1) & 3);
         bool ok = true;
         for (int unit_iter = 0; ok; ++unit_iter) {
             const int slot = unit_iter % kUnitSlots;
@@ -845,66 +827,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
                 grow = static_cast<size_t>(U.rs) * p.R + (store ? r : 0);
             const float lse = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
-            if (kTmaStoreO && p.part_O == nullptr && (!VARLEN || rt0 + kBM <= R)) {
-                // O / l rounded to 16 bit, region by region through the tile's slot:
-                // each thread writes its row (swizzled), the warps signal the issuer,
-                // which stores the region with one TMA copy (rows past R are not
-                // written). Before a slot is rewritten, the issuer waits until the
-                // previous store has read it.
-                const uint32_t slot = sO + t * L::kSlotBytes;
-                int y, z;
-                q_coords<VARLEN>(U, rt0, y, z);
-#pragma unroll
-                for (int g = 0; g < kRegions; ++g) {
-                    // this region of the row, packed, before waiting for the slot
-                    uint32_t pk[G::kCols / 2];
-#pragma unroll
-                    for (int c = 0; c < G::kCols / 32; ++c) {
-                        uint32_t o[32];
-                        tmem_ld32(tO + g * G::kCols + c * 32, o);
-                        tmem_ld_wait(o);
-#pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            pk[c * 16 + e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l,
-                                                         __uint_as_float(o[2 * e + 1]) * inv_l);
-                    }
-                    if (o_uses > 0) {
-                        if (issuer) {
-                            bulk_wait_read_all();
-                            mbar_arrive(bar(kBarOSlotFree + t));
-                        }
-                        ok = __all_sync(0xffffffffu,
-                                        mbar_wait_bounded(bar(kBarOSlotFree + t), (o_uses - 1) & 1,
-                                                          abort_flag, budget));
-                        if (!ok) break;
-                    }
-#pragma unroll
-                    for (int q = 0; q < G::kCols / 8; ++q)
-                        st_shared_v4(slot + row * G::kRowBytes + ((static_cast<uint32_t>(q) ^ swz) << 4),
-                                     pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(kBarOStaged + t));
-                    bool staged = true;
-                    if (issuer) {
-                        staged = mbar_wait_bounded(bar(kBarOStaged + t), o_uses & 1, abort_flag, budget);
-                        if (staged) {
-                            tma_store_3d(&tmO, slot, G::kCols * g, y, z);
-                            bulk_commit_group();
-                        }
-                    }
-                    ++o_uses;
-                    ok = __shfl_sync(0xffffffffu, staged ? 1 : 0, 0) != 0;
-                    if (!ok) break;
-                }
-                if (!ok) {
-                    if (lane == 0) record_timeout(p, abort_flag, kRoleSoftmax, u);
-                    break;
-                }
-                if (store) p.LSE[grow] = lse;
-            } else if (p.part_O == nullptr) {
-                // a ragged tile of a variable-length batch: rows past the sequence
-                // belong to the next one, so each thread stores its own row
+            if (p.part_O == nullptr) {
+                // O / l rounded to 16 bit, and LSE
                 uint8_t *orow = reinterpret_cast<uint8_t *>(p.O) + grow * (D * 2);
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
@@ -946,8 +870,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(bar(kBarOFree + t));
         }
-        // No store may still be reading the slot, or writing O, when the CTA exits.
-        if (issuer) bulk_wait_all();
       }
     }
 

@@ -107,39 +107,11 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-// 3-D tiled copy shared -> global, tracked by this thread's bulk async-groups.
-// Elements outside the tensor are not written. c0 (innermost) must be a
-// multiple of 8 elements for 16-bit data; no coordinate may be negative.
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int32_t c0,
-                                             int32_t c1, int32_t c2) {
-    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
-                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(c0), "r"(c1), "r"(c2)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_commit_group() {
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// Until every committed group of this thread has finished reading shared memory.
-__device__ __forceinline__ void bulk_wait_read_all() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-// Until every committed group of this thread has completed.
-__device__ __forceinline__ void bulk_wait_all() {
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
 // One 32-byte global store (address 32-byte aligned): half the store
 // instructions of 16-byte stores for the same row.
 __device__ __forceinline__ void st_global_v8(void *p, const uint32_t *r) {
     asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(r[0]),
                  "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-                 : "memory");
-}
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
                  : "memory");
 }
 
