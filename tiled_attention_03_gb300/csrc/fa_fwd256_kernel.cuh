@@ -487,9 +487,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e = 0; e < 16; ++e)
                     pk[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
                 if (store) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 64);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                    st_global_v8(orow + c * 64, pk);
+                    st_global_v8(orow + c * 64 + 32, pk + 8);
                 }
             }
             if (store) p.LSE[grow] = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;

@@ -856,13 +856,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld32(tO + c * 32, o);
                     tmem_ld_wait(o);
                     if (store) {
-                        float4 *dst = reinterpret_cast<float4 *>(orow + c * 32);
 #pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            dst[q] = make_float4(__uint_as_float(o[4 * q]) * inv_l,
-                                                 __uint_as_float(o[4 * q + 1]) * inv_l,
-                                                 __uint_as_float(o[4 * q + 2]) * inv_l,
-                                                 __uint_as_float(o[4 * q + 3]) * inv_l);
+                        for (int e = 0; e < 32; ++e)
+                            o[e] = __float_as_uint(__uint_as_float(o[e]) * inv_l);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) st_global_v8(orow + c * 32 + q * 8, o + q * 8);
                     }
                 }
                 if (store) p.part_LSE[prow] = lse;
