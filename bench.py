@@ -18,6 +18,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -130,8 +131,7 @@ class ClockSampler:
 
 
 def _tmp_path(tag):
-    d = os.path.join(ROOT, "gpurun_out") if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else "/tmp"
-    return os.path.join(d, f".bench_{tag}_{os.getpid()}.csv")
+    return os.path.join(tempfile.gettempdir(), f".bench_{tag}_{os.getpid()}.csv")
 
 
 def dist_setup(n_gpus: int):
