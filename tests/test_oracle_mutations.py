@@ -41,6 +41,20 @@ MUTATIONS = [
      "dO columns reversed in dV"),
     (BWD, "const int64_t bh = b * jb->H + hk * group + g;", "const int64_t bh = b * jb->H + hk + g * jb->Hk;",
      "query heads of a group interleaved"),
+    (BWD, "    if (mask == 1) return j <= pos;", "    if (mask == 1) return j < pos;",
+     "backward causal mask off by one"),
+    (BWD, "        const int64_t pos = i + N - Nq;", "        const int64_t pos = i;",
+     "backward queries not placed at the last key positions"),
+    (BWD, "dk[j * d + c] += jb->scale * ds * q[i * d + c];", "dk[j * d + c] += ds * q[i * d + c];",
+     "dK without the scale"),
+    (BWD, "for (int64_t j = 0; j < N; ++j) p[j] /= l;", "for (int64_t j = 0; j < N; ++j) p[j] /= (l + 1.0);",
+     "backward P not normalised"),
+    (BWD, "    if (mask == 2) return j >= pos - wl && j <= pos + wr;",
+     "    if (mask == 2) return j >= pos - wl && j < pos + wr;", "backward window right bound exclusive"),
+    (FWD, "v = ldexp((double)(f | 0x80), e - 134);", "v = ldexp((double)(f | 0x80), e - 133);",
+     "bf16 exponent bias"),
+    (FWD, "v = ldexp((double)f, -24); /* subnormal", "v = ldexp((double)f, -23); /* subnormal",
+     "fp16 subnormal scale"),
 ]
 
 
