@@ -16,6 +16,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import tempfile
@@ -51,10 +52,15 @@ def kernel_family(w) -> str:
 
 
 def kernel_source_hash(family: str) -> str:
+    """Hash of the family's sources with comments and whitespace removed, so that
+    an edit of comments alone keeps the measured counters."""
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES[family]:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

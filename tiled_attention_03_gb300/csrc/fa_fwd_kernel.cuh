@@ -16,9 +16,10 @@
 // ("ai6s.net/6a0ed07b662f9a54cb761aa2", Epilogue Builder). Two Q blocks are
 // kept in flight so that the matrix unit works on one while the softmax of the
 // other runs: the GPU form of the Cube/Vector overlap of
-// "ai6s.net/6af30f4d40858c2d8819b6d5" §3.3 (1). The CTA grid is persistent
-// and walks a static list of work units, the form of the per-core Q-block
-// split of the same page's host tiling (§3.2-§3.3).
+// "ai6s.net/6af30f4d40858c2d8819b6d5" §3.3 (1). The CTA grid is persistent and
+// takes work units (the per-core Q-block split of the same page's host tiling,
+// §3.2-§3.3) from a launch-wide counter, heaviest first under causal and window
+// masks.
 //
 // One CTA (384 threads) runs on each SM and loops over work units; a unit is
 // 256 query rows (two 128-row Q tiles, t = 0, 1) of one (b, h):
@@ -40,6 +41,11 @@
 // O_t += P_t(j) V_j directly: tcgen05.mma operations of one thread execute in
 // issue order, so the P read of the earlier MMA precedes the S write of the
 // later one.
+//
+// Each softmax thread stores its row of O / l with 32-byte stores (one TMEM lane
+// per thread, so a warp's stores go to 32 rows; the wider stores halve the store
+// instructions, which share the memory-instruction queue with every warp's
+// mbarrier operations).
 //
 // The output accumulator is rescaled lazily: the reference max of a row only
 // moves when a block's max exceeds it by more than 2^8 (in log2 units), so
