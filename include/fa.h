@@ -60,7 +60,7 @@ typedef enum { FA_DTYPE_FP16 = 0, FA_DTYPE_BF16 = 1 } fa_dtype;
  * d       : head dimension: 32, 64, 128 or 256 (else FA_ERR_UNSUPPORTED). d = 256
  *           runs its own kernel (one 128-row Q tile per unit, 64-key K/V tiles)
  *           and is available in fa_forward and fa_forward_gqa only; the split-KV
- *           and variable-length calls take 32, 64 and 128, fa_backward 64 and 128.
+ *           and variable-length calls take 32, 64 and 128, as does fa_backward.
  * scale   : multiplier of the logits, finite and > 0 (typically 1/sqrt(d)).
  * mask_mode, window_left, window_right : see fa_mask_mode. The window
  *           arguments are read only for FA_MASK_WINDOW and must then be >= 0
@@ -282,7 +282,7 @@ size_t fa_backward_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d);
  * max_seqlen_q / max_seqlen_k bound every sequence's lengths. Gradients of
  * keys that no query sees, and of queries that see no key, are zero.
  * `workspace`: fa_backward_varlen_workspace_bytes(B, H, total_q) bytes, 16-byte
- * aligned. d is 64 or 128. Deterministic. Errors as fa_backward; the device
+ * aligned. d is 32, 64 or 128. Deterministic. Errors as fa_backward; the device
  * arrays are clamped to the tensors, as in fa_forward_varlen.
  */
 fa_status fa_backward_varlen(const void *Q, const void *K, const void *V, const void *O,

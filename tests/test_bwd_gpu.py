@@ -74,7 +74,7 @@ def compare(q, k, v, do, scale, mask, window, dq, dk, dv, kv_heads=None):
 
 
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [32, 64, 128])
 @pytest.mark.parametrize("N", [1, 63, 128, 129, 300])
 @pytest.mark.parametrize("mask,window", [("none", (0, 0)), ("causal", (0, 0)), ("window", (70, 5))])
 def test_bwd_parity(mask, window, N, d, dtype):

@@ -68,7 +68,7 @@ CASES = [
 
 
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [32, 64, 128])
 @pytest.mark.parametrize("mask,window", [("none", (0, 0)), ("causal", (0, 0)), ("window", (90, 3))])
 @pytest.mark.parametrize("case", range(len(CASES)))
 def test_bwd_varlen_parity(case, mask, window, d, dtype):

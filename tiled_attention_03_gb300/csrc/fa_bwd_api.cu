@@ -49,7 +49,9 @@ cudaError_t bwd_device_init(int dev) {
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     BwdDeviceState &s = g_bwd_dev[dev];
     std::call_once(s.once, [&s] {
-        cudaError_t e = configure_bwd<64, false>();
+        cudaError_t e = configure_bwd<32, false>();
+        if (e == cudaSuccess) e = configure_bwd<32, true>();
+        if (e == cudaSuccess) e = configure_bwd<64, false>();
         if (e == cudaSuccess) e = configure_bwd<64, true>();
         if (e == cudaSuccess) e = configure_bwd<128, false>();
         if (e == cudaSuccess) e = configure_bwd<128, true>();
@@ -156,7 +158,7 @@ fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O
     for (const void *q : ptrs)
         if (!aligned16(q)) return FA_ERR_INVALID_ARG;
     if (!fa_host::aligned4(LSE)) return FA_ERR_INVALID_ARG;
-    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (d != 32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
     if (N > (int64_t{1} << 29) || B * H > (int64_t{1} << 31)) return FA_ERR_UNSUPPORTED;
     const int64_t BH = B * H, BHkv = B * H_kv;
     const int64_t Npad = padded_rows(N);
@@ -247,7 +249,10 @@ fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    if (d == 64)
+    if (d == 32)
+        e = bf16 ? launch_bwd<32, true>(pp, mq, mk, mv, mdo, pkv, pq, info.sm_count, st)
+                 : launch_bwd<32, false>(pp, mq, mk, mv, mdo, pkv, pq, info.sm_count, st);
+    else if (d == 64)
         e = bf16 ? launch_bwd<64, true>(pp, mq, mk, mv, mdo, pkv, pq, info.sm_count, st)
                  : launch_bwd<64, false>(pp, mq, mk, mv, mdo, pkv, pq, info.sm_count, st);
     else
@@ -302,7 +307,7 @@ fa_status fa_backward_varlen(const void *Q, const void *K, const void *V, const 
     if (mask_mode == FA_MASK_WINDOW && (window_left < 0 || window_right < 0))
         return FA_ERR_INVALID_ARG;
     if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
-    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (d != 32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
     if (total_q > (int64_t{1} << 29) || total_k > (int64_t{1} << 29) || max_seqlen_q > total_q ||
         max_seqlen_k > total_k || B > (int64_t{1} << 20))
         return FA_ERR_UNSUPPORTED;
@@ -423,7 +428,10 @@ fa_status fa_backward_varlen(const void *Q, const void *K, const void *V, const 
     pq.sched = fa_host::next_sched_slot(info.sched);
 
     cudaError_t e;
-    if (d == 64)
+    if (d == 32)
+        e = bf16 ? launch_bwd_varlen<32, true>(pp, mq, mk, mv, mdo, pkv, pq, info.sm_count, st)
+                 : launch_bwd_varlen<32, false>(pp, mq, mk, mv, mdo, pkv, pq, info.sm_count, st);
+    else if (d == 64)
         e = bf16 ? launch_bwd_varlen<64, true>(pp, mq, mk, mv, mdo, pkv, pq, info.sm_count, st)
                  : launch_bwd_varlen<64, false>(pp, mq, mk, mv, mdo, pkv, pq, info.sm_count, st);
     else

@@ -58,7 +58,16 @@ constexpr int kTma2Warp = 10;
 constexpr int kRegsCompute = 208;
 constexpr int kRegsControl = 88;
 constexpr int kRegsNeeded = 256 * kRegsCompute + 128 * kRegsControl;
-constexpr int kRegionBytes = 128 * 128;  // 128 rows x 128 B: one 64-column swizzle region
+// Tiles are stored as regions of min(d, 64) columns x 128 rows with the swizzle of
+// that row width (128 B; 64 B at d = 32), as TMA writes them.
+template <int D>
+struct Rg {
+    static constexpr int kCols = D < 64 ? D : 64;
+    static constexpr int kRowBytes = kCols * 2;
+    static constexpr int kBytes = 128 * kRowBytes;   // one region
+    static constexpr int kCount = D / kCols;
+    static constexpr int kStepsPerRegion = kCols / 16;  // K-steps of 16 columns per region
+};
 constexpr uint32_t kTmemCols = 512;
 constexpr unsigned kStatusTimeout = 4;   // FA_ERR_TIMEOUT
 constexpr int kMaxDynSmem = 232448;      // per-CTA opt-in limit of sm_100-class GPUs
@@ -119,6 +128,23 @@ __device__ __forceinline__ SeqInfo seq_info(int b, const BwdParams &p) {
     return S;
 }
 
+// 32 lanes x 16 consecutive 32-bit TMEM columns into registers, waited for.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
+}
+
 // Units are taken from a launch-wide counter by the TMA producer and handed to
 // the other roles through a two-slot ring in shared memory (id -1 ends every
 // role's loop), so that CTAs that finish early take more of the units.
@@ -159,8 +185,8 @@ __device__ __forceinline__ int group_head(int bkv, int g, const BwdParams &p) {
 // which comes earlier. The Q ring is the deeper one: its slots are held longer.
 template <int D>
 struct KvSmem {
-    static constexpr int kQStages = D == 64 ? 4 : 3;
-    static constexpr int kOStages = D == 64 ? 4 : 2;
+    static constexpr int kQStages = D <= 64 ? 4 : 3;
+    static constexpr int kOStages = D <= 64 ? 4 : 2;
     static constexpr int kTileBytes = kTile * D * 2;
     static constexpr int kVecBytes = kTile * 4;
     static constexpr int kK = 0;
@@ -207,11 +233,11 @@ struct KvTmem {
     static constexpr uint32_t kDP = 128;     // dP^T, then dS^T (16-bit) over 128-159, 192-223
     static constexpr uint32_t kDV = 256;
     static constexpr uint32_t kDK = 256 + D;
-    // d = 64 leaves 128 columns for a second S^T buffer (query block n uses buffer
+    // d <= 64 leaves 128 columns for a second S^T buffer (query block n uses buffer
     // n mod 2), so S^T(n+2) needs only dV(n) before it, not the whole chain.
-    static constexpr bool kDoubleS = D == 64;
+    static constexpr bool kDoubleS = D <= 64;
     static constexpr uint32_t kS1 = kDoubleS ? 256 + 2 * D : kS;
-    static_assert(D == 64 || D == 128, "head dim");
+    static_assert(D == 32 || D == 64 || D == 128, "head dim");
     __device__ static constexpr uint32_t s_buf(int it) { return (kDoubleS && (it & 1)) ? kS1 : kS; }
 };
 
@@ -317,7 +343,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const BwdParams p) {
     using L = KvSmem<D>;
     using T = KvTmem<D>;
-    constexpr int kRegions = D / 64;
+    using G = Rg<D>;
+    constexpr int kRegions = G::kCount;
     constexpr int kQS = L::kQStages;
     constexpr int kOS = L::kOStages;
 
@@ -423,8 +450,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     int ky, kz;
                     kv_coords(U, U.bkv, U.k0, p, ky, kz);
                     for (int g = 0; g < kRegions; ++g) {
-                        tma_load_3d(sK + g * kRegionBytes, &tmK, bar(kKvKVFull), 64 * g, ky, kz);
-                        tma_load_3d(sV + g * kRegionBytes, &tmV, bar(kKvKVFull), 64 * g, ky, kz);
+                        tma_load_3d(sK + g * G::kBytes, &tmK, bar(kKvKVFull), G::kCols * g, ky, kz);
+                        tma_load_3d(sV + g * G::kBytes, &tmV, bar(kKvKVFull), G::kCols * g, ky, kz);
                     }
                 }
                 ++kv_loads;
@@ -437,8 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     int wy, wz;
                     kv_coords(W, W.bkv, W.k0, p, wy, wz);
                     for (int g = 0; g < kRegions; ++g) {
-                        tma_prefetch_l2_3d(&tmK, 64 * g, wy, wz);
-                        tma_prefetch_l2_3d(&tmV, 64 * g, wy, wz);
+                        tma_prefetch_l2_3d(&tmK, G::kCols * g, wy, wz);
+                        tma_prefetch_l2_3d(&tmV, G::kCols * g, wy, wz);
                     }
                 }
                 for (int n = 0; ok && n < U.n_it; ++n, ++it) {
@@ -454,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t fb = bar(kKvQFull + qs);
                     mbar_arrive_expect_tx(fb, L::kTileBytes + L::kVecBytes);
                     for (int g = 0; g < kRegions; ++g)
-                        tma_load_3d(sQ(it) + g * kRegionBytes, &tmQ, fb, 64 * g, qy, qz);
+                        tma_load_3d(sQ(it) + g * G::kBytes, &tmQ, fb, G::kCols * g, qy, qz);
                     bulk_load(sbase + L::kL + qs * L::kVecBytes, p.Lw + vrow, L::kVecBytes, fb);
                     ++q_loads;
                     // dO_i and D of its rows
@@ -464,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fb = bar(kKvOFull + os);
                     mbar_arrive_expect_tx(fb, L::kTileBytes + L::kVecBytes);
                     for (int g = 0; g < kRegions; ++g)
-                        tma_load_3d(sdO(it) + g * kRegionBytes, &tmdO, fb, 64 * g, qy, qz);
+                        tma_load_3d(sdO(it) + g * G::kBytes, &tmdO, fb, G::kCols * g, qy, qz);
                     bulk_load(sbase + L::kDv + os * L::kVecBytes, p.Dw + vrow, L::kVecBytes, fb);
                 }
                 u = u_next;
@@ -492,8 +519,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ================================================================ MMA issuer
         constexpr uint32_t idesc_kk = idesc_f16_ab(BF16, kTile, kTile, false, false);
         constexpr uint32_t idesc_tn = idesc_f16_ab(BF16, kTile, D, false, true);
-        constexpr uint32_t kRegion16 = kRegionBytes >> 4;
-        constexpr uint32_t kKStep16 = (16 * 128) >> 4;  // 16 rows of 128 B
+        constexpr uint32_t kRegion16 = G::kBytes >> 4;
+        constexpr uint32_t kKStep16 = (16 * G::kRowBytes) >> 4;  // 16 rows of the tile
         auto wait = [&](int b, uint32_t parity) {
             return __all_sync(0xffffffffu, mbar_wait_bounded(bar(b), parity, abort_flag, budget));
         };
@@ -504,12 +531,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // C[128 x 128] = A B^T with A, B both K-major (rows of d): S^T = K Q^T, dP^T = V dO^T.
         auto issue_kk = [&](uint32_t a_s, uint32_t b_s, uint32_t dcol) {
             tc_fence_after();
-            const uint64_t da = sw128_desc(a_s, 16, 1024);
-            const uint64_t db = sw128_desc(b_s, 16, 1024);
+            const uint64_t da = swz_desc<G::kRowBytes>(a_s, 16);
+            const uint64_t db = swz_desc<G::kRowBytes>(b_s, 16);
             if (elect_one()) {
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k >> 2) * kRegion16 + (k & 3) * 2;
+                    const uint32_t off = (k / G::kStepsPerRegion) * kRegion16 +
+                                         (k % G::kStepsPerRegion) * 2;
                     umma_f16_ss(tmem + dcol, da + off, db + off, idesc_kk, k > 0 ? 1u : 0u);
                 }
             }
@@ -519,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // columns acol + 64 w ...) and B MN-major in shared memory (rows = queries).
         auto issue_tn = [&](uint32_t acol, uint32_t b_s, uint32_t dcol, bool accumulate) {
             tc_fence_after();
-            const uint64_t db = sw128_desc(b_s, kRegionBytes, 1024);
+            const uint64_t db = swz_desc<G::kRowBytes>(b_s, G::kBytes);
             const uint32_t acc0 = accumulate ? 1u : 0u;
             if (elect_one()) {
 #pragma unroll
@@ -781,8 +809,8 @@ template <int D>
 struct QSmem {
     // K and V rings: K_j is read by S(j) and, later, by dQ += dS K_j, so its ring
     // is one deeper than V's (V_j is read by dP(j) only).
-    static constexpr int kKStages = D == 64 ? 4 : 3;
-    static constexpr int kVStages = D == 64 ? 4 : 2;
+    static constexpr int kKStages = D <= 64 ? 4 : 3;
+    static constexpr int kVStages = D <= 64 ? 4 : 2;
     static constexpr int kTileBytes = kTile * D * 2;
     static constexpr int kQ = 0;
     static constexpr int kdO = kQ + kTileBytes;
@@ -819,7 +847,7 @@ struct QTmem {
     static constexpr uint32_t kS = 0;        // S buffers b = 0, 1 at 128 b; dS (16-bit) over their columns 0-31, 64-95
     static constexpr uint32_t kDP = 256;
     static constexpr uint32_t kDQ = 384;
-    static_assert(D == 64 || D == 128, "head dim");
+    static_assert(D == 32 || D == 64 || D == 128, "head dim");
 };
 
 // A dQ unit: query block (rows i0 .. i0+127) of query head bh and the key blocks
@@ -866,7 +894,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const BwdParams p) {
     using L = QSmem<D>;
     using T = QTmem<D>;
-    constexpr int kRegions = D / 64;
+    using G = Rg<D>;
+    constexpr int kRegions = G::kCount;
     constexpr int kKS = L::kKStages;
     constexpr int kVS = L::kVStages;
 
@@ -976,8 +1005,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     int qy, qz;
                     q_coords(U, U.bh, U.i0, p, qy, qz);
                     for (int g = 0; g < kRegions; ++g) {
-                        tma_load_3d(sQ + g * kRegionBytes, &tmQ, bar(kQQFull), 64 * g, qy, qz);
-                        tma_load_3d(sdO + g * kRegionBytes, &tmdO, bar(kQQFull), 64 * g, qy, qz);
+                        tma_load_3d(sQ + g * G::kBytes, &tmQ, bar(kQQFull), G::kCols * g, qy, qz);
+                        tma_load_3d(sdO + g * G::kBytes, &tmdO, bar(kQQFull), G::kCols * g, qy, qz);
                     }
                     ++q_loads;
                     // Claim the next unit now; its Q and dO go to L2 while this unit
@@ -989,8 +1018,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         int wy, wz;
                         q_coords(W, W.bh, W.i0, p, wy, wz);
                         for (int g = 0; g < kRegions; ++g) {
-                            tma_prefetch_l2_3d(&tmQ, 64 * g, wy, wz);
-                            tma_prefetch_l2_3d(&tmdO, 64 * g, wy, wz);
+                            tma_prefetch_l2_3d(&tmQ, G::kCols * g, wy, wz);
+                            tma_prefetch_l2_3d(&tmdO, G::kCols * g, wy, wz);
                         }
                     }
                 }
@@ -1003,7 +1032,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     int ky, kz;
                     kv_coords(U, U.bkv, j * kTile, p, ky, kz);
                     for (int g = 0; g < kRegions; ++g)
-                        tma_load_3d(dst + g * kRegionBytes, map, bar(full0 + st), 64 * g, ky, kz);
+                        tma_load_3d(dst + g * G::kBytes, map, bar(full0 + st), G::kCols * g, ky, kz);
                 }
                 if (!ok) break;
                 if (!kq) u_next = take(unit_iter + 1);
@@ -1023,8 +1052,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ================================================================ MMA issuer
         constexpr uint32_t idesc_s = idesc_f16_ab(BF16, kTile, kTile, false, false);
         constexpr uint32_t idesc_q = idesc_f16_ab(BF16, kTile, D, false, true);
-        constexpr uint32_t kRegion16 = kRegionBytes >> 4;
-        constexpr uint32_t kKStep16 = (16 * 128) >> 4;
+        constexpr uint32_t kRegion16 = G::kBytes >> 4;
+        constexpr uint32_t kKStep16 = (16 * G::kRowBytes) >> 4;  // 16 rows of the tile
         auto wait = [&](int b, uint32_t parity) {
             return __all_sync(0xffffffffu, mbar_wait_bounded(bar(b), parity, abort_flag, budget));
         };
@@ -1035,12 +1064,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // C[128 x 128] = A B^T, A (Q or dO) and B (K or V) K-major.
         auto issue_kk = [&](uint32_t a_s, uint32_t b_s, uint32_t dcol) {
             tc_fence_after();
-            const uint64_t da = sw128_desc(a_s, 16, 1024);
-            const uint64_t db = sw128_desc(b_s, 16, 1024);
+            const uint64_t da = swz_desc<G::kRowBytes>(a_s, 16);
+            const uint64_t db = swz_desc<G::kRowBytes>(b_s, 16);
             if (elect_one()) {
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k >> 2) * kRegion16 + (k & 3) * 2;
+                    const uint32_t off = (k / G::kStepsPerRegion) * kRegion16 +
+                                         (k % G::kStepsPerRegion) * 2;
                     umma_f16_ss(tmem + dcol, da + off, db + off, idesc_s, k > 0 ? 1u : 0u);
                 }
             }
@@ -1050,7 +1080,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // K MN-major in shared memory (rows = keys).
         auto issue_dq = [&](uint32_t acol, uint32_t k_s, bool accumulate) {
             tc_fence_after();
-            const uint64_t db = sw128_desc(k_s, kRegionBytes, 1024);
+            const uint64_t db = swz_desc<G::kRowBytes>(k_s, G::kBytes);
             const uint32_t acc0 = accumulate ? 1u : 0u;
             if (elect_one()) {
 #pragma unroll
@@ -1237,20 +1267,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else
                     orow = static_cast<size_t>(U.bh) * p.N + (store ? i : 0);
                 uint8_t *out = reinterpret_cast<uint8_t *>(p.dQ) + (orow * D + wg * (D / 2)) * 2;
+                if constexpr (D / 2 >= 32) {
 #pragma unroll
-                for (int c = 0; c < D / 2; c += 32) {
-                    uint32_t a[32];
-                    tmem_ld32(tl + T::kDQ + wg * (D / 2) + c, a);
-                    tmem_ld_wait(a);
-                    uint32_t pk[16];
+                    for (int c = 0; c < D / 2; c += 32) {
+                        uint32_t a[32];
+                        tmem_ld32(tl + T::kDQ + wg * (D / 2) + c, a);
+                        tmem_ld_wait(a);
+                        uint32_t pk[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
+                        for (int e = 0; e < 16; ++e)
+                            pk[e] = pack2<BF16>(__uint_as_float(a[2 * e]) * p.scale,
+                                                __uint_as_float(a[2 * e + 1]) * p.scale);
+                        if (store) {
+                            st_global_v8(out + c * 2, pk);
+                            st_global_v8(out + c * 2 + 32, pk + 8);
+                        }
+                    }
+                } else {
+                    // d = 32: 16 columns per warpgroup
+                    uint32_t a[16];
+                    tmem_ld16(tl + T::kDQ + wg * (D / 2), a);
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
                         pk[e] = pack2<BF16>(__uint_as_float(a[2 * e]) * p.scale,
                                             __uint_as_float(a[2 * e + 1]) * p.scale);
-                    if (store) {
-                        st_global_v8(out + c * 2, pk);
-                        st_global_v8(out + c * 2 + 32, pk + 8);
-                    }
+                    if (store) st_global_v8(out, pk);
                 }
             }
             tc_fence_before();

@@ -117,6 +117,8 @@ BWD_WORKLOADS = [
              seed=10, backward=True),
     Workload("bwd_gqa_causal_b2h32kv8n4096d64", 2, 32, 4096, 64, torch.float16, MASK_CAUSAL, 0, 0,
              seed=11, H_kv=8, backward=True),
+    Workload("bwd_b4h32n4096d32", 4, 32, 4096, 32, torch.bfloat16, MASK_NONE, 0, 0, seed=19,
+             backward=True),
 ]
 
 # A packed batch of 16 causal sequences of mixed lengths (N/8 .. N), token-major.
