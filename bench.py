@@ -604,8 +604,8 @@ def main():
                 "kernel": (f"fa_bwd prep + dK/dV + dQ kernels <{w.d}, {w.dtype_name}"
                            + (", varlen>" if w.varlen else ">") if w.backward
                            else f"fa_fwd_kernel<{w.d}, {w.dtype_name}, varlen>" if w.varlen
-                           else f"fa_fwd256_kernel<{w.dtype_name}>" if w.d == 256
-                           else f"fa_fwd_kernel<{w.d}, {w.dtype_name}>"
+                           else (f"fa_fwd256_kernel<{w.dtype_name}>" if w.d == 256
+                                 else f"fa_fwd_kernel<{w.d}, {w.dtype_name}>")
                            + (f" + merge ({splits} key splits)" if splits > 1 else ""))},
             "cpu_baseline": cpu,
             "e2e": e2e,

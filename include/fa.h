@@ -59,8 +59,8 @@ typedef enum { FA_DTYPE_FP16 = 0, FA_DTYPE_BF16 = 1 } fa_dtype;
  *           rows and keys past N are handled inside the kernel).
  * d       : head dimension: 32, 64, 128 or 256 (else FA_ERR_UNSUPPORTED). d = 256
  *           runs its own kernel (one 128-row Q tile per unit, 64-key K/V tiles)
- *           and is available in fa_forward and fa_forward_gqa only; the split-KV
- *           and variable-length calls take 32, 64 and 128, as does fa_backward.
+ *           in fa_forward, fa_forward_gqa, the split-KV calls and fa_forward_host;
+ *           the variable-length calls take 32, 64 and 128, as does fa_backward.
  * scale   : multiplier of the logits, finite and > 0 (typically 1/sqrt(d)).
  * mask_mode, window_left, window_right : see fa_mask_mode. The window
  *           arguments are read only for FA_MASK_WINDOW and must then be >= 0

@@ -85,13 +85,14 @@ def test_d256_gqa_long(mask):
     compare(o, lse, q, k, v, 256 ** -0.5, mask)
 
 
-def test_d256_rejects_split_and_rectangular():
+def test_d256_varlen_rejected():
+    """d = 256 has no variable-length form: the call is refused before anything
+    is enqueued, and the next call still works."""
     dev = torch.device("cuda", 0)
-    q, k, v = (t.to(dev) for t in make_qkv(1, 2, 64, 256, torch.float16, seed=0))
-    o, lse = torch.empty_like(q), torch.empty(1, 2, 64, device=dev)
-    with pytest.raises(fa.FaError):
-        fa.fa_forward_splitkv(q, k, v, o, lse, 0.0625, "none", 0, 0, 2)
-    with pytest.raises(fa.FaError):
-        fa.fa_forward_splitkv(q[:, :, :10].contiguous(), k, v, o[:, :, :10].contiguous(),
-                              lse[:, :, :10].contiguous(), 0.0625, "none", 0, 0, 1)
+    q, k, v = (t.to(dev).view(64, 2, 256) for t in make_qkv(1, 2, 64, 256, torch.float16, seed=0))
+    o, lse = torch.empty_like(q), torch.empty(64, 2, device=dev)
+    cu = torch.tensor([0, 30, 64], dtype=torch.int32, device=dev)
+    with pytest.raises(fa.FaError) as e:
+        fa.fa_forward_varlen(q, k, v, o, lse, cu, cu, 34, 0.0625)
+    assert e.value.status == fa.FA_ERR_UNSUPPORTED
     assert fa.fa_sync_status() == fa.FA_OK

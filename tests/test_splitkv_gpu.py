@@ -44,6 +44,21 @@ def test_splitkv_parity(splits, mask, window, Nq, Nk, d, dtype):
     compare(o, lse, q, k, v, d ** -0.5, mask, window)
 
 
+# d = 256 runs its own kernel (64-key K/V tiles, so a split of s 128-key tiles is 2s of
+# its tiles); queries may also outnumber the keys when there is no mask.
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("Nq,Nk", [(1, 1), (1, 5000), (4, 1000), (100, 3000), (300, 300), (200, 70)])
+@pytest.mark.parametrize("mask,window", [("none", (0, 0)), ("causal", (0, 0)), ("window", (500, 0))])
+@pytest.mark.parametrize("splits", [1, 3, 40])
+def test_splitkv_parity_d256(splits, mask, window, Nq, Nk, dtype):
+    if Nq > Nk and mask != "none":
+        pytest.skip("masks place the queries at the last key positions: Nq <= Nk")
+    q, _, _ = make_qkv(1, 4, Nq, 256, dtype, seed=Nq + splits + 1)
+    _, k, v = make_qkv(1, 2, Nk, 256, dtype, seed=Nk + 3 * splits + 1, H_kv=2)
+    o, lse = run_split(q, k, v, 0.0625, mask, window, splits)
+    compare(o, lse, q, k, v, 0.0625, mask, window)
+
+
 # Few queries per head with grouped K/V heads: the query heads of a K/V head share
 # one row space, so 128-row tiles hold several heads and cut through heads.
 @pytest.mark.parametrize("B,H,Hk,Nq,Nk", [
@@ -60,9 +75,10 @@ def test_packed_query_heads(splits, mask, window, B, H, Hk, Nq, Nk):
     compare(o, lse, q, k, v, 0.09, mask, window)
 
 
+@pytest.mark.parametrize("d", [128, 256])
 @pytest.mark.parametrize("mask", ["none", "causal"])
-def test_splitkv_matches_unsplit_kernel(mask):
-    q, k, v = make_qkv(2, 8, 2000, 128, torch.bfloat16, seed=5)
+def test_splitkv_matches_unsplit_kernel(mask, d):
+    q, k, v = make_qkv(2, 8, 2000, d, torch.bfloat16, seed=5)
     o1, l1 = run_cuda(q, k, v, 0.088, mask)
     for splits in (2, 5, 16):
         o2, l2 = run_split(q, k, v, 0.088, mask, splits=splits)

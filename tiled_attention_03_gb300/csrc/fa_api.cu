@@ -276,16 +276,18 @@ cudaError_t launch_combine(const fa::CombineParams &c, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-// Head dimension 256: its own kernel (one 128-row Q tile per unit, 64-key K/V
-// tiles), for queries and keys at the same positions and without key splits.
+// Head dimension 256: its own kernel, set up once per device.
 struct D256State {
     std::once_flag once;
     cudaError_t err = cudaSuccess;
 };
 D256State g_d256[kMaxDevices];
 
-fa_status run_forward_256(const Call &c, DeviceState *ds, int dev) {
-    if (c.Nq != c.Nk || c.num_splits != 1) return FA_ERR_UNSUPPORTED;
+// d = 256: its own kernel (one 128-row Q tile per unit, 64-key K/V tiles). The key
+// splits are those of the generic path (split_tiles 128-key tiles each, so the
+// workspace and the merge are the same); the kernel counts them in 64-key tiles.
+fa_status run_forward_256(const Call &c, DeviceState *ds, int dev, int64_t n_splits,
+                          int64_t split_tiles) {
     if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
     D256State &s = g_d256[dev];
     std::call_once(s.once, [&s] {
@@ -298,33 +300,47 @@ fa_status run_forward_256(const Call &c, DeviceState *ds, int dev) {
         s.err = e;
     });
     if (s.err != cudaSuccess) return FA_ERR_CUDA;
-    const int64_t B = c.B, H = c.H, H_kv = c.H_kv, N = c.Nq, d = 256;
+    const int64_t B = c.B, H = c.H, H_kv = c.H_kv, Nq = c.Nq, Nk = c.Nk, d = 256;
     const bool bf16 = c.dtype == FA_DTYPE_BF16;
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, c.Q, bf16, B * H, N, d, fa::d256::kBM) ||
-        !make_map(&mk, c.K, bf16, B * H_kv, N, d, fa::d256::kBN) ||
-        !make_map(&mv, c.V, bf16, B * H_kv, N, d, fa::d256::kBN))
+    if (!make_map(&mq, c.Q, bf16, B * H, Nq, d, fa::d256::kBM) ||
+        !make_map(&mk, c.K, bf16, B * H_kv, Nk, d, fa::d256::kBN) ||
+        !make_map(&mv, c.V, bf16, B * H_kv, Nk, d, fa::d256::kBN))
         return FA_ERR_CUDA;
+    const bool split = n_splits > 1;
+    const int64_t BH = B * H;
     fa::d256::Params p{};
     p.O = c.O;
     p.LSE = c.LSE;
-    p.N = static_cast<int>(N);
+    if (split) {
+        p.part_LSE = static_cast<float *>(c.workspace);
+        p.part_O = reinterpret_cast<float *>(static_cast<uint8_t *>(c.workspace) +
+                                             align256(static_cast<size_t>(n_splits) * BH * Nq *
+                                                      sizeof(float)));
+    }
+    p.Nq = static_cast<int>(Nq);
+    p.Nk = static_cast<int>(Nk);
+    p.q_off = static_cast<int>(Nk - Nq);
     p.H = static_cast<int>(H);
+    p.BH = static_cast<int>(BH);
     p.kv_group = static_cast<int>(H / H_kv);
-    const int64_t n_qb = (N + fa::d256::kBM - 1) / fa::d256::kBM;
-    const int64_t n_units = B * H * n_qb;
+    const int64_t n_qb = (Nq + fa::d256::kBM - 1) / fa::d256::kBM;
+    const int64_t n_units = BH * n_qb * n_splits;
     if (n_units > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
     p.n_units = static_cast<int>(n_units);
     p.n_qb = static_cast<int>(n_qb);
-    int64_t wl = N, wr = N;
+    p.n_splits = static_cast<int>(n_splits);
+    p.split_tiles = static_cast<int>(split_tiles * (fa::kBN / fa::d256::kBN));
+    const int64_t all = Nq + Nk;
+    int64_t wl = all, wr = all;
     if (c.mask_mode == FA_MASK_CAUSAL) wr = 0;
     if (c.mask_mode == FA_MASK_WINDOW) {
-        wl = c.window_left < N ? c.window_left : N;
-        wr = c.window_right < N ? c.window_right : N;
+        wl = c.window_left < all ? c.window_left : all;
+        wr = c.window_right < all ? c.window_right : all;
     }
     p.wl = static_cast<int>(wl);
     p.wr = static_cast<int>(wr);
-    p.heavy_first = wr < N ? 1 : 0;
+    p.heavy_first = wr < Nk ? 1 : 0;
     p.scale_log2 = static_cast<float>(static_cast<double>(c.scale) * 1.4426950408889634074);
     p.wait_budget_ns = wait_budget();
     p.status = ds->status;
@@ -339,6 +355,24 @@ fa_status run_forward_256(const Call &c, DeviceState *ds, int dev) {
             mq, mk, mv, p);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     g_launches.fetch_add(1);
+    if (split) {
+        fa::CombineParams cp{};
+        cp.part_O = p.part_O;
+        cp.part_LSE = p.part_LSE;
+        cp.O = c.O;
+        cp.LSE = c.LSE;
+        cp.BH = p.BH;
+        cp.Nq = p.Nq;
+        cp.Nk = p.Nk;
+        cp.q_off = p.q_off;
+        cp.wl = p.wl;
+        cp.wr = p.wr;
+        cp.n_splits = p.n_splits;
+        cp.split_keys = static_cast<int>(split_tiles * fa::kBN);
+        const cudaError_t e = bf16 ? launch_combine<256, true>(cp, st) : launch_combine<256, false>(cp, st);
+        if (e != cudaSuccess) return FA_ERR_CUDA;
+        g_launches.fetch_add(1);
+    }
     return FA_OK;
 }
 
@@ -411,7 +445,7 @@ fa_status run_forward(const Call &c) {
     if (!on_device(Q, dev) || !on_device(K, dev) || !on_device(V, dev) || !on_device(O, dev) ||
         !on_device(LSE, dev) || (split && !on_device(c.workspace, dev)))
         return FA_ERR_INVALID_ARG;
-    if (d == 256) return run_forward_256(c, ds, dev);
+    if (d == 256) return run_forward_256(c, ds, dev, n_splits, split_tiles);
 
     const bool bf16 = c.dtype == FA_DTYPE_BF16;
     CUtensorMap mq, mk, mv;

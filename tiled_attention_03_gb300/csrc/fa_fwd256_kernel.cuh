@@ -16,6 +16,10 @@
 // alternating barriers, one per parity of j, so that a skipped wait never
 // confuses phases: a product two blocks later cannot complete first).
 //
+// Queries may be fewer than keys (Nq <= Nk: query i at key position i + Nk - Nq), and
+// the keys may be cut into splits whose fp32 partial results fa_combine_kernel merges,
+// as in fa_fwd_kernel.cuh.
+//
 // Warps (256 threads): 0-3 softmax, 4 scheduler + Q and K producer, 5 MMA issuer,
 // 6 V producer, 7 idle. Every wait is bounded; on expiry the CTA records the
 // failure, drains its copies and MMAs, frees its tensor memory and returns.
@@ -49,10 +53,16 @@ enum : int { kRoleSoftmax = 1, kRoleTma = 2, kRoleMma = 3 };
 struct Params {
     void *O;
     float *LSE;
-    int N, H, kv_group;
-    int n_units, n_qb;   // (b*H + h, 128-row block) units; blocks per head
+    float *part_O;       // key split: fp32 partial O / l [split][b*H+h][Nq][d]; null: write O, LSE
+    float *part_LSE;     // key split: partial log-sum-exps [split][b*H+h][Nq]
+    int Nq, Nk;          // queries and keys per head
+    int q_off;           // query i stands at key position i + q_off (Nk - Nq)
+    int H, BH, kv_group;
+    int n_units, n_qb;   // (b*H + h, 128-row block, key split) units; blocks per head
+    int n_splits;        // key splits per block (1: none)
+    int split_tiles;     // 64-key K/V tiles per split
     int heavy_first;
-    int wl, wr;          // key j visible to query i iff i - wl <= j <= i + wr
+    int wl, wr;          // key j visible to query i iff i + q_off - wl <= j <= i + q_off + wr
     float scale_log2;
     unsigned long long wait_budget_ns;
     unsigned int *status;
@@ -98,21 +108,30 @@ static_assert(kNumBarsUsed <= Smem::kNumBars, "barrier slots");
 constexpr uint32_t kTmemS = 0;
 constexpr uint32_t kTmemO = 256;
 
+// A unit: rows r0 .. r0+127 of query head bh, restricted to the K/V tiles of key
+// split `split`; j0 .. j1 are the tiles holding a key some row sees (empty when
+// j1 < j0, possible only with key splits).
 struct Unit {
-    int bh, bkv, r0, j0, j1;
+    int bh, bkv, r0, j0, j1, split;
 };
 
 __device__ __forceinline__ Unit decode(int u, const Params &p) {
     Unit U;
-    U.bh = u / p.n_qb;
-    int qb = u - U.bh * p.n_qb;
+    const int per_bh = p.n_qb * p.n_splits;
+    U.bh = u / per_bh;
+    const int rem = u - U.bh * per_bh;
+    int qb = rem / p.n_splits;
+    U.split = rem - qb * p.n_splits;
     if (p.heavy_first) qb = p.n_qb - 1 - qb;
     const int b = U.bh / p.H, h = U.bh - b * p.H;
     U.bkv = b * (p.H / p.kv_group) + h / p.kv_group;
     U.r0 = qb * kBM;
-    const int rl = min(U.r0 + kBM, p.N) - 1;
-    U.j0 = max(0, U.r0 - p.wl) / kBN;
-    U.j1 = min(p.N - 1, rl + p.wr) / kBN;
+    const int rl = min(U.r0 + kBM, p.Nq) - 1;
+    const int lo_key = max(0, U.r0 + p.q_off - p.wl);
+    const int hi_key = min(p.Nk - 1, rl + p.q_off + p.wr);
+    const int s_lo = U.split * p.split_tiles, s_hi = s_lo + p.split_tiles - 1;
+    U.j0 = max(lo_key / kBN, s_lo);
+    U.j1 = hi_key < 0 ? -1 : min(hi_key / kBN, s_hi);
     return U;
 }
 
@@ -211,8 +230,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = mbar_wait_bounded(bar(kBarUnitEmpty + slot), ((k / kUnitSlots) & 1) ^ 1,
                                        abort_flag, budget);
                 if (!ok) return -1;
-                const unsigned next = atomicAdd(p.sched, 1u);
-                const int v = next < static_cast<unsigned>(p.n_units) ? static_cast<int>(next) : -1;
+                // units whose key split holds no key of theirs are skipped here
+                int v = -1;
+                while (true) {
+                    const unsigned next = atomicAdd(p.sched, 1u);
+                    if (next >= static_cast<unsigned>(p.n_units)) break;
+                    const Unit W = decode(static_cast<int>(next), p);
+                    if (W.j0 <= W.j1) {
+                        v = static_cast<int>(next);
+                        break;
+                    }
+                }
                 unit_ring[slot] = v;
                 mbar_arrive(bar(kBarUnitFull + slot));
                 return v;
@@ -380,12 +408,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             u = take_unit(unit_iter, ok);
             if (!ok || u < 0) break;
             const Unit U = decode(u, p);
-            const int i = U.r0 + row;
-            const int rl = min(U.r0 + kBM, p.N) - 1;
-            const int lo_i = max(0, i - p.wl);
-            const int hi_i = min(p.N - 1, i + p.wr);
-            const int lo_last = max(0, rl - p.wl);
-            const int hi_first = min(p.N - 1, U.r0 + p.wr);
+            const int i = U.r0 + row;  // query index; key position i + q_off
+            const int rl = min(U.r0 + kBM, p.Nq) - 1;
+            const int lo_i = max(0, i + p.q_off - p.wl);
+            const int hi_i = min(p.Nk - 1, i + p.q_off + p.wr);
+            const int lo_last = max(0, rl + p.q_off - p.wl);
+            const int hi_first = min(p.Nk - 1, U.r0 + p.q_off + p.wr);
             float m = -INFINITY, l = 0.f;
             for (int j = U.j0; j <= U.j1; ++j, ++t) {
                 const uint32_t tS = tl + kTmemS + (t % kSBufs) * kBN;
@@ -474,24 +502,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
-            const bool store = i < p.N;
-            const size_t grow = static_cast<size_t>(U.bh) * p.N + (store ? i : 0);
-            uint8_t *orow = reinterpret_cast<uint8_t *>(p.O) + grow * (D * 2);
+            const bool store = i < p.Nq;
+            const size_t grow = static_cast<size_t>(U.bh) * p.Nq + (store ? i : 0);
+            const float lse = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+            if (p.part_O == nullptr) {
+                uint8_t *orow = reinterpret_cast<uint8_t *>(p.O) + grow * (D * 2);
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                tmem_ld32(tl + kTmemO + c * 32, o);
-                tmem_ld_wait(o);
-                uint32_t pk[16];
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tl + kTmemO + c * 32, o);
+                    tmem_ld_wait(o);
+                    uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    pk[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
-                if (store) {
-                    st_global_v8(orow + c * 64, pk);
-                    st_global_v8(orow + c * 64 + 32, pk + 8);
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
+                    if (store) {
+                        st_global_v8(orow + c * 64, pk);
+                        st_global_v8(orow + c * 64 + 32, pk + 8);
+                    }
                 }
+                if (store) p.LSE[grow] = lse;
+            } else {
+                // key split: the split's own O / l in fp32 and its LSE, merged later
+                const size_t prow = static_cast<size_t>(U.split) * p.BH * p.Nq + grow;
+                float *orow = p.part_O + prow * D;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tl + kTmemO + c * 32, o);
+                    tmem_ld_wait(o);
+                    if (store) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            o[e] = __float_as_uint(__uint_as_float(o[e]) * inv_l);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) st_global_v8(orow + c * 32 + q * 8, o + q * 8);
+                    }
+                }
+                if (store) p.part_LSE[prow] = lse;
             }
-            if (store) p.LSE[grow] = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
             tc_fence_before();
             mbar_arrive(bar(kBarOFree));
         }

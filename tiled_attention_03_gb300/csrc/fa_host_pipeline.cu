@@ -62,8 +62,7 @@ struct Plan {
     size_t total = 0;
 };
 
-// Shape checks of fa_forward_splitkv (and of fa_forward for d = 256, which has
-// no key-split form); false when invalid, with the status to return.
+// Shape checks of fa_forward_splitkv; false when invalid, with the status to return.
 bool plan(int64_t B, int64_t H, int64_t H_kv, int64_t Nq, int64_t Nk, int64_t d,
           int64_t num_splits, int64_t chunk_bytes, Plan &pl, fa_status &why) {
     why = FA_ERR_INVALID_ARG;
@@ -74,7 +73,6 @@ bool plan(int64_t B, int64_t H, int64_t H_kv, int64_t Nq, int64_t Nk, int64_t d,
     if (Nq > (int64_t{1} << 29) || Nk > (int64_t{1} << 29) || B * H > (int64_t{1} << 31))
         return false;
     pl.split = num_splits > 0 || Nq != Nk;
-    if (d == 256 && pl.split) return false;
     pl.group = H / H_kv;
     const int64_t per_kv_head = (pl.group * Nq + 2 * Nk) * d * kElem;
     const int64_t chunk = chunk_bytes > 0 ? chunk_bytes : kDefaultChunkBytes;

@@ -107,6 +107,11 @@ EXTRA_WORKLOADS = [
     # head dimension 256 (its own kernel), same FLOPs as the bench shape
     Workload("full_b4h16n4096d256", 4, 16, 4096, 256, torch.bfloat16, MASK_NONE, 0, 0, seed=14),
     Workload("causal_b4h16n4096d256", 4, 16, 4096, 256, torch.bfloat16, MASK_CAUSAL, 0, 0, seed=15),
+    # split-KV at head dimension 256: a decode step and a 512-query chunk on a long cache
+    Workload("decode_b8h16kv4_nq1_nk32768_d256", 8, 16, 32768, 256, torch.bfloat16, MASK_CAUSAL,
+             0, 0, seed=20, H_kv=4, Nq=1, splits=0),
+    Workload("chunk_b1h16kv4_nq512_nk16384_d256", 1, 16, 16384, 256, torch.bfloat16, MASK_CAUSAL,
+             0, 0, seed=21, H_kv=4, Nq=512, splits=0),
 ]
 
 # Backward pass on the bench shape (dO drawn after Q, K, V from the same generator).
