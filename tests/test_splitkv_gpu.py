@@ -60,17 +60,19 @@ def test_splitkv_parity_d256(splits, mask, window, Nq, Nk, dtype):
 
 
 # Few queries per head with grouped K/V heads: the query heads of a K/V head share
-# one row space, so 128-row tiles hold several heads and cut through heads.
+# one row space, so 128-row tiles hold several heads and cut through heads (both
+# the d = 128 kernel and the d = 256 kernel).
 @pytest.mark.parametrize("B,H,Hk,Nq,Nk", [
     (2, 16, 2, 1, 3000), (1, 16, 2, 33, 1500), (1, 8, 1, 64, 700), (3, 12, 4, 7, 129),
     (1, 32, 8, 5, 40), (2, 6, 3, 64, 64), (1, 4, 2, 65, 900)])
 @pytest.mark.parametrize("mask,window", [("none", (0, 0)), ("causal", (0, 0)),
                                          ("window", (200, 0)), ("window", (30, 20))])
 @pytest.mark.parametrize("splits", [1, 4])
-def test_packed_query_heads(splits, mask, window, B, H, Hk, Nq, Nk):
+@pytest.mark.parametrize("d", [128, 256])
+def test_packed_query_heads(d, splits, mask, window, B, H, Hk, Nq, Nk):
     dtype = torch.bfloat16
-    q, _, _ = make_qkv(B, H, Nq, 128, dtype, seed=Nq * 7 + splits)
-    _, k, v = make_qkv(B, Hk, Nk, 128, dtype, seed=Nk + H, H_kv=Hk)
+    q, _, _ = make_qkv(B, H, Nq, d, dtype, seed=Nq * 7 + splits)
+    _, k, v = make_qkv(B, Hk, Nk, d, dtype, seed=Nk + H, H_kv=Hk)
     o, lse = run_split(q, k, v, 0.09, mask, window, splits)
     compare(o, lse, q, k, v, 0.09, mask, window)
 

@@ -302,8 +302,13 @@ fa_status run_forward_256(const Call &c, DeviceState *ds, int dev, int64_t n_spl
     if (s.err != cudaSuccess) return FA_ERR_CUDA;
     const int64_t B = c.B, H = c.H, H_kv = c.H_kv, Nq = c.Nq, Nk = c.Nk, d = 256;
     const bool bf16 = c.dtype == FA_DTYPE_BF16;
+    // few queries with grouped heads: one row space per K/V head (its query heads'
+    // rows in turn), so that each K/V tile is read once for all of them
+    const bool packed = pack_rows(H, H_kv, Nq);
+    const int64_t hps = packed ? H / H_kv : 1;
+    const int64_t spaces = B * H / hps, R = hps * Nq;
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, c.Q, bf16, B * H, Nq, d, fa::d256::kBM) ||
+    if (!make_map(&mq, c.Q, bf16, spaces, R, d, fa::d256::kBM) ||
         !make_map(&mk, c.K, bf16, B * H_kv, Nk, d, fa::d256::kBN) ||
         !make_map(&mv, c.V, bf16, B * H_kv, Nk, d, fa::d256::kBN))
         return FA_ERR_CUDA;
@@ -321,11 +326,12 @@ fa_status run_forward_256(const Call &c, DeviceState *ds, int dev, int64_t n_spl
     p.Nq = static_cast<int>(Nq);
     p.Nk = static_cast<int>(Nk);
     p.q_off = static_cast<int>(Nk - Nq);
-    p.H = static_cast<int>(H);
     p.BH = static_cast<int>(BH);
     p.kv_group = static_cast<int>(H / H_kv);
-    const int64_t n_qb = (Nq + fa::d256::kBM - 1) / fa::d256::kBM;
-    const int64_t n_units = BH * n_qb * n_splits;
+    p.hps = static_cast<int>(hps);
+    p.R = static_cast<int>(R);
+    const int64_t n_qb = (R + fa::d256::kBM - 1) / fa::d256::kBM;
+    const int64_t n_units = spaces * n_qb * n_splits;
     if (n_units > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
     p.n_units = static_cast<int>(n_units);
     p.n_qb = static_cast<int>(n_qb);

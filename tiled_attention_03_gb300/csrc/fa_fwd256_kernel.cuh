@@ -16,9 +16,10 @@
 // alternating barriers, one per parity of j, so that a skipped wait never
 // confuses phases: a product two blocks later cannot complete first).
 //
-// Queries may be fewer than keys (Nq <= Nk: query i at key position i + Nk - Nq), and
-// the keys may be cut into splits whose fp32 partial results fa_combine_kernel merges,
-// as in fa_fwd_kernel.cuh.
+// As in fa_fwd_kernel.cuh, query i stands at key position i + Nk - Nq (the last
+// positions when Nq < Nk), the query heads of one K/V head share a row space when
+// they have few queries each, and the keys may be cut into splits whose fp32 partial
+// results fa_combine_kernel merges.
 //
 // Warps (256 threads): 0-3 softmax, 4 scheduler + Q and K producer, 5 MMA issuer,
 // 6 V producer, 7 idle. Every wait is bounded; on expiry the CTA records the
@@ -57,8 +58,9 @@ struct Params {
     float *part_LSE;     // key split: partial log-sum-exps [split][b*H+h][Nq]
     int Nq, Nk;          // queries and keys per head
     int q_off;           // query i stands at key position i + q_off (Nk - Nq)
-    int H, BH, kv_group;
-    int n_units, n_qb;   // (b*H + h, 128-row block, key split) units; blocks per head
+    int BH, kv_group;    // query heads B*H; query heads per K/V head
+    int hps, R;          // query heads per row space (1, or kv_group when packed); rows hps*Nq
+    int n_units, n_qb;   // (row space, 128-row block, key split) units; blocks per space
     int n_splits;        // key splits per block (1: none)
     int split_tiles;     // 64-key K/V tiles per split
     int heavy_first;
@@ -108,27 +110,35 @@ static_assert(kNumBarsUsed <= Smem::kNumBars, "barrier slots");
 constexpr uint32_t kTmemS = 0;
 constexpr uint32_t kTmemO = 256;
 
-// A unit: rows r0 .. r0+127 of query head bh, restricted to the K/V tiles of key
-// split `split`; j0 .. j1 are the tiles holding a key some row sees (empty when
-// j1 < j0, possible only with key splits).
+// A row space holds the queries of hps consecutive query heads (b*H + h order), row
+// r being query r % Nq of head sp*hps + r / Nq: one head each, or, with few queries,
+// all heads of one K/V head, which then shares each K/V tile among them. In memory
+// it is rows sp*R .. sp*R + R - 1 of the [B*H*Nq] row order of Q, O and LSE.
+//
+// A unit: rows r0 .. rl of row space sp, restricted to the K/V tiles of key split
+// `split`; qmin .. qmax are the query indices among its rows; j0 .. j1 are the tiles
+// holding a key some row sees (empty when j1 < j0, possible only with key splits).
 struct Unit {
-    int bh, bkv, r0, j0, j1, split;
+    int sp, bkv, r0, rl, qmin, qmax, j0, j1, split;
 };
 
 __device__ __forceinline__ Unit decode(int u, const Params &p) {
     Unit U;
-    const int per_bh = p.n_qb * p.n_splits;
-    U.bh = u / per_bh;
-    const int rem = u - U.bh * per_bh;
+    const int per_sp = p.n_qb * p.n_splits;
+    U.sp = u / per_sp;
+    const int rem = u - U.sp * per_sp;
     int qb = rem / p.n_splits;
     U.split = rem - qb * p.n_splits;
     if (p.heavy_first) qb = p.n_qb - 1 - qb;
-    const int b = U.bh / p.H, h = U.bh - b * p.H;
-    U.bkv = b * (p.H / p.kv_group) + h / p.kv_group;
+    U.bkv = U.sp * p.hps / p.kv_group;  // (b*H + h) / group = b*H_kv + h / group
     U.r0 = qb * kBM;
-    const int rl = min(U.r0 + kBM, p.Nq) - 1;
-    const int lo_key = max(0, U.r0 + p.q_off - p.wl);
-    const int hi_key = min(p.Nk - 1, rl + p.q_off + p.wr);
+    U.rl = min(U.r0 + kBM, p.R) - 1;
+    // rows of one head: queries r0 % Nq .. rl % Nq; rows across a head boundary: all
+    const bool one_head = U.r0 / p.Nq == U.rl / p.Nq;
+    U.qmin = one_head ? U.r0 % p.Nq : 0;
+    U.qmax = one_head ? U.rl % p.Nq : p.Nq - 1;
+    const int lo_key = max(0, U.qmin + p.q_off - p.wl);
+    const int hi_key = min(p.Nk - 1, U.qmax + p.q_off + p.wr);
     const int s_lo = U.split * p.split_tiles, s_hi = s_lo + p.split_tiles - 1;
     U.j0 = max(lo_key / kBN, s_lo);
     U.j1 = hi_key < 0 ? -1 : min(hi_key / kBN, s_hi);
@@ -252,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 mbar_arrive_expect_tx(bar(kBarQFull), L::kQBytes);
                 for (int g = 0; g < 4; ++g)
-                    tma_load_3d(sQ + g * L::kQRegion, &tmQ, bar(kBarQFull), 64 * g, U.r0, U.bh);
+                    tma_load_3d(sQ + g * L::kQRegion, &tmQ, bar(kBarQFull), 64 * g, U.r0, U.sp);
                 ++q_loads;
                 int u_next = -1;
                 bool claimed = false;
@@ -263,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!ok) break;
                         if (u_next >= 0) {
                             const Unit W = decode(u_next, p);
-                            for (int g = 0; g < 4; ++g) tma_prefetch_l2_3d(&tmQ, 64 * g, W.r0, W.bh);
+                            for (int g = 0; g < 4; ++g) tma_prefetch_l2_3d(&tmQ, 64 * g, W.r0, W.sp);
                         }
                     }
                     const int st = t % kKStages;
@@ -408,12 +418,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             u = take_unit(unit_iter, ok);
             if (!ok || u < 0) break;
             const Unit U = decode(u, p);
-            const int i = U.r0 + row;  // query index; key position i + q_off
-            const int rl = min(U.r0 + kBM, p.Nq) - 1;
+            const int r = U.r0 + row;  // row of the space
+            const int i = r % p.Nq;    // its query index; key position i + q_off
             const int lo_i = max(0, i + p.q_off - p.wl);
             const int hi_i = min(p.Nk - 1, i + p.q_off + p.wr);
-            const int lo_last = max(0, rl + p.q_off - p.wl);
-            const int hi_first = min(p.Nk - 1, U.r0 + p.q_off + p.wr);
+            // a tile with keys in [lo_last, hi_first] only is visible to every row
+            const int lo_last = max(0, U.qmax + p.q_off - p.wl);
+            const int hi_first = min(p.Nk - 1, U.qmin + p.q_off + p.wr);
             float m = -INFINITY, l = 0.f;
             for (int j = U.j0; j <= U.j1; ++j, ++t) {
                 const uint32_t tS = tl + kTmemS + (t % kSBufs) * kBN;
@@ -502,8 +513,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
-            const bool store = i < p.Nq;
-            const size_t grow = static_cast<size_t>(U.bh) * p.Nq + (store ? i : 0);
+            const bool store = r < p.R;
+            const size_t grow = static_cast<size_t>(U.sp) * p.R + (store ? r : 0);
             const float lse = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
             if (p.part_O == nullptr) {
                 uint8_t *orow = reinterpret_cast<uint8_t *>(p.O) + grow * (D * 2);
