@@ -39,16 +39,30 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
 CSRC = "tiled_attention_03_gb300/csrc/"
 KERNEL_SOURCES = {
     "fwd": (CSRC + "fa_fwd_kernel.cuh", CSRC + "fa_combine.cuh", CSRC + "ptx.cuh"),
-    "fwd256": (CSRC + "fa_fwd256_kernel.cuh", CSRC + "ptx.cuh"),
+    "fwd1t": (CSRC + "fa_fwd1t_kernel.cuh", CSRC + "fa_combine.cuh", CSRC + "ptx.cuh"),
     "bwd": (CSRC + "fa_bwd_kernel.cuh", CSRC + "ptx.cuh"),
 }
 TRAFFIC_DIR = os.path.join(ROOT, "profiles")
 
 
+def one_tile(w) -> bool:
+    """Whether the library runs this forward on its one-tile kernel: always at d = 256,
+    and at d = 64 / 128 when a row space (one head's queries, or the queries of all
+    query heads of one K/V head when each has at most 64) holds at most 128 rows."""
+    if w.backward or w.varlen:
+        return False
+    if w.d == 256:
+        return True
+    if w.d not in (64, 128):
+        return False
+    packed = w.kv_heads < w.H and w.q_rows <= 64
+    return (w.H // w.kv_heads if packed else 1) * w.q_rows <= 128
+
+
 def kernel_family(w) -> str:
     if w.backward:
         return "bwd"
-    return "fwd256" if w.d == 256 else "fwd"
+    return "fwd1t" if one_tile(w) else "fwd"
 
 
 def kernel_source_hash(family: str) -> str:
@@ -604,7 +618,7 @@ def main():
                 "kernel": (f"fa_bwd prep + dK/dV + dQ kernels <{w.d}, {w.dtype_name}"
                            + (", varlen>" if w.varlen else ">") if w.backward
                            else f"fa_fwd_kernel<{w.d}, {w.dtype_name}, varlen>" if w.varlen
-                           else (f"fa_fwd256_kernel<{w.dtype_name}>" if w.d == 256
+                           else (f"fa_fwd1t_kernel<{w.d}, {w.dtype_name}>" if one_tile(w)
                                  else f"fa_fwd_kernel<{w.d}, {w.dtype_name}>")
                            + (f" + merge ({splits} key splits)" if splits > 1 else ""))},
             "cpu_baseline": cpu,

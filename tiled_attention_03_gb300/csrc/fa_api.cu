@@ -12,7 +12,7 @@
 
 #include "fa.h"
 #include "fa_combine.cuh"
-#include "fa_fwd256_kernel.cuh"
+#include "fa_fwd1t_kernel.cuh"
 #include "fa_fwd_kernel.cuh"
 #include "fa_host.h"
 
@@ -276,31 +276,56 @@ cudaError_t launch_combine(const fa::CombineParams &c, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-// Head dimension 256: its own kernel, set up once per device.
-struct D256State {
+// The one-tile kernel (fa_fwd1t_kernel.cuh), set up once per device.
+struct OneTileState {
     std::once_flag once;
     cudaError_t err = cudaSuccess;
 };
-D256State g_d256[kMaxDevices];
+OneTileState g_onetile[kMaxDevices];
 
-// d = 256: its own kernel (one 128-row Q tile per unit, 64-key K/V tiles). The key
-// splits are those of the generic path (split_tiles 128-key tiles each, so the
-// workspace and the merge are the same); the kernel counts them in 64-key tiles.
-fa_status run_forward_256(const Call &c, DeviceState *ds, int dev, int64_t n_splits,
-                          int64_t split_tiles) {
+template <int D, bool BF16>
+cudaError_t onetile_attr() {
+    return cudaFuncSetAttribute(fa::onetile::fa_fwd1t_kernel<D, BF16>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                fa::onetile::Smem<D>::kAlloc);
+}
+
+template <int D, bool BF16>
+cudaError_t launch_onetile(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                           const fa::onetile::Params &p, unsigned blocks, cudaStream_t st) {
+    fa::onetile::fa_fwd1t_kernel<D, BF16>
+        <<<blocks, fa::onetile::kThreads, fa::onetile::Smem<D>::kAlloc, st>>>(q, k, v, p);
+    return cudaGetLastError();
+}
+
+// Which kernel runs a dense forward: the one-tile kernel for d = 256, and for
+// d = 64 / 128 when a row space holds at most 128 rows (one Q tile: the two-tile
+// kernel would run one tile and wait on its softmax between S products).
+bool use_onetile(int64_t H, int64_t H_kv, int64_t Nq, int64_t d) {
+    if (d == 256) return true;
+    if (d != 64 && d != 128) return false;
+    const int64_t R = pack_rows(H, H_kv, Nq) ? (H / H_kv) * Nq : Nq;
+    return R <= fa::onetile::kBM;
+}
+
+// One 128-row Q tile per unit, 64-key K/V tiles. The key splits are those of the
+// two-tile path (split_tiles 128-key tiles each, so the workspace and the merge are
+// the same); the kernel counts them in 64-key tiles.
+fa_status run_forward_1t(const Call &c, DeviceState *ds, int dev, int64_t n_splits,
+                         int64_t split_tiles) {
     if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
-    D256State &s = g_d256[dev];
+    OneTileState &s = g_onetile[dev];
     std::call_once(s.once, [&s] {
-        constexpr int smem = fa::d256::Smem::kAlloc;
-        cudaError_t e = cudaFuncSetAttribute(fa::d256::fa_fwd256_kernel<false>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(fa::d256::fa_fwd256_kernel<true>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e = onetile_attr<64, false>();
+        if (e == cudaSuccess) e = onetile_attr<64, true>();
+        if (e == cudaSuccess) e = onetile_attr<128, false>();
+        if (e == cudaSuccess) e = onetile_attr<128, true>();
+        if (e == cudaSuccess) e = onetile_attr<256, false>();
+        if (e == cudaSuccess) e = onetile_attr<256, true>();
         s.err = e;
     });
     if (s.err != cudaSuccess) return FA_ERR_CUDA;
-    const int64_t B = c.B, H = c.H, H_kv = c.H_kv, Nq = c.Nq, Nk = c.Nk, d = 256;
+    const int64_t B = c.B, H = c.H, H_kv = c.H_kv, Nq = c.Nq, Nk = c.Nk, d = c.d;
     const bool bf16 = c.dtype == FA_DTYPE_BF16;
     // few queries with grouped heads: one row space per K/V head (its query heads'
     // rows in turn), so that each K/V tile is read once for all of them
@@ -308,13 +333,13 @@ fa_status run_forward_256(const Call &c, DeviceState *ds, int dev, int64_t n_spl
     const int64_t hps = packed ? H / H_kv : 1;
     const int64_t spaces = B * H / hps, R = hps * Nq;
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, c.Q, bf16, spaces, R, d, fa::d256::kBM) ||
-        !make_map(&mk, c.K, bf16, B * H_kv, Nk, d, fa::d256::kBN) ||
-        !make_map(&mv, c.V, bf16, B * H_kv, Nk, d, fa::d256::kBN))
+    if (!make_map(&mq, c.Q, bf16, spaces, R, d, fa::onetile::kBM) ||
+        !make_map(&mk, c.K, bf16, B * H_kv, Nk, d, fa::onetile::kBN) ||
+        !make_map(&mv, c.V, bf16, B * H_kv, Nk, d, fa::onetile::kBN))
         return FA_ERR_CUDA;
     const bool split = n_splits > 1;
     const int64_t BH = B * H;
-    fa::d256::Params p{};
+    fa::onetile::Params p{};
     p.O = c.O;
     p.LSE = c.LSE;
     if (split) {
@@ -330,13 +355,13 @@ fa_status run_forward_256(const Call &c, DeviceState *ds, int dev, int64_t n_spl
     p.kv_group = static_cast<int>(H / H_kv);
     p.hps = static_cast<int>(hps);
     p.R = static_cast<int>(R);
-    const int64_t n_qb = (R + fa::d256::kBM - 1) / fa::d256::kBM;
+    const int64_t n_qb = (R + fa::onetile::kBM - 1) / fa::onetile::kBM;
     const int64_t n_units = spaces * n_qb * n_splits;
     if (n_units > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
     p.n_units = static_cast<int>(n_units);
     p.n_qb = static_cast<int>(n_qb);
     p.n_splits = static_cast<int>(n_splits);
-    p.split_tiles = static_cast<int>(split_tiles * (fa::kBN / fa::d256::kBN));
+    p.split_tiles = static_cast<int>(split_tiles * (fa::kBN / fa::onetile::kBN));
     const int64_t all = Nq + Nk;
     int64_t wl = all, wr = all;
     if (c.mask_mode == FA_MASK_CAUSAL) wr = 0;
@@ -353,13 +378,17 @@ fa_status run_forward_256(const Call &c, DeviceState *ds, int dev, int64_t n_spl
     p.sched = ds->sched + 2 * (g_sched_next.fetch_add(1) % kSchedSlots);
     const unsigned blocks = static_cast<unsigned>(n_units < ds->sm_count ? n_units : ds->sm_count);
     cudaStream_t st = static_cast<cudaStream_t>(c.stream);
-    if (bf16)
-        fa::d256::fa_fwd256_kernel<true><<<blocks, fa::d256::kThreads, fa::d256::Smem::kAlloc, st>>>(
-            mq, mk, mv, p);
+    cudaError_t le;
+    if (d == 64)
+        le = bf16 ? launch_onetile<64, true>(mq, mk, mv, p, blocks, st)
+                  : launch_onetile<64, false>(mq, mk, mv, p, blocks, st);
+    else if (d == 128)
+        le = bf16 ? launch_onetile<128, true>(mq, mk, mv, p, blocks, st)
+                  : launch_onetile<128, false>(mq, mk, mv, p, blocks, st);
     else
-        fa::d256::fa_fwd256_kernel<false><<<blocks, fa::d256::kThreads, fa::d256::Smem::kAlloc, st>>>(
-            mq, mk, mv, p);
-    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+        le = bf16 ? launch_onetile<256, true>(mq, mk, mv, p, blocks, st)
+                  : launch_onetile<256, false>(mq, mk, mv, p, blocks, st);
+    if (le != cudaSuccess) return FA_ERR_CUDA;
     g_launches.fetch_add(1);
     if (split) {
         fa::CombineParams cp{};
@@ -375,7 +404,13 @@ fa_status run_forward_256(const Call &c, DeviceState *ds, int dev, int64_t n_spl
         cp.wr = p.wr;
         cp.n_splits = p.n_splits;
         cp.split_keys = static_cast<int>(split_tiles * fa::kBN);
-        const cudaError_t e = bf16 ? launch_combine<256, true>(cp, st) : launch_combine<256, false>(cp, st);
+        cudaError_t e;
+        if (d == 64)
+            e = bf16 ? launch_combine<64, true>(cp, st) : launch_combine<64, false>(cp, st);
+        else if (d == 128)
+            e = bf16 ? launch_combine<128, true>(cp, st) : launch_combine<128, false>(cp, st);
+        else
+            e = bf16 ? launch_combine<256, true>(cp, st) : launch_combine<256, false>(cp, st);
         if (e != cudaSuccess) return FA_ERR_CUDA;
         g_launches.fetch_add(1);
     }
@@ -451,7 +486,7 @@ fa_status run_forward(const Call &c) {
     if (!on_device(Q, dev) || !on_device(K, dev) || !on_device(V, dev) || !on_device(O, dev) ||
         !on_device(LSE, dev) || (split && !on_device(c.workspace, dev)))
         return FA_ERR_INVALID_ARG;
-    if (d == 256) return run_forward_256(c, ds, dev, n_splits, split_tiles);
+    if (use_onetile(H, H_kv, Nq, d)) return run_forward_1t(c, ds, dev, n_splits, split_tiles);
 
     const bool bf16 = c.dtype == FA_DTYPE_BF16;
     CUtensorMap mq, mk, mv;

@@ -1,14 +1,21 @@
-// fa_fwd256_kernel.cuh -- attention forward for head dimension 256 on sm_103a.
+// fa_fwd1t_kernel.cuh -- attention forward with one 128-row Q tile per work unit,
+// for head dimensions 64, 128 and 256 on sm_103a.
 //
 // Same method as fa_fwd_kernel.cuh (tiles of Q against K/V blocks, online softmax
 // with a lazily moved reference max, P in tensor memory, O divided by l once;
-// "ai6s.net/6af30f4d40858c2d8819b6d5" §2.2-§2.5), shaped for d = 256, where two
-// 128-row Q tiles would need 2 x 256 TMEM columns for O alone and 128-key K/V
-// tiles 64 KB each:
-//   * a unit is one 128-row Q tile (64 KB of shared memory);
-//   * K/V tiles hold 64 keys (32 KB each): K ring 3 deep, V ring 2 deep;
+// "ai6s.net/6af30f4d40858c2d8819b6d5" §2.2-§2.5), with one Q tile per unit and three
+// S buffers for it instead of two Q tiles with one S buffer each. It serves
+//   * d = 256, where two 128-row Q tiles would need 2 x 256 TMEM columns for O alone
+//     and 128-key K/V tiles would be 64 KB each;
+//   * row spaces of at most 128 rows (decode steps: the few queries of the heads of
+//     one K/V head), where the two-tile kernel would run one tile and wait on its own
+//     softmax between S(j) and S(j+1).
+// Layout:
+//   * a unit is one 128-row Q tile (128 x D, 16-bit);
+//   * K/V tiles hold 64 keys; the K and V rings are as deep as shared memory allows
+//     (3 and 2 at d = 256, 4 and 4 at d = 128, 6 and 6 at d = 64);
 //   * S is formed in one of three 64-column TMEM buffers, so that the softmax of
-//     block j runs while S(j+1) and S(j+2) are computed; O (256 columns) stays in
+//     block j runs while S(j+1) and S(j+2) are computed; O (D columns) stays in
 //     TMEM for the unit. MMA order: ... O += P(j) V_j | S(j+3) | O += P(j+1) V_{j+1} ...
 //   * one softmax warpgroup (thread = query row = TMEM lane, 64 keys per block).
 // When the reference max of a row moves (rare), the softmax thread rescales its O
@@ -32,17 +39,19 @@
 #include "ptx.cuh"
 
 namespace fa {
-namespace d256 {
+namespace onetile {
 
-constexpr int D = 256;
 constexpr int kBM = 128;        // query rows per unit
 constexpr int kBN = 64;         // keys per K/V tile
 constexpr int kThreads = 256;
 constexpr int kTmaWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kVWarp = 6;
-constexpr int kKStages = 3;
-constexpr int kVStages = 2;
+// K and V ring depths: what shared memory holds next to the Q tile (K/V tiles are
+// 64 x D, 16-bit)
+__host__ __device__ constexpr int k_stages(int D) { return D == 256 ? 3 : D == 128 ? 4 : 6; }
+__host__ __device__ constexpr int v_stages(int D) { return D == 256 ? 2 : D == 128 ? 4 : 6; }
+constexpr int kMaxStages = 6;
 constexpr int kSBufs = 3;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units, as in fa_fwd_kernel.cuh
@@ -71,40 +80,48 @@ struct Params {
     unsigned int *sched; // this launch's {next unit, finished CTAs}
 };
 
+// Tiles are stored as regions of 64 columns (128 bytes, the 128-byte swizzle).
+template <int D>
 struct Smem {
+    static_assert(D == 64 || D == 128 || D == 256, "head dimension");
+    static constexpr int kRegions = D / 64;
     static constexpr int kQRegion = kBM * 128;   // 128 rows x 128 B (64 columns)
     static constexpr int kKVRegion = kBN * 128;  // 64 rows x 128 B
-    static constexpr int kQBytes = 4 * kQRegion;
-    static constexpr int kKVBytes = 4 * kKVRegion;
+    static constexpr int kQBytes = kRegions * kQRegion;
+    static constexpr int kKVBytes = kRegions * kKVRegion;
     static constexpr int kQ = 0;
     static constexpr int kK = kQ + kQBytes;
-    static constexpr int kV = kK + kKStages * kKVBytes;
-    static constexpr int kBar = kV + kVStages * kKVBytes;
-    static constexpr int kNumBars = 32;
+    static constexpr int kV = kK + k_stages(D) * kKVBytes;
+    static constexpr int kBar = kV + v_stages(D) * kKVBytes;
+    static constexpr int kNumBars = 48;
     static constexpr int kMisc = kBar + kNumBars * 8;
     static constexpr int kUnitRing = kMisc + 16;
     static constexpr int kBytes = kUnitRing + 16;
-    static constexpr int kAlloc = kBytes + 1024;
+    // more than half of the SM's shared memory, so that one CTA (and one holder of
+    // all 512 TMEM columns) runs per SM
+    static constexpr int kAlloc = kBytes + 1024 > 120 * 1024 ? kBytes + 1024 : 120 * 1024;
+    static_assert(kAlloc <= 227 * 1024, "shared memory");
 };
 
 enum : int {
     kBarQFull = 0,
     kBarQEmpty = 1,
-    kBarKFull = 2,       // + stage (3)
-    kBarKEmpty = 5,      // + stage (3)
-    kBarVFull = 8,       // + stage (2)
-    kBarVEmpty = 10,     // + stage (2)
-    kBarSFull = 12,      // + buffer (3)
-    kBarPFull = 15,      // + buffer (3)
-    kBarPVDone = 18,     // + parity of the block (2)
-    kBarODone = 20,
-    kBarOFree = 21,
-    kBarUnitFull = 22,   // + slot (2)
-    kBarUnitEmpty = 24,  // + slot (2)
-    kBarDrainIdx = 26,
-    kNumBarsUsed = 27,
+    kBarKFull = 2,                         // + stage
+    kBarKEmpty = kBarKFull + kMaxStages,   // + stage
+    kBarVFull = kBarKEmpty + kMaxStages,   // + stage
+    kBarVEmpty = kBarVFull + kMaxStages,   // + stage
+    kBarSFull = kBarVEmpty + kMaxStages,   // + buffer (3)
+    kBarPFull = kBarSFull + kSBufs,        // + buffer (3)
+    kBarPVDone = kBarPFull + kSBufs,       // + parity of the block (2)
+    kBarODone = kBarPVDone + 2,
+    kBarOFree = kBarODone + 1,
+    kBarUnitFull = kBarOFree + 1,          // + slot (2)
+    kBarUnitEmpty = kBarUnitFull + kUnitSlots,  // + slot (2)
+    kBarDrainIdx = kBarUnitEmpty + kUnitSlots,
+    kNumBarsUsed = kBarDrainIdx + 1,
 };
-static_assert(kNumBarsUsed <= Smem::kNumBars, "barrier slots");
+static_assert(kNumBarsUsed <= Smem<256>::kNumBars, "barrier slots");
+static_assert(k_stages(64) <= kMaxStages && v_stages(64) <= kMaxStages, "ring depth");
 
 // TMEM columns: S buffers at 64 b, O at 256.
 constexpr uint32_t kTmemS = 0;
@@ -156,11 +173,13 @@ __device__ __forceinline__ void record_timeout(const Params &p, volatile int *ab
     }
 }
 
-template <bool BF16>
+template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
-    fa_fwd256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, const Params p) {
-    using L = Smem;
+    fa_fwd1t_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const Params p) {
+    using L = Smem<D>;
+    constexpr int kKStages = k_stages(D);
+    constexpr int kVStages = v_stages(D);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -261,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = mbar_wait_bounded(bar(kBarQEmpty), (unit_iter & 1) ^ 1, abort_flag, budget);
                 if (!ok) break;
                 mbar_arrive_expect_tx(bar(kBarQFull), L::kQBytes);
-                for (int g = 0; g < 4; ++g)
+                for (int g = 0; g < L::kRegions; ++g)
                     tma_load_3d(sQ + g * L::kQRegion, &tmQ, bar(kBarQFull), 64 * g, U.r0, U.sp);
                 ++q_loads;
                 int u_next = -1;
@@ -273,14 +292,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!ok) break;
                         if (u_next >= 0) {
                             const Unit W = decode(u_next, p);
-                            for (int g = 0; g < 4; ++g) tma_prefetch_l2_3d(&tmQ, 64 * g, W.r0, W.sp);
+                            for (int g = 0; g < L::kRegions; ++g) tma_prefetch_l2_3d(&tmQ, 64 * g, W.r0, W.sp);
                         }
                     }
                     const int st = t % kKStages;
                     ok = mbar_wait_bounded(bar(kBarKEmpty + st), ((t / kKStages) & 1) ^ 1, abort_flag, budget);
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(kBarKFull + st), L::kKVBytes);
-                    for (int g = 0; g < 4; ++g)
+                    for (int g = 0; g < L::kRegions; ++g)
                         tma_load_3d(sK(t) + g * L::kKVRegion, &tmK, bar(kBarKFull + st), 64 * g,
                                     j * kBN, U.bkv);
                 }
@@ -309,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = mbar_wait_bounded(bar(kBarVEmpty + st), ((t / kVStages) & 1) ^ 1, abort_flag, budget);
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(kBarVFull + st), L::kKVBytes);
-                    for (int g = 0; g < 4; ++g)
+                    for (int g = 0; g < L::kRegions; ++g)
                         tma_load_3d(sV(t) + g * L::kKVRegion, &tmV, bar(kBarVFull + st), 64 * g,
                                     j * kBN, U.bkv);
                 }
@@ -573,5 +592,5 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-}  // namespace d256
+}  // namespace onetile
 }  // namespace fa
