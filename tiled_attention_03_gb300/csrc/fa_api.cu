@@ -308,9 +308,9 @@ bool use_onetile(int64_t H, int64_t H_kv, int64_t Nq, int64_t d) {
     return R <= fa::onetile::kBM;
 }
 
-// One 128-row Q tile per unit, 64-key K/V tiles. The key splits are those of the
+// One 128-row Q tile per unit, bn(d)-key K/V tiles. The key splits are those of the
 // two-tile path (split_tiles 128-key tiles each, so the workspace and the merge are
-// the same); the kernel counts them in 64-key tiles.
+// the same); the kernel counts them in its own tiles.
 fa_status run_forward_1t(const Call &c, DeviceState *ds, int dev, int64_t n_splits,
                          int64_t split_tiles) {
     if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
@@ -334,8 +334,8 @@ fa_status run_forward_1t(const Call &c, DeviceState *ds, int dev, int64_t n_spli
     const int64_t spaces = B * H / hps, R = hps * Nq;
     CUtensorMap mq, mk, mv;
     if (!make_map(&mq, c.Q, bf16, spaces, R, d, fa::onetile::kBM) ||
-        !make_map(&mk, c.K, bf16, B * H_kv, Nk, d, fa::onetile::kBN) ||
-        !make_map(&mv, c.V, bf16, B * H_kv, Nk, d, fa::onetile::kBN))
+        !make_map(&mk, c.K, bf16, B * H_kv, Nk, d, fa::onetile::bn(static_cast<int>(d))) ||
+        !make_map(&mv, c.V, bf16, B * H_kv, Nk, d, fa::onetile::bn(static_cast<int>(d))))
         return FA_ERR_CUDA;
     const bool split = n_splits > 1;
     const int64_t BH = B * H;
@@ -361,7 +361,7 @@ fa_status run_forward_1t(const Call &c, DeviceState *ds, int dev, int64_t n_spli
     p.n_units = static_cast<int>(n_units);
     p.n_qb = static_cast<int>(n_qb);
     p.n_splits = static_cast<int>(n_splits);
-    p.split_tiles = static_cast<int>(split_tiles * (fa::kBN / fa::onetile::kBN));
+    p.split_tiles = static_cast<int>(split_tiles * (fa::kBN / fa::onetile::bn(static_cast<int>(d))));
     const int64_t all = Nq + Nk;
     int64_t wl = all, wr = all;
     if (c.mask_mode == FA_MASK_CAUSAL) wr = 0;

@@ -12,12 +12,14 @@
 //     softmax between S(j) and S(j+1).
 // Layout:
 //   * a unit is one 128-row Q tile (128 x D, 16-bit);
-//   * K/V tiles hold 64 keys; the K and V rings are as deep as shared memory allows
-//     (3 and 2 at d = 256, 4 and 4 at d = 128, 6 and 6 at d = 64);
-//   * S is formed in one of three 64-column TMEM buffers, so that the softmax of
+//   * K/V tiles hold bn(D) keys (128 for d <= 128, 64 at d = 256, where three
+//     128-column S buffers and O would not fit the 512 TMEM columns); the K and V rings
+//     are as deep as shared memory allows (3 and 2 at d = 256, 3 and 3 at d = 128,
+//     6 and 6 at d = 64);
+//   * S is formed in one of three bn(D)-column TMEM buffers, so that the softmax of
 //     block j runs while S(j+1) and S(j+2) are computed; O (D columns) stays in
 //     TMEM for the unit. MMA order: ... O += P(j) V_j | S(j+3) | O += P(j+1) V_{j+1} ...
-//   * one softmax warpgroup (thread = query row = TMEM lane, 64 keys per block).
+//   * one softmax warpgroup (thread = query row = TMEM lane, bn(D) keys per block).
 // When the reference max of a row moves (rare), the softmax thread rescales its O
 // row, after waiting for the product O += P(j-1) V_{j-1} to complete (two
 // alternating barriers, one per parity of j, so that a skipped wait never
@@ -42,15 +44,17 @@ namespace fa {
 namespace onetile {
 
 constexpr int kBM = 128;        // query rows per unit
-constexpr int kBN = 64;         // keys per K/V tile
+// keys per K/V tile: 128 where three 128-column S buffers and O fit the 512 TMEM
+// columns (D <= 128), else 64
+__host__ __device__ constexpr int bn(int D) { return D == 256 ? 64 : 128; }
 constexpr int kThreads = 256;
 constexpr int kTmaWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kVWarp = 6;
 // K and V ring depths: what shared memory holds next to the Q tile (K/V tiles are
-// 64 x D, 16-bit)
-__host__ __device__ constexpr int k_stages(int D) { return D == 256 ? 3 : D == 128 ? 4 : 6; }
-__host__ __device__ constexpr int v_stages(int D) { return D == 256 ? 2 : D == 128 ? 4 : 6; }
+// bn(D) x D, 16-bit: 32 KB at d = 256 and 128, 16 KB at d = 64)
+__host__ __device__ constexpr int k_stages(int D) { return D == 64 ? 6 : 3; }
+__host__ __device__ constexpr int v_stages(int D) { return D == 64 ? 6 : D == 128 ? 3 : 2; }
 constexpr int kMaxStages = 6;
 constexpr int kSBufs = 3;
 constexpr uint32_t kTmemCols = 512;
@@ -71,7 +75,7 @@ struct Params {
     int hps, R;          // query heads per row space (1, or kv_group when packed); rows hps*Nq
     int n_units, n_qb;   // (row space, 128-row block, key split) units; blocks per space
     int n_splits;        // key splits per block (1: none)
-    int split_tiles;     // 64-key K/V tiles per split
+    int split_tiles;     // bn(D)-key K/V tiles per split
     int heavy_first;
     int wl, wr;          // key j visible to query i iff i + q_off - wl <= j <= i + q_off + wr
     float scale_log2;
@@ -86,7 +90,7 @@ struct Smem {
     static_assert(D == 64 || D == 128 || D == 256, "head dimension");
     static constexpr int kRegions = D / 64;
     static constexpr int kQRegion = kBM * 128;   // 128 rows x 128 B (64 columns)
-    static constexpr int kKVRegion = kBN * 128;  // 64 rows x 128 B
+    static constexpr int kKVRegion = bn(D) * 128;  // bn(D) rows x 128 B
     static constexpr int kQBytes = kRegions * kQRegion;
     static constexpr int kKVBytes = kRegions * kKVRegion;
     static constexpr int kQ = 0;
@@ -123,9 +127,9 @@ enum : int {
 static_assert(kNumBarsUsed <= Smem<256>::kNumBars, "barrier slots");
 static_assert(k_stages(64) <= kMaxStages && v_stages(64) <= kMaxStages, "ring depth");
 
-// TMEM columns: S buffers at 64 b, O at 256.
+// TMEM columns: S buffers at bn(D) b, O after them (256 at d = 256, 384 below).
 constexpr uint32_t kTmemS = 0;
-constexpr uint32_t kTmemO = 256;
+__host__ __device__ constexpr uint32_t tmem_o(int D) { return D == 256 ? 256u : 384u; }
 
 // A row space holds the queries of hps consecutive query heads (b*H + h order), row
 // r being query r % Nq of head sp*hps + r / Nq: one head each, or, with few queries,
@@ -139,6 +143,7 @@ struct Unit {
     int sp, bkv, r0, rl, qmin, qmax, j0, j1, split;
 };
 
+template <int kBN>
 __device__ __forceinline__ Unit decode(int u, const Params &p) {
     Unit U;
     const int per_sp = p.n_qb * p.n_splits;
@@ -178,6 +183,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd1t_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const Params p) {
     using L = Smem<D>;
+    constexpr int kBN = bn(D);
+    constexpr uint32_t kTmemO = tmem_o(D);
+    static_assert(kSBufs * kBN <= static_cast<int>(kTmemO) && kTmemO + D <= kTmemCols, "TMEM columns");
     constexpr int kKStages = k_stages(D);
     constexpr int kVStages = v_stages(D);
     extern __shared__ uint8_t smem_raw[];
@@ -264,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 while (true) {
                     const unsigned next = atomicAdd(p.sched, 1u);
                     if (next >= static_cast<unsigned>(p.n_units)) break;
-                    const Unit W = decode(static_cast<int>(next), p);
+                    const Unit W = decode<kBN>(static_cast<int>(next), p);
                     if (W.j0 <= W.j1) {
                         v = static_cast<int>(next);
                         break;
@@ -276,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             int u = publish(0);
             for (; ok && u >= 0; ++unit_iter) {
-                const Unit U = decode(u, p);
+                const Unit U = decode<kBN>(u, p);
                 ok = mbar_wait_bounded(bar(kBarQEmpty), (unit_iter & 1) ^ 1, abort_flag, budget);
                 if (!ok) break;
                 mbar_arrive_expect_tx(bar(kBarQFull), L::kQBytes);
@@ -291,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         u_next = publish(unit_iter + 1);
                         if (!ok) break;
                         if (u_next >= 0) {
-                            const Unit W = decode(u_next, p);
+                            const Unit W = decode<kBN>(u_next, p);
                             for (int g = 0; g < L::kRegions; ++g) tma_prefetch_l2_3d(&tmQ, 64 * g, W.r0, W.sp);
                         }
                     }
@@ -321,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int unit_iter = 0; ok; ++unit_iter) {
             const int u = take_unit(unit_iter, ok);
             if (!ok || u < 0) break;
-            const Unit U = decode(u, p);
+            const Unit U = decode<kBN>(u, p);
             if (lane == 0) {
                 for (int j = U.j0; ok && j <= U.j1; ++j, ++t) {
                     const int st = t % kVStages;
@@ -371,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
         };
-        // O (+)= P(t) V_t, P read from the first 32 columns of S buffer t mod 3.
+        // O (+)= P(t) V_t, P read from the first kBN / 2 columns of S buffer t mod 3.
         auto issue_pv = [&](int t, bool first) {
             tc_fence_after();
             const uint64_t dv = sw128_desc(sV(t), L::kKVRegion, 1024);
@@ -391,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (; ok; ++unit_iter) {
             u = take_unit(unit_iter, ok);
             if (!ok || u < 0) break;
-            const Unit U = decode(u, p);
+            const Unit U = decode<kBN>(u, p);
             const int n = U.j1 - U.j0 + 1;
             ok = wait(kBarQFull, unit_iter & 1);
             // S for the first min(3, n) blocks
@@ -436,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (; ok; ++unit_iter) {
             u = take_unit(unit_iter, ok);
             if (!ok || u < 0) break;
-            const Unit U = decode(u, p);
+            const Unit U = decode<kBN>(u, p);
             const int r = U.r0 + row;  // row of the space
             const int i = r % p.Nq;    // its query index; key position i + q_off
             const int lo_i = max(0, i + p.q_off - p.wl);
@@ -452,16 +460,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 tc_fence_after();
                 float x[kBN];
-                {
+#pragma unroll
+                for (int h = 0; h < kBN; h += 64) {
                     uint32_t a[32], b[32];
-                    tmem_ld32(tS, a);
-                    tmem_ld32(tS + 32, b);
+                    tmem_ld32(tS + h, a);
+                    tmem_ld32(tS + h + 32, b);
                     tmem_ld_wait(a);
                     tmem_ld_wait(b);
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
-                        x[c] = __uint_as_float(a[c]);
-                        x[c + 32] = __uint_as_float(b[c]);
+                        x[h + c] = __uint_as_float(a[c]);
+                        x[h + c + 32] = __uint_as_float(b[c]);
                     }
                 }
                 const int kv0 = j * kBN;
@@ -493,11 +502,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fadd2(s0, s1, x[c], x[c + 1]);
                     fadd2(s2, s3, x[c + 2], x[c + 3]);
                 }
-                uint32_t pk[32];
+                // P(j) as 16-bit pairs over the first kBN / 2 columns of the buffer
 #pragma unroll
-                for (int e = 0; e < 32; ++e) pk[e] = pack2<BF16>(x[2 * e], x[2 * e + 1]);
-                tmem_st16(tS, pk);
-                tmem_st16(tS + 16, pk + 16);
+                for (int h = 0; h < kBN; h += 64) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) pk[e] = pack2<BF16>(x[h + 2 * e], x[h + 2 * e + 1]);
+                    tmem_st16(tS + h / 2, pk);
+                    tmem_st16(tS + h / 2 + 16, pk + 16);
+                }
                 l = l * corr + ((s0 + s1) + (s2 + s3));
                 // The reference max moved: O holds the sum through block j-1 once that
                 // product completes; rescale this row's O before P(j) is released.
