@@ -101,6 +101,9 @@ EXTRA_WORKLOADS = [
              0, 0, seed=7, H_kv=8, Nq=1, splits=0),
     Workload("chunk_b1h32kv8_nq512_nk16384_d128", 1, 32, 16384, 128, torch.bfloat16, MASK_CAUSAL,
              0, 0, seed=8, H_kv=8, Nq=512, splits=0),
+    # the d = 64 decode step (one-tile kernel with 128-key tiles at d = 64)
+    Workload("decode_b8h32kv8_nq1_nk32768_d64", 8, 32, 32768, 64, torch.bfloat16, MASK_CAUSAL,
+             0, 0, seed=22, H_kv=8, Nq=1, splits=0),
     # head dimension 32 (64-byte swizzled tiles) and 64 on the bench shape
     Workload("full_b4h32n4096d32", 4, 32, 4096, 32, torch.bfloat16, MASK_NONE, 0, 0, seed=13),
     Workload("full_b4h32n4096d64", 4, 32, 4096, 64, torch.bfloat16, MASK_NONE, 0, 0, seed=18),
