@@ -75,3 +75,33 @@ def test_reference_arm_other_ranks_exit_quietly():
     r = _run_ref(1, 2)
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
+
+
+def test_kernel_family_follows_the_forward_dispatch():
+    """bench.py keys measured traffic to the kernel family that runs a workload; its
+    rule restates the library's (fa_api.cu use_onetile): the one-tile kernel for
+    d = 256, and for d = 64 / 128 when a row space holds at most 128 rows, a row space
+    being one head's queries or, with at most 64 queries and grouped heads, those of
+    all query heads of one K/V head."""
+    sys.path.insert(0, ROOT)
+    import dataclasses
+    import bench
+    from tiled_attention_03_gb300.workloads import BY_NAME
+    fam = lambda name: bench.kernel_family(BY_NAME[name])
+    assert fam("full_b4h32n4096d128") == "fwd"
+    assert fam("full_b4h32n4096d32") == "fwd"
+    assert fam("full_b4h32n4096d64") == "fwd"
+    assert fam("chunk_b1h32kv8_nq512_nk16384_d128") == "fwd"
+    assert fam("varlen_causal_b16h32n4096d128") == "fwd"
+    for name in ("decode_b8h32kv8_nq1_nk32768_d128", "decode_b8h32kv8_nq1_nk32768_d64",
+                 "decode_b8h16kv4_nq1_nk32768_d256", "chunk_b1h16kv4_nq512_nk16384_d256",
+                 "full_b4h16n4096d256", "causal_b4h16n4096d256"):
+        assert fam(name) == "fwd1t", name
+    assert fam("bwd_b4h32n4096d128") == "bwd"
+    base = BY_NAME["full_b4h32n4096d128"]
+    cut = lambda **kw: bench.kernel_family(dataclasses.replace(base, **kw))
+    assert cut(H=4, N=128) == "fwd1t" and cut(H=4, N=129) == "fwd"
+    assert cut(H=16, H_kv=2, Nq=16) == "fwd1t"    # 8 heads x 16 queries = 128 rows
+    assert cut(H=16, H_kv=2, Nq=17) == "fwd"      # 136 rows
+    assert cut(H=4, H_kv=2, Nq=100) == "fwd1t"    # not packed (Nq > 64): 100 rows
+    assert cut(H=4, N=100, d=32) == "fwd"         # d = 32 has no one-tile form
