@@ -362,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (elect_one()) umma_commit(bar(b));
             __syncwarp();
         };
-        // S(t) = Q K_t^T into S buffer t mod 3 (64 columns).
+        // S(t) = Q K_t^T into S buffer t mod 3 (kBN columns).
         auto issue_s = [&](int t) {
             tc_fence_after();
             const uint64_t dq = sw128_desc(sQ, 16, 1024);
