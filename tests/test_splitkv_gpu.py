@@ -59,16 +59,33 @@ def test_splitkv_parity_d256(splits, mask, window, Nq, Nk, dtype):
     compare(o, lse, q, k, v, 0.0625, mask, window)
 
 
+# Row spaces of at most 128 rows run on the one-tile kernel at d = 64 and 128 too
+# (128-key K/V tiles there): queries fewer or more than the keys, a single key, a
+# full 128-row tile, every split count.
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("Nq,Nk,mask", [(100, 50, "none"), (128, 1, "none"), (1, 1, "causal"),
+                                        (64, 200, "causal"), (128, 129, "causal"),
+                                        (77, 1000, "window"), (120, 4000, "none")])
+@pytest.mark.parametrize("splits", [1, 2, 7])
+def test_one_tile_rows(splits, mask, Nq, Nk, d):
+    q, _, _ = make_qkv(2, 3, Nq, d, torch.float16, seed=Nq + 5 * splits)
+    _, k, v = make_qkv(2, 3, Nk, d, torch.float16, seed=Nk + 11 * splits)
+    window = (300, 40) if mask == "window" else (0, 0)
+    o, lse = run_split(q, k, v, d ** -0.5, mask, window, splits)
+    compare(o, lse, q, k, v, d ** -0.5, mask, window)
+
+
 # Few queries per head with grouped K/V heads: the query heads of a K/V head share
-# one row space, so 128-row tiles hold several heads and cut through heads (both
-# the d = 128 kernel and the d = 256 kernel).
+# one row space, so 128-row tiles hold several heads and cut through heads (row
+# spaces of at most 128 rows on the one-tile kernel, longer ones on the two-tile
+# kernel at d = 64 and 128).
 @pytest.mark.parametrize("B,H,Hk,Nq,Nk", [
     (2, 16, 2, 1, 3000), (1, 16, 2, 33, 1500), (1, 8, 1, 64, 700), (3, 12, 4, 7, 129),
     (1, 32, 8, 5, 40), (2, 6, 3, 64, 64), (1, 4, 2, 65, 900)])
 @pytest.mark.parametrize("mask,window", [("none", (0, 0)), ("causal", (0, 0)),
                                          ("window", (200, 0)), ("window", (30, 20))])
 @pytest.mark.parametrize("splits", [1, 4])
-@pytest.mark.parametrize("d", [128, 256])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_packed_query_heads(d, splits, mask, window, B, H, Hk, Nq, Nk):
     dtype = torch.bfloat16
     q, _, _ = make_qkv(B, H, Nq, d, dtype, seed=Nq * 7 + splits)
