@@ -168,6 +168,11 @@ def test_host_pipeline_workspace_size(lib):
     # Nq < Nk adds the split scratch of the largest chunk
     assert (lib.fa_forward_host_workspace_bytes(1, 2, 2, 4, 4096, 64, 0, 0) >
             lib.fa_forward_host_workspace_bytes(1, 2, 2, 4, 4, 64, 0, 0))
+    # d = 256 takes the split form too (Nq < Nk, or splits requested)
+    assert (lib.fa_forward_host_workspace_bytes(1, 2, 2, 64, 128, 256, 0, 0) >
+            lib.fa_forward_host_workspace_bytes(1, 2, 2, 64, 64, 256, 0, 0) > 0)
+    assert (lib.fa_forward_host_workspace_bytes(1, 2, 2, 1024, 1024, 256, 2, 0) >
+            lib.fa_forward_host_workspace_bytes(1, 2, 2, 1024, 1024, 256, 0, 0) > 0)
     for bad in [(0, 2, 2, 128, 128, 64, 0, 0), (1, 3, 2, 128, 128, 64, 0, 0),
                 (1, 2, 2, 128, 128, 96, 0, 0), (1, 2, 2, 128, 128, 64, -1, 0)]:
         assert lib.fa_forward_host_workspace_bytes(*bad) == 0
