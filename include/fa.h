@@ -72,9 +72,11 @@ typedef enum { FA_DTYPE_FP16 = 0, FA_DTYPE_BF16 = 1 } fa_dtype;
  * stream  : a cudaStream_t (NULL = the legacy default stream).
  *
  * Ownership: every pointer is owned by the caller; the library keeps none and
- * allocates no device memory per call. Q, K, V and O must be 16-byte aligned
- * (they are read and written by tensor-memory-access copies); LSE, accessed one
- * float at a time, 4-byte aligned. All on the current device.
+ * allocates no device memory per call. Q, K and V must be 16-byte aligned
+ * (they are read by tensor-memory-access copies), O 32-byte aligned (each row is
+ * written with 32-byte vector stores); LSE, accessed one float at a time, 4-byte
+ * aligned. All on the current device; a pointer that breaks one of these rules is
+ * FA_ERR_INVALID_ARG.
  *
  * Errors: arguments are checked before anything is enqueued; an invalid call
  * returns FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED and launches nothing. A
@@ -116,7 +118,7 @@ fa_status fa_forward_gqa(const void *Q, const void *K, const void *V, void *O, f
  * number; fa_splitkv_default_splits suggests one). The result equals
  * fa_forward_gqa's up to rounding.
  *
- * workspace: device memory owned by the caller, 16-byte aligned, at least
+ * workspace: device memory owned by the caller, 32-byte aligned, at least
  * fa_splitkv_workspace_bytes(B, H, Nq, d, num_splits) bytes, not overlapping
  * the other buffers; its contents are scratch (fp32 partial results) and are
  * overwritten. With num_splits = 1 it is not used (it may then be NULL).
@@ -152,9 +154,11 @@ int64_t fa_splitkv_default_splits(int64_t B, int64_t H, int64_t H_kv, int64_t Nq
  * The scratch is one fixed array of FA_SPLITKV_STATIC_SCRATCH_BYTES bytes in
  * device memory, part of the library: every GPU that loads the library holds
  * it until the process exits, and this call allocates nothing. Requests whose
- * fa_splitkv_workspace_bytes(B, H, Nq, d, num_splits) exceeds that size are
- * rejected with FA_ERR_UNSUPPORTED before anything is enqueued (use fewer
- * splits, or fa_forward_splitkv with a workspace). num_splits >= 1.
+ * fa_splitkv_workspace_bytes(B, H, Nq, d, n) exceeds that size are rejected
+ * with FA_ERR_UNSUPPORTED before anything is enqueued (use fewer splits, or
+ * fa_forward_splitkv with a workspace); n is the split count the call runs,
+ * num_splits clamped to the number of 128-key tiles (and lowered further when
+ * rounding the tiles per split up leaves a split empty). num_splits >= 1.
  *
  * All calls on a device share the one array and leave their partial results
  * in it; nothing in it needs to start at zero. Calls whose kernels overlap on
@@ -184,7 +188,7 @@ fa_status fa_forward_splitkv_static(const void *Q, const void *K, const void *V,
  * Layout (token-major): Q and O total_q x H x d, K and V total_k x H_kv x d, in
  * `dtype`; LSE total_q x H float32; cu_seqlens_q and cu_seqlens_k are B + 1
  * int32 on the device, non-decreasing from 0 to total_q / total_k. All on the
- * current device; Q, K, V, O 16-byte aligned, LSE 4-byte. max_seqlen_q >= every L_q (rows
+ * current device; Q, K, V 16-byte aligned, O 32-byte, LSE 4-byte. max_seqlen_q >= every L_q (rows
  * past it are not computed). With a mask, every sequence needs L_q <= L_k;
  * every sequence with queries needs L_k >= 1. The device arrays are read by
  * the kernel, not checked on the host; offsets are clamped to the tensors, so
@@ -213,7 +217,7 @@ fa_status fa_forward_varlen(const void *Q, const void *K, const void *V, void *O
  * Q, K, V, O, LSE: host memory (page-locked memory makes the copies
  * asynchronous; pageable memory works, with the host waiting on each copy), in
  * the layout of fa_forward_splitkv; O and LSE overlap no input. `workspace`:
- * device memory owned by the caller, 16-byte aligned, at least
+ * device memory owned by the caller, 32-byte aligned, at least
  * fa_forward_host_workspace_bytes(...) bytes with the same sizes, num_splits and
  * chunk_bytes; it holds the device copies. num_splits: 0 runs Nq == Nk
  * unsplit and Nq < Nk with fa_splitkv_default_splits per chunk; n >= 1 runs
@@ -254,11 +258,12 @@ fa_status fa_forward_host(const void *Q, const void *K, const void *V, void *O, 
  *
  * Layout: Q, O, dO and dQ are contiguous B x H x N x d; K, V, dK and dV are
  * B x H_kv x N x d (H_kv divides H); LSE is B x H x N float32; all in `dtype`
- * except LSE, on the current device, 16-byte aligned (LSE: 4-byte). Queries and keys share
+ * except LSE, on the current device; Q, K, V, O and dO 16-byte aligned, dQ, dK and
+ * dV 32-byte aligned (32-byte vector stores), LSE 4-byte. Queries and keys share
  * positions (as in fa_forward); the mask arguments are those of fa_forward.
  * `workspace` is caller-owned device memory of at least
  * fa_backward_workspace_bytes(B, H, N, d) bytes (two fp32 row terms per query
- * row), 16-byte aligned; its contents on entry do not matter. dQ, dK, dV and
+ * row), 32-byte aligned; its contents on entry do not matter. dQ, dK, dV and
  * the workspace overlap no input and no other output. The results are
  * deterministic: no atomics, fixed summation order.
  *
@@ -283,8 +288,8 @@ size_t fa_backward_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d);
  * outputs; dO and dQ are total_q x H x d, dK and dV total_k x H_kv x d.
  * max_seqlen_q / max_seqlen_k bound every sequence's lengths. Gradients of
  * keys that no query sees, and of queries that see no key, are zero.
- * `workspace`: fa_backward_varlen_workspace_bytes(B, H, total_q) bytes, 16-byte
- * aligned. d is 32, 64 or 128. Deterministic. Errors as fa_backward; the device
+ * `workspace`: fa_backward_varlen_workspace_bytes(B, H, total_q) bytes, 32-byte
+ * aligned; pointer alignment as in fa_backward. d is 32, 64 or 128. Deterministic. Errors as fa_backward; the device
  * arrays are clamped to the tensors, as in fa_forward_varlen.
  */
 fa_status fa_backward_varlen(const void *Q, const void *K, const void *V, const void *O,

@@ -49,6 +49,7 @@ def call(lib, q=A, k=B_, v=C, o=O_, lse=L_, B=1, H=1, N=16, d=64, scale=0.125, m
     dict(mask=2, wl=-1), dict(mask=2, wr=-1),
     dict(scale=0.0), dict(scale=-0.5), dict(scale=float("inf")), dict(scale=float("nan")),
     dict(q=A + 8), dict(o=O_ + 2), dict(lse=L_ + 2),
+    dict(o=O_ + 16),        # O takes 32-byte stores: 16-byte alignment is not enough
     dict(o=A),              # O aliases Q
     dict(lse=O_ + 64),      # LSE inside O
 ])
@@ -112,6 +113,7 @@ def test_backward_workspace_size(lib):
     dict(B=0), dict(N=0), dict(Hk=0), dict(Hk=3), dict(dtype=5), dict(mask=7),
     dict(mask=2, wl=-1), dict(scale=0.0), dict(scale=float("nan")),
     dict(q=0x100008), dict(dk=0x800004), dict(ws=0xA00002),
+    dict(dq=0x700010), dict(dk=0x800010), dict(dv=0x900010), dict(ws=0xA00010),  # 32-byte stores
     dict(dq=0x100000),            # dQ aliases Q
     dict(dk=0x700000),            # dK overlaps dQ
     dict(ws=0x500000),            # workspace overlaps dO
@@ -138,6 +140,7 @@ def varlen_call(lib, B=2, H=2, Hk=2, tq=100, tk=100, maxq=60, d=64, scale=0.125,
 @pytest.mark.parametrize("kw", [
     dict(q=0), dict(cq=0), dict(ck=0), dict(B=0), dict(Hk=3), dict(tk=0), dict(tq=-1),
     dict(dtype=4), dict(mask=2, wr=-1), dict(scale=-1.0), dict(q=0x100004), dict(cq=0x700002),
+    dict(o=0x400010),            # O 16- but not 32-byte aligned
     dict(o=0x100000),            # O aliases Q
     dict(lse=0x400010),          # LSE inside O
 ])
@@ -182,6 +185,7 @@ def test_host_pipeline_workspace_size(lib):
     dict(q=0), dict(o=0), dict(lse=0), dict(ws=0), dict(B=0), dict(Hk=3), dict(Nq=0),
     dict(dtype=2), dict(mask=3), dict(mask=2, wl=-1), dict(scale=0.0), dict(splits=-1),
     dict(mask=1, Nq=200), dict(lse=0x600002),
+    dict(ws=0x700010),           # workspace 16- but not 32-byte aligned
 ])
 def test_host_pipeline_invalid_arguments(lib, kw):
     assert host_call(lib, **kw) == fa.FA_ERR_INVALID_ARG
@@ -190,3 +194,12 @@ def test_host_pipeline_invalid_arguments(lib, kw):
 @pytest.mark.parametrize("kw", [dict(d=96), dict(d=16), dict(d=512)])
 def test_host_pipeline_unsupported(lib, kw):
     assert host_call(lib, **kw) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_splitkv_workspace_must_be_32_byte_aligned(lib):
+    # the split scratch takes 32-byte stores: a workspace only 16-byte aligned is refused
+    # before anything else is looked at
+    args = [0x100000, 0x200000, 0x300000, 0x400000, 0x600000, 1, 2, 2, 4, 4096, 64, 0.125, 0, 0,
+            0, 0, 4]
+    assert lib.fa_forward_splitkv(*args, 0x700010, 1 << 24, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_forward_splitkv(*args, 0x700008, 1 << 24, None) == fa.FA_ERR_INVALID_ARG

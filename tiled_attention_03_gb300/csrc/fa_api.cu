@@ -144,6 +144,9 @@ DeviceState *device_state(int dev) {
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// Buffers the kernels write with 32-byte vector stores (O, the split scratch, and
+// the gradients): a row starts on a 32-byte boundary only if the base does.
+bool aligned32(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 // LSE is read and written one float at a time: float alignment is enough.
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
@@ -376,6 +379,7 @@ fa_status run_forward_1t(const Call &c, DeviceState *ds, int dev, int64_t n_spli
     p.wait_budget_ns = wait_budget();
     p.status = ds->status;
     p.sched = ds->sched + 2 * (g_sched_next.fetch_add(1) % kSchedSlots);
+    p.fault_skip_k = g_fault_pos.exchange(-1);
     const unsigned blocks = static_cast<unsigned>(n_units < ds->sm_count ? n_units : ds->sm_count);
     cudaStream_t st = static_cast<cudaStream_t>(c.stream);
     cudaError_t le;
@@ -436,7 +440,7 @@ fa_status run_forward(const Call &c) {
     // would leave rows with no visible key.
     if (mask_mode != FA_MASK_NONE && Nq > Nk) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(c.scale) || !(c.scale > 0.f)) return FA_ERR_INVALID_ARG;
-    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned4(LSE))
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned32(O) || !aligned4(LSE))
         return FA_ERR_INVALID_ARG;
     if (c.num_splits < 1) return FA_ERR_INVALID_ARG;
     if (d != 32 && d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
@@ -604,7 +608,7 @@ fa_status run_forward_varlen(const VarlenCall &c) {
     if (c.mask_mode == FA_MASK_WINDOW && (c.window_left < 0 || c.window_right < 0))
         return FA_ERR_INVALID_ARG;
     if (!std::isfinite(c.scale) || !(c.scale > 0.f)) return FA_ERR_INVALID_ARG;
-    if (!aligned16(c.Q) || !aligned16(c.K) || !aligned16(c.V) || !aligned16(c.O) ||
+    if (!aligned16(c.Q) || !aligned16(c.K) || !aligned16(c.V) || !aligned32(c.O) ||
         !aligned4(c.LSE) || (reinterpret_cast<uintptr_t>(c.cu_q) & 3u) ||
         (reinterpret_cast<uintptr_t>(c.cu_k) & 3u))
         return FA_ERR_INVALID_ARG;
@@ -720,6 +724,7 @@ DeviceInfo device_info(int dev) {
     return info;
 }
 bool aligned16(const void *p) { return ::aligned16(p); }
+bool aligned32(const void *p) { return ::aligned32(p); }
 bool aligned4(const void *p) { return ::aligned4(p); }
 bool overlaps(const void *a, size_t na, const void *b, size_t nb) { return ::overlaps(a, na, b, nb); }
 bool on_device(const void *p, int dev) { return ::on_device(p, dev); }
@@ -796,7 +801,7 @@ fa_status fa_forward_splitkv(const void *Q, const void *K, const void *V, void *
                              int64_t window_left, int64_t window_right, fa_dtype dtype,
                              int64_t num_splits, void *workspace, size_t workspace_bytes,
                              void *stream) {
-    if (workspace != nullptr && !aligned16(workspace)) return FA_ERR_INVALID_ARG;
+    if (workspace != nullptr && !aligned32(workspace)) return FA_ERR_INVALID_ARG;
     Call c{Q, K, V, O, LSE, B, H, H_kv, Nq, Nk, d, scale, mask_mode, window_left, window_right,
            dtype, num_splits, workspace, workspace_bytes, stream};
     return run_forward(c);
@@ -822,9 +827,16 @@ fa_status fa_forward_splitkv_static(const void *Q, const void *K, const void *V,
     });
     if (sc.err != cudaSuccess || sc.ptr == nullptr) return FA_ERR_CUDA;
     if (num_splits < 1) return FA_ERR_INVALID_ARG;
-    if (B >= 1 && H >= 1 && Nq >= 1 && d >= 1 &&
-        fa_splitkv_workspace_bytes(B, H, Nq, d, num_splits) > kStaticScratchBytes)
-        return FA_ERR_UNSUPPORTED;  // the request needs more than the fixed scratch
+    if (B >= 1 && H >= 1 && Nq >= 1 && Nk >= 1 && d >= 1 && Nk <= (int64_t{1} << 29)) {
+        // The split count the launch will use: at most one split per 128-key tile,
+        // and no split left empty by rounding the tiles per split up.
+        const int64_t kv_tiles = (Nk + fa::kBN - 1) / fa::kBN;
+        const int64_t splits = num_splits < kv_tiles ? num_splits : kv_tiles;
+        const int64_t split_tiles = (kv_tiles + splits - 1) / splits;
+        const int64_t n_splits = (kv_tiles + split_tiles - 1) / split_tiles;
+        if (fa_splitkv_workspace_bytes(B, H, Nq, d, n_splits) > kStaticScratchBytes)
+            return FA_ERR_UNSUPPORTED;  // the request needs more than the fixed scratch
+    }
     Call c{Q, K, V, O, LSE, B, H, H_kv, Nq, Nk, d, scale, mask_mode, window_left, window_right,
            dtype, num_splits, sc.ptr, kStaticScratchBytes, stream};
     return run_forward(c);

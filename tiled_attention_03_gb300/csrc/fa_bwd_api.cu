@@ -154,9 +154,13 @@ fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O
     if (mask_mode == FA_MASK_WINDOW && (window_left < 0 || window_right < 0))
         return FA_ERR_INVALID_ARG;
     if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
-    const void *ptrs[] = {Q, K, V, O, dO, dQ, dK, dV, workspace};
+    const void *ptrs[] = {Q, K, V, O, dO};
     for (const void *q : ptrs)
         if (!aligned16(q)) return FA_ERR_INVALID_ARG;
+    // the gradients and the workspace take 32-byte vector stores
+    const void *stored[] = {dQ, dK, dV, workspace};
+    for (const void *q : stored)
+        if (!fa_host::aligned32(q)) return FA_ERR_INVALID_ARG;
     if (!fa_host::aligned4(LSE)) return FA_ERR_INVALID_ARG;
     if (d != 32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
     if (N > (int64_t{1} << 29) || B * H > (int64_t{1} << 31)) return FA_ERR_UNSUPPORTED;
@@ -312,9 +316,13 @@ fa_status fa_backward_varlen(const void *Q, const void *K, const void *V, const 
         max_seqlen_k > total_k || B > (int64_t{1} << 20))
         return FA_ERR_UNSUPPORTED;
     if (total_q == 0 && total_k == 0) return FA_OK;  // nothing to read or write
-    const void *ptrs[] = {Q, K, V, O, dO, dQ, dK, dV, workspace};
+    const void *ptrs[] = {Q, K, V, O, dO};
     for (const void *q : ptrs)
         if (q == nullptr || !aligned16(q)) return FA_ERR_INVALID_ARG;
+    // the gradients and the workspace take 32-byte vector stores
+    const void *stored[] = {dQ, dK, dV, workspace};
+    for (const void *q : stored)
+        if (q == nullptr || !fa_host::aligned32(q)) return FA_ERR_INVALID_ARG;
     if (LSE == nullptr || !fa_host::aligned4(LSE)) return FA_ERR_INVALID_ARG;
     if (!cu_seqlens_q || !cu_seqlens_k || (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) ||
         (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u))

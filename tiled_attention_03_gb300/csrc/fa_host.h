@@ -22,6 +22,7 @@ struct DeviceInfo {
 // nullptr-free: err is cudaErrorInvalidDevice for an out-of-range ordinal.
 DeviceInfo device_info(int dev);
 bool aligned16(const void *p);
+bool aligned32(const void *p);
 bool aligned4(const void *p);
 bool overlaps(const void *a, size_t na, const void *b, size_t nb);
 bool on_device(const void *p, int dev);

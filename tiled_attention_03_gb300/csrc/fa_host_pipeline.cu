@@ -162,7 +162,7 @@ fa_status fa_forward_host(const void *Q, const void *K, const void *V, void *O, 
     if (fa_host::overlaps(O, pl.q_bytes, LSE, pl.lse_bytes)) return FA_ERR_INVALID_ARG;
     int dev = 0;
     if (!ok(cudaGetDevice(&dev))) return FA_ERR_CUDA;
-    if (!fa_host::aligned16(workspace) || !fa_host::on_device(workspace, dev) ||
+    if (!fa_host::aligned32(workspace) || !fa_host::on_device(workspace, dev) ||
         workspace_bytes < pl.total)
         return FA_ERR_INVALID_ARG;
     Pipe *pp = pipe_for(dev);
