@@ -87,3 +87,34 @@ def test_backward_wait_timeout_is_reported_and_gpu_recovers(varlen):
     assert fa.fa_sync_status() == fa.FA_OK
     dq, dk, dv = run_bwd(q, k, v, do, 0.125, "causal")
     bwd_compare(q, k, v, do, 0.125, "causal", (0, 0), dq, dk, dv)
+
+
+@pytest.mark.parametrize("d,n", [(256, 600), (128, 100)])
+def test_onetile_timeout_consumes_the_hook(d, n):
+    """The one-tile kernel (every d = 256 forward; a d = 128 head of at most 128
+    queries) takes the hook too: its launch times out and reports it, and the hook
+    is spent, so the next launch of the two-tile kernel is correct."""
+    q, k, v = make_qkv(1, 2, n, d, torch.bfloat16, seed=5)
+    dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
+    o = torch.empty_like(dq)
+    lse = torch.empty(dq.shape[:-1], device="cuda")
+    assert fa.fa_sync_status() == fa.FA_OK
+    fa.fa_set_wait_budget_ns(50_000_000)
+    try:
+        fa.fa_test_arm_fault(0)
+        t0 = time.time()
+        fa.fa_forward(dq, dk, dv, o, lse, d ** -0.5, "none")
+        st = fa.fa_sync_status()
+        elapsed = time.time() - t0
+        # the hook was consumed by that launch: this one (two-tile kernel) runs clean
+        q2, k2, v2 = make_qkv(1, 2, 600, 64, torch.float16, seed=6)
+        o2, lse2 = run_cuda(q2, k2, v2, 0.125, "causal")
+        st2 = fa.fa_sync_status()
+    finally:
+        fa.fa_set_wait_budget_ns(0)
+    assert st == fa.FA_ERR_TIMEOUT, fa.fa_status_string(st)
+    assert elapsed < 5.0
+    assert st2 == fa.FA_OK, fa.fa_status_string(st2)
+    compare(o2, lse2, q2, k2, v2, 0.125, "causal")
+    o3, lse3 = run_cuda(q, k, v, d ** -0.5, "none")
+    compare(o3, lse3, q, k, v, d ** -0.5, "none")

@@ -2,9 +2,11 @@
 device memory (runtimes that reserve all their memory up front, hosts that give the
 library no allocator). Its scratch is a fixed array inside the library.
 
-Called through the C ABI and compared with fa_forward_splitkv (caller workspace) on
-two calls in a row: the second call, on other inputs and a smaller shape, runs on the
-scratch the first one left behind. This file is collected last."""
+Called through the C ABI on two calls in a row (the second call, on other inputs and
+a smaller shape, runs on the scratch the first one left behind). Both calls run the
+same kernels with the same split count as fa_forward_splitkv with a caller workspace,
+so their results must be bit-identical to it; they are also compared element by
+element with the oracle. This file is collected last."""
 
 import ctypes
 
@@ -15,7 +17,7 @@ import tiled_attention_03_gb300 as fa
 from tiled_attention_03_gb300.binding import FA_DTYPE_BF16, FA_DTYPE_FP16, load_library
 from tiled_attention_03_gb300.workloads import make_qkv
 
-from parity_util import TOL_LSE, TOL_O
+from parity_util import compare
 
 pytestmark = pytest.mark.gpu
 
@@ -65,9 +67,31 @@ def test_static_scratch_matches_workspace_entry_on_two_calls():
         rc = _static(lib, q, k, v, o, lse, scale, mask, window, splits)
         assert rc == fa.FA_OK, fa.fa_status_string(rc)
         assert fa.fa_sync_status() == fa.FA_OK
-        assert float((o.float() - o_ref.float()).abs().max()) <= TOL_O[dtype]
-        assert float((lse - l_ref).abs().max()) <= TOL_LSE
-        assert bool(torch.isfinite(o).all()) and bool(torch.isfinite(lse).all())
+        # same kernels, same splits: bit for bit the workspace entry's result
+        assert torch.equal(o, o_ref)
+        assert torch.equal(lse, l_ref)
+        compare(o, lse, q.cpu(), k.cpu(), v.cpu(), scale, mask, window)
+
+
+def test_static_scratch_checks_the_split_count_it_runs():
+    """The size rule counts the splits the call runs: a split count far above the
+    number of 128-key tiles is clamped to it, and is accepted when the clamped
+    count fits the scratch."""
+    lib = _lib()
+    B, H, Nq, Nk, d, splits = 1, 8, 256, 256, 128, 1000
+    assert fa.fa_splitkv_workspace_bytes(B, H, Nq, d, splits) > fa.FA_SPLITKV_STATIC_SCRATCH_BYTES
+    assert fa.fa_splitkv_workspace_bytes(B, H, Nq, d, 2) <= fa.FA_SPLITKV_STATIC_SCRATCH_BYTES
+    q, k, v = make_qkv(B, H, Nq, d, torch.bfloat16, seed=7)
+    q, k, v = q.cuda(), k.cuda(), v.cuda()
+    o_ref = torch.empty_like(q)
+    l_ref = torch.empty(q.shape[:-1], device="cuda")
+    fa.fa_forward_splitkv(q, k, v, o_ref, l_ref, d ** -0.5, "causal", 0, 0, 2)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], device="cuda")
+    rc = _static(lib, q, k, v, o, lse, d ** -0.5, "causal", (0, 0), splits)
+    assert rc == fa.FA_OK, fa.fa_status_string(rc)
+    assert fa.fa_sync_status() == fa.FA_OK
+    assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
 
 
 def test_static_scratch_rejects_requests_beyond_its_size():

@@ -82,6 +82,7 @@ struct Params {
     unsigned long long wait_budget_ns;
     unsigned int *status;
     unsigned int *sched; // this launch's {next unit, finished CTAs}
+    int fault_skip_k;    // test hook: every CTA skips the K load at this ring position (-1: none)
 };
 
 // Tiles are stored as regions of 64 columns (128 bytes, the 128-byte swizzle).
@@ -306,10 +307,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int st = t % kKStages;
                     ok = mbar_wait_bounded(bar(kBarKEmpty + st), ((t / kKStages) & 1) ^ 1, abort_flag, budget);
                     if (!ok) break;
-                    mbar_arrive_expect_tx(bar(kBarKFull + st), L::kKVBytes);
-                    for (int g = 0; g < L::kRegions; ++g)
-                        tma_load_3d(sK(t) + g * L::kKVRegion, &tmK, bar(kBarKFull + st), 64 * g,
-                                    j * kBN, U.bkv);
+                    if (t != p.fault_skip_k) {
+                        mbar_arrive_expect_tx(bar(kBarKFull + st), L::kKVBytes);
+                        for (int g = 0; g < L::kRegions; ++g)
+                            tma_load_3d(sK(t) + g * L::kKVRegion, &tmK, bar(kBarKFull + st),
+                                        64 * g, j * kBN, U.bkv);
+                    }
                 }
                 if (!claimed && ok) u_next = publish(unit_iter + 1);
                 u = u_next;
