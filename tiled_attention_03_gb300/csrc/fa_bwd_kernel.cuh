@@ -71,13 +71,6 @@ struct Rg {
 constexpr uint32_t kTmemCols = 512;
 constexpr unsigned kStatusTimeout = 4;   // FA_ERR_TIMEOUT
 constexpr int kMaxDynSmem = 232448;      // per-CTA opt-in limit of sm_100-class GPUs
-// Of every 32 probabilities, how many are computed on the FMA pipe (exp2_poly2)
-// instead of the MUFU unit, which otherwise bounds the probability phase.
-#ifndef FA_BWD_POLY_EXP
-#define FA_BWD_POLY_EXP 0
-#endif
-constexpr int kPolyExp = FA_BWD_POLY_EXP;
-static_assert(kPolyExp % 2 == 0 && kPolyExp <= 32, "poly share");
 enum : int { kRoleCompute = 1, kRoleTma = 2, kRoleMma = 3 };
 
 struct BwdParams {
@@ -692,14 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ffma2(pr[c + 2], pr[c + 3], sl2, sl2, -lw.z, -lw.w);
                 }
 #pragma unroll
-                for (int c = 0; c < 64; c += 2) {
-                    if ((c & 31) < kPolyExp) {
-                        exp2_poly2(pr[c], pr[c + 1]);
-                    } else {
-                        pr[c] = ex2_approx(pr[c]);
-                        pr[c + 1] = ex2_approx(pr[c + 1]);
-                    }
-                }
+                for (int c = 0; c < 64; ++c) pr[c] = ex2_approx(pr[c]);
                 if (boundary) {
 #pragma unroll
                     for (int c = 0; c < 64; ++c) {
@@ -1209,14 +1195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < 64; c += 2) ffma2(pr[c], pr[c + 1], sl2, sl2, -lw, -lw);
 #pragma unroll
-                for (int c = 0; c < 64; c += 2) {
-                    if ((c & 31) < kPolyExp) {
-                        exp2_poly2(pr[c], pr[c + 1]);
-                    } else {
-                        pr[c] = ex2_approx(pr[c]);
-                        pr[c + 1] = ex2_approx(pr[c + 1]);
-                    }
-                }
+                for (int c = 0; c < 64; ++c) pr[c] = ex2_approx(pr[c]);
                 if (boundary) {
 #pragma unroll
                     for (int c = 0; c < 64; ++c) {

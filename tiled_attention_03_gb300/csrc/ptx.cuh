@@ -371,35 +371,4 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     return r;
 }
 
-// 2^y for two values on the FMA pipe (relieves the MUFU unit, which would
-// otherwise bound the softmax). Method: range reduction 2^y = 2^n * 2^f with
-// n = rint(y) (the 1.5 * 2^23 shifter: adding it leaves rint(y) in the low
-// mantissa bits) and f = y - n in [-1/2, 1/2]; 2^f = e^(f ln 2) by its Taylor
-// polynomial of degree 4, coefficients (ln 2)^k / k!, whose truncation error is
-// below (ln 2 / 2)^5 / 5! * sqrt(2) = 5.9e-5 relative; 2^n is added to the
-// exponent field of the result. Inputs are clamped to >= -125 so the exponent
-// stays normal (values below 2^-125 are negligible next to the row max term).
-__device__ __forceinline__ void exp2_poly2(float &a, float &b) {
-    constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
-    constexpr float c1 = 0.69314718055994529f, c2 = 0.24022650695910069f,
-                    c3 = 0.055504108664821576f, c4 = 0.0096181291076284769f;
-    a = fmaxf(a, -125.f);
-    b = fmaxf(b, -125.f);
-    float ta = a, tb = b;
-    fadd2(ta, tb, kShift, kShift);      // low bits of t = rint(y)
-    float na = ta, nb = tb;
-    fadd2(na, nb, -kShift, -kShift);    // n = rint(y) as a float
-    float fa = a, fb = b;
-    fadd2(fa, fb, -na, -nb);            // f = y - n
-    float pa = c4, pb = c4;
-    ffma2(pa, pb, fa, fb, c3, c3);
-    ffma2(pa, pb, fa, fb, c2, c2);
-    ffma2(pa, pb, fa, fb, c1, c1);
-    ffma2(pa, pb, fa, fb, 1.f, 1.f);    // 2^f
-    // bits(t) = bits(1.5 * 2^23) + n and bits(1.5 * 2^23) << 23 == 0 (mod 2^32),
-    // so (bits(t) << 23) adds exactly n to the exponent field.
-    a = __int_as_float(__float_as_int(pa) + (__float_as_int(ta) << 23));
-    b = __int_as_float(__float_as_int(pb) + (__float_as_int(tb) << 23));
-}
-
 }  // namespace fa
