@@ -96,15 +96,10 @@ struct Regions {
 };
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: probabilities stay <= 2^8
-// Of every 32 probabilities, how many use the FMA-pipe exp2 (the rest use MUFU),
-// and how many keys the softmax packs per TMEM store of P.
-#ifndef FA_POLY_EXP
-#define FA_POLY_EXP 0
-#endif
+// How many keys the softmax packs per TMEM store of P.
 #ifndef FA_P_CHUNK
 #define FA_P_CHUNK 32
 #endif
-constexpr int kPolyExp = FA_POLY_EXP;
 constexpr int kPChunk = FA_P_CHUNK;
 
 constexpr unsigned kStatusTimeout = 4;  // same value as FA_ERR_TIMEOUT
@@ -148,16 +143,24 @@ struct FwdParams {
     unsigned int *sched;   // this launch's {next unit, finished CTAs} counters (zero at launch)
 };
 
+#ifndef FA_KSTAGES_128
+#define FA_KSTAGES_128 2
+#endif
+#ifndef FA_VSTAGES_128
+#define FA_VSTAGES_128 2
+#endif
 template <int D>
 struct SmemLayout {
-    // K/V ring depth. The footprint stays above half of the SM's shared
-    // memory, so one CTA (holding all 512 TMEM columns) runs per SM.
-    static constexpr int kStages = D == 128 ? 2 : 4;
+    // K and V ring depths. The footprint stays above half of the SM's shared
+    // memory, so one CTA (holding all 512 TMEM columns) runs per SM. K_j is
+    // needed a whole softmax earlier than V_j, so its ring is the deeper one.
+    static constexpr int kStagesK = D == 128 ? FA_KSTAGES_128 : 4;
+    static constexpr int kStagesV = D == 128 ? FA_VSTAGES_128 : 4;
     static constexpr int kTileBytes = kBM * D * 2;
     static constexpr int kQ = 0;
     static constexpr int kK = kQ + kQTiles * kTileBytes;
-    static constexpr int kV = kK + kStages * kTileBytes;
-    static constexpr int kBar = kV + kStages * kTileBytes;
+    static constexpr int kV = kK + kStagesK * kTileBytes;
+    static constexpr int kBar = kV + kStagesV * kTileBytes;
     static constexpr int kNumBars = 40;
     static constexpr int kMisc = kBar + kNumBars * 8;
     static constexpr int kUnitRing = kMisc + 16;  // kUnitSlots ints: unit ids handed out to the roles
@@ -328,12 +331,9 @@ __device__ __forceinline__ void record_timeout(const FwdParams &p, volatile int 
 // tP (64 columns). Returns the factor by which the caller must rescale O
 // (1 when the reference max did not move). The stores are left in flight:
 // the caller waits with tcgen05.wait::st before signalling.
-// kPoly of every 32 probabilities are computed with exp2_poly2, the rest with
-// the MUFU ex2 instruction.
-template <bool BF16, int kPoly, int kPChunk>
+template <bool BF16, int kPChunk>
 __device__ __forceinline__ float softmax_tile(uint32_t tS, uint32_t tP, bool boundary, int kv0,
                                               int lo_i, int hi_i, float sl2, float &m, float &l) {
-    static_assert(kPoly % 2 == 0 && kPoly <= 32, "poly share");
     uint32_t sr[4][32];
 #pragma unroll
     for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
@@ -375,12 +375,8 @@ __device__ __forceinline__ float softmax_tile(uint32_t tS, uint32_t tP, bool bou
 #pragma unroll
         for (int e = 0; e < kPChunk; e += 2) {
             ffma2(x[c + e], x[c + e + 1], sl2, sl2, nm, nm);
-            if ((e & 31) < kPoly) {
-                exp2_poly2(x[c + e], x[c + e + 1]);
-            } else {
-                x[c + e] = ex2_approx(x[c + e]);
-                x[c + e + 1] = ex2_approx(x[c + e + 1]);
-            }
+            x[c + e] = ex2_approx(x[c + e]);
+            x[c + e + 1] = ex2_approx(x[c + e + 1]);
         }
 #pragma unroll
         for (int e = 0; e < kPChunk; e += 4) {
@@ -433,8 +429,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     using L = SmemLayout<D>;
     using G = Regions<D>;
     constexpr int kRegions = G::kCount;
-    constexpr int kStages = L::kStages;
-    static_assert(kStages <= kMaxStages && kNumBarsUsed <= L::kNumBars, "barrier slots");
+    constexpr int kStagesK = L::kStagesK;
+    constexpr int kStagesV = L::kStagesV;
+    static_assert(kStagesK <= kMaxStages && kStagesV <= kMaxStages && kNumBarsUsed <= L::kNumBars,
+                  "barrier slots");
+    static_assert(L::kAlloc <= 232448, "shared memory per CTA");
     static_assert(D == 32 || D == 64 || D == 128, "head dim");
 
     extern __shared__ uint8_t smem_raw[];
@@ -468,10 +467,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(kBarODone + t), 1);
             mbar_init(bar(kBarOFree + t), 128);
         }
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kStagesK; ++s) {
             mbar_init(bar(kBarKFull + s), 1);
-            mbar_init(bar(kBarVFull + s), 1);
             mbar_init(bar(kBarKEmpty + s), 1);
+        }
+        for (int s = 0; s < kStagesV; ++s) {
+            mbar_init(bar(kBarVFull + s), 1);
             mbar_init(bar(kBarVEmpty + s), 1);
         }
         mbar_init(bar(kBarDrain), 1);
@@ -560,8 +561,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!ok) break;
                         if (u_next >= 0) prefetch_q_l2(u_next);
                     }
-                    const int st = kv_iter % kStages;
-                    const uint32_t ph = (kv_iter / kStages) & 1;
+                    const int st = kv_iter % kStagesK;
+                    const uint32_t ph = (kv_iter / kStagesK) & 1;
                     ok = mbar_wait_bounded(bar(kBarKEmpty + st), ph ^ 1, abort_flag, budget);
                     if (!ok) break;
                     if (kv_iter != p.fault_skip_k) {
@@ -580,10 +581,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (q_loads > 0)
                 for (int t = 0; t < kQTiles; ++t)
                     mbar_wait_bounded(bar(kBarQFull + t), (q_loads - 1) & 1, nullptr, budget);
-            for (int s = 0; s < kStages; ++s) {
+            for (int s = 0; s < kStagesK; ++s) {
                 if (kv_iter > s) {
-                    const int last = kv_iter - 1 - ((kv_iter - 1 - s) % kStages);
-                    mbar_wait_bounded(bar(kBarKFull + s), (last / kStages) & 1, nullptr, budget);
+                    const int last = kv_iter - 1 - ((kv_iter - 1 - s) % kStagesK);
+                    mbar_wait_bounded(bar(kBarKFull + s), (last / kStagesK) & 1, nullptr, budget);
                 }
             }
         }
@@ -602,8 +603,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (u < 0) break;
                 const auto U = decode_unit<PACKED, VARLEN>(u, p);
                 for (int j = U.j0; ok && j <= U.j1; ++j, ++kv_iter) {
-                    const int st = kv_iter % kStages;
-                    ok = mbar_wait_bounded(bar(kBarVEmpty + st), ((kv_iter / kStages) & 1) ^ 1,
+                    const int st = kv_iter % kStagesV;
+                    ok = mbar_wait_bounded(bar(kBarVEmpty + st), ((kv_iter / kStagesV) & 1) ^ 1,
                                            abort_flag, budget);
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(kBarVFull + st), L::kTileBytes);
@@ -617,10 +618,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) record_timeout(p, abort_flag, kRoleTma, -1);
             // Drain: no copy may still be landing in shared memory when the CTA exits.
-            for (int s = 0; s < kStages; ++s) {
+            for (int s = 0; s < kStagesV; ++s) {
                 if (kv_iter > s) {
-                    const int last = kv_iter - 1 - ((kv_iter - 1 - s) % kStages);
-                    mbar_wait_bounded(bar(kBarVFull + s), (last / kStages) & 1, nullptr, budget);
+                    const int last = kv_iter - 1 - ((kv_iter - 1 - s) % kStagesV);
+                    mbar_wait_bounded(bar(kBarVFull + s), (last / kStagesV) & 1, nullptr, budget);
                 }
             }
         }
@@ -700,34 +701,81 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int j0 = U.j0;
             const int j1 = U.j1;
             auto in = [&U](int t, int j) { return j >= U.a[t] && j <= U.b[t]; };
-            for (int j = j0; ok && j <= j1 + 1; ++j) {
+            // Tile 1's visible keys start exactly one K/V tile after tile 0's (a
+            // sliding window whose left edge moves one tile per Q tile): pair the
+            // tiles by their own block index instead of by key position. Iteration
+            // i then computes S_0 on K/V tile j0 + i and S_1 on j0 + 1 + i, both Q
+            // tiles are busy in every iteration (in key order, tile 0 alone would
+            // run the first one and tile 1 alone the last), and both P V products
+            // of iteration i read the same V tile.
+            const bool shifted = U.a[0] <= U.b[0] && U.a[1] <= U.b[1] && U.a[1] == U.a[0] + 1;
+            if (shifted) {
+                const int last_s = max(U.b[0] - j0, U.b[1] - j0 - 1);  // iteration of the last S
+                for (int i = 0; ok && i <= j1 - j0; ++i) {
+                    const int ja = j0 + i;
+                    const int pa = kv_base + i, pb = pa + 1;  // ring positions of K/V tiles ja, ja + 1
+                    const int ka = pa % kStagesK, kb = pb % kStagesK, va = pa % kStagesV;
+                    const uint32_t kpa = (pa / kStagesK) & 1, kpb = (pb / kStagesK) & 1;
+                    const uint32_t vpa = (pa / kStagesV) & 1;
+                    const bool s0 = in(0, ja);      // S_0 on tile ja, then O_0 += P_0 V_ja
+                    const bool s1 = in(1, ja + 1);  // S_1 on tile ja + 1
+                    const bool v1 = in(1, ja);      // O_1 += P_1 V_ja (S_1 of the last iteration)
+                    // K_ja was already waited for by S_1 of the last iteration
+                    if (s0 && !v1) ok = wait(kBarKFull + ka, kpa);
+                    if (ok && s0) issue_s(0, ka);
+                    if (ok && v1) {
+                        ok = wait(kBarVFull + va, vpa) && wait(kBarPFull + 1, pv_count[1] & 1);
+                        if (ok && ja == U.a[1]) ok = wait(kBarOFree + 1, (epi_count[1] & 1) ^ 1);
+                        if (ok) issue_pv(1, va, ja == U.a[1]);
+                    }
+                    if (ok && s1) {
+                        ok = wait(kBarKFull + kb, kpb);
+                        if (ok) issue_s(1, kb);
+                    }
+                    if (ok) {
+                        commit(kBarKEmpty + ka);  // S_1(i - 1) and S_0(i) were K_ja's readers
+                        if (i == last_s)
+                            for (int t = 0; t < kQTiles; ++t) commit(kBarQEmpty + t);
+                    }
+                    if (ok && s0) {
+                        if (!v1) ok = wait(kBarVFull + va, vpa);
+                        ok = ok && wait(kBarPFull + 0, pv_count[0] & 1);
+                        if (ok && ja == U.a[0]) ok = wait(kBarOFree + 0, (epi_count[0] & 1) ^ 1);
+                        if (ok) issue_pv(0, va, ja == U.a[0]);
+                    }
+                    if (ok) commit(kBarVEmpty + va);  // both products of this iteration read V_ja
+                }
+            }
+            for (int j = j0; !shifted && ok && j <= j1 + 1; ++j) {
                 const int pos = kv_base + (j - j0);  // ring position of K_j / V_j
-                const int st = pos % kStages;
-                const uint32_t ph = (pos / kStages) & 1;
-                const int pst = (pos - 1 + kStages) % kStages;
-                const uint32_t pph = ((pos - 1) / kStages) & 1;
-                if (j <= j1) ok = wait(kBarKFull + st, ph);
-                if (ok && in(0, j)) issue_s(0, st);
+                const int kst = pos % kStagesK;
+                const uint32_t kph = (pos / kStagesK) & 1;
+                const int vst = pos % kStagesV;
+                const uint32_t vph = (pos / kStagesV) & 1;
+                const int pvst = (pos - 1 + kStagesV) % kStagesV;
+                const uint32_t pvph = ((pos - 1) / kStagesV) & 1;
+                if (j <= j1) ok = wait(kBarKFull + kst, kph);
+                if (ok && in(0, j)) issue_s(0, kst);
                 if (ok && in(1, j - 1)) {
                     // V_{j-1} was already waited for by O_0 += P_0(j-1) V_{j-1}
-                    if (!in(0, j - 1)) ok = wait(kBarVFull + pst, pph);
+                    if (!in(0, j - 1)) ok = wait(kBarVFull + pvst, pvph);
                     ok = ok && wait(kBarPFull + 1, pv_count[1] & 1);
                     if (ok && j - 1 == U.a[1]) ok = wait(kBarOFree + 1, (epi_count[1] & 1) ^ 1);
-                    if (ok) issue_pv(1, pst, j - 1 == U.a[1]);
+                    if (ok) issue_pv(1, pvst, j - 1 == U.a[1]);
                 }
-                if (ok && in(1, j)) issue_s(1, st);
+                if (ok && in(1, j)) issue_s(1, kst);
                 if (ok && j <= j1) {
-                    commit(kBarKEmpty + st);  // K_j is free once its S MMAs complete
-                    if (j == j1)              // both Q buffers too
+                    commit(kBarKEmpty + kst);  // K_j is free once its S MMAs complete
+                    if (j == j1)               // both Q buffers too
                         for (int t = 0; t < kQTiles; ++t) commit(kBarQEmpty + t);
                 }
                 if (ok && in(0, j)) {
-                    ok = wait(kBarVFull + st, ph) && wait(kBarPFull + 0, pv_count[0] & 1);
+                    ok = wait(kBarVFull + vst, vph) && wait(kBarPFull + 0, pv_count[0] & 1);
                     if (ok && j == U.a[0]) ok = wait(kBarOFree + 0, (epi_count[0] & 1) ^ 1);
-                    if (ok) issue_pv(0, st, j == U.a[0]);
+                    if (ok) issue_pv(0, vst, j == U.a[0]);
                 }
                 // V_{j-1} is free once O_1 += P_1(j-1) V_{j-1} (issued above) completes.
-                if (ok && j > j0) commit(kBarVEmpty + pst);
+                if (ok && j > j0) commit(kBarVEmpty + pvst);
             }
             kv_base += j1 - j0 + 1;
             for (int t = 0; t < kQTiles; ++t)
@@ -788,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 tc_fence_after();
                 const int kv0 = j * kBN;
-                const float corr = softmax_tile<BF16, kPolyExp, kPChunk>(
+                const float corr = softmax_tile<BF16, kPChunk>(
                     tS, tS, !(kv0 >= lo_last && kv0 + kBN - 1 <= hi_first), kv0, lo_i, hi_i, sl2, m, l);
                 // O_t holds the sum up to block j-1: that MMA was issued before S_t(j),
                 // whose completion (s_full) implies its completion.
