@@ -45,6 +45,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "fa_mask.cuh"
 #include "ptx.cuh"
 
 namespace fa {
@@ -686,13 +687,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
 #pragma unroll
                 for (int c = 0; c < 64; ++c) pr[c] = ex2_approx(pr[c]);
-                if (boundary) {
-#pragma unroll
-                    for (int c = 0; c < 64; ++c) {
-                        const int q = q0 + c;
-                        if (q < key - p.wr || q > key + p.wl) pr[c] = 0.f;
-                    }
-                }
+                // column c is query position q0 + c: visible iff key - wr <= q0 + c <= key + wl
+                if (boundary) mask_outside_run(pr, key - p.wr - q0, key + p.wl - q0, 0.f);
                 if (!key_ok) {
 #pragma unroll
                     for (int c = 0; c < 64; ++c) pr[c] = 0.f;
@@ -1196,13 +1192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < 64; c += 2) ffma2(pr[c], pr[c + 1], sl2, sl2, -lw, -lw);
 #pragma unroll
                 for (int c = 0; c < 64; ++c) pr[c] = ex2_approx(pr[c]);
-                if (boundary) {
-#pragma unroll
-                    for (int c = 0; c < 64; ++c) {
-                        const int key = kc0 + c;
-                        if (key < lo_i || key > hi_i) pr[c] = 0.f;
-                    }
-                }
+                if (boundary) mask_outside_run(pr, lo_i - kc0, hi_i - kc0, 0.f);
                 ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kQDPFull), t & 1, abort_flag, budget));
                 if (!ok) break;
                 tc_fence_after();

@@ -38,6 +38,7 @@
 #include <cstdint>
 #include <cuda.h>
 
+#include "fa_mask.cuh"
 #include "ptx.cuh"
 
 namespace fa {
@@ -477,11 +478,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 const int kv0 = j * kBN;
-                if (!(kv0 >= lo_last && kv0 + kBN - 1 <= hi_first)) {
-#pragma unroll
-                    for (int c = 0; c < kBN; ++c)
-                        if (kv0 + c < lo_i || kv0 + c > hi_i) x[c] = -INFINITY;
-                }
+                if (!(kv0 >= lo_last && kv0 + kBN - 1 <= hi_first))
+                    mask_outside_run(x, lo_i - kv0, hi_i - kv0, -INFINITY);
                 float ma = fmaxf(x[0], x[1]), mb = fmaxf(x[2], x[3]);
 #pragma unroll
                 for (int c = 4; c < kBN; c += 4) {

@@ -60,6 +60,7 @@
 #include <cstdint>
 #include <cuda.h>
 
+#include "fa_mask.cuh"
 #include "ptx.cuh"
 
 namespace fa {
@@ -326,14 +327,14 @@ __device__ __forceinline__ void record_timeout(const FwdParams &p, volatile int 
 
 // One online-softmax step of this thread's row over a 128-key tile whose fp32
 // scores sit at TMEM address tS (this warp's lanes). Masks hidden keys (only
-// when `boundary`), moves the reference max m lazily, adds the tile's
+// in the kMasked instance), moves the reference max m lazily, adds the tile's
 // probabilities to l, and stores them as packed 16-bit pairs at TMEM address
 // tP (64 columns). Returns the factor by which the caller must rescale O
 // (1 when the reference max did not move). The stores are left in flight:
 // the caller waits with tcgen05.wait::st before signalling.
-template <bool BF16, int kPChunk>
-__device__ __forceinline__ float softmax_tile(uint32_t tS, uint32_t tP, bool boundary, int kv0,
-                                              int lo_i, int hi_i, float sl2, float &m, float &l) {
+template <bool BF16, int kPChunk, bool kMasked>
+__device__ __forceinline__ float softmax_tile(uint32_t tS, uint32_t tP, int kv0, int lo_i, int hi_i,
+                                              float sl2, float &m, float &l) {
     uint32_t sr[4][32];
 #pragma unroll
     for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
@@ -342,13 +343,7 @@ __device__ __forceinline__ float softmax_tile(uint32_t tS, uint32_t tP, bool bou
     float x[kBN];
 #pragma unroll
     for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(sr[c >> 5][c & 31]);
-    if (boundary) {
-#pragma unroll
-        for (int c = 0; c < kBN; ++c) {
-            const int key = kv0 + c;
-            if (key < lo_i || key > hi_i) x[c] = -INFINITY;
-        }
-    }
+    if constexpr (kMasked) mask_outside_run(x, lo_i - kv0, hi_i - kv0, -INFINITY);
     // Row max: four independent chains of 3-input max.
     float ma = fmaxf(x[0], x[1]), mb = fmaxf(x[2], x[3]);
     float mc = fmaxf(x[4], x[5]), md = fmaxf(x[6], x[7]);
@@ -836,8 +831,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 tc_fence_after();
                 const int kv0 = j * kBN;
-                const float corr = softmax_tile<BF16, kPChunk>(
-                    tS, tS, !(kv0 >= lo_last && kv0 + kBN - 1 <= hi_first), kv0, lo_i, hi_i, sl2, m, l);
+                // Tiles visible to every row of the Q tile take the unmasked instance.
+                const float corr =
+                    kv0 >= lo_last && kv0 + kBN - 1 <= hi_first
+                        ? softmax_tile<BF16, kPChunk, false>(tS, tS, kv0, lo_i, hi_i, sl2, m, l)
+                        : softmax_tile<BF16, kPChunk, true>(tS, tS, kv0, lo_i, hi_i, sl2, m, l);
                 // O_t holds the sum up to block j-1: that MMA was issued before S_t(j),
                 // whose completion (s_full) implies its completion.
                 if (j > U.a[t] && __any_sync(0xffffffffu, corr != 1.f)) {
