@@ -3,12 +3,15 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <functional>
 #include <mutex>
+#include <vector>
 
 #include "fa.h"
 #include "fa_combine.cuh"
@@ -421,6 +424,102 @@ fa_status run_forward_1t(const Call &c, DeviceState *ds, int dev, int64_t n_spli
     return FA_OK;
 }
 
+// Row spaces per scheduling group of the heavy-first order (FwdParams::group).
+// The launch-wide counter hands units to whichever CTA is free, so the launch
+// ends when the last CTA finishes its last unit; with few units per CTA that
+// tail is a large share. Grouping spaces puts the lightest units of many spaces
+// at the end. The group size is chosen by simulating that greedy assignment on
+// the units' K/V tile counts for a few sizes (cached per shape), among groups
+// whose K and V stay well inside L2 (their units run concurrently and share it).
+struct GroupKey {
+    int v[12];
+    bool operator==(const GroupKey &o) const {
+        for (int i = 0; i < 12; ++i)
+            if (v[i] != o.v[i]) return false;
+        return true;
+    }
+};
+std::mutex g_group_mu;
+GroupKey g_group_keys[16];
+int g_group_vals[16];
+int g_group_n = 0;
+
+int unit_group(const fa::FwdParams &p, int grid, size_t kv_head_bytes) {
+    const int spaces = p.n_spaces;
+    const int64_t n_units = static_cast<int64_t>(p.n_units);
+    if (spaces < 2 || grid < 1 || n_units > 32 * static_cast<int64_t>(grid)) return 1;
+    const GroupKey key{{p.n_qb, p.n_splits, spaces, p.split_tiles, p.wl, p.wr, p.R, p.Nk,
+                        p.q_off, grid, p.kv_group, static_cast<int>(kv_head_bytes >> 10)}};
+    {
+        std::lock_guard<std::mutex> lk(g_group_mu);
+        for (int i = 0; i < g_group_n && i < 16; ++i)
+            if (g_group_keys[i] == key) return g_group_vals[i];
+    }
+    // Weight of unit (row block qb, split s): its MMA iterations (K/V tiles, plus one
+    // to drain unless its two Q tiles pair one tile apart) and a fixed share for
+    // the unit's start and epilogue. Same visibility rule as decode_unit.
+    std::vector<int> w(static_cast<size_t>(p.n_qb) * p.n_splits, 0);
+    for (int qb = 0; qb < p.n_qb; ++qb)
+        for (int sp = 0; sp < p.n_splits; ++sp) {
+            const int s_lo = sp * p.split_tiles, s_hi = s_lo + p.split_tiles - 1;
+            int a[2] = {1, 1}, b[2] = {0, 0}, j0 = 0x7fffffff, j1 = -1;
+            for (int t = 0; t < 2; ++t) {
+                const int rt0 = qb * fa::kUnitRows + t * fa::kBM;
+                if (rt0 >= p.R) continue;
+                const int rl = std::min(rt0 + fa::kBM, p.R) - 1;
+                const int64_t lo_key = static_cast<int64_t>(rt0) + p.q_off - p.wl;
+                const int64_t hi_key = static_cast<int64_t>(rl) + p.q_off + p.wr;
+                if (hi_key < 0 || lo_key > p.Nk - 1) continue;
+                const int at = std::max(static_cast<int>(std::max<int64_t>(0, lo_key) / fa::kBN), s_lo);
+                const int bt = std::min(static_cast<int>(std::min<int64_t>(p.Nk - 1, hi_key) / fa::kBN), s_hi);
+                if (at > bt) continue;
+                a[t] = at;
+                b[t] = bt;
+                j0 = std::min(j0, at);
+                j1 = std::max(j1, bt);
+            }
+            if (j1 < j0) continue;
+            const bool paired = a[0] <= b[0] && a[1] <= b[1] && a[1] == a[0] + 1;
+            w[static_cast<size_t>(qb) * p.n_splits + sp] = (j1 - j0 + 1) + (paired ? 0 : 1) + 3;
+        }
+    const size_t l2_budget = size_t{48} << 20;
+    const int cands[] = {1, 2, 4, 8, 12, 16, 24, 32, 48, 64};
+    int best = 1;
+    int64_t best_t = -1;
+    std::vector<int64_t> heap(static_cast<size_t>(grid));
+    for (int g : cands) {
+        if (g > spaces) break;
+        const size_t kv_heads = static_cast<size_t>((g + p.kv_group - 1) / p.kv_group + 1);
+        if (g > 1 && kv_heads * kv_head_bytes > l2_budget) break;
+        std::fill(heap.begin(), heap.end(), 0);  // a min-heap of the CTAs' finishing times
+        for (int base = 0; base < spaces; base += g) {
+            const int gs = std::min(g, spaces - base);
+            for (int qbi = 0; qbi < p.n_qb; ++qbi) {
+                const int qb = p.n_qb - 1 - qbi;
+                for (int h = 0; h < gs; ++h)
+                    for (int sp = 0; sp < p.n_splits; ++sp) {
+                        const int wu = w[static_cast<size_t>(qb) * p.n_splits + sp];
+                        if (wu == 0) continue;
+                        std::pop_heap(heap.begin(), heap.end(), std::greater<int64_t>());
+                        heap.back() += wu;
+                        std::push_heap(heap.begin(), heap.end(), std::greater<int64_t>());
+                    }
+            }
+        }
+        const int64_t t = *std::max_element(heap.begin(), heap.end());
+        if (best_t < 0 || t < best_t) {
+            best_t = t;
+            best = g;
+        }
+    }
+    std::lock_guard<std::mutex> lk(g_group_mu);
+    const int slot = g_group_n % 16;
+    g_group_keys[slot] = key;
+    g_group_vals[slot] = best;
+    ++g_group_n;
+    return best;
+}
+
 fa_status run_forward(const Call &c) {
     const void *Q = c.Q, *K = c.K, *V = c.V;
     void *O = c.O;
@@ -538,9 +637,14 @@ fa_status run_forward(const Call &c) {
     p.status = ds->status;
     p.fault_skip_k = g_fault_pos.exchange(-1);
     p.sched = ds->sched + 2 * (g_sched_next.fetch_add(1) % kSchedSlots);
+    p.n_spaces = static_cast<int>(spaces);
 
     // Persistent grid: one CTA per SM (each holds the SM's whole tensor memory).
     const int64_t blocks = n_units < ds->sm_count ? n_units : ds->sm_count;
+    p.group = p.heavy_first && !packed
+                  ? unit_group(p, static_cast<int>(blocks),
+                               static_cast<size_t>(Nk) * static_cast<size_t>(d) * 4)
+                  : 1;
     cudaStream_t st = static_cast<cudaStream_t>(c.stream);
     cudaError_t e;
     if (d == 32)

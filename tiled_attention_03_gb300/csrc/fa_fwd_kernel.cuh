@@ -127,7 +127,14 @@ struct FwdParams {
     int n_qb;         // 256-row blocks per row space: ceil(R / 256)
     int n_splits;     // key splits per row block (1: no split)
     int split_tiles;  // K/V tiles per key split
-    int heavy_first;  // 1: within a head, visit row blocks from the last (most keys) to the first
+    int heavy_first;  // 1: visit row blocks from the last (most keys) to the first
+    // Order in which the scheduler hands out units (scheduled_unit): row spaces
+    // in groups of `group`, and within a group all spaces' first row blocks in
+    // the visiting order (the heaviest, with heavy_first), then their second ones:
+    // the lightest units of the launch then come last, where they even out the
+    // CTAs' finishing times. 1: one space at a time (space-major).
+    int group;
+    int n_spaces;     // row spaces of the launch
     int wl, wr;       // key j visible to query i iff i + q_off - wl <= j <= i + q_off + wr
     float scale_log2; // scale * log2(e)
     unsigned long long wait_budget_ns;
@@ -313,6 +320,24 @@ __device__ __forceinline__ Unit<VARLEN> decode_unit(int u, const FwdParams &p) {
 }
 
 __device__ __forceinline__ bool unit_empty(const UnitBase &U) { return U.j1 < U.j0; }
+
+// The unit id (numbered space-major, as decode_unit reads it) of the n-th unit the
+// launch-wide counter hands out. With p.group > 1 the spaces are taken in groups:
+// within a group, every space's first row block in the visiting order, then every
+// space's second one, and so on. Only the scheduler calls this, once per unit.
+__device__ __forceinline__ int scheduled_unit(int n, const FwdParams &p) {
+    if (p.group <= 1) return n;
+    const int per_space = p.n_qb * p.n_splits;
+    const int g = n / (p.group * per_space);
+    const int base = g * p.group;
+    const int gs = min(p.group, p.n_spaces - base);  // spaces in this group
+    const int rem = n - base * per_space;
+    const int qbi = rem / (gs * p.n_splits);
+    const int rem2 = rem - qbi * gs * p.n_splits;
+    const int hi = rem2 / p.n_splits;
+    const int split = rem2 - hi * p.n_splits;
+    return (base + hi) * per_space + qbi * p.n_splits + split;
+}
 
 __device__ __forceinline__ void record_timeout(const FwdParams &p, volatile int *abort_flag,
                                                int role, int unit) {
@@ -513,8 +538,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 while (true) {
                     const unsigned next = atomicAdd(p.sched, 1u);
                     if (next >= static_cast<unsigned>(p.n_units)) break;
-                    if (!unit_empty(decode_unit<PACKED, VARLEN>(static_cast<int>(next), p))) {
-                        v = static_cast<int>(next);
+                    const int un = scheduled_unit(static_cast<int>(next), p);
+                    if (!unit_empty(decode_unit<PACKED, VARLEN>(un, p))) {
+                        v = un;
                         break;
                     }
                 }
