@@ -38,17 +38,28 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
 # the sources of the kernels it was measured on are unchanged.
 CSRC = "tiled_attention_03_gb300/csrc/"
 KERNEL_SOURCES = {
-    "fwd": (CSRC + "fa_fwd_kernel.cuh", CSRC + "fa_combine.cuh", CSRC + "ptx.cuh"),
-    "fwd1t": (CSRC + "fa_fwd1t_kernel.cuh", CSRC + "fa_combine.cuh", CSRC + "ptx.cuh"),
-    "bwd": (CSRC + "fa_bwd_kernel.cuh", CSRC + "ptx.cuh"),
+    "fwd": (CSRC + "fa_fwd_kernel.cuh", CSRC + "fa_combine.cuh", CSRC + "fa_mask.cuh",
+            CSRC + "ptx.cuh"),
+    "fwd1t": (CSRC + "fa_fwd1t_kernel.cuh", CSRC + "fa_combine.cuh", CSRC + "fa_mask.cuh",
+              CSRC + "ptx.cuh"),
+    "bwd": (CSRC + "fa_bwd_kernel.cuh", CSRC + "fa_mask.cuh", CSRC + "ptx.cuh"),
 }
 TRAFFIC_DIR = os.path.join(ROOT, "profiles")
 
 
-def one_tile(w) -> bool:
+def sm_count() -> int:
+    import torch
+    if torch.cuda.is_available():
+        return torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return 152  # GB300
+
+
+def one_tile(w, sms: int | None = None) -> bool:
     """Whether the library runs this forward on its one-tile kernel: always at d = 256,
     and at d = 64 / 128 when a row space (one head's queries, or the queries of all
-    query heads of one K/V head when each has at most 64) holds at most 128 rows."""
+    query heads of one K/V head when each has at most 64) holds at most 128 rows, or
+    when the call has one key split and the two-tile kernel's 256-row units would
+    fill at most half of the SMs."""
     if w.backward or w.varlen:
         return False
     if w.d == 256:
@@ -56,13 +67,23 @@ def one_tile(w) -> bool:
     if w.d not in (64, 128):
         return False
     packed = w.kv_heads < w.H and w.q_rows <= 64
-    return (w.H // w.kv_heads if packed else 1) * w.q_rows <= 128
+    rows = (w.H // w.kv_heads if packed else 1) * w.q_rows
+    if rows <= 128:
+        return True
+    sms = sms if sms is not None else sm_count()
+    spaces = w.B * (w.kv_heads if packed else w.H)
+    units = spaces * ((rows + 255) // 256)
+    tiles = (w.N + 127) // 128
+    # the split count the call runs: the workload's, or the library's default (one wave)
+    splits = 1 if w.splits < 0 else w.splits if w.splits > 0 else (
+        1 if units >= sms else max(1, min(sms // units, max(1, tiles // 4), 256)))
+    return min(splits, tiles) == 1 and 2 * units <= sms
 
 
-def kernel_family(w) -> str:
+def kernel_family(w, sms: int | None = None) -> str:
     if w.backward:
         return "bwd"
-    return "fwd1t" if one_tile(w) else "fwd"
+    return "fwd1t" if one_tile(w, sms) else "fwd"
 
 
 def kernel_source_hash(family: str) -> str:

@@ -82,12 +82,13 @@ def test_kernel_family_follows_the_forward_dispatch():
     rule restates the library's (fa_api.cu use_onetile): the one-tile kernel for
     d = 256, and for d = 64 / 128 when a row space holds at most 128 rows, a row space
     being one head's queries or, with at most 64 queries and grouped heads, those of
-    all query heads of one K/V head."""
+    all query heads of one K/V head, or when the problem's 256-row units fill at most
+    half of the SMs (152 on GB300)."""
     sys.path.insert(0, ROOT)
     import dataclasses
     import bench
     from tiled_attention_03_gb300.workloads import BY_NAME
-    fam = lambda name: bench.kernel_family(BY_NAME[name])
+    fam = lambda name: bench.kernel_family(BY_NAME[name], sms=152)
     assert fam("full_b4h32n4096d128") == "fwd"
     assert fam("full_b4h32n4096d32") == "fwd"
     assert fam("full_b4h32n4096d64") == "fwd"
@@ -99,9 +100,14 @@ def test_kernel_family_follows_the_forward_dispatch():
         assert fam(name) == "fwd1t", name
     assert fam("bwd_b4h32n4096d128") == "bwd"
     base = BY_NAME["full_b4h32n4096d128"]
-    cut = lambda **kw: bench.kernel_family(dataclasses.replace(base, **kw))
-    assert cut(H=4, N=128) == "fwd1t" and cut(H=4, N=129) == "fwd"
-    assert cut(H=16, H_kv=2, Nq=16) == "fwd1t"    # 8 heads x 16 queries = 128 rows
-    assert cut(H=16, H_kv=2, Nq=17) == "fwd"      # 136 rows
-    assert cut(H=4, H_kv=2, Nq=100) == "fwd1t"    # not packed (Nq > 64): 100 rows
-    assert cut(H=4, N=100, d=32) == "fwd"         # d = 32 has no one-tile form
+    cut = lambda **kw: bench.kernel_family(dataclasses.replace(base, **kw), sms=152)
+    assert cut(B=40, H=4, N=128) == "fwd1t" and cut(B=40, H=4, N=129) == "fwd"
+    # small problems: 256-row units on at most half of the 152 SMs
+    for name in ("tiny_full", "causal_short"):
+        assert fam(name) == "fwd1t", name
+    assert fam("mqa_causal_b2h16kv1n2048d64") == "fwd"  # 256 units
+    assert cut(B=19, H=4, N=129) == "fwd1t" and cut(B=20, H=4, N=129) == "fwd"  # 76 / 80 units
+    assert cut(B=40, H=16, H_kv=2, Nq=16) == "fwd1t"    # 8 heads x 16 queries = 128 rows
+    assert cut(B=40, H=16, H_kv=2, Nq=17) == "fwd"      # 136 rows
+    assert cut(B=40, H=4, H_kv=2, Nq=100) == "fwd1t"    # not packed (Nq > 64): 100 rows
+    assert cut(H=4, N=100, d=32) == "fwd"               # d = 32 has no one-tile form

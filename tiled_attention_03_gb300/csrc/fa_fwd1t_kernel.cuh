@@ -269,10 +269,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = mbar_wait_bounded(bar(kBarUnitEmpty + slot), ((k / kUnitSlots) & 1) ^ 1,
                                        abort_flag, budget);
                 if (!ok) return -1;
-                // units whose key split holds no key of theirs are skipped here
+                // units whose key split holds no key of theirs are skipped here; a
+                // CTA's first unit is the one numbered like the CTA (no counter round
+                // trip at start-up), the counter numbers the rest from gridDim.x on
                 int v = -1;
-                while (true) {
-                    const unsigned next = atomicAdd(p.sched, 1u);
+                unsigned next = k == 0 ? blockIdx.x : gridDim.x + atomicAdd(p.sched, 1u);
+                for (;; next = gridDim.x + atomicAdd(p.sched, 1u)) {
                     if (next >= static_cast<unsigned>(p.n_units)) break;
                     const Unit W = decode<kBN>(static_cast<int>(next), p);
                     if (W.j0 <= W.j1) {

@@ -533,10 +533,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        abort_flag, budget);
                 if (!ok) return -1;
                 // Units with no visible key in their split (possible only with key
-                // splits) are skipped here, so every published unit has work.
+                // splits) are skipped here, so every published unit has work. A CTA's
+                // first unit is the one numbered like the CTA (the grid never exceeds
+                // the unit count), which spares the launch-wide counter's round trip
+                // at start-up; the counter then numbers the rest from gridDim.x on.
                 int v = -1;
-                while (true) {
-                    const unsigned next = atomicAdd(p.sched, 1u);
+                unsigned next = k == 0 ? blockIdx.x : gridDim.x + atomicAdd(p.sched, 1u);
+                for (;; next = gridDim.x + atomicAdd(p.sched, 1u)) {
                     if (next >= static_cast<unsigned>(p.n_units)) break;
                     const int un = scheduled_unit(static_cast<int>(next), p);
                     if (!unit_empty(decode_unit<PACKED, VARLEN>(un, p))) {
