@@ -60,10 +60,12 @@ def one_tile(w, sms: int | None = None) -> bool:
     query heads of one K/V head when each has at most 64) holds at most 128 rows, or
     when the call has one key split and the two-tile kernel's 256-row units would
     fill at most half of the SMs."""
-    if w.backward or w.varlen:
+    if w.backward:
         return False
     if w.d == 256:
         return True
+    if w.varlen:
+        return False
     if w.d not in (64, 128):
         return False
     packed = w.kv_heads < w.H and w.q_rows <= 64
@@ -638,7 +640,8 @@ def main():
                 "traffic": traffic, "algorithmic_bytes": nbytes,
                 "kernel": (f"fa_bwd prep + dK/dV + dQ kernels <{w.d}, {w.dtype_name}"
                            + (", varlen>" if w.varlen else ">") if w.backward
-                           else f"fa_fwd_kernel<{w.d}, {w.dtype_name}, varlen>" if w.varlen
+                           else (f"fa_fwd1t_kernel<{w.d}, {w.dtype_name}, varlen>" if w.d == 256
+                                 else f"fa_fwd_kernel<{w.d}, {w.dtype_name}, varlen>") if w.varlen
                            else (f"fa_fwd1t_kernel<{w.d}, {w.dtype_name}>" if one_tile(w)
                                  else f"fa_fwd_kernel<{w.d}, {w.dtype_name}>")
                            + (f" + merge ({splits} key splits)" if splits > 1 else ""))},

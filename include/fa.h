@@ -57,12 +57,12 @@ typedef enum { FA_DTYPE_FP16 = 0, FA_DTYPE_BF16 = 1 } fa_dtype;
  * LSE     : device pointer, contiguous B x H x N float32. Written.
  * B, H, N : >= 1. Any N is accepted (no padding is required of the caller;
  *           rows and keys past N are handled inside the kernel).
- * d       : head dimension: 32, 64, 128 or 256 (else FA_ERR_UNSUPPORTED). d = 256
- *           runs on a kernel with one 128-row Q tile per unit (as do d = 64 and 128
- *           when a head's queries, or the queries of one K/V head's query heads, fit
- *           in one tile), in fa_forward, fa_forward_gqa, the split-KV calls and
- *           fa_forward_host; the variable-length calls take 32, 64 and 128, as does
- *           fa_backward.
+ * d       : head dimension: 32, 64, 128 or 256 (else FA_ERR_UNSUPPORTED), in every
+ *           forward call. d = 256 runs on a kernel with one 128-row Q tile per unit,
+ *           as do d = 64 and 128 when a head's queries, or the queries of one K/V
+ *           head's query heads, fit in one tile, and small unsplit problems (whose
+ *           256-row units would fill at most half of the SMs). fa_backward and
+ *           fa_backward_varlen take 32, 64 and 128.
  * scale   : multiplier of the logits, finite and > 0 (typically 1/sqrt(d)).
  * mask_mode, window_left, window_right : see fa_mask_mode. The window
  *           arguments are read only for FA_MASK_WINDOW and must then be >= 0

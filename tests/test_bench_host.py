@@ -94,6 +94,7 @@ def test_kernel_family_follows_the_forward_dispatch():
     assert fam("full_b4h32n4096d64") == "fwd"
     assert fam("chunk_b1h32kv8_nq512_nk16384_d128") == "fwd"
     assert fam("varlen_causal_b16h32n4096d128") == "fwd"
+    assert fam("varlen_causal_b16h16n4096d256") == "fwd1t"
     for name in ("decode_b8h32kv8_nq1_nk32768_d128", "decode_b8h32kv8_nq1_nk32768_d64",
                  "decode_b8h16kv4_nq1_nk32768_d256", "chunk_b1h16kv4_nq512_nk16384_d256",
                  "full_b4h16n4096d256", "causal_b4h16n4096d256"):

@@ -85,14 +85,11 @@ def test_d256_gqa_long(mask):
     compare(o, lse, q, k, v, 256 ** -0.5, mask)
 
 
-def test_d256_varlen_rejected():
-    """d = 256 has no variable-length form: the call is refused before anything
-    is enqueued, and the next call still works."""
-    dev = torch.device("cuda", 0)
-    q, k, v = (t.to(dev).view(64, 2, 256) for t in make_qkv(1, 2, 64, 256, torch.float16, seed=0))
-    o, lse = torch.empty_like(q), torch.empty(64, 2, device=dev)
-    cu = torch.tensor([0, 30, 64], dtype=torch.int32, device=dev)
-    with pytest.raises(fa.FaError) as e:
-        fa.fa_forward_varlen(q, k, v, o, lse, cu, cu, 34, 0.0625)
-    assert e.value.status == fa.FA_ERR_UNSUPPORTED
-    assert fa.fa_sync_status() == fa.FA_OK
+def test_d256_varlen_uneven_lengths():
+    """d = 256 in a packed batch of uneven sequences (the one-tile kernel's
+    variable-length form): every sequence against the oracle, GQA, causal."""
+    from test_varlen_gpu import check, packed_inputs, run_varlen
+    seqs, Q, K, V, cu_q, cu_k = packed_inputs([30, 0, 300, 129], [30, 0, 700, 129], 4, 2, 256,
+                                              torch.bfloat16, seed=31)
+    o, lse = run_varlen(Q, K, V, cu_q, cu_k, 300, 0.0625, "causal", (0, 0))
+    check(seqs, o, lse, cu_q, 0.0625, "causal", (0, 0), torch.bfloat16)

@@ -70,7 +70,7 @@ CASES = [
 
 
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("mask,window", [("none", (0, 0)), ("causal", (0, 0)), ("window", (90, 3))])
 @pytest.mark.parametrize("case", range(len(CASES)))
 def test_varlen_parity(case, mask, window, d, dtype):
@@ -82,9 +82,10 @@ def test_varlen_parity(case, mask, window, d, dtype):
     check(seqs, o, lse, cu_q, scale, mask, window, dtype)
 
 
-def test_varlen_matches_dense_batch():
+@pytest.mark.parametrize("d", [128, 256])
+def test_varlen_matches_dense_batch(d):
     """Equal lengths: the same numbers as fa_forward on the (B, H, N, d) layout."""
-    B, H, N, d = 3, 4, 333, 128
+    B, H, N = 3, 4, 333
     q, k, v = make_qkv(B, H, N, d, torch.bfloat16, seed=3)
     dev = torch.device("cuda", 0)
     o_d, l_d = fa.forward(q.to(dev), k.to(dev), v.to(dev), d ** -0.5, "causal")
@@ -106,11 +107,12 @@ def test_varlen_no_queries_is_a_no_op():
     assert fa.fa_sync_status() == fa.FA_OK
 
 
-def test_varlen_workload_sampled():
-    """The benchmark's packed batch at full size, in its launch configuration;
+@pytest.mark.parametrize("name", ["varlen_causal_b16h32n4096d128", "varlen_causal_b16h16n4096d256"])
+def test_varlen_workload_sampled(name):
+    """The benchmark's packed batches at full size, in their launch configuration;
     sampled (sequence, head, 128-row block) slices against the oracle."""
     from tiled_attention_03_gb300.workloads import BY_NAME, varlen_inputs, varlen_lengths
-    w = BY_NAME["varlen_causal_b16h32n4096d128"]
+    w = BY_NAME[name]
     Q, K, V, cu = varlen_inputs(w)
     lens = varlen_lengths(w)
     o, lse = run_varlen(Q, K, V, cu, cu, max(lens), w.scale, "causal", (0, 0))

@@ -209,14 +209,14 @@ cudaError_t launch(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap
 // tokens): box = 64 columns x 1 head x 128 tokens, 128-byte swizzle (the same
 // shared-memory tile as make_map's); tokens past the end read as zero.
 bool make_map_tokens(CUtensorMap *map, const void *base, bool bf16, int64_t tokens,
-                     int64_t heads, int64_t d) {
+                     int64_t heads, int64_t d, uint32_t box_tokens = 128) {
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return false;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
                                 static_cast<cuuint64_t>(tokens)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * 2),
                                    static_cast<cuuint64_t>(heads * d * 2)};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(d < 64 ? d : 64), 1, 128};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(d < 64 ? d : 64), 1, box_tokens};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r =
         enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
@@ -289,24 +289,21 @@ struct OneTileState {
 };
 OneTileState g_onetile[kMaxDevices];
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool VARLEN = false>
 cudaError_t onetile_attr() {
-    return cudaFuncSetAttribute(fa::onetile::fa_fwd1t_kernel<D, BF16>,
+    return cudaFuncSetAttribute(fa::onetile::fa_fwd1t_kernel<D, BF16, VARLEN>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 fa::onetile::Smem<D>::kAlloc);
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool VARLEN = false>
 cudaError_t launch_onetile(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                            const fa::onetile::Params &p, unsigned blocks, cudaStream_t st) {
-    fa::onetile::fa_fwd1t_kernel<D, BF16>
+    fa::onetile::fa_fwd1t_kernel<D, BF16, VARLEN>
         <<<blocks, fa::onetile::kThreads, fa::onetile::Smem<D>::kAlloc, st>>>(q, k, v, p);
     return cudaGetLastError();
 }
 
-// Which kernel runs a dense forward: the one-tile kernel for d = 256, and for
-// d = 64 / 128 when a row space holds at most 128 rows (one Q tile: the two-tile
-// kernel would run one tile and wait on its softmax between S products).
 // The one-tile kernel runs d = 256; at d = 64 / 128 it runs row spaces of at most
 // 128 rows (decode steps), and small unsplit problems: those whose 256-row units
 // of the two-tile kernel would fill at most half of the SMs. There, twice as many
@@ -325,12 +322,8 @@ bool use_onetile(int64_t B, int64_t H, int64_t H_kv, int64_t Nq, int64_t d, int6
     return n_splits == 1 && 2 * spaces * ((R + fa::kUnitRows - 1) / fa::kUnitRows) <= sms;
 }
 
-// One 128-row Q tile per unit, bn(d)-key K/V tiles. The key splits are those of the
-// two-tile path (split_tiles 128-key tiles each, so the workspace and the merge are
-// the same); the kernel counts them in its own tiles.
-fa_status run_forward_1t(const Call &c, DeviceState *ds, int dev, int64_t n_splits,
-                         int64_t split_tiles) {
-    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+// Shared-memory opt-in of every one-tile kernel instance, once per device.
+bool onetile_ready(int dev) {
     OneTileState &s = g_onetile[dev];
     std::call_once(s.once, [&s] {
         cudaError_t e = onetile_attr<64, false>();
@@ -339,9 +332,20 @@ fa_status run_forward_1t(const Call &c, DeviceState *ds, int dev, int64_t n_spli
         if (e == cudaSuccess) e = onetile_attr<128, true>();
         if (e == cudaSuccess) e = onetile_attr<256, false>();
         if (e == cudaSuccess) e = onetile_attr<256, true>();
+        if (e == cudaSuccess) e = onetile_attr<256, false, true>();
+        if (e == cudaSuccess) e = onetile_attr<256, true, true>();
         s.err = e;
     });
-    if (s.err != cudaSuccess) return FA_ERR_CUDA;
+    return s.err == cudaSuccess;
+}
+
+// One 128-row Q tile per unit, bn(d)-key K/V tiles. The key splits are those of the
+// two-tile path (split_tiles 128-key tiles each, so the workspace and the merge are
+// the same); the kernel counts them in its own tiles.
+fa_status run_forward_1t(const Call &c, DeviceState *ds, int dev, int64_t n_splits,
+                         int64_t split_tiles) {
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+    if (!onetile_ready(dev)) return FA_ERR_CUDA;
     const int64_t B = c.B, H = c.H, H_kv = c.H_kv, Nq = c.Nq, Nk = c.Nk, d = c.d;
     const bool bf16 = c.dtype == FA_DTYPE_BF16;
     // few queries with grouped heads: one row space per K/V head (its query heads'
@@ -709,6 +713,68 @@ struct VarlenCall {
     void *stream;
 };
 
+// Variable-length batch at d = 256: the one-tile kernel's VARLEN instance. Units are
+// (sequence, head, 128-row block) of the longest sequence; K/V tiles hold 64 keys.
+fa_status run_forward_varlen_1t(const VarlenCall &c, DeviceState *ds, int dev) {
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+    if (!onetile_ready(dev)) return FA_ERR_CUDA;
+    const int64_t B = c.B, H = c.H, H_kv = c.H_kv;
+    constexpr int kD = 256;
+    constexpr int kBn = fa::onetile::bn(kD);
+    const bool bf16 = c.dtype == FA_DTYPE_BF16;
+    CUtensorMap mq, mk, mv;
+    if (!make_map_tokens(&mq, c.Q, bf16, c.total_q, H, kD, fa::onetile::kBM) ||
+        !make_map_tokens(&mk, c.K, bf16, c.total_k, H_kv, kD, kBn) ||
+        !make_map_tokens(&mv, c.V, bf16, c.total_k, H_kv, kD, kBn))
+        return FA_ERR_CUDA;
+    const int64_t BH = B * H;
+    const int64_t n_qb = (c.max_q + fa::onetile::kBM - 1) / fa::onetile::kBM;
+    const int64_t n_units = BH * n_qb;
+    if (n_units > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+    fa::onetile::Params p{};
+    p.O = c.O;
+    p.LSE = c.LSE;
+    p.Nq = static_cast<int>(c.max_q);
+    p.Nk = static_cast<int>(c.total_k);
+    p.BH = static_cast<int>(BH);
+    p.kv_group = static_cast<int>(H / H_kv);
+    p.hps = 1;
+    p.R = static_cast<int>(c.max_q);
+    p.n_units = static_cast<int>(n_units);
+    p.n_qb = static_cast<int>(n_qb);
+    p.n_splits = 1;
+    p.split_tiles = static_cast<int>((c.total_k + kBn - 1) / kBn);  // one split: every tile
+    // Every sequence's query-key offset lies in [-total_q, total_k], so a window
+    // of total_q + total_k stands for "all keys".
+    const int64_t all = c.total_q + c.total_k;
+    int64_t wl = all, wr = all;
+    if (c.mask_mode == FA_MASK_CAUSAL) wr = 0;
+    if (c.mask_mode == FA_MASK_WINDOW) {
+        wl = c.window_left < all ? c.window_left : all;
+        wr = c.window_right < all ? c.window_right : all;
+    }
+    p.wl = static_cast<int>(wl);
+    p.wr = static_cast<int>(wr);
+    p.heavy_first = wr < all ? 1 : 0;
+    p.scale_log2 = static_cast<float>(static_cast<double>(c.scale) * 1.4426950408889634074);
+    p.wait_budget_ns = wait_budget();
+    p.status = ds->status;
+    p.sched = ds->sched + 2 * (g_sched_next.fetch_add(1) % kSchedSlots);
+    p.fault_skip_k = g_fault_pos.exchange(-1);
+    p.cu_q = c.cu_q;
+    p.cu_k = c.cu_k;
+    p.total_q = static_cast<int>(c.total_q);
+    p.total_k = static_cast<int>(c.total_k);
+    p.H = static_cast<int>(H);
+    const unsigned blocks = static_cast<unsigned>(n_units < ds->sm_count ? n_units : ds->sm_count);
+    cudaStream_t st = static_cast<cudaStream_t>(c.stream);
+    const cudaError_t le = bf16 ? launch_onetile<kD, true, true>(mq, mk, mv, p, blocks, st)
+                                : launch_onetile<kD, false, true>(mq, mk, mv, p, blocks, st);
+    if (le != cudaSuccess) return FA_ERR_CUDA;
+    g_launches.fetch_add(1);
+    return FA_OK;
+}
+
 fa_status run_forward_varlen(const VarlenCall &c) {
     const int64_t B = c.B, H = c.H, H_kv = c.H_kv, d = c.d;
     // ---- host-side checks: nothing is enqueued on failure
@@ -728,7 +794,7 @@ fa_status run_forward_varlen(const VarlenCall &c) {
         !aligned4(c.LSE) || (reinterpret_cast<uintptr_t>(c.cu_q) & 3u) ||
         (reinterpret_cast<uintptr_t>(c.cu_k) & 3u))
         return FA_ERR_INVALID_ARG;
-    if (d != 32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (d != 32 && d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
     if (c.total_q > (int64_t{1} << 29) || c.total_k > (int64_t{1} << 29) || c.max_q > c.total_q ||
         B * H > (int64_t{1} << 31))
         return FA_ERR_UNSUPPORTED;
@@ -764,6 +830,7 @@ fa_status run_forward_varlen(const VarlenCall &c) {
         !on_device(c.cu_k, dev))
         return FA_ERR_INVALID_ARG;
 
+    if (d == 256) return run_forward_varlen_1t(c, ds, dev);
     const bool bf16 = c.dtype == FA_DTYPE_BF16;
     CUtensorMap mq, mk, mv;
     if (!make_map_tokens(&mq, c.Q, bf16, c.total_q, H, d) ||

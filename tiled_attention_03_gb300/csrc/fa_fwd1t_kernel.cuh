@@ -84,6 +84,15 @@ struct Params {
     unsigned int *status;
     unsigned int *sched; // this launch's {next unit, finished CTAs}
     int fault_skip_k;    // test hook: every CTA skips the K load at this ring position (-1: none)
+    // Variable-length batches (kernel template flag VARLEN): row space sp = b*H + h
+    // holds the queries of sequence b for query head h; the sequence's query tokens
+    // are cu_q[b] .. cu_q[b+1]-1 and its keys cu_k[b] .. cu_k[b+1]-1 of token-major
+    // tensors (tokens x heads x d), its queries at its last key positions. Offsets
+    // are clamped to [0, total], so no stray value addresses memory outside the
+    // tensors. Nq and R stand for the longest sequence's query count.
+    const int *cu_q, *cu_k;
+    int total_q, total_k;
+    int H;
 };
 
 // Tiles are stored as regions of 64 columns (128 bytes, the 128-byte swizzle).
@@ -141,11 +150,16 @@ __host__ __device__ constexpr uint32_t tmem_o(int D) { return D == 256 ? 256u : 
 // A unit: rows r0 .. rl of row space sp, restricted to the K/V tiles of key split
 // `split`; qmin .. qmax are the query indices among its rows; j0 .. j1 are the tiles
 // holding a key some row sees (empty when j1 < j0, possible only with key splits).
+//
+// Variable-length batches: the unit also carries its sequence's sizes (nq queries,
+// nk keys, query-key offset q_off), its first query and key tokens and its query and
+// K/V heads; a block past the sequence's queries is empty.
 struct Unit {
     int sp, bkv, r0, rl, qmin, qmax, j0, j1, split;
+    int nq, nk, q_off, q_tok0, k_tok0, h, hkv;
 };
 
-template <int kBN>
+template <int kBN, bool VARLEN>
 __device__ __forceinline__ Unit decode(int u, const Params &p) {
     Unit U;
     const int per_sp = p.n_qb * p.n_splits;
@@ -154,15 +168,45 @@ __device__ __forceinline__ Unit decode(int u, const Params &p) {
     int qb = rem / p.n_splits;
     U.split = rem - qb * p.n_splits;
     if (p.heavy_first) qb = p.n_qb - 1 - qb;
-    U.bkv = U.sp * p.hps / p.kv_group;  // (b*H + h) / group = b*H_kv + h / group
     U.r0 = qb * kBM;
-    U.rl = min(U.r0 + kBM, p.R) - 1;
-    // rows of one head: queries r0 % Nq .. rl % Nq; rows across a head boundary: all
-    const bool one_head = U.r0 / p.Nq == U.rl / p.Nq;
-    U.qmin = one_head ? U.r0 % p.Nq : 0;
-    U.qmax = one_head ? U.rl % p.Nq : p.Nq - 1;
-    const int lo_key = max(0, U.qmin + p.q_off - p.wl);
-    const int hi_key = min(p.Nk - 1, U.qmax + p.q_off + p.wr);
+    if constexpr (VARLEN) {
+        const int b = U.sp / p.H;
+        U.h = U.sp - b * p.H;
+        U.hkv = U.h / p.kv_group;
+        const int q0 = min(max(p.cu_q[b], 0), p.total_q);
+        const int q1 = min(max(p.cu_q[b + 1], q0), p.total_q);
+        const int k0 = min(max(p.cu_k[b], 0), p.total_k);
+        const int k1 = min(max(p.cu_k[b + 1], k0), p.total_k);
+        U.q_tok0 = q0;
+        U.k_tok0 = k0;
+        U.nq = q1 - q0;
+        U.nk = k1 - k0;
+        U.q_off = U.nk - U.nq;
+        U.bkv = 0;
+        if (U.r0 >= U.nq) {  // past the sequence's queries: no work
+            U.rl = U.r0;
+            U.qmin = U.qmax = 0;
+            U.j0 = 0;
+            U.j1 = -1;
+            return U;
+        }
+        U.rl = min(U.r0 + kBM, U.nq) - 1;
+        U.qmin = U.r0;
+        U.qmax = U.rl;
+    } else {
+        U.nq = p.Nq;
+        U.nk = p.Nk;
+        U.q_off = p.q_off;
+        U.q_tok0 = U.k_tok0 = U.h = U.hkv = 0;
+        U.bkv = U.sp * p.hps / p.kv_group;  // (b*H + h) / group = b*H_kv + h / group
+        U.rl = min(U.r0 + kBM, p.R) - 1;
+        // rows of one head: queries r0 % Nq .. rl % Nq; rows across a head boundary: all
+        const bool one_head = U.r0 / p.Nq == U.rl / p.Nq;
+        U.qmin = one_head ? U.r0 % p.Nq : 0;
+        U.qmax = one_head ? U.rl % p.Nq : p.Nq - 1;
+    }
+    const int lo_key = max(0, U.qmin + U.q_off - p.wl);
+    const int hi_key = min(U.nk - 1, U.qmax + U.q_off + p.wr);
     const int s_lo = U.split * p.split_tiles, s_hi = s_lo + p.split_tiles - 1;
     U.j0 = max(lo_key / kBN, s_lo);
     U.j1 = hi_key < 0 ? -1 : min(hi_key / kBN, s_hi);
@@ -180,7 +224,30 @@ __device__ __forceinline__ void record_timeout(const Params &p, volatile int *ab
     }
 }
 
-template <int D, bool BF16>
+// TMA coordinates of a unit's Q tile and of its K/V tile j: dense maps are
+// (d, rows, row spaces), variable-length maps (d, heads, tokens).
+template <bool VARLEN>
+__device__ __forceinline__ void q_coords(const Unit &U, int &y, int &z) {
+    if constexpr (VARLEN) {
+        y = U.h;
+        z = U.q_tok0 + U.r0;
+    } else {
+        y = U.r0;
+        z = U.sp;
+    }
+}
+template <bool VARLEN>
+__device__ __forceinline__ void kv_coords(const Unit &U, int j, int bn, int &y, int &z) {
+    if constexpr (VARLEN) {
+        y = U.hkv;
+        z = U.k_tok0 + j * bn;
+    } else {
+        y = j * bn;
+        z = U.bkv;
+    }
+}
+
+template <int D, bool BF16, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd1t_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const Params p) {
@@ -276,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 unsigned next = k == 0 ? blockIdx.x : gridDim.x + atomicAdd(p.sched, 1u);
                 for (;; next = gridDim.x + atomicAdd(p.sched, 1u)) {
                     if (next >= static_cast<unsigned>(p.n_units)) break;
-                    const Unit W = decode<kBN>(static_cast<int>(next), p);
+                    const Unit W = decode<kBN, VARLEN>(static_cast<int>(next), p);
                     if (W.j0 <= W.j1) {
                         v = static_cast<int>(next);
                         break;
@@ -288,12 +355,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             int u = publish(0);
             for (; ok && u >= 0; ++unit_iter) {
-                const Unit U = decode<kBN>(u, p);
+                const Unit U = decode<kBN, VARLEN>(u, p);
                 ok = mbar_wait_bounded(bar(kBarQEmpty), (unit_iter & 1) ^ 1, abort_flag, budget);
                 if (!ok) break;
                 mbar_arrive_expect_tx(bar(kBarQFull), L::kQBytes);
+                int qy, qz;
+                q_coords<VARLEN>(U, qy, qz);
                 for (int g = 0; g < L::kRegions; ++g)
-                    tma_load_3d(sQ + g * L::kQRegion, &tmQ, bar(kBarQFull), 64 * g, U.r0, U.sp);
+                    tma_load_3d(sQ + g * L::kQRegion, &tmQ, bar(kBarQFull), 64 * g, qy, qz);
                 ++q_loads;
                 int u_next = -1;
                 bool claimed = false;
@@ -303,18 +372,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         u_next = publish(unit_iter + 1);
                         if (!ok) break;
                         if (u_next >= 0) {
-                            const Unit W = decode<kBN>(u_next, p);
-                            for (int g = 0; g < L::kRegions; ++g) tma_prefetch_l2_3d(&tmQ, 64 * g, W.r0, W.sp);
+                            const Unit W = decode<kBN, VARLEN>(u_next, p);
+                            int wy, wz;
+                            q_coords<VARLEN>(W, wy, wz);
+                            for (int g = 0; g < L::kRegions; ++g) tma_prefetch_l2_3d(&tmQ, 64 * g, wy, wz);
                         }
                     }
                     const int st = t % kKStages;
                     ok = mbar_wait_bounded(bar(kBarKEmpty + st), ((t / kKStages) & 1) ^ 1, abort_flag, budget);
                     if (!ok) break;
                     if (t != p.fault_skip_k) {
+                        int ky, kz;
+                        kv_coords<VARLEN>(U, j, kBN, ky, kz);
                         mbar_arrive_expect_tx(bar(kBarKFull + st), L::kKVBytes);
                         for (int g = 0; g < L::kRegions; ++g)
                             tma_load_3d(sK(t) + g * L::kKVRegion, &tmK, bar(kBarKFull + st),
-                                        64 * g, j * kBN, U.bkv);
+                                        64 * g, ky, kz);
                     }
                 }
                 if (!claimed && ok) u_next = publish(unit_iter + 1);
@@ -335,16 +408,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int unit_iter = 0; ok; ++unit_iter) {
             const int u = take_unit(unit_iter, ok);
             if (!ok || u < 0) break;
-            const Unit U = decode<kBN>(u, p);
+            const Unit U = decode<kBN, VARLEN>(u, p);
             if (lane == 0) {
                 for (int j = U.j0; ok && j <= U.j1; ++j, ++t) {
                     const int st = t % kVStages;
                     ok = mbar_wait_bounded(bar(kBarVEmpty + st), ((t / kVStages) & 1) ^ 1, abort_flag, budget);
                     if (!ok) break;
+                    int vy, vz;
+                    kv_coords<VARLEN>(U, j, kBN, vy, vz);
                     mbar_arrive_expect_tx(bar(kBarVFull + st), L::kKVBytes);
                     for (int g = 0; g < L::kRegions; ++g)
                         tma_load_3d(sV(t) + g * L::kKVRegion, &tmV, bar(kBarVFull + st), 64 * g,
-                                    j * kBN, U.bkv);
+                                    vy, vz);
                 }
             }
             ok = __all_sync(0xffffffffu, ok);
@@ -405,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (; ok; ++unit_iter) {
             u = take_unit(unit_iter, ok);
             if (!ok || u < 0) break;
-            const Unit U = decode<kBN>(u, p);
+            const Unit U = decode<kBN, VARLEN>(u, p);
             const int n = U.j1 - U.j0 + 1;
             ok = wait(kBarQFull, unit_iter & 1);
             // S for the first min(3, n) blocks
@@ -450,14 +525,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (; ok; ++unit_iter) {
             u = take_unit(unit_iter, ok);
             if (!ok || u < 0) break;
-            const Unit U = decode<kBN>(u, p);
+            const Unit U = decode<kBN, VARLEN>(u, p);
             const int r = U.r0 + row;  // row of the space
-            const int i = r % p.Nq;    // its query index; key position i + q_off
-            const int lo_i = max(0, i + p.q_off - p.wl);
-            const int hi_i = min(p.Nk - 1, i + p.q_off + p.wr);
+            const int i = VARLEN ? r : r % p.Nq;  // its query index; key position i + q_off
+            const int lo_i = max(0, i + U.q_off - p.wl);
+            const int hi_i = min(U.nk - 1, i + U.q_off + p.wr);
             // a tile with keys in [lo_last, hi_first] only is visible to every row
-            const int lo_last = max(0, U.qmax + p.q_off - p.wl);
-            const int hi_first = min(p.Nk - 1, U.qmin + p.q_off + p.wr);
+            const int lo_last = max(0, U.qmax + U.q_off - p.wl);
+            const int hi_first = min(U.nk - 1, U.qmin + U.q_off + p.wr);
             float m = -INFINITY, l = 0.f;
             for (int j = U.j0; j <= U.j1; ++j, ++t) {
                 const uint32_t tS = tl + kTmemS + (t % kSBufs) * kBN;
@@ -548,8 +623,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
-            const bool store = r < p.R;
-            const size_t grow = static_cast<size_t>(U.sp) * p.R + (store ? r : 0);
+            // global row of O and LSE: (row space, row), or (token, head) when VARLEN
+            const bool store = r < (VARLEN ? U.nq : p.R);
+            const size_t grow = VARLEN ? (static_cast<size_t>(U.q_tok0) + (store ? r : 0)) * p.H + U.h
+                                       : static_cast<size_t>(U.sp) * p.R + (store ? r : 0);
             const float lse = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
             if (p.part_O == nullptr) {
                 uint8_t *orow = reinterpret_cast<uint8_t *>(p.O) + grow * (D * 2);

@@ -133,6 +133,9 @@ BWD_WORKLOADS = [
 VARLEN_WORKLOADS = [
     Workload("varlen_causal_b16h32n4096d128", 16, 32, 4096, 128, torch.bfloat16, MASK_CAUSAL, 0, 0,
              seed=12, varlen=True),
+    # the same length mix at head dimension 256 (16 heads)
+    Workload("varlen_causal_b16h16n4096d256", 16, 16, 4096, 256, torch.bfloat16, MASK_CAUSAL, 0, 0,
+             seed=23, varlen=True),
     # its backward (dO drawn like the dense backward workloads, then packed)
     Workload("bwd_varlen_causal_b16h32n4096d128", 16, 32, 4096, 128, torch.bfloat16, MASK_CAUSAL,
              0, 0, seed=12, varlen=True, backward=True),
