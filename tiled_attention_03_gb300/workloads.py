@@ -105,6 +105,10 @@ EXTRA_WORKLOADS = [
     Workload("decode_b8h32kv8_nq1_nk32768_d64", 8, 32, 32768, 64, torch.bfloat16, MASK_CAUSAL,
              0, 0, seed=22, H_kv=8, Nq=1, splits=0),
     # head dimension 32 (64-byte swizzled tiles) and 64 on the bench shape
+    # the long causal workload with 4 of its 8 batch entries: the same per-head shape
+    # and scheduling, small enough for a many-pass ncu capture (its traffic doubles to
+    # the full one's)
+    Workload("causal_b4h40n8192", 4, 40, 8192, 128, torch.bfloat16, MASK_CAUSAL, 0, 0, seed=4),
     Workload("full_b4h32n4096d32", 4, 32, 4096, 32, torch.bfloat16, MASK_NONE, 0, 0, seed=13),
     Workload("full_b4h32n4096d64", 4, 32, 4096, 64, torch.bfloat16, MASK_NONE, 0, 0, seed=18),
     # head dimension 256 (its own kernel), same FLOPs as the bench shape
