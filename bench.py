@@ -242,6 +242,28 @@ def cpu_oracle_rate(w, min_seconds: float, max_units: int | None = None, slab=No
     return flops / dt / 1e12, cores, f"{len(units)} x (1 head, {min(128, rows)}-row block, all {w.N} keys)", dt
 
 
+def cpu_oracle_full(w, min_seconds: float, threads: int):
+    """Time the fp64 oracle on the WHOLE workload (every head, every row), repeated
+    until min_seconds have passed, on `threads` host threads. Only for the small
+    workloads that the oracle finishes in milliseconds. Returns (TFLOP/s, seconds per
+    pass)."""
+    import oracle
+    from tiled_attention_03_gb300.workloads import algorithmic_flops, workload_inputs
+    q, k, v = workload_inputs(w)[:3]
+    mask = {0: "none", 1: "causal", 2: "window"}[w.mask]
+    reps, dt = 0, 0.0
+    t0 = time.perf_counter()
+    while dt < min_seconds or reps == 0:
+        oracle.attention(q, k, v, w.scale, mask, (w.window_left, w.window_right), nthreads=threads)
+        reps += 1
+        dt = time.perf_counter() - t0
+    return algorithmic_flops(w) * reps / dt / 1e12, dt / reps
+
+
+# The two small parity workloads: the oracle runs them whole, on all cores and on one.
+SMALL_WORKLOADS = ("tiny_full", "causal_short")
+
+
 def cpu_oracle_rate_bwd(w, min_seconds: float, max_heads: int | None = None):
     """Time the fp64 gradient oracle on a sample of whole K/V heads (each with the
     query heads reading it) of the workload's shape, on every core. Returns
@@ -325,20 +347,56 @@ def run_e2e(args, w, q_h, k_h, v_h, mask, stream, dev, world, flops):
     barrier(world)
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
-    e2 = torch.cuda.Event(enable_timing=True)
-    e3 = torch.cuda.Event(enable_timing=True)
-    e2.record(stream)
-    for _ in range(args.e2e_steps):
+    # an event after every step (the stream waits for each step's last copy out)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.e2e_steps + 1)]
+    ev[0].record(stream)
+    for i in range(args.e2e_steps):
         run()
-    e3.record(stream)
+        ev[i + 1].record(stream)
     torch.cuda.synchronize(dev)
     wall_ms = (time.perf_counter() - t0) * 1e3 / args.e2e_steps
-    e2e_ms = max_over_ranks(max(e2.elapsed_time(e3) / args.e2e_steps, wall_ms), world)
+    e2e_ms = max_over_ranks(max(ev[0].elapsed_time(ev[-1]) / args.e2e_steps, wall_ms), world)
+    per = sorted(ev[i].elapsed_time(ev[i + 1]) for i in range(args.e2e_steps))
+    pct = lambda f: per[min(len(per) - 1, int(f * len(per)))]
     elems = q_h.numel()  # O has Q's shape
     h2d = (q_h.numel() + k_h.numel() + v_h.numel()) * q_h.element_size()
     d2h = elems * q_h.element_size() + (elems // w.d) * 4
     return {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+            "step_ms": {"p10": pct(0.1), "p50": pct(0.5), "p90": pct(0.9)},
+            "copy_floor": copy_floor(qp, kp, vp, out, lse_out, dev)}
+
+
+def copy_floor(qp, kp, vp, out, lse_out, dev, reps: int = 5):
+    """The step's copies alone, in the same run: Q, K, V host -> device, then O and LSE
+    device -> host, each direction by itself and both at once on two streams (the
+    least time the end-to-end step could take). Median of `reps`, in ms and GB/s."""
+    ins = [torch.empty_like(t, device=dev) for t in (qp, kp, vp)]
+    outs = [torch.empty_like(t, device=dev) for t in (out, lse_out)]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def timed(do_in, do_out):
+        ts = []
+        for _ in range(reps):
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            if do_in:
+                with torch.cuda.stream(s_in):
+                    for d, h in zip(ins, (qp, kp, vp)):
+                        d.copy_(h, non_blocking=True)
+            if do_out:
+                with torch.cuda.stream(s_out):
+                    for h, d in zip((out, lse_out), outs):
+                        h.copy_(d, non_blocking=True)
+            torch.cuda.synchronize(dev)
+            ts.append((time.perf_counter() - t0) * 1e3)
+        return sorted(ts)[len(ts) // 2]
+
+    b_in = sum(t.numel() * t.element_size() for t in (qp, kp, vp))
+    b_out = sum(t.numel() * t.element_size() for t in (out, lse_out))
+    t_in, t_out, t_both = timed(True, False), timed(False, True), timed(True, True)
+    return {"h2d_ms": t_in, "h2d_gbs": b_in / t_in / 1e6, "d2h_ms": t_out,
+            "d2h_gbs": b_out / t_out / 1e6, "both_ms": t_both}
 
 
 def run_e2e_varlen(args, w, host, max_q, mask, stream, dev, world, flops):
@@ -606,6 +664,14 @@ def main():
             cpu_v, cores, sample, _ = cpu_oracle_rate_bwd(w, args.cpu_seconds)
             cpu = {"value": cpu_v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                    "sample": sample}
+        elif args.cpu_seconds > 0 and w.name in SMALL_WORKLOADS:
+            cores = len(os.sched_getaffinity(0))
+            cpu_v, per_pass = cpu_oracle_full(w, min(args.cpu_seconds, 5.0), cores)
+            one_v, one_pass = cpu_oracle_full(w, min(args.cpu_seconds, 5.0), 1)
+            cpu = {"value": cpu_v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                   "sample": f"the whole workload ({per_pass * 1e3:.2f} ms per pass)",
+                   "one_core": {"value": one_v, "unit": "TFLOP/s", "cores": 1,
+                                "sample": f"the whole workload ({one_pass * 1e3:.2f} ms per pass)"}}
         elif args.cpu_seconds > 0:
             cpu_v, cores, sample, _ = cpu_oracle_rate(w, args.cpu_seconds)
             cpu = {"value": cpu_v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
