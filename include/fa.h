@@ -36,7 +36,9 @@ typedef enum {
     FA_ERR_INVALID_ARG = 1, /* a null/misaligned/aliased pointer, a bad size or enum, a bad scale */
     FA_ERR_UNSUPPORTED = 2, /* a valid request this build does not implement (head dim, device) */
     FA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (launch, attribute, tensor map) */
-    FA_ERR_TIMEOUT = 4      /* a bounded in-kernel wait ran out (reported by fa_sync_status) */
+    FA_ERR_TIMEOUT = 4,     /* a bounded in-kernel wait ran out (reported by fa_sync_status) */
+    FA_ERR_BOUNDS = 5       /* debug builds only: a kernel refused an out-of-range store
+                               (reported by fa_sync_status) */
 } fa_status;
 
 typedef enum {
@@ -341,6 +343,31 @@ int64_t fa_launch_count(void);
  * `kv_position`, with the same outcome.
  */
 void fa_test_arm_fault(int32_t kv_position);
+
+/*
+ * Debug builds. The library can be compiled with two checks that release builds
+ * leave out (tiled_attention_03_gb300/build.py, debug="serialize" / "bounds"); the
+ * pages have no counterpart, they are aids for changing the kernels. They apply
+ * to the two-tile forward kernel (every forward at d = 32, and at d = 64 / 128
+ * unless the one-tile kernel runs it).
+ *  - FA_DEBUG_SERIALIZE: the kernel runs with the least overlap its protocol
+ *    allows (K/V rings two deep, the next unit claimed with the current unit's
+ *    last K/V tile, every group of matrix products completed before the next is
+ *    issued), so that an ordering mistake shows as a wrong result or a timeout.
+ *  - FA_DEBUG_BOUNDS: every store of O, LSE and the split buffers is checked
+ *    against the output first; an out-of-range row is not stored, and the first
+ *    one is recorded in the status word, which fa_sync_status then reports as
+ *    FA_ERR_BOUNDS, instead of a memory fault.
+ * fa_debug_flags returns which checks the loaded library has (0 in release builds).
+ * fa_test_arm_row_shift(rows) is the test hook of the bounds check: the next
+ * two-tile forward launch adds `rows` to every row it stores, so that rows at or
+ * past the end of the output are refused and reported. Release builds ignore the
+ * shift.
+ */
+#define FA_DEBUG_SERIALIZE_FLAG 1
+#define FA_DEBUG_BOUNDS_FLAG 2
+int32_t fa_debug_flags(void);
+void fa_test_arm_row_shift(int64_t rows);
 
 #ifdef __cplusplus
 }

@@ -203,3 +203,8 @@ def test_splitkv_workspace_must_be_32_byte_aligned(lib):
             0, 0, 4]
     assert lib.fa_forward_splitkv(*args, 0x700010, 1 << 24, None) == fa.FA_ERR_INVALID_ARG
     assert lib.fa_forward_splitkv(*args, 0x700008, 1 << 24, None) == fa.FA_ERR_INVALID_ARG
+
+
+def test_release_build_has_no_debug_checks(lib):
+    assert lib.fa_debug_flags() == 0
+    lib.fa_test_arm_row_shift(0)  # accepted (and ignored) by release builds

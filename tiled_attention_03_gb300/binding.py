@@ -16,7 +16,8 @@ import torch
 
 from .build import INCLUDE, LIB
 
-FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT, FA_ERR_BOUNDS = range(6)
+FA_DEBUG_SERIALIZE_FLAG, FA_DEBUG_BOUNDS_FLAG = 1, 2
 FA_MASK_NONE, FA_MASK_CAUSAL, FA_MASK_WINDOW = range(3)
 FA_DTYPE_FP16, FA_DTYPE_BF16 = range(2)
 
@@ -39,6 +40,13 @@ def load_library(path: str = LIB) -> ctypes.CDLL:
     global _lib
     if _lib is not None:
         return _lib
+    _lib = load_library_at(path)
+    return _lib
+
+
+def load_library_at(path: str) -> ctypes.CDLL:
+    """Load a build of the library at `path` (for example a debug build) with its
+    argument types declared, without replacing the one the binding uses."""
     if not os.path.exists(path):
         raise RuntimeError(f"CUDA library not built: {path} is missing (run __graft_entry__.build())")
     lib = ctypes.CDLL(path)
@@ -99,7 +107,10 @@ def load_library(path: str = LIB) -> ctypes.CDLL:
     lib.fa_launch_count.argtypes = []
     lib.fa_test_arm_fault.restype = None
     lib.fa_test_arm_fault.argtypes = [ctypes.c_int32]
-    _lib = lib
+    lib.fa_test_arm_row_shift.restype = None
+    lib.fa_test_arm_row_shift.argtypes = [ctypes.c_int64]
+    lib.fa_debug_flags.restype = ctypes.c_int32
+    lib.fa_debug_flags.argtypes = []
     return lib
 
 

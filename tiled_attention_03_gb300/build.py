@@ -28,10 +28,18 @@ def _deps():
         sorted(glob.glob(os.path.join(INCLUDE, "*.h"))) + [os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+# Debug builds (never the default; see include/fa.h): the extra compile flags and the
+# file each one is built to.
+DEBUG_BUILDS = {
+    "serialize": (["-DFA_DEBUG_SERIALIZE"], os.path.join(PKG, "libfa_debug_serialize.so")),
+    "bounds": (["-DFA_DEBUG_BOUNDS"], os.path.join(PKG, "libfa_debug_bounds.so")),
+}
+
+
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
@@ -40,15 +48,17 @@ def nvcc() -> str:
     return cand if os.path.exists(cand) else "nvcc"
 
 
-def build_library(force: bool = False, verbose: bool = False) -> str:
-    """Compile each translation unit in parallel, then link the shared library."""
-    if not force and up_to_date():
-        return LIB
-    tag = f".tmp{os.getpid()}"
+def build_library(force: bool = False, verbose: bool = False, debug: str | None = None) -> str:
+    """Compile each translation unit in parallel, then link the shared library
+    (with debug = "serialize" or "bounds": that debug build, to its own file)."""
+    extra, lib = DEBUG_BUILDS[debug] if debug else ([], LIB)
+    if not force and up_to_date(lib):
+        return lib
+    tag = f".tmp{os.getpid()}" + (f"_{debug}" if debug else "")
     objs, procs = [], []
     for src in _sources():
         obj = os.path.join(CSRC, os.path.basename(src)[:-3] + tag + ".o")
-        cmd = [nvcc(), *NVCC_FLAGS, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
+        cmd = [nvcc(), *NVCC_FLAGS, *extra, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd))
         objs.append(obj)
@@ -57,17 +67,17 @@ def build_library(force: bool = False, verbose: bool = False) -> str:
     try:
         if any(failed):
             raise subprocess.CalledProcessError(max(failed), "nvcc")
-        tmp = LIB + tag
+        tmp = lib + tag
         cmd = [nvcc(), "-shared", "-gencode", "arch=compute_103a,code=sm_103a", *objs, "-o", tmp]
         if verbose:
             print(" ".join(cmd))
         subprocess.check_call(cmd)
-        os.replace(tmp, LIB)
+        os.replace(tmp, lib)
     finally:
         for o in objs:
             if os.path.exists(o):
                 os.remove(o)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

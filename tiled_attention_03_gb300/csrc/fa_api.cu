@@ -52,6 +52,9 @@ constexpr uint64_t kDefaultBudgetNs = 2000000000ull;
 std::atomic<int64_t> g_launches{0};
 std::atomic<uint64_t> g_sched_next{0};
 std::atomic<int> g_fault_pos{-1};
+// Debug builds with bounds checks: rows added to every stored row of the next
+// two-tile forward launch (fa_test_arm_row_shift); 0 = none.
+std::atomic<long long> g_row_shift{0};
 std::atomic<uint64_t> g_budget_ns{0};
 
 struct DeviceState {
@@ -654,6 +657,8 @@ fa_status run_forward(const Call &c) {
     p.fault_skip_k = g_fault_pos.exchange(-1);
     p.sched = ds->sched + 2 * (g_sched_next.fetch_add(1) % kSchedSlots);
     p.n_spaces = static_cast<int>(spaces);
+    p.out_rows = static_cast<long long>(BH) * Nq;
+    p.row_shift = g_row_shift.exchange(0);
 
     // Persistent grid: one CTA per SM (each holds the SM's whole tensor memory).
     const int64_t blocks = n_units < ds->sm_count ? n_units : ds->sm_count;
@@ -872,6 +877,8 @@ fa_status run_forward_varlen(const VarlenCall &c) {
     p.cu_k = c.cu_k;
     p.total_q = static_cast<int>(c.total_q);
     p.total_k = static_cast<int>(c.total_k);
+    p.out_rows = static_cast<long long>(c.total_q) * H;
+    p.row_shift = g_row_shift.exchange(0);
 
     const int64_t blocks = n_units < ds->sm_count ? n_units : ds->sm_count;
     cudaStream_t st = static_cast<cudaStream_t>(c.stream);
@@ -936,6 +943,7 @@ const char *fa_status_string(fa_status s) {
         case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: not supported by this build or device";
         case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call failed";
         case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a bounded in-kernel wait ran out";
+        case FA_ERR_BOUNDS: return "FA_ERR_BOUNDS: a debug build's kernel refused an out-of-range store";
     }
     return "unknown fa_status";
 }
@@ -945,6 +953,13 @@ void fa_set_wait_budget_ns(uint64_t ns) { g_budget_ns.store(ns); }
 int64_t fa_launch_count(void) { return g_launches.load(); }
 
 void fa_test_arm_fault(int32_t kv_position) { g_fault_pos.store(kv_position < 0 ? -1 : kv_position); }
+
+void fa_test_arm_row_shift(int64_t rows) { g_row_shift.store(rows < 0 ? 0 : rows); }
+
+int32_t fa_debug_flags(void) {
+    return (fa::kDebugSerialize ? FA_DEBUG_SERIALIZE_FLAG : 0) |
+           (fa::kDebugBounds ? FA_DEBUG_BOUNDS_FLAG : 0);
+}
 
 fa_status fa_forward_gqa(const void *Q, const void *K, const void *V, void *O, float *LSE,
                          int64_t B, int64_t H, int64_t H_kv, int64_t N, int64_t d, float scale,
@@ -1052,9 +1067,11 @@ fa_status fa_sync_status(void *stream) {
         cudaGetLastError();
         return FA_ERR_CUDA;
     }
-    // The kernels store FA_ERR_TIMEOUT, or FA_ERR_UNSUPPORTED for a shared-memory
-    // layout they cannot use.
-    return st[0] == static_cast<unsigned>(FA_ERR_UNSUPPORTED) ? FA_ERR_UNSUPPORTED : FA_ERR_TIMEOUT;
+    // The kernels store FA_ERR_TIMEOUT, FA_ERR_UNSUPPORTED for a shared-memory
+    // layout they cannot use, or (debug builds with bounds checks) FA_ERR_BOUNDS.
+    if (st[0] == static_cast<unsigned>(FA_ERR_UNSUPPORTED)) return FA_ERR_UNSUPPORTED;
+    if (st[0] == static_cast<unsigned>(FA_ERR_BOUNDS)) return FA_ERR_BOUNDS;
+    return FA_ERR_TIMEOUT;
 }
 
 }  // extern "C"

@@ -139,6 +139,10 @@ struct FwdParams {
     float scale_log2; // scale * log2(e)
     unsigned long long wait_budget_ns;
     unsigned int *status;  // [code, role, unit, block]
+    // Debug builds with FA_DEBUG_BOUNDS: rows of O / LSE (and of each split's part
+    // buffers), and a test shift added to every stored row (0 unless armed).
+    long long out_rows;
+    long long row_shift;
     int fault_skip_k;      // test hook: every CTA skips the K load at this ring position (-1: none)
     // Variable-length batches (kernel template flag): sequence b holds query tokens
     // cu_q[b] .. cu_q[b+1]-1 and keys cu_k[b] .. cu_k[b+1]-1 of token-major tensors
@@ -151,6 +155,26 @@ struct FwdParams {
     unsigned int *sched;   // this launch's {next unit, finished CTAs} counters (zero at launch)
 };
 
+// Debug builds (never the default):
+//  * FA_DEBUG_SERIALIZE: the least overlap the kernel's protocol allows, to expose
+//    ordering mistakes: K/V rings two deep (the minimum: an iteration reads two
+//    tiles), the next unit claimed only with the current unit's last K/V tile,
+//    and every group of MMAs completed before the next one is issued.
+//  * FA_DEBUG_BOUNDS: every store of O, LSE and the split buffers is checked against
+//    the output's rows first; an out-of-range row is not stored, and the first one
+//    is recorded in the status word (code 5, FA_ERR_BOUNDS) instead of faulting.
+#ifdef FA_DEBUG_SERIALIZE
+constexpr bool kDebugSerialize = true;
+#else
+constexpr bool kDebugSerialize = false;
+#endif
+#ifdef FA_DEBUG_BOUNDS
+constexpr bool kDebugBounds = true;
+#else
+constexpr bool kDebugBounds = false;
+#endif
+constexpr unsigned kStatusBounds = 5;  // same value as FA_ERR_BOUNDS
+
 #ifndef FA_KSTAGES_128
 #define FA_KSTAGES_128 2
 #endif
@@ -162,8 +186,8 @@ struct SmemLayout {
     // K and V ring depths. The footprint stays above half of the SM's shared
     // memory, so one CTA (holding all 512 TMEM columns) runs per SM. K_j is
     // needed a whole softmax earlier than V_j, so its ring is the deeper one.
-    static constexpr int kStagesK = D == 128 ? FA_KSTAGES_128 : 4;
-    static constexpr int kStagesV = D == 128 ? FA_VSTAGES_128 : 4;
+    static constexpr int kStagesK = kDebugSerialize ? 2 : D == 128 ? FA_KSTAGES_128 : 4;
+    static constexpr int kStagesV = kDebugSerialize ? 2 : D == 128 ? FA_VSTAGES_128 : 4;
     static constexpr int kTileBytes = kBM * D * 2;
     static constexpr int kQ = 0;
     static constexpr int kK = kQ + kQTiles * kTileBytes;
@@ -196,7 +220,8 @@ enum : int {
     kBarDrain = kBarOFree + kQTiles,
     kBarUnitFull = kBarDrain + 1,           // + slot
     kBarUnitEmpty = kBarUnitFull + 2,       // + slot
-    kNumBarsUsed = kBarUnitEmpty + 2,
+    kBarSerial = kBarUnitEmpty + 2,         // FA_DEBUG_SERIALIZE: completion of each MMA group
+    kNumBarsUsed = kBarSerial + 1,
 };
 
 // A work unit: rows [r0, r0 + 256) of row space rs (global rows rs * R + r)
@@ -496,6 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(kBarVEmpty + s), 1);
         }
         mbar_init(bar(kBarDrain), 1);
+        mbar_init(bar(kBarSerial), 1);
         for (int k = 0; k < kUnitSlots; ++k) {
             mbar_init(bar(kBarUnitFull + k), 1);
             mbar_init(bar(kBarUnitEmpty + k), kUnitConsumers);
@@ -579,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int j1 = U.j1;
                 for (int j = U.j0; ok && j <= j1; ++j, ++kv_iter) {
                     // claim the next unit after the first two K loads (or at the last one)
-                    if (!claimed && (j == U.j0 + 2 || j == j1)) {
+                    if (!claimed && ((!kDebugSerialize && j == U.j0 + 2) || j == j1)) {
                         claimed = true;
                         u_next = publish(unit_iter + 1);
                         if (!ok) break;
@@ -673,6 +699,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         int pv_count[kQTiles] = {0, 0};   // O_t += P_t V issued so far
         int epi_count[kQTiles] = {0, 0};  // units in which Q tile t had an epilogue
         bool ok = true;
+        int serial_count = 0;  // FA_DEBUG_SERIALIZE: MMA groups waited for
+        // FA_DEBUG_SERIALIZE: the group just issued completes before anything else
+        auto serialize = [&]() {
+            if constexpr (kDebugSerialize) {
+                if (elect_one()) umma_commit(bar(kBarSerial));
+                __syncwarp();
+                ok = ok && wait(kBarSerial, serial_count++ & 1);
+            }
+        };
         // S_t(j) = Q_t K_j^T into TMEM columns t * 128.
         auto issue_s = [&](int t, int st) {
             tc_fence_after();
@@ -690,6 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma_commit(bar(kBarSFull + t));
             }
             __syncwarp();
+            serialize();
         };
         // O_t (+)= P_t V_j, P_t read from TMEM.
         auto issue_pv = [&](int t, int st, bool first) {
@@ -706,11 +742,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
             ++pv_count[t];
+            serialize();
         };
         auto commit = [&](int b) {
             if (elect_one()) umma_commit(bar(b));
             __syncwarp();
         };
+
         for (; ok; ++unit_iter) {
             const int slot = unit_iter % kUnitSlots;
             ok = wait(kBarUnitFull + slot, (unit_iter / kUnitSlots) & 1);
@@ -908,6 +946,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
                 grow = static_cast<size_t>(U.rs) * p.R + (store ? r : 0);
             const float lse = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+            bool store_ok = store;
+            if constexpr (kDebugBounds) {
+                grow += static_cast<size_t>(p.row_shift);
+                if (store && grow >= static_cast<size_t>(p.out_rows)) {
+                    store_ok = false;  // refused: recorded instead of written
+                    if (atomicCAS(p.status, 0u, kStatusBounds) == 0u) {
+                        p.status[1] = static_cast<unsigned>(kRoleSoftmax);
+                        p.status[2] = static_cast<unsigned>(grow);
+                        p.status[3] = blockIdx.x;
+                        __threadfence();
+                    }
+                }
+            }
             if (p.part_O == nullptr) {
                 // O / l rounded to 16 bit, and LSE
                 uint8_t *orow = reinterpret_cast<uint8_t *>(p.O) + grow * (D * 2);
@@ -921,12 +972,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int e = 0; e < 16; ++e)
                         pk[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l,
                                             __uint_as_float(o[2 * e + 1]) * inv_l);
-                    if (store) {
+                    if (store_ok) {
                         st_global_v8(orow + c * 64, pk);
                         st_global_v8(orow + c * 64 + 32, pk + 8);
                     }
                 }
-                if (store) p.LSE[grow] = lse;
+                if (store_ok) p.LSE[grow] = lse;
             } else {
                 // key split: the split's own O / l in fp32 and its LSE, merged later
                 const size_t prow = static_cast<size_t>(U.split) * p.BH * p.Nq + grow;
@@ -936,7 +987,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t o[32];
                     tmem_ld32(tO + c * 32, o);
                     tmem_ld_wait(o);
-                    if (store) {
+                    if (store_ok) {
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
                             o[e] = __float_as_uint(__uint_as_float(o[e]) * inv_l);
@@ -944,7 +995,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int q = 0; q < 4; ++q) st_global_v8(orow + c * 32 + q * 8, o + q * 8);
                     }
                 }
-                if (store) p.part_LSE[prow] = lse;
+                if (store_ok) p.part_LSE[prow] = lse;
             }
             tc_fence_before();
             mbar_arrive(bar(kBarOFree + t));
