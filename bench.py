@@ -43,6 +43,8 @@ KERNEL_SOURCES = {
     "fwd1t": (CSRC + "fa_fwd1t_kernel.cuh", CSRC + "fa_combine.cuh", CSRC + "fa_mask.cuh",
               CSRC + "ptx.cuh"),
     "bwd": (CSRC + "fa_bwd_kernel.cuh", CSRC + "fa_mask.cuh", CSRC + "ptx.cuh"),
+    "bwd256": (CSRC + "fa_bwd256_kernel.cuh", CSRC + "fa_bwd_kernel.cuh", CSRC + "fa_mask.cuh",
+               CSRC + "ptx.cuh"),
 }
 TRAFFIC_DIR = os.path.join(ROOT, "profiles")
 
@@ -84,7 +86,7 @@ def one_tile(w, sms: int | None = None) -> bool:
 
 def kernel_family(w, sms: int | None = None) -> str:
     if w.backward:
-        return "bwd"
+        return "bwd256" if w.d == 256 else "bwd"
     return "fwd1t" if one_tile(w, sms) else "fwd"
 
 
@@ -704,8 +706,9 @@ def main():
                           "frac": nbytes / (kernel_ms * 1e-3) / 1e9 / peak_gbs,
                           "peak_source": f"{peak_src} copy bandwidth"}) | {
                 "traffic": traffic, "algorithmic_bytes": nbytes,
-                "kernel": (f"fa_bwd prep + dK/dV + dQ kernels <{w.d}, {w.dtype_name}"
-                           + (", varlen>" if w.varlen else ">") if w.backward
+                "kernel": ((f"fa_bwd prep + dV, dK, dQ passes <256, {w.dtype_name}>" if w.d == 256
+                            else f"fa_bwd prep + dK/dV + dQ kernels <{w.d}, {w.dtype_name}"
+                            + (", varlen>" if w.varlen else ">")) if w.backward
                            else (f"fa_fwd1t_kernel<{w.d}, {w.dtype_name}, varlen>" if w.d == 256
                                  else f"fa_fwd_kernel<{w.d}, {w.dtype_name}, varlen>") if w.varlen
                            else (f"fa_fwd1t_kernel<{w.d}, {w.dtype_name}>" if one_tile(w)

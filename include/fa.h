@@ -63,8 +63,8 @@ typedef enum { FA_DTYPE_FP16 = 0, FA_DTYPE_BF16 = 1 } fa_dtype;
  *           forward call. d = 256 runs on a kernel with one 128-row Q tile per unit,
  *           as do d = 64 and 128 when a head's queries, or the queries of one K/V
  *           head's query heads, fit in one tile, and small unsplit problems (whose
- *           256-row units would fill at most half of the SMs). fa_backward and
- *           fa_backward_varlen take 32, 64 and 128.
+ *           256-row units would fill at most half of the SMs). fa_backward takes
+ *           32, 64, 128 and 256, fa_backward_varlen 32, 64 and 128.
  * scale   : multiplier of the logits, finite and > 0 (typically 1/sqrt(d)).
  * mask_mode, window_left, window_right : see fa_mask_mode. The window
  *           arguments are read only for FA_MASK_WINDOW and must then be >= 0
@@ -269,9 +269,13 @@ fa_status fa_forward_host(const void *Q, const void *K, const void *V, void *O, 
  * the workspace overlap no input and no other output. The results are
  * deterministic: no atomics, fixed summation order.
  *
+ * d is 32, 64, 128 or 256. At d = 256 each gradient has its own pass (a 128 x 256
+ * tile of each operand and both accumulators do not fit one SM's shared and
+ * tensor memory): four launches (row terms, dV, dK, dQ) instead of three.
+ *
  * Errors: as fa_forward, plus FA_ERR_INVALID_ARG for a missing or small
  * workspace. Asynchronous on `stream` (three kernel launches: row terms, dK/dV,
- * dQ); timeouts are reported by fa_sync_status.
+ * dQ; four at d = 256); timeouts are reported by fa_sync_status.
  */
 fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O, const void *dO,
                       const float *LSE, void *dQ, void *dK, void *dV, int64_t B, int64_t H,

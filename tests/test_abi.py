@@ -123,7 +123,7 @@ def test_backward_invalid_arguments(lib, kw):
     assert bwd_call(lib, **kw) == fa.FA_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("d", [16, 96, 256])
+@pytest.mark.parametrize("d", [16, 96, 512])
 def test_backward_unsupported_head_dim(lib, d):
     assert bwd_call(lib, d=d) == fa.FA_ERR_UNSUPPORTED
 

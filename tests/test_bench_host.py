@@ -100,6 +100,7 @@ def test_kernel_family_follows_the_forward_dispatch():
                  "full_b4h16n4096d256", "causal_b4h16n4096d256"):
         assert fam(name) == "fwd1t", name
     assert fam("bwd_b4h32n4096d128") == "bwd"
+    assert fam("bwd_b4h16n4096d256") == "bwd256"
     base = BY_NAME["full_b4h32n4096d128"]
     cut = lambda **kw: bench.kernel_family(dataclasses.replace(base, **kw), sms=152)
     assert cut(B=40, H=4, N=128) == "fwd1t" and cut(B=40, H=4, N=129) == "fwd"

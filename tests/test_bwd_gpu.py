@@ -74,7 +74,7 @@ def compare(q, k, v, do, scale, mask, window, dq, dk, dv, kv_heads=None):
 
 
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
-@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("d", [32, 64, 128, 256])
 @pytest.mark.parametrize("N", [1, 63, 128, 129, 300])
 @pytest.mark.parametrize("mask,window", [("none", (0, 0)), ("causal", (0, 0)), ("window", (70, 5))])
 def test_bwd_parity(mask, window, N, d, dtype):
@@ -107,11 +107,36 @@ def test_bwd_long_sampled():
     compare(q, k, v, do, d ** -0.5, "causal", (0, 0), dq, dk, dv, kv_heads=[1])
 
 
-def test_bwd_deterministic():
+@pytest.mark.parametrize("Hk", [1, 2])
+@pytest.mark.parametrize("mask,window", [("none", (0, 0)), ("causal", (0, 0)), ("window", (200, 30))])
+def test_bwd_d256_gqa(mask, window, Hk):
+    """Head dimension 256 (its own three-pass kernels): grouped K/V heads, 64-row
+    streamed tiles crossing 128-row blocks, a ragged last block."""
+    B, H, N, d = 2, 4, 333, 256
+    q, _, _ = make_qkv(B, H, N, d, torch.bfloat16, seed=31)
+    _, k, v = make_qkv(B, Hk, N, d, torch.bfloat16, seed=32, H_kv=Hk)
+    do = make_qkv(B, H, N, d, torch.bfloat16, seed=33)[0]
+    dq, dk, dv = run_bwd(q, k, v, do, d ** -0.5, mask, window)
+    compare(q, k, v, do, d ** -0.5, mask, window, dq, dk, dv)
+
+
+def test_bwd_d256_long_sampled():
+    """d = 256 with many streamed tiles per unit (1024 positions, causal, 2 query heads
+    per K/V head), checked on one K/V head."""
+    B, H, Hk, N, d = 1, 4, 2, 1024, 256
+    q, _, _ = make_qkv(B, H, N, d, torch.float16, seed=34)
+    _, k, v = make_qkv(B, Hk, N, d, torch.float16, seed=35, H_kv=Hk)
+    do = make_qkv(B, H, N, d, torch.float16, seed=36)[0]
+    dq, dk, dv = run_bwd(q, k, v, do, d ** -0.5, "causal")
+    compare(q, k, v, do, d ** -0.5, "causal", (0, 0), dq, dk, dv, kv_heads=[0])
+
+
+@pytest.mark.parametrize("d", [64, 256])
+def test_bwd_deterministic(d):
     """dQ, dK and dV are accumulated in tensor memory in a fixed order, without
     atomics: reruns are bit-identical."""
-    q, k, v = make_qkv(1, 4, 500, 64, torch.float16, seed=12)
-    do = make_qkv(1, 4, 500, 64, torch.float16, seed=13)[0]
+    q, k, v = make_qkv(1, 4, 500, d, torch.float16, seed=12)
+    do = make_qkv(1, 4, 500, d, torch.float16, seed=13)[0]
     a = run_bwd(q, k, v, do, 0.125, "causal")
     b = run_bwd(q, k, v, do, 0.125, "causal")
     assert all(torch.equal(x, y) for x, y in zip(a, b))

@@ -918,8 +918,9 @@ bool aligned32(const void *p) { return ::aligned32(p); }
 bool aligned4(const void *p) { return ::aligned4(p); }
 bool overlaps(const void *a, size_t na, const void *b, size_t nb) { return ::overlaps(a, na, b, nb); }
 bool on_device(const void *p, int dev) { return ::on_device(p, dev); }
-bool make_map(CUtensorMap *map, const void *base, bool bf16, int64_t BH, int64_t N, int64_t d) {
-    return ::make_map(map, base, bf16, BH, N, d);
+bool make_map(CUtensorMap *map, const void *base, bool bf16, int64_t BH, int64_t N, int64_t d,
+              uint32_t box_rows) {
+    return ::make_map(map, base, bf16, BH, N, d, box_rows);
 }
 uint64_t wait_budget() { return ::wait_budget(); }
 bool make_map_tokens(CUtensorMap *map, const void *base, bool bf16, int64_t tokens, int64_t heads,

@@ -1,0 +1,598 @@
+// fa_bwd256_kernel.cuh -- attention backward at head dimension 256 on sm_103a.
+//
+// Same method as fa_bwd_kernel.cuh: the scores and probabilities are recomputed
+// block by block from the forward's saved row statistics instead of storing P
+// ("ai6s.net/6af30f4d40858c2d8819b6d5" §2.4). With L_i = LSE_i log2(e) and
+// D_i = sum_c dO_ic O_ic (both from the prep kernel of fa_bwd_kernel.cuh):
+//     P_ij = 2^(s_ij scale log2(e) - L_i)      dP_ij = dO_i . V_j
+//     dS_ij = P_ij (dP_ij - D_i)
+//     dQ_i = scale sum_j dS_ij K_j    dK_j = scale sum_i dS_ij Q_i    dV_j = sum_i P_ij dO_i
+//
+// Why a kernel of its own. At d = 256 a 128 x 256 16-bit tile is 64 KB and a
+// 128 x 256 fp32 accumulator takes 256 of the SM's 512 tensor-memory columns, so
+// the d <= 128 layout (K_j, V_j, Q_i and dO_i tiles in shared memory, dK_j and dV_j
+// both in TMEM) would need 256 KB and 768 columns. Here each gradient has its own
+// pass. A pass keeps the 128 rows it accumulates for (its "resident" tiles) in
+// shared memory and streams the other side in tiles of 64 rows:
+//   dQ pass: rows = 128 queries; Q_i, dO_i, L_i, D_i resident; K_j, V_j streamed.
+//            X = Q_i K_j^T, Y = dO_i V_j^T, A = P (Y - D), dQ_i += A K_j.
+//   dK pass: rows = 128 keys; K_j, V_j resident; Q_i (+ L), dO_i (+ D) streamed.
+//            X = K_j Q_i^T, Y = V_j dO_i^T, A = P^T (Y - D), dK_j += A Q_i.
+//   dV pass: rows = 128 keys; K_j resident; Q_i (+ L), dO_i streamed.
+//            X = K_j Q_i^T, A = P^T, dV_j += A dO_i.
+// X and Y are M = 128, N = 64, K = 256 products (K-major operands in shared
+// memory); A is written by the compute warps as 16-bit pairs into TMEM over X's
+// columns and the accumulation is an M = 128, N = 256, K = 64 product with A from
+// TMEM and B (the streamed tile, 64 rows of 256 columns) MN-major. The scores are
+// recomputed once per pass (S three times in all, against twice in the d <= 128
+// kernels), the price of fitting one SM.
+//
+// Warps (192 threads): 0-3 compute (thread = resident row = TMEM lane), 4 TMA
+// producer and scheduler, 5 MMA issuer. Units come from a launch-wide counter (a
+// CTA's first unit is its own index). Every wait is bounded (global-timer budget);
+// on expiry the CTA records the failure in the status word, drains its copies and
+// MMAs, frees its tensor memory and returns.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+#include "fa_mask.cuh"
+#include "ptx.cuh"
+
+namespace fa {
+namespace bwd256 {
+
+constexpr int kD = 256;
+constexpr int kRows = 128;    // resident rows (TMEM lanes)
+constexpr int kCols = 64;     // rows of a streamed tile = columns of X and Y
+constexpr int kThreads = 192;
+constexpr int kTmaWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr uint32_t kTmemCols = 512;
+constexpr unsigned kStatusTimeout = 4;  // FA_ERR_TIMEOUT
+enum : int { kRoleCompute = 1, kRoleTma = 2, kRoleMma = 3 };
+enum : int { kPassDQ = 0, kPassDK = 1, kPassDV = 2 };
+
+// 16-bit tiles are stored as regions of 64 columns (128 bytes per row, the 128-byte
+// swizzle TMA writes): 4 regions per 256-column row.
+constexpr int kRegions = kD / 64;
+constexpr int kResRegion = kRows * 128;  // 16 KB
+constexpr int kStrRegion = kCols * 128;  // 8 KB
+constexpr int kResBytes = kRegions * kResRegion;  // 64 KB
+constexpr int kStrBytes = kRegions * kStrRegion;  // 32 KB
+constexpr int kVecSlots = 3;  // ring of the streamed tiles' row-term vectors (see the producer)
+
+// TMEM columns: X (fp32, 64), then A (16-bit pairs) over its first 32; Y (fp32, 64);
+// the accumulator (fp32, 256).
+constexpr uint32_t kTmemX = 0;
+constexpr uint32_t kTmemY = 64;
+constexpr uint32_t kTmemAcc = 256;
+
+template <int PASS>
+struct Layout {
+    // The second resident tile (dO_i in the dQ pass, V_j in the dK pass).
+    static constexpr bool kRes1 = PASS != kPassDV;
+    // Ring depths of the two streamed tiles: s0 (K_j in the dQ pass, Q_i in the
+    // others) and s1 (V_j, or dO_i), as deep as shared memory allows.
+    static constexpr int kS0 = PASS == kPassDV ? 3 : 2;
+    static constexpr int kS1 = PASS == kPassDV ? 2 : 1;
+    static constexpr int kRes0 = 0;
+    static constexpr int kRes1Off = kRes0 + kResBytes;
+    static constexpr int kStr0 = kRes1Off + (kRes1 ? kResBytes : 0);
+    static constexpr int kStr1 = kStr0 + kS0 * kStrBytes;
+    static constexpr int kVec = kStr1 + kS1 * kStrBytes;  // dQ: L_i, D_i (2 x 128); else L, D rings
+    static constexpr int kVecBytes = PASS == kPassDQ ? 2 * kRows * 4 : 2 * kVecSlots * kCols * 4;
+    static constexpr int kBar = kVec + kVecBytes;
+    static constexpr int kNumBars = 24;
+    static constexpr int kMisc = kBar + kNumBars * 8;  // tmem slot, abort flag, unit ring
+    static constexpr int kBytes = kMisc + 16;
+    static constexpr int kAlloc = kBytes + 1024;       // slack to align the base to 1024 B
+    static_assert(kAlloc <= 232448, "shared memory per CTA");
+};
+
+enum : int {
+    kBarResFull = 0,
+    kBarResEmpty = 1,
+    kBarS0Full = 2,                  // + slot (<= 3)
+    kBarS0Empty = kBarS0Full + 3,    // + slot
+    kBarS1Full = kBarS0Empty + 3,    // + slot (<= 2)
+    kBarS1Empty = kBarS1Full + 2,    // + slot
+    kBarXFull = kBarS1Empty + 2,
+    kBarYFull = kBarXFull + 1,
+    kBarAReady = kBarYFull + 1,
+    kBarAccDone = kBarAReady + 1,
+    kBarAccFree = kBarAccDone + 1,
+    kBarUnitFull = kBarAccFree + 1,  // + slot (2)
+    kBarUnitEmpty = kBarUnitFull + 2,
+    kBarDrain = kBarUnitEmpty + 2,
+    kNumBarsUsed = kBarDrain + 1,
+};
+static_assert(kNumBarsUsed <= Layout<0>::kNumBars, "barrier slots");
+constexpr int kUnitSlots = 2;
+constexpr int kUnitConsumers = 5;  // the MMA warp and the 4 compute warps
+
+struct Params {
+    void *out;                // dQ (B*H x N x 256), dK or dV (B*H_kv x N x 256), 16-bit
+    const float *Lw, *Dw;     // B*H x Npad row terms (prep kernel)
+    int N, Npad;              // queries = keys per head; N rounded up to 128
+    int H, Hkv, group;        // query heads, K/V heads, H / H_kv
+    int n_blk;                // 128-row blocks per head
+    int n_units;
+    int wl, wr;               // key j visible to query i iff i - wl <= j <= i + wr
+    float scale_log2, out_scale;
+    unsigned long long wait_budget_ns;
+    unsigned int *status;     // [code, role, unit, block]
+    unsigned int *sched;      // this launch's {next unit, finished CTAs} (zero at launch)
+    int fault_unit;           // test hook: every CTA skips its resident load of this unit (-1: none)
+};
+
+// A unit: 128 resident rows r0 .. r0+127 of head `head` (a query head in the dQ
+// pass, a K/V head in the others) and the streamed tiles t = 0 .. n_t-1 that hold a
+// visible pair: tile t is 64-row block lo + t % per of head `head` (dQ pass), or of
+// query head group_head(head, t / per) (dK / dV passes).
+struct Unit {
+    int head, r0, lo, per, n_t;
+};
+
+template <int PASS>
+__device__ __forceinline__ Unit decode(int u, const Params &p) {
+    Unit U;
+    U.head = u / p.n_blk;
+    U.r0 = (u - U.head * p.n_blk) * kRows;
+    const int r1 = min(U.r0 + kRows, p.N) - 1;
+    // dQ: rows are queries, streamed rows keys; dK / dV: the other way round.
+    const int lo = PASS == kPassDQ ? max(0, U.r0 - p.wl) : max(0, U.r0 - p.wr);
+    const int hi = PASS == kPassDQ ? min(p.N - 1, r1 + p.wr) : min(p.N - 1, r1 + p.wl);
+    U.lo = lo / kCols;
+    U.per = hi / kCols - U.lo + 1;
+    U.n_t = (PASS == kPassDQ ? 1 : p.group) * U.per;
+    return U;
+}
+
+// Head of the streamed tile t: the unit's own (dQ pass), or the query head of the
+// group reading K/V head `head` (dK / dV passes).
+template <int PASS>
+__device__ __forceinline__ void tile_of(const Unit &U, int t, const Params &p, int &head, int &row0) {
+    const int g = t / U.per;
+    row0 = (U.lo + (t - g * U.per)) * kCols;
+    if constexpr (PASS == kPassDQ) {
+        head = U.head / p.H * p.Hkv + (U.head % p.H) / p.group;  // K/V head of query head U.head
+    } else {
+        const int b = U.head / p.Hkv, hk = U.head - b * p.Hkv;
+        head = b * p.H + hk * p.group + g;
+    }
+}
+
+__device__ __forceinline__ void record_timeout(const Params &p, volatile int *abort_flag, int role,
+                                               int unit) {
+    *abort_flag = 1;
+    if (atomicCAS(p.status, 0u, kStatusTimeout) == 0u) {
+        p.status[1] = static_cast<unsigned>(role);
+        p.status[2] = static_cast<unsigned>(unit);
+        p.status[3] = blockIdx.x;
+        __threadfence();
+    }
+}
+
+// The resident tiles are read through a 128-row TMA map of their tensor, the
+// streamed ones through a 64-row map: tmR0 / tmR1 (Q / dO in the dQ pass, K / V
+// otherwise) and tmS0 / tmS1 (K / V in the dQ pass, Q / dO otherwise).
+template <int PASS, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_bwd256_kernel(const __grid_constant__ CUtensorMap tmR0, const __grid_constant__ CUtensorMap tmR1,
+                     const __grid_constant__ CUtensorMap tmS0, const __grid_constant__ CUtensorMap tmS1,
+                     const Params p) {
+    using L = Layout<PASS>;
+    constexpr int kS0 = L::kS0, kS1 = L::kS1;
+    constexpr bool kHasY = PASS != kPassDV;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sR0 = sbase + L::kRes0, sR1 = sbase + L::kRes1Off;
+    auto sS0 = [sbase](int it) { return sbase + L::kStr0 + (it % kS0) * kStrBytes; };
+    auto sS1 = [sbase](int it) { return sbase + L::kStr1 + (it % kS1) * kStrBytes; };
+    // row-term vectors: dQ pass L_i, D_i (128 each); dK / dV passes the L (and D) of
+    // each streamed tile's 64 rows in a ring of kVecSlots
+    float *vec = reinterpret_cast<float *>(smem + L::kVec);
+    const uint32_t sVec = sbase + L::kVec;
+    const uint32_t bar0 = sbase + L::kBar;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
+    volatile int *unit_ring = reinterpret_cast<volatile int *>(smem + L::kMisc + 8);
+    auto bar = [bar0](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint64_t budget = p.wait_budget_ns;
+
+    // ---- setup
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == kTmaWarp * 32) {
+        mbar_init(bar(kBarResFull), 1);
+        mbar_init(bar(kBarResEmpty), 1);
+        for (int s = 0; s < kS0; ++s) {
+            mbar_init(bar(kBarS0Full + s), 1);
+            mbar_init(bar(kBarS0Empty + s), 1);
+        }
+        for (int s = 0; s < kS1; ++s) {
+            mbar_init(bar(kBarS1Full + s), 1);
+            mbar_init(bar(kBarS1Empty + s), 1);
+        }
+        mbar_init(bar(kBarXFull), 1);
+        mbar_init(bar(kBarYFull), 1);
+        mbar_init(bar(kBarAReady), 128);
+        mbar_init(bar(kBarAccDone), 1);
+        mbar_init(bar(kBarAccFree), 128);
+        for (int k = 0; k < kUnitSlots; ++k) {
+            mbar_init(bar(kBarUnitFull + k), 1);
+            mbar_init(bar(kBarUnitEmpty + k), kUnitConsumers);
+        }
+        mbar_init(bar(kBarDrain), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmR0);
+        if constexpr (L::kRes1) tma_prefetch_desc(&tmR1);
+        tma_prefetch_desc(&tmS0);
+        tma_prefetch_desc(&tmS1);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    // Consumers take each unit id from the ring (id -1 ends their loop).
+    auto take_unit = [&](int unit_iter, bool &ok) -> int {
+        const int slot = unit_iter % kUnitSlots;
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarUnitFull + slot),
+                                                       (unit_iter / kUnitSlots) & 1, abort_flag, budget));
+        if (!ok) return -1;
+        const int u = unit_ring[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarUnitEmpty + slot));
+        return u;
+    };
+
+    if (warp == kTmaWarp) {
+        // ================================================================ TMA producer
+        if (lane == 0) {
+            int it = 0, unit_iter = 0, res_loads = 0;
+            bool ok = true;
+            auto publish = [&](int k) -> int {
+                const int slot = k % kUnitSlots;
+                ok = mbar_wait_bounded(bar(kBarUnitEmpty + slot), ((k / kUnitSlots) & 1) ^ 1,
+                                       abort_flag, budget);
+                if (!ok) return -1;
+                // a CTA's first unit is its own index (the grid never exceeds the unit
+                // count); the counter numbers the rest from gridDim.x on
+                const unsigned next = k == 0 ? blockIdx.x : gridDim.x + atomicAdd(p.sched, 1u);
+                const int v = next < static_cast<unsigned>(p.n_units) ? static_cast<int>(next) : -1;
+                unit_ring[slot] = v;
+                mbar_arrive(bar(kBarUnitFull + slot));
+                return v;
+            };
+            int u = publish(0);
+            for (; ok && u >= 0; ++unit_iter) {
+                const Unit U = decode<PASS>(u, p);
+                // resident tiles (and, in the dQ pass, their rows' L and D)
+                ok = mbar_wait_bounded(bar(kBarResEmpty), (unit_iter & 1) ^ 1, abort_flag, budget);
+                if (!ok) break;
+                if (unit_iter != p.fault_unit) {
+                    constexpr uint32_t kResTx =
+                        (L::kRes1 ? 2 : 1) * kResBytes + (PASS == kPassDQ ? 2 * kRows * 4 : 0);
+                    mbar_arrive_expect_tx(bar(kBarResFull), kResTx);
+                    for (int g = 0; g < kRegions; ++g) {
+                        tma_load_3d(sR0 + g * kResRegion, &tmR0, bar(kBarResFull), 64 * g, U.r0, U.head);
+                        if constexpr (L::kRes1)
+                            tma_load_3d(sR1 + g * kResRegion, &tmR1, bar(kBarResFull), 64 * g, U.r0,
+                                        U.head);
+                    }
+                    if constexpr (PASS == kPassDQ) {
+                        const size_t vrow = static_cast<size_t>(U.head) * p.Npad + U.r0;
+                        bulk_load(sVec, p.Lw + vrow, kRows * 4, bar(kBarResFull));
+                        bulk_load(sVec + kRows * 4, p.Dw + vrow, kRows * 4, bar(kBarResFull));
+                    }
+                }
+                ++res_loads;
+                const int u_next = publish(unit_iter + 1);
+                if (!ok) break;
+                for (int t = 0; ok && t < U.n_t; ++t, ++it) {
+                    int head, row0;
+                    tile_of<PASS>(U, t, p, head, row0);
+                    // The L / D vectors of a streamed tile go to slot it % kVecSlots of
+                    // their ring, completing on the tile's barrier. Before writing them
+                    // this thread has waited for s0's slot of tile it - kS0 to be free,
+                    // which the MMA warp signals only after the compute warps finished
+                    // tile it - kS0 (dK pass: after its accumulation; dV pass: after its
+                    // A was ready), so tile it - 3 and every older one are done with
+                    // their vectors.
+                    const size_t vrow = static_cast<size_t>(head) * p.Npad + row0;
+                    const int vs = it % kVecSlots;
+                    int s = it % kS0;
+                    ok = mbar_wait_bounded(bar(kBarS0Empty + s), ((it / kS0) & 1) ^ 1, abort_flag, budget);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar(kBarS0Full + s),
+                                          kStrBytes + (PASS == kPassDQ ? 0 : kCols * 4));
+                    for (int g = 0; g < kRegions; ++g)
+                        tma_load_3d(sS0(it) + g * kStrRegion, &tmS0, bar(kBarS0Full + s), 64 * g, row0, head);
+                    if constexpr (PASS != kPassDQ)
+                        bulk_load(sVec + vs * kCols * 4, p.Lw + vrow, kCols * 4, bar(kBarS0Full + s));
+                    s = it % kS1;
+                    ok = mbar_wait_bounded(bar(kBarS1Empty + s), ((it / kS1) & 1) ^ 1, abort_flag, budget);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar(kBarS1Full + s),
+                                          kStrBytes + (PASS == kPassDK ? kCols * 4 : 0));
+                    for (int g = 0; g < kRegions; ++g)
+                        tma_load_3d(sS1(it) + g * kStrRegion, &tmS1, bar(kBarS1Full + s), 64 * g, row0, head);
+                    if constexpr (PASS == kPassDK)
+                        bulk_load(sVec + (kVecSlots + vs) * kCols * 4, p.Dw + vrow, kCols * 4,
+                                  bar(kBarS1Full + s));
+                }
+                u = u_next;
+            }
+            if (!ok) record_timeout(p, abort_flag, kRoleTma, u);
+            // Drain: no copy may still be landing in shared memory when the CTA exits.
+            if (res_loads > 0)
+                mbar_wait_bounded(bar(kBarResFull), (res_loads - 1) & 1, nullptr, budget);
+            for (int s = 0; s < kS0; ++s)
+                if (it > s) {
+                    const int last = it - 1 - ((it - 1 - s) % kS0);
+                    mbar_wait_bounded(bar(kBarS0Full + s), (last / kS0) & 1, nullptr, budget);
+                }
+            for (int s = 0; s < kS1; ++s)
+                if (it > s) {
+                    const int last = it - 1 - ((it - 1 - s) % kS1);
+                    mbar_wait_bounded(bar(kBarS1Full + s), (last / kS1) & 1, nullptr, budget);
+                }
+        }
+    } else if (warp == kMmaWarp) {
+        // ================================================================ MMA issuer
+        // Per streamed tile t (it counts tiles over the CTA's whole sequence):
+        //   X(t) [, Y(t)] ... acc += A(t) B(t) | X(t+1) [, Y(t+1)] ...
+        // X(t+1) overwrites the A(t) that the accumulation before it reads, and Y(t+1)
+        // the Y(t) the compute warps read before signalling A(t): tcgen05.mma
+        // operations of one thread execute in issue order.
+        constexpr uint32_t idesc_x = idesc_f16_ab(BF16, kRows, kCols, false, false);
+        constexpr uint32_t idesc_acc = idesc_f16_ab(BF16, kRows, kD, false, true);
+        auto wait = [&](int b, uint32_t parity) {
+            return __all_sync(0xffffffffu, mbar_wait_bounded(bar(b), parity, abort_flag, budget));
+        };
+        auto commit = [&](int b) {
+            if (elect_one()) umma_commit(bar(b));
+            __syncwarp();
+        };
+        // C[128 x 64] = A B^T, A the resident tile (128 rows), B a streamed tile (64
+        // rows), both K-major; K-step k reads 16 columns of region k / 4.
+        auto issue_x = [&](uint32_t a_s, uint32_t b_s, uint32_t dcol) {
+            tc_fence_after();
+            const uint64_t da = swz_desc<128>(a_s, 16);
+            const uint64_t db = swz_desc<128>(b_s, 16);
+            if (elect_one()) {
+#pragma unroll
+                for (int k = 0; k < kD / 16; ++k) {
+                    const uint32_t oa = (k / 4) * (kResRegion >> 4) + (k % 4) * 2;
+                    const uint32_t ob = (k / 4) * (kStrRegion >> 4) + (k % 4) * 2;
+                    umma_f16_ss(tmem + dcol, da + oa, db + ob, idesc_x, k > 0 ? 1u : 0u);
+                }
+            }
+            __syncwarp();
+        };
+        // acc[128 x 256] (+)= A[128 x 64] B[64 x 256]: A 16-bit pairs in TMEM over X's
+        // columns, B the streamed tile MN-major (its 64-column regions 8 KB apart,
+        // 16 rows = 2 KB per K-step).
+        auto issue_acc = [&](uint32_t b_s, bool accumulate) {
+            tc_fence_after();
+            const uint64_t db = swz_desc<128>(b_s, kStrRegion);
+            if (elect_one()) {
+#pragma unroll
+                for (int k = 0; k < kCols / 16; ++k)
+                    umma_f16_ts(tmem + kTmemAcc, tmem + kTmemX + 8 * k, db + k * ((16 * 128) >> 4),
+                                idesc_acc, (k > 0 || accumulate) ? 1u : 0u);
+            }
+            __syncwarp();
+        };
+        int it = 0, unit_iter = 0, u = -1;
+        bool ok = true;
+        for (; ok; ++unit_iter) {
+            u = take_unit(unit_iter, ok);
+            if (!ok || u < 0) break;
+            const Unit U = decode<PASS>(u, p);
+            ok = wait(kBarResFull, unit_iter & 1);
+            for (int t = 0; ok && t < U.n_t; ++t, ++it) {
+                const int s0 = it % kS0, s1 = it % kS1;
+                ok = wait(kBarS0Full + s0, (it / kS0) & 1);
+                if (!ok) break;
+                issue_x(sR0, sS0(it), kTmemX);
+                commit(kBarXFull);
+                if constexpr (kHasY) {
+                    ok = wait(kBarS1Full + s1, (it / kS1) & 1);
+                    if (!ok) break;
+                    issue_x(sR1, sS1(it), kTmemY);
+                    commit(kBarYFull);
+                    commit(kBarS1Empty + s1);  // V_j / dO_i: Y was its one reader
+                }
+                ok = wait(kBarAReady, it & 1);
+                if (ok && t == 0 && unit_iter > 0) ok = wait(kBarAccFree, (unit_iter - 1) & 1);
+                if (!ok) break;
+                if constexpr (PASS == kPassDV) {
+                    commit(kBarS0Empty + s0);  // Q_i: X was its one product reader
+                    ok = wait(kBarS1Full + s1, (it / kS1) & 1);
+                    if (!ok) break;
+                    issue_acc(sS1(it), t > 0);  // dV += P^T dO_i
+                    commit(kBarS1Empty + s1);
+                } else {
+                    issue_acc(sS0(it), t > 0);  // dQ += dS K_j, dK += dS^T Q_i
+                    commit(kBarS0Empty + s0);
+                }
+            }
+            if (!ok) break;
+            commit(kBarResEmpty);  // resident tiles free once the unit's products complete
+            commit(kBarAccDone);   // and the accumulator is final
+        }
+        if (!ok && lane == 0) record_timeout(p, abort_flag, kRoleMma, u);
+        // Drain: every MMA this warp issued has completed before TMEM is freed.
+        if (elect_one()) umma_commit(bar(kBarDrain));
+        __syncwarp();
+        if (lane == 0) mbar_wait_bounded(bar(kBarDrain), 0, nullptr, budget);
+        __syncwarp();
+    } else if (warp < 4) {
+        // ================================================================ compute warpgroup
+        const int r = threadIdx.x;  // resident row = TMEM lane
+        const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const float sl2 = p.scale_log2;
+        int it = 0, unit_iter = 0, u = -1;
+        bool ok = true;
+        for (; ok; ++unit_iter) {
+            u = take_unit(unit_iter, ok);
+            if (!ok || u < 0) break;
+            const Unit U = decode<PASS>(u, p);
+            const int row = U.r0 + r;  // query (dQ pass) or key of this thread
+            const bool row_ok = row < p.N;
+            // dQ pass: this row's L and D, resident for the unit
+            float Lrow = 0.f, Drow = 0.f;
+            if constexpr (PASS == kPassDQ) {
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarResFull), unit_iter & 1,
+                                                               abort_flag, budget));
+                if (!ok) break;
+                Lrow = vec[r];
+                Drow = vec[kRows + r];
+            }
+            for (int t = 0; t < U.n_t; ++t, ++it) {
+                int head, c0;
+                tile_of<PASS>(U, t, p, head, c0);  // column c is streamed row c0 + c
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarXFull), it & 1, abort_flag, budget));
+                if (!ok) break;
+                tc_fence_after();
+                float x[kCols];
+                {
+                    uint32_t a[32], b[32];
+                    tmem_ld32(tl + kTmemX, a);
+                    tmem_ld32(tl + kTmemX + 32, b);
+                    tmem_ld_wait(a);
+                    tmem_ld_wait(b);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        x[c] = __uint_as_float(a[c]);
+                        x[c + 32] = __uint_as_float(b[c]);
+                    }
+                }
+                // P = 2^(x scale log2 e - L) with L of the query: the row's (dQ pass) or
+                // the column's (the streamed query rows' L, from the vector ring)
+                const int vs = it % kVecSlots;
+                if constexpr (PASS == kPassDQ) {
+#pragma unroll
+                    for (int c = 0; c < kCols; c += 2) ffma2(x[c], x[c + 1], sl2, sl2, -Lrow, -Lrow);
+                } else {
+                    const float *lv = vec + vs * kCols;
+#pragma unroll
+                    for (int c = 0; c < kCols; c += 4) {
+                        const float4 l4 = *reinterpret_cast<const float4 *>(lv + c);
+                        ffma2(x[c], x[c + 1], sl2, sl2, -l4.x, -l4.y);
+                        ffma2(x[c + 2], x[c + 3], sl2, sl2, -l4.z, -l4.w);
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < kCols; ++c) x[c] = ex2_approx(x[c]);
+                // visible pairs: key j and query i with i - wl <= j <= i + wr, both < N
+                if constexpr (PASS == kPassDQ) {
+                    // row = query, columns = keys c0 + c
+                    mask_outside_run(x, max(0, row - p.wl) - c0, min(p.N - 1, row + p.wr) - c0, 0.f);
+                } else {
+                    // row = key, columns = queries c0 + c
+                    mask_outside_run(x, max(0, row - p.wr) - c0, min(p.N - 1, row + p.wl) - c0, 0.f);
+                    if (!row_ok) {
+#pragma unroll
+                        for (int c = 0; c < kCols; ++c) x[c] = 0.f;
+                    }
+                }
+                if constexpr (kHasY) {
+                    // dS = P (dP - D), D of the query: the row's or the column's
+                    ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarYFull), it & 1, abort_flag, budget));
+                    if (!ok) break;
+                    tc_fence_after();
+                    uint32_t a[32], b[32];
+                    tmem_ld32(tl + kTmemY, a);
+                    tmem_ld32(tl + kTmemY + 32, b);
+                    tmem_ld_wait(a);
+                    tmem_ld_wait(b);
+                    const float *dv = vec + (kVecSlots + vs) * kCols;
+#pragma unroll
+                    for (int c = 0; c < kCols; c += 2) {
+                        const uint32_t *src = c < 32 ? a + c : b + (c - 32);
+                        float y0 = __uint_as_float(src[0]), y1 = __uint_as_float(src[1]);
+                        if constexpr (PASS == kPassDQ) {
+                            fadd2(y0, y1, -Drow, -Drow);
+                        } else {
+                            const float2 d2 = *reinterpret_cast<const float2 *>(dv + c);
+                            fadd2(y0, y1, -d2.x, -d2.y);
+                        }
+                        fmul2(y0, y1, x[c], x[c + 1]);
+                        x[c] = y0;
+                        x[c + 1] = y1;
+                    }
+                }
+                // A as 16-bit pairs over X's first 32 columns
+                {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) pk[e] = pack2<BF16>(x[2 * e], x[2 * e + 1]);
+                    tmem_st16(tl + kTmemX, pk);
+                    tmem_st16(tl + kTmemX + 16, pk + 16);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(bar(kBarAReady));
+            }
+            if (!ok) break;
+            // ---- epilogue: the row of the accumulator times out_scale, in 16 bit
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarAccDone), unit_iter & 1, abort_flag, budget));
+            if (!ok) break;
+            tc_fence_after();
+            {
+                const float f = p.out_scale;
+                uint8_t *out = reinterpret_cast<uint8_t *>(p.out) +
+                               (static_cast<size_t>(U.head) * p.N + (row_ok ? row : 0)) * (kD * 2);
+#pragma unroll 1
+                for (int c = 0; c < kD / 32; ++c) {
+                    uint32_t a[32];
+                    tmem_ld32(tl + kTmemAcc + c * 32, a);
+                    tmem_ld_wait(a);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack2<BF16>(__uint_as_float(a[2 * e]) * f, __uint_as_float(a[2 * e + 1]) * f);
+                    if (row_ok) {
+                        st_global_v8(out + c * 64, pk);
+                        st_global_v8(out + c * 64 + 32, pk + 8);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(kBarAccFree));
+        }
+        if (!ok && lane == 0) record_timeout(p, abort_flag, kRoleCompute, u);
+    }
+
+    // ---- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+    // The last CTA to finish zeroes this launch's scheduler counters for the next
+    // launch that uses them (every CTA has stopped taking units by now).
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+            atomicExch(p.sched, 0u);
+            atomicExch(p.sched + 1, 0u);
+        }
+    }
+}
+
+}  // namespace bwd256
+}  // namespace fa

@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "fa.h"
+#include "fa_bwd256_kernel.cuh"
 #include "fa_bwd_kernel.cuh"
 #include "fa_host.h"
 
@@ -45,6 +46,22 @@ cudaError_t configure_bwd() {
     return e;
 }
 
+// d = 256: the three passes of fa_bwd256_kernel.cuh (192 threads, no setmaxnreg).
+template <bool BF16>
+cudaError_t configure_bwd256() {
+    using namespace fa::bwd256;
+    cudaError_t e = cudaFuncSetAttribute(fa_bwd256_kernel<kPassDQ, BF16>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Layout<kPassDQ>::kAlloc);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fa_bwd256_kernel<kPassDK, BF16>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<kPassDK>::kAlloc);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fa_bwd256_kernel<kPassDV, BF16>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<kPassDV>::kAlloc);
+    return e;
+}
+
 cudaError_t bwd_device_init(int dev) {
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     BwdDeviceState &s = g_bwd_dev[dev];
@@ -55,6 +72,8 @@ cudaError_t bwd_device_init(int dev) {
         if (e == cudaSuccess) e = configure_bwd<64, true>();
         if (e == cudaSuccess) e = configure_bwd<128, false>();
         if (e == cudaSuccess) e = configure_bwd<128, true>();
+        if (e == cudaSuccess) e = configure_bwd256<false>();
+        if (e == cudaSuccess) e = configure_bwd256<true>();
         s.err = e;
     });
     return s.err;
@@ -106,6 +125,35 @@ cudaError_t launch_main(const CUtensorMap &mq, const CUtensorMap &mk, const CUte
     if (e != cudaSuccess) return e;
     fa_bwd_dq_kernel<D, BF16, VARLEN><<<static_cast<unsigned>(pq.n_units < sms ? pq.n_units : sms),
                                         kThreads, QSmem<D>::kAlloc, st>>>(mq, mk, mv, mdo, pq);
+    return cudaGetLastError();
+}
+
+// d = 256: prep, then the dV, dK and dQ passes (fa_bwd256_kernel.cuh). Maps: q128 /
+// do128 and k128 / v128 are the 128-row views of the resident tiles, q64 / do64 and
+// k64 / v64 the 64-row views of the streamed ones.
+template <bool BF16>
+cudaError_t launch_bwd256(const fa::bwd::PrepParams &pp, const CUtensorMap &q128,
+                          const CUtensorMap &do128, const CUtensorMap &k128, const CUtensorMap &v128,
+                          const CUtensorMap &q64, const CUtensorMap &do64, const CUtensorMap &k64,
+                          const CUtensorMap &v64, const fa::bwd256::Params &pdq,
+                          const fa::bwd256::Params &pdk, const fa::bwd256::Params &pdv, int sms,
+                          cudaStream_t st) {
+    using namespace fa::bwd256;
+    const int64_t prep_rows = static_cast<int64_t>(pp.BH) * pp.Npad;
+    fa::bwd::fa_bwd_prep_kernel<256, BF16>
+        <<<static_cast<unsigned>((prep_rows + fa::bwd::kPrepWarps - 1) / fa::bwd::kPrepWarps),
+           fa::bwd::kPrepWarps * 32, 0, st>>>(pp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    auto grid = [sms](const Params &q) { return static_cast<unsigned>(q.n_units < sms ? q.n_units : sms); };
+    fa_bwd256_kernel<kPassDV, BF16>
+        <<<grid(pdv), kThreads, Layout<kPassDV>::kAlloc, st>>>(k128, k128, q64, do64, pdv);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    fa_bwd256_kernel<kPassDK, BF16>
+        <<<grid(pdk), kThreads, Layout<kPassDK>::kAlloc, st>>>(k128, v128, q64, do64, pdk);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    fa_bwd256_kernel<kPassDQ, BF16>
+        <<<grid(pdq), kThreads, Layout<kPassDQ>::kAlloc, st>>>(q128, do128, k64, v64, pdq);
     return cudaGetLastError();
 }
 
@@ -162,7 +210,7 @@ fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O
     for (const void *q : stored)
         if (!fa_host::aligned32(q)) return FA_ERR_INVALID_ARG;
     if (!fa_host::aligned4(LSE)) return FA_ERR_INVALID_ARG;
-    if (d != 32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (d != 32 && d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
     if (N > (int64_t{1} << 29) || B * H > (int64_t{1} << 31)) return FA_ERR_UNSUPPORTED;
     const int64_t BH = B * H, BHkv = B * H_kv;
     const int64_t Npad = padded_rows(N);
@@ -202,6 +250,13 @@ fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O
     CUtensorMap mq, mk, mv, mdo;
     if (!fa_host::make_map(&mq, Q, bf16, BH, N, d) || !fa_host::make_map(&mk, K, bf16, BHkv, N, d) ||
         !fa_host::make_map(&mv, V, bf16, BHkv, N, d) || !fa_host::make_map(&mdo, dO, bf16, BH, N, d))
+        return FA_ERR_CUDA;
+    CUtensorMap mq64, mk64, mv64, mdo64;  // d = 256: 64-row views of the streamed tiles
+    if (d == 256 &&
+        (!fa_host::make_map(&mq64, Q, bf16, BH, N, d, 64) ||
+         !fa_host::make_map(&mk64, K, bf16, BHkv, N, d, 64) ||
+         !fa_host::make_map(&mv64, V, bf16, BHkv, N, d, 64) ||
+         !fa_host::make_map(&mdo64, dO, bf16, BH, N, d, 64)))
         return FA_ERR_CUDA;
 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -252,6 +307,45 @@ fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O
     pq.heavy_first = wrv < N ? 1 : 0;              // later blocks see more keys
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (d == 256) {
+        fa::bwd256::Params b{};
+        b.Lw = pp.Lw;
+        b.Dw = pp.Dw;
+        b.N = p.N;
+        b.Npad = p.Npad;
+        b.H = p.H;
+        b.Hkv = p.Hkv;
+        b.group = p.group;
+        b.n_blk = p.n_blk;
+        b.wl = p.wl;
+        b.wr = p.wr;
+        b.scale_log2 = p.scale_log2;
+        b.wait_budget_ns = p.wait_budget_ns;
+        b.status = p.status;
+        b.fault_unit = -1;
+        fa::bwd256::Params pdq = b, pdk = b, pdv = b;
+        pdq.out = dQ;
+        pdq.out_scale = scale;
+        pdq.n_units = static_cast<int>(BH * n_blk);      // (query head, 128-query block)
+        pdk.out = dK;
+        pdk.out_scale = scale;
+        pdk.n_units = static_cast<int>(BHkv * n_blk);    // (K/V head, 128-key block)
+        pdv.out = dV;
+        pdv.out_scale = 1.f;
+        pdv.n_units = pdk.n_units;
+        pdv.fault_unit = pkv.fault_unit;                 // the hook applies to the first pass
+        pdq.sched = pq.sched;
+        pdk.sched = pkv.sched;
+        pdv.sched = fa_host::next_sched_slot(info.sched);
+        const cudaError_t e =
+            bf16 ? launch_bwd256<true>(pp, mq, mdo, mk, mv, mq64, mdo64, mk64, mv64, pdq, pdk, pdv,
+                                       info.sm_count, st)
+                 : launch_bwd256<false>(pp, mq, mdo, mk, mv, mq64, mdo64, mk64, mv64, pdq, pdk, pdv,
+                                        info.sm_count, st);
+        if (e != cudaSuccess) return FA_ERR_CUDA;
+        fa_host::count_launches(4);
+        return FA_OK;
+    }
     cudaError_t e;
     if (d == 32)
         e = bf16 ? launch_bwd<32, true>(pp, mq, mk, mv, mdo, pkv, pq, info.sm_count, st)

@@ -28,7 +28,8 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb);
 bool on_device(const void *p, int dev);
 // 3-D TMA map over a contiguous BH x N x d 16-bit tensor: box 64 columns x 128
 // rows, 128-byte swizzle, rows past N read as zero.
-bool make_map(CUtensorMap *map, const void *base, bool bf16, int64_t BH, int64_t N, int64_t d);
+bool make_map(CUtensorMap *map, const void *base, bool bf16, int64_t BH, int64_t N, int64_t d,
+              uint32_t box_rows = 128);
 // The same over a token-major tokens x heads x d tensor, ordered (d, heads,
 // tokens) with a 64-column x 1-head x 128-token box.
 bool make_map_tokens(CUtensorMap *map, const void *base, bool bf16, int64_t tokens, int64_t heads,

@@ -131,6 +131,11 @@ BWD_WORKLOADS = [
              seed=11, H_kv=8, backward=True),
     Workload("bwd_b4h32n4096d32", 4, 32, 4096, 32, torch.bfloat16, MASK_NONE, 0, 0, seed=19,
              backward=True),
+    # head dimension 256 (its own three-pass kernels)
+    Workload("bwd_b4h16n4096d256", 4, 16, 4096, 256, torch.bfloat16, MASK_NONE, 0, 0, seed=24,
+             backward=True),
+    Workload("bwd_causal_b4h16n4096d256", 4, 16, 4096, 256, torch.bfloat16, MASK_CAUSAL, 0, 0,
+             seed=25, backward=True),
 ]
 
 # A packed batch of 16 causal sequences of mixed lengths (N/8 .. N), token-major.
