@@ -64,7 +64,7 @@ typedef enum { FA_DTYPE_FP16 = 0, FA_DTYPE_BF16 = 1 } fa_dtype;
  *           as do d = 64 and 128 when a head's queries, or the queries of one K/V
  *           head's query heads, fit in one tile, and small unsplit problems (whose
  *           256-row units would fill at most half of the SMs). fa_backward takes
- *           32, 64, 128 and 256, fa_backward_varlen 32, 64 and 128.
+ *           32, 64, 128 and 256, and so does fa_backward_varlen.
  * scale   : multiplier of the logits, finite and > 0 (typically 1/sqrt(d)).
  * mask_mode, window_left, window_right : see fa_mask_mode. The window
  *           arguments are read only for FA_MASK_WINDOW and must then be >= 0
@@ -295,8 +295,11 @@ size_t fa_backward_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d);
  * max_seqlen_q / max_seqlen_k bound every sequence's lengths. Gradients of
  * keys that no query sees, and of queries that see no key, are zero.
  * `workspace`: fa_backward_varlen_workspace_bytes(B, H, total_q) bytes, 32-byte
- * aligned; pointer alignment as in fa_backward. d is 32, 64 or 128. Deterministic. Errors as fa_backward; the device
- * arrays are clamped to the tensors, as in fa_forward_varlen.
+ * aligned; pointer alignment as in fa_backward. d is 32, 64, 128 or 256.
+ * Deterministic. Errors as fa_backward; the device arrays are clamped to the
+ * tensors, as in fa_forward_varlen. Asynchronous on `stream`: three zero-fills
+ * of dQ, dK and dV, then four kernel launches (padded row offsets, row terms,
+ * dK/dV, dQ), five at d = 256 (one pass per gradient).
  */
 fa_status fa_backward_varlen(const void *Q, const void *K, const void *V, const void *O,
                              const void *dO, const float *LSE, const int32_t *cu_seqlens_q,

@@ -157,6 +157,21 @@ def test_varlen_unsupported(lib, kw):
     assert varlen_call(lib, **kw) == fa.FA_ERR_UNSUPPORTED
 
 
+def bwd_varlen_call(lib, d=64, **kw):
+    # host checks only: every pointer is fake and every check before the device
+    # lookup is on the arguments alone
+    B, H, tq = 2, 2, 100
+    return lib.fa_backward_varlen(0x100000, 0x200000, 0x300000, 0x400000, 0x500000, 0x600000,
+                                  0x700000, 0x700100, 0x800000, 0x900000, 0xA00000, B, H, H, tq, tq,
+                                  60, 60, d, 0.125, 0, 0, 0, 0, 0xB00000,
+                                  lib.fa_backward_varlen_workspace_bytes(B, H, tq), None)
+
+
+@pytest.mark.parametrize("d", [16, 96, 512])
+def test_backward_varlen_unsupported_head_dim(lib, d):
+    assert bwd_varlen_call(lib, d=d) == fa.FA_ERR_UNSUPPORTED
+
+
 def host_call(lib, B=1, H=2, Hk=2, Nq=128, Nk=128, d=64, scale=0.125, mask=0, wl=0, wr=0,
               dtype=0, splits=0, chunk=0, ws_bytes=1 << 30, **ptrs):
     a = dict(q=0x100000, k=0x200000, v=0x300000, o=0x400000, lse=0x600000, ws=0x700000)

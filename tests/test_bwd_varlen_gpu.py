@@ -38,11 +38,18 @@ def run_case(lens_q, lens_k, H, Hk, d, dtype, mask, window, seed):
     O = torch.empty_like(Q)
     LSE = torch.empty(Q.shape[:2], dtype=torch.float32, device=dev)
     fa.fa_forward_varlen(Q, K, V, O, LSE, cq, ck, max(lens_q), scale, mask, window[0], window[1])
-    dQ, dK, dV = (torch.full_like(t, 9.0) for t in (Q, K, V))
+    # outputs inside sentinel-filled buffers: a store outside them shows as a changed guard
+    G = 4096
+    bufs = [torch.full((t.numel() + 2 * G,), -555.0, dtype=t.dtype, device=dev) for t in (Q, K, V)]
+    dQ, dK, dV = (b[G:G + t.numel()].view(t.shape) for b, t in zip(bufs, (Q, K, V)))
+    for t in (dQ, dK, dV):
+        t.fill_(9.0)
     fa.fa_backward_varlen(Q, K, V, O, DO, LSE, cq, ck, dQ, dK, dV, max(lens_q), max(lens_k), scale,
                           mask, window[0], window[1])
     st = fa.fa_sync_status()
     assert st == fa.FA_OK, fa.fa_status_string(st)
+    for b in bufs:
+        assert bool((b[:G] == -555.0).all()) and bool((b[-G:] == -555.0).all()), "stray write"
     dQ, dK, dV = dQ.cpu(), dK.cpu(), dV.cpu()
     for b, (q, k, v, do) in enumerate(seqs):
         lq, lk = q.shape[2], k.shape[2]
@@ -68,7 +75,7 @@ CASES = [
 
 
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
-@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("d", [32, 64, 128, 256])
 @pytest.mark.parametrize("mask,window", [("none", (0, 0)), ("causal", (0, 0)), ("window", (90, 3))])
 @pytest.mark.parametrize("case", range(len(CASES)))
 def test_bwd_varlen_parity(case, mask, window, d, dtype):
@@ -76,11 +83,12 @@ def test_bwd_varlen_parity(case, mask, window, d, dtype):
     run_case(lens_q, lens_k or lens_q, H, Hk, d, dtype, mask, window, seed=31 * case + d)
 
 
-def test_bwd_varlen_matches_dense():
+@pytest.mark.parametrize("d", [64, 256])
+def test_bwd_varlen_matches_dense(d):
     """Equal lengths: bit-identical to fa_backward on the (B, H, N, d) layout."""
     from test_bwd_gpu import run_bwd
     dev = torch.device("cuda", 0)
-    B, H, N, d = 3, 4, 333, 64
+    B, H, N = 3, 4, 333
     q, k, v = make_qkv(B, H, N, d, torch.bfloat16, seed=5)
     do = make_qkv(B, H, N, d, torch.bfloat16, seed=6)[0]
     dq_d, dk_d, dv_d = run_bwd(q, k, v, do, 0.125, "causal")

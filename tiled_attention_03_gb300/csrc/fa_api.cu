@@ -924,8 +924,8 @@ bool make_map(CUtensorMap *map, const void *base, bool bf16, int64_t BH, int64_t
 }
 uint64_t wait_budget() { return ::wait_budget(); }
 bool make_map_tokens(CUtensorMap *map, const void *base, bool bf16, int64_t tokens, int64_t heads,
-                     int64_t d) {
-    return ::make_map_tokens(map, base, bf16, tokens, heads, d);
+                     int64_t d, uint32_t box_tokens) {
+    return ::make_map_tokens(map, base, bf16, tokens, heads, d, box_tokens);
 }
 void count_launches(int64_t n) { g_launches += n; }
 int take_fault_position() { return g_fault_pos.exchange(-1); }

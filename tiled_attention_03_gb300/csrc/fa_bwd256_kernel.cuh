@@ -125,33 +125,64 @@ struct Params {
     unsigned int *status;     // [code, role, unit, block]
     unsigned int *sched;      // this launch's {next unit, finished CTAs} (zero at launch)
     int fault_unit;           // test hook: every CTA skips its resident load of this unit (-1: none)
+    // Variable-length batches (template flag VARLEN): token-major tensors, sequence b
+    // owning query tokens cu_q[b] .. cu_q[b+1]-1 and keys cu_k[b] .. cu_k[b+1]-1
+    // (clamped to [0, total]), its queries at its last key positions; the row terms
+    // of sequence b, head h start at h * vstride + cu_pad[b]; n_blk counts 128-row
+    // blocks of the longest sequence's resident side.
+    const int *cu_q, *cu_k, *cu_pad;
+    int total_q, total_k, vstride;
 };
 
 // A unit: 128 resident rows r0 .. r0+127 of head `head` (a query head in the dQ
 // pass, a K/V head in the others) and the streamed tiles t = 0 .. n_t-1 that hold a
 // visible pair: tile t is 64-row block lo + t % per of head `head` (dQ pass), or of
 // query head group_head(head, t / per) (dK / dV passes).
+// Positions are the sequence's own (queries 0 .. nq-1 at key positions q_off ..
+// q_off + nq - 1, keys 0 .. nk-1); the dense case is one sequence of N per head.
+// n_t = 0 marks a unit without work (rows past its sequence, or no visible pair).
 struct Unit {
     int head, r0, lo, per, n_t;
+    int nq, nk, q_off, q_tok0, k_tok0, pad0;
 };
 
-template <int PASS>
+template <int PASS, bool VARLEN>
 __device__ __forceinline__ Unit decode(int u, const Params &p) {
     Unit U;
     U.head = u / p.n_blk;
     U.r0 = (u - U.head * p.n_blk) * kRows;
-    const int r1 = min(U.r0 + kRows, p.N) - 1;
-    // dQ: rows are queries, streamed rows keys; dK / dV: the other way round.
-    const int lo = PASS == kPassDQ ? max(0, U.r0 - p.wl) : max(0, U.r0 - p.wr);
-    const int hi = PASS == kPassDQ ? min(p.N - 1, r1 + p.wr) : min(p.N - 1, r1 + p.wl);
+    if constexpr (VARLEN) {
+        const int b = U.head / (PASS == kPassDQ ? p.H : p.Hkv);
+        const int q0 = min(max(p.cu_q[b], 0), p.total_q);
+        const int q1 = min(max(p.cu_q[b + 1], q0), p.total_q);
+        const int k0 = min(max(p.cu_k[b], 0), p.total_k);
+        const int k1 = min(max(p.cu_k[b + 1], k0), p.total_k);
+        U.nq = q1 - q0;
+        U.nk = k1 - k0;
+        U.q_tok0 = q0;
+        U.k_tok0 = k0;
+        U.pad0 = p.cu_pad[b];
+    } else {
+        U.nq = U.nk = p.N;
+        U.q_tok0 = U.k_tok0 = U.pad0 = 0;
+    }
+    U.q_off = U.nk - U.nq;
+    // dQ: resident rows are queries, streamed rows keys; dK / dV: the other way round.
+    const int n_res = PASS == kPassDQ ? U.nq : U.nk;
+    const int n_str = PASS == kPassDQ ? U.nk : U.nq;
+    const int r1 = min(U.r0 + kRows, n_res) - 1;
+    const int lo = PASS == kPassDQ ? max(0, U.r0 + U.q_off - p.wl) : max(0, U.r0 - U.q_off - p.wr);
+    const int hi = PASS == kPassDQ ? min(n_str - 1, r1 + U.q_off + p.wr)
+                                   : min(n_str - 1, r1 - U.q_off + p.wl);
     U.lo = lo / kCols;
     U.per = hi / kCols - U.lo + 1;
-    U.n_t = (PASS == kPassDQ ? 1 : p.group) * U.per;
+    U.n_t = U.r0 < n_res && lo <= hi ? (PASS == kPassDQ ? 1 : p.group) * U.per : 0;
     return U;
 }
 
 // Head of the streamed tile t: the unit's own (dQ pass), or the query head of the
-// group reading K/V head `head` (dK / dV passes).
+// group reading K/V head `head` (dK / dV passes). Heads are b * H + h (queries) or
+// b * H_kv + h (K/V).
 template <int PASS>
 __device__ __forceinline__ void tile_of(const Unit &U, int t, const Params &p, int &head, int &row0) {
     const int g = t / U.per;
@@ -162,6 +193,29 @@ __device__ __forceinline__ void tile_of(const Unit &U, int t, const Params &p, i
         const int b = U.head / p.Hkv, hk = U.head - b * p.Hkv;
         head = b * p.H + hk * p.group + g;
     }
+}
+
+// TMA coordinates (y, z) of a tile starting at row `row` of head `head` of a tensor
+// with `heads` heads per batch entry whose sequence starts at token tok0: dense
+// maps are (d, N, heads), variable-length maps (d, heads, tokens).
+template <bool VARLEN>
+__device__ __forceinline__ void coords(int head, int heads, int tok0, int row, int &y, int &z) {
+    if constexpr (VARLEN) {
+        y = head % heads;
+        z = tok0 + row;
+    } else {
+        y = row;
+        z = head;
+    }
+}
+
+// Row of the row-term vectors for query row `row` of query head `head`.
+template <bool VARLEN>
+__device__ __forceinline__ size_t vec_row(const Unit &U, int head, int row, const Params &p) {
+    if constexpr (VARLEN)
+        return static_cast<size_t>(head % p.H) * p.vstride + U.pad0 + row;
+    else
+        return static_cast<size_t>(head) * p.Npad + row;
 }
 
 __device__ __forceinline__ void record_timeout(const Params &p, volatile int *abort_flag, int role,
@@ -178,7 +232,7 @@ __device__ __forceinline__ void record_timeout(const Params &p, volatile int *ab
 // The resident tiles are read through a 128-row TMA map of their tensor, the
 // streamed ones through a 64-row map: tmR0 / tmR1 (Q / dO in the dQ pass, K / V
 // otherwise) and tmS0 / tmS1 (K / V in the dQ pass, Q / dO otherwise).
-template <int PASS, bool BF16>
+template <int PASS, bool BF16, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd256_kernel(const __grid_constant__ CUtensorMap tmR0, const __grid_constant__ CUtensorMap tmR1,
                      const __grid_constant__ CUtensorMap tmS0, const __grid_constant__ CUtensorMap tmS1,
@@ -268,7 +322,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) return -1;
                 // a CTA's first unit is its own index (the grid never exceeds the unit
                 // count); the counter numbers the rest from gridDim.x on
-                const unsigned next = k == 0 ? blockIdx.x : gridDim.x + atomicAdd(p.sched, 1u);
+                unsigned next = k == 0 ? blockIdx.x : gridDim.x + atomicAdd(p.sched, 1u);
+                if constexpr (VARLEN)  // blocks past their sequence, or without a visible pair
+                    while (next < static_cast<unsigned>(p.n_units) &&
+                           decode<PASS, VARLEN>(static_cast<int>(next), p).n_t == 0)
+                        next = gridDim.x + atomicAdd(p.sched, 1u);
                 const int v = next < static_cast<unsigned>(p.n_units) ? static_cast<int>(next) : -1;
                 unit_ring[slot] = v;
                 mbar_arrive(bar(kBarUnitFull + slot));
@@ -276,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             int u = publish(0);
             for (; ok && u >= 0; ++unit_iter) {
-                const Unit U = decode<PASS>(u, p);
+                const Unit U = decode<PASS, VARLEN>(u, p);
                 // resident tiles (and, in the dQ pass, their rows' L and D)
                 ok = mbar_wait_bounded(bar(kBarResEmpty), (unit_iter & 1) ^ 1, abort_flag, budget);
                 if (!ok) break;
@@ -284,14 +342,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     constexpr uint32_t kResTx =
                         (L::kRes1 ? 2 : 1) * kResBytes + (PASS == kPassDQ ? 2 * kRows * 4 : 0);
                     mbar_arrive_expect_tx(bar(kBarResFull), kResTx);
+                    int ry, rz;
+                    coords<VARLEN>(U.head, PASS == kPassDQ ? p.H : p.Hkv,
+                                   PASS == kPassDQ ? U.q_tok0 : U.k_tok0, U.r0, ry, rz);
                     for (int g = 0; g < kRegions; ++g) {
-                        tma_load_3d(sR0 + g * kResRegion, &tmR0, bar(kBarResFull), 64 * g, U.r0, U.head);
+                        tma_load_3d(sR0 + g * kResRegion, &tmR0, bar(kBarResFull), 64 * g, ry, rz);
                         if constexpr (L::kRes1)
-                            tma_load_3d(sR1 + g * kResRegion, &tmR1, bar(kBarResFull), 64 * g, U.r0,
-                                        U.head);
+                            tma_load_3d(sR1 + g * kResRegion, &tmR1, bar(kBarResFull), 64 * g, ry, rz);
                     }
                     if constexpr (PASS == kPassDQ) {
-                        const size_t vrow = static_cast<size_t>(U.head) * p.Npad + U.r0;
+                        const size_t vrow = vec_row<VARLEN>(U, U.head, U.r0, p);
                         bulk_load(sVec, p.Lw + vrow, kRows * 4, bar(kBarResFull));
                         bulk_load(sVec + kRows * 4, p.Dw + vrow, kRows * 4, bar(kBarResFull));
                     }
@@ -309,15 +369,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // tile it - kS0 (dK pass: after its accumulation; dV pass: after its
                     // A was ready), so tile it - 3 and every older one are done with
                     // their vectors.
-                    const size_t vrow = static_cast<size_t>(head) * p.Npad + row0;
+                    const size_t vrow = PASS == kPassDQ ? 0 : vec_row<VARLEN>(U, head, row0, p);
                     const int vs = it % kVecSlots;
+                    int sy, sz;
+                    coords<VARLEN>(head, PASS == kPassDQ ? p.Hkv : p.H,
+                                   PASS == kPassDQ ? U.k_tok0 : U.q_tok0, row0, sy, sz);
                     int s = it % kS0;
                     ok = mbar_wait_bounded(bar(kBarS0Empty + s), ((it / kS0) & 1) ^ 1, abort_flag, budget);
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(kBarS0Full + s),
                                           kStrBytes + (PASS == kPassDQ ? 0 : kCols * 4));
                     for (int g = 0; g < kRegions; ++g)
-                        tma_load_3d(sS0(it) + g * kStrRegion, &tmS0, bar(kBarS0Full + s), 64 * g, row0, head);
+                        tma_load_3d(sS0(it) + g * kStrRegion, &tmS0, bar(kBarS0Full + s), 64 * g, sy, sz);
                     if constexpr (PASS != kPassDQ)
                         bulk_load(sVec + vs * kCols * 4, p.Lw + vrow, kCols * 4, bar(kBarS0Full + s));
                     s = it % kS1;
@@ -326,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(bar(kBarS1Full + s),
                                           kStrBytes + (PASS == kPassDK ? kCols * 4 : 0));
                     for (int g = 0; g < kRegions; ++g)
-                        tma_load_3d(sS1(it) + g * kStrRegion, &tmS1, bar(kBarS1Full + s), 64 * g, row0, head);
+                        tma_load_3d(sS1(it) + g * kStrRegion, &tmS1, bar(kBarS1Full + s), 64 * g, sy, sz);
                     if constexpr (PASS == kPassDK)
                         bulk_load(sVec + (kVecSlots + vs) * kCols * 4, p.Dw + vrow, kCols * 4,
                                   bar(kBarS1Full + s));
@@ -399,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (; ok; ++unit_iter) {
             u = take_unit(unit_iter, ok);
             if (!ok || u < 0) break;
-            const Unit U = decode<PASS>(u, p);
+            const Unit U = decode<PASS, VARLEN>(u, p);
             ok = wait(kBarResFull, unit_iter & 1);
             for (int t = 0; ok && t < U.n_t; ++t, ++it) {
                 const int s0 = it % kS0, s1 = it % kS1;
@@ -448,9 +511,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (; ok; ++unit_iter) {
             u = take_unit(unit_iter, ok);
             if (!ok || u < 0) break;
-            const Unit U = decode<PASS>(u, p);
-            const int row = U.r0 + r;  // query (dQ pass) or key of this thread
-            const bool row_ok = row < p.N;
+            const Unit U = decode<PASS, VARLEN>(u, p);
+            const int row = U.r0 + r;  // query (dQ pass) or key of this thread, in its sequence
+            const bool row_ok = row < (PASS == kPassDQ ? U.nq : U.nk);
             // dQ pass: this row's L and D, resident for the unit
             float Lrow = 0.f, Drow = 0.f;
             if constexpr (PASS == kPassDQ) {
@@ -498,11 +561,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < kCols; ++c) x[c] = ex2_approx(x[c]);
                 // visible pairs: key j and query i with i - wl <= j <= i + wr, both < N
                 if constexpr (PASS == kPassDQ) {
-                    // row = query, columns = keys c0 + c
-                    mask_outside_run(x, max(0, row - p.wl) - c0, min(p.N - 1, row + p.wr) - c0, 0.f);
+                    // row = query (key position row + q_off), columns = keys c0 + c
+                    mask_outside_run(x, max(0, row + U.q_off - p.wl) - c0,
+                                     min(U.nk - 1, row + U.q_off + p.wr) - c0, 0.f);
                 } else {
-                    // row = key, columns = queries c0 + c
-                    mask_outside_run(x, max(0, row - p.wr) - c0, min(p.N - 1, row + p.wl) - c0, 0.f);
+                    // row = key, columns = queries c0 + c (at key positions c0 + c + q_off)
+                    mask_outside_run(x, max(0, row - U.q_off - p.wr) - c0,
+                                     min(U.nq - 1, row - U.q_off + p.wl) - c0, 0.f);
                     if (!row_ok) {
 #pragma unroll
                         for (int c = 0; c < kCols; ++c) x[c] = 0.f;
@@ -553,8 +618,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             {
                 const float f = p.out_scale;
-                uint8_t *out = reinterpret_cast<uint8_t *>(p.out) +
-                               (static_cast<size_t>(U.head) * p.N + (row_ok ? row : 0)) * (kD * 2);
+                // global row: (head, row), or (token, head) in a variable-length batch
+                size_t orow;
+                if constexpr (VARLEN) {
+                    const int heads = PASS == kPassDQ ? p.H : p.Hkv;
+                    orow = (static_cast<size_t>(PASS == kPassDQ ? U.q_tok0 : U.k_tok0) + (row_ok ? row : 0)) *
+                               heads + U.head % heads;
+                } else {
+                    orow = static_cast<size_t>(U.head) * p.N + (row_ok ? row : 0);
+                }
+                uint8_t *out = reinterpret_cast<uint8_t *>(p.out) + orow * (kD * 2);
 #pragma unroll 1
                 for (int c = 0; c < kD / 32; ++c) {
                     uint32_t a[32];

@@ -47,17 +47,17 @@ cudaError_t configure_bwd() {
 }
 
 // d = 256: the three passes of fa_bwd256_kernel.cuh (192 threads, no setmaxnreg).
-template <bool BF16>
+template <bool BF16, bool VARLEN>
 cudaError_t configure_bwd256() {
     using namespace fa::bwd256;
-    cudaError_t e = cudaFuncSetAttribute(fa_bwd256_kernel<kPassDQ, BF16>,
+    cudaError_t e = cudaFuncSetAttribute(fa_bwd256_kernel<kPassDQ, BF16, VARLEN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Layout<kPassDQ>::kAlloc);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(fa_bwd256_kernel<kPassDK, BF16>,
+        e = cudaFuncSetAttribute(fa_bwd256_kernel<kPassDK, BF16, VARLEN>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<kPassDK>::kAlloc);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(fa_bwd256_kernel<kPassDV, BF16>,
+        e = cudaFuncSetAttribute(fa_bwd256_kernel<kPassDV, BF16, VARLEN>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<kPassDV>::kAlloc);
     return e;
 }
@@ -72,8 +72,10 @@ cudaError_t bwd_device_init(int dev) {
         if (e == cudaSuccess) e = configure_bwd<64, true>();
         if (e == cudaSuccess) e = configure_bwd<128, false>();
         if (e == cudaSuccess) e = configure_bwd<128, true>();
-        if (e == cudaSuccess) e = configure_bwd256<false>();
-        if (e == cudaSuccess) e = configure_bwd256<true>();
+        if (e == cudaSuccess) e = configure_bwd256<false, false>();
+        if (e == cudaSuccess) e = configure_bwd256<true, false>();
+        if (e == cudaSuccess) e = configure_bwd256<false, true>();
+        if (e == cudaSuccess) e = configure_bwd256<true, true>();
         s.err = e;
     });
     return s.err;
@@ -128,9 +130,30 @@ cudaError_t launch_main(const CUtensorMap &mq, const CUtensorMap &mk, const CUte
     return cudaGetLastError();
 }
 
-// d = 256: prep, then the dV, dK and dQ passes (fa_bwd256_kernel.cuh). Maps: q128 /
-// do128 and k128 / v128 are the 128-row views of the resident tiles, q64 / do64 and
-// k64 / v64 the 64-row views of the streamed ones.
+// d = 256: the dV, dK and dQ passes (fa_bwd256_kernel.cuh) after the row-term
+// prep. Maps: q128 / do128 and k128 / v128 are the 128-row views of the resident
+// tiles, q64 / do64 and k64 / v64 the 64-row views of the streamed ones.
+template <bool BF16, bool VARLEN>
+cudaError_t launch_bwd256_passes(const CUtensorMap &q128, const CUtensorMap &do128,
+                                 const CUtensorMap &k128, const CUtensorMap &v128,
+                                 const CUtensorMap &q64, const CUtensorMap &do64,
+                                 const CUtensorMap &k64, const CUtensorMap &v64,
+                                 const fa::bwd256::Params &pdq, const fa::bwd256::Params &pdk,
+                                 const fa::bwd256::Params &pdv, int sms, cudaStream_t st) {
+    using namespace fa::bwd256;
+    cudaError_t e;
+    auto grid = [sms](const Params &q) { return static_cast<unsigned>(q.n_units < sms ? q.n_units : sms); };
+    fa_bwd256_kernel<kPassDV, BF16, VARLEN>
+        <<<grid(pdv), kThreads, Layout<kPassDV>::kAlloc, st>>>(k128, k128, q64, do64, pdv);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    fa_bwd256_kernel<kPassDK, BF16, VARLEN>
+        <<<grid(pdk), kThreads, Layout<kPassDK>::kAlloc, st>>>(k128, v128, q64, do64, pdk);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    fa_bwd256_kernel<kPassDQ, BF16, VARLEN>
+        <<<grid(pdq), kThreads, Layout<kPassDQ>::kAlloc, st>>>(q128, do128, k64, v64, pdq);
+    return cudaGetLastError();
+}
+
 template <bool BF16>
 cudaError_t launch_bwd256(const fa::bwd::PrepParams &pp, const CUtensorMap &q128,
                           const CUtensorMap &do128, const CUtensorMap &k128, const CUtensorMap &v128,
@@ -138,23 +161,37 @@ cudaError_t launch_bwd256(const fa::bwd::PrepParams &pp, const CUtensorMap &q128
                           const CUtensorMap &v64, const fa::bwd256::Params &pdq,
                           const fa::bwd256::Params &pdk, const fa::bwd256::Params &pdv, int sms,
                           cudaStream_t st) {
-    using namespace fa::bwd256;
     const int64_t prep_rows = static_cast<int64_t>(pp.BH) * pp.Npad;
     fa::bwd::fa_bwd_prep_kernel<256, BF16>
         <<<static_cast<unsigned>((prep_rows + fa::bwd::kPrepWarps - 1) / fa::bwd::kPrepWarps),
            fa::bwd::kPrepWarps * 32, 0, st>>>(pp);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_bwd256_passes<BF16, false>(q128, do128, k128, v128, q64, do64, k64, v64, pdq, pdk,
+                                             pdv, sms, st);
+}
+
+// Variable-length batches at d = 256: padded row offsets, the row terms, then the
+// three passes over token-major maps.
+template <bool BF16>
+cudaError_t launch_bwd256_varlen(const fa::bwd::PrepVarlenParams &pp, const CUtensorMap &q128,
+                                 const CUtensorMap &do128, const CUtensorMap &k128,
+                                 const CUtensorMap &v128, const CUtensorMap &q64,
+                                 const CUtensorMap &do64, const CUtensorMap &k64,
+                                 const CUtensorMap &v64, const fa::bwd256::Params &pdq,
+                                 const fa::bwd256::Params &pdk, const fa::bwd256::Params &pdv,
+                                 int sms, cudaStream_t st) {
+    using namespace fa::bwd;
+    fa_bwd_cu_pad_kernel<<<1, 32, 0, st>>>(pp.cu_q, pp.B, pp.total_q, const_cast<int *>(pp.cu_pad));
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    auto grid = [sms](const Params &q) { return static_cast<unsigned>(q.n_units < sms ? q.n_units : sms); };
-    fa_bwd256_kernel<kPassDV, BF16>
-        <<<grid(pdv), kThreads, Layout<kPassDV>::kAlloc, st>>>(k128, k128, q64, do64, pdv);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    fa_bwd256_kernel<kPassDK, BF16>
-        <<<grid(pdk), kThreads, Layout<kPassDK>::kAlloc, st>>>(k128, v128, q64, do64, pdk);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    fa_bwd256_kernel<kPassDQ, BF16>
-        <<<grid(pdq), kThreads, Layout<kPassDQ>::kAlloc, st>>>(q128, do128, k64, v64, pdq);
-    return cudaGetLastError();
+    const int64_t rows = static_cast<int64_t>(pp.H) * pp.vstride;
+    fa_bwd_prep_varlen_kernel<256, BF16><<<static_cast<unsigned>((rows + kPrepWarps - 1) / kPrepWarps),
+                                           kPrepWarps * 32, 0, st>>>(pp);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_bwd256_passes<BF16, true>(q128, do128, k128, v128, q64, do64, k64, v64, pdq, pdk,
+                                            pdv, sms, st);
 }
 
 template <int D, bool BF16>
@@ -405,7 +442,7 @@ fa_status fa_backward_varlen(const void *Q, const void *K, const void *V, const 
     if (mask_mode == FA_MASK_WINDOW && (window_left < 0 || window_right < 0))
         return FA_ERR_INVALID_ARG;
     if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
-    if (d != 32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (d != 32 && d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
     if (total_q > (int64_t{1} << 29) || total_k > (int64_t{1} << 29) || max_seqlen_q > total_q ||
         max_seqlen_k > total_k || B > (int64_t{1} << 20))
         return FA_ERR_UNSUPPORTED;
@@ -529,6 +566,58 @@ fa_status fa_backward_varlen(const void *Q, const void *K, const void *V, const 
     pkv.sched = fa_host::next_sched_slot(info.sched);
     pq.sched = fa_host::next_sched_slot(info.sched);
 
+    if (d == 256) {
+        CUtensorMap mq64, mk64, mv64, mdo64;
+        if (!fa_host::make_map_tokens(&mq64, Q, bf16, total_q, H, d, 64) ||
+            !fa_host::make_map_tokens(&mk64, K, bf16, total_k, H_kv, d, 64) ||
+            !fa_host::make_map_tokens(&mv64, V, bf16, total_k, H_kv, d, 64) ||
+            !fa_host::make_map_tokens(&mdo64, dO, bf16, total_q, H, d, 64))
+            return FA_ERR_CUDA;
+        fa::bwd256::Params b{};
+        b.Lw = pp.Lw;
+        b.Dw = pp.Dw;
+        b.N = p.N;
+        b.H = p.H;
+        b.Hkv = p.Hkv;
+        b.group = p.group;
+        b.wl = p.wl;
+        b.wr = p.wr;
+        b.scale_log2 = p.scale_log2;
+        b.wait_budget_ns = p.wait_budget_ns;
+        b.status = p.status;
+        b.fault_unit = -1;
+        b.cu_q = cu_seqlens_q;
+        b.cu_k = cu_seqlens_k;
+        b.cu_pad = pp.cu_pad;
+        b.total_q = p.total_q;
+        b.total_k = p.total_k;
+        b.vstride = p.vstride;
+        fa::bwd256::Params pdq = b, pdk = b, pdv = b;
+        pdq.out = dQ;
+        pdq.out_scale = scale;
+        pdq.n_blk = pq.n_blk;                       // (sequence, query head, 128-query block)
+        pdq.n_units = pq.n_units;
+        pdk.out = dK;
+        pdk.out_scale = scale;
+        pdk.n_blk = pkv.n_blk;                      // (sequence, K/V head, 128-key block)
+        pdk.n_units = pkv.n_units;
+        pdv.out = dV;
+        pdv.out_scale = 1.f;
+        pdv.n_blk = pkv.n_blk;
+        pdv.n_units = pkv.n_units;
+        pdv.fault_unit = pkv.fault_unit;            // the hook applies to the first pass
+        pdq.sched = pq.sched;
+        pdk.sched = pkv.sched;
+        pdv.sched = fa_host::next_sched_slot(info.sched);
+        const cudaError_t e =
+            bf16 ? launch_bwd256_varlen<true>(pp, mq, mdo, mk, mv, mq64, mdo64, mk64, mv64, pdq, pdk,
+                                              pdv, info.sm_count, st)
+                 : launch_bwd256_varlen<false>(pp, mq, mdo, mk, mv, mq64, mdo64, mk64, mv64, pdq,
+                                               pdk, pdv, info.sm_count, st);
+        if (e != cudaSuccess) return FA_ERR_CUDA;
+        fa_host::count_launches(5);
+        return FA_OK;
+    }
     cudaError_t e;
     if (d == 32)
         e = bf16 ? launch_bwd_varlen<32, true>(pp, mq, mk, mv, mdo, pkv, pq, info.sm_count, st)

@@ -31,9 +31,9 @@ bool on_device(const void *p, int dev);
 bool make_map(CUtensorMap *map, const void *base, bool bf16, int64_t BH, int64_t N, int64_t d,
               uint32_t box_rows = 128);
 // The same over a token-major tokens x heads x d tensor, ordered (d, heads,
-// tokens) with a 64-column x 1-head x 128-token box.
+// tokens) with a 64-column x 1-head x box_tokens-token box.
 bool make_map_tokens(CUtensorMap *map, const void *base, bool bf16, int64_t tokens, int64_t heads,
-                     int64_t d);
+                     int64_t d, uint32_t box_tokens = 128);
 uint64_t wait_budget();
 void count_launches(int64_t n);
 // The armed test-hook position (fa_test_arm_fault), disarming it; -1 if none.
