@@ -16,9 +16,14 @@
 //     128-column S buffers and O would not fit the 512 TMEM columns); the K and V rings
 //     are as deep as shared memory allows (3 and 2 at d = 256, 3 and 3 at d = 128,
 //     6 and 6 at d = 64);
-//   * S is formed in one of three bn(D)-column TMEM buffers, so that the softmax of
-//     block j runs while S(j+1) and S(j+2) are computed; O (D columns) stays in
-//     TMEM for the unit. MMA order: ... O += P(j) V_j | S(j+3) | O += P(j+1) V_{j+1} ...
+//   * S is formed in one of three bn(D)-column TMEM buffers (two at d = 256), so that
+//     the softmax of block j runs while S(j+1) and S(j+2) are computed; O (D
+//     columns) stays in TMEM for the unit. MMA order (three buffers):
+//     ... O += P(j) V_j | S(j+3) | O += P(j+1) V_{j+1} ...
+//   * at d = 256 the Q tile is also copied into TMEM (128 columns of 16-bit pairs) by
+//     the softmax warpgroup, and S = Q K^T takes Q from there: with 64-key tiles the
+//     shared-memory form would read 6 KB of operands per 32-cycle MMA, more than the
+//     SM's 128 bytes per cycle of shared-memory bandwidth, while K alone is 2 KB;
 //   * one softmax warpgroup (thread = query row = TMEM lane, bn(D) keys per block).
 // When the reference max of a row moves (rare), the softmax thread rescales its O
 // row, after waiting for the product O += P(j-1) V_{j-1} to complete (two
@@ -57,7 +62,10 @@ constexpr int kVWarp = 6;
 __host__ __device__ constexpr int k_stages(int D) { return D == 64 ? 6 : 3; }
 __host__ __device__ constexpr int v_stages(int D) { return D == 64 ? 6 : D == 128 ? 3 : 2; }
 constexpr int kMaxStages = 6;
-constexpr int kSBufs = 3;
+constexpr int kSBufs = 3;  // S buffers (barrier slots); s_bufs(D) are used
+__host__ __device__ constexpr int s_bufs(int D) { return D == 256 ? 2 : 3; }
+// Q read by S = Q K^T from TMEM (d = 256) instead of shared memory
+__host__ __device__ constexpr bool q_in_tmem(int D) { return D == 256; }
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units, as in fa_fwd_kernel.cuh
 constexpr unsigned kStatusTimeout = 4;
@@ -133,14 +141,17 @@ enum : int {
     kBarUnitFull = kBarOFree + 1,          // + slot (2)
     kBarUnitEmpty = kBarUnitFull + kUnitSlots,  // + slot (2)
     kBarDrainIdx = kBarUnitEmpty + kUnitSlots,
-    kNumBarsUsed = kBarDrainIdx + 1,
+    kBarQReady = kBarDrainIdx + 1,         // Q copied into TMEM (d = 256)
+    kNumBarsUsed = kBarQReady + 1,
 };
 static_assert(kNumBarsUsed <= Smem<256>::kNumBars, "barrier slots");
 static_assert(k_stages(64) <= kMaxStages && v_stages(64) <= kMaxStages, "ring depth");
 
-// TMEM columns: S buffers at bn(D) b, O after them (256 at d = 256, 384 below).
+// TMEM columns: S buffers at bn(D) b, O after them (256 at d = 256, 384 below); at
+// d = 256 the Q tile sits between them (columns 128 .. 255).
 constexpr uint32_t kTmemS = 0;
 __host__ __device__ constexpr uint32_t tmem_o(int D) { return D == 256 ? 256u : 384u; }
+__host__ __device__ constexpr uint32_t tmem_q(int D) { return D == 256 ? 128u : 0u; }
 
 // A row space holds the queries of hps consecutive query heads (b*H + h order), row
 // r being query r % Nq of head sp*hps + r / Nq: one head each, or, with few queries,
@@ -254,7 +265,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     using L = Smem<D>;
     constexpr int kBN = bn(D);
     constexpr uint32_t kTmemO = tmem_o(D);
-    static_assert(kSBufs * kBN <= static_cast<int>(kTmemO) && kTmemO + D <= kTmemCols, "TMEM columns");
+    constexpr int kSB = s_bufs(D);
+    constexpr bool kQT = q_in_tmem(D);
+    constexpr uint32_t kTmemQ = tmem_q(D);
+    static_assert(kSB <= kSBufs, "S buffers");
+    static_assert(kQT ? (kSB * kBN <= static_cast<int>(kTmemQ) && kTmemQ + D / 2 <= kTmemO)
+                      : kSB * kBN <= static_cast<int>(kTmemO),
+                  "TMEM columns");
+    static_assert(kTmemO + D <= kTmemCols, "TMEM columns");
     constexpr int kKStages = k_stages(D);
     constexpr int kVStages = v_stages(D);
     extern __shared__ uint8_t smem_raw[];
@@ -280,7 +298,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (threadIdx.x == kTmaWarp * 32) {
         mbar_init(bar(kBarQFull), 1);
-        mbar_init(bar(kBarQEmpty), 1);
+        // Q's shared-memory copy is released by the MMA warp's commit, or at d = 256
+        // by the softmax threads once they have copied it into TMEM
+        mbar_init(bar(kBarQEmpty), kQT ? 128 : 1);
+        mbar_init(bar(kBarQReady), 128);
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(bar(kBarKFull + s), 1);
             mbar_init(bar(kBarKEmpty + s), 1);
@@ -289,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(kBarVFull + s), 1);
             mbar_init(bar(kBarVEmpty + s), 1);
         }
-        for (int b = 0; b < kSBufs; ++b) {
+        for (int b = 0; b < kSB; ++b) {
             mbar_init(bar(kBarSFull + b), 1);
             mbar_init(bar(kBarPFull + b), 128);
         }
@@ -443,7 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (elect_one()) umma_commit(bar(b));
             __syncwarp();
         };
-        // S(t) = Q K_t^T into S buffer t mod 3 (kBN columns).
+        // S(t) = Q K_t^T into S buffer t mod kSB (kBN columns); Q from shared memory,
+        // or from TMEM (K-step k of 16 columns = 8 TMEM columns).
         auto issue_s = [&](int t) {
             tc_fence_after();
             const uint64_t dq = sw128_desc(sQ, 16, 1024);
@@ -453,14 +475,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t offq = (k >> 2) * (L::kQRegion >> 4) + (k & 3) * 2;
                     const uint32_t offk = (k >> 2) * (L::kKVRegion >> 4) + (k & 3) * 2;
-                    umma_f16_ss(tmem + kTmemS + (t % kSBufs) * kBN, dq + offq, dk + offk, idesc_s,
-                                k > 0 ? 1u : 0u);
+                    if constexpr (kQT)
+                        umma_f16_ts(tmem + kTmemS + (t % kSB) * kBN, tmem + kTmemQ + k * 8, dk + offk,
+                                    idesc_s, k > 0 ? 1u : 0u);
+                    else
+                        umma_f16_ss(tmem + kTmemS + (t % kSB) * kBN, dq + offq, dk + offk, idesc_s,
+                                    k > 0 ? 1u : 0u);
                 }
-                umma_commit(bar(kBarSFull + t % kSBufs));
+                umma_commit(bar(kBarSFull + t % kSB));
             }
             __syncwarp();
         };
-        // O (+)= P(t) V_t, P read from the first kBN / 2 columns of S buffer t mod 3.
+        // O (+)= P(t) V_t, P read from the first kBN / 2 columns of S buffer t mod kSB.
         auto issue_pv = [&](int t, bool first) {
             tc_fence_after();
             const uint64_t dv = sw128_desc(sV(t), L::kKVRegion, 1024);
@@ -468,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (elect_one()) {
 #pragma unroll
                 for (int k = 0; k < kBN / 16; ++k)
-                    umma_f16_ts(tmem + kTmemO, tmem + kTmemS + (t % kSBufs) * kBN + k * 8,
+                    umma_f16_ts(tmem + kTmemO, tmem + kTmemS + (t % kSB) * kBN + k * 8,
                                 dv + k * ((16 * 128) >> 4), idesc_o, k > 0 ? 1u : acc0);
                 umma_commit(bar(kBarPVDone + (t & 1)));
             }
@@ -482,9 +508,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok || u < 0) break;
             const Unit U = decode<kBN, VARLEN>(u, p);
             const int n = U.j1 - U.j0 + 1;
-            ok = wait(kBarQFull, unit_iter & 1);
-            // S for the first min(3, n) blocks
-            for (int x = 0; ok && x < n && x < kSBufs; ++x) {
+            ok = wait(kQT ? kBarQReady : kBarQFull, unit_iter & 1);
+            // S for the first min(kSB, n) blocks
+            for (int x = 0; ok && x < n && x < kSB; ++x) {
                 ok = wait(kBarKFull + (t + x) % kKStages, ((t + x) / kKStages) & 1);
                 if (ok) {
                     issue_s(t + x);
@@ -492,21 +518,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             for (int x = 0; ok && x < n; ++x, ++t) {
-                ok = wait(kBarPFull + t % kSBufs, (t / kSBufs) & 1) &&
+                ok = wait(kBarPFull + t % kSB, (t / kSB) & 1) &&
                      wait(kBarVFull + t % kVStages, (t / kVStages) & 1);
                 if (ok && x == 0 && unit_iter > 0) ok = wait(kBarOFree, (unit_iter - 1) & 1);
                 if (!ok) break;
                 issue_pv(t, x == 0);
                 commit(kBarVEmpty + t % kVStages);
-                if (x + kSBufs < n) {
-                    ok = wait(kBarKFull + (t + kSBufs) % kKStages, ((t + kSBufs) / kKStages) & 1);
+                if (x + kSB < n) {
+                    ok = wait(kBarKFull + (t + kSB) % kKStages, ((t + kSB) / kKStages) & 1);
                     if (!ok) break;
-                    issue_s(t + kSBufs);  // reuses buffer t mod 3 after O += P(t) V_t
-                    commit(kBarKEmpty + (t + kSBufs) % kKStages);
+                    issue_s(t + kSB);  // reuses buffer t mod kSB after O += P(t) V_t
+                    commit(kBarKEmpty + (t + kSB) % kKStages);
                 }
             }
             if (!ok) break;
-            commit(kBarQEmpty);
+            if constexpr (!kQT) commit(kBarQEmpty);
             commit(kBarODone);
         }
         if (!ok && lane == 0) record_timeout(p, abort_flag, kRoleMma, u);
@@ -519,11 +545,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = threadIdx.x & 127;
         const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
         const float sl2 = p.scale_log2;
+        // d = 256: copy the k-th unit's Q tile from shared memory into TMEM, this
+        // thread's row into its lane (128-byte swizzle: 16-byte chunk c of row r sits
+        // at chunk c ^ (r mod 8) of the row), then release both copies' barriers.
+        auto copy_q = [&](int k) -> bool {
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarQFull), k & 1, abort_flag, budget)))
+                return false;
+#pragma unroll
+            for (int g = 0; g < L::kRegions; ++g) {
+                uint32_t w[32];
+                const uint8_t *src = smem + L::kQ + g * L::kQRegion + row * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(src + ((c ^ (row & 7)) << 4));
+                    w[4 * c] = v.x;
+                    w[4 * c + 1] = v.y;
+                    w[4 * c + 2] = v.z;
+                    w[4 * c + 3] = v.w;
+                }
+                tmem_st32(tl + kTmemQ + g * 32, w);
+            }
+            tmem_st_wait();
+            mbar_arrive(bar(kBarQEmpty));
+            tc_fence_before();
+            mbar_arrive(bar(kBarQReady));
+            return true;
+        };
         int t = 0;
         bool ok = true;
-        int unit_iter = 0, u = -1;
+        int unit_iter = 0, u = -1, u_next = -1;
         for (; ok; ++unit_iter) {
-            u = take_unit(unit_iter, ok);
+            if (kQT && unit_iter > 0) {
+                u = u_next;  // taken, and its Q copied, before the previous unit's epilogue
+            } else {
+                u = take_unit(unit_iter, ok);
+                if (ok && kQT && u >= 0) ok = copy_q(unit_iter);
+            }
             if (!ok || u < 0) break;
             const Unit U = decode<kBN, VARLEN>(u, p);
             const int r = U.r0 + row;  // row of the space
@@ -535,8 +592,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int hi_first = min(U.nk - 1, U.qmin + U.q_off + p.wr);
             float m = -INFINITY, l = 0.f;
             for (int j = U.j0; j <= U.j1; ++j, ++t) {
-                const uint32_t tS = tl + kTmemS + (t % kSBufs) * kBN;
-                ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarSFull + t % kSBufs), (t / kSBufs) & 1,
+                const uint32_t tS = tl + kTmemS + (t % kSB) * kBN;
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarSFull + t % kSB), (t / kSB) & 1,
                                                                abort_flag, budget));
                 if (!ok) break;
                 tc_fence_after();
@@ -615,9 +672,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(bar(kBarPFull + t % kSBufs));
+                mbar_arrive(bar(kBarPFull + t % kSB));
             }
             if (!ok) break;
+            if constexpr (kQT) {
+                // every S of this unit has completed (its last S buffer was read), so
+                // the next unit's Q can replace this one's in TMEM during the epilogue
+                u_next = take_unit(unit_iter + 1, ok);
+                if (ok && u_next >= 0) ok = copy_q(unit_iter + 1);
+                if (!ok) break;
+            }
             // ---- epilogue: O / l rounded to 16 bit, LSE = ln 2 (m + log2 l)
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarODone), unit_iter & 1, abort_flag, budget));
             if (!ok) break;
