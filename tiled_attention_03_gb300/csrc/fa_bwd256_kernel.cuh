@@ -20,8 +20,12 @@
 //            X = K_j Q_i^T, Y = V_j dO_i^T, A = P^T (Y - D), dK_j += A Q_i.
 //   dV pass: rows = 128 keys; K_j resident; Q_i (+ L), dO_i streamed.
 //            X = K_j Q_i^T, A = P^T, dV_j += A dO_i.
-// X and Y are M = 128, N = 64, K = 256 products (K-major operands in shared
-// memory); A is written by the compute warps as 16-bit pairs into TMEM over X's
+// X and Y are M = 128, N = 64, K = 256 products (K-major operands). X takes its
+// resident operand from TMEM, where the compute warps copy the first resident tile
+// at the start of each unit: from shared memory, both operands of an N = 64
+// product are 6 KB per 32-cycle MMA, more than the SM's 128 bytes per cycle of
+// shared-memory bandwidth. Y reads both from shared memory (TMEM has no room for
+// the second resident tile). A is written by the compute warps as 16-bit pairs into TMEM over X's
 // columns and the accumulation is an M = 128, N = 256, K = 64 product with A from
 // TMEM and B (the streamed tile, 64 rows of 256 columns) MN-major. The scores are
 // recomputed once per pass (S three times in all, against twice in the d <= 128
@@ -64,9 +68,10 @@ constexpr int kStrBytes = kRegions * kStrRegion;  // 32 KB
 constexpr int kVecSlots = 3;  // ring of the streamed tiles' row-term vectors (see the producer)
 
 // TMEM columns: X (fp32, 64), then A (16-bit pairs) over its first 32; Y (fp32, 64);
-// the accumulator (fp32, 256).
+// the first resident tile (16-bit pairs, 128); the accumulator (fp32, 256).
 constexpr uint32_t kTmemX = 0;
 constexpr uint32_t kTmemY = 64;
+constexpr uint32_t kTmemR0 = 128;
 constexpr uint32_t kTmemAcc = 256;
 
 template <int PASS>
@@ -106,7 +111,8 @@ enum : int {
     kBarUnitFull = kBarAccFree + 1,  // + slot (2)
     kBarUnitEmpty = kBarUnitFull + 2,
     kBarDrain = kBarUnitEmpty + 2,
-    kNumBarsUsed = kBarDrain + 1,
+    kBarR0Ready = kBarDrain + 1,     // first resident tile copied into TMEM
+    kNumBarsUsed = kBarR0Ready + 1,
 };
 static_assert(kNumBarsUsed <= Layout<0>::kNumBars, "barrier slots");
 constexpr int kUnitSlots = 2;
@@ -286,6 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(kBarUnitEmpty + k), kUnitConsumers);
         }
         mbar_init(bar(kBarDrain), 1);
+        mbar_init(bar(kBarR0Ready), 128);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmR0);
@@ -443,6 +450,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
         };
+        // The same with A the first resident tile in TMEM (K-step k: 8 columns).
+        auto issue_x_t = [&](uint32_t b_s, uint32_t dcol) {
+            tc_fence_after();
+            const uint64_t db = swz_desc<128>(b_s, 16);
+            if (elect_one()) {
+#pragma unroll
+                for (int k = 0; k < kD / 16; ++k) {
+                    const uint32_t ob = (k / 4) * (kStrRegion >> 4) + (k % 4) * 2;
+                    umma_f16_ts(tmem + dcol, tmem + kTmemR0 + 8 * k, db + ob, idesc_x, k > 0 ? 1u : 0u);
+                }
+            }
+            __syncwarp();
+        };
         // acc[128 x 256] (+)= A[128 x 64] B[64 x 256]: A 16-bit pairs in TMEM over X's
         // columns, B the streamed tile MN-major (its 64-column regions 8 KB apart,
         // 16 rows = 2 KB per K-step).
@@ -463,12 +483,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             u = take_unit(unit_iter, ok);
             if (!ok || u < 0) break;
             const Unit U = decode<PASS, VARLEN>(u, p);
-            ok = wait(kBarResFull, unit_iter & 1);
+            ok = wait(kBarResFull, unit_iter & 1) && wait(kBarR0Ready, unit_iter & 1);
             for (int t = 0; ok && t < U.n_t; ++t, ++it) {
                 const int s0 = it % kS0, s1 = it % kS1;
                 ok = wait(kBarS0Full + s0, (it / kS0) & 1);
                 if (!ok) break;
-                issue_x(sR0, sS0(it), kTmemX);
+                issue_x_t(sS0(it), kTmemX);
                 commit(kBarXFull);
                 if constexpr (kHasY) {
                     ok = wait(kBarS1Full + s1, (it / kS1) & 1);
@@ -514,12 +534,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Unit U = decode<PASS, VARLEN>(u, p);
             const int row = U.r0 + r;  // query (dQ pass) or key of this thread, in its sequence
             const bool row_ok = row < (PASS == kPassDQ ? U.nq : U.nk);
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarResFull), unit_iter & 1, abort_flag,
+                                                           budget));
+            if (!ok) break;
+            // The first resident tile into TMEM, this thread's row into its lane (128-byte
+            // swizzle: 16-byte chunk c of row r sits at chunk c ^ (r mod 8)). Every MMA of
+            // the previous unit has completed (its accumulator was read).
+#pragma unroll
+            for (int g = 0; g < kRegions; ++g) {
+                uint32_t w[32];
+                const uint8_t *src = smem + L::kRes0 + g * kResRegion + r * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(src + ((c ^ (r & 7)) << 4));
+                    w[4 * c] = v.x;
+                    w[4 * c + 1] = v.y;
+                    w[4 * c + 2] = v.z;
+                    w[4 * c + 3] = v.w;
+                }
+                tmem_st32(tl + kTmemR0 + g * 32, w);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar(kBarR0Ready));
             // dQ pass: this row's L and D, resident for the unit
             float Lrow = 0.f, Drow = 0.f;
             if constexpr (PASS == kPassDQ) {
-                ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarResFull), unit_iter & 1,
-                                                               abort_flag, budget));
-                if (!ok) break;
                 Lrow = vec[r];
                 Drow = vec[kRows + r];
             }
