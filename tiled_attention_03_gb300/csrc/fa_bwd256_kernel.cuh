@@ -68,7 +68,9 @@ constexpr int kStrBytes = kRegions * kStrRegion;  // 32 KB
 constexpr int kVecSlots = 3;  // ring of the streamed tiles' row-term vectors (see the producer)
 
 // TMEM columns: X (fp32, 64), then A (16-bit pairs) over its first 32; Y (fp32, 64);
-// the first resident tile (16-bit pairs, 128); the accumulator (fp32, 256).
+// the first resident tile (16-bit pairs, 128); the accumulator (fp32, 256). The dV
+// pass has no Y and alternates X between columns 0 and 64, so that X(t+1) is formed
+// while the compute warps turn X(t) into A(t).
 constexpr uint32_t kTmemX = 0;
 constexpr uint32_t kTmemY = 64;
 constexpr uint32_t kTmemR0 = 128;
@@ -89,7 +91,7 @@ struct Layout {
     static constexpr int kVec = kStr1 + kS1 * kStrBytes;  // dQ: L_i, D_i (2 x 128); else L, D rings
     static constexpr int kVecBytes = PASS == kPassDQ ? 2 * kRows * 4 : 2 * kVecSlots * kCols * 4;
     static constexpr int kBar = kVec + kVecBytes;
-    static constexpr int kNumBars = 24;
+    static constexpr int kNumBars = 32;
     static constexpr int kMisc = kBar + kNumBars * 8;  // tmem slot, abort flag, unit ring
     static constexpr int kBytes = kMisc + 16;
     static constexpr int kAlloc = kBytes + 1024;       // slack to align the base to 1024 B
@@ -103,10 +105,10 @@ enum : int {
     kBarS0Empty = kBarS0Full + 3,    // + slot
     kBarS1Full = kBarS0Empty + 3,    // + slot (<= 2)
     kBarS1Empty = kBarS1Full + 2,    // + slot
-    kBarXFull = kBarS1Empty + 2,
-    kBarYFull = kBarXFull + 1,
-    kBarAReady = kBarYFull + 1,
-    kBarAccDone = kBarAReady + 1,
+    kBarXFull = kBarS1Empty + 2,     // + X buffer (2)
+    kBarYFull = kBarXFull + 2,
+    kBarAReady = kBarYFull + 1,      // + X buffer (2)
+    kBarAccDone = kBarAReady + 2,
     kBarAccFree = kBarAccDone + 1,
     kBarUnitFull = kBarAccFree + 1,  // + slot (2)
     kBarUnitEmpty = kBarUnitFull + 2,
@@ -246,6 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     using L = Layout<PASS>;
     constexpr int kS0 = L::kS0, kS1 = L::kS1;
     constexpr bool kHasY = PASS != kPassDV;
+    constexpr int kXBufs = kHasY ? 1 : 2;  // X buffers: tile it uses it % kXBufs
+    auto xcol = [](int it) { return kTmemX + static_cast<uint32_t>((it % kXBufs) * 64); };
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -282,9 +286,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(kBarS1Full + s), 1);
             mbar_init(bar(kBarS1Empty + s), 1);
         }
-        mbar_init(bar(kBarXFull), 1);
+        for (int b = 0; b < kXBufs; ++b) {
+            mbar_init(bar(kBarXFull + b), 1);
+            mbar_init(bar(kBarAReady + b), 128);
+        }
         mbar_init(bar(kBarYFull), 1);
-        mbar_init(bar(kBarAReady), 128);
         mbar_init(bar(kBarAccDone), 1);
         mbar_init(bar(kBarAccFree), 128);
         for (int k = 0; k < kUnitSlots; ++k) {
@@ -421,10 +427,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp) {
         // ================================================================ MMA issuer
         // Per streamed tile t (it counts tiles over the CTA's whole sequence):
-        //   X(t) [, Y(t)] ... acc += A(t) B(t) | X(t+1) [, Y(t+1)] ...
-        // X(t+1) overwrites the A(t) that the accumulation before it reads, and Y(t+1)
-        // the Y(t) the compute warps read before signalling A(t): tcgen05.mma
-        // operations of one thread execute in issue order.
+        //   dQ / dK: X(t), Y(t) ... acc += A(t) B(t) | X(t+1), Y(t+1) ...
+        //   dV:      X(t+1) ... acc += A(t) B(t) | X(t+2) ...
+        // An X overwrites the A that the accumulation before it reads, and Y(t+1) the
+        // Y(t) the compute warps read before signalling A(t): tcgen05.mma operations
+        // of one thread execute in issue order.
         constexpr uint32_t idesc_x = idesc_f16_ab(BF16, kRows, kCols, false, false);
         constexpr uint32_t idesc_acc = idesc_f16_ab(BF16, kRows, kD, false, true);
         auto wait = [&](int b, uint32_t parity) {
@@ -466,13 +473,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // acc[128 x 256] (+)= A[128 x 64] B[64 x 256]: A 16-bit pairs in TMEM over X's
         // columns, B the streamed tile MN-major (its 64-column regions 8 KB apart,
         // 16 rows = 2 KB per K-step).
-        auto issue_acc = [&](uint32_t b_s, bool accumulate) {
+        auto issue_acc = [&](uint32_t b_s, uint32_t acol, bool accumulate) {
             tc_fence_after();
             const uint64_t db = swz_desc<128>(b_s, kStrRegion);
             if (elect_one()) {
 #pragma unroll
                 for (int k = 0; k < kCols / 16; ++k)
-                    umma_f16_ts(tmem + kTmemAcc, tmem + kTmemX + 8 * k, db + k * ((16 * 128) >> 4),
+                    umma_f16_ts(tmem + kTmemAcc, tmem + acol + 8 * k, db + k * ((16 * 128) >> 4),
                                 idesc_acc, (k > 0 || accumulate) ? 1u : 0u);
             }
             __syncwarp();
@@ -484,30 +491,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok || u < 0) break;
             const Unit U = decode<PASS, VARLEN>(u, p);
             ok = wait(kBarResFull, unit_iter & 1) && wait(kBarR0Ready, unit_iter & 1);
-            for (int t = 0; ok && t < U.n_t; ++t, ++it) {
-                const int s0 = it % kS0, s1 = it % kS1;
-                ok = wait(kBarS0Full + s0, (it / kS0) & 1);
-                if (!ok) break;
-                issue_x_t(sS0(it), kTmemX);
-                commit(kBarXFull);
-                if constexpr (kHasY) {
+            // X(t) of the unit's tile t (ring position it0 + t) into its buffer
+            auto form_x = [&](int pos) -> bool {
+                if (!wait(kBarS0Full + pos % kS0, (pos / kS0) & 1)) return false;
+                issue_x_t(sS0(pos), xcol(pos));
+                commit(kBarXFull + pos % kXBufs);
+                return true;
+            };
+            if constexpr (PASS == kPassDV) {
+                // X one tile ahead: X(t+1) goes into the other buffer before A(t) is
+                // awaited, and the accumulation of A(t) precedes X(t+2), which
+                // overwrites it (one thread's MMAs execute in issue order).
+                if (ok && U.n_t > 0) ok = form_x(it);
+                for (int t = 0; ok && t < U.n_t; ++t, ++it) {
+                    if (t + 1 < U.n_t && !(ok = form_x(it + 1))) break;
+                    ok = wait(kBarAReady + it % kXBufs, (it / kXBufs) & 1);
+                    if (ok && t == 0 && unit_iter > 0) ok = wait(kBarAccFree, (unit_iter - 1) & 1);
+                    if (!ok) break;
+                    commit(kBarS0Empty + it % kS0);  // Q_i: X was its one product reader
+                    ok = wait(kBarS1Full + it % kS1, (it / kS1) & 1);
+                    if (!ok) break;
+                    issue_acc(sS1(it), xcol(it), t > 0);  // dV += P^T dO_i
+                    commit(kBarS1Empty + it % kS1);
+                }
+            } else {
+                for (int t = 0; ok && t < U.n_t; ++t, ++it) {
+                    const int s0 = it % kS0, s1 = it % kS1;
+                    if (!(ok = form_x(it))) break;
                     ok = wait(kBarS1Full + s1, (it / kS1) & 1);
                     if (!ok) break;
                     issue_x(sR1, sS1(it), kTmemY);
                     commit(kBarYFull);
                     commit(kBarS1Empty + s1);  // V_j / dO_i: Y was its one reader
-                }
-                ok = wait(kBarAReady, it & 1);
-                if (ok && t == 0 && unit_iter > 0) ok = wait(kBarAccFree, (unit_iter - 1) & 1);
-                if (!ok) break;
-                if constexpr (PASS == kPassDV) {
-                    commit(kBarS0Empty + s0);  // Q_i: X was its one product reader
-                    ok = wait(kBarS1Full + s1, (it / kS1) & 1);
+                    ok = wait(kBarAReady, it & 1);
+                    if (ok && t == 0 && unit_iter > 0) ok = wait(kBarAccFree, (unit_iter - 1) & 1);
                     if (!ok) break;
-                    issue_acc(sS1(it), t > 0);  // dV += P^T dO_i
-                    commit(kBarS1Empty + s1);
-                } else {
-                    issue_acc(sS0(it), t > 0);  // dQ += dS K_j, dK += dS^T Q_i
+                    issue_acc(sS0(it), kTmemX, t > 0);  // dQ += dS K_j, dK += dS^T Q_i
                     commit(kBarS0Empty + s0);
                 }
             }
@@ -566,14 +585,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = 0; t < U.n_t; ++t, ++it) {
                 int head, c0;
                 tile_of<PASS>(U, t, p, head, c0);  // column c is streamed row c0 + c
-                ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarXFull), it & 1, abort_flag, budget));
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarXFull + it % kXBufs),
+                                                               (it / kXBufs) & 1, abort_flag, budget));
                 if (!ok) break;
                 tc_fence_after();
                 float x[kCols];
                 {
                     uint32_t a[32], b[32];
-                    tmem_ld32(tl + kTmemX, a);
-                    tmem_ld32(tl + kTmemX + 32, b);
+                    tmem_ld32(tl + xcol(it), a);
+                    tmem_ld32(tl + xcol(it) + 32, b);
                     tmem_ld_wait(a);
                     tmem_ld_wait(b);
 #pragma unroll
@@ -644,12 +664,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t pk[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) pk[e] = pack2<BF16>(x[2 * e], x[2 * e + 1]);
-                    tmem_st16(tl + kTmemX, pk);
-                    tmem_st16(tl + kTmemX + 16, pk + 16);
+                    tmem_st16(tl + xcol(it), pk);
+                    tmem_st16(tl + xcol(it) + 16, pk + 16);
                 }
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(bar(kBarAReady));
+                mbar_arrive(bar(kBarAReady + it % kXBufs));
             }
             if (!ok) break;
             // ---- epilogue: the row of the accumulator times out_scale, in 16 bit
