@@ -148,6 +148,9 @@ VARLEN_WORKLOADS = [
     # its backward (dO drawn like the dense backward workloads, then packed)
     Workload("bwd_varlen_causal_b16h32n4096d128", 16, 32, 4096, 128, torch.bfloat16, MASK_CAUSAL,
              0, 0, seed=12, varlen=True, backward=True),
+    # and at head dimension 256
+    Workload("bwd_varlen_causal_b16h16n4096d256", 16, 16, 4096, 256, torch.bfloat16, MASK_CAUSAL,
+             0, 0, seed=23, varlen=True, backward=True),
 ]
 
 BY_NAME = {w.name: w for w in WORKLOADS + EXTRA_WORKLOADS + BWD_WORKLOADS + VARLEN_WORKLOADS}
