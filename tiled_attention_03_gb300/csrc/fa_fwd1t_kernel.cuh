@@ -360,9 +360,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // units whose key split holds no key of theirs are skipped here; a
                 // CTA's first unit is the one numbered like the CTA (no counter round
                 // trip at start-up), the counter numbers the rest from gridDim.x on
+                // (when the grid covers every unit, nothing is left to count)
                 int v = -1;
-                unsigned next = k == 0 ? blockIdx.x : gridDim.x + atomicAdd(p.sched, 1u);
-                for (;; next = gridDim.x + atomicAdd(p.sched, 1u)) {
+                auto take_next = [&]() -> unsigned {
+                    return static_cast<unsigned>(p.n_units) <= gridDim.x
+                               ? static_cast<unsigned>(p.n_units)
+                               : gridDim.x + atomicAdd(p.sched, 1u);
+                };
+                unsigned next = k == 0 ? blockIdx.x : take_next();
+                for (;; next = take_next()) {
                     if (next >= static_cast<unsigned>(p.n_units)) break;
                     const Unit W = decode<kBN, VARLEN>(static_cast<int>(next), p);
                     if (W.j0 <= W.j1) {
@@ -740,7 +746,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
-    if (threadIdx.x == 0) {
+    // The last CTA to finish zeroes this launch's scheduler counters (untouched when
+    // the grid covered every unit).
+    if (threadIdx.x == 0 && static_cast<unsigned>(p.n_units) > gridDim.x) {
         __threadfence();
         if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
             atomicExch(p.sched, 0u);
