@@ -296,6 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
+    int pre_k = -1;  // K tiles of the first unit requested during setup (-1: none, nor Q)
     if (threadIdx.x == kTmaWarp * 32) {
         mbar_init(bar(kBarQFull), 1);
         // Q's shared-memory copy is released by the MMA warp's commit, or at d = 256
@@ -328,6 +329,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
+        // The CTA's first unit is its own index (when it has work): its Q tile and
+        // first K tiles are requested now, while the other warps still set up; the
+        // producer loop below skips them.
+        if (blockIdx.x < static_cast<unsigned>(p.n_units)) {
+            const Unit W = decode<kBN, VARLEN>(static_cast<int>(blockIdx.x), p);
+            if (W.j0 <= W.j1) {
+                mbar_arrive_expect_tx(bar(kBarQFull), L::kQBytes);
+                int qy, qz;
+                q_coords<VARLEN>(W, qy, qz);
+                for (int g = 0; g < L::kRegions; ++g)
+                    tma_load_3d(sQ + g * L::kQRegion, &tmQ, bar(kBarQFull), 64 * g, qy, qz);
+                pre_k = min(kKStages, W.j1 - W.j0 + 1);
+                for (int x = 0; x < pre_k; ++x) {
+                    if (x == p.fault_skip_k) continue;
+                    int ky, kz;
+                    kv_coords<VARLEN>(W, W.j0 + x, kBN, ky, kz);
+                    mbar_arrive_expect_tx(bar(kBarKFull + x), L::kKVBytes);
+                    for (int g = 0; g < L::kRegions; ++g)
+                        tma_load_3d(sK(x) + g * L::kKVRegion, &tmK, bar(kBarKFull + x), 64 * g, ky, kz);
+                }
+            }
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -383,13 +406,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             int u = publish(0);
             for (; ok && u >= 0; ++unit_iter) {
                 const Unit U = decode<kBN, VARLEN>(u, p);
-                ok = mbar_wait_bounded(bar(kBarQEmpty), (unit_iter & 1) ^ 1, abort_flag, budget);
-                if (!ok) break;
-                mbar_arrive_expect_tx(bar(kBarQFull), L::kQBytes);
-                int qy, qz;
-                q_coords<VARLEN>(U, qy, qz);
-                for (int g = 0; g < L::kRegions; ++g)
-                    tma_load_3d(sQ + g * L::kQRegion, &tmQ, bar(kBarQFull), 64 * g, qy, qz);
+                const bool early = unit_iter == 0 && pre_k >= 0;  // Q and K(0 .. pre_k-1) in flight
+                if (!early) {
+                    ok = mbar_wait_bounded(bar(kBarQEmpty), (unit_iter & 1) ^ 1, abort_flag, budget);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar(kBarQFull), L::kQBytes);
+                    int qy, qz;
+                    q_coords<VARLEN>(U, qy, qz);
+                    for (int g = 0; g < L::kRegions; ++g)
+                        tma_load_3d(sQ + g * L::kQRegion, &tmQ, bar(kBarQFull), 64 * g, qy, qz);
+                }
                 ++q_loads;
                 int u_next = -1;
                 bool claimed = false;
@@ -405,6 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int g = 0; g < L::kRegions; ++g) tma_prefetch_l2_3d(&tmQ, 64 * g, wy, wz);
                         }
                     }
+                    if (early && t < pre_k) continue;  // requested during setup
                     const int st = t % kKStages;
                     ok = mbar_wait_bounded(bar(kBarKEmpty + st), ((t / kKStages) & 1) ^ 1, abort_flag, budget);
                     if (!ok) break;
