@@ -114,7 +114,8 @@ enum : int {
     kBarUnitEmpty = kBarUnitFull + 2,
     kBarDrain = kBarUnitEmpty + 2,
     kBarR0Ready = kBarDrain + 1,     // first resident tile copied into TMEM
-    kNumBarsUsed = kBarR0Ready + 1,
+    kBarXRead = kBarR0Ready + 1,     // dQ / dK passes: the compute warps have loaded X
+    kNumBarsUsed = kBarXRead + 1,
 };
 static_assert(kNumBarsUsed <= Layout<0>::kNumBars, "barrier slots");
 constexpr int kUnitSlots = 2;
@@ -299,6 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(bar(kBarDrain), 1);
         mbar_init(bar(kBarR0Ready), 128);
+        mbar_init(bar(kBarXRead), 128);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmR0);
@@ -427,11 +429,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp) {
         // ================================================================ MMA issuer
         // Per streamed tile t (it counts tiles over the CTA's whole sequence):
-        //   dQ / dK: X(t), Y(t) ... acc += A(t) B(t) | X(t+1), Y(t+1) ...
-        //   dV:      X(t+1) ... acc += A(t) B(t) | X(t+2) ...
-        // An X overwrites the A that the accumulation before it reads, and Y(t+1) the
-        // Y(t) the compute warps read before signalling A(t): tcgen05.mma operations
-        // of one thread execute in issue order.
+        //   dQ / dK: ... X(t+1) ... acc += A(t) B(t) | Y(t+1) | X(t+2) ...
+        //   dV:      ... X(t+1) ... acc += A(t) B(t) | X(t+2) ...
+        // A(t) lies over Y's columns (dQ, dK) or over X(t)'s buffer (dV), and the
+        // product that overwrites it (Y(t+1), X(t+2)) follows the accumulation that
+        // reads it; X(t+1) waits until the compute warps have loaded X(t) (dQ, dK) or
+        // goes to the other buffer (dV): tcgen05.mma operations of one thread execute
+        // in issue order.
         constexpr uint32_t idesc_x = idesc_f16_ab(BF16, kRows, kCols, false, false);
         constexpr uint32_t idesc_acc = idesc_f16_ab(BF16, kRows, kD, false, true);
         auto wait = [&](int b, uint32_t parity) {
@@ -515,19 +519,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     commit(kBarS1Empty + it % kS1);
                 }
             } else {
-                for (int t = 0; ok && t < U.n_t; ++t, ++it) {
-                    const int s0 = it % kS0, s1 = it % kS1;
-                    if (!(ok = form_x(it))) break;
-                    ok = wait(kBarS1Full + s1, (it / kS1) & 1);
-                    if (!ok) break;
-                    issue_x(sR1, sS1(it), kTmemY);
+                // A(t) goes over Y's columns, so X(t+1) can run while the compute warps
+                // form A(t) (once they have loaded X(t)); Y(t+1) follows the
+                // accumulation that reads A(t).
+                auto form_y = [&](int pos) -> bool {
+                    if (!wait(kBarS1Full + pos % kS1, (pos / kS1) & 1)) return false;
+                    issue_x(sR1, sS1(pos), kTmemY);
                     commit(kBarYFull);
-                    commit(kBarS1Empty + s1);  // V_j / dO_i: Y was its one reader
+                    commit(kBarS1Empty + pos % kS1);  // V_j / dO_i: Y was its one reader
+                    return true;
+                };
+                if (ok && U.n_t > 0) ok = form_x(it) && form_y(it);
+                for (int t = 0; ok && t < U.n_t; ++t, ++it) {
+                    if (t + 1 < U.n_t && !(ok = wait(kBarXRead, it & 1) && form_x(it + 1))) break;
                     ok = wait(kBarAReady, it & 1);
                     if (ok && t == 0 && unit_iter > 0) ok = wait(kBarAccFree, (unit_iter - 1) & 1);
                     if (!ok) break;
-                    issue_acc(sS0(it), kTmemX, t > 0);  // dQ += dS K_j, dK += dS^T Q_i
-                    commit(kBarS0Empty + s0);
+                    issue_acc(sS0(it), kTmemY, t > 0);  // dQ += dS K_j, dK += dS^T Q_i
+                    commit(kBarS0Empty + it % kS0);
+                    if (t + 1 < U.n_t && !(ok = form_y(it + 1))) break;
                 }
             }
             if (!ok) break;
@@ -602,6 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         x[c + 32] = __uint_as_float(b[c]);
                     }
                 }
+                if constexpr (kHasY) mbar_arrive(bar(kBarXRead));  // X may be overwritten
                 // P = 2^(x scale log2 e - L) with L of the query: the row's (dQ pass) or
                 // the column's (the streamed query rows' L, from the vector ring)
                 const int vs = it % kVecSlots;
@@ -659,13 +670,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         x[c + 1] = y1;
                     }
                 }
-                // A as 16-bit pairs over X's first 32 columns
+                // A as 16-bit pairs over the first 32 columns of Y (dQ, dK: this thread
+                // has read its Y row) or of X (dV)
                 {
+                    const uint32_t acol = kHasY ? kTmemY : xcol(it);
                     uint32_t pk[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) pk[e] = pack2<BF16>(x[2 * e], x[2 * e + 1]);
-                    tmem_st16(tl + xcol(it), pk);
-                    tmem_st16(tl + xcol(it) + 16, pk + 16);
+                    tmem_st16(tl + acol, pk);
+                    tmem_st16(tl + acol + 16, pk + 16);
                 }
                 tmem_st_wait();
                 tc_fence_before();
