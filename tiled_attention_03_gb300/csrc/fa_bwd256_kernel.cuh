@@ -12,8 +12,8 @@
 // 128 x 256 fp32 accumulator takes 256 of the SM's 512 tensor-memory columns, so
 // the d <= 128 layout (K_j, V_j, Q_i and dO_i tiles in shared memory, dK_j and dV_j
 // both in TMEM) would need 256 KB and 768 columns. Here each gradient has its own
-// pass. A pass keeps the 128 rows it accumulates for (its "resident" tiles) in
-// shared memory and streams the other side in tiles of 64 rows:
+// pass. A pass keeps the 128 rows it accumulates for (its "resident" tiles) on the
+// SM and streams the other side in tiles of 64 rows:
 //   dQ pass: rows = 128 queries; Q_i, dO_i, L_i, D_i resident; K_j, V_j streamed.
 //            X = Q_i K_j^T, Y = dO_i V_j^T, A = P (Y - D), dQ_i += A K_j.
 //   dK pass: rows = 128 keys; K_j, V_j resident; Q_i (+ L), dO_i (+ D) streamed.
@@ -21,13 +21,15 @@
 //   dV pass: rows = 128 keys; K_j resident; Q_i (+ L), dO_i streamed.
 //            X = K_j Q_i^T, A = P^T, dV_j += A dO_i.
 // X and Y are M = 128, N = 64, K = 256 products (K-major operands). X takes its
-// resident operand from TMEM, where the compute warps copy the first resident tile
-// at the start of each unit: from shared memory, both operands of an N = 64
-// product are 6 KB per 32-cycle MMA, more than the SM's 128 bytes per cycle of
-// shared-memory bandwidth. Y reads both from shared memory (TMEM has no room for
-// the second resident tile). A is written by the compute warps as 16-bit pairs into TMEM over X's
-// columns and the accumulation is an M = 128, N = 256, K = 64 product with A from
-// TMEM and B (the streamed tile, 64 rows of 256 columns) MN-major. The scores are
+// resident operand from TMEM, where the compute warps load the first resident tile
+// (each thread its row, from global memory) before each unit: from shared memory,
+// both operands of an N = 64 product are 6 KB per 32-cycle MMA, more than the SM's
+// 128 bytes per cycle of shared-memory bandwidth, and the 64 KB the tile no longer
+// takes there deepen the streamed rings. Y reads both operands from shared memory
+// (TMEM has no room for the second resident tile). A is written by the compute warps
+// as 16-bit pairs into TMEM (over Y's columns, or over X's in the dV pass) and the
+// accumulation is an M = 128, N = 256, K = 64 product with A from TMEM and B (the
+// streamed tile, 64 rows of 256 columns) MN-major. The scores are
 // recomputed once per pass (S three times in all, against twice in the d <= 128
 // kernels), the price of fitting one SM.
 //
@@ -65,7 +67,6 @@ constexpr int kResRegion = kRows * 128;  // 16 KB
 constexpr int kStrRegion = kCols * 128;  // 8 KB
 constexpr int kResBytes = kRegions * kResRegion;  // 64 KB
 constexpr int kStrBytes = kRegions * kStrRegion;  // 32 KB
-constexpr int kVecSlots = 3;  // ring of the streamed tiles' row-term vectors (see the producer)
 
 // TMEM columns: X (fp32, 64), then A (16-bit pairs) over its first 32; Y (fp32, 64);
 // the first resident tile (16-bit pairs, 128); the accumulator (fp32, 256). The dV
@@ -78,18 +79,22 @@ constexpr uint32_t kTmemAcc = 256;
 
 template <int PASS>
 struct Layout {
-    // The second resident tile (dO_i in the dQ pass, V_j in the dK pass).
+    // The second resident tile (dO_i in the dQ pass, V_j in the dK pass), the one
+    // kept in shared memory (the first lives in TMEM).
     static constexpr bool kRes1 = PASS != kPassDV;
     // Ring depths of the two streamed tiles: s0 (K_j in the dQ pass, Q_i in the
     // others) and s1 (V_j, or dO_i), as deep as shared memory allows.
-    static constexpr int kS0 = PASS == kPassDV ? 3 : 2;
-    static constexpr int kS1 = PASS == kPassDV ? 2 : 1;
-    static constexpr int kRes0 = 0;
-    static constexpr int kRes1Off = kRes0 + kResBytes;
+    static constexpr int kS0 = PASS == kPassDV ? 4 : 3;
+    static constexpr int kS1 = PASS == kPassDV ? 3 : 2;
+    static constexpr int kRes1Off = 0;
     static constexpr int kStr0 = kRes1Off + (kRes1 ? kResBytes : 0);
     static constexpr int kStr1 = kStr0 + kS0 * kStrBytes;
     static constexpr int kVec = kStr1 + kS1 * kStrBytes;  // dQ: L_i, D_i (2 x 128); else L, D rings
-    static constexpr int kVecBytes = PASS == kPassDQ ? 2 * kRows * 4 : 2 * kVecSlots * kCols * 4;
+    // ring of the streamed tiles' row-term vectors (L, and D in the dK pass), as
+    // deep as the s0 ring (see the producer)
+    static constexpr int kVecSlots = kS0;
+    static constexpr int kVecBytes =
+        PASS == kPassDQ ? 2 * kRows * 4 : (PASS == kPassDK ? 2 : 1) * kVecSlots * kCols * 4;
     static constexpr int kBar = kVec + kVecBytes;
     static constexpr int kNumBars = 32;
     static constexpr int kMisc = kBar + kNumBars * 8;  // tmem slot, abort flag, unit ring
@@ -101,11 +106,11 @@ struct Layout {
 enum : int {
     kBarResFull = 0,
     kBarResEmpty = 1,
-    kBarS0Full = 2,                  // + slot (<= 3)
-    kBarS0Empty = kBarS0Full + 3,    // + slot
-    kBarS1Full = kBarS0Empty + 3,    // + slot (<= 2)
-    kBarS1Empty = kBarS1Full + 2,    // + slot
-    kBarXFull = kBarS1Empty + 2,     // + X buffer (2)
+    kBarS0Full = 2,                  // + slot (<= 4)
+    kBarS0Empty = kBarS0Full + 4,    // + slot
+    kBarS1Full = kBarS0Empty + 4,    // + slot (<= 3)
+    kBarS1Empty = kBarS1Full + 3,    // + slot
+    kBarXFull = kBarS1Empty + 3,     // + X buffer (2)
     kBarYFull = kBarXFull + 2,
     kBarAReady = kBarYFull + 1,      // + X buffer (2)
     kBarAccDone = kBarAReady + 2,
@@ -140,6 +145,7 @@ struct Params {
     // of sequence b, head h start at h * vstride + cu_pad[b]; n_blk counts 128-row
     // blocks of the longest sequence's resident side.
     const int *cu_q, *cu_k, *cu_pad;
+    const void *res0;         // the first resident tile's tensor: Q (dQ pass) or K
     int total_q, total_k, vstride;
 };
 
@@ -240,14 +246,16 @@ __device__ __forceinline__ void record_timeout(const Params &p, volatile int *ab
 
 // The resident tiles are read through a 128-row TMA map of their tensor, the
 // streamed ones through a 64-row map: tmR0 / tmR1 (Q / dO in the dQ pass, K / V
-// otherwise) and tmS0 / tmS1 (K / V in the dQ pass, Q / dO otherwise).
+// otherwise) and tmS0 / tmS1 (K / V in the dQ pass, Q / dO otherwise). The first
+// resident tile is read by the compute warps from p.res0; tmR0 serves its L2
+// prefetch.
 template <int PASS, bool BF16, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd256_kernel(const __grid_constant__ CUtensorMap tmR0, const __grid_constant__ CUtensorMap tmR1,
                      const __grid_constant__ CUtensorMap tmS0, const __grid_constant__ CUtensorMap tmS1,
                      const Params p) {
     using L = Layout<PASS>;
-    constexpr int kS0 = L::kS0, kS1 = L::kS1;
+    constexpr int kS0 = L::kS0, kS1 = L::kS1, kVecSlots = L::kVecSlots;
     constexpr bool kHasY = PASS != kPassDV;
     constexpr int kXBufs = kHasY ? 1 : 2;  // X buffers: tile it uses it % kXBufs
     auto xcol = [](int it) { return kTmemX + static_cast<uint32_t>((it % kXBufs) * 64); };
@@ -255,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t sR0 = sbase + L::kRes0, sR1 = sbase + L::kRes1Off;
+    const uint32_t sR1 = sbase + L::kRes1Off;
     auto sS0 = [sbase](int it) { return sbase + L::kStr0 + (it % kS0) * kStrBytes; };
     auto sS1 = [sbase](int it) { return sbase + L::kStr1 + (it % kS1) * kStrBytes; };
     // row-term vectors: dQ pass L_i, D_i (128 each); dK / dV passes the L (and D) of
@@ -355,16 +363,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 if (unit_iter != p.fault_unit) {
                     constexpr uint32_t kResTx =
-                        (L::kRes1 ? 2 : 1) * kResBytes + (PASS == kPassDQ ? 2 * kRows * 4 : 0);
+                        (L::kRes1 ? kResBytes : 0) + (PASS == kPassDQ ? 2 * kRows * 4 : 0);
                     mbar_arrive_expect_tx(bar(kBarResFull), kResTx);
                     int ry, rz;
                     coords<VARLEN>(U.head, PASS == kPassDQ ? p.H : p.Hkv,
                                    PASS == kPassDQ ? U.q_tok0 : U.k_tok0, U.r0, ry, rz);
-                    for (int g = 0; g < kRegions; ++g) {
-                        tma_load_3d(sR0 + g * kResRegion, &tmR0, bar(kBarResFull), 64 * g, ry, rz);
-                        if constexpr (L::kRes1)
+                    if constexpr (L::kRes1)
+                        for (int g = 0; g < kRegions; ++g)
                             tma_load_3d(sR1 + g * kResRegion, &tmR1, bar(kBarResFull), 64 * g, ry, rz);
-                    }
                     if constexpr (PASS == kPassDQ) {
                         const size_t vrow = vec_row<VARLEN>(U, U.head, U.r0, p);
                         bulk_load(sVec, p.Lw + vrow, kRows * 4, bar(kBarResFull));
@@ -374,6 +380,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++res_loads;
                 const int u_next = publish(unit_iter + 1);
                 if (!ok) break;
+                if (u_next >= 0) {
+                    // the next unit's first resident rows into L2 for the compute warps
+                    const Unit W = decode<PASS, VARLEN>(u_next, p);
+                    int wy, wz;
+                    coords<VARLEN>(W.head, PASS == kPassDQ ? p.H : p.Hkv,
+                                   PASS == kPassDQ ? W.q_tok0 : W.k_tok0, W.r0, wy, wz);
+                    for (int g = 0; g < kRegions; ++g) tma_prefetch_l2_3d(&tmR0, 64 * g, wy, wz);
+                }
                 for (int t = 0; ok && t < U.n_t; ++t, ++it) {
                     int head, row0;
                     tile_of<PASS>(U, t, p, head, row0);
@@ -382,8 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // this thread has waited for s0's slot of tile it - kS0 to be free,
                     // which the MMA warp signals only after the compute warps finished
                     // tile it - kS0 (dK pass: after its accumulation; dV pass: after its
-                    // A was ready), so tile it - 3 and every older one are done with
-                    // their vectors.
+                    // A was ready), so tile it - kS0 and every older one are done with
+                    // their vectors, and the kS0 - 1 tiles after it hold the other slots.
                     const size_t vrow = PASS == kPassDQ ? 0 : vec_row<VARLEN>(U, head, row0, p);
                     const int vs = it % kVecSlots;
                     int sy, sz;
@@ -555,37 +569,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = threadIdx.x;  // resident row = TMEM lane
         const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
         const float sl2 = p.scale_log2;
-        int it = 0, unit_iter = 0, u = -1;
-        bool ok = true;
-        for (; ok; ++unit_iter) {
-            u = take_unit(unit_iter, ok);
-            if (!ok || u < 0) break;
-            const Unit U = decode<PASS, VARLEN>(u, p);
-            const int row = U.r0 + r;  // query (dQ pass) or key of this thread, in its sequence
-            const bool row_ok = row < (PASS == kPassDQ ? U.nq : U.nk);
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarResFull), unit_iter & 1, abort_flag,
-                                                           budget));
-            if (!ok) break;
-            // The first resident tile into TMEM, this thread's row into its lane (128-byte
-            // swizzle: 16-byte chunk c of row r sits at chunk c ^ (r mod 8)). Every MMA of
-            // the previous unit has completed (its accumulator was read).
+        // Unit uu's first resident tile into TMEM: this thread's row (512 contiguous
+        // bytes, zeros past the rows) into its lane, 16-bit pairs in column order.
+        // Called once every X of the previous unit has completed.
+        auto load_r0 = [&](int uu) {
+            const Unit W = decode<PASS, VARLEN>(uu, p);
+            const int wrow = W.r0 + r;
+            const bool wok = wrow < (PASS == kPassDQ ? W.nq : W.nk);
+            size_t grow;
+            if constexpr (VARLEN) {
+                const int heads = PASS == kPassDQ ? p.H : p.Hkv;
+                grow = (static_cast<size_t>(PASS == kPassDQ ? W.q_tok0 : W.k_tok0) + (wok ? wrow : 0)) * heads +
+                       W.head % heads;
+            } else {
+                grow = static_cast<size_t>(W.head) * p.N + (wok ? wrow : 0);
+            }
+            const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(p.res0) +
+                                                               grow * (kD * 2));
+            uint4 v[kD / 8];
+#pragma unroll
+            for (int c = 0; c < kD / 8; ++c) v[c] = wok ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
             for (int g = 0; g < kRegions; ++g) {
                 uint32_t w[32];
-                const uint8_t *src = smem + L::kRes0 + g * kResRegion + r * 128;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(src + ((c ^ (r & 7)) << 4));
-                    w[4 * c] = v.x;
-                    w[4 * c + 1] = v.y;
-                    w[4 * c + 2] = v.z;
-                    w[4 * c + 3] = v.w;
+                    w[4 * c] = v[8 * g + c].x;
+                    w[4 * c + 1] = v[8 * g + c].y;
+                    w[4 * c + 2] = v[8 * g + c].z;
+                    w[4 * c + 3] = v[8 * g + c].w;
                 }
                 tmem_st32(tl + kTmemR0 + g * 32, w);
             }
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar(kBarR0Ready));
+        };
+        int it = 0, unit_iter = 0, u = -1, u_next = -1;
+        bool ok = true;
+        for (; ok; ++unit_iter) {
+            if (unit_iter > 0) {
+                u = u_next;  // taken, and its resident tile loaded, before the last epilogue
+            } else {
+                u = take_unit(unit_iter, ok);
+                if (ok && u >= 0) load_r0(u);
+            }
+            if (!ok || u < 0) break;
+            const Unit U = decode<PASS, VARLEN>(u, p);
+            const int row = U.r0 + r;  // query (dQ pass) or key of this thread, in its sequence
+            const bool row_ok = row < (PASS == kPassDQ ? U.nq : U.nk);
+            if constexpr (PASS == kPassDQ) {
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarResFull), unit_iter & 1,
+                                                               abort_flag, budget));
+                if (!ok) break;
+            }
             // dQ pass: this row's L and D, resident for the unit
             float Lrow = 0.f, Drow = 0.f;
             if constexpr (PASS == kPassDQ) {
@@ -685,6 +722,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(bar(kBarAReady + it % kXBufs));
             }
             if (!ok) break;
+            // The next unit's first resident tile replaces this one's in TMEM: every X
+            // of this unit has completed (its last one was read above), and the MMA
+            // warp can form the next unit's first X during this epilogue.
+            u_next = take_unit(unit_iter + 1, ok);
+            if (!ok) break;
+            if (u_next >= 0) load_r0(u_next);
             // ---- epilogue: the row of the accumulator times out_scale, in 16 bit
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarAccDone), unit_iter & 1, abort_flag, budget));
             if (!ok) break;

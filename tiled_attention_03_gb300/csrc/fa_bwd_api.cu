@@ -362,6 +362,9 @@ fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O
         b.fault_unit = -1;
         fa::bwd256::Params pdq = b, pdk = b, pdv = b;
         pdq.out = dQ;
+        pdq.res0 = Q;
+        pdk.res0 = K;
+        pdv.res0 = K;
         pdq.out_scale = scale;
         pdq.n_units = static_cast<int>(BH * n_blk);      // (query head, 128-query block)
         pdk.out = dK;
@@ -594,6 +597,9 @@ fa_status fa_backward_varlen(const void *Q, const void *K, const void *V, const 
         b.vstride = p.vstride;
         fa::bwd256::Params pdq = b, pdk = b, pdv = b;
         pdq.out = dQ;
+        pdq.res0 = Q;
+        pdk.res0 = K;
+        pdv.res0 = K;
         pdq.out_scale = scale;
         pdq.n_blk = pq.n_blk;                       // (sequence, query head, 128-query block)
         pdq.n_units = pq.n_units;
