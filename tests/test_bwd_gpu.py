@@ -131,6 +131,19 @@ def test_bwd_d256_long_sampled():
     compare(q, k, v, do, d ** -0.5, "causal", (0, 0), dq, dk, dv, kv_heads=[0])
 
 
+@pytest.mark.parametrize("d", [128, 256])
+def test_bwd_many_units_per_cta(d):
+    """256 units per pass on 152 SMs: the CTAs that take a second unit (from the
+    launch-wide counter) load its resident tile and restart their accumulators
+    between units. Checked on the first K/V head (first units) and the last one
+    (second units)."""
+    B, H, N = 1, 16, 2048
+    q, k, v = make_qkv(B, H, N, d, torch.bfloat16, seed=37)
+    do = make_qkv(B, H, N, d, torch.bfloat16, seed=38)[0]
+    dq, dk, dv = run_bwd(q, k, v, do, d ** -0.5, "causal")
+    compare(q, k, v, do, d ** -0.5, "causal", (0, 0), dq, dk, dv, kv_heads=[0, H - 1])
+
+
 @pytest.mark.parametrize("d", [64, 256])
 def test_bwd_deterministic(d):
     """dQ, dK and dV are accumulated in tensor memory in a fixed order, without

@@ -83,6 +83,14 @@ def test_bwd_varlen_parity(case, mask, window, d, dtype):
     run_case(lens_q, lens_k or lens_q, H, Hk, d, dtype, mask, window, seed=31 * case + d)
 
 
+@pytest.mark.parametrize("d", [128, 256])
+def test_bwd_varlen_many_units_per_cta(d):
+    """16 sequences of up to 512 tokens, 4 heads: 256 units per pass on 152 SMs, so
+    CTAs run a second unit of another sequence."""
+    lens = [512, 300, 129, 512, 64, 511, 200, 512, 384, 1, 450, 512, 257, 128, 500, 33]
+    run_case(lens, lens, 4, 4, d, torch.bfloat16, "causal", (0, 0), seed=71)
+
+
 @pytest.mark.parametrize("d", [64, 256])
 def test_bwd_varlen_matches_dense(d):
     """Equal lengths: bit-identical to fa_backward on the (B, H, N, d) layout."""
