@@ -881,6 +881,12 @@ fa_status run_forward_varlen(const VarlenCall &c) {
     p.row_shift = g_row_shift.exchange(0);
 
     const int64_t blocks = n_units < ds->sm_count ? n_units : ds->sm_count;
+    // Causal / window: heaviest blocks first over groups of 16 row spaces (heads of one
+    // sequence), so that the last units handed out are light ones. The lengths are on
+    // the device, so the group is fixed rather than simulated as for dense calls
+    // (16 measured best of 1-64 on the mixed-length causal workload, by under 1 %).
+    p.n_spaces = static_cast<int>(BH);
+    p.group = p.heavy_first ? 16 : 1;
     cudaStream_t st = static_cast<cudaStream_t>(c.stream);
     cudaError_t e;
     if (d == 32)
