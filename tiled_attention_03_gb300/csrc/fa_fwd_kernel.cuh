@@ -375,6 +375,21 @@ __device__ __forceinline__ void record_timeout(const FwdParams &p, volatile int 
     }
 }
 
+// A TMEM load of 32 fp32 columns that also returns their maximum in m (the reducing
+// form of tcgen05.ld: one value per lane, NaN inputs ignored), and the wait for it;
+// neither r nor m may be used before tmem_ld_max_wait.
+__device__ __forceinline__ void tmem_ld32_max(uint32_t taddr, uint32_t (&r)[32], float &m) {
+    asm volatile(
+        "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, %32, [%33];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=f"(m)
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_max_wait(uint32_t (&r)[32], float &m) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]), "+f"(m) : : "memory");
+}
+
 // One online-softmax step of this thread's row over a 128-key tile whose fp32
 // scores sit at TMEM address tS (this warp's lanes). Masks hidden keys (only
 // in the kMasked instance), moves the reference max m lazily, adds the tile's
@@ -386,25 +401,38 @@ template <bool BF16, int kPChunk, bool kMasked>
 __device__ __forceinline__ float softmax_tile(uint32_t tS, uint32_t tP, int kv0, int lo_i, int hi_i,
                                               float sl2, float &m, float &l) {
     uint32_t sr[4][32];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
     float x[kBN];
+    float m_tile;
+    if constexpr (kMasked) {
 #pragma unroll
-    for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(sr[c >> 5][c & 31]);
-    if constexpr (kMasked) mask_outside_run(x, lo_i - kv0, hi_i - kv0, -INFINITY);
-    // Row max: four independent chains of 3-input max.
-    float ma = fmaxf(x[0], x[1]), mb = fmaxf(x[2], x[3]);
-    float mc = fmaxf(x[4], x[5]), md = fmaxf(x[6], x[7]);
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
 #pragma unroll
-    for (int c = 8; c < kBN; c += 8) {
-        ma = max3f(ma, x[c + 0], x[c + 1]);
-        mb = max3f(mb, x[c + 2], x[c + 3]);
-        mc = max3f(mc, x[c + 4], x[c + 5]);
-        md = max3f(md, x[c + 6], x[c + 7]);
+        for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
+#pragma unroll
+        for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(sr[c >> 5][c & 31]);
+        mask_outside_run(x, lo_i - kv0, hi_i - kv0, -INFINITY);
+        // Row max: four independent chains of 3-input max.
+        float ma = fmaxf(x[0], x[1]), mb = fmaxf(x[2], x[3]);
+        float mc = fmaxf(x[4], x[5]), md = fmaxf(x[6], x[7]);
+#pragma unroll
+        for (int c = 8; c < kBN; c += 8) {
+            ma = max3f(ma, x[c + 0], x[c + 1]);
+            mb = max3f(mb, x[c + 2], x[c + 3]);
+            mc = max3f(mc, x[c + 4], x[c + 5]);
+            md = max3f(md, x[c + 6], x[c + 7]);
+        }
+        m_tile = fmaxf(fmaxf(ma, mb), fmaxf(mc, md)) * sl2;
+    } else {
+        // every key visible: the TMEM loads reduce each 32-column run to its maximum
+        float mr[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32_max(tS + c * 32, sr[c], mr[c]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld_max_wait(sr[c], mr[c]);
+#pragma unroll
+        for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(sr[c >> 5][c & 31]);
+        m_tile = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3])) * sl2;
     }
-    const float m_tile = fmaxf(fmaxf(ma, mb), fmaxf(mc, md)) * sl2;
     // Lazy rescale: move the reference max only when this block's max exceeds
     // it by more than the threshold.
     const float m_old = m;
