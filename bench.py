@@ -39,9 +39,9 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
 CSRC = "tiled_attention_03_gb300/csrc/"
 KERNEL_SOURCES = {
     "fwd": (CSRC + "fa_fwd_kernel.cuh", CSRC + "fa_combine.cuh", CSRC + "fa_mask.cuh",
-            CSRC + "ptx.cuh"),
+            CSRC + "fa_tmem_max.cuh", CSRC + "ptx.cuh"),
     "fwd1t": (CSRC + "fa_fwd1t_kernel.cuh", CSRC + "fa_combine.cuh", CSRC + "fa_mask.cuh",
-              CSRC + "ptx.cuh"),
+              CSRC + "fa_tmem_max.cuh", CSRC + "ptx.cuh"),
     "bwd": (CSRC + "fa_bwd_kernel.cuh", CSRC + "fa_mask.cuh", CSRC + "ptx.cuh"),
     "bwd256": (CSRC + "fa_bwd256_kernel.cuh", CSRC + "fa_bwd_kernel.cuh", CSRC + "fa_mask.cuh",
                CSRC + "ptx.cuh"),

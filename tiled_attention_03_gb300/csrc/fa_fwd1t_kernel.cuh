@@ -44,6 +44,7 @@
 #include <cuda.h>
 
 #include "fa_mask.cuh"
+#include "fa_tmem_max.cuh"
 #include "ptx.cuh"
 
 namespace fa {
@@ -631,29 +632,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 tc_fence_after();
                 float x[kBN];
-#pragma unroll
-                for (int h = 0; h < kBN; h += 64) {
-                    uint32_t a[32], b[32];
-                    tmem_ld32(tS + h, a);
-                    tmem_ld32(tS + h + 32, b);
-                    tmem_ld_wait(a);
-                    tmem_ld_wait(b);
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        x[h + c] = __uint_as_float(a[c]);
-                        x[h + c + 32] = __uint_as_float(b[c]);
-                    }
-                }
                 const int kv0 = j * kBN;
-                if (!(kv0 >= lo_last && kv0 + kBN - 1 <= hi_first))
-                    mask_outside_run(x, lo_i - kv0, hi_i - kv0, -INFINITY);
-                float ma = fmaxf(x[0], x[1]), mb = fmaxf(x[2], x[3]);
+                float m_tile;
+                if (kv0 >= lo_last && kv0 + kBN - 1 <= hi_first) {
+                    // every key visible: the TMEM loads reduce each 32-column run to
+                    // its maximum
+                    float mr[kBN / 32];
 #pragma unroll
-                for (int c = 4; c < kBN; c += 4) {
-                    ma = max3f(ma, x[c], x[c + 1]);
-                    mb = max3f(mb, x[c + 2], x[c + 3]);
+                    for (int h = 0; h < kBN; h += 64) {
+                        uint32_t a[32], b[32];
+                        tmem_ld32_max(tS + h, a, mr[h / 32]);
+                        tmem_ld32_max(tS + h + 32, b, mr[h / 32 + 1]);
+                        tmem_ld_max_wait(a, mr[h / 32]);
+                        tmem_ld_max_wait(b, mr[h / 32 + 1]);
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            x[h + c] = __uint_as_float(a[c]);
+                            x[h + c + 32] = __uint_as_float(b[c]);
+                        }
+                    }
+                    float mm = mr[0];
+#pragma unroll
+                    for (int c = 1; c < kBN / 32; ++c) mm = fmaxf(mm, mr[c]);
+                    m_tile = mm * sl2;
+                } else {
+#pragma unroll
+                    for (int h = 0; h < kBN; h += 64) {
+                        uint32_t a[32], b[32];
+                        tmem_ld32(tS + h, a);
+                        tmem_ld32(tS + h + 32, b);
+                        tmem_ld_wait(a);
+                        tmem_ld_wait(b);
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            x[h + c] = __uint_as_float(a[c]);
+                            x[h + c + 32] = __uint_as_float(b[c]);
+                        }
+                    }
+                    mask_outside_run(x, lo_i - kv0, hi_i - kv0, -INFINITY);
+                    float ma = fmaxf(x[0], x[1]), mb = fmaxf(x[2], x[3]);
+#pragma unroll
+                    for (int c = 4; c < kBN; c += 4) {
+                        ma = max3f(ma, x[c], x[c + 1]);
+                        mb = max3f(mb, x[c + 2], x[c + 3]);
+                    }
+                    m_tile = fmaxf(ma, mb) * sl2;
                 }
-                const float m_tile = fmaxf(ma, mb) * sl2;
                 const float m_old = m;
                 if (m_tile > m + kRescaleThreshold) m = m_tile;
                 const float corr = m != m_old ? ex2_approx(m_old - m) : 1.f;
