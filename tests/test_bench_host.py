@@ -113,3 +113,30 @@ def test_kernel_family_follows_the_forward_dispatch():
     assert cut(B=40, H=16, H_kv=2, Nq=17) == "fwd"      # 136 rows
     assert cut(B=40, H=4, H_kv=2, Nq=100) == "fwd1t"    # not packed (Nq > 64): 100 rows
     assert cut(H=4, N=100, d=32) == "fwd"               # d = 32 has no one-tile form
+
+
+def test_kernel_source_hash_covers_every_included_header():
+    """A family's traffic figure is reported only while the hash of its sources is
+    unchanged, so those sources must include every local header its kernel file pulls
+    in, directly or through another header."""
+    sys.path.insert(0, ROOT)
+    import re
+    import bench
+    csrc = os.path.join(ROOT, "tiled_attention_03_gb300", "csrc")
+
+    def includes(name, seen):
+        if name in seen:
+            return seen
+        seen.add(name)
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            for inc in re.findall(r'#include "([^"]+)"', f.read()):
+                if os.path.exists(os.path.join(csrc, inc)):
+                    includes(inc, seen)
+        return seen
+
+    kernels = {"fwd": "fa_fwd_kernel.cuh", "fwd1t": "fa_fwd1t_kernel.cuh",
+               "bwd": "fa_bwd_kernel.cuh", "bwd256": "fa_bwd256_kernel.cuh"}
+    for family, top in kernels.items():
+        hashed = {os.path.basename(p) for p in bench.KERNEL_SOURCES[family]}
+        missing = includes(top, set()) - hashed
+        assert not missing, (family, missing)
