@@ -9,7 +9,8 @@
 //     and 128-key K/V tiles would be 64 KB each;
 //   * row spaces of at most 128 rows (decode steps: the few queries of the heads of
 //     one K/V head), where the two-tile kernel would run one tile and wait on its own
-//     softmax between S(j) and S(j+1).
+//     softmax between S(j) and S(j+1);
+//   * small unsplit problems, whose 256-row units would fill at most half of the SMs.
 // Layout:
 //   * a unit is one 128-row Q tile (128 x D, 16-bit);
 //   * K/V tiles hold bn(D) keys (128 for d <= 128, 64 at d = 256, where three
@@ -24,7 +25,12 @@
 //     the softmax warpgroup, and S = Q K^T takes Q from there: with 64-key tiles the
 //     shared-memory form would read 6 KB of operands per 32-cycle MMA, more than the
 //     SM's 128 bytes per cycle of shared-memory bandwidth, while K alone is 2 KB;
-//   * one softmax warpgroup (thread = query row = TMEM lane, bn(D) keys per block).
+//   * one softmax warpgroup (thread = query row = TMEM lane, bn(D) keys per block); on
+//     blocks that every row sees whole, the row maximum comes from the reducing TMEM
+//     load (fa_tmem_max.cuh).
+// Start-up: the thread that initialises the barriers also requests the CTA's first
+// unit's Q tile and first K tiles, and a launch whose grid covers every unit never
+// touches the scheduler counters.
 // When the reference max of a row moves (rare), the softmax thread rescales its O
 // row, after waiting for the product O += P(j-1) V_{j-1} to complete (two
 // alternating barriers, one per parity of j, so that a skipped wait never
