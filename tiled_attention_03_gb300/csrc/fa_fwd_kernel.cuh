@@ -42,6 +42,9 @@
 // issue order, so the P read of the earlier MMA precedes the S write of the
 // later one.
 //
+// On K/V blocks that every row of the Q tile sees whole, the row maximum comes from
+// the reducing TMEM load (fa_tmem_max.cuh) instead of 128 comparisons per thread.
+//
 // Each softmax thread stores its row of O / l with 32-byte stores (one TMEM lane
 // per thread, so a warp's stores go to 32 rows; the wider stores halve the store
 // instructions, which share the memory-instruction queue with every warp's
